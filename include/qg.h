@@ -1,0 +1,246 @@
+/*
+ * qg.h -- C ABI of the batch-1 hybrid Gated-DeltaNet / full-attention decode
+ * step with GGUF Q4_K / Q6_K weights, for NVIDIA GB300 (sm_103a).
+ *
+ * Every function returns QG_OK (0) or a negative QG_ERR_* code and never
+ * throws; qg_last_error() gives a message for the calling thread.  Device
+ * pointers ("_dev", "device") are CUDA global-memory addresses on the
+ * library's current device; host pointers are plain CPU memory.  `qg_stream`
+ * is a cudaStream_t (NULL = the legacy default stream).
+ *
+ * The operations and their order are those of forward_qwen35_cuda.rs
+ * (aprender-serve 0.68.2): the Gated DeltaNet layer (deltanet_layer_inner),
+ * the full-attention layer (attention_layer_inner) and the whole token
+ * (forward_single), ending, as in aprender PR #4332 ("Greedy GPU argmax"), in
+ * an on-device argmax that returns a 4-byte token id, first index on ties.
+ */
+#ifndef QG_H
+#define QG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qg_stream; /* == cudaStream_t */
+
+/* ------------------------------------------------------------ status codes */
+enum {
+    QG_OK = 0,
+    QG_ERR_SHAPE = -1,      /* a dimension the kernels cannot serve (e.g. k % 256 != 0,
+                               n_v_heads % n_k_heads != 0, max_seq_len == 0, lm_head
+                               shape != vocab x hidden) */
+    QG_ERR_QTYPE = -2,      /* a tensor type with no kernel here */
+    QG_ERR_EMPTY = -3,      /* an empty tensor (n == 0 or no data) */
+    QG_ERR_POS = -4,        /* position >= the state's max_seq_len */
+    QG_ERR_TOKEN = -5,      /* token id >= vocab */
+    QG_ERR_LAYER_KIND = -6, /* layer index of the other kind, or out of range */
+    QG_ERR_CUDA = -7,       /* a CUDA runtime call failed (message has the CUDA error) */
+    QG_ERR_TIMEOUT = -8,    /* a bounded device-side wait gave up (kernel set the error word) */
+    QG_ERR_ARG = -9,        /* NULL or misaligned pointer, negative size, bad argument */
+    QG_ERR_OOM = -10        /* device or pinned host allocation failed */
+};
+
+/* GGML type ids of the supported k-quants. */
+enum { QG_QTYPE_Q4_K = 12, QG_QTYPE_Q6_K = 14 };
+/* Layer kinds (forward_qwen35_cuda.rs, enum CudaLayer). */
+enum { QG_LAYER_DELTANET = 0, QG_LAYER_ATTENTION = 1 };
+
+/* Shapes of the model (forward_qwen35_cuda.rs, struct Qwen35CudaDims).
+ * conv_dim = 2 * n_k_heads * head_k_dim + n_v_heads * head_v_dim.
+ * Served: hidden, ffn, n_v_heads*head_v_dim and n_heads*head_dim multiples of
+ * 256; head_k_dim == 128; head_v_dim a multiple of 16; head_dim == 256;
+ * n_rot even and <= head_dim; n_v_heads % n_k_heads == 0; n_heads % n_kv_heads
+ * == 0 with at most 8 query heads per kv head. */
+typedef struct qg_config {
+    int32_t n_layers, hidden, ffn, vocab;
+    int32_t n_k_heads, n_v_heads, head_k_dim, head_v_dim, conv_kernel;
+    int32_t n_heads, n_kv_heads, head_dim, n_rot;
+    float eps;                  /* every RMSNorm, per-head norm, gated norm and L2 norm */
+    float rope_theta;           /* theta_scale = rope_theta^(-2/n_rot) is formed on the host */
+    const int32_t* layer_kinds; /* host, n_layers entries of QG_LAYER_* */
+} qg_config;
+
+/* A quantized tensor in HOST memory, raw GGUF layout: n rows of k weights,
+ * each row k/256 super-blocks (Q4_K 144 bytes, Q6_K 210 bytes). */
+typedef struct qg_qtensor {
+    const void* data;
+    int32_t qtype; /* QG_QTYPE_* */
+    int32_t n, k;
+} qg_qtensor;
+
+/* One layer's HOST weights (forward_qwen35_cuda.rs, CudaDeltaNetLayer and
+ * CudaAttentionLayer).  Fields of the other kind are ignored.  Quantized
+ * projections are Q4_K except ffn_down, which is Q6_K (QG_ERR_QTYPE otherwise). */
+typedef struct qg_layer_weights {
+    int32_t kind;
+    const float* attn_norm;           /* [hidden] */
+    const float* post_attention_norm; /* [hidden] */
+    qg_qtensor ffn_gate, ffn_up;      /* [ffn x hidden] */
+    qg_qtensor ffn_down;              /* [hidden x ffn] */
+    /* Gated DeltaNet */
+    const float* ssm_conv1d;  /* [conv_dim][conv_kernel] */
+    const float* ssm_a_log;   /* [n_v_heads]: A_log; the decay rate a = -exp(A_log) is formed at create */
+    const float* ssm_dt_bias; /* [n_v_heads] */
+    const float* ssm_norm;    /* [head_v_dim], shared by the value heads */
+    qg_qtensor attn_qkv;      /* [conv_dim x hidden] */
+    qg_qtensor ssm_alpha, ssm_beta; /* [n_v_heads x hidden] */
+    qg_qtensor attn_gate;     /* [n_v_heads*head_v_dim x hidden] */
+    qg_qtensor ssm_out;       /* [hidden x n_v_heads*head_v_dim] */
+    /* full attention */
+    const float* attn_q_norm; /* [head_dim] */
+    const float* attn_k_norm; /* [head_dim] */
+    qg_qtensor attn_q;        /* [2*n_heads*head_dim x hidden], per head [q | gate] */
+    qg_qtensor attn_k, attn_v;/* [n_kv_heads*head_dim x hidden] */
+    qg_qtensor attn_output;   /* [hidden x n_heads*head_dim] */
+} qg_layer_weights;
+
+typedef struct qg_host_weights {
+    const float* token_embd;  /* [vocab][hidden] f32 */
+    const float* output_norm; /* [hidden] */
+    qg_qtensor lm_head;       /* Q6_K [vocab x hidden], no bias */
+    const qg_layer_weights* layers; /* n_layers entries */
+} qg_host_weights;
+
+typedef struct qg_model qg_model; /* device-resident weights (opaque) */
+typedef struct qg_state qg_state; /* per-sequence decode state (opaque) */
+
+/* Host-side counters of one state (aprender PR #4332 test counters:
+ * device_allocs_total, device_to_host_bytes_total). */
+typedef struct qg_stats {
+    uint64_t device_allocs;   /* cudaMalloc/cudaHostAlloc calls made for this state */
+    uint64_t h2d_bytes;       /* host-to-device bytes copied by decode calls */
+    uint64_t d2h_bytes;       /* device-to-host bytes copied by decode calls */
+    uint64_t graph_launches;  /* CUDA graph launches */
+    uint64_t graph_captures;  /* CUDA graphs captured */
+    uint64_t graph_kernel_nodes; /* kernel nodes of the per-token graph */
+    uint64_t steps;           /* tokens decoded */
+} qg_stats;
+
+/* ---------------------------------------------------------- model / state */
+
+/* Copies the host weights to `device` (the caller keeps its buffers):
+ * fuses the projections that share an input, forms a = -exp(A_log) and
+ * repacks every Q6_K tensor to the planar layout below
+ * (forward_qwen35_cuda.rs, with_max_seq_len, build_layer).
+ * Errors: QG_ERR_SHAPE, QG_ERR_QTYPE, QG_ERR_EMPTY, QG_ERR_ARG, QG_ERR_OOM, QG_ERR_CUDA. */
+int qg_model_create(const qg_config* cfg, const qg_host_weights* w, int device, qg_model** out);
+int qg_model_destroy(qg_model* m);
+
+/* A fresh zeroed state (forward_qwen35_cuda.rs, new_state / build_state):
+ * per DeltaNet layer a conv window [conv_dim][conv_kernel-1] (oldest first)
+ * and a recurrent state [n_v_heads][head_v_dim][head_k_dim] with
+ * s[j*head_k_dim + i] == S[i][j]; per attention layer f32 K and V caches
+ * [max_seq_len][n_kv_heads*head_dim]; all scratch, the device token/position
+ * slots, pinned host slots and its own CUDA stream.  Allocates everything a
+ * decode needs up front.  Errors: QG_ERR_SHAPE (max_seq_len < 1), QG_ERR_OOM. */
+int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out);
+int qg_state_destroy(qg_state* s);
+/* Zero every window, state and cache; kv_len = 0. */
+int qg_state_reset(qg_state* s);
+
+/* Teacher forcing (forward_qwen35_cuda.rs upload_layer, upload_attention_kv,
+ * download_layer).  HOST buffers.  upload_layer: conv [conv_dim*(conv_kernel-1)]
+ * and ssm [n_v_heads*head_v_dim*head_k_dim] of DeltaNet layer il.
+ * upload_kv: `rows` whole K and V rows of attention layer il, sets kv_len = rows.
+ * download_layer: DeltaNet -> (conv, ssm), *n = max of the two lengths written
+ * as (conv_len, ssm_len) into a and b; attention -> the kv_len*kv_row K and V
+ * values written so far (*n = kv_len * n_kv_heads*head_dim; 0 on a fresh
+ * state).  Pass a == b == NULL to query *n (DeltaNet: *n = ssm_len).
+ * Errors: QG_ERR_LAYER_KIND, QG_ERR_SHAPE, QG_ERR_ARG, QG_ERR_CUDA. */
+int qg_state_upload_layer(qg_state* s, int il, const float* conv, const float* ssm);
+int qg_state_upload_kv(qg_state* s, int il, const float* k, const float* v, int rows);
+int qg_state_download_layer(qg_state* s, int il, float* a, float* b, size_t* n);
+/* The residual stream after the last completed step ([hidden], host). */
+int qg_state_download_hidden(qg_state* s, float* hidden_host);
+int qg_state_kv_len(const qg_state* s, int* kv_len);
+int qg_state_stats(const qg_state* s, qg_stats* out);
+
+/* ------------------------------------------------------- building blocks
+ * Device pointers, the caller's stream, no allocation, no synchronisation. */
+
+/* y[n] = sum_k deq(W[n][k]) * x[k] (forward_qwen35_cuda.rs gemv_dispatch,
+ * float variant).  x enters as a 24-bit block-fixed-point value: each element
+ * to within 2^-23 of the largest magnitude of its 32-element block (the
+ * precision of f32 for that largest element); sub-block sums are exact
+ * integers, accumulated in f32.
+ * w: Q4_K, raw GGUF layout, 16-byte aligned.  x: [k] f32.  y: [n] f32.
+ * k % 256 == 0 else QG_ERR_SHAPE; n == 0 or k == 0 -> QG_ERR_EMPTY. */
+int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream stream);
+
+/* The same for Q6_K in the library's planar layout (made by qg_q6k_to_planar). */
+int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream);
+
+/* Planar Q6_K: n8 = n rounded up to 8 rows, nb = k/256; four planes, each
+ * 16-byte aligned, holding exactly the GGUF bytes (n8*nb*210 in total):
+ *   QL [n8*nb][128]: per super-block, for quarter-chunk c = 2*half + part
+ *      (0..3), the 16 low-4-bit bytes ql[64*half + 16*part ..] followed by
+ *      ql[64*half + 32 + 16*part ..];
+ *   QH [n8*nb][64] (as in GGUF), SC [n8*nb][16] int8 scales, D [n8*nb] fp16.
+ * Rows n..n8-1 are zero.  qg_q6k_planar_bytes gives the size; src is the raw
+ * GGUF tensor and both are device pointers, 16-byte aligned. */
+size_t qg_q6k_planar_bytes(int n, int k);
+int qg_q6k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream);
+
+/* Fused lm_head GEMV + argmax (forward_qwen35_cuda.rs forward_single tail;
+ * aprender PR #4332 greedy argmax): *tok_dev = min{ i : l_i = max_j l_j },
+ * l = W x, no bias, logits never stored.  NaN logits never win; if all are
+ * NaN the result is 0.  w: planar Q6_K [n_vocab x k].  workspace: device,
+ * qg_lmhead_argmax_workspace_bytes() bytes, zero-filled before the first
+ * call; every call leaves it zero-filled; calls sharing a workspace must not
+ * overlap on the GPU. */
+size_t qg_lmhead_argmax_workspace_bytes(void);
+int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, void* workspace,
+                     uint32_t* tok_dev, qg_stream stream);
+
+/* First index of the maximum of x[n] (NaN never wins) -> *idx_dev. */
+int qg_argmax_f32(const float* x, int n, uint32_t* idx_dev, qg_stream stream);
+
+/* One Gated DeltaNet layer (forward_qwen35_cuda.rs forward_deltanet_layer)
+ * on hidden_dev [hidden], in place; the layer's conv window and recurrent
+ * state advance one step.  No position: the caller feeds steps in order.
+ * Errors: QG_ERR_LAYER_KIND, QG_ERR_ARG, QG_ERR_CUDA. */
+int qg_deltanet_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, qg_stream stream);
+
+/* One full-attention layer (forward_qwen35_cuda.rs forward_attention_layer)
+ * on hidden_dev at `pos`: K/V rows land at pos, attention covers rows
+ * 0..pos, kv_len = max(kv_len, pos + 1).  Errors: QG_ERR_POS,
+ * QG_ERR_LAYER_KIND, QG_ERR_ARG, QG_ERR_CUDA. */
+int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, int pos,
+                        qg_stream stream);
+
+/* ----------------------------------------------------------- whole token */
+
+/* One token at `pos` through every layer, the output norm and the fused
+ * lm_head + argmax, replayed as one CUDA graph captured on the first call
+ * (memra decode.rs GraphSession::step): 8 bytes host-to-device (token,
+ * pos), 4 bytes device-to-host (the token id), no allocation after the first
+ * call.  Blocks until *next_token is on the host.  Positions of DeltaNet
+ * layers advance per call, so feed pos = 0, 1, 2, ... in order.
+ * Errors: QG_ERR_TOKEN, QG_ERR_POS, QG_ERR_TIMEOUT, QG_ERR_CUDA. */
+int qg_decode_token(qg_model* m, qg_state* s, uint32_t token, int pos, uint32_t* next_token);
+
+/* The same step enqueued kernel by kernel without a graph (bit-identical). */
+int qg_decode_token_eager(qg_model* m, qg_state* s, uint32_t token, int pos, uint32_t* next_token);
+
+/* Greedy continuation kept on the device: n_steps tokens from pos0, each
+ * step's input the previous step's argmax (the first: the token the last
+ * decode call produced), the position advanced on the device.  One graph
+ * replay per token, no host round trip between them; tokens_host[n_steps]
+ * receives the ids at the end.  Errors as qg_decode_token. */
+int qg_decode_greedy(qg_model* m, qg_state* s, int pos0, int n_steps, uint32_t* tokens_host);
+
+/* Error word of the building blocks on the current device: QG_OK, or
+ * QG_ERR_TIMEOUT when a building-block kernel gave up on a bounded wait since
+ * the last check (the word is cleared).  Synchronous. */
+int qg_device_status(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* qg_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QG_H */

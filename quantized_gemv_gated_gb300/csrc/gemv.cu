@@ -1,0 +1,231 @@
+// Building-block entry points: Q4_K / Q6_K GEMV, the Q6_K planar repack, the
+// fused lm_head GEMV + argmax and a plain argmax; plus the error plumbing
+// shared by the whole library.
+#include <cstring>
+
+#include "qg_host.cuh"
+
+namespace qg {
+
+static thread_local char g_msg[512];
+
+int set_err(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_err(cudaError_t e, const char* what) {
+    return set_err(e == cudaErrorMemoryAllocation ? QG_ERR_OOM : QG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (v < 1) v = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = v;
+    return v;
+}
+
+// Error word of the building blocks (one per device that loads the library).
+__device__ unsigned g_block_err;
+
+static unsigned* block_err_ptr() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static unsigned* cache[64] = {nullptr};
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    unsigned* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_block_err) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) cache[dev] = p;
+    return p;
+}
+
+// --------------------------------------------------------- Q6_K planar repack
+// One thread per super-block of the n8-row padded matrix (see qg.h).
+__global__ void q6k_planar_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n, int n8, int nb) {
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long total = static_cast<long long>(n8) * nb;
+    if (idx >= total) return;
+    const long long r = idx / nb;
+    uint8_t* ql = dst + idx * 128;
+    uint8_t* qh = dst + total * 128 + idx * 64;
+    uint8_t* sc = dst + total * 192 + idx * 16;
+    uint8_t* dd = dst + total * 208 + idx * 2;
+    if (r >= n) {
+        for (int i = 0; i < 128; ++i) ql[i] = 0;
+        for (int i = 0; i < 64; ++i) qh[i] = 0;
+        for (int i = 0; i < 16; ++i) sc[i] = 0;
+        dd[0] = dd[1] = 0;
+        return;
+    }
+    const uint8_t* b = src + idx * 210;  // rows are contiguous: block idx of the padded grid == of the source
+    for (int c = 0; c < 4; ++c) {
+        const int half = c >> 1, part = c & 1;
+        for (int i = 0; i < 16; ++i) {
+            ql[32 * c + i] = b[64 * half + 16 * part + i];
+            ql[32 * c + 16 + i] = b[64 * half + 32 + 16 * part + i];
+        }
+    }
+    for (int i = 0; i < 64; ++i) qh[i] = b[128 + i];
+    for (int i = 0; i < 16; ++i) sc[i] = b[192 + i];
+    dd[0] = b[208];
+    dd[1] = b[209];
+}
+
+int q6k_to_planar(const void* src, void* dst, int n, int k, cudaStream_t st) {
+    const int nb = k / 256, n8 = (n + 7) & ~7;
+    const long long total = static_cast<long long>(n8) * nb;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    q6k_planar_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(static_cast<const uint8_t*>(src),
+                                                                       static_cast<uint8_t*>(dst), n, n8, nb);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+// -------------------------------------------------------------- argmax f32
+__global__ void __launch_bounds__(1024) argmax_f32_kernel(const float* __restrict__ x, int n, uint32_t* out) {
+    __shared__ unsigned long long red[32];
+    unsigned long long best = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const unsigned long long key = argmax_key(__ldcg(x + i), static_cast<unsigned>(i));
+        best = key > best ? key : best;
+    }
+    best = warp_max_u64(best);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0ull;
+        v = warp_max_u64(v);
+        if (threadIdx.x == 0) *out = v ? argmax_key_index(v) : 0u;
+    }
+}
+
+// ------------------------------------------------- lm_head GEMV + argmax epilogue
+// Per-row keys reduce to one per CTA, CTAs combine with a 64-bit atomicMax
+// (max is exact, so the result does not depend on arrival order), and the
+// last CTA to arrive publishes the token and re-zeroes the workspace.
+struct EpiArgmax : EpiBase {
+    unsigned long long* ws;  // ws[0]: best key; ws[1] low word: arrivals
+    uint32_t* tok;
+    unsigned long long best;
+    __device__ void start() { best = 0ull; }
+    __device__ void row(int r, float v) {
+        const unsigned long long key = argmax_key(v, static_cast<unsigned>(r));
+        best = key > best ? key : best;
+    }
+    __device__ void finish(float* sm, int tid) {
+        unsigned long long* red = reinterpret_cast<unsigned long long*>(sm);
+        best = warp_max_u64(best);
+        if ((tid & 31) == 0) red[tid >> 5] = best;
+        bar_sync(1, kConsumers);
+        if (tid == 0) {
+            unsigned long long m = 0ull;
+            for (int i = 0; i < kConsumerWarps; ++i) m = red[i] > m ? red[i] : m;
+            atomicMax(ws, m);
+            __threadfence();
+            const unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(ws + 1), 1u);
+            if (prev == gridDim.x - 1) {
+                __threadfence();
+                const unsigned long long key = atomicExch(ws, 0ull);
+                atomicExch(reinterpret_cast<unsigned*>(ws + 1), 0u);
+                *tok = key ? argmax_key_index(key) : 0u;
+            }
+        }
+    }
+};
+
+}  // namespace qg
+
+using namespace qg;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_gemv_args(const void* w, const float* x, const void* y, int n, int k) {
+    if (!w || !x || !y) return set_err(QG_ERR_ARG, "gemv: NULL pointer");
+    if (n < 0 || k < 0) return set_err(QG_ERR_ARG, "gemv: negative size n=%d k=%d", n, k);
+    if (n == 0 || k == 0) return set_err(QG_ERR_EMPTY, "gemv: empty tensor n=%d k=%d", n, k);
+    if (k % 256) return set_err(QG_ERR_SHAPE, "gemv: k=%d is not a multiple of 256", k);
+    if (!aligned16(w) || !aligned16(x)) return set_err(QG_ERR_ARG, "gemv: w and x must be 16-byte aligned");
+    return QG_OK;
+}
+
+extern "C" {
+
+const char* qg_last_error(void) { return g_msg; }
+
+int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream stream) {
+    int rc = check_gemv_args(w, x, y, n, k);
+    if (rc) return rc;
+    EpiStore epi{};
+    epi.y = y;
+    return launch_gemv<QT_Q4K, false>(w, nullptr, n, k, ProPlain{x}, epi, reinterpret_cast<cudaStream_t>(stream),
+                                      true, block_err_ptr());
+}
+
+int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream) {
+    int rc = check_gemv_args(w_planar, x, y, n, k);
+    if (rc) return rc;
+    EpiStore epi{};
+    epi.y = y;
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n, k, ProPlain{x}, epi,
+                                      reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
+}
+
+size_t qg_q6k_planar_bytes(int n, int k) {
+    if (n <= 0 || k <= 0 || k % 256) return 0;
+    return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 210;
+}
+
+int qg_q6k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream) {
+    if (!src || !dst) return set_err(QG_ERR_ARG, "q6k_to_planar: NULL pointer");
+    if (n <= 0 || k <= 0) return set_err(QG_ERR_EMPTY, "q6k_to_planar: empty tensor n=%d k=%d", n, k);
+    if (k % 256) return set_err(QG_ERR_SHAPE, "q6k_to_planar: k=%d is not a multiple of 256", k);
+    if (!aligned16(dst)) return set_err(QG_ERR_ARG, "q6k_to_planar: dst must be 16-byte aligned");
+    return q6k_to_planar(src, dst, n, k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t qg_lmhead_argmax_workspace_bytes(void) { return 16; }
+
+int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, void* workspace, uint32_t* tok_dev,
+                     qg_stream stream) {
+    int rc = check_gemv_args(w_planar, x, tok_dev, n_vocab, k);
+    if (rc) return rc;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 7u))
+        return set_err(QG_ERR_ARG, "lmhead_argmax: workspace must be 8-byte aligned device memory");
+    EpiArgmax epi{};
+    epi.ws = static_cast<unsigned long long*>(workspace);
+    epi.tok = tok_dev;
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlain{x}, epi,
+                                      reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
+}
+
+int qg_argmax_f32(const float* x, int n, uint32_t* idx_dev, qg_stream stream) {
+    if (!x || !idx_dev) return set_err(QG_ERR_ARG, "argmax_f32: NULL pointer");
+    if (n <= 0) return set_err(QG_ERR_EMPTY, "argmax_f32: n=%d", n);
+    argmax_f32_kernel<<<1, 1024, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, n, idx_dev);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+int qg_device_status(void) {
+    unsigned* p = block_err_ptr();
+    if (!p) return set_err(QG_ERR_CUDA, "device_status: no device error word");
+    unsigned v = 0;
+    QG_CUDA(cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost));
+    if (v) {
+        const unsigned zero = 0;
+        QG_CUDA(cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice));
+        return set_err(QG_ERR_TIMEOUT, "a building-block kernel gave up on a bounded wait (flags 0x%x)", v);
+    }
+    return QG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,486 @@
+// GEMV engine for GGUF k-quant weights on GB300 (sm_103a).
+//
+// y[n] = sum_k deq(W[n][k]) * x[k], one launch per projection (or per group
+// of projections sharing an input), in the role of the float ("mwv") Q4_K /
+// Q6_K GEMV of forward_qwen35_cuda.rs (gemv_dispatch, pin_float_gemv).
+//
+// Memory side.  Each CTA owns a contiguous range of rows (in units of 8).  A
+// producer warp streams them global -> shared with 1-D bulk copies
+// (cp.async.bulk, the TMA engine) into a ring of stages guarded by mbarriers,
+// with an L2 evict-first policy (weights are read once per token).  The copies
+// are issued at kernel start, before the programmatic-dependent-launch wait,
+// so a kernel's weights stream in while the previous kernel finishes.
+//
+// Arithmetic side.  x (K floats, after the kernel's prologue: RMSNorm, gated
+// norm, ...) is held in shared memory as a 24-bit block-fixed-point integer
+// per element: in every 32-element block, n_i = rint(x_i * 2^(22-e)) with 2^e
+// <= max|x| < 2^(e+1), so |n_i| < 2^23 and the representation keeps the 24
+// significant bits of the block's largest element (f32 keeps 24).  n_i is
+// stored as three byte planes (n = n2*65536 + n1*256 + n0, n2 signed), and
+// every sum of quant*n over a sub-block is computed EXACTLY with dp4a integer
+// dot products.  Sub-block sums are then scaled and accumulated in f32.  This
+// is not the int8 activation quantisation forward_qwen35_cuda.rs rejects
+// (pin_float_gemv): the only rounding of x is below 2^-23 of its block's
+// largest magnitude, and the per-sub-block sums carry no rounding at all.
+//
+//   Q4_K sub-block j (32 weights): d*sc_j*sum(q*x) - dmin*m_j*sum(x)
+//   Q6_K group of 16 weights:      d*sc*sum((q-32)*x)
+#pragma once
+#include "qg_common.cuh"
+
+namespace qg {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxStages = 4;
+constexpr int QT_Q4K = 12;
+constexpr int QT_Q6K = 14;
+
+// Geometry of one launch (identical on host and device).
+struct GemvShape {
+    const uint8_t* w0;  // Q4_K: GGUF rows; Q6_K: planar base
+    const uint8_t* w1;  // second matrix of a dual launch (same shape), else null
+    int n, n8, k, nb, cr;
+    int lg;      // log2(lanes per row)
+    int rs;      // rows per stage (multiple of 8 * rows per warp)
+    int stages;  // ring depth
+    int units;   // ceil(n / 8)
+    int stage_bytes;
+    int pro_floats;  // prologue scratch floats
+    unsigned* err;
+};
+
+// Shared-memory layout offsets.
+__host__ __device__ inline int xaux_bytes(int qt, int k) { return qt == QT_Q4K ? (k / 32) * 8 : k; }
+__host__ __device__ inline int off_dig() { return 64; }
+__host__ __device__ inline int off_aux(int k) { return 64 + 3 * k; }
+__host__ __device__ inline int off_pro(int qt, int k) { return ((off_aux(k) + xaux_bytes(qt, k)) + 15) & ~15; }
+__host__ __device__ inline int off_ring(int qt, int k, int pro_floats) {
+    return (off_pro(qt, k) + 4 * pro_floats + 127) & ~127;
+}
+
+// 16-byte-unit swizzles of the digit planes, chosen so that the 8 lanes of
+// one shared-memory phase read 8 distinct bank groups.
+__device__ __forceinline__ unsigned swz(int qt, unsigned u) {
+    return qt == QT_Q4K ? (u ^ ((u >> 3) & 3u)) : (u ^ ((u >> 2) & 6u));
+}
+
+__device__ __forceinline__ unsigned dp4a_uu(unsigned a, unsigned b, unsigned c) { return __dp4a(a, b, c); }
+__device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ---------------------------------------------------------- x representation
+// Warps split the K/32 blocks; lane i of a warp holds element 32b+i.
+template <int QT, class Pro>
+__device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, void* aux, int k, int warp,
+                           int lane) {
+    const int nblk = k >> 5;
+    for (int b = warp; b < nblk; b += kConsumerWarps) {
+        const int i = 32 * b + lane;
+        const float x = pro.value(sm, i);
+        const unsigned amax = __reduce_max_sync(FULL, __float_as_uint(x) & 0x7fffffffu);
+        int e = static_cast<int>(amax >> 23) - 127;
+        e = e < -100 ? -100 : e;
+        const float mul = __uint_as_float(static_cast<unsigned>(149 - e) << 23);   // 2^(22-e)
+        const float unit = __uint_as_float(static_cast<unsigned>(105 + e) << 23);  // 2^(e-22)
+        int n = __float2int_rn(x * mul);
+        n = n > 8388607 ? 8388607 : (n < -8388607 ? -8388607 : n);
+        const unsigned off = (swz(QT, static_cast<unsigned>(i) >> 4) << 4) | (i & 15);
+        dig[off] = static_cast<uint8_t>(n & 255);
+        dig[k + off] = static_cast<uint8_t>((n >> 8) & 255);
+        dig[2 * k + off] = static_cast<uint8_t>((n >> 16) & 255);
+        if constexpr (QT == QT_Q4K) {
+            const int s = __reduce_add_sync(FULL, n);
+            if (lane == 0) reinterpret_cast<float2*>(aux)[b] = make_float2(unit, static_cast<float>(s) * unit);
+        } else {
+            // per 16-group digit sums, folded into the dp4a start value as -32*N
+            int p01 = (n & 255) | (((n >> 8) & 255) << 16);
+            int p2 = n >> 16;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                p01 += __shfl_xor_sync(FULL, p01, o);
+                p2 += __shfl_xor_sync(FULL, p2, o);
+            }
+            if ((lane & 15) == 0) {
+                const unsigned g = static_cast<unsigned>(i) >> 4;
+                reinterpret_cast<int4*>(aux)[swz(QT, g)] =
+                    make_int4(-32 * (p01 & 0xffff), -32 * (p01 >> 16), -32 * p2, __float_as_int(unit));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ chunk kernels
+// One lane, one 64-weight chunk.  Q4_K: group g of super-block `blk`.
+__device__ __forceinline__ void chunk_q4k(const uint8_t* blk, int g, int xo, const uint8_t* dig,
+                                          const float2* bs, int k, float& acc) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * g);
+    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * g);
+    const unsigned u0 = static_cast<unsigned>(xo) >> 4;
+    unsigned a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    int a2 = 0, b2 = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint4 q = h ? qb : qa;
+        const unsigned ul = swz(QT_Q4K, u0 + h) << 4, uh = swz(QT_Q4K, u0 + 2 + h) << 4;
+        const uint4 l0 = *reinterpret_cast<const uint4*>(dig + ul);
+        const uint4 l1 = *reinterpret_cast<const uint4*>(dig + k + ul);
+        const uint4 l2 = *reinterpret_cast<const uint4*>(dig + 2 * k + ul);
+        const uint4 h0 = *reinterpret_cast<const uint4*>(dig + uh);
+        const uint4 h1 = *reinterpret_cast<const uint4*>(dig + k + uh);
+        const uint4 h2 = *reinterpret_cast<const uint4*>(dig + 2 * k + uh);
+        const unsigned qw[4] = {q.x, q.y, q.z, q.w};
+        const unsigned L0[4] = {l0.x, l0.y, l0.z, l0.w}, L1[4] = {l1.x, l1.y, l1.z, l1.w},
+                       L2[4] = {l2.x, l2.y, l2.z, l2.w};
+        const unsigned H0[4] = {h0.x, h0.y, h0.z, h0.w}, H1[4] = {h1.x, h1.y, h1.z, h1.w},
+                       H2[4] = {h2.x, h2.y, h2.z, h2.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const unsigned lo = qw[w] & 0x0f0f0f0fu, hi = (qw[w] >> 4) & 0x0f0f0f0fu;
+            a0 = dp4a_uu(lo, L0[w], a0);
+            a1 = dp4a_uu(lo, L1[w], a1);
+            a2 = dp4a_us(lo, L2[w], a2);
+            b0 = dp4a_uu(hi, H0[w], b0);
+            b1 = dp4a_uu(hi, H1[w], b1);
+            b2 = dp4a_us(hi, H2[w], b2);
+        }
+    }
+    // scale / min of sub-blocks j = 2g (low nibbles) and 2g+1 (high nibbles)
+    const float d = f16_to_f32(static_cast<uint16_t>(hdr.x & 0xffffu));
+    const float dmin = f16_to_f32(static_cast<uint16_t>(hdr.x >> 16));
+    int sc[2], mn[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int j = 2 * g + t, sh = 8 * (j & 3);
+        const unsigned by = (hdr.y >> sh) & 0xffu, bz = (hdr.z >> sh) & 0xffu, bw = (hdr.w >> sh) & 0xffu;
+        if (j < 4) {
+            sc[t] = static_cast<int>(by & 63u);
+            mn[t] = static_cast<int>(bz & 63u);
+        } else {
+            sc[t] = static_cast<int>((bw & 15u) | ((by >> 6) << 4));
+            mn[t] = static_cast<int>((bw >> 4) | ((bz >> 6) << 4));
+        }
+    }
+    const float4 ab = *reinterpret_cast<const float4*>(bs + (xo >> 5));  // unitA, sumA, unitB, sumB
+    const float sa = fmaf(static_cast<float>(a2), 65536.0f, static_cast<float>(static_cast<int>(a1 * 256u + a0)));
+    const float sb = fmaf(static_cast<float>(b2), 65536.0f, static_cast<float>(static_cast<int>(b1 * 256u + b0)));
+    acc = fmaf(d * static_cast<float>(sc[0]), sa * ab.x, acc);
+    acc = fmaf(-(dmin * static_cast<float>(mn[0])), ab.y, acc);
+    acc = fmaf(d * static_cast<float>(sc[1]), sb * ab.z, acc);
+    acc = fmaf(-(dmin * static_cast<float>(mn[1])), ab.w, acc);
+}
+
+// Q6_K planar: quarter-chunk cq = 2*half + part of super-block b.
+__device__ __forceinline__ void chunk_q6k(const uint8_t* ql, const uint8_t* qhp, const uint8_t* scp,
+                                          const uint16_t* dp, int b, int cq, int xo, const uint8_t* dig,
+                                          const int4* gc, int k, float& acc) {
+    const int half = cq >> 1, part = cq & 1;
+    const int f = b & 1;  // read the two 16-byte pieces in an order that avoids bank conflicts
+    const uint4 p0 = *reinterpret_cast<const uint4*>(ql + 32 * cq + 16 * f);
+    const uint4 p1 = *reinterpret_cast<const uint4*>(ql + 32 * cq + 16 * (1 - f));
+    const uint4 A = f ? p1 : p0;  // ql[64*half + 16*part ..]      quarters 0 (low), 2 (high)
+    const uint4 B = f ? p0 : p1;  // ql[64*half + 32 + 16*part ..] quarters 1 (low), 3 (high)
+    const uint4 H = *reinterpret_cast<const uint4*>(qhp + 16 * cq);
+    const uint2 S = *reinterpret_cast<const uint2*>(scp + 8 * half);
+    const float d = f16_to_f32(*dp);
+    const unsigned Aw[4] = {A.x, A.y, A.z, A.w}, Bw[4] = {B.x, B.y, B.z, B.w}, Hw[4] = {H.x, H.y, H.z, H.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int pos = xo + 128 * half + 32 * s + 16 * part;
+        const unsigned u = swz(QT_Q6K, static_cast<unsigned>(pos) >> 4);
+        const int4 gcv = gc[u];
+        const uint4 D0 = *reinterpret_cast<const uint4*>(dig + (u << 4));
+        const uint4 D1 = *reinterpret_cast<const uint4*>(dig + k + (u << 4));
+        const uint4 D2 = *reinterpret_cast<const uint4*>(dig + 2 * k + (u << 4));
+        const unsigned d0[4] = {D0.x, D0.y, D0.z, D0.w}, d1[4] = {D1.x, D1.y, D1.z, D1.w},
+                       d2[4] = {D2.x, D2.y, D2.z, D2.w};
+        int t0 = gcv.x, t1 = gcv.y, t2 = gcv.z;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            unsigned q;
+            if (s == 0) q = (Aw[w] & 0x0f0f0f0fu) | ((Hw[w] << 4) & 0x30303030u);
+            else if (s == 1) q = (Bw[w] & 0x0f0f0f0fu) | ((Hw[w] << 2) & 0x30303030u);
+            else if (s == 2) q = ((Aw[w] >> 4) & 0x0f0f0f0fu) | (Hw[w] & 0x30303030u);
+            else q = ((Bw[w] >> 4) & 0x0f0f0f0fu) | ((Hw[w] >> 2) & 0x30303030u);
+            t0 = static_cast<int>(dp4a_uu(q, d0[w], static_cast<unsigned>(t0)));
+            t1 = static_cast<int>(dp4a_uu(q, d1[w], static_cast<unsigned>(t1)));
+            t2 = dp4a_us(q, d2[w], t2);
+        }
+        const float T = fmaf(static_cast<float>(t2), 65536.0f, static_cast<float>(t1 * 256 + t0));
+        const int si = part + 2 * s;
+        const int sc = static_cast<int>(static_cast<int8_t>(((si < 4 ? S.x : S.y) >> (8 * (si & 3))) & 0xffu));
+        acc = fmaf(d * static_cast<float>(sc), T * __int_as_float(gcv.w), acc);
+    }
+}
+
+// Partial dot product of one row over the chunks c = lg0, lg0 + G, ...
+template <int QT>
+__device__ __forceinline__ float row_partial(const uint8_t* stage, int rs, int lrow, int nb, int cr, int G, int lg0,
+                                             const uint8_t* dig, const void* aux, int k) {
+    float acc = 0.0f;
+    if constexpr (QT == QT_Q4K) {
+        const uint8_t* row = stage + static_cast<size_t>(lrow) * nb * 144;
+        for (int c = lg0; c < cr; c += G)
+            chunk_q4k(row + (c >> 2) * 144, c & 3, 64 * c, dig, reinterpret_cast<const float2*>(aux), k, acc);
+    } else {
+        const uint8_t* ql = stage + static_cast<size_t>(lrow) * nb * 128;
+        const uint8_t* qh = stage + static_cast<size_t>(rs) * nb * 128 + static_cast<size_t>(lrow) * nb * 64;
+        const uint8_t* sc = stage + static_cast<size_t>(rs) * nb * 192 + static_cast<size_t>(lrow) * nb * 16;
+        const uint16_t* dd =
+            reinterpret_cast<const uint16_t*>(stage + static_cast<size_t>(rs) * nb * 208) + static_cast<size_t>(lrow) * nb;
+        for (int c = lg0; c < cr; c += G) {
+            const int b = c >> 2;
+            chunk_q6k(ql + b * 128, qh + b * 64, sc + b * 16, dd + b, b, c & 3, 256 * b, dig,
+                      reinterpret_cast<const int4*>(aux), k, acc);
+        }
+    }
+    return acc;
+}
+
+// Bytes of one stage per matrix for `rows` rows (Q6_K copies whole 8-row groups).
+__host__ __device__ inline size_t rows_bytes(int qt, int rows, int nb) {
+    return static_cast<size_t>(rows) * nb * (qt == QT_Q4K ? 144 : 210);
+}
+
+// -------------------------------------------------------------- the kernel
+// Pro: prepare(float* sm, int k, int tid) fills its scratch (consumers only),
+//      value(const float* sm, int i) gives x_i.
+// Epi: start() after the dependency wait, row(r, v) / row2(r, v0, v1) by the
+//      lane leading each row group, finish(float* red, int tid) once per CTA.
+template <int QT, bool DUAL, class Pro, class Epi>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvShape sh, const Pro pro_in, const Epi epi_in) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    uint8_t* dig = smem + off_dig();
+    void* aux = smem + off_aux(sh.k);
+    float* psm = reinterpret_cast<float*>(smem + off_pro(QT, sh.k));
+    uint8_t* ring = smem + off_ring(QT, sh.k, sh.pro_floats);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
+
+    // this CTA's rows [r0, r1), in whole 8-row units
+    const int u0 = static_cast<int>((static_cast<long long>(blockIdx.x) * sh.units) / gridDim.x);
+    const int u1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * sh.units) / gridDim.x);
+    const int r0 = 8 * u0, r1 = min(8 * u1, sh.n);
+    const int nst = r1 > r0 ? (r1 - r0 + sh.rs - 1) / sh.rs : 0;
+    const int S = sh.stages;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // --------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            const int nb = sh.nb;
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < nst; ++t) {
+                const int slot = t % S;
+                if (t >= S && !mbar_wait(&empty[slot], ((t / S) - 1) & 1)) {
+                    atomicOr(sh.err, DEVERR_EMPTY_WAIT);
+                    ok = false;
+                    break;
+                }
+                const int row0 = r0 + t * sh.rs;
+                const int rows = min(sh.rs, r1 - row0);
+                uint8_t* st = ring + static_cast<size_t>(slot) * sh.stage_bytes;
+                if constexpr (QT == QT_Q4K) {
+                    const unsigned bytes = static_cast<unsigned>(rows_bytes(QT, rows, nb));
+                    mbar_arrive_expect_tx(&full[slot], DUAL ? 2 * bytes : bytes);
+                    bulk_g2s(st, sh.w0 + rows_bytes(QT, row0, nb), bytes, &full[slot], pol);
+                    if constexpr (DUAL)
+                        bulk_g2s(st + rows_bytes(QT, sh.rs, nb), sh.w1 + rows_bytes(QT, row0, nb), bytes, &full[slot],
+                                 pol);
+                } else {
+                    const int rows8 = (rows + 7) & ~7;
+                    const size_t plane = static_cast<size_t>(sh.n8) * nb;
+                    const unsigned tot = static_cast<unsigned>(rows_bytes(QT, rows8, nb));
+                    mbar_arrive_expect_tx(&full[slot], DUAL ? 2 * tot : tot);
+                    const uint8_t* ws[2] = {sh.w0, sh.w1};
+#pragma unroll
+                    for (int m = 0; m < (DUAL ? 2 : 1); ++m) {
+                        const uint8_t* w = ws[m];
+                        uint8_t* d = st + m * rows_bytes(QT, sh.rs, nb);
+                        const size_t rb = static_cast<size_t>(row0) * nb;
+                        bulk_g2s(d, w + rb * 128, rows8 * nb * 128, &full[slot], pol);
+                        bulk_g2s(d + static_cast<size_t>(sh.rs) * nb * 128, w + plane * 128 + rb * 64, rows8 * nb * 64,
+                                 &full[slot], pol);
+                        bulk_g2s(d + static_cast<size_t>(sh.rs) * nb * 192, w + plane * 192 + rb * 16, rows8 * nb * 16,
+                                 &full[slot], pol);
+                        bulk_g2s(d + static_cast<size_t>(sh.rs) * nb * 208, w + plane * 208 + rb * 2, rows8 * nb * 2,
+                                 &full[slot], pol);
+                    }
+                }
+                issued = t + 1;
+            }
+            if (!ok) {
+                // do not leave while copies into this CTA's shared memory are in flight
+                for (int t = max(0, issued - S); t < issued; ++t)
+                    if (!mbar_wait(&full[t % S], (t / S) & 1)) atomicOr(sh.err, DEVERR_DRAIN_WAIT);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    pdl_wait();
+    Pro pro = pro_in;
+    Epi epi = epi_in;
+    pro.prepare(psm, sh.k, tid);
+    bar_sync(1, kConsumers);
+    build_xrep<QT>(pro, psm, dig, aux, sh.k, warp, lane);
+    epi.start();
+    bar_sync(1, kConsumers);
+
+    const int G = 1 << sh.lg, rw = 32 / G;
+    const int grp = lane >> sh.lg, lg0 = lane & (G - 1);
+    const size_t second = rows_bytes(QT, sh.rs, sh.nb);
+    for (int t = 0; t < nst; ++t) {
+        const int slot = t % S;
+        if (!mbar_wait(&full[slot], (t / S) & 1)) {
+            atomicOr(sh.err, DEVERR_FULL_WAIT);
+            break;
+        }
+        const uint8_t* st = ring + static_cast<size_t>(slot) * sh.stage_bytes;
+        const int row0 = r0 + t * sh.rs;
+        const int rows = min(sh.rs, r1 - row0);
+        for (int base = warp * rw; base < rows; base += kConsumerWarps * rw) {
+            const int lr = base + grp;
+            const bool valid = lr < rows;
+            float v0 = valid ? row_partial<QT>(st, sh.rs, lr, sh.nb, sh.cr, G, lg0, dig, aux, sh.k) : 0.0f;
+            float v1 = 0.0f;
+            if constexpr (DUAL)
+                v1 = valid ? row_partial<QT>(st + second, sh.rs, lr, sh.nb, sh.cr, G, lg0, dig, aux, sh.k) : 0.0f;
+            for (int o = G >> 1; o > 0; o >>= 1) {
+                v0 += __shfl_xor_sync(FULL, v0, o);
+                if constexpr (DUAL) v1 += __shfl_xor_sync(FULL, v1, o);
+            }
+            if (valid && lg0 == 0) {
+                if constexpr (DUAL) epi.row2(row0 + lr, v0, v1);
+                else epi.row(row0 + lr, v0);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    epi.finish(psm, tid);
+}
+
+// ------------------------------------------------------------- prologues
+struct ProPlain {
+    const float* x;
+    __host__ __device__ int floats(int k) const { return k; }
+    __device__ void prepare(float* sm, int k, int tid) {
+#pragma unroll 4
+        for (int i = 4 * tid; i < k; i += 4 * kConsumers)
+            *reinterpret_cast<float4*>(sm + i) = ldcg4(x + i);
+    }
+    __device__ float value(const float* sm, int i) const { return sm[i]; }
+};
+
+// x = RMSNorm(h) * w (rmsnorm_into).  With `tok` set, h is row *tok of the
+// embedding table and CTA 0 also stores it to h_out (the residual stream).
+struct ProRmsNorm {
+    const float* h;
+    const float* w;
+    const int* tok;
+    float* h_out;
+    float eps;
+    int kdim;  // = k
+    float r;
+    __host__ __device__ int floats(int k) const { return 2 * k + 32; }
+    __device__ void prepare(float* sm, int k, int tid) {
+        const float* src = h;
+        if (tok) src = h + static_cast<size_t>(__ldcg(tok)) * k;
+        float ss = 0.0f;
+#pragma unroll 4
+        for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
+            const float4 v = ldcg4(src + i);
+            const float4 ww = __ldg(reinterpret_cast<const float4*>(w + i));
+            *reinterpret_cast<float4*>(sm + i) = v;
+            *reinterpret_cast<float4*>(sm + k + i) = ww;
+            if (tok && blockIdx.x == 0) *reinterpret_cast<float4*>(h_out + i) = v;
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+        ss = warp_sum(ss);
+        float* red = sm + 2 * k;
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        bar_sync(1, kConsumers);
+        float tot = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kConsumerWarps; ++i) tot += red[i];
+        r = 1.0f / sqrtf(tot / static_cast<float>(k) + eps);
+    }
+    __device__ float value(const float* sm, int i) const { return (sm[i] * r) * sm[kdim + i]; }
+};
+
+// x = per-head RMSNorm(o_h) * w * silu(z_h) (gdn_gated_rmsnorm_into).
+struct ProGatedNorm {
+    const float* o;
+    const float* z;
+    const float* w;
+    int dv;
+    float eps;
+    int kdim;  // = k
+    __host__ __device__ int floats(int k) const { return 2 * k + dv + k / dv + 8; }
+    __device__ void prepare(float* sm, int k, int tid) {
+        float* zs = sm + k;
+        float* wsm = sm + 2 * k;
+        float* rh = wsm + dv;
+#pragma unroll 4
+        for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
+            *reinterpret_cast<float4*>(sm + i) = ldcg4(o + i);
+            *reinterpret_cast<float4*>(zs + i) = ldcg4(z + i);
+        }
+        for (int i = tid; i < dv; i += kConsumers) wsm[i] = __ldg(w + i);
+        bar_sync(1, kConsumers);
+        const int warp = tid >> 5, lane = tid & 31, nh = k / dv;
+        for (int hh = warp; hh < nh; hh += kConsumerWarps) {
+            float ss = 0.0f;
+            for (int j = lane; j < dv; j += 32) ss = fmaf(sm[hh * dv + j], sm[hh * dv + j], ss);
+            ss = warp_sum(ss);
+            if (lane == 0) rh[hh] = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
+        }
+    }
+    __device__ float value(const float* sm, int i) const {
+        const int hh = i / dv, j = i - hh * dv;
+        return ((sm[i] * sm[2 * kdim + dv + hh]) * sm[2 * kdim + j]) * silu(sm[kdim + i]);
+    }
+};
+
+// ------------------------------------------------------------- epilogues
+struct EpiBase {
+    __device__ void start() {}
+    __device__ void finish(float*, int) {}
+};
+struct EpiStore : EpiBase {
+    float* y;
+    __device__ void row(int r, float v) { y[r] = v; }
+};
+struct EpiResidual : EpiBase {  // h += W x (residual_add_into)
+    float* h;
+    __device__ void row(int r, float v) { h[r] = __ldcg(h + r) + v; }
+};
+struct EpiSwiGlu : EpiBase {  // act = silu(W_gate x) * (W_up x) (fused_swiglu_into)
+    float* act;
+    __device__ void row2(int r, float g, float u) { act[r] = silu(g) * u; }
+};
+
+}  // namespace qg

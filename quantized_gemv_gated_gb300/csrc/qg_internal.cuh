@@ -1,0 +1,79 @@
+// Internal layout of qg_model / qg_state and the per-layer launchers.
+#pragma once
+#include <vector>
+
+#include "qg_host.cuh"
+
+// Device-resident weights of one layer.
+struct qg_layer_dev {
+    int kind;
+    float* attn_norm;
+    float* post_norm;
+    uint8_t* w_in;   // fused input projection, Q4_K rows: DeltaNet [qkv | alpha | beta | gate],
+                     // attention [q|gate per head | k | v]
+    int n_in;
+    uint8_t* w_out;  // ssm_out / attn_output, Q4_K
+    uint8_t* w_gate; // Q4_K [ffn x hidden]
+    uint8_t* w_up;
+    uint8_t* w_down; // Q6_K planar [hidden x ffn]
+    // Gated DeltaNet
+    float* conv_w;   // [conv_dim][conv_kernel]
+    float* a;        // -exp(A_log) [n_v_heads]
+    float* dt_bias;
+    float* ssm_norm; // [head_v_dim]
+    // full attention
+    float* q_norm;
+    float* k_norm;
+};
+
+struct qg_model {
+    qg_config cfg;
+    std::vector<int32_t> kinds;
+    int device;
+    int k_dim, v_dim, conv_dim, q_dim, kv_dim;
+    float theta_scale;
+    std::vector<qg_layer_dev> layers;
+    float* embd;
+    float* out_norm;
+    uint8_t* lm_head;  // Q6_K planar [vocab x hidden]
+    std::vector<void*> allocs;
+};
+
+struct qg_state {
+    const qg_model* m;
+    int max_seq;
+    int kv_len;
+    cudaStream_t stream;
+    std::vector<float*> conv, ssm, kc, vc;  // per layer, null for the other kind
+    // scratch
+    float *h, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *attn;
+    float *part_acc, *part_ml;
+    unsigned* attn_count;       // [n_kv_heads] split arrivals (left at 0)
+    unsigned long long* am_ws;  // lm_head argmax workspace (left at 0)
+    int* slots;                 // device: [0] token in, [1] position, [2] token out (bit 31: device error)
+    uint32_t* hist;             // device: greedy token per position [max_seq]
+    unsigned* err;              // device error word
+    int* pinned;                // pinned host: [0] token, [1] position, [2] token out
+    int keys_per_split, max_splits;
+    cudaGraphExec_t exec_step;
+    cudaGraphExec_t exec_greedy;
+    qg_stats stats;
+    std::vector<void*> allocs;
+};
+
+namespace qg {
+
+// Enqueue one layer on `st`.  `h` is the residual stream; `embed` makes the
+// first kernel gather h from the embedding row of slots[0]; `pdl_first`
+// allows the first kernel to overlap the previous kernel on the stream.
+int run_deltanet_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
+                       bool pdl_first);
+int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
+                        bool pdl_first);
+// Output norm + fused lm_head GEMV + argmax -> slots[0] / slots[2];
+// `advance` also records hist[pos] and moves slots[1] to pos + 1.
+int run_lmhead(const qg_model* m, qg_state* s, const float* h, cudaStream_t st, bool advance);
+// a = -exp(A_log) on the device.
+int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st);
+
+}  // namespace qg

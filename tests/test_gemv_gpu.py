@@ -1,0 +1,217 @@
+"""GEMV, Q6_K planar repack, fused lm_head + argmax and argmax on the GPU,
+through the C ABI, against the CPU oracle on the same seeded inputs.
+
+Bar (pages' float-GEMV parity, forward_qwen35_cuda.rs pin_reference_gemv):
+the GPU result must sit inside the error bound of the exact (f64) product
+that its arithmetic guarantees -- x held to 2^-23 of each 32-element block's
+largest magnitude M_b, exact integer sub-block sums, f32 accumulation:
+|y - y_exact| <= 2^-23 * sum_k |w_k| M_b(k) + 8 * 2^-24 * sum_k |w_k x_k| --
+and within 1e-5 normwise of the f32 oracle.  Argmax indices are compared
+bit-exactly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+qg = pytest.importorskip("quantized_gemv_gated_gb300")
+
+F32_EPS = 2.0 ** -24
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def planar(t):
+    """Device planar copy of a synth Q6_K tensor (through the library's repack)."""
+    src = dev(t.data)
+    dst = torch.empty(qg.qg_q6k_planar_bytes(t.n, t.k), dtype=torch.uint8, device="cuda")
+    qg.qg_q6k_to_planar(src, dst, t.n, t.k)
+    return dst
+
+
+def run_gemv(t, x):
+    y = torch.empty(t.n, dtype=torch.float32, device="cuda")
+    xd = dev(x)
+    if t.qtype == synth.QTYPE_Q4_K:
+        w = dev(t.data)
+        qg.qg_gemv_q4k(w, xd, y, t.n, t.k)
+    else:
+        w = planar(t)
+        qg.qg_gemv_q6k(w, xd, y, t.n, t.k)
+    torch.cuda.synchronize()
+    qg.qg_device_status()
+    return y.cpu().numpy()
+
+
+def check_against_oracle(t, x, y):
+    exact = oracle.gemv_f64(t, x)
+    W = np.abs(oracle.dequant(t).astype(np.float64))
+    ax = np.abs(x.astype(np.float64))
+    blockmax = np.repeat(ax.reshape(-1, 32).max(axis=1), 32)
+    bound = 2 * F32_EPS * (W @ blockmax) + 8 * F32_EPS * (W @ ax) + 1e-30
+    err = np.abs(y.astype(np.float64) - exact)
+    assert np.all(err <= bound), f"max err/bound {float(np.max(err / bound)):.3g}"
+    ref = oracle.gemv(t, x)
+    rel = np.max(np.abs(y - ref)) / max(np.max(np.abs(ref)), 1e-30)
+    assert rel <= 1e-5, rel
+
+
+SMALL = [(1, 256), (13, 256), (37, 768), (300, 2560), (1000, 1024), (129, 3584), (64, 4096)]
+
+
+@pytest.mark.parametrize("n,k", SMALL)
+@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
+def test_gemv_small_shapes(qtype, n, k):
+    gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
+    t = gen(1000 + n + k, n, k)
+    x = synth.normal(77 + n, k)
+    check_against_oracle(t, x, run_gemv(t, x))
+
+
+@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
+def test_gemv_special_inputs(qtype):
+    gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
+    t = gen(5, 40, 512)
+    for x in [np.zeros(512, np.float32),
+              np.full(512, 3.0, np.float32),
+              (synth.normal(6, 512) * np.float32(1e-30)).astype(np.float32),  # tiny blocks
+              (synth.normal(7, 512) * np.float32(1e20)).astype(np.float32),   # huge values
+              np.where(np.arange(512) % 32 == 5, 100.0, 1e-3).astype(np.float32)]:  # one large per block
+        y = run_gemv(t, x)
+        if not np.any(x):
+            assert np.all(y == 0)
+        else:
+            check_against_oracle(t, x, y)
+
+
+# the standalone-kernel sweep shapes, all rows against the oracle
+SWEEP = [(1024, 1024), (6144, 1024), (9216, 2560), (2560, 9216)]
+
+
+@pytest.mark.parametrize("n,k", SWEEP)
+@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
+def test_gemv_sweep_shapes(qtype, n, k):
+    gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
+    t = gen(synth.subseed(synth.MASTER_SEED, f"sweep.{qtype}.{n}x{k}"), n, k)
+    x = synth.normal(synth.subseed(synth.MASTER_SEED, f"sweep.x.{k}"), k)
+    y = run_gemv(t, x)
+    ref = oracle.gemv(t, x)
+    rel = np.max(np.abs(y - ref)) / np.max(np.abs(ref))
+    assert rel <= 1e-5, rel
+    rows = np.arange(0, n, max(1, n // 97))
+    sub = synth.QTensor(t.data.reshape(n, -1)[rows].ravel().copy(), t.qtype, len(rows), k)
+    check_against_oracle(sub, x, y[rows])
+
+
+def test_q6k_planar_roundtrip_bytes():
+    t = synth.q6k_tensor(3, 13, 512)
+    p = planar(t).cpu().numpy()
+    n8, nb = 16, 2
+    assert p.size == n8 * nb * 210
+    blocks = t.data.reshape(13 * nb, 210)
+    ql = p[:n8 * nb * 128].reshape(n8 * nb, 128)
+    qh = p[n8 * nb * 128:n8 * nb * 192].reshape(n8 * nb, 64)
+    sc = p[n8 * nb * 192:n8 * nb * 208].reshape(n8 * nb, 16)
+    dd = p[n8 * nb * 208:].reshape(n8 * nb, 2)
+    for i in range(13 * nb):
+        b = blocks[i]
+        for c in range(4):
+            half, part = c >> 1, c & 1
+            assert np.array_equal(ql[i, 32 * c:32 * c + 16], b[64 * half + 16 * part:64 * half + 16 * part + 16])
+            assert np.array_equal(ql[i, 32 * c + 16:32 * c + 32],
+                                  b[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
+        assert np.array_equal(qh[i], b[128:192]) and np.array_equal(sc[i], b[192:208])
+        assert np.array_equal(dd[i], b[208:210])
+    assert not np.any(ql[13 * nb:]) and not np.any(dd[13 * nb:])
+
+
+# ------------------------------------------------------------------ argmax
+
+def lmhead(t, x):
+    w = planar(t)
+    ws = torch.zeros(qg.qg_lmhead_argmax_workspace_bytes() // 8, dtype=torch.int64, device="cuda")
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qg.qg_lmhead_argmax(w, dev(x), t.n, t.k, ws, tok)
+    torch.cuda.synchronize()
+    assert int(ws.abs().sum()) == 0  # the workspace is left zeroed
+    return int(tok.item())
+
+
+def test_lmhead_argmax_full_vocab():
+    V, H = 248320, 1024
+    t = synth.q6k_tensor(synth.subseed(synth.MASTER_SEED, "lmhead.test"), V, H)
+    x = synth.normal(synth.subseed(synth.MASTER_SEED, "lmhead.x"), H)
+    logits = oracle.gemv(t, x)
+    a, b = oracle.top2(logits)
+    assert a - b > 1e-3 * abs(a)  # a clear winner for this seed
+    assert lmhead(t, x) == oracle.argmax(logits)
+
+
+def test_lmhead_argmax_planted_ties_pick_first_index():
+    V, H = 50000, 1024
+    t = synth.q6k_tensor(11, V, H)
+    x = synth.normal(12, H)
+    rows = t.data.reshape(V, -1)
+    best = oracle.argmax(oracle.gemv(t, x))
+    rng = np.random.default_rng(3)
+    for trial in range(3):
+        copies = rng.choice(V, size=rng.integers(2, 8), replace=False)
+        data = rows.copy()
+        data[copies] = rows[best]  # identical bytes -> identical logits
+        tt = synth.QTensor(data.ravel(), t.qtype, V, H)
+        expect = int(min(list(copies) + [best]))
+        assert oracle.argmax(oracle.gemv(tt, x)) == expect
+        assert lmhead(tt, x) == expect
+
+
+def test_lmhead_ragged_vocab():
+    t = synth.q6k_tensor(21, 3001, 512)
+    x = synth.normal(22, 512)
+    assert lmhead(t, x) == oracle.argmax(oracle.gemv(t, x))
+
+
+def test_argmax_f32_planted_ties_inf_nan():
+    rng = np.random.default_rng(9)
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for trial in range(10):
+        n = int(rng.integers(1, 300000))
+        x = rng.standard_normal(n).astype(np.float32)
+        idx = np.sort(rng.choice(n, size=min(n, int(rng.integers(1, 9))), replace=False))
+        x[idx] = np.float32(x.max() + 1)
+        qg.qg_argmax_f32(dev(x), n, out)
+        torch.cuda.synchronize()
+        assert int(out.item()) == oracle.argmax(x) == idx[0]
+    x = np.zeros(1000, np.float32)
+    x[10], x[500], x[3] = np.nan, np.inf, np.nan
+    qg.qg_argmax_f32(dev(x), 1000, out)
+    torch.cuda.synchronize()
+    assert int(out.item()) == 500 == oracle.argmax(x)
+    x = np.full(7, np.nan, np.float32)
+    qg.qg_argmax_f32(dev(x), 7, out)
+    torch.cuda.synchronize()
+    assert int(out.item()) == 0 == oracle.argmax(x)
+    x = np.array([-1.0, -0.0, 0.0], np.float32)
+    qg.qg_argmax_f32(dev(x), 3, out)
+    torch.cuda.synchronize()
+    assert int(out.item()) == 1 == oracle.argmax(x)
+
+
+def test_gemv_argument_errors():
+    w = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1024, dtype=torch.float32, device="cuda")
+    y = torch.zeros(4, dtype=torch.float32, device="cuda")
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_gemv_q4k(w, x, y, 4, 300)
+    assert e.value.code == qg.QG_ERR_SHAPE
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_gemv_q4k(w, x, y, 0, 256)
+    assert e.value.code == qg.QG_ERR_EMPTY
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_gemv_q4k(w.data_ptr() + 4, x, y, 1, 256)
+    assert e.value.code == qg.QG_ERR_ARG
