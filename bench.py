@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Batch-1 decode benchmark of the hybrid Gated-DeltaNet / attention model on GB300.
+
+One step = one whole token (every layer, output norm, lm_head + argmax) of
+the chosen workload.  Default workload: the 0.8B-shaped hybrid (24 layers,
+850 prompt tokens fed one per step, then greedy tokens).  Prints ONE JSON line.
+
+  value      tokens/s of the device-resident greedy loop (qg_decode_greedy: one
+             CUDA-graph replay per token, token and position stay on the GPU),
+             timed with CUDA events on the state's stream, max over ranks.
+  e2e        tokens/s through qg_decode_token: per token an 8-byte H2D of
+             (token, position) from pinned memory and a 4-byte D2H of the id.
+  roofline   the dominant kernel (fused lm_head GEMV + argmax over the
+             248,320-row Q6_K table) timed live with CUDA events on its stream,
+             algorithmic bytes per launch / duration vs the measured HBM peak.
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload.
+
+  python bench.py [--workload 0.8b|4b|4b-long] [--steps K] [--warmup W]
+  python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+Multi-GPU: torchrun --nproc-per-node N bench.py --gpus N: N independent
+replicas (weak scaling, no collective on the data path).
+"""
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "batch-1 decode tok/s and achieved HBM GB/s vs 8 TB/s roofline, 1×GB300"
+WORKLOADS = {
+    "0.8b": (synth.CFG_0P8B, "random-init 0.8B-shaped hybrid: 24 layers (18 Gated DeltaNet + 6 full attention), "
+                             "hidden 1024, FFN 3584, vocab 248320, Q4_K + Q6_K (ffn_down, lm_head); "
+                             "850 seeded prompt tokens then greedy decode"),
+    "4b": (synth.CFG_4B, "random-init 4B-shaped hybrid: 32 layers (24 Gated DeltaNet + 8 full attention), "
+                         "hidden 2560, FFN 9216, vocab 248320, 32 v-heads over 16 k-heads; "
+                         "850 seeded prompt tokens then greedy decode"),
+    "4b-long": (synth.CFG_4B_LONG, "4B-shaped hybrid, f32 KV cache of 8192 positions prefilled with N(0,1) rows "
+                                   "0..7999, greedy decode from position 8000"),
+}
+
+
+def algorithmic_bytes(cfg, t_rows):
+    """HBM bytes one token must move at KV length t_rows (rows read, incl. the
+    new one): every weight as stored (Q4_K 144 B / Q6_K 210 B per 256), the f32
+    vectors the kernels read, DeltaNet state and conv window read + write, the
+    KV rows read plus the K/V row written, the embedding row."""
+    H, F = cfg.hidden, cfg.ffn
+    q4 = lambda n, k: n * k // 256 * 144  # noqa: E731
+    q6 = lambda n, k: n * k // 256 * 210  # noqa: E731
+    total = 0
+    for kind in cfg.kinds():
+        total += 2 * q4(F, H) + q6(H, F) + 2 * H * 4
+        if kind == synth.DELTANET:
+            total += q4(cfg.conv_dim + 2 * cfg.n_v_heads + cfg.v_dim, H) + q4(H, cfg.v_dim)
+            total += cfg.conv_dim * cfg.conv_kernel * 4 + 2 * cfg.n_v_heads * 4 + cfg.head_v_dim * 4
+            total += 2 * cfg.n_v_heads * cfg.head_v_dim * cfg.head_k_dim * 4  # state r + w
+            total += 2 * cfg.conv_dim * (cfg.conv_kernel - 1) * 4              # window r + w
+        else:
+            total += q4(2 * cfg.q_dim + 2 * cfg.kv_dim, H) + q4(H, cfg.q_dim) + 2 * cfg.head_dim * 4
+            total += 2 * t_rows * cfg.kv_dim * 4 + 2 * cfg.kv_dim * 4            # KV read + row write
+    total += q6(cfg.vocab, H) + H * 4 + H * 4                                   # lm_head, out norm, embed row
+    return total
+
+
+def lmhead_bytes(cfg):
+    return cfg.vocab * cfg.hidden // 256 * 210 + cfg.hidden * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("sources") != kernel_sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        rows = [ln.split(",") for ln in self.f.read().strip().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def prefill(qg, m, st, cfg, long_ctx):
+    """Bring a state to the start of the timed decode; returns the next position
+    and the token to feed there."""
+    if long_ctx:
+        for il, kind in enumerate(cfg.kinds()):
+            if kind == synth.DELTANET:
+                st.upload_layer(il, *synth.initial_deltanet_state(cfg, il))
+            else:
+                st.upload_kv(il, *synth.long_context_kv(cfg, il, synth.LONG_PREFILL))
+        first = int(synth.tokens(synth.subseed(synth.MASTER_SEED, "long.first"), cfg.vocab, 1)[0])
+        tok = qg.qg_decode_token(m, st, first, synth.LONG_PREFILL)
+        return synth.LONG_PREFILL + 1, tok
+    toks = synth.prompt_tokens(cfg)
+    tok = 0
+    for pos, t in enumerate(toks):
+        tok = qg.qg_decode_token(m, st, int(t), pos)
+    return len(toks), tok
+
+
+def cpu_baseline(cfg, budget_s=12.0):
+    """The oracle as it stands, on the host cores, decoding the workload's prompt
+    from position 0 until the time budget is spent."""
+    import oracle
+    w = synth.make_model_weights(cfg)
+    om = oracle.Model(w)
+    ost = oracle.State(om)
+    toks = synth.prompt_tokens(cfg)
+    n, t0 = 0, time.perf_counter()
+    while n < len(toks) and (n < 2 or time.perf_counter() - t0 < budget_s):
+        oracle.forward_token(om, ost, int(toks[n]), n)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 4), "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} prompt tokens decoded from position 0 by the f32 C oracle (OpenMP over GEMV rows), "
+                      f"{dt:.1f} s"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import quantized_gemv_gated_gb300 as qg
+    torch.cuda.set_device(local)
+    cfg, desc = WORKLOADS[args.workload]
+    long_ctx = args.workload == "4b-long"
+    K, W = args.steps, args.warmup
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w, device=local)
+    st = qg.State(m, cfg.max_seq_len)
+    # warm up (graph capture, clocks), then restart the sequence for the timed run
+    pos, _ = prefill(qg, m, st, cfg, long_ctx)
+    qg.qg_decode_greedy(m, st, pos, W)
+    st.reset()
+    pos0, _ = prefill(qg, m, st, cfg, long_ctx)
+    assert pos0 + K <= cfg.max_seq_len, "steps exceed the KV cache"
+    ext = torch.cuda.ExternalStream(st.stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    e0.record(ext)
+    toks = qg.qg_decode_greedy(m, st, pos0, K)
+    e1.record(ext)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    barrier(world)
+    dt = max_over_ranks(e0.elapsed_time(e1) / 1000.0, world)
+    stats = st.stats()
+    nodes = stats["graph_kernel_nodes"]
+
+    # e2e: the host API, one decode_token per step on a second state
+    st2 = qg.State(m, cfg.max_seq_len)
+    p2, tok = prefill(qg, m, st2, cfg, long_ctx)
+    ext2 = torch.cuda.ExternalStream(st2.stream)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    f0.record(ext2)
+    for i in range(K):
+        tok = qg.qg_decode_token(m, st2, tok, p2 + i)
+    f1.record(ext2)
+    f1.synchronize()
+    dt2 = max_over_ranks(f0.elapsed_time(f1) / 1000.0, world)
+    st2.close()
+
+    # dominant kernel: fused lm_head GEMV + argmax, timed alone on its stream
+    wl = torch.from_numpy(w.lm_head.data).cuda()
+    wp = torch.empty(qg.qg_q6k_planar_bytes(cfg.vocab, cfg.hidden), dtype=torch.uint8, device="cuda")
+    qg.qg_q6k_to_planar(wl, wp, cfg.vocab, cfg.hidden)
+    del wl
+    x = torch.from_numpy(synth.normal(7, cfg.hidden)).cuda()
+    ws = torch.zeros(2, dtype=torch.int64, device="cuda")
+    tk = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s3 = torch.cuda.Stream()
+    with torch.cuda.stream(s3):
+        for _ in range(3):
+            qg.qg_lmhead_argmax(wp, x, cfg.vocab, cfg.hidden, ws, tk, s3)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        g0.record(s3)
+        for _ in range(reps):
+            qg.qg_lmhead_argmax(wp, x, cfg.vocab, cfg.hidden, ws, tk, s3)
+        g1.record(s3)
+    g1.synchronize()
+    t_lm = g0.elapsed_time(g1) / 1000.0 / reps
+    peak, peak_kind = measured_peaks()
+    lm_gbs = lmhead_bytes(cfg) / t_lm / 1e9
+    qg.qg_device_status()
+
+    tokps = world * K / dt
+    mean_t = pos0 + (K + 1) / 2.0  # KV rows read, averaged over the timed steps
+    bpt = algorithmic_bytes(cfg, mean_t)
+    step_gbs = bpt * K / dt / 1e9 * world
+    out = {
+        "metric": METRIC, "value": round(tokps, 3), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(1000.0 * dt / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
+        "config": {"workload": f"{args.workload}: {desc}", "global_batch": world, "seq_len": cfg.max_seq_len,
+                   "parallelism": f"replicas x{world}", "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
+                   "l2": f"no flush: {bpt / 1e6:.1f} MB of weights and state per token > 129 MB L2",
+                   "greedy_tokens_head": [int(t) for t in toks[:4]]},
+        "bytes_per_token": int(bpt),
+        "step_roofline": {"achieved": round(step_gbs / world, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(step_gbs / world / peak, 4), "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": "lm_head GEMV + argmax (Q6_K, vocab x hidden)",
+                     "achieved": round(lm_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(lm_gbs / peak, 4),
+                     "traffic": ncu_traffic("lmhead_argmax"), "bytes_per_launch": lmhead_bytes(cfg),
+                     "launch_us": round(t_lm * 1e6, 2), "peak_kind": peak_kind},
+        "clocks": clocks,
+        "e2e": {"value": round(world * K / dt2, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": int(nodes * K),
+        "kernels_per_token": int(nodes),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    cfg, desc = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    w = synth.make_model_weights(cfg)
+    om = oracle.Model(w)
+    ost = oracle.State(om)
+    toks = synth.prompt_tokens(cfg)
+    for i in range(W):
+        oracle.forward_token(om, ost, int(toks[i]), i)
+    t0 = time.perf_counter()
+    for i in range(W, W + K):
+        oracle.forward_token(om, ost, int(toks[i % len(toks)]), i)
+    dt = time.perf_counter() - t0
+    v = round(K / dt, 4)
+    sample = (f"{K} tokens of the workload's prompt decoded at positions {W}..{W + K - 1} by the f32 C oracle "
+              f"(OpenMP over GEMV rows) after {W} warm-up tokens")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(1000.0 * dt / K, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
+        "config": {"workload": f"{args.workload}: {desc}", "global_batch": 1, "seq_len": cfg.max_seq_len},
+        "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="0.8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        args.steps = min(args.steps, 16)  # bounded sample of the CPU oracle
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

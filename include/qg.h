@@ -156,6 +156,9 @@ int qg_state_download_layer(qg_state* s, int il, float* a, float* b, size_t* n);
 /* The residual stream after the last completed step ([hidden], host). */
 int qg_state_download_hidden(qg_state* s, float* hidden_host);
 int qg_state_kv_len(const qg_state* s, int* kv_len);
+/* The CUDA stream every decode call of this state runs on (owned by the
+ * state), e.g. to record timing events around qg_decode_greedy. */
+int qg_state_stream(const qg_state* s, qg_stream* out);
 int qg_state_stats(const qg_state* s, qg_stats* out);
 
 /* ------------------------------------------------------- building blocks

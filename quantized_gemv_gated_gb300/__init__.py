@@ -27,7 +27,7 @@ ERROR_NAMES = {0: "QG_OK", -1: "QG_ERR_SHAPE", -2: "QG_ERR_QTYPE", -3: "QG_ERR_E
 EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
-    "qg_state_kv_len", "qg_state_stats", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
+    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
@@ -102,6 +102,7 @@ def lib():
             "qg_state_download_layer": [p, i, p, p, ctypes.POINTER(sz)],
             "qg_state_download_hidden": [p, p],
             "qg_state_kv_len": [p, ctypes.POINTER(i)],
+            "qg_state_stream": [p, ctypes.POINTER(p)],
             "qg_state_stats": [p, ctypes.POINTER(QgStats)],
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
@@ -320,6 +321,13 @@ class State:
         v = ctypes.c_int()
         _check(lib().qg_state_kv_len(self.handle, ctypes.byref(v)))
         return v.value
+
+    @property
+    def stream(self):
+        """The state's CUDA stream handle (int)."""
+        v = ctypes.c_void_p()
+        _check(lib().qg_state_stream(self.handle, ctypes.byref(v)))
+        return v.value or 0
 
     def stats(self):
         st = QgStats()

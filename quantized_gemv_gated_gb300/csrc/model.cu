@@ -527,6 +527,12 @@ int qg_state_kv_len(const qg_state* s, int* kv_len) {
     return QG_OK;
 }
 
+int qg_state_stream(const qg_state* s, qg_stream* out) {
+    if (!s || !out) return set_err(QG_ERR_ARG, "state_stream: NULL argument");
+    *out = reinterpret_cast<qg_stream>(s->stream);
+    return QG_OK;
+}
+
 int qg_state_stats(const qg_state* s, qg_stats* out) {
     if (!s || !out) return set_err(QG_ERR_ARG, "stats: NULL argument");
     *out = s->stats;

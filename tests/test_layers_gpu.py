@@ -1,0 +1,254 @@
+"""Layer and whole-token parity on the GPU through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Bars (the benchmark spec): hidden states within 1e-3 max relative error (normwise:
+max|gpu - ref| / max|ref|), token ids and KV/state indexing exact; graph and
+eager replays of the step bitwise identical.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+qg = pytest.importorskip("quantized_gemv_gated_gb300")
+
+TOL = 1e-3
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+@pytest.fixture(scope="module")
+def layer_model():
+    cfg = synth.CFG_LAYER
+    w = synth.make_model_weights(cfg)
+    return cfg, w, qg.Model(w), oracle.Model(w)
+
+
+def _gentle_gates(w, cfg):
+    """Same layer with small ssm_alpha / ssm_beta scales, so that the decay g
+    and beta sit inside (0, 1) instead of saturating (random full-scale
+    weights drive |alpha|, |beta| to ~100)."""
+    w2 = dataclasses.replace(w, layers=list(w.layers))
+    L = dataclasses.replace(w.layers[0])
+    s = synth.subseed(synth.MASTER_SEED, "gentle")
+    L.ssm_alpha = synth.q4k_tensor(s + 1, cfg.n_v_heads, cfg.hidden, dmax=2e-4)
+    L.ssm_beta = synth.q4k_tensor(s + 2, cfg.n_v_heads, cfg.hidden, dmax=2e-4)
+    w2.layers[0] = L
+    return w2
+
+
+@pytest.mark.parametrize("gentle", [False, True])
+def test_deltanet_layer_8_steps_from_seed(layer_model, gentle):
+    cfg, w, m, om = layer_model
+    if gentle:
+        w = _gentle_gates(w, cfg)
+        m, om = qg.Model(w), oracle.Model(w)
+    st = qg.State(m, 16)
+    ost = oracle.State(om)
+    conv0, ssm0 = synth.initial_deltanet_state(cfg, 0)
+    st.upload_layer(0, conv0, ssm0)
+    ost.conv[0][:] = conv0
+    ost.ssm[0][:] = ssm0
+    xs = synth.layer_inputs(cfg, 8)
+    worst = 0.0
+    for step in range(8):
+        h = dev(xs[step])
+        qg.qg_deltanet_step(m, st, 0, h)
+        torch.cuda.synchronize()
+        ref = oracle.deltanet_layer(om, ost, 0, xs[step])
+        got = h.cpu().numpy()
+        e = rel(got, ref)
+        worst = max(worst, e)
+        assert e <= TOL, f"step {step}: hidden {e:.3g}"
+        conv, ssm = st.download_layer(0)
+        assert rel(conv, ost.conv[0]) <= 1e-5, f"step {step}: conv window"
+        assert rel(ssm, ost.ssm[0]) <= TOL, f"step {step}: recurrent state {rel(ssm, ost.ssm[0]):.3g}"
+    qg.qg_device_status()
+    print(f"deltanet layer, 8 free-running steps, worst hidden rel err {worst:.3g}")
+
+
+def test_deltanet_layer_teacher_forced_each_step(layer_model):
+    cfg, w, m, om = layer_model
+    st = qg.State(m, 16)
+    ost = oracle.State(om)
+    conv0, ssm0 = synth.initial_deltanet_state(cfg, 0)
+    ost.conv[0][:] = conv0
+    ost.ssm[0][:] = ssm0
+    xs = synth.layer_inputs(cfg, 8)
+    for step in range(8):
+        st.upload_layer(0, ost.conv[0], ost.ssm[0])  # both sides start the step from the oracle state
+        h = dev(xs[step])
+        qg.qg_deltanet_step(m, st, 0, h)
+        ref = oracle.deltanet_layer(om, ost, 0, xs[step])
+        assert rel(h.cpu().numpy(), ref) <= 1e-4
+        conv, ssm = st.download_layer(0)
+        assert rel(conv, ost.conv[0]) <= 1e-5 and rel(ssm, ost.ssm[0]) <= 1e-4
+
+
+def _attn_cfg(base, max_seq):
+    return dataclasses.replace(base, name=base.name + "-attn1", n_layers=1, vocab=512,
+                               layer_kinds=(synth.ATTENTION,), max_seq_len=max_seq)
+
+
+@pytest.mark.parametrize("base,max_seq,positions", [
+    (synth.CFG_TINY, 96, [0, 1, 31, 32, 33, 63, 64, 95]),
+    (synth.CFG_0P8B, 1024, [0, 849, 914, 1023]),
+    (synth.CFG_4B, 8192, [8000, 8191]),
+])
+def test_attention_layer_positions(base, max_seq, positions):
+    cfg = _attn_cfg(base, max_seq)
+    w = synth.make_model_weights(cfg)
+    m, om = qg.Model(w), oracle.Model(w)
+    for pos in positions:
+        st = qg.State(m, max_seq)
+        ost = oracle.State(om)
+        if pos > 0:
+            k, v = synth.long_context_kv(cfg, 0, pos)
+            st.upload_kv(0, k, v)
+            ost.kc[0][:pos] = k
+            ost.vc[0][:pos] = v
+        x = synth.normal(synth.subseed(synth.MASTER_SEED, f"attn.x.{pos}"), cfg.hidden)
+        h = dev(x)
+        qg.qg_attn_decode_step(m, st, 0, h, pos)
+        ref = oracle.attention_layer(om, ost, 0, x, pos)
+        e = rel(h.cpu().numpy(), ref)
+        assert e <= TOL, f"pos {pos}: hidden {e:.3g}"
+        kk, vv = st.download_layer(0)
+        assert kk.shape[0] == pos + 1 and st.kv_len == pos + 1
+        assert rel(kk[pos], ost.kc[0][pos]) <= 1e-5, f"pos {pos}: K row"
+        assert rel(vv[pos], ost.vc[0][pos]) <= 1e-5, f"pos {pos}: V row"
+        if pos > 0:  # rows below pos are untouched
+            assert np.array_equal(kk[:pos], ost.kc[0][:pos]) and np.array_equal(vv[:pos], ost.vc[0][:pos])
+        st.close()
+    qg.qg_device_status()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg = synth.CFG_TINY
+    w = synth.make_model_weights(cfg)
+    return cfg, w, qg.Model(w), oracle.Model(w)
+
+
+def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny):
+    cfg, w, m, om = tiny
+    sg, se = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
+    ost = oracle.State(om)
+    toks = synth.prompt_tokens(cfg, 40)
+    worst = 0.0
+    for pos, t in enumerate(toks):
+        a = qg.qg_decode_token(m, sg, int(t), pos)
+        b = qg.qg_decode_token_eager(m, se, int(t), pos)
+        ref, ref_h, logits = oracle.forward_token(om, ost, int(t), pos, want_logits=True)
+        hg, he = sg.download_hidden(), se.download_hidden()
+        assert np.array_equal(hg, he) and a == b, f"pos {pos}: graph and eager differ"
+        e = rel(hg, ref_h)
+        worst = max(worst, e)
+        assert e <= TOL, f"pos {pos}: hidden {e:.3g}"
+        if a != ref:
+            v1, v2 = oracle.top2(logits)
+            pytest.fail(f"pos {pos}: token {a} != oracle {ref} (oracle top-2 margin {v1 - v2:.4g})")
+    st = sg.stats()
+    assert st["graph_captures"] == 1 and st["graph_launches"] == len(toks)
+    assert st["d2h_bytes"] == 4 * len(toks) and st["h2d_bytes"] == 8 * len(toks)
+    print(f"tiny model, 40 tokens: worst hidden rel err {worst:.3g}, {st['graph_kernel_nodes']} kernel nodes")
+
+
+def test_greedy_device_loop_matches_oracle_greedy(tiny):
+    cfg, w, m, om = tiny
+    st = qg.State(m, cfg.max_seq_len)
+    ost = oracle.State(om)
+    toks = synth.prompt_tokens(cfg, 12)
+    for pos, t in enumerate(toks):
+        last = qg.qg_decode_token(m, st, int(t), pos)
+        ref, _, _ = oracle.forward_token(om, ost, int(t), pos)
+        assert last == ref
+    n = 30
+    got = qg.qg_decode_greedy(m, st, len(toks), n)
+    expect, cur = [], ref
+    for i in range(n):
+        cur, _, _ = oracle.forward_token(om, ost, cur, len(toks) + i)
+        expect.append(cur)
+    assert got.tolist() == expect
+    assert st.kv_len == len(toks) + n
+
+
+def test_no_allocation_after_first_step(tiny):
+    cfg, w, m, om = tiny
+    st = qg.State(m, cfg.max_seq_len)
+    toks = synth.prompt_tokens(cfg, 20)
+    qg.qg_decode_token(m, st, int(toks[0]), 0)
+    s0 = st.stats()
+    free0 = torch.cuda.mem_get_info()[0]
+    for pos in range(1, 20):
+        qg.qg_decode_token(m, st, int(toks[pos]), pos)
+    s1 = st.stats()
+    assert s1["device_allocs"] == s0["device_allocs"] and s1["graph_captures"] == 1
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert s1["d2h_bytes"] - s0["d2h_bytes"] == 4 * 19
+
+
+def test_state_reset_replays_identically(tiny):
+    cfg, w, m, om = tiny
+    st = qg.State(m, cfg.max_seq_len)
+    toks = synth.prompt_tokens(cfg, 8)
+    a = [qg.qg_decode_token(m, st, int(t), p) for p, t in enumerate(toks)]
+    ha = st.download_hidden()
+    st.reset()
+    assert st.kv_len == 0
+    b = [qg.qg_decode_token(m, st, int(t), p) for p, t in enumerate(toks)]
+    assert a == b and np.array_equal(ha, st.download_hidden())
+
+
+def test_error_codes(tiny):
+    cfg, w, m, om = tiny
+    st = qg.State(m, cfg.max_seq_len)
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_decode_token(m, st, cfg.vocab, 0)
+    assert e.value.code == qg.QG_ERR_TOKEN
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_decode_token(m, st, 1, cfg.max_seq_len)
+    assert e.value.code == qg.QG_ERR_POS
+    h = torch.zeros(cfg.hidden, device="cuda")
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_deltanet_step(m, st, 3, h)  # layer 3 is attention
+    assert e.value.code == qg.QG_ERR_LAYER_KIND
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_attn_decode_step(m, st, 0, h, 0)
+    assert e.value.code == qg.QG_ERR_LAYER_KIND
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_attn_decode_step(m, st, 3, h, cfg.max_seq_len)
+    assert e.value.code == qg.QG_ERR_POS
+    with pytest.raises(qg.QgError) as e:
+        qg.State(m, 0)
+    assert e.value.code == qg.QG_ERR_SHAPE
+    k, v = st.download_layer(3)
+    assert k.size == 0 and v.size == 0  # nothing written yet
+    with pytest.raises(qg.QgError) as e:
+        st.upload_layer(3, np.zeros(1, np.float32), np.zeros(1, np.float32))
+    assert e.value.code == qg.QG_ERR_LAYER_KIND
+    # a lm_head whose shape is not vocab x hidden, a wrong qtype, an empty tensor
+    bad = dataclasses.replace(w, lm_head=synth.q6k_tensor(1, cfg.vocab - 1, cfg.hidden))
+    with pytest.raises(qg.QgError) as e:
+        qg.Model(bad)
+    assert e.value.code == qg.QG_ERR_SHAPE
+    L0 = dataclasses.replace(w.layers[0], ffn_down=synth.q4k_tensor(1, cfg.hidden, cfg.ffn))
+    with pytest.raises(qg.QgError) as e:
+        qg.Model(dataclasses.replace(w, layers=[L0] + list(w.layers[1:])))
+    assert e.value.code == qg.QG_ERR_QTYPE
+    bad_heads = dataclasses.replace(cfg, n_v_heads=3)
+    with pytest.raises(qg.QgError) as e:
+        qg.Model(dataclasses.replace(w, cfg=bad_heads))
+    assert e.value.code == qg.QG_ERR_SHAPE
