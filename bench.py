@@ -180,7 +180,7 @@ def barrier(world):
         dist.barrier()
 
 
-def prefill(qg, m, st, cfg, long_ctx):
+def prefill(qg, m, st, cfg, long_ctx, n_prompt=synth.PROMPT_LEN):
     """Bring a state to the start of the timed decode; returns the next position
     and the token to feed there."""
     if long_ctx:
@@ -192,7 +192,7 @@ def prefill(qg, m, st, cfg, long_ctx):
         first = int(synth.tokens(synth.subseed(synth.MASTER_SEED, "long.first"), cfg.vocab, 1)[0])
         tok = qg.qg_decode_token(m, st, first, synth.LONG_PREFILL)
         return synth.LONG_PREFILL + 1, tok
-    toks = synth.prompt_tokens(cfg)
+    toks = synth.prompt_tokens(cfg, n_prompt)
     tok = 0
     for pos, t in enumerate(toks):
         tok = qg.qg_decode_token(m, st, int(t), pos)
@@ -228,10 +228,10 @@ def run_ours(args, rank, world, local):
     m = qg.Model(w, device=local)
     st = qg.State(m, cfg.max_seq_len)
     # warm up (graph capture, clocks), then restart the sequence for the timed run
-    pos, _ = prefill(qg, m, st, cfg, long_ctx)
+    pos, _ = prefill(qg, m, st, cfg, long_ctx, args.prompt)
     qg.qg_decode_greedy(m, st, pos, W)
     st.reset()
-    pos0, _ = prefill(qg, m, st, cfg, long_ctx)
+    pos0, _ = prefill(qg, m, st, cfg, long_ctx, args.prompt)
     assert pos0 + K <= cfg.max_seq_len, "steps exceed the KV cache"
     ext = torch.cuda.ExternalStream(st.stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -250,19 +250,21 @@ def run_ours(args, rank, world, local):
     nodes = stats["graph_kernel_nodes"]
 
     # e2e: the host API, one decode_token per step on a second state
-    st2 = qg.State(m, cfg.max_seq_len)
-    p2, tok = prefill(qg, m, st2, cfg, long_ctx)
-    ext2 = torch.cuda.ExternalStream(st2.stream)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    f0.record(ext2)
-    for i in range(K):
-        tok = qg.qg_decode_token(m, st2, tok, p2 + i)
-    f1.record(ext2)
-    f1.synchronize()
-    dt2 = max_over_ranks(f0.elapsed_time(f1) / 1000.0, world)
-    st2.close()
+    dt2 = None
+    if not args.no_e2e:
+        st2 = qg.State(m, cfg.max_seq_len)
+        p2, tok = prefill(qg, m, st2, cfg, long_ctx, args.prompt)
+        ext2 = torch.cuda.ExternalStream(st2.stream)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        f0.record(ext2)
+        for i in range(K):
+            tok = qg.qg_decode_token(m, st2, tok, p2 + i)
+        f1.record(ext2)
+        f1.synchronize()
+        dt2 = max_over_ranks(f0.elapsed_time(f1) / 1000.0, world)
+        st2.close()
 
     # dominant kernel: fused lm_head GEMV + argmax, timed alone on its stream
     wl = torch.from_numpy(w.lm_head.data).cuda()
@@ -308,8 +310,8 @@ def run_ours(args, rank, world, local):
                      "traffic": ncu_traffic("lmhead_argmax"), "bytes_per_launch": lmhead_bytes(cfg),
                      "launch_us": round(t_lm * 1e6, 2), "peak_kind": peak_kind},
         "clocks": clocks,
-        "e2e": {"value": round(world * K / dt2, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
-                "d2h_bytes_per_step": 4},
+        "e2e": ({"value": round(world * K / dt2, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
+                 "d2h_bytes_per_step": 4} if dt2 else None),
         "gpu_launches": int(nodes * K),
         "kernels_per_token": int(nodes),
     }
@@ -356,7 +358,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="0.8b")
+    ap.add_argument("--prompt", type=int, default=synth.PROMPT_LEN,
+                    help="prompt tokens fed before the timed decode (default 850)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

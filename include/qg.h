@@ -166,7 +166,7 @@ int qg_state_stats(const qg_state* s, qg_stats* out);
 
 /* y[n] = sum_k deq(W[n][k]) * x[k] (forward_qwen35_cuda.rs gemv_dispatch,
  * float variant).  x enters as a 24-bit block-fixed-point value: each element
- * to within 2^-23 of the largest magnitude of its 32-element block (the
+ * to within 2^-23 of the largest magnitude of its 256-element block (the
  * precision of f32 for that largest element); sub-block sums are exact
  * integers, accumulated in f32.
  * w: Q4_K, raw GGUF layout, 16-byte aligned.  x: [k] f32.  y: [n] f32.

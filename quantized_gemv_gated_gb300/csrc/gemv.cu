@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(1024) argmax_f32_kernel(const float* __restric
 // (max is exact, so the result does not depend on arrival order), and the
 // last CTA to arrive publishes the token and re-zeroes the workspace.
 struct EpiArgmax : EpiBase {
+    static constexpr bool kDeferred = false;
     unsigned long long* ws;  // ws[0]: best key; ws[1] low word: arrivals
     uint32_t* tok;
     unsigned long long best;

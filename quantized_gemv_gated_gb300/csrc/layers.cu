@@ -38,7 +38,10 @@ struct EpiDnIn : EpiBase {
     float* dt;
     float* beta;
     float* z;
-    __device__ void row(int r, float v) {
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) row_out(r, ys[r - r0]);
+    }
+    __device__ void row_out(int r, float v) {
         if (r < C) {
             // causal conv1d + SiLU, then roll the window (gdn_causal_conv1d_silu_into)
             const float* kw = wconv + static_cast<size_t>(r) * K;
@@ -74,10 +77,13 @@ struct EpiAttnIn : EpiBase {
     int qd2, kvd;
     int pos;
     __device__ void start() { pos = __ldcg(slots + 1); }
-    __device__ void row(int r, float v) {
-        if (r < qd2) qf[r] = v;
-        else if (r < qd2 + kvd) kraw[r - qd2] = v;
-        else vcache[static_cast<size_t>(pos) * kvd + (r - qd2 - kvd)] = v;
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) {
+            const float v = ys[r - r0];
+            if (r < qd2) qf[r] = v;
+            else if (r < qd2 + kvd) kraw[r - qd2] = v;
+            else vcache[static_cast<size_t>(pos) * kvd + (r - qd2 - kvd)] = v;
+        }
     }
 };
 
@@ -85,6 +91,7 @@ struct EpiAttnIn : EpiBase {
 // (the next step's embedding input) and slots[2] (the host readback, with
 // bit 31 set when any kernel of the step set the device error word).
 struct EpiArgmaxStep : EpiBase {
+    static constexpr bool kDeferred = false;
     unsigned long long* ws;
     int* slots;
     uint32_t* hist;
@@ -186,10 +193,16 @@ __global__ void __launch_bounds__(256) delta_kernel(const float* __restrict__ co
 }
 
 // ------------------------------------------------------ GQA decode attention
-// Grid (max_splits, n_kv_heads).  CTA (s, g) covers cache rows
-// [s*T, min((s+1)*T, pos+1)) for the GS query heads of kv group g (contiguous
-// groups).  head_dim = 256: lane owns dims 4*lane..+3 and 128+4*lane..+3.
+// Grid (max_splits, n_kv_heads), 8 consumer warps + 1 producer warp.  CTA
+// (s, g) covers cache rows [s*T, min((s+1)*T, pos+1)) for the GS query heads
+// of kv group g (contiguous groups).  The producer streams the split's K and V
+// rows of group g (1 KB each) into a shared-memory ring with bulk copies,
+// 8 keys per stage; rows older than pos are fetched before the dependency
+// wait, V[pos] (written by the previous kernel) after it, and K[pos] is
+// computed here.  head_dim = 256: lane owns dims 4*lane..+3 and 128+4*lane..+3.
 constexpr int kHd = 256;
+constexpr int kAttnStages = 4;
+constexpr int kKeysPerStage = 8;
 
 struct AttnArgs {
     const float* qf;     // [nh][2*hd]: q then gate per head
@@ -203,39 +216,105 @@ struct AttnArgs {
     float* part_ml;      // [nkv][max_splits][GS][2]
     unsigned* count;     // [nkv]
     float* out;          // [nh*hd], gated
+    unsigned* err;
     int kvd, T, max_splits, n_rot;
     float theta_scale, eps;
 };
 
+template <int GS>
+__host__ __device__ inline int attn_smem_floats() {
+    return GS * kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd + 64 * GS * 2 + kAttnStages * kKeysPerStage * 2 * kHd;
+}
+
+__device__ __forceinline__ void row8(const float* p, int lane, float* v) {
+    const float4 a = *reinterpret_cast<const float4*>(p + 4 * lane);
+    const float4 b = *reinterpret_cast<const float4*>(p + 128 + 4 * lane);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 __device__ __forceinline__ void load_row8(const float* p, int lane, float* v) {
     const float4 a = __ldcg(reinterpret_cast<const float4*>(p + 4 * lane));
     const float4 b = __ldcg(reinterpret_cast<const float4*>(p + 128 + 4 * lane));
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+__device__ __forceinline__ int dim8(int lane, int j) { return j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4; }
 
 template <int GS>
-__global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
-    extern __shared__ __align__(16) float sm[];
-    float* q_s = sm;                     // [GS][hd]
-    float* k_s = q_s + GS * kHd;         // [hd]
-    float* cs = k_s + kHd;               // [hd/2]
-    float* sn = cs + kHd / 2;            // [hd/2]
-    float* wml = sn + kHd / 2;           // [8][GS][2]
-    float* wacc = wml + 8 * GS * 2;      // [8][GS][hd]
+__global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
+    extern __shared__ __align__(128) float sm[];
+    __shared__ uint64_t full[kAttnStages], empty[kAttnStages];
     __shared__ int last_flag;
+    float* ring = sm;                                        // [stages][8 keys][K row | V row]
+    float* q_s = ring + kAttnStages * kKeysPerStage * 2 * kHd;  // [GS][hd]
+    float* k_s = q_s + GS * kHd;                             // [hd]
+    float* cs = k_s + kHd;                                   // [hd/2]
+    float* sn = cs + kHd / 2;                                // [hd/2]
+    float* wml = sn + kHd / 2;                               // [8][GS][2]
+    float* wacc = wml + 8 * GS * 2;                          // [8][GS][hd]
+    float* cml = wacc + 8 * GS * kHd;                        // [64][GS][2] split (m, l) of the combine
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x, g = blockIdx.y;
     pdl_launch_dependents();
-    pdl_wait();
+    // the position is written before the first kernel of the step: safe to read now
     const int pos = __ldcg(a.slots + 1);
     const int t_len = pos + 1;
     const int n_act = (t_len + a.T - 1) / a.T;
     if (s >= n_act) return;
     const bool has_new = (s == n_act - 1);  // the split holding row pos
+    const int t0 = s * a.T, t1 = min(t0 + a.T, t_len);
+    const int nst = (t1 - t0 + kKeysPerStage - 1) / kKeysPerStage;
     const int half = a.n_rot / 2;
 
+    if (tid == 0) {
+        for (int i = 0; i < kAttnStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 8);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 8) {
+        // ----------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            bool waited = false, ok = true;
+            int issued = 0;
+            for (int st = 0; st < nst; ++st) {
+                const int slot = st % kAttnStages;
+                if (st >= kAttnStages && !mbar_wait(&empty[slot], ((st / kAttnStages) - 1) & 1)) {
+                    atomicOr(a.err, DEVERR_EMPTY_WAIT);
+                    ok = false;
+                    break;
+                }
+                const int k0 = t0 + st * kKeysPerStage, k1 = min(k0 + kKeysPerStage, t1);
+                if (!waited && k1 > pos) {
+                    pdl_wait();  // V[pos] is written by the previous kernel
+                    waited = true;
+                }
+                unsigned bytes = 0;
+                for (int t = k0; t < k1; ++t) bytes += (t == pos ? 1u : 2u) * kHd * 4u;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+                float* st_base = ring + static_cast<size_t>(slot) * kKeysPerStage * 2 * kHd;
+                for (int t = k0; t < k1; ++t) {
+                    float* dst = st_base + (t - k0) * 2 * kHd;
+                    const size_t off = static_cast<size_t>(t) * a.kvd + g * kHd;
+                    if (t != pos) bulk_g2s(dst, a.kc + off, kHd * 4, &full[slot], pol);
+                    bulk_g2s(dst + kHd, a.vc + off, kHd * 4, &full[slot], pol);
+                }
+                issued = st + 1;
+            }
+            if (!ok)
+                for (int st = max(0, issued - kAttnStages); st < issued; ++st)
+                    if (!mbar_wait(&full[st % kAttnStages], (st / kAttnStages) & 1)) atomicOr(a.err, DEVERR_DRAIN_WAIT);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    pdl_wait();
     // rope angles: theta_0 = pos, theta_{i+1} = theta_i * theta_scale (f32 running product)
     if (tid < half) {
         float th = static_cast<float>(pos);
@@ -258,12 +337,9 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
         ss = warp_sum(ss);
         const float r = 1.0f / sqrtf(ss / static_cast<float>(kHd) + a.eps);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int d = (i < 4 ? 4 * lane + i : 128 + 4 * lane + i - 4);
-            dst[d] = (v[i] * r) * __ldg(w + d);
-        }
+        for (int i = 0; i < 8; ++i) dst[dim8(lane, i)] = (v[i] * r) * __ldg(w + dim8(lane, i));
     }
-    __syncthreads();
+    bar_sync(1, 256);
     // partial NEOX rope on pairs (i, i + n_rot/2), i < n_rot/2 (gdn_partial_neox_rope_into)
     const int jobs = GS + (has_new ? 1 : 0);
     for (int p = tid; p < jobs * half; p += 256) {
@@ -273,15 +349,14 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
         vec[i] = x0 * cs[i] - x1 * sn[i];
         vec[i + half] = x0 * sn[i] + x1 * cs[i];
     }
-    __syncthreads();
+    bar_sync(1, 256);
     if (has_new) a.kc[static_cast<size_t>(pos) * a.kvd + g * kHd + tid] = k_s[tid];  // K append at pos
 
-    // ------------------------------------------------- keys of this split
     float q[GS][8];
 #pragma unroll
     for (int i = 0; i < GS; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) q[i][j] = q_s[i * kHd + (j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4)];
+        for (int j = 0; j < 8; ++j) q[i][j] = q_s[i * kHd + dim8(lane, j)];
     float m[GS], l[GS], acc[GS][8];
 #pragma unroll
     for (int i = 0; i < GS; ++i) {
@@ -291,29 +366,34 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
     }
     const float scale = 1.0f / sqrtf(static_cast<float>(kHd));
-    const int t0 = s * a.T, t1 = min(t0 + a.T, t_len);
-    for (int t = t0 + warp; t < t1; t += 8) {
-        float kv[8], vv[8];
-        if (t == pos) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) kv[j] = k_s[j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4];
-        } else {
-            load_row8(a.kc + static_cast<size_t>(t) * a.kvd + g * kHd, lane, kv);
+    for (int st = 0; st < nst; ++st) {
+        const int slot = st % kAttnStages;
+        if (!mbar_wait(&full[slot], (st / kAttnStages) & 1)) {
+            atomicOr(a.err, DEVERR_FULL_WAIT);
+            break;
         }
-        load_row8(a.vc + static_cast<size_t>(t) * a.kvd + g * kHd, lane, vv);
+        const int t = t0 + st * kKeysPerStage + warp;
+        if (t < t1) {
+            const float* kv_row = ring + (static_cast<size_t>(slot) * kKeysPerStage + warp) * 2 * kHd;
+            float kv[8], vv[8];
+            row8(t == pos ? k_s : kv_row, lane, kv);
+            row8(kv_row + kHd, lane, vv);
 #pragma unroll
-        for (int i = 0; i < GS; ++i) {
-            float dot = 0.0f;
+            for (int i = 0; i < GS; ++i) {
+                float dot = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dot = fmaf(q[i][j], kv[j], dot);
-            const float sc = warp_sum(dot) * scale;
-            const float mn = fmaxf(m[i], sc);
-            const float c = expf(m[i] - mn), p = expf(sc - mn);
-            l[i] = fmaf(l[i], c, p);
+                for (int j = 0; j < 8; ++j) dot = fmaf(q[i][j], kv[j], dot);
+                const float sc = warp_sum(dot) * scale;
+                const float mn = fmaxf(m[i], sc);
+                const float c = expf(m[i] - mn), p = expf(sc - mn);
+                l[i] = fmaf(l[i], c, p);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(acc[i][j], c, p * vv[j]);
-            m[i] = mn;
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(acc[i][j], c, p * vv[j]);
+                m[i] = mn;
+            }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
     }
 #pragma unroll
     for (int i = 0; i < GS; ++i) {
@@ -322,10 +402,9 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
             wml[(warp * GS + i) * 2 + 1] = l[i];
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            wacc[(warp * GS + i) * kHd + (j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4)] = acc[i][j];
+        for (int j = 0; j < 8; ++j) wacc[(warp * GS + i) * kHd + dim8(lane, j)] = acc[i][j];
     }
-    __syncthreads();
+    bar_sync(1, 256);
     // combine the 8 warps: thread tid owns dim tid of every head
     const size_t pbase = (static_cast<size_t>(g) * a.max_splits + s) * GS;
     for (int i = 0; i < GS; ++i) {
@@ -345,25 +424,49 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
         }
     }
     __threadfence();
-    __syncthreads();
+    bar_sync(1, 256);
     if (tid == 0) last_flag = (atomicAdd(a.count + g, 1u) == static_cast<unsigned>(n_act - 1));
-    __syncthreads();
+    bar_sync(1, 256);
     if (!last_flag) return;
     __threadfence();
     // last CTA of group g: combine the splits in order, then the sigmoid gate
-    for (int i = 0; i < GS; ++i) {
-        const size_t hb = static_cast<size_t>(g) * a.max_splits * GS;
+    const size_t hb = static_cast<size_t>(g) * a.max_splits * GS;
+    for (int e = tid; e < n_act * GS * 2; e += 256) cml[e] = __ldcg(a.part_ml + hb * 2 + e);
+    bar_sync(1, 256);
+    for (int job = tid; job < GS * (kHd / 4); job += 256) {
+        const int i = job / (kHd / 4), d4 = 4 * (job - i * (kHd / 4));
         float M = -INFINITY;
-        for (int sp = 0; sp < n_act; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (hb + sp * GS + i) * 2));
-        float L = 0.0f, A = 0.0f;
-        for (int sp = 0; sp < n_act; ++sp) {
-            const float f = expf(__ldcg(a.part_ml + (hb + sp * GS + i) * 2) - M);
-            L = fmaf(__ldcg(a.part_ml + (hb + sp * GS + i) * 2 + 1), f, L);
-            A = fmaf(__ldcg(a.part_acc + (hb + sp * GS + i) * kHd + tid), f, A);
+        for (int sp = 0; sp < n_act; ++sp) M = fmaxf(M, cml[(sp * GS + i) * 2]);
+        float L = 0.0f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp0 = 0; sp0 < n_act; sp0 += 8) {
+            float4 v[8];
+            float f[8], lw[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const bool in = sp0 + u < n_act;
+                const int sp = in ? sp0 + u : sp0;
+                v[u] = __ldcg(reinterpret_cast<const float4*>(a.part_acc + (hb + sp * GS + i) * kHd + d4));
+                f[u] = in ? expf(cml[(sp * GS + i) * 2] - M) : 0.0f;
+                lw[u] = cml[(sp * GS + i) * 2 + 1];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                L = fmaf(lw[u], f[u], L);
+                A.x = fmaf(v[u].x, f[u], A.x);
+                A.y = fmaf(v[u].y, f[u], A.y);
+                A.z = fmaf(v[u].z, f[u], A.z);
+                A.w = fmaf(v[u].w, f[u], A.w);
+            }
         }
         const int h = g * GS + i;
-        const float gate = __ldcg(a.qf + static_cast<size_t>(h) * 2 * kHd + kHd + tid);
-        a.out[h * kHd + tid] = (A / L) * sigmoid(gate);  // gdn_sigmoid_gate_into
+        const float4 gt = __ldcg(reinterpret_cast<const float4*>(a.qf + static_cast<size_t>(h) * 2 * kHd + kHd + d4));
+        float4 o;  // (A / L) * sigmoid(gate)  (gdn_sigmoid_gate_into)
+        o.x = (A.x / L) * sigmoid(gt.x);
+        o.y = (A.y / L) * sigmoid(gt.y);
+        o.z = (A.z / L) * sigmoid(gt.z);
+        o.w = (A.w / L) * sigmoid(gt.w);
+        *reinterpret_cast<float4*>(a.out + h * kHd + d4) = o;
     }
     if (tid == 0) a.count[g] = 0u;
 }
@@ -447,13 +550,13 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStr
 
 template <int GS>
 static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
-    const int smem = (GS * kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd) * 4;
+    const int smem = attn_smem_floats<GS>() * 4;
     static int configured = 0;
     if (smem > configured) {
         QG_CUDA(cudaFuncSetAttribute(attn_kernel<GS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         configured = smem;
     }
-    return launch_pdl(attn_kernel<GS>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(256), smem, st, true, a);
+    return launch_pdl(attn_kernel<GS>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
 }
 
 int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
@@ -482,6 +585,7 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaSt
     a.part_ml = s->part_ml;
     a.count = s->attn_count;
     a.out = s->attn;
+    a.err = s->err;
     a.kvd = m->kv_dim;
     a.T = s->keys_per_split;
     a.max_splits = s->max_splits;

@@ -356,8 +356,10 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
     s->ssm.assign(c.n_layers, nullptr);
     s->kc.assign(c.n_layers, nullptr);
     s->vc.assign(c.n_layers, nullptr);
-    // keys per split: at most 64 splits, at least 32 keys, a multiple of 8
-    int T = (max_seq_len + 63) / 64;
+    // keys per split: at most 32 splits (the combine reads every split), at
+    // least 32 keys, a multiple of 8; fixed per state, so the key partition
+    // of a step depends on its position only
+    int T = (max_seq_len + 31) / 32;
     T = ((T + 7) / 8) * 8;
     if (T < 32) T = 32;
     s->keys_per_split = T;

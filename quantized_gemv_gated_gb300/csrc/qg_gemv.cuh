@@ -13,15 +13,17 @@
 //
 // Arithmetic side.  x (K floats, after the kernel's prologue: RMSNorm, gated
 // norm, ...) is held in shared memory as a 24-bit block-fixed-point integer
-// per element: in every 32-element block, n_i = rint(x_i * 2^(22-e)) with 2^e
-// <= max|x| < 2^(e+1), so |n_i| < 2^23 and the representation keeps the 24
-// significant bits of the block's largest element (f32 keeps 24).  n_i is
-// stored as three byte planes (n = n2*65536 + n1*256 + n0, n2 signed), and
-// every sum of quant*n over a sub-block is computed EXACTLY with dp4a integer
-// dot products.  Sub-block sums are then scaled and accumulated in f32.  This
-// is not the int8 activation quantisation forward_qwen35_cuda.rs rejects
+// per element: in every 256-element block (one k-quant super-block of the
+// weights), n_i = rint(x_i * 2^(22-e)) with 2^e <= max|x| < 2^(e+1), so
+// |n_i| < 2^23 and the representation keeps the 24 significant bits of the
+// block's largest element (f32 keeps 24).  n_i is stored as three byte planes
+// (n = n2*65536 + n1*256 + n0, n2 signed), every sum of quant*n over a
+// sub-block is computed EXACTLY with dp4a integer dot products, and the
+// sub-block sums of a 64-weight chunk are weighted by their integer scales in
+// integer arithmetic; one float per chunk is accumulated in f32.  This is not
+// the int8 activation quantisation forward_qwen35_cuda.rs rejects
 // (pin_float_gemv): the only rounding of x is below 2^-23 of its block's
-// largest magnitude, and the per-sub-block sums carry no rounding at all.
+// largest magnitude, and the integer sums carry no rounding at all.
 //
 //   Q4_K sub-block j (32 weights): d*sc_j*sum(q*x) - dmin*m_j*sum(x)
 //   Q6_K group of 16 weights:      d*sc*sum((q-32)*x)
@@ -33,7 +35,7 @@ namespace qg {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int QT_Q4K = 12;
 constexpr int QT_Q6K = 14;
 
@@ -48,16 +50,23 @@ struct GemvShape {
     int units;   // ceil(n / 8)
     int stage_bytes;
     int pro_floats;  // prologue scratch floats
+    int rows_cta;    // most rows one CTA owns (row-result buffer of deferred epilogues)
     unsigned* err;
 };
 
-// Shared-memory layout offsets.
-__host__ __device__ inline int xaux_bytes(int qt, int k) { return qt == QT_Q4K ? (k / 32) * 8 : k; }
-__host__ __device__ inline int off_dig() { return 64; }
-__host__ __device__ inline int off_aux(int k) { return 64 + 3 * k; }
+// Shared-memory layout offsets.  aux: per 256-element super-block the unit
+// 2^(e-22) (float), then Q4_K: per 32-element sub-block the sum of n (float);
+// Q6_K: per 16-element group {-32*N0, -32*N1, -32*N2, 0} (digit-plane sums).
+__host__ __device__ inline int xaux_bytes(int qt, int k) {
+    return ((4 * (k / 256) + 15) & ~15) + (qt == QT_Q4K ? 4 * (k / 32) : k);
+}
+__host__ __device__ inline int aux_tail(int k) { return (4 * (k / 256) + 15) & ~15; }
+__host__ __device__ inline int off_dig() { return 16 * kMaxStages; }
+__host__ __device__ inline int off_aux(int k) { return off_dig() + 3 * k; }
 __host__ __device__ inline int off_pro(int qt, int k) { return ((off_aux(k) + xaux_bytes(qt, k)) + 15) & ~15; }
-__host__ __device__ inline int off_ring(int qt, int k, int pro_floats) {
-    return (off_pro(qt, k) + 4 * pro_floats + 127) & ~127;
+__host__ __device__ inline int off_ys(int qt, int k, int pro_floats) { return off_pro(qt, k) + 4 * pro_floats; }
+__host__ __device__ inline int off_ring(int qt, int k, int pro_floats, int ys_floats) {
+    return (off_ys(qt, k, pro_floats) + 4 * ys_floats + 127) & ~127;
 }
 
 // 16-byte-unit swizzles of the digit planes, chosen so that the 8 lanes of
@@ -72,52 +81,78 @@ __device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
+__device__ __forceinline__ int dp4a_su(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // ---------------------------------------------------------- x representation
-// Warps split the K/32 blocks; lane i of a warp holds element 32b+i.
+// One warp per 256-element super-block, 8 consecutive elements per lane:
+// n_i = rint(x_i * 2^(22-e)) with 2^e <= max|x| over the super-block
+// (clamped to |n| < 2^23), stored as three byte planes.
 template <int QT, class Pro>
-__device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, void* aux, int k, int warp,
+__device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, uint8_t* aux, int k, int warp,
                            int lane) {
-    const int nblk = k >> 5;
-    for (int b = warp; b < nblk; b += kConsumerWarps) {
-        const int i = 32 * b + lane;
-        const float x = pro.value(sm, i);
-        const unsigned amax = __reduce_max_sync(FULL, __float_as_uint(x) & 0x7fffffffu);
-        int e = static_cast<int>(amax >> 23) - 127;
+    const int nsb = k >> 8;
+    float* units = reinterpret_cast<float*>(aux);
+    for (int b = warp; b < nsb; b += kConsumerWarps) {
+        const int i0 = 256 * b + 8 * lane;
+        float x[8];
+        unsigned am = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            x[j] = pro.value(sm, i0 + j);
+            am = max(am, __float_as_uint(x[j]) & 0x7fffffffu);
+        }
+        am = __reduce_max_sync(FULL, am);
+        int e = static_cast<int>(am >> 23) - 127;
         e = e < -100 ? -100 : e;
         const float mul = __uint_as_float(static_cast<unsigned>(149 - e) << 23);   // 2^(22-e)
         const float unit = __uint_as_float(static_cast<unsigned>(105 + e) << 23);  // 2^(e-22)
-        int n = __float2int_rn(x * mul);
-        n = n > 8388607 ? 8388607 : (n < -8388607 ? -8388607 : n);
-        const unsigned off = (swz(QT, static_cast<unsigned>(i) >> 4) << 4) | (i & 15);
-        dig[off] = static_cast<uint8_t>(n & 255);
-        dig[k + off] = static_cast<uint8_t>((n >> 8) & 255);
-        dig[2 * k + off] = static_cast<uint8_t>((n >> 16) & 255);
-        if constexpr (QT == QT_Q4K) {
-            const int s = __reduce_add_sync(FULL, n);
-            if (lane == 0) reinterpret_cast<float2*>(aux)[b] = make_float2(unit, static_cast<float>(s) * unit);
-        } else {
-            // per 16-group digit sums, folded into the dp4a start value as -32*N
-            int p01 = (n & 255) | (((n >> 8) & 255) << 16);
-            int p2 = n >> 16;
+        unsigned w0[2] = {0u, 0u}, w1[2] = {0u, 0u}, w2[2] = {0u, 0u};
+        int nsum = 0;
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                p01 += __shfl_xor_sync(FULL, p01, o);
-                p2 += __shfl_xor_sync(FULL, p2, o);
-            }
-            if ((lane & 15) == 0) {
-                const unsigned g = static_cast<unsigned>(i) >> 4;
-                reinterpret_cast<int4*>(aux)[swz(QT, g)] =
-                    make_int4(-32 * (p01 & 0xffff), -32 * (p01 >> 16), -32 * p2, __float_as_int(unit));
-            }
+        for (int j = 0; j < 8; ++j) {
+            int n = __float2int_rn(x[j] * mul);
+            n = n > 8388607 ? 8388607 : (n < -8388607 ? -8388607 : n);
+            nsum += n;
+            const int sh = 8 * (j & 3);
+            w0[j >> 2] |= static_cast<unsigned>(n & 255) << sh;
+            w1[j >> 2] |= static_cast<unsigned>((n >> 8) & 255) << sh;
+            w2[j >> 2] |= static_cast<unsigned>((n >> 16) & 255) << sh;
+        }
+        const unsigned u = static_cast<unsigned>(i0) >> 4;
+        const unsigned off = (swz(QT, u) << 4) + 8 * (lane & 1);
+        *reinterpret_cast<uint2*>(dig + off) = make_uint2(w0[0], w0[1]);
+        *reinterpret_cast<uint2*>(dig + k + off) = make_uint2(w1[0], w1[1]);
+        *reinterpret_cast<uint2*>(dig + 2 * k + off) = make_uint2(w2[0], w2[1]);
+        if (lane == 0) units[b] = unit;
+        if constexpr (QT == QT_Q4K) {
+            nsum += __shfl_xor_sync(FULL, nsum, 1);
+            nsum += __shfl_xor_sync(FULL, nsum, 2);
+            if ((lane & 3) == 0)
+                reinterpret_cast<float*>(aux + aux_tail(k))[8 * b + (lane >> 2)] = static_cast<float>(nsum);
+        } else {
+            int n0 = static_cast<int>(dp4a_uu(w0[0], 0x01010101u, dp4a_uu(w0[1], 0x01010101u, 0u)));
+            int n1 = static_cast<int>(dp4a_uu(w1[0], 0x01010101u, dp4a_uu(w1[1], 0x01010101u, 0u)));
+            int n2 = dp4a_su(w2[0], 0x01010101u, dp4a_su(w2[1], 0x01010101u, 0));
+            n0 += __shfl_xor_sync(FULL, n0, 1);
+            n1 += __shfl_xor_sync(FULL, n1, 1);
+            n2 += __shfl_xor_sync(FULL, n2, 1);
+            if ((lane & 1) == 0)
+                reinterpret_cast<int4*>(aux + aux_tail(k))[swz(QT, u)] = make_int4(-32 * n0, -32 * n1, -32 * n2, 0);
         }
     }
 }
 
 // ------------------------------------------------------------ chunk kernels
-// One lane, one 64-weight chunk.  Q4_K: group g of super-block `blk`.
+// One lane, one 64-weight chunk.  Sub-block sums are exact integers; they are
+// weighted by their integer scales in integer arithmetic and turned into one
+// float per chunk, scaled by the super-block's unit.
+// Q4_K: group g (sub-blocks 2g and 2g+1) of super-block `blk`, x offset xo.
 __device__ __forceinline__ void chunk_q4k(const uint8_t* blk, int g, int xo, const uint8_t* dig,
-                                          const float2* bs, int k, float& acc) {
+                                          const uint8_t* aux, int k, float& acc) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * g);
     const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * g);
@@ -166,19 +201,21 @@ __device__ __forceinline__ void chunk_q4k(const uint8_t* blk, int g, int xo, con
             mn[t] = static_cast<int>((bw >> 4) | ((bz >> 6) << 4));
         }
     }
-    const float4 ab = *reinterpret_cast<const float4*>(bs + (xo >> 5));  // unitA, sumA, unitB, sumB
-    const float sa = fmaf(static_cast<float>(a2), 65536.0f, static_cast<float>(static_cast<int>(a1 * 256u + a0)));
-    const float sb = fmaf(static_cast<float>(b2), 65536.0f, static_cast<float>(static_cast<int>(b1 * 256u + b0)));
-    acc = fmaf(d * static_cast<float>(sc[0]), sa * ab.x, acc);
-    acc = fmaf(-(dmin * static_cast<float>(mn[0])), ab.y, acc);
-    acc = fmaf(d * static_cast<float>(sc[1]), sb * ab.z, acc);
-    acc = fmaf(-(dmin * static_cast<float>(mn[1])), ab.w, acc);
+    // |sc * sum| < 63 * 15 * 255 * 32 per sub-block: the weighted sums fit in int32
+    const int I0 = sc[0] * static_cast<int>(a0) + sc[1] * static_cast<int>(b0);
+    const int I1 = sc[0] * static_cast<int>(a1) + sc[1] * static_cast<int>(b1);
+    const int I2 = sc[0] * a2 + sc[1] * b2;
+    const float F = fmaf(static_cast<float>(I2), 65536.0f, fmaf(static_cast<float>(I1), 256.0f, static_cast<float>(I0)));
+    const float2 ns = *reinterpret_cast<const float2*>(aux + aux_tail(k) + 4 * (xo >> 5));
+    const float M = fmaf(static_cast<float>(mn[0]), ns.x, static_cast<float>(mn[1]) * ns.y);
+    const float unit = reinterpret_cast<const float*>(aux)[xo >> 8];
+    acc = fmaf(unit, fmaf(d, F, -(dmin * M)), acc);
 }
 
-// Q6_K planar: quarter-chunk cq = 2*half + part of super-block b.
+// Q6_K planar: quarter-chunk cq = 2*half + part of super-block b (x offset 256*b).
 __device__ __forceinline__ void chunk_q6k(const uint8_t* ql, const uint8_t* qhp, const uint8_t* scp,
-                                          const uint16_t* dp, int b, int cq, int xo, const uint8_t* dig,
-                                          const int4* gc, int k, float& acc) {
+                                          const uint16_t* dp, int b, int cq, const uint8_t* dig,
+                                          const uint8_t* aux, int k, float& acc) {
     const int half = cq >> 1, part = cq & 1;
     const int f = b & 1;  // read the two 16-byte pieces in an order that avoids bank conflicts
     const uint4 p0 = *reinterpret_cast<const uint4*>(ql + 32 * cq + 16 * f);
@@ -189,9 +226,11 @@ __device__ __forceinline__ void chunk_q6k(const uint8_t* ql, const uint8_t* qhp,
     const uint2 S = *reinterpret_cast<const uint2*>(scp + 8 * half);
     const float d = f16_to_f32(*dp);
     const unsigned Aw[4] = {A.x, A.y, A.z, A.w}, Bw[4] = {B.x, B.y, B.z, B.w}, Hw[4] = {H.x, H.y, H.z, H.w};
+    const int4* gc = reinterpret_cast<const int4*>(aux + aux_tail(k));
+    int I0 = 0, I1 = 0, I2 = 0;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-        const int pos = xo + 128 * half + 32 * s + 16 * part;
+        const int pos = 256 * b + 128 * half + 32 * s + 16 * part;
         const unsigned u = swz(QT_Q6K, static_cast<unsigned>(pos) >> 4);
         const int4 gcv = gc[u];
         const uint4 D0 = *reinterpret_cast<const uint4*>(dig + (u << 4));
@@ -211,22 +250,25 @@ __device__ __forceinline__ void chunk_q6k(const uint8_t* ql, const uint8_t* qhp,
             t1 = static_cast<int>(dp4a_uu(q, d1[w], static_cast<unsigned>(t1)));
             t2 = dp4a_us(q, d2[w], t2);
         }
-        const float T = fmaf(static_cast<float>(t2), 65536.0f, static_cast<float>(t1 * 256 + t0));
         const int si = part + 2 * s;
         const int sc = static_cast<int>(static_cast<int8_t>(((si < 4 ? S.x : S.y) >> (8 * (si & 3))) & 0xffu));
-        acc = fmaf(d * static_cast<float>(sc), T * __int_as_float(gcv.w), acc);
+        // |sc * t| <= 128 * 32 * 255 * 16 per group, four groups: fits in int32
+        I0 += sc * t0;
+        I1 += sc * t1;
+        I2 += sc * t2;
     }
+    const float F = fmaf(static_cast<float>(I2), 65536.0f, fmaf(static_cast<float>(I1), 256.0f, static_cast<float>(I0)));
+    acc = fmaf(d * reinterpret_cast<const float*>(aux)[b], F, acc);
 }
 
 // Partial dot product of one row over the chunks c = lg0, lg0 + G, ...
 template <int QT>
 __device__ __forceinline__ float row_partial(const uint8_t* stage, int rs, int lrow, int nb, int cr, int G, int lg0,
-                                             const uint8_t* dig, const void* aux, int k) {
+                                             const uint8_t* dig, const uint8_t* aux, int k) {
     float acc = 0.0f;
     if constexpr (QT == QT_Q4K) {
         const uint8_t* row = stage + static_cast<size_t>(lrow) * nb * 144;
-        for (int c = lg0; c < cr; c += G)
-            chunk_q4k(row + (c >> 2) * 144, c & 3, 64 * c, dig, reinterpret_cast<const float2*>(aux), k, acc);
+        for (int c = lg0; c < cr; c += G) chunk_q4k(row + (c >> 2) * 144, c & 3, 64 * c, dig, aux, k, acc);
     } else {
         const uint8_t* ql = stage + static_cast<size_t>(lrow) * nb * 128;
         const uint8_t* qh = stage + static_cast<size_t>(rs) * nb * 128 + static_cast<size_t>(lrow) * nb * 64;
@@ -235,8 +277,7 @@ __device__ __forceinline__ float row_partial(const uint8_t* stage, int rs, int l
             reinterpret_cast<const uint16_t*>(stage + static_cast<size_t>(rs) * nb * 208) + static_cast<size_t>(lrow) * nb;
         for (int c = lg0; c < cr; c += G) {
             const int b = c >> 2;
-            chunk_q6k(ql + b * 128, qh + b * 64, sc + b * 16, dd + b, b, c & 3, 256 * b, dig,
-                      reinterpret_cast<const int4*>(aux), k, acc);
+            chunk_q6k(ql + b * 128, qh + b * 64, sc + b * 16, dd + b, b, c & 3, dig, aux, k, acc);
         }
     }
     return acc;
@@ -250,17 +291,21 @@ __host__ __device__ inline size_t rows_bytes(int qt, int rows, int nb) {
 // -------------------------------------------------------------- the kernel
 // Pro: prepare(float* sm, int k, int tid) fills its scratch (consumers only),
 //      value(const float* sm, int i) gives x_i.
-// Epi: start() after the dependency wait, row(r, v) / row2(r, v0, v1) by the
-//      lane leading each row group, finish(float* red, int tid) once per CTA.
+// Epi: start() after the dependency wait; with kDeferred, the row results of
+//      the CTA go to shared memory and apply(r0, r1, ys, ys2, tid) runs once
+//      over all of them with every consumer thread (one memory round trip for
+//      the whole CTA); otherwise row(r, v) / row2(r, v0, v1) is called by the
+//      lane leading each row group.  finish(float* red, int tid) once per CTA.
 template <int QT, bool DUAL, class Pro, class Epi>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvShape sh, const Pro pro_in, const Epi epi_in) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, const Pro pro_in, const Epi epi_in) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     uint8_t* dig = smem + off_dig();
-    void* aux = smem + off_aux(sh.k);
+    uint8_t* aux = smem + off_aux(sh.k);
     float* psm = reinterpret_cast<float*>(smem + off_pro(QT, sh.k));
-    uint8_t* ring = smem + off_ring(QT, sh.k, sh.pro_floats);
+    float* ys = reinterpret_cast<float*>(smem + off_ys(QT, sh.k, sh.pro_floats));
+    uint8_t* ring = smem + off_ring(QT, sh.k, sh.pro_floats, (DUAL ? 2 : 1) * sh.rows_cta);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();
@@ -370,12 +415,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvShape sh, c
                 if constexpr (DUAL) v1 += __shfl_xor_sync(FULL, v1, o);
             }
             if (valid && lg0 == 0) {
-                if constexpr (DUAL) epi.row2(row0 + lr, v0, v1);
-                else epi.row(row0 + lr, v0);
+                if constexpr (Epi::kDeferred) {
+                    ys[row0 + lr - r0] = v0;
+                    if constexpr (DUAL) ys[sh.rows_cta + row0 + lr - r0] = v1;
+                } else {
+                    if constexpr (DUAL) epi.row2(row0 + lr, v0, v1);
+                    else epi.row(row0 + lr, v0);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if constexpr (Epi::kDeferred) {
+        bar_sync(1, kConsumers);
+        epi.apply(r0, r1, ys, ys + sh.rows_cta, tid);
     }
     epi.finish(psm, tid);
 }
@@ -467,20 +521,29 @@ struct ProGatedNorm {
 
 // ------------------------------------------------------------- epilogues
 struct EpiBase {
+    static constexpr bool kDeferred = true;
     __device__ void start() {}
+    __device__ void row(int, float) {}
+    __device__ void row2(int, float, float) {}
     __device__ void finish(float*, int) {}
 };
 struct EpiStore : EpiBase {
     float* y;
-    __device__ void row(int r, float v) { y[r] = v; }
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) y[r] = ys[r - r0];
+    }
 };
 struct EpiResidual : EpiBase {  // h += W x (residual_add_into)
     float* h;
-    __device__ void row(int r, float v) { h[r] = __ldcg(h + r) + v; }
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) h[r] = __ldcg(h + r) + ys[r - r0];
+    }
 };
 struct EpiSwiGlu : EpiBase {  // act = silu(W_gate x) * (W_up x) (fused_swiglu_into)
     float* act;
-    __device__ void row2(int r, float g, float u) { act[r] = silu(g) * u; }
+    __device__ void apply(int r0, int r1, const float* ys, const float* ys2, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) act[r] = silu(ys[r - r0]) * ys2[r - r0];
+    }
 };
 
 }  // namespace qg

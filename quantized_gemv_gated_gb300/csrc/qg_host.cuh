@@ -22,12 +22,12 @@ int device_sms();
     } while (0)
 
 // Bytes of dynamic shared memory one GEMV launch needs.
-inline int gemv_smem(int qt, int k, int pro_floats, int stages, int stage_bytes) {
-    return off_ring(qt, k, pro_floats) + stages * stage_bytes;
+inline int gemv_smem(int qt, bool dual, int k, int pro_floats, int rows_cta, int stages, int stage_bytes) {
+    return off_ring(qt, k, pro_floats, (dual ? 2 : 1) * rows_cta) + stages * stage_bytes;
 }
 
-constexpr int kStageMaxBytes = 48 * 1024;  // one stage of the ring
-constexpr int kRingMaxBytes = 96 * 1024;   // the ring: room for two CTAs per SM
+constexpr int kStageMaxBytes = 16 * 1024;  // one stage of the ring
+constexpr int kCtaSmemBytes = 110 * 1024;  // per CTA: two CTAs per SM fit in 228 KB
 
 // Geometry for n rows of k weights (dual: two matrices streamed together).
 inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1, int n, int k, int pro_floats,
@@ -56,6 +56,7 @@ inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1
     if (grid > sh.units) grid = sh.units;
     if (grid < 1) grid = 1;
     const int rows_cta = 8 * ((sh.units + grid - 1) / grid);
+    sh.rows_cta = rows_cta;
     int rs = unit_rows * (kStageMaxBytes / (unit_rows * per_row) > 0 ? kStageMaxBytes / (unit_rows * per_row) : 1);
     const int need = ((rows_cta + unit_rows - 1) / unit_rows) * unit_rows;
     if (rs > need) rs = need;
@@ -63,7 +64,8 @@ inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1
     sh.stage_bytes = rs * per_row;
     int stages = (rows_cta + rs - 1) / rs;
     if (stages > kMaxStages) stages = kMaxStages;
-    while (stages > 1 && stages * sh.stage_bytes > kRingMaxBytes) --stages;
+    const int fixed = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * rows_cta);
+    while (stages > 1 && fixed + stages * sh.stage_bytes > kCtaSmemBytes) --stages;
     sh.stages = stages < 1 ? 1 : stages;
     *grid_out = grid;
     return sh;
@@ -77,11 +79,13 @@ int launch_gemv(const void* w0, const void* w1, int n, int k, const Pro& pro, co
                 bool pdl, unsigned* err, int max_ctas = 0) {
     int grid = 1;
     const GemvShape sh = gemv_geometry(QT, DUAL, w0, w1, n, k, pro.floats(k), max_ctas, err, &grid);
-    const int smem = gemv_smem(QT, k, sh.pro_floats, sh.stages, sh.stage_bytes);
+    const int smem = gemv_smem(QT, DUAL, k, sh.pro_floats, sh.rows_cta, sh.stages, sh.stage_bytes);
     auto kern = gemv_kernel<QT, DUAL, Pro, Epi>;
     static int configured = 0;  // per instantiation: largest dynamic smem granted so far
     if (smem > configured) {
         QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     static_cast<int>(cudaSharedmemCarveoutMaxShared)));
         configured = smem;
     }
     cudaLaunchConfig_t cfg{};

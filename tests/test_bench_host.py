@@ -1,0 +1,73 @@
+"""Host logic of bench.py without a GPU: the replica timing reduction over
+ranks (gloo, world size 2), the per-token byte count, and the reference arm's
+JSON line (the CPU oracle), including under torchrun with two ranks where
+only rank 0 prints."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.max_over_ranks(1.5 + rank, world)
+    bench.barrier(world)
+    q.put((rank, t))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert res == [(0, 2.5), (1, 2.5)]
+
+
+def test_bytes_per_token_closed_forms():
+    # 0.8B: 553.63 MB fixed + 24,576 B per KV row read; 4B: 2,833.0 MB + 65,536 B
+    c8, c4 = synth.CFG_0P8B, synth.CFG_4B
+    assert bench.algorithmic_bytes(c8, 1) - bench.algorithmic_bytes(c8, 0) == 6 * 2 * 2 * 256 * 4
+    assert bench.algorithmic_bytes(c4, 1) - bench.algorithmic_bytes(c4, 0) == 8 * 2 * 4 * 256 * 4
+    assert abs(bench.algorithmic_bytes(c8, 0) / 1e6 - 553.63) < 0.01
+    assert abs(bench.algorithmic_bytes(c4, 0) / 1e6 - 2833.03) < 0.01
+    assert bench.lmhead_bytes(c8) == 248320 * 1024 // 256 * 210 + 1024 * 4
+
+
+@pytest.mark.slow
+def test_reference_arm_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tok/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.slow
+def test_reference_arm_torchrun_world2_rank0_prints_only():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(29700 + os.getpid() % 200),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2

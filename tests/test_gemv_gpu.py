@@ -3,7 +3,7 @@ through the C ABI, against the CPU oracle on the same seeded inputs.
 
 Bar (pages' float-GEMV parity, forward_qwen35_cuda.rs pin_reference_gemv):
 the GPU result must sit inside the error bound of the exact (f64) product
-that its arithmetic guarantees -- x held to 2^-23 of each 32-element block's
+that its arithmetic guarantees -- x held to 2^-23 of each 256-element block's
 largest magnitude M_b, exact integer sub-block sums, f32 accumulation:
 |y - y_exact| <= 2^-23 * sum_k |w_k| M_b(k) + 8 * 2^-24 * sum_k |w_k x_k| --
 and within 1e-5 normwise of the f32 oracle.  Argmax indices are compared
@@ -49,17 +49,17 @@ def run_gemv(t, x):
     return y.cpu().numpy()
 
 
-def check_against_oracle(t, x, y):
+def check_against_oracle(t, x, y, tight=True):
     exact = oracle.gemv_f64(t, x)
     W = np.abs(oracle.dequant(t).astype(np.float64))
     ax = np.abs(x.astype(np.float64))
-    blockmax = np.repeat(ax.reshape(-1, 32).max(axis=1), 32)
+    blockmax = np.repeat(ax.reshape(-1, 256).max(axis=1), 256)
     bound = 2 * F32_EPS * (W @ blockmax) + 8 * F32_EPS * (W @ ax) + 1e-30
     err = np.abs(y.astype(np.float64) - exact)
     assert np.all(err <= bound), f"max err/bound {float(np.max(err / bound)):.3g}"
     ref = oracle.gemv(t, x)
     rel = np.max(np.abs(y - ref)) / max(np.max(np.abs(ref)), 1e-30)
-    assert rel <= 1e-5, rel
+    assert rel <= (1e-5 if tight else 1e-4), rel
 
 
 SMALL = [(1, 256), (13, 256), (37, 768), (300, 2560), (1000, 1024), (129, 3584), (64, 4096)]
@@ -78,16 +78,19 @@ def test_gemv_small_shapes(qtype, n, k):
 def test_gemv_special_inputs(qtype):
     gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
     t = gen(5, 40, 512)
-    for x in [np.zeros(512, np.float32),
-              np.full(512, 3.0, np.float32),
-              (synth.normal(6, 512) * np.float32(1e-30)).astype(np.float32),  # tiny blocks
-              (synth.normal(7, 512) * np.float32(1e20)).astype(np.float32),   # huge values
-              np.where(np.arange(512) % 32 == 5, 100.0, 1e-3).astype(np.float32)]:  # one large per block
+    cases = [(np.zeros(512, np.float32), True),
+             (np.full(512, 3.0, np.float32), True),
+             ((synth.normal(6, 512) * np.float32(1e-30)).astype(np.float32), True),  # tiny blocks
+             ((synth.normal(7, 512) * np.float32(1e20)).astype(np.float32), True),   # huge values
+             # one large element per 256-block: the small ones keep only 2^-23 of the block's
+             # largest magnitude, so only the representation bound is promised
+             (np.where(np.arange(512) % 256 == 5, 100.0, 1e-3).astype(np.float32), False)]
+    for x, tight in cases:
         y = run_gemv(t, x)
         if not np.any(x):
             assert np.all(y == 0)
         else:
-            check_against_oracle(t, x, y)
+            check_against_oracle(t, x, y, tight)
 
 
 # the standalone-kernel sweep shapes, all rows against the oracle
