@@ -21,13 +21,19 @@
 //   3. attn_output GEMV + residual, 4.-5. the FFN as above.
 // Token tail (forward_single): output-RMSNorm prologue + lm_head GEMV with an
 // argmax epilogue (first index on ties).
+#include <algorithm>
+
 #include "qg_internal.cuh"
 
 namespace qg {
 
 // ------------------------------------------------------------ epilogues
 // DeltaNet input projection rows: [0, C) qkv -> conv; [C, C+nv) alpha;
-// [C+nv, C+2nv) beta; [C+2nv, C+2nv+v_dim) z.
+// [C+nv, C+2nv) beta; [C+2nv, C+2nv+v_dim) z.  Each consumer thread owns rows
+// r0 + tid, r0 + tid + 256, ...; the conv window and weights of its first row
+// (state of the previous token, and constants) are loaded before the
+// dependency wait.
+constexpr int kMaxConvTaps = 8;
 struct EpiDnIn : EpiBase {
     int C, nv, K;
     float* win;          // [C][K-1], oldest first
@@ -38,21 +44,48 @@ struct EpiDnIn : EpiBase {
     float* dt;
     float* beta;
     float* z;
+    int pre_row;
+    float pw[kMaxConvTaps], pwin[kMaxConvTaps], plast;
+    __device__ void pre(int r0, int r1, int tid) {
+        pre_row = r0 + tid;
+        if (pre_row < r1 && pre_row < C) {
+            const float* kw = wconv + static_cast<size_t>(pre_row) * K;
+            const float* wc = win + static_cast<size_t>(pre_row) * (K - 1);
+#pragma unroll
+            for (int t = 0; t < kMaxConvTaps - 1; ++t) {
+                if (t < K - 1) {
+                    pw[t] = kw[t];
+                    pwin[t] = __ldcg(wc + t);
+                }
+            }
+            plast = kw[K - 1];
+        }
+    }
     __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
         for (int r = r0 + tid; r < r1; r += kConsumers) row_out(r, ys[r - r0]);
     }
     __device__ void row_out(int r, float v) {
         if (r < C) {
             // causal conv1d + SiLU, then roll the window (gdn_causal_conv1d_silu_into)
-            const float* kw = wconv + static_cast<size_t>(r) * K;
             float* wc = win + static_cast<size_t>(r) * (K - 1);
             float acc = 0.0f;
-            for (int t = 0; t < K - 1; ++t) {
-                const float wt = __ldcg(wc + t);
-                acc += kw[t] * wt;
-                if (t > 0) wc[t - 1] = wt;  // roll: shift left, append the new input
+            if (r == pre_row) {
+#pragma unroll
+                for (int t = 0; t < kMaxConvTaps - 1; ++t)
+                    if (t < K - 1) acc += pw[t] * pwin[t];
+#pragma unroll
+                for (int t = 1; t < kMaxConvTaps - 1; ++t)
+                    if (t < K - 1) wc[t - 1] = pwin[t];
+                acc += plast * v;
+            } else {
+                const float* kw = wconv + static_cast<size_t>(r) * K;
+                for (int t = 0; t < K - 1; ++t) {
+                    const float wt = __ldcg(wc + t);
+                    acc += kw[t] * wt;
+                    if (t > 0) wc[t - 1] = wt;
+                }
+                acc += kw[K - 1] * v;
             }
-            acc += kw[K - 1] * v;
             conv_out[r] = silu(acc);
             wc[K - 2] = v;
         } else if (r < C + nv) {
@@ -133,63 +166,141 @@ struct EpiArgmaxStep : EpiBase {
 };
 
 // ------------------------------------------------------------ delta rule
-// One CTA: 16 rows j of value head h (8 warps x 2 rows), head_k_dim = 128
-// (4 per lane).  State row j of head h: s[(h*dv + j)*128 + i] == S[i][j].
+// One CTA per value head h (gdn_delta_rule_into + gdn_gated_rmsnorm_into),
+// head_k_dim = 128 (4 per lane), dv/8 rows per warp.  The head's state tile
+// (dv rows of 128, s[j*128 + i] == S[i][j]) arrives in shared memory with one
+// bulk copy issued before the dependency wait; rows are processed four at a
+// time so that their warp reductions overlap; the gated RMSNorm of the head
+// (a sum of o^2 over its dv rows) is reduced inside the CTA in warp order and
+// the kernel writes u = rmsnorm(o_h) * w * silu(z_h), the ssm_out input.
 constexpr int kDk = 128;
+constexpr int kMaxRowsPerWarp = 16;
 
-__global__ void __launch_bounds__(256) delta_kernel(const float* __restrict__ conv_out, const float* __restrict__ dt,
-                                                    const float* __restrict__ beta, float* __restrict__ S,
-                                                    float* __restrict__ o, int nk, int dv, int kdim, float eps) {
+struct DeltaArgs {
+    const float* conv_out;  // [q | k | v] after conv + SiLU
+    const float* dt;        // log-decay per value head
+    const float* beta;
+    float* S;               // [nv][dv][128]
+    const float* z;         // gate [v_dim]
+    const float* w_norm;    // [dv]
+    float* u;               // [v_dim]
+    unsigned* err;
+    L2Prefetch next;
+    int nk, dv, kdim;
+    float eps;
+};
+
+__global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
+    extern __shared__ __align__(16) float st[];  // [dv][128]
     __shared__ __align__(16) float qs[kDk];
     __shared__ __align__(16) float ks[kDk];
-    const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kh = h % nk;  // value head h reads key head h % nk (check_head_grouping)
+    __shared__ float wss[8];
+    __shared__ __align__(8) uint64_t bar;
+    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kh = h % a.nk;  // value head h reads key head h % nk (check_head_grouping)
+    const int rpw = a.dv / 8, j0 = warp * rpw;
     pdl_launch_dependents();
-    // the state tile does not depend on the previous kernel: fetch it first
-    float4 s[2];
-    int js[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        js[r] = blockIdx.x * 16 + warp * 2 + r;
-        s[r] = __ldcg(reinterpret_cast<const float4*>(S + (static_cast<size_t>(h) * dv + js[r]) * kDk + 4 * lane));
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
     }
+    __syncthreads();
+    if (tid == 0) {  // the state does not depend on the previous kernel
+        const unsigned bytes = static_cast<unsigned>(a.dv) * kDk * 4u;
+        mbar_arrive_expect_tx(&bar, bytes);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(st)),
+            "l"(a.S + static_cast<size_t>(h) * a.dv * kDk), "r"(bytes), "r"(smem_u32(&bar))
+            : "memory");
+        a.next.issue();
+    }
+    float wn = lane < rpw ? __ldg(a.w_norm + j0 + lane) : 0.0f;
     pdl_wait();
     if (warp < 2) {  // per-head L2 norm of q (warp 0) and k (warp 1) (gdn_per_head_l2_norm_into)
-        const float4 v = ldcg4(conv_out + (warp ? kdim : 0) + kh * kDk + 4 * lane);
+        const float4 v = ldcg4(a.conv_out + (warp ? a.kdim : 0) + kh * kDk + 4 * lane);
         float ss = v.x * v.x;
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
         ss = fmaf(v.w, v.w, ss);
         ss = warp_sum(ss);
-        const float r = 1.0f / sqrtf(ss + eps);
+        const float r = 1.0f / sqrtf(ss + a.eps);
         float* dst = warp ? ks : qs;
         *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(v.x * r, v.y * r, v.z * r, v.w * r);
     }
+    // lane i < rpw holds v and z of row j0 + i
+    const float vl = lane < rpw ? __ldcg(a.conv_out + 2 * a.kdim + h * a.dv + j0 + lane) : 0.0f;
+    const float zl = lane < rpw ? __ldcg(a.z + h * a.dv + j0 + lane) : 0.0f;
+    const float g = expf(__ldcg(a.dt + h)), be = __ldcg(a.beta + h);
     __syncthreads();
-    const float g = expf(__ldcg(dt + h)), be = __ldcg(beta + h);
+    if (!mbar_wait(&bar, 0)) {
+        atomicOr(a.err, DEVERR_FULL_WAIT);
+        if (!mbar_wait(&bar, 0)) atomicOr(a.err, DEVERR_DRAIN_WAIT);
+        return;
+    }
     const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
     const float4 kk = *reinterpret_cast<const float4*>(ks + 4 * lane);
     const float4 qq = *reinterpret_cast<const float4*>(qs + 4 * lane);
+    float o[kMaxRowsPerWarp];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const float4 rr = make_float4(g * s[r].x, g * s[r].y, g * s[r].z, g * s[r].w);  // decay
-        float dot = rr.x * kk.x;
-        dot = fmaf(rr.y, kk.y, dot);
-        dot = fmaf(rr.z, kk.z, dot);
-        dot = fmaf(rr.w, kk.w, dot);
-        dot = warp_sum(dot);                                                     // read
-        const float vj = __ldcg(conv_out + 2 * kdim + h * dv + js[r]);
-        const float d = be * (vj - dot);
-        const float4 sn = make_float4(fmaf(kk.x, d, rr.x), fmaf(kk.y, d, rr.y), fmaf(kk.z, d, rr.z),
-                                      fmaf(kk.w, d, rr.w));  // rank-1 update
-        *reinterpret_cast<float4*>(S + (static_cast<size_t>(h) * dv + js[r]) * kDk + 4 * lane) = sn;
-        float oq = sn.x * qq.x;
-        oq = fmaf(sn.y, qq.y, oq);
-        oq = fmaf(sn.z, qq.z, oq);
-        oq = fmaf(sn.w, qq.w, oq);
-        oq = warp_sum(oq);  // query
-        if (lane == 0) o[h * dv + js[r]] = oq * scale;
+    for (int i0 = 0; i0 < kMaxRowsPerWarp; i0 += 4) {
+        if (i0 >= rpw) break;
+        float4 rr[4];
+        float dot[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float4 sv = *reinterpret_cast<const float4*>(st + (j0 + i0 + t) * kDk + 4 * lane);
+            rr[t] = make_float4(g * sv.x, g * sv.y, g * sv.z, g * sv.w);  // decay
+            float d = rr[t].x * kk.x;
+            d = fmaf(rr[t].y, kk.y, d);
+            d = fmaf(rr[t].z, kk.z, d);
+            dot[t] = fmaf(rr[t].w, kk.w, d);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) dot[t] += __shfl_xor_sync(FULL, dot[t], off);  // read
+        float oq[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int j = j0 + i0 + t;
+            const float d = be * (__shfl_sync(FULL, vl, i0 + t) - dot[t]);
+            const float4 sn = make_float4(fmaf(kk.x, d, rr[t].x), fmaf(kk.y, d, rr[t].y), fmaf(kk.z, d, rr[t].z),
+                                          fmaf(kk.w, d, rr[t].w));  // rank-1 update
+            *reinterpret_cast<float4*>(a.S + (static_cast<size_t>(h) * a.dv + j) * kDk + 4 * lane) = sn;
+            float q = sn.x * qq.x;
+            q = fmaf(sn.y, qq.y, q);
+            q = fmaf(sn.z, qq.z, q);
+            oq[t] = fmaf(sn.w, qq.w, q);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) oq[t] += __shfl_xor_sync(FULL, oq[t], off);  // query
+#pragma unroll
+        for (int t = 0; t < 4; ++t) o[i0 + t] = oq[t] * scale;
     }
+    // gated RMSNorm over the head's dv rows (warp partials in order)
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerWarp; ++i)
+        if (i < rpw) ss = fmaf(o[i], o[i], ss);
+    if (lane == 0) wss[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < 8; ++w) tot += wss[w];
+    const float rn = 1.0f / sqrtf(tot / static_cast<float>(a.dv) + a.eps);
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerWarp; ++i)
+        if (lane == i) mine = o[i];
+    if (lane < rpw) a.u[h * a.dv + j0 + lane] = ((mine * rn) * wn) * silu(zl);
+}
+
+__global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y, int n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) h[i] = __ldcg(h + i) + __ldcg(y + i);
 }
 
 // ------------------------------------------------------ GQA decode attention
@@ -217,6 +328,7 @@ struct AttnArgs {
     unsigned* count;     // [nkv]
     float* out;          // [nh*hd], gated
     unsigned* err;
+    L2Prefetch next;
     int kvd, T, max_splits, n_rot;
     float theta_scale, eps;
 };
@@ -305,6 +417,7 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
                     bulk_g2s(dst + kHd, a.vc + off, kHd * 4, &full[slot], pol);
                 }
                 issued = st + 1;
+                if (st == 0) a.next.issue();
             }
             if (!ok)
                 for (int st = max(0, issued - kAttnStages); st < issued; ++st)
@@ -483,37 +596,64 @@ int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------- launchers
-static int ffn(const qg_model* m, qg_state* s, const qg_layer_dev& L, float* h, cudaStream_t st) {
+static size_t q4_bytes(int n, int k) { return static_cast<size_t>(n) * (k / 256) * 144; }
+static size_t q6_bytes(int n, int k) { return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 210; }
+static L2Prefetch prefetch_of(const void* p0, size_t b0, const void* p1 = nullptr, size_t b1 = 0) {
+    L2Prefetch pf{};
+    pf.p[0] = static_cast<const uint8_t*>(p0);
+    pf.bytes[0] = b0;
+    pf.p[1] = static_cast<const uint8_t*>(p1);
+    pf.bytes[1] = b1;
+    return pf;
+}
+// Operands of the first kernel of layer il + 1 (or of the lm_head), for the
+// L2 prefetch issued by the last kernel of layer il.
+static L2Prefetch next_layer_prefetch(const qg_model* m, const qg_state* s, int il) {
     const qg_config& c = m->cfg;
+    if (il + 1 >= c.n_layers)  // the lm_head: its first 8 MB
+        return prefetch_of(m->lm_head, std::min<size_t>(q6_bytes(c.vocab, c.hidden), 8u << 20));
+    const qg_layer_dev& N = m->layers[il + 1];
+    if (N.kind == QG_LAYER_DELTANET)
+        return prefetch_of(N.w_in, q4_bytes(N.n_in, c.hidden), N.conv_w, sizeof(float) * m->conv_dim * c.conv_kernel);
+    return prefetch_of(N.w_in, q4_bytes(N.n_in, c.hidden));
+}
+// Residual stream: a layer maps (A, pending y) -> (A, pending y') with B as
+// the temporary: its first kernel stores A + y (or the embedding row) to B,
+// its ffn_up stores B + y_mixer to A; the output GEMVs only store y.
+static ProRmsNorm norm_pro(const float* h, const float* y, const float* w, const int* tok, float* h_out, float eps,
+                           int k) {
     ProRmsNorm pn{};
     pn.h = h;
-    pn.w = L.post_norm;
-    pn.tok = nullptr;
-    pn.h_out = nullptr;
-    pn.eps = c.eps;
-    pn.kdim = c.hidden;
-    EpiSwiGlu sw{};
-    sw.act = s->act;
-    int rc = launch_gemv<QT_Q4K, true>(L.w_gate, L.w_up, c.ffn, c.hidden, pn, sw, st, true, s->err);
-    if (rc) return rc;
-    EpiResidual er{};
-    er.h = h;
-    return launch_gemv<QT_Q6K, false>(L.w_down, nullptr, c.hidden, c.ffn, ProPlain{s->act}, er, st, true, s->err);
-}
-
-static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev& L, float* h, bool embed) {
-    ProRmsNorm pn{};
-    pn.h = embed ? m->embd : h;
-    pn.w = L.attn_norm;
-    pn.tok = embed ? s->slots : nullptr;
-    pn.h_out = h;
-    pn.eps = m->cfg.eps;
-    pn.kdim = m->cfg.hidden;
+    pn.y = y;
+    pn.w = w;
+    pn.tok = tok;
+    pn.h_out = h_out;
+    pn.eps = eps;
+    pn.kdim = k;
     return pn;
 }
 
-int run_deltanet_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
-                       bool pdl_first) {
+static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const qg_layer_dev& L = m->layers[il];
+    EpiSwiGlu sw{};
+    sw.act = s->act;
+    int rc = launch_gemv<QT_Q4K, true>(L.w_gate, L.w_up, c.ffn, c.hidden,
+                                       norm_pro(io.b, s->y, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
+                                       s->err, prefetch_of(L.w_down, q6_bytes(c.hidden, c.ffn)));
+    if (rc) return rc;
+    EpiStore ey{};
+    ey.y = s->y;
+    return launch_gemv<QT_Q6K, false>(L.w_down, nullptr, c.hidden, c.ffn, ProPlain{s->act}, ey, st, true, s->err,
+                                      next_layer_prefetch(m, s, il));
+}
+
+static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev& L, const ResidualIO& io) {
+    if (io.embed) return norm_pro(m->embd, nullptr, L.attn_norm, s->slots, io.b, m->cfg.eps, m->cfg.hidden);
+    return norm_pro(io.a, io.y_pending ? s->y : nullptr, L.attn_norm, nullptr, io.b, m->cfg.eps, m->cfg.hidden);
+}
+
+int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
     EpiDnIn ei{};
@@ -528,24 +668,40 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStr
     ei.dt = s->dt;
     ei.beta = s->beta;
     ei.z = s->z;
-    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, h, embed), ei, st,
-                                        pdl_first, s->err);
+    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ei, st, pdl_first,
+                                        s->err,
+                                        prefetch_of(s->ssm[il], sizeof(float) * c.n_v_heads * c.head_v_dim * kDk));
     if (rc) return rc;
-    rc = launch_pdl(delta_kernel, dim3(c.head_v_dim / 16, c.n_v_heads), dim3(256), 0, st, true, s->conv_out, s->dt,
-                    s->beta, s->ssm[il], s->o, c.n_k_heads, c.head_v_dim, m->k_dim, c.eps);
+    {
+        DeltaArgs da{};
+        da.conv_out = s->conv_out;
+        da.dt = s->dt;
+        da.beta = s->beta;
+        da.S = s->ssm[il];
+        da.z = s->z;
+        da.w_norm = L.ssm_norm;
+        da.u = s->o;
+        da.err = s->err;
+        da.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->v_dim));
+        da.nk = c.n_k_heads;
+        da.dv = c.head_v_dim;
+        da.kdim = m->k_dim;
+        da.eps = c.eps;
+        const int smem = c.head_v_dim * kDk * 4;
+        static int configured = 0;
+        if (smem > configured) {
+            QG_CUDA(cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+            configured = smem;
+        }
+        rc = launch_pdl(delta_kernel, dim3(c.n_v_heads), dim3(256), smem, st, true, da);
+        if (rc) return rc;
+    }
+    EpiStore ey{};
+    ey.y = s->y;
+    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->v_dim, ProPlain{s->o}, ey, st, true, s->err,
+                                    prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
-    ProGatedNorm pg{};
-    pg.o = s->o;
-    pg.z = s->z;
-    pg.w = L.ssm_norm;
-    pg.dv = c.head_v_dim;
-    pg.eps = c.eps;
-    pg.kdim = m->v_dim;
-    EpiResidual er{};
-    er.h = h;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->v_dim, pg, er, st, true, s->err);
-    if (rc) return rc;
-    return ffn(m, s, L, h, st);
+    return ffn(m, s, il, io, st);
 }
 
 template <int GS>
@@ -559,7 +715,7 @@ static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaSt
     return launch_pdl(attn_kernel<GS>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
 }
 
-int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
+int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
                         bool pdl_first) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
@@ -570,10 +726,11 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaSt
     ea.slots = s->slots;
     ea.qd2 = 2 * m->q_dim;
     ea.kvd = m->kv_dim;
-    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, h, embed), ea, st,
-                                        pdl_first, s->err);
+    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ea, st, pdl_first,
+                                        s->err);
     if (rc) return rc;
     AttnArgs a{};
+    a.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->q_dim));
     a.qf = s->qf;
     a.kraw = s->kraw;
     a.kc = s->kc[il];
@@ -600,29 +757,29 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaSt
         default: return set_err(QG_ERR_SHAPE, "attention: %d query heads per kv head", c.n_heads / c.n_kv_heads);
     }
     if (rc) return rc;
-    EpiResidual er{};
-    er.h = h;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->q_dim, ProPlain{s->attn}, er, st, true, s->err);
+    EpiStore ey{};
+    ey.y = s->y;
+    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->q_dim, ProPlain{s->attn}, ey, st, true, s->err,
+                                    prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
-    return ffn(m, s, L, h, st);
+    return ffn(m, s, il, io, st);
 }
 
-int run_lmhead(const qg_model* m, qg_state* s, const float* h, cudaStream_t st, bool advance) {
+int run_residual(float* h, const float* y, int n, cudaStream_t st) {
+    return launch_pdl(residual_add_kernel, dim3((n + 255) / 256), dim3(256), 0, st, true, h, y, n);
+}
+
+int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance) {
     const qg_config& c = m->cfg;
-    ProRmsNorm pn{};
-    pn.h = h;
-    pn.w = m->out_norm;
-    pn.tok = nullptr;
-    pn.h_out = nullptr;
-    pn.eps = c.eps;
-    pn.kdim = c.hidden;
     EpiArgmaxStep ea{};
     ea.ws = s->am_ws;
     ea.slots = s->slots;
     ea.hist = s->hist;
     ea.err = s->err;
     ea.advance = advance ? 1 : 0;
-    return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden, pn, ea, st, true, s->err);
+    return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden,
+                                      norm_pro(a, s->y, m->out_norm, nullptr, h_final, c.eps, c.hidden), ea, st, true,
+                                      s->err);
 }
 
 }  // namespace qg

@@ -113,11 +113,13 @@ int check_config(const qg_config* c) {
                            "(%d) must be a positive multiple of n_k_heads (%d)",
                            c->n_v_heads, c->n_k_heads);
         if (c->head_k_dim != 128) return set_err(QG_ERR_SHAPE, "config: head_k_dim %d (served: 128)", c->head_k_dim);
-        if (c->head_v_dim < 16 || c->head_v_dim % 16)
-            return set_err(QG_ERR_SHAPE, "config: head_v_dim %d is not a multiple of 16", c->head_v_dim);
         if ((c->n_v_heads * c->head_v_dim) % 256)
             return set_err(QG_ERR_SHAPE, "config: n_v_heads*head_v_dim must be a multiple of 256");
-        if (c->conv_kernel < 2) return set_err(QG_ERR_SHAPE, "config: conv_kernel %d < 2", c->conv_kernel);
+        if (c->conv_kernel < 2 || c->conv_kernel > 8)
+            return set_err(QG_ERR_SHAPE, "config: conv_kernel %d (served: 2..8)", c->conv_kernel);
+        if (c->head_v_dim > 128)
+            return set_err(QG_ERR_SHAPE, "config: head_v_dim %d (served: up to 128)", c->head_v_dim);
+        if (c->head_v_dim % 32) return set_err(QG_ERR_SHAPE, "config: head_v_dim %d is not a multiple of 32", c->head_v_dim);
     }
     if (has_attn) {
         if (c->head_dim != 256) return set_err(QG_ERR_SHAPE, "config: head_dim %d (served: 256)", c->head_dim);
@@ -143,11 +145,12 @@ void free_all(std::vector<void*>& v) {
 int enqueue_token(qg_model* m, qg_state* s, cudaStream_t st, bool advance) {
     for (int il = 0; il < m->cfg.n_layers; ++il) {
         const bool first = il == 0;
-        int rc = m->kinds[il] == QG_LAYER_DELTANET ? run_deltanet_layer(m, s, il, s->h, st, first, !first)
-                                                     : run_attention_layer(m, s, il, s->h, st, first, !first);
+        const ResidualIO io{s->hres, s->h, !first, first};
+        int rc = m->kinds[il] == QG_LAYER_DELTANET ? run_deltanet_layer(m, s, il, io, st, !first)
+                                                     : run_attention_layer(m, s, il, io, st, !first);
         if (rc) return rc;
     }
-    return run_lmhead(m, s, s->h, st, advance);
+    return run_lmhead(m, s, s->hres, s->h, st, advance);
 }
 
 int count_kernel_nodes(cudaGraph_t g, uint64_t* out) {
@@ -377,7 +380,8 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
     }
     if (!rc) {
         const size_t H = c.hidden;
-        (void)((rc = dalloc(s->allocs, &s->h, H, cnt)) || (rc = dalloc(s->allocs, &s->conv_out, m->conv_dim, cnt)) ||
+        (void)((rc = dalloc(s->allocs, &s->h, H, cnt)) || (rc = dalloc(s->allocs, &s->hres, H, cnt)) ||
+               (rc = dalloc(s->allocs, &s->y, H, cnt)) || (rc = dalloc(s->allocs, &s->conv_out, m->conv_dim, cnt)) ||
                (rc = dalloc(s->allocs, &s->dt, c.n_v_heads + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->beta, c.n_v_heads + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->z, m->v_dim + 1, cnt)) || (rc = dalloc(s->allocs, &s->o, m->v_dim + 1, cnt)) ||
@@ -448,6 +452,8 @@ int qg_state_reset(qg_state* s) {
         if (s->vc[il]) QG_CUDA(cudaMemset(s->vc[il], 0, sizeof(float) * static_cast<size_t>(s->max_seq) * m->kv_dim));
     }
     QG_CUDA(cudaMemset(s->h, 0, sizeof(float) * c.hidden));
+    QG_CUDA(cudaMemset(s->hres, 0, sizeof(float) * c.hidden));
+    QG_CUDA(cudaMemset(s->y, 0, sizeof(float) * c.hidden));
     QG_CUDA(cudaMemset(s->attn_count, 0, sizeof(unsigned) * (c.n_kv_heads + 1)));
     QG_CUDA(cudaMemset(s->am_ws, 0, 2 * sizeof(unsigned long long)));
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
@@ -548,7 +554,11 @@ int qg_deltanet_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, 
         return set_err(QG_ERR_LAYER_KIND, "deltanet_step: layer %d is a full-attention layer", il);
     if (reinterpret_cast<uintptr_t>(hidden_dev) & 15u) return set_err(QG_ERR_ARG, "deltanet_step: hidden not 16-byte aligned");
     DeviceGuard dg(m->device);
-    return run_deltanet_layer(m, s, il, hidden_dev, reinterpret_cast<cudaStream_t>(stream), false, true);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const ResidualIO io{hidden_dev, s->h, false, false};
+    int rc = run_deltanet_layer(m, s, il, io, st, true);
+    if (rc) return rc;
+    return run_residual(hidden_dev, s->y, m->cfg.hidden, st);
 }
 
 int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, int pos, qg_stream stream) {
@@ -563,7 +573,9 @@ int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_de
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int p = pos;  // pageable source: the copy is staged before the call returns
     QG_CUDA(cudaMemcpyAsync(s->slots + 1, &p, sizeof(int), cudaMemcpyHostToDevice, st));
-    int rc = run_attention_layer(m, s, il, hidden_dev, st, false, false);
+    const ResidualIO io{hidden_dev, s->h, false, false};
+    int rc = run_attention_layer(m, s, il, io, st, false);
+    if (!rc) rc = run_residual(hidden_dev, s->y, m->cfg.hidden, st);
     if (rc) return rc;
     if (s->kv_len < pos + 1) s->kv_len = pos + 1;
     return QG_OK;

@@ -78,6 +78,33 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
+// Hint the TMA engine to pull [src, src + bytes) into L2 (no shared memory
+// involved); src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Prefetch ranges for the kernel that runs next: each CTA of the current
+// kernel pulls its 1/gridDim share of every range into L2, so that the next
+// kernel's bulk copies hit L2 even when its CTAs become resident late.
+struct L2Prefetch {
+    const uint8_t* p[2];
+    unsigned long long bytes[2];
+    __device__ void issue() const {
+        const unsigned long long nb = gridDim.x * gridDim.y;
+        const unsigned long long id = blockIdx.x + static_cast<unsigned long long>(blockIdx.y) * gridDim.x;
+        for (int i = 0; i < 2; ++i) {
+            if (!p[i] || bytes[i] == 0) continue;
+            const unsigned long long units = (bytes[i] + 15) / 16;  // 16-byte units
+            const unsigned long long u0 = units * id / nb, u1 = units * (id + 1) / nb;
+            for (unsigned long long u = u0; u < u1; u += 4096) {  // at most 64 KB per instruction
+                const unsigned long long n = (u1 - u < 4096 ? u1 - u : 4096);
+                bulk_prefetch_l2(p[i] + 16 * u, static_cast<unsigned>(16 * n));
+            }
+        }
+    }
+};
+
 // ------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -113,8 +140,12 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 __device__ __forceinline__ float f16_to_f32(uint16_t bits) {
     return __half2float(__ushort_as_half(bits));
 }
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+// x / (1 + exp(-x)) and 1 / (1 + exp(-x)) with the quotient taken as a
+// reciprocal-multiply (2 ulp): activations of magnitude ~100 make exp(-x)
+// overflow to inf, where an IEEE division would take its slow path; here the
+// reciprocal of inf is 0 and the result the same signed zero.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + expf(-x)); }
 __device__ __forceinline__ float softplus(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
 
 // Loads of activations written by an earlier kernel: cached in L2 only.

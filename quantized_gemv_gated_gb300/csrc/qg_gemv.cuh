@@ -52,6 +52,7 @@ struct GemvShape {
     int pro_floats;  // prologue scratch floats
     int rows_cta;    // most rows one CTA owns (row-result buffer of deferred epilogues)
     unsigned* err;
+    L2Prefetch next;  // operands of the next kernel, pulled into L2 by the producer
 };
 
 // Shared-memory layout offsets.  aux: per 256-element super-block the unit
@@ -291,7 +292,8 @@ __host__ __device__ inline size_t rows_bytes(int qt, int rows, int nb) {
 // -------------------------------------------------------------- the kernel
 // Pro: prepare(float* sm, int k, int tid) fills its scratch (consumers only),
 //      value(const float* sm, int i) gives x_i.
-// Epi: start() after the dependency wait; with kDeferred, the row results of
+// Epi: pre(r0, r1, tid) before the dependency wait (loads of data no kernel
+//      of the current step writes), start() after it; with kDeferred, the row results of
 //      the CTA go to shared memory and apply(r0, r1, ys, ys2, tid) runs once
 //      over all of them with every consumer thread (one memory round trip for
 //      the whole CTA); otherwise row(r, v) / row2(r, v0, v1) is called by the
@@ -371,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
                     }
                 }
                 issued = t + 1;
+                if (t == 0) sh.next.issue();  // after this CTA's first stage is on its way
             }
+            if (nst == 0) sh.next.issue();
             if (!ok) {
                 // do not leave while copies into this CTA's shared memory are in flight
                 for (int t = max(0, issued - S); t < issued; ++t)
@@ -382,9 +386,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
     }
 
     // ------------------------------------------------------------ consumers
-    pdl_wait();
     Pro pro = pro_in;
     Epi epi = epi_in;
+    epi.pre(r0, r1, tid);  // inputs of the epilogue that no earlier kernel of this step writes
+    pdl_wait();
     pro.prepare(psm, sh.k, tid);
     bar_sync(1, kConsumers);
     build_xrep<QT>(pro, psm, dig, aux, sh.k, warp, lane);
@@ -446,10 +451,14 @@ struct ProPlain {
     __device__ float value(const float* sm, int i) const { return sm[i]; }
 };
 
-// x = RMSNorm(h) * w (rmsnorm_into).  With `tok` set, h is row *tok of the
-// embedding table and CTA 0 also stores it to h_out (the residual stream).
+// x = RMSNorm(h + y) * w (residual_add_into then rmsnorm_into): the residual
+// add of the previous GEMV is done here, by every CTA on its own copy, and
+// CTA 0 stores h + y to h_out (the residual stream, double-buffered so that
+// no CTA of this kernel reads what CTA 0 writes).  y may be null.  With
+// `tok` set, h is row *tok of the embedding table (the step's first layer).
 struct ProRmsNorm {
     const float* h;
+    const float* y;
     const float* w;
     const int* tok;
     float* h_out;
@@ -463,11 +472,18 @@ struct ProRmsNorm {
         float ss = 0.0f;
 #pragma unroll 4
         for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
-            const float4 v = ldcg4(src + i);
+            float4 v = ldcg4(src + i);
+            if (y) {
+                const float4 a = ldcg4(y + i);
+                v.x += a.x;
+                v.y += a.y;
+                v.z += a.z;
+                v.w += a.w;
+            }
             const float4 ww = __ldg(reinterpret_cast<const float4*>(w + i));
             *reinterpret_cast<float4*>(sm + i) = v;
             *reinterpret_cast<float4*>(sm + k + i) = ww;
-            if (tok && blockIdx.x == 0) *reinterpret_cast<float4*>(h_out + i) = v;
+            if (h_out && blockIdx.x == 0) *reinterpret_cast<float4*>(h_out + i) = v;
             ss = fmaf(v.x, v.x, ss);
             ss = fmaf(v.y, v.y, ss);
             ss = fmaf(v.z, v.z, ss);
@@ -485,43 +501,10 @@ struct ProRmsNorm {
     __device__ float value(const float* sm, int i) const { return (sm[i] * r) * sm[kdim + i]; }
 };
 
-// x = per-head RMSNorm(o_h) * w * silu(z_h) (gdn_gated_rmsnorm_into).
-struct ProGatedNorm {
-    const float* o;
-    const float* z;
-    const float* w;
-    int dv;
-    float eps;
-    int kdim;  // = k
-    __host__ __device__ int floats(int k) const { return 2 * k + dv + k / dv + 8; }
-    __device__ void prepare(float* sm, int k, int tid) {
-        float* zs = sm + k;
-        float* wsm = sm + 2 * k;
-        float* rh = wsm + dv;
-#pragma unroll 4
-        for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
-            *reinterpret_cast<float4*>(sm + i) = ldcg4(o + i);
-            *reinterpret_cast<float4*>(zs + i) = ldcg4(z + i);
-        }
-        for (int i = tid; i < dv; i += kConsumers) wsm[i] = __ldg(w + i);
-        bar_sync(1, kConsumers);
-        const int warp = tid >> 5, lane = tid & 31, nh = k / dv;
-        for (int hh = warp; hh < nh; hh += kConsumerWarps) {
-            float ss = 0.0f;
-            for (int j = lane; j < dv; j += 32) ss = fmaf(sm[hh * dv + j], sm[hh * dv + j], ss);
-            ss = warp_sum(ss);
-            if (lane == 0) rh[hh] = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
-        }
-    }
-    __device__ float value(const float* sm, int i) const {
-        const int hh = i / dv, j = i - hh * dv;
-        return ((sm[i] * sm[2 * kdim + dv + hh]) * sm[2 * kdim + j]) * silu(sm[kdim + i]);
-    }
-};
-
 // ------------------------------------------------------------- epilogues
 struct EpiBase {
     static constexpr bool kDeferred = true;
+    __device__ void pre(int, int, int) {}
     __device__ void start() {}
     __device__ void row(int, float) {}
     __device__ void row2(int, float, float) {}
@@ -531,12 +514,6 @@ struct EpiStore : EpiBase {
     float* y;
     __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
         for (int r = r0 + tid; r < r1; r += kConsumers) y[r] = ys[r - r0];
-    }
-};
-struct EpiResidual : EpiBase {  // h += W x (residual_add_into)
-    float* h;
-    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
-        for (int r = r0 + tid; r < r1; r += kConsumers) h[r] = __ldcg(h + r) + ys[r - r0];
     }
 };
 struct EpiSwiGlu : EpiBase {  // act = silu(W_gate x) * (W_up x) (fused_swiglu_into)

@@ -76,9 +76,10 @@ inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1
 // previous kernel on the stream finishes).
 template <int QT, bool DUAL, class Pro, class Epi>
 int launch_gemv(const void* w0, const void* w1, int n, int k, const Pro& pro, const Epi& epi, cudaStream_t st,
-                bool pdl, unsigned* err, int max_ctas = 0) {
+                bool pdl, unsigned* err, const L2Prefetch& next = L2Prefetch{}, int max_ctas = 0) {
     int grid = 1;
-    const GemvShape sh = gemv_geometry(QT, DUAL, w0, w1, n, k, pro.floats(k), max_ctas, err, &grid);
+    GemvShape sh = gemv_geometry(QT, DUAL, w0, w1, n, k, pro.floats(k), max_ctas, err, &grid);
+    sh.next = next;
     const int smem = gemv_smem(QT, DUAL, k, sh.pro_floats, sh.rows_cta, sh.stages, sh.stage_bytes);
     auto kern = gemv_kernel<QT, DUAL, Pro, Epi>;
     static int configured = 0;  // per instantiation: largest dynamic smem granted so far

@@ -45,8 +45,10 @@ struct qg_state {
     int kv_len;
     cudaStream_t stream;
     std::vector<float*> conv, ssm, kc, vc;  // per layer, null for the other kind
-    // scratch
-    float *h, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *attn;
+    // scratch; h: the residual stream after the last step (the lm_head input
+    // plus the last pending y), hres: the residual stream between layers, y:
+    // the output of the last GEMV, not yet added
+    float *h, *hres, *y, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *attn;
     float *part_acc, *part_ml;
     unsigned* attn_count;       // [n_kv_heads] split arrivals (left at 0)
     unsigned long long* am_ws;  // lm_head argmax workspace (left at 0)
@@ -63,16 +65,27 @@ struct qg_state {
 
 namespace qg {
 
-// Enqueue one layer on `st`.  `h` is the residual stream; `embed` makes the
-// first kernel gather h from the embedding row of slots[0]; `pdl_first`
-// allows the first kernel to overlap the previous kernel on the stream.
-int run_deltanet_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
-                       bool pdl_first);
-int run_attention_layer(const qg_model* m, qg_state* s, int il, float* h, cudaStream_t st, bool embed,
+// Residual-stream buffers of one layer: the layer reads a (+ the pending
+// state y when y_pending, or the embedding row of slots[0] when embed), keeps
+// its intermediate stream in b, and leaves the stream in a with its last
+// GEMV's output pending in the state's y.
+struct ResidualIO {
+    float* a;
+    float* b;
+    bool y_pending;
+    bool embed;
+};
+
+// Enqueue one layer on `st`; `pdl_first` allows its first kernel to overlap
+// the previous kernel on the stream.
+int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first);
+int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
                         bool pdl_first);
-// Output norm + fused lm_head GEMV + argmax -> slots[0] / slots[2];
-// `advance` also records hist[pos] and moves slots[1] to pos + 1.
-int run_lmhead(const qg_model* m, qg_state* s, const float* h, cudaStream_t st, bool advance);
+// h += y (closes a layer run on its own).
+int run_residual(float* h, const float* y, int n, cudaStream_t st);
+// Output norm of a + y (stored to h_final) + fused lm_head GEMV + argmax ->
+// slots[0] / slots[2]; `advance` also records hist[pos] and moves slots[1].
+int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance);
 // a = -exp(A_log) on the device.
 int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st);
 
