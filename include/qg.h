@@ -199,6 +199,22 @@ size_t qg_lmhead_argmax_workspace_bytes(void);
 int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, void* workspace,
                      uint32_t* tok_dev, qg_stream stream);
 
+/* qg_lmhead_argmax with its workspace in the library's static device memory
+ * (16 of 256 bytes per device): no allocation of any kind, no workspace
+ * argument; same arguments, result and errors otherwise.  For callers that
+ * must not allocate (device memory reserved up front by a pool; a loop on a
+ * latency budget, where an allocation call can synchronise the device).  The
+ * first call on each device (the device current at the call) resolves the
+ * scratch address and zeroes it, synchronously: make that first call before
+ * any stream capture.  Every call leaves the scratch zeroed.  There is one
+ * scratch per device, so calls on one device must not overlap on the GPU
+ * (two streams at once race on it).  The pages have no counterpart of this
+ * entry point.  Errors: those of qg_lmhead_argmax, QG_ERR_CUDA when the
+ * scratch cannot be resolved, QG_ERR_SHAPE if the kernel's workspace ever
+ * outgrew the static area. */
+int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, int k, uint32_t* tok_dev,
+                             qg_stream stream);
+
 /* First index of the maximum of x[n] (NaN never wins) -> *idx_dev. */
 int qg_argmax_f32(const float* x, int n, uint32_t* idx_dev, qg_stream stream);
 

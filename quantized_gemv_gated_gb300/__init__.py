@@ -28,7 +28,8 @@ EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
     "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
-    "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_argmax_f32",
+    "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
+    "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
 ]
@@ -108,6 +109,7 @@ def lib():
             "qg_gemv_q6k": [p, p, p, i, i, p],
             "qg_q6k_to_planar": [p, p, i, i, p],
             "qg_lmhead_argmax": [p, p, i, i, p, p, p],
+            "qg_lmhead_argmax_noalloc": [p, p, i, i, p, p],
             "qg_argmax_f32": [p, i, p, p],
             "qg_deltanet_step": [p, p, i, p, p],
             "qg_attn_decode_step": [p, p, i, p, i, p],
@@ -191,6 +193,10 @@ def qg_lmhead_argmax_workspace_bytes():
 def qg_lmhead_argmax(w_planar, x, n_vocab, k, workspace, tok, stream=None):
     return _check(lib().qg_lmhead_argmax(_dev(w_planar), _dev(x), n_vocab, k, _dev(workspace), _dev(tok),
                                          _stream(stream)))
+
+
+def qg_lmhead_argmax_noalloc(w_planar, x, n_vocab, k, tok, stream=None):
+    return _check(lib().qg_lmhead_argmax_noalloc(_dev(w_planar), _dev(x), n_vocab, k, _dev(tok), _stream(stream)))
 
 
 def qg_argmax_f32(x, n, idx, stream=None):

@@ -2,6 +2,7 @@
 // fused lm_head GEMV + argmax and a plain argmax; plus the error plumbing
 // shared by the whole library.
 #include <cstring>
+#include <mutex>
 
 #include "qg_host.cuh"
 
@@ -45,6 +46,29 @@ static unsigned* block_err_ptr() {
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_block_err) != cudaSuccess) return nullptr;
     if (dev >= 0 && dev < 64) cache[dev] = p;
     return p;
+}
+
+// Static scratch of qg_lmhead_argmax_noalloc: the fused argmax's workspace
+// (best key, arrival count), 16 of its 256 bytes in use.  Every call leaves it
+// zeroed again; it is zeroed once per device before the first call.
+static __device__ __align__(256) unsigned long long g_lmhead_scratch[32];
+
+static int lmhead_scratch(unsigned long long** out) {
+    static std::mutex mu;
+    static unsigned long long* cache[64] = {nullptr};
+    int dev = 0;
+    QG_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_err(QG_ERR_ARG, "lmhead_argmax_noalloc: device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        unsigned long long* p = nullptr;
+        QG_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_lmhead_scratch));
+        QG_CUDA(cudaMemset(p, 0, sizeof(g_lmhead_scratch)));
+        QG_CUDA(cudaDeviceSynchronize());
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return QG_OK;
 }
 
 // --------------------------------------------------------- Q6_K planar repack
@@ -203,6 +227,30 @@ int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, v
         return set_err(QG_ERR_ARG, "lmhead_argmax: workspace must be 8-byte aligned device memory");
     EpiArgmax epi{};
     epi.ws = static_cast<unsigned long long*>(workspace);
+    epi.tok = tok_dev;
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlain{x}, epi,
+                                      reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
+}
+
+// The same GEMV + argmax with its workspace in static device memory, for
+// callers that must not allocate: a process whose device memory is reserved up
+// front by a pool (a cudaMalloc there fails or evicts the pool), or a decode
+// loop on a latency budget, where an allocation call can synchronise the
+// device.  Nothing here calls cudaMalloc / cudaFree or an allocating library
+// routine; the first call on a device resolves the scratch address with
+// cudaGetSymbolAddress and zeroes it, later calls only launch.
+int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, int k, uint32_t* tok_dev,
+                             qg_stream stream) {
+    int rc = check_gemv_args(w_planar, x, tok_dev, n_vocab, k);
+    if (rc) return rc;
+    if (qg_lmhead_argmax_workspace_bytes() > sizeof(g_lmhead_scratch))
+        return set_err(QG_ERR_SHAPE, "lmhead_argmax_noalloc: the kernel needs %zu bytes of scratch, the static area "
+                                     "holds %zu", qg_lmhead_argmax_workspace_bytes(), sizeof(g_lmhead_scratch));
+    unsigned long long* ws = nullptr;
+    rc = lmhead_scratch(&ws);
+    if (rc) return rc;
+    EpiArgmax epi{};
+    epi.ws = ws;
     epi.tok = tok_dev;
     return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlain{x}, epi,
                                       reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
