@@ -8,11 +8,15 @@ tests/golden/stream_<workload>.json.
 
   0.8b / 4b : 850 seeded prompt tokens fed at positions 0..849, then 128
               greedy tokens (each step's input = the previous step's argmax).
+  0.8b-varied: the 0.8b workload with every quantized matrix's d / dmin
+              drawn below 5e-5 instead of 0.02: the residual stream stays
+              near unit scale, so the argmax follows the token (at 0.02 one
+              token wins every step by a margin of ~50 logits).
   4b-long   : every attention layer's K/V rows 0..7999 ~ N(0,1), DeltaNet
               windows and states ~ N(0,0.1), a seeded first token at
               position 8000, then 63 greedy tokens (64 steps in all).
 
-  python oracle/make_golden.py 0.8b [4b 4b-long] [--threads N]
+  python oracle/make_golden.py 0.8b [0.8b-varied 4b 4b-long] [--threads N]
 """
 import argparse
 import base64
@@ -30,7 +34,8 @@ import oracle  # noqa: E402
 import synth  # noqa: E402
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
-CFGS = {"0.8b": synth.CFG_0P8B, "4b": synth.CFG_4B, "4b-long": synth.CFG_4B_LONG}
+CFGS = {"0.8b": synth.CFG_0P8B, "0.8b-varied": synth.CFG_0P8B, "4b": synth.CFG_4B, "4b-long": synth.CFG_4B_LONG}
+DMAX = {"0.8b-varied": 5e-5}  # quantized-scale bound per workload (default 0.02)
 
 
 def b64(a):
@@ -39,7 +44,7 @@ def b64(a):
 
 def run(name, log=print):
     cfg = CFGS[name]
-    w = synth.make_model_weights(cfg)
+    w = synth.make_model_weights(cfg, dmax=DMAX.get(name, 0.02))
     om = oracle.Model(w)
     st = oracle.State(om)
     steps = []  # (pos, input token)
@@ -80,7 +85,7 @@ def run(name, log=print):
     doc = {
         "source": "written by oracle/make_golden.py from the CPU oracle (f32, natural-order accumulation) on the "
                   "seeded synthetic workload; master seed 0x5147",
-        "workload": name, "config": cfg.as_dict(), "start_pos": start, "n_prompt": n_prompt,
+        "workload": name, "config": cfg.as_dict(), "dmax": DMAX.get(name, 0.02), "start_pos": start, "n_prompt": n_prompt,
         "n_greedy": n_greedy, "prompt": prompt, "tokens": out_tok, "top1": top1, "margin": margin,
         "hidden": hidden, "oracle_threads": oracle.max_threads(), "seconds": round(time.time() - t0, 1),
     }

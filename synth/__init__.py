@@ -172,7 +172,10 @@ class ModelWeights:
     layers: List[LayerWeights]
 
 
-def make_model_weights(cfg: ModelConfig, master: int = MASTER_SEED) -> ModelWeights:
+def make_model_weights(cfg: ModelConfig, master: int = MASTER_SEED, dmax: float = 0.02) -> ModelWeights:
+    """Seeded random-init weights of a model config.  `dmax` bounds the fp16
+    super-block scales d / dmin of every quantized matrix (uniform in
+    [0, dmax)); the model workloads use 0.02."""
     s = lambda name: subseed(master, name)  # noqa: E731
     H, F = cfg.hidden, cfg.ffn
     layers = []
@@ -181,9 +184,9 @@ def make_model_weights(cfg: ModelConfig, master: int = MASTER_SEED) -> ModelWeig
         common = dict(
             attn_norm=normal(s(p + "attn_norm"), H, 1.0, 0.1),
             post_attention_norm=normal(s(p + "post_attention_norm"), H, 1.0, 0.1),
-            ffn_gate=q4k_tensor(s(p + "ffn_gate"), F, H),
-            ffn_up=q4k_tensor(s(p + "ffn_up"), F, H),
-            ffn_down=q6k_tensor(s(p + "ffn_down"), H, F),
+            ffn_gate=q4k_tensor(s(p + "ffn_gate"), F, H, dmax),
+            ffn_up=q4k_tensor(s(p + "ffn_up"), F, H, dmax),
+            ffn_down=q6k_tensor(s(p + "ffn_down"), H, F, dmax),
         )
         if kind == DELTANET:
             lw = LayerWeights(
@@ -192,28 +195,28 @@ def make_model_weights(cfg: ModelConfig, master: int = MASTER_SEED) -> ModelWeig
                 ssm_a_log=uniform(s(p + "ssm_a_log"), cfg.n_v_heads, -1.0, 1.0),
                 ssm_dt_bias=normal(s(p + "ssm_dt_bias"), cfg.n_v_heads, 0.0, 0.5),
                 ssm_norm=normal(s(p + "ssm_norm"), cfg.head_v_dim, 1.0, 0.1),
-                attn_qkv=q4k_tensor(s(p + "attn_qkv"), cfg.conv_dim, H),
-                ssm_alpha=q4k_tensor(s(p + "ssm_alpha"), cfg.n_v_heads, H),
-                ssm_beta=q4k_tensor(s(p + "ssm_beta"), cfg.n_v_heads, H),
-                attn_gate=q4k_tensor(s(p + "attn_gate"), cfg.v_dim, H),
-                ssm_out=q4k_tensor(s(p + "ssm_out"), H, cfg.v_dim),
+                attn_qkv=q4k_tensor(s(p + "attn_qkv"), cfg.conv_dim, H, dmax),
+                ssm_alpha=q4k_tensor(s(p + "ssm_alpha"), cfg.n_v_heads, H, dmax),
+                ssm_beta=q4k_tensor(s(p + "ssm_beta"), cfg.n_v_heads, H, dmax),
+                attn_gate=q4k_tensor(s(p + "attn_gate"), cfg.v_dim, H, dmax),
+                ssm_out=q4k_tensor(s(p + "ssm_out"), H, cfg.v_dim, dmax),
             )
         else:
             lw = LayerWeights(
                 kind=kind, **common,
                 attn_q_norm=normal(s(p + "attn_q_norm"), cfg.head_dim, 1.0, 0.1),
                 attn_k_norm=normal(s(p + "attn_k_norm"), cfg.head_dim, 1.0, 0.1),
-                attn_q=q4k_tensor(s(p + "attn_q"), 2 * cfg.q_dim, H),
-                attn_k=q4k_tensor(s(p + "attn_k"), cfg.kv_dim, H),
-                attn_v=q4k_tensor(s(p + "attn_v"), cfg.kv_dim, H),
-                attn_output=q4k_tensor(s(p + "attn_output"), H, cfg.q_dim),
+                attn_q=q4k_tensor(s(p + "attn_q"), 2 * cfg.q_dim, H, dmax),
+                attn_k=q4k_tensor(s(p + "attn_k"), cfg.kv_dim, H, dmax),
+                attn_v=q4k_tensor(s(p + "attn_v"), cfg.kv_dim, H, dmax),
+                attn_output=q4k_tensor(s(p + "attn_output"), H, cfg.q_dim, dmax),
             )
         layers.append(lw)
     return ModelWeights(
         cfg=cfg,
         token_embd=normal(s("token_embd"), (cfg.vocab, H), 0.0, 1.0),
         output_norm=normal(s("output_norm"), H, 1.0, 0.1),
-        lm_head=q6k_tensor(s("output"), cfg.vocab, H),
+        lm_head=q6k_tensor(s("output"), cfg.vocab, H, dmax),
         layers=layers,
     )
 

@@ -1,0 +1,92 @@
+"""Whole-model greedy streams on the GPU against the oracle's stored streams.
+
+Each golden file under tests/golden/stream_<workload>.json was written by
+oracle/make_golden.py from the CPU oracle alone.  Here the same seeded
+weights and prompt go through the C ABI: the prompt token by token
+(qg_decode_token, one graph replay per call), then the greedy continuation on
+the device (qg_decode_greedy).  Bars: every token id identical, the residual
+stream at the sampled positions within 1e-3 normwise relative error.
+
+The 0.8b / 4b workloads (d, dmin < 0.02) repeat one token at every step, each
+by a top-1 margin of 50+ logits; 0.8b-varied (d, dmin < 5e-5) keeps the
+residual near unit scale, so its argmax changes with the token and the margins
+are ~0.03-1 logit.
+"""
+import base64
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+qg = pytest.importorskip("quantized_gemv_gated_gb300")
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TOL = 1e-3
+CFGS = {"0.8b": synth.CFG_0P8B, "0.8b-varied": synth.CFG_0P8B, "4b": synth.CFG_4B, "4b-long": synth.CFG_4B_LONG}
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def _golden(name):
+    path = os.path.join(GOLDEN, f"stream_{name}.json")
+    if not os.path.exists(path):
+        pytest.skip(f"no stored stream for {name}")
+    with open(path) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("name", ["0.8b", "0.8b-varied", "4b", "4b-long"])
+def test_greedy_stream_matches_oracle(name):
+    g = _golden(name)
+    cfg = CFGS[name]
+    assert g["config"] == cfg.as_dict(), "stored stream was written for another config"
+    w = synth.make_model_weights(cfg, dmax=g.get("dmax", 0.02))
+    m = qg.Model(w)
+    st = qg.State(m, cfg.max_seq_len)
+    start, n_prompt, n_greedy = g["start_pos"], g["n_prompt"], g["n_greedy"]
+    if name == "4b-long":
+        for il, kind in enumerate(cfg.kinds()):
+            if kind == synth.DELTANET:
+                st.upload_layer(il, *synth.initial_deltanet_state(cfg, il))
+            else:
+                st.upload_kv(il, *synth.long_context_kv(cfg, il, start))
+    del w
+    want_h = {int(p): np.frombuffer(base64.b64decode(b), np.float32) for p, b in g["hidden"].items()}
+    errs = {}
+
+    def check_hidden(pos):
+        if pos in want_h:
+            e = rel(st.download_hidden(), want_h[pos])
+            errs[pos] = e
+            assert e <= TOL, f"{name} pos {pos}: hidden rel err {e:.3g}"
+
+    got = []
+    for i in range(n_prompt):
+        pos = start + i
+        got.append(qg.qg_decode_token(m, st, int(g["prompt"][i]), pos))
+        if got[-1] != g["tokens"][i]:
+            pytest.fail(f"{name} pos {pos}: token {got[-1]} != oracle {g['tokens'][i]} "
+                        f"(oracle margin {g['margin'][i]:.4g})")
+        check_hidden(pos)
+    pos, end = start + n_prompt, start + n_prompt + n_greedy
+    while pos < end:
+        # run the device loop up to the next sampled position, then read the stream
+        stop = min([p for p in want_h if p >= pos] + [end - 1])
+        n = stop - pos + 1
+        got.extend(int(t) for t in qg.qg_decode_greedy(m, st, pos, n))
+        pos += n
+        check_hidden(stop)
+    for i, (a, b) in enumerate(zip(got, g["tokens"])):
+        assert a == b, f"{name} step {i} (pos {start + i}): token {a} != oracle {b} (margin {g['margin'][i]:.4g})"
+    assert len(got) == len(g["tokens"])
+    assert st.kv_len == end
+    print(f"{name}: {len(got)} tokens identical ({len(set(got))} distinct), "
+          f"hidden rel err at {sorted(errs)}: max {max(errs.values()):.3g}")
