@@ -226,7 +226,9 @@ def run_ours(args, rank, world, local):
     K, W = args.steps, args.warmup
     w = synth.make_model_weights(cfg)
     m = qg.Model(w, device=local)
+    mode = qg.STEP_PERSISTENT if args.step_mode == "persistent" else qg.STEP_KERNELS
     st = qg.State(m, cfg.max_seq_len)
+    st.set_step_mode(mode)
     # warm up (graph capture, clocks), then restart the sequence for the timed run
     pos, _ = prefill(qg, m, st, cfg, long_ctx, args.prompt)
     qg.qg_decode_greedy(m, st, pos, W)
@@ -253,6 +255,7 @@ def run_ours(args, rank, world, local):
     dt2 = None
     if not args.no_e2e:
         st2 = qg.State(m, cfg.max_seq_len)
+        st2.set_step_mode(mode)
         p2, tok = prefill(qg, m, st2, cfg, long_ctx, args.prompt)
         ext2 = torch.cuda.ExternalStream(st2.stream)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -299,7 +302,7 @@ def run_ours(args, rank, world, local):
         "ms_per_step": round(1000.0 * dt / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
         "config": {"workload": f"{args.workload}: {desc}", "global_batch": world, "seq_len": cfg.max_seq_len,
-                   "parallelism": f"replicas x{world}", "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
+                   "parallelism": f"replicas x{world}", "step_mode": args.step_mode, "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
                    "l2": f"no flush: {bpt / 1e6:.1f} MB of weights and state per token > 129 MB L2",
                    "greedy_tokens_head": [int(t) for t in toks[:4]]},
         "bytes_per_token": int(bpt),
@@ -362,6 +365,8 @@ def main():
                     help="prompt tokens fed before the timed decode (default 850)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
+    ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
+                    help="whole-token step: one kernel per fused op, or one persistent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

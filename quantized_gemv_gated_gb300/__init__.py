@@ -27,12 +27,15 @@ ERROR_NAMES = {0: "QG_OK", -1: "QG_ERR_SHAPE", -2: "QG_ERR_QTYPE", -3: "QG_ERR_E
 EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
-    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
+    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_step_mode", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
     "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
 ]
+
+
+STEP_KERNELS, STEP_PERSISTENT = 0, 1  # qg_state_set_step_mode
 
 
 class QgError(RuntimeError):
@@ -105,6 +108,7 @@ def lib():
             "qg_state_kv_len": [p, ctypes.POINTER(i)],
             "qg_state_stream": [p, ctypes.POINTER(p)],
             "qg_state_stats": [p, ctypes.POINTER(QgStats)],
+            "qg_state_set_step_mode": [p, i],
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
             "qg_q6k_to_planar": [p, p, i, i, p],
@@ -339,6 +343,10 @@ class State:
         st = QgStats()
         _check(lib().qg_state_stats(self.handle, ctypes.byref(st)))
         return st.as_dict()
+
+    def set_step_mode(self, mode):
+        """STEP_KERNELS (default) or STEP_PERSISTENT (qg_state_set_step_mode)."""
+        _check(lib().qg_state_set_step_mode(self.handle, int(mode)))
 
 
 def qg_deltanet_step(model, state, il, hidden, stream=None):

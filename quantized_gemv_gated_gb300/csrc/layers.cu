@@ -23,147 +23,9 @@
 // argmax epilogue (first index on ties).
 #include <algorithm>
 
-#include "qg_internal.cuh"
+#include "qg_layers.cuh"
 
 namespace qg {
-
-// ------------------------------------------------------------ epilogues
-// DeltaNet input projection rows: [0, C) qkv -> conv; [C, C+nv) alpha;
-// [C+nv, C+2nv) beta; [C+2nv, C+2nv+v_dim) z.  Each consumer thread owns rows
-// r0 + tid, r0 + tid + 256, ...; the conv window and weights of its first row
-// (state of the previous token, and constants) are loaded before the
-// dependency wait.
-constexpr int kMaxConvTaps = 8;
-struct EpiDnIn : EpiBase {
-    int C, nv, K;
-    float* win;          // [C][K-1], oldest first
-    const float* wconv;  // [C][K]
-    float* conv_out;
-    const float* dt_bias;
-    const float* a;
-    float* dt;
-    float* beta;
-    float* z;
-    int pre_row;
-    float pw[kMaxConvTaps], pwin[kMaxConvTaps], plast;
-    __device__ void pre(int r0, int r1, int tid) {
-        pre_row = r0 + tid;
-        if (pre_row < r1 && pre_row < C) {
-            const float* kw = wconv + static_cast<size_t>(pre_row) * K;
-            const float* wc = win + static_cast<size_t>(pre_row) * (K - 1);
-#pragma unroll
-            for (int t = 0; t < kMaxConvTaps - 1; ++t) {
-                if (t < K - 1) {
-                    pw[t] = kw[t];
-                    pwin[t] = __ldcg(wc + t);
-                }
-            }
-            plast = kw[K - 1];
-        }
-    }
-    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
-        for (int r = r0 + tid; r < r1; r += kConsumers) row_out(r, ys[r - r0]);
-    }
-    __device__ void row_out(int r, float v) {
-        if (r < C) {
-            // causal conv1d + SiLU, then roll the window (gdn_causal_conv1d_silu_into)
-            float* wc = win + static_cast<size_t>(r) * (K - 1);
-            float acc = 0.0f;
-            if (r == pre_row) {
-#pragma unroll
-                for (int t = 0; t < kMaxConvTaps - 1; ++t)
-                    if (t < K - 1) acc += pw[t] * pwin[t];
-#pragma unroll
-                for (int t = 1; t < kMaxConvTaps - 1; ++t)
-                    if (t < K - 1) wc[t - 1] = pwin[t];
-                acc += plast * v;
-            } else {
-                const float* kw = wconv + static_cast<size_t>(r) * K;
-                for (int t = 0; t < K - 1; ++t) {
-                    const float wt = __ldcg(wc + t);
-                    acc += kw[t] * wt;
-                    if (t > 0) wc[t - 1] = wt;
-                }
-                acc += kw[K - 1] * v;
-            }
-            conv_out[r] = silu(acc);
-            wc[K - 2] = v;
-        } else if (r < C + nv) {
-            const int h = r - C;  // dt = softplus(alpha + dt_bias) * a (gdn_gates_into)
-            dt[h] = softplus(v + dt_bias[h]) * a[h];
-        } else if (r < C + 2 * nv) {
-            beta[r - C - nv] = sigmoid(v);
-        } else {
-            z[r - C - 2 * nv] = v;
-        }
-    }
-};
-
-// Attention input projection rows: [0, 2qd) [q | gate] per head; [2qd,
-// 2qd+kvd) k before its norm; [2qd+kvd, 2qd+2kvd) v, straight into the V
-// cache row at the position in slots[1] (the cache append).
-struct EpiAttnIn : EpiBase {
-    float* qf;
-    float* kraw;
-    float* vcache;
-    const int* slots;
-    int qd2, kvd;
-    int pos;
-    __device__ void start() { pos = __ldcg(slots + 1); }
-    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
-        for (int r = r0 + tid; r < r1; r += kConsumers) {
-            const float v = ys[r - r0];
-            if (r < qd2) qf[r] = v;
-            else if (r < qd2 + kvd) kraw[r - qd2] = v;
-            else vcache[static_cast<size_t>(pos) * kvd + (r - qd2 - kvd)] = v;
-        }
-    }
-};
-
-// lm_head argmax of the whole-token step: publishes the token to slots[0]
-// (the next step's embedding input) and slots[2] (the host readback, with
-// bit 31 set when any kernel of the step set the device error word).
-struct EpiArgmaxStep : EpiBase {
-    static constexpr bool kDeferred = false;
-    unsigned long long* ws;
-    int* slots;
-    uint32_t* hist;
-    const unsigned* err;
-    int advance;
-    unsigned long long best;
-    __device__ void start() { best = 0ull; }
-    __device__ void row(int r, float v) {
-        const unsigned long long key = argmax_key(v, static_cast<unsigned>(r));
-        best = key > best ? key : best;
-    }
-    __device__ void finish(float* sm, int tid) {
-        unsigned long long* red = reinterpret_cast<unsigned long long*>(sm);
-        best = warp_max_u64(best);
-        if ((tid & 31) == 0) red[tid >> 5] = best;
-        bar_sync(1, kConsumers);
-        if (tid == 0) {
-            unsigned long long m = 0ull;
-            for (int i = 0; i < kConsumerWarps; ++i) m = red[i] > m ? red[i] : m;
-            atomicMax(ws, m);
-            __threadfence();
-            const unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(ws + 1), 1u);
-            if (prev == gridDim.x - 1) {
-                __threadfence();
-                const unsigned long long key = atomicExch(ws, 0ull);
-                atomicExch(reinterpret_cast<unsigned*>(ws + 1), 0u);
-                const unsigned tok = key ? argmax_key_index(key) : 0u;
-                const unsigned e = __ldcg(err);
-                slots[0] = static_cast<int>(tok);
-                slots[2] = static_cast<int>(tok | (e ? 0x80000000u : 0u));
-                if (advance) {
-                    const int pos = __ldcg(slots + 1);
-                    hist[pos] = tok;
-                    slots[1] = pos + 1;
-                }
-            }
-        }
-    }
-};
 
 // ------------------------------------------------------------ delta rule
 // One CTA per value head h (gdn_delta_rule_into + gdn_gated_rmsnorm_into),
@@ -173,9 +35,6 @@ struct EpiArgmaxStep : EpiBase {
 // time so that their warp reductions overlap; the gated RMSNorm of the head
 // (a sum of o^2 over its dv rows) is reduced inside the CTA in warp order and
 // the kernel writes u = rmsnorm(o_h) * w * silu(z_h), the ssm_out input.
-constexpr int kDk = 128;
-constexpr int kMaxRowsPerWarp = 16;
-
 struct DeltaArgs {
     const float* conv_out;  // [q | k | v] after conv + SiLU
     const float* dt;        // log-decay per value head
@@ -237,47 +96,14 @@ __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
         if (!mbar_wait(&bar, 0)) atomicOr(a.err, DEVERR_DRAIN_WAIT);
         return;
     }
-    const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
     const float4 kk = *reinterpret_cast<const float4*>(ks + 4 * lane);
     const float4 qq = *reinterpret_cast<const float4*>(qs + 4 * lane);
     float o[kMaxRowsPerWarp];
 #pragma unroll
     for (int i0 = 0; i0 < kMaxRowsPerWarp; i0 += 4) {
         if (i0 >= rpw) break;
-        float4 rr[4];
-        float dot[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float4 sv = *reinterpret_cast<const float4*>(st + (j0 + i0 + t) * kDk + 4 * lane);
-            rr[t] = make_float4(g * sv.x, g * sv.y, g * sv.z, g * sv.w);  // decay
-            float d = rr[t].x * kk.x;
-            d = fmaf(rr[t].y, kk.y, d);
-            d = fmaf(rr[t].z, kk.z, d);
-            dot[t] = fmaf(rr[t].w, kk.w, d);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) dot[t] += __shfl_xor_sync(FULL, dot[t], off);  // read
-        float oq[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int j = j0 + i0 + t;
-            const float d = be * (__shfl_sync(FULL, vl, i0 + t) - dot[t]);
-            const float4 sn = make_float4(fmaf(kk.x, d, rr[t].x), fmaf(kk.y, d, rr[t].y), fmaf(kk.z, d, rr[t].z),
-                                          fmaf(kk.w, d, rr[t].w));  // rank-1 update
-            *reinterpret_cast<float4*>(a.S + (static_cast<size_t>(h) * a.dv + j) * kDk + 4 * lane) = sn;
-            float q = sn.x * qq.x;
-            q = fmaf(sn.y, qq.y, q);
-            q = fmaf(sn.z, qq.z, q);
-            oq[t] = fmaf(sn.w, qq.w, q);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) oq[t] += __shfl_xor_sync(FULL, oq[t], off);  // query
-#pragma unroll
-        for (int t = 0; t < 4; ++t) o[i0 + t] = oq[t] * scale;
+        delta_rows4(st + (j0 + i0) * kDk, a.S + (static_cast<size_t>(h) * a.dv + j0 + i0) * kDk, kk, qq, vl, i0, g, be,
+                    lane, o + i0);
     }
     // gated RMSNorm over the head's dv rows (warp partials in order)
     float ss = 0.0f;
@@ -303,18 +129,6 @@ __global__ void residual_add_kernel(float* __restrict__ h, const float* __restri
     if (i < n) h[i] = __ldcg(h + i) + __ldcg(y + i);
 }
 
-// ------------------------------------------------------ GQA decode attention
-// Grid (max_splits, n_kv_heads), 8 consumer warps + 1 producer warp.  CTA
-// (s, g) covers cache rows [s*T, min((s+1)*T, pos+1)) for the GS query heads
-// of kv group g (contiguous groups).  The producer streams the split's K and V
-// rows of group g (1 KB each) into a shared-memory ring with bulk copies,
-// 8 keys per stage; rows older than pos are fetched before the dependency
-// wait, V[pos] (written by the previous kernel) after it, and K[pos] is
-// computed here.  head_dim = 256: lane owns dims 4*lane..+3 and 128+4*lane..+3.
-constexpr int kHd = 256;
-constexpr int kAttnStages = 4;
-constexpr int kKeysPerStage = 8;
-
 struct AttnArgs {
     const float* qf;     // [nh][2*hd]: q then gate per head
     const float* kraw;   // [nkv*hd]
@@ -338,19 +152,6 @@ __host__ __device__ inline int attn_smem_floats() {
     return GS * kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd + 64 * GS * 2 + kAttnStages * kKeysPerStage * 2 * kHd;
 }
 
-__device__ __forceinline__ void row8(const float* p, int lane, float* v) {
-    const float4 a = *reinterpret_cast<const float4*>(p + 4 * lane);
-    const float4 b = *reinterpret_cast<const float4*>(p + 128 + 4 * lane);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load_row8(const float* p, int lane, float* v) {
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(p + 4 * lane));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(p + 128 + 4 * lane));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ int dim8(int lane, int j) { return j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4; }
 
 template <int GS>
 __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {

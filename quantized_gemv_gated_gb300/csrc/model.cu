@@ -179,7 +179,7 @@ int capture(qg_model* m, qg_state* s, bool greedy, cudaGraphExec_t* exec) {
         cudaError_t e = cudaMemcpyAsync(s->slots, s->pinned, 2 * sizeof(int), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) rc = cuda_err(e, "capture H2D");
     }
-    if (!rc) rc = enqueue_token(m, s, st, greedy);
+    if (!rc) rc = s->step_mode == QG_STEP_PERSISTENT ? run_step(s, st, greedy) : enqueue_token(m, s, st, greedy);
     if (!rc && !greedy) {
         cudaError_t e = cudaMemcpyAsync(s->pinned + 2, s->slots + 2, sizeof(int), cudaMemcpyDeviceToHost, st);
         if (e != cudaSuccess) rc = cuda_err(e, "capture D2H");
@@ -351,6 +351,10 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
     s->kv_len = 0;
     s->exec_step = nullptr;
     s->exec_greedy = nullptr;
+    s->step = nullptr;
+    s->step_mode = QG_STEP_KERNELS;
+    s->step_grid = s->step_smem = 0;
+    s->gbar = nullptr;
     std::memset(&s->stats, 0, sizeof s->stats);
     const qg_config& c = m->cfg;
     uint64_t* cnt = &s->stats.device_allocs;
@@ -394,7 +398,8 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                             cnt)) ||
                (rc = dalloc(s->allocs, &s->attn_count, c.n_kv_heads + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->am_ws, 2, cnt)) || (rc = dalloc(s->allocs, &s->slots, 4, cnt)) ||
-               (rc = dalloc(s->allocs, &s->hist, max_seq_len, cnt)) || (rc = dalloc(s->allocs, &s->err, 1, cnt)));
+               (rc = dalloc(s->allocs, &s->hist, max_seq_len, cnt)) || (rc = dalloc(s->allocs, &s->err, 1, cnt)) ||
+               (rc = dalloc(s->allocs, &s->gbar, 4, cnt)));
     }
     if (!rc) {
         void* p = nullptr;
@@ -415,6 +420,7 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
         rc = qg_state_reset(s);
     }
     if (rc) {
+        delete s->step;
         if (s->pinned) cudaFreeHost(s->pinned);
         free_all(s->allocs);
         delete s;
@@ -433,6 +439,7 @@ int qg_state_destroy(qg_state* s) {
     if (s->stream) cudaStreamDestroy(s->stream);
     if (s->pinned) cudaFreeHost(s->pinned);
     free_all(s->allocs);
+    delete s->step;
     delete s;
     return QG_OK;
 }
@@ -458,6 +465,7 @@ int qg_state_reset(qg_state* s) {
     QG_CUDA(cudaMemset(s->am_ws, 0, 2 * sizeof(unsigned long long)));
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
     QG_CUDA(cudaMemset(s->err, 0, sizeof(unsigned)));
+    QG_CUDA(cudaMemset(s->gbar, 0, 4 * sizeof(unsigned)));
     QG_CUDA(cudaDeviceSynchronize());
     s->kv_len = 0;
     return QG_OK;
@@ -538,6 +546,30 @@ int qg_state_kv_len(const qg_state* s, int* kv_len) {
 int qg_state_stream(const qg_state* s, qg_stream* out) {
     if (!s || !out) return set_err(QG_ERR_ARG, "state_stream: NULL argument");
     *out = reinterpret_cast<qg_stream>(s->stream);
+    return QG_OK;
+}
+
+int qg_state_set_step_mode(qg_state* s, int mode) {
+    if (!s) return set_err(QG_ERR_ARG, "set_step_mode: NULL state");
+    if (mode != QG_STEP_KERNELS && mode != QG_STEP_PERSISTENT)
+        return set_err(QG_ERR_ARG, "set_step_mode: unknown mode %d", mode);
+    if (mode == s->step_mode) return QG_OK;
+    DeviceGuard dg(s->m->device);
+    QG_CUDA(cudaStreamSynchronize(s->stream));
+    if (mode == QG_STEP_PERSISTENT && !s->step) {
+        s->step = new (std::nothrow) StepParams();
+        if (!s->step) return set_err(QG_ERR_OOM, "set_step_mode: host allocation");
+        const int rc = step_setup(s->m, s);
+        if (rc) {
+            delete s->step;
+            s->step = nullptr;
+            return rc;
+        }
+    }
+    if (s->exec_step) cudaGraphExecDestroy(s->exec_step);
+    if (s->exec_greedy) cudaGraphExecDestroy(s->exec_greedy);
+    s->exec_step = s->exec_greedy = nullptr;
+    s->step_mode = mode;
     return QG_OK;
 }
 

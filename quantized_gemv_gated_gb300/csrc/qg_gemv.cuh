@@ -284,6 +284,32 @@ __device__ __forceinline__ float row_partial(const uint8_t* stage, int rs, int l
     return acc;
 }
 
+// The chunks c in [4 b0, 4 (b0 + kbs)) with c == lg0 (mod G) of one row,
+// accumulated into acc in chunk order, from a stage holding ur rows x kbs
+// super-blocks that start at block b0 (Q6_K: its D region holds whole rows of
+// nb blocks).  A row split over consecutive stages sums exactly as in one.
+template <int QT>
+__device__ __forceinline__ float row_acc_slice(const uint8_t* stage, int ur, int lrow, int kbs, int b0, int nb, int G,
+                                               int lg0, const uint8_t* dig, const uint8_t* aux, int k, float acc) {
+    const int c_lo = 4 * b0, c_hi = 4 * (b0 + kbs);
+    int c = c_lo + ((lg0 - c_lo) & (G - 1));
+    if constexpr (QT == QT_Q4K) {
+        const uint8_t* row = stage + static_cast<size_t>(lrow) * kbs * 144;
+        for (; c < c_hi; c += G) chunk_q4k(row + ((c >> 2) - b0) * 144, c & 3, 64 * c, dig, aux, k, acc);
+    } else {
+        const uint8_t* ql = stage + static_cast<size_t>(lrow) * kbs * 128;
+        const uint8_t* qh = stage + static_cast<size_t>(ur) * kbs * 128 + static_cast<size_t>(lrow) * kbs * 64;
+        const uint8_t* sc = stage + static_cast<size_t>(ur) * kbs * 192 + static_cast<size_t>(lrow) * kbs * 16;
+        const uint16_t* dd =
+            reinterpret_cast<const uint16_t*>(stage + static_cast<size_t>(ur) * kbs * 208) + static_cast<size_t>(lrow) * nb;
+        for (; c < c_hi; c += G) {
+            const int b = c >> 2, lb = b - b0;
+            chunk_q6k(ql + lb * 128, qh + lb * 64, sc + lb * 16, dd + b, b, c & 3, dig, aux, k, acc);
+        }
+    }
+    return acc;
+}
+
 // Bytes of one stage per matrix for `rows` rows (Q6_K copies whole 8-row groups).
 __host__ __device__ inline size_t rows_bytes(int qt, int rows, int nb) {
     return static_cast<size_t>(rows) * nb * (qt == QT_Q4K ? 144 : 210);

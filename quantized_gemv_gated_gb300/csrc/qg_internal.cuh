@@ -3,6 +3,7 @@
 #include <vector>
 
 #include "qg_host.cuh"
+#include "qg_step.cuh"
 
 // Device-resident weights of one layer.
 struct qg_layer_dev {
@@ -59,6 +60,12 @@ struct qg_state {
     int keys_per_split, max_splits;
     cudaGraphExec_t exec_step;
     cudaGraphExec_t exec_greedy;
+    // persistent whole-step kernel: parameters (null when the model shape is
+    // not served by it) and whether decode calls use it
+    qg::StepParams* step;
+    int step_mode;
+    int step_grid, step_smem;
+    unsigned* gbar;             // device: its barrier words [3] (left at 0)
     qg_stats stats;
     std::vector<void*> allocs;
 };
@@ -86,6 +93,9 @@ int run_residual(float* h, const float* y, int n, cudaStream_t st);
 // Output norm of a + y (stored to h_final) + fused lm_head GEMV + argmax ->
 // slots[0] / slots[2]; `advance` also records hist[pos] and moves slots[1].
 int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance);
+// Persistent step kernel: fill s->step (once per state), launch one step.
+int step_setup(const qg_model* m, qg_state* s);
+int run_step(qg_state* s, cudaStream_t st, bool advance);
 // a = -exp(A_log) on the device.
 int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st);
 

@@ -142,9 +142,13 @@ def tiny():
     return cfg, w, qg.Model(w), oracle.Model(w)
 
 
-def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny):
+@pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
+def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
+    """The graph step (per-kernel or persistent) against the kernel-by-kernel
+    eager step (bitwise) and the oracle (tolerance, exact token)."""
     cfg, w, m, om = tiny
     sg, se = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
+    sg.set_step_mode(mode)
     ost = oracle.State(om)
     toks = synth.prompt_tokens(cfg, 40)
     worst = 0.0
@@ -162,13 +166,16 @@ def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny):
             pytest.fail(f"pos {pos}: token {a} != oracle {ref} (oracle top-2 margin {v1 - v2:.4g})")
     st = sg.stats()
     assert st["graph_captures"] == 1 and st["graph_launches"] == len(toks)
+    assert st["graph_kernel_nodes"] == 1 if mode == qg.STEP_PERSISTENT else st["graph_kernel_nodes"] > 1
     assert st["d2h_bytes"] == 4 * len(toks) and st["h2d_bytes"] == 8 * len(toks)
     print(f"tiny model, 40 tokens: worst hidden rel err {worst:.3g}, {st['graph_kernel_nodes']} kernel nodes")
 
 
-def test_greedy_device_loop_matches_oracle_greedy(tiny):
+@pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
+def test_greedy_device_loop_matches_oracle_greedy(tiny, mode):
     cfg, w, m, om = tiny
     st = qg.State(m, cfg.max_seq_len)
+    st.set_step_mode(mode)
     ost = oracle.State(om)
     toks = synth.prompt_tokens(cfg, 12)
     for pos, t in enumerate(toks):
