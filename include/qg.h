@@ -184,20 +184,22 @@ int qg_state_set_step_mode(qg_state* s, int mode);
  * precision of f32 for that largest element); sub-block sums are exact
  * integers, accumulated in f32.
  * w: Q4_K, raw GGUF layout, 16-byte aligned.  x: [k] f32.  y: [n] f32.
- * k % 256 == 0 else QG_ERR_SHAPE; n == 0 or k == 0 -> QG_ERR_EMPTY. */
+ * k a multiple of 256 up to 16384 else QG_ERR_SHAPE; n == 0 or k == 0 ->
+ * QG_ERR_EMPTY. */
 int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream stream);
 
 /* The same for Q6_K in the library's planar layout (made by qg_q6k_to_planar). */
 int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream);
 
-/* Planar Q6_K: n8 = n rounded up to 8 rows, nb = k/256; four planes, each
- * 16-byte aligned, holding exactly the GGUF bytes (n8*nb*210 in total):
- *   QL [n8*nb][128]: per super-block, for quarter-chunk c = 2*half + part
- *      (0..3), the 16 low-4-bit bytes ql[64*half + 16*part ..] followed by
- *      ql[64*half + 32 + 16*part ..];
- *   QH [n8*nb][64] (as in GGUF), SC [n8*nb][16] int8 scales, D [n8*nb] fp16.
- * Rows n..n8-1 are zero.  qg_q6k_planar_bytes gives the size; src is the raw
- * GGUF tensor and both are device pointers, 16-byte aligned. */
+/* Planar Q6_K (the layout the GEMV engine streams): n8 = n rounded up to 8
+ * rows, nb = k/256.  For every 8-row group g and super-block b one 1680-byte
+ * group-block at ((g*nb) + b)*1680 holding exactly the GGUF bytes of those 8
+ * blocks: QL [8][128] (per row, for quarter-chunk c = 2*half + part (0..3),
+ * the 16 low-4-bit bytes ql[64*half + 16*part ..] followed by
+ * ql[64*half + 32 + 16*part ..]), QH [8][64] (as in GGUF), SC [8][16] int8
+ * scales, D [8] fp16.  Rows n..n8-1 are zero.  qg_q6k_planar_bytes gives the
+ * size (n8*nb*210); src is the raw GGUF tensor and both are device pointers,
+ * 16-byte aligned. */
 size_t qg_q6k_planar_bytes(int n, int k);
 int qg_q6k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream);
 

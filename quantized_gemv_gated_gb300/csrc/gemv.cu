@@ -71,45 +71,75 @@ static int lmhead_scratch(unsigned long long** out) {
     return QG_OK;
 }
 
-// --------------------------------------------------------- Q6_K planar repack
-// One thread per super-block of the n8-row padded matrix (see qg.h).
-__global__ void q6k_planar_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n, int n8, int nb) {
+// ------------------------------------------------- grouped weight layouts
+// One thread per (8-row group, super-block) of the padded matrix; rows n..n8-1
+// are zero.  Q6_K: [QL 8 x 128 | QH 8 x 64 | scales 8 x 16 | d 8 x 2] with each
+// row's QL reordered so that the two 16-byte halves of every 64-weight
+// quarter cq = 2 half + part are adjacent (ql[64 half + 16 part ..] then
+// ql[64 half + 32 + 16 part ..]).  Q4_K: the 8 rows' 144-byte blocks.
+__global__ void q6k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n, int n8, int nb) {
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long total = static_cast<long long>(n8) * nb;
+    const long long total = static_cast<long long>(n8 / 8) * nb;
     if (idx >= total) return;
-    const long long r = idx / nb;
-    uint8_t* ql = dst + idx * 128;
-    uint8_t* qh = dst + total * 128 + idx * 64;
-    uint8_t* sc = dst + total * 192 + idx * 16;
-    uint8_t* dd = dst + total * 208 + idx * 2;
-    if (r >= n) {
-        for (int i = 0; i < 128; ++i) ql[i] = 0;
-        for (int i = 0; i < 64; ++i) qh[i] = 0;
-        for (int i = 0; i < 16; ++i) sc[i] = 0;
-        dd[0] = dd[1] = 0;
-        return;
-    }
-    const uint8_t* b = src + idx * 210;  // rows are contiguous: block idx of the padded grid == of the source
-    for (int c = 0; c < 4; ++c) {
-        const int half = c >> 1, part = c & 1;
-        for (int i = 0; i < 16; ++i) {
-            ql[32 * c + i] = b[64 * half + 16 * part + i];
-            ql[32 * c + 16 + i] = b[64 * half + 32 + 16 * part + i];
+    const long long g = idx / nb, b = idx - g * nb;
+    uint8_t* gb = dst + idx * 1680;
+    for (int rr = 0; rr < 8; ++rr) {
+        const long long r = 8 * g + rr;
+        uint8_t* ql = gb + rr * 128;
+        uint8_t* qh = gb + 1024 + rr * 64;
+        uint8_t* sc = gb + 1536 + rr * 16;
+        uint8_t* dd = gb + 1664 + rr * 2;
+        if (r >= n) {
+            for (int i = 0; i < 128; ++i) ql[i] = 0;
+            for (int i = 0; i < 64; ++i) qh[i] = 0;
+            for (int i = 0; i < 16; ++i) sc[i] = 0;
+            dd[0] = dd[1] = 0;
+            continue;
         }
+        const uint8_t* blk = src + (r * nb + b) * 210;
+        for (int c = 0; c < 4; ++c) {
+            const int half = c >> 1, part = c & 1;
+            for (int i = 0; i < 16; ++i) {
+                ql[32 * c + i] = blk[64 * half + 16 * part + i];
+                ql[32 * c + 16 + i] = blk[64 * half + 32 + 16 * part + i];
+            }
+        }
+        for (int i = 0; i < 64; ++i) qh[i] = blk[128 + i];
+        for (int i = 0; i < 16; ++i) sc[i] = blk[192 + i];
+        dd[0] = blk[208];
+        dd[1] = blk[209];
     }
-    for (int i = 0; i < 64; ++i) qh[i] = b[128 + i];
-    for (int i = 0; i < 16; ++i) sc[i] = b[192 + i];
-    dd[0] = b[208];
-    dd[1] = b[209];
+}
+
+__global__ void q4k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n, int n8, int nb) {
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long total = static_cast<long long>(n8 / 8) * nb;
+    if (idx >= total) return;
+    const long long g = idx / nb, b = idx - g * nb;
+    uint4* gb = reinterpret_cast<uint4*>(dst + idx * 1152);
+    for (int rr = 0; rr < 8; ++rr) {
+        const long long r = 8 * g + rr;
+        for (int i = 0; i < 9; ++i)
+            gb[rr * 9 + i] = r < n ? reinterpret_cast<const uint4*>(src + (r * nb + b) * 144)[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+int q4k_to_grouped(const void* src, void* dst, int n, int k, cudaStream_t st) {
+    const int nb = k / 256, n8 = (n + 7) & ~7;
+    const long long total = static_cast<long long>(n8 / 8) * nb;
+    const long long blocks = (total + 255) / 256;
+    q4k_grouped_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint8_t*>(src),
+                                                                     static_cast<uint8_t*>(dst), n, n8, nb);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
 }
 
 int q6k_to_planar(const void* src, void* dst, int n, int k, cudaStream_t st) {
     const int nb = k / 256, n8 = (n + 7) & ~7;
-    const long long total = static_cast<long long>(n8) * nb;
-    const int threads = 256;
-    const long long blocks = (total + threads - 1) / threads;
-    q6k_planar_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(static_cast<const uint8_t*>(src),
-                                                                       static_cast<uint8_t*>(dst), n, n8, nb);
+    const long long total = static_cast<long long>(n8 / 8) * nb;
+    const long long blocks = (total + 255) / 256;
+    q6k_grouped_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint8_t*>(src),
+                                                                     static_cast<uint8_t*>(dst), n, n8, nb);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
@@ -137,14 +167,15 @@ __global__ void __launch_bounds__(1024) argmax_f32_kernel(const float* __restric
 // (max is exact, so the result does not depend on arrival order), and the
 // last CTA to arrive publishes the token and re-zeroes the workspace.
 struct EpiArgmax : EpiBase {
-    static constexpr bool kDeferred = false;
     unsigned long long* ws;  // ws[0]: best key; ws[1] low word: arrivals
     uint32_t* tok;
     unsigned long long best;
     __device__ void start() { best = 0ull; }
-    __device__ void row(int r, float v) {
-        const unsigned long long key = argmax_key(v, static_cast<unsigned>(r));
-        best = key > best ? key : best;
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) {
+            const unsigned long long key = argmax_key(ys[r - r0], static_cast<unsigned>(r));
+            best = key > best ? key : best;
+        }
     }
     __device__ void finish(float* sm, int tid) {
         unsigned long long* red = reinterpret_cast<unsigned long long*>(sm);
@@ -177,7 +208,7 @@ static int check_gemv_args(const void* w, const float* x, const void* y, int n, 
     if (!w || !x || !y) return set_err(QG_ERR_ARG, "gemv: NULL pointer");
     if (n < 0 || k < 0) return set_err(QG_ERR_ARG, "gemv: negative size n=%d k=%d", n, k);
     if (n == 0 || k == 0) return set_err(QG_ERR_EMPTY, "gemv: empty tensor n=%d k=%d", n, k);
-    if (k % 256) return set_err(QG_ERR_SHAPE, "gemv: k=%d is not a multiple of 256", k);
+    if (!gemv_k_served(k)) return set_err(QG_ERR_SHAPE, "gemv: k=%d is not a multiple of 256 up to 16384", k);
     if (!aligned16(w) || !aligned16(x)) return set_err(QG_ERR_ARG, "gemv: w and x must be 16-byte aligned");
     return QG_OK;
 }
@@ -191,8 +222,8 @@ int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream
     if (rc) return rc;
     EpiStore epi{};
     epi.y = y;
-    return launch_gemv<QT_Q4K, false>(w, nullptr, n, k, ProPlain{x}, epi, reinterpret_cast<cudaStream_t>(stream),
-                                      true, block_err_ptr());
+    return launch_gemv<QT_Q4K, false, LAYOUT_RAW>(w, nullptr, n, k, ProPlainG{x}, epi,
+                                                  reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 
 int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream) {
@@ -200,7 +231,7 @@ int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg
     if (rc) return rc;
     EpiStore epi{};
     epi.y = y;
-    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n, k, ProPlain{x}, epi,
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n, k, ProPlainG{x}, epi,
                                       reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 
@@ -228,7 +259,7 @@ int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, v
     EpiArgmax epi{};
     epi.ws = static_cast<unsigned long long*>(workspace);
     epi.tok = tok_dev;
-    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlain{x}, epi,
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlainG{x}, epi,
                                       reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 
@@ -252,7 +283,7 @@ int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, 
     EpiArgmax epi{};
     epi.ws = ws;
     epi.tok = tok_dev;
-    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlain{x}, epi,
+    return launch_gemv<QT_Q6K, false>(w_planar, nullptr, n_vocab, k, ProPlainG{x}, epi,
                                       reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 

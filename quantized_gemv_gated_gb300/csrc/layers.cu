@@ -397,7 +397,7 @@ int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------- launchers
-static size_t q4_bytes(int n, int k) { return static_cast<size_t>(n) * (k / 256) * 144; }
+static size_t q4_bytes(int n, int k) { return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 144; }
 static size_t q6_bytes(int n, int k) { return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 210; }
 static L2Prefetch prefetch_of(const void* p0, size_t b0, const void* p1 = nullptr, size_t b1 = 0) {
     L2Prefetch pf{};
@@ -445,7 +445,7 @@ static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cud
     if (rc) return rc;
     EpiStore ey{};
     ey.y = s->y;
-    return launch_gemv<QT_Q6K, false>(L.w_down, nullptr, c.hidden, c.ffn, ProPlain{s->act}, ey, st, true, s->err,
+    return launch_gemv<QT_Q6K, false>(L.w_down, nullptr, c.hidden, c.ffn, ProPlainG{s->act}, ey, st, true, s->err,
                                       next_layer_prefetch(m, s, il));
 }
 
@@ -499,7 +499,7 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
     }
     EpiStore ey{};
     ey.y = s->y;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->v_dim, ProPlain{s->o}, ey, st, true, s->err,
+    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->v_dim, ProPlainG{s->o}, ey, st, true, s->err,
                                     prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);
@@ -560,7 +560,7 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
     if (rc) return rc;
     EpiStore ey{};
     ey.y = s->y;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->q_dim, ProPlain{s->attn}, ey, st, true, s->err,
+    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->q_dim, ProPlainG{s->attn}, ey, st, true, s->err,
                                     prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);

@@ -61,24 +61,32 @@ int upload_f32(qg_model* m, float** dst, const float* src, size_t n, const char*
     return upload(*dst, src, n * sizeof(float));
 }
 
-// Concatenate Q4_K tensors with the same k into one row-major matrix.
+// Concatenate Q4_K tensors with the same k row-wise and store them in the
+// grouped layout of the GEMV engine (8-row groups, rows padded to 8).
 int upload_fused(qg_model* m, uint8_t** dst, const qg_qtensor* const* parts, int count, int* rows) {
     size_t total = 0;
     int n = 0;
+    const int k = parts[0]->k;
     for (int i = 0; i < count; ++i) {
         total += qbytes(*parts[i]);
         n += parts[i]->n;
     }
-    int rc = dalloc(m->allocs, dst, total);
+    const size_t grouped = static_cast<size_t>((n + 7) & ~7) * (k / 256) * 144;
+    int rc = dalloc(m->allocs, dst, grouped);
     if (rc) return rc;
+    uint8_t* tmp = nullptr;
+    QG_CUDA(cudaMalloc(&tmp, total));
     size_t off = 0;
-    for (int i = 0; i < count; ++i) {
-        rc = upload(*dst + off, parts[i]->data, qbytes(*parts[i]));
-        if (rc) return rc;
+    for (int i = 0; i < count && !rc; ++i) {
+        rc = upload(tmp + off, parts[i]->data, qbytes(*parts[i]));
         off += qbytes(*parts[i]);
     }
+    if (!rc) rc = q4k_to_grouped(tmp, *dst, n, k, nullptr);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(tmp);
+    if (!rc && e != cudaSuccess) rc = cuda_err(e, "q4k repack");
     *rows = n;
-    return QG_OK;
+    return rc;
 }
 
 int upload_q6k(qg_model* m, uint8_t** dst, const qg_qtensor& t) {
@@ -100,6 +108,9 @@ int check_config(const qg_config* c) {
     if (c->n_layers < 1 || c->hidden < 1 || c->ffn < 1 || c->vocab < 1)
         return set_err(QG_ERR_EMPTY, "config: empty model");
     if (c->hidden % 256 || c->ffn % 256) return set_err(QG_ERR_SHAPE, "config: hidden and ffn must be multiples of 256");
+    if (c->hidden > 16384 || c->ffn > 16384 || c->n_heads * c->head_dim > 16384 ||
+        c->n_v_heads * c->head_v_dim > 16384)
+        return set_err(QG_ERR_SHAPE, "config: a GEMV input is longer than 16384 (the engine's limit)");
     bool has_dn = false, has_attn = false;
     for (int i = 0; i < c->n_layers; ++i) {
         if (c->layer_kinds[i] == QG_LAYER_DELTANET) has_dn = true;

@@ -21,15 +21,11 @@ int device_sms();
         if (e_ != cudaSuccess) return ::qg::cuda_err(e_, #call);   \
     } while (0)
 
-// Bytes of dynamic shared memory one GEMV launch needs.
-inline int gemv_smem(int qt, bool dual, int k, int pro_floats, int rows_cta, int stages, int stage_bytes) {
-    return off_ring(qt, k, pro_floats, (dual ? 2 : 1) * rows_cta) + stages * stage_bytes;
-}
-
-constexpr int kStageMaxBytes = 16 * 1024;  // one stage of the ring
 constexpr int kCtaSmemBytes = 110 * 1024;  // per CTA: two CTAs per SM fit in 228 KB
 
-// Geometry for n rows of k weights (dual: two matrices streamed together).
+// Geometry for n rows of k weights (dual: two matrices streamed together)
+// over at most max_ctas CTAs (0: two per SM).  K is cut into slices of 32
+// chunks, then the binary digits of the remainder (16, 8, 4 chunks).
 inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1, int n, int k, int pro_floats,
                                int max_ctas, unsigned* err, int* grid_out) {
     GemvShape sh{};
@@ -42,46 +38,55 @@ inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1
     sh.cr = k / 64;
     sh.err = err;
     sh.pro_floats = pro_floats;
-    const int per_row = (qt == QT_Q4K ? 144 : 210) * sh.nb * (dual ? 2 : 1);
-    // lanes per row: the largest power of two <= 32 dividing the chunk count,
-    // widened while one pass of 8 warps would not fit a stage
-    int G = 1;
-    while (G < 32 && sh.cr % (2 * G) == 0) G *= 2;
-    while (G < 32 && 8 * (32 / G) * per_row > kStageMaxBytes) G *= 2;
-    sh.lg = 0;
-    while ((1 << sh.lg) < G) ++sh.lg;
-    const int unit_rows = 8 * (32 / G);  // rows of one pass of the 8 consumer warps
+    int c = 0;
+    sh.nsl = 0;
+    while (sh.cr - c >= 32 && sh.nsl < kMaxSlices) {
+        sh.sl_c0[sh.nsl] = c;
+        sh.sl_lg[sh.nsl++] = 5;
+        c += 32;
+    }
+    for (int lg = 4; lg >= 2; --lg)
+        if ((((sh.cr - c) >> lg) & 1) && sh.nsl < kMaxSlices) {
+            sh.sl_c0[sh.nsl] = c;
+            sh.sl_lg[sh.nsl++] = lg;
+            c += 1 << lg;
+        }
     sh.units = (n + 7) / 8;
     int grid = max_ctas > 0 ? max_ctas : 2 * device_sms();
     if (grid > sh.units) grid = sh.units;
     if (grid < 1) grid = 1;
-    const int rows_cta = 8 * ((sh.units + grid - 1) / grid);
-    sh.rows_cta = rows_cta;
-    int rs = unit_rows * (kStageMaxBytes / (unit_rows * per_row) > 0 ? kStageMaxBytes / (unit_rows * per_row) : 1);
-    const int need = ((rows_cta + unit_rows - 1) / unit_rows) * unit_rows;
-    if (rs > need) rs = need;
-    sh.rs = rs;
-    sh.stage_bytes = rs * per_row;
-    int stages = (rows_cta + rs - 1) / rs;
+    sh.rows_cta = 8 * ((sh.units + grid - 1) / grid);
+    const int fixed = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * sh.rows_cta);
+    int stages = (kCtaSmemBytes - fixed) / stage_bytes_of(qt);
     if (stages > kMaxStages) stages = kMaxStages;
-    const int fixed = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * rows_cta);
-    while (stages > 1 && fixed + stages * sh.stage_bytes > kCtaSmemBytes) --stages;
     sh.stages = stages < 1 ? 1 : stages;
     *grid_out = grid;
     return sh;
 }
 
+// k the engine serves: a multiple of 256 whose slices fit kMaxSlices.
+inline bool gemv_k_served(int k) { return k > 0 && k % 256 == 0 && k <= 16384; }
+
+// Bytes of dynamic shared memory one GEMV launch needs.
+inline int gemv_smem(const GemvShape& sh, int qt, bool dual) {
+    return off_ring(qt, sh.k, sh.pro_floats, (dual ? 2 : 1) * sh.rows_cta) + sh.stages * stage_bytes_of(qt);
+}
+
 // Launch one GEMV-engine kernel on `st` (with programmatic stream
 // serialisation when `pdl`, so the weights of this launch stream in while the
-// previous kernel on the stream finishes).
-template <int QT, bool DUAL, class Pro, class Epi>
+// previous kernel on the stream finishes).  err: the device error word, which
+// the kernel also reads as its abort flag.
+template <int QT, bool DUAL, int LAYOUT = LAYOUT_GROUPED, class Pro, class Epi>
 int launch_gemv(const void* w0, const void* w1, int n, int k, const Pro& pro, const Epi& epi, cudaStream_t st,
                 bool pdl, unsigned* err, const L2Prefetch& next = L2Prefetch{}, int max_ctas = 0) {
+    if (!err) return set_err(QG_ERR_CUDA, "gemv: no device error word");
     int grid = 1;
     GemvShape sh = gemv_geometry(QT, DUAL, w0, w1, n, k, pro.floats(k), max_ctas, err, &grid);
     sh.next = next;
-    const int smem = gemv_smem(QT, DUAL, k, sh.pro_floats, sh.rows_cta, sh.stages, sh.stage_bytes);
-    auto kern = gemv_kernel<QT, DUAL, Pro, Epi>;
+    const int smem = gemv_smem(sh, QT, DUAL);
+    if (smem > 227 * 1024)
+        return set_err(QG_ERR_SHAPE, "gemv: %d x %d needs %d bytes of shared memory per CTA", n, k, smem);
+    auto kern = gemv_kernel<QT, LAYOUT, DUAL, Pro, Epi>;
     static int configured = 0;  // per instantiation: largest dynamic smem granted so far
     if (smem > configured) {
         QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));

@@ -96,6 +96,8 @@ int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, c
 // Persistent step kernel: fill s->step (once per state), launch one step.
 int step_setup(const qg_model* m, qg_state* s);
 int run_step(qg_state* s, cudaStream_t st, bool advance);
+// Raw GGUF Q4_K rows -> the engine's grouped layout ((n+7)/8*8 x k/256 x 144 bytes).
+int q4k_to_grouped(const void* src, void* dst, int n, int k, cudaStream_t st);
 // a = -exp(A_log) on the device.
 int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st);
 

@@ -103,7 +103,6 @@ struct EpiAttnIn : EpiBase {
 // (the next step's embedding input) and slots[2] (the host readback, with
 // bit 31 set when any kernel of the step set the device error word).
 struct EpiArgmaxStep : EpiBase {
-    static constexpr bool kDeferred = false;
     unsigned long long* ws;
     int* slots;
     uint32_t* hist;
@@ -111,9 +110,11 @@ struct EpiArgmaxStep : EpiBase {
     int advance;
     unsigned long long best;
     __device__ void start() { best = 0ull; }
-    __device__ void row(int r, float v) {
-        const unsigned long long key = argmax_key(v, static_cast<unsigned>(r));
-        best = key > best ? key : best;
+    __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
+        for (int r = r0 + tid; r < r1; r += kConsumers) {
+            const unsigned long long key = argmax_key(ys[r - r0], static_cast<unsigned>(r));
+            best = key > best ? key : best;
+        }
     }
     __device__ void finish(float* sm, int tid) {
         unsigned long long* red = reinterpret_cast<unsigned long long*>(sm);
@@ -145,14 +146,6 @@ struct EpiArgmaxStep : EpiBase {
 };
 
 // ------------------------------------------------------------ prologues
-// x read straight from global memory (written by an earlier phase; L2 only).
-struct ProPlainG {
-    const float* x;
-    __host__ __device__ int floats(int) const { return 0; }
-    __device__ void prepare(float*, int, int) {}
-    __device__ float value(const float*, int i) const { return __ldcg(x + i); }
-};
-
 // x = gated RMSNorm of the delta-rule output (gdn_gated_rmsnorm_into):
 // u_i = (o_i * rn_h) * w_j * silu(z_i), i = h dv + j, with rn_h = 1 /
 // sqrt(mean_j o^2 + eps).  o and z are staged in shared memory; the sum of
@@ -193,10 +186,12 @@ struct ProGatedNorm {
             sm[h] = 1.0f / sqrtf(tot / static_cast<float>(dv) + eps);
         }
     }
-    __device__ float value(const float* sm, int i) const {
-        const int h = i / dv, j = i - h * dv;
+    __device__ void value8(const float* sm, int i0, float* v) const {
+        const int h = i0 / dv, j0 = i0 - h * dv;  // dv % 8 == 0: the 8 elements share a head
         const float* os = sm + 9 * kMaxGatedHeads;
-        return ((os[i] * sm[h]) * __ldg(w + j)) * silu(os[vk + i]);
+        const float rn = sm[h];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = ((os[i0 + t] * rn) * __ldg(w + j0 + t)) * silu(os[vk + i0 + t]);
     }
 };
 

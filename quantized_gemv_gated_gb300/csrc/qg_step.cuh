@@ -4,6 +4,8 @@
 #pragma once
 #include <cstdint>
 
+#include "qg_gemv.cuh"
+
 namespace qg {
 
 constexpr int kStepMaxLayers = 64;
@@ -12,13 +14,6 @@ constexpr int kStepMaxSlots = 8;           // the ring's mbarriers (16 * kMaxSta
 constexpr int kStepSmemPerCta = 112 * 1024;  // two CTAs per SM
 
 enum StepGemv { SG_DN_IN, SG_ATTN_IN, SG_SSM_OUT, SG_ATTN_OUT, SG_FFN_UP, SG_FFN_DOWN, SG_LMHEAD, SG_COUNT };
-
-// One GEMV phase: n rows of k weights; lanes per row 2^lg (as the GEMV
-// engine picks them), ur = rows of one pass of the 8 consumer warps, kb =
-// super-blocks per stage (nb when a pass fits a slot, else a K-slice).
-struct StepGeo {
-    int n, n8, k, nb, cr, lg, ur, kb, units, rows_cta;
-};
 
 struct StepLayer {
     const uint8_t* w_in;
@@ -42,7 +37,7 @@ struct StepLayer {
 };
 
 struct StepParams {
-    StepGeo geo[SG_COUNT];
+    GemvShape geo[SG_COUNT];  // geometry of each GEMV phase (weights per layer below)
     StepLayer L[kStepMaxLayers];
     int n_layers, hidden, ffn, vocab, conv_dim, conv_k, nv, nk, dv, k_dim, v_dim, q_dim, kv_dim;
     int gs, n_kv, n_rot, T, max_splits;

@@ -27,19 +27,6 @@
 
 namespace qg {
 
-// ------------------------------------------------------------------ ring
-struct Ring {
-    uint64_t* full;
-    uint64_t* empty;
-    uint8_t* base;
-    int ns;
-    unsigned q;  // stages taken so far (same count on both sides)
-    __device__ uint8_t* cur() const { return base + static_cast<size_t>(q % ns) * kSlotBytes; }
-    __device__ uint64_t* cur_full() const { return &full[q % ns]; }
-    __device__ uint64_t* cur_empty() const { return &empty[q % ns]; }
-    __device__ unsigned parity() const { return (q / ns) & 1u; }
-};
-
 __device__ __forceinline__ bool aborted(const StepParams& P) { return __ldcg(P.gbar + 2) != 0u; }
 
 __device__ __forceinline__ void raise_abort(const StepParams& P, unsigned bit) {
@@ -47,189 +34,72 @@ __device__ __forceinline__ void raise_abort(const StepParams& P, unsigned bit) {
     atomicExch(P.gbar + 2, 1u);
 }
 
-// Bounded wait on an mbarrier phase that also gives up when another CTA has
-// aborted the step.
-__device__ bool step_wait(uint64_t* bar, unsigned parity, const StepParams& P) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    int n = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if ((n++ & 255) == 0 && aborted(P)) return false;
-        if (clock64() - t0 > kWaitCycles) return false;
-    }
-    return true;
-}
-
-// Rows [r0, r1) of a phase with `units` 8-row units (the GEMV engine's split).
-__device__ __forceinline__ void cta_rows(int units, int n, int& r0, int& r1) {
-    const int u0 = static_cast<int>((static_cast<long long>(blockIdx.x) * units) / gridDim.x);
-    const int u1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * units) / gridDim.x);
-    r0 = 8 * u0;
-    r1 = min(8 * u1, n);
-}
-
 // ============================================================== producer
-// The whole producer warp runs this (lane-uniform control flow); lane 0 owns
-// the mbarrier protocol, the lanes issue a stage's copies in parallel.
-struct Producer {
-    Ring R;
-    uint64_t pol;
-    int lane;
-    bool ok;
-    // Claim the next slot (wait until the consumers released its last use).
-    __device__ bool acquire(const StepParams& P) {
-        int good = 1;
-        if (lane == 0 && R.q >= static_cast<unsigned>(R.ns))
-            good = step_wait(R.cur_empty(), ((R.q / R.ns) - 1u) & 1u, P) ? 1 : 0;
-        good = __shfl_sync(FULL, good, 0);
-        if (!good) {
-            if (lane == 0) raise_abort(P, DEVERR_EMPTY_WAIT);
-            ok = false;
-        }
-        return good != 0;
-    }
-    __device__ void expect(unsigned bytes) {
-        if (lane == 0) mbar_arrive_expect_tx(R.cur_full(), bytes);
-        __syncwarp();
-    }
-    __device__ void copy(void* dst, const void* src, unsigned bytes) {
-        bulk_g2s(dst, src, bytes, R.cur_full(), pol);
-    }
-    // Wait for every copy this CTA has in flight (error exit).
-    __device__ void drain(const StepParams& P) {
-        if (lane != 0) return;
-        const unsigned lo = R.q > static_cast<unsigned>(R.ns) ? R.q - R.ns : 0u;
-        for (unsigned t = lo; t < R.q; ++t) {
-            const long long t0 = clock64();
-            while (!mbar_try_wait(&R.full[t % R.ns], (t / R.ns) & 1u))
-                if (clock64() - t0 > kWaitCycles) {
-                    atomicOr(P.err, DEVERR_DRAIN_WAIT);
-                    break;
-                }
-        }
-    }
-};
-
-template <int QT, bool DUAL>
-__device__ bool produce_gemv(Producer& pr, const StepParams& P, const StepGeo& g, const uint8_t* w0,
-                             const uint8_t* w1) {
-    int r0, r1;
-    cta_rows(g.units, g.n, r0, r1);
-    const int nb = g.nb, ur = g.ur;
-    for (int row0 = r0; row0 < r1; row0 += ur) {
-        const int rows = min(ur, r1 - row0);
-        for (int b0 = 0; b0 < nb; b0 += g.kb) {
-            const int kbs = min(g.kb, nb - b0);
-            if (!pr.acquire(P)) return false;
-            uint8_t* st = pr.R.cur();
-            if constexpr (QT == QT_Q4K) {
-                constexpr int M = DUAL ? 2 : 1;
-                if (kbs == nb) {
-                    const unsigned bytes = static_cast<unsigned>(rows) * nb * 144u;
-                    pr.expect(M * bytes);
-                    if (pr.lane < M)
-                        pr.copy(st + static_cast<size_t>(pr.lane) * ur * nb * 144,
-                                (pr.lane ? w1 : w0) + static_cast<size_t>(row0) * nb * 144, bytes);
-                } else {
-                    const unsigned piece = static_cast<unsigned>(kbs) * 144u;
-                    pr.expect(M * rows * piece);
-                    for (int i = pr.lane; i < M * rows; i += 32) {
-                        const int m = i / rows, r = i - m * rows;
-                        pr.copy(st + static_cast<size_t>(m) * ur * kbs * 144 + static_cast<size_t>(r) * piece,
-                                (m ? w1 : w0) + (static_cast<size_t>(row0 + r) * nb + b0) * 144, piece);
-                    }
-                }
-            } else {
-                const size_t plane = static_cast<size_t>(g.n8) * nb;
-                const int rows8 = (rows + 7) & ~7;
-                const size_t rb = static_cast<size_t>(row0) * nb;
-                if (kbs == nb) {
-                    pr.expect(static_cast<unsigned>(rows8) * nb * 210u);
-                    if (pr.lane == 0) pr.copy(st, w0 + rb * 128, rows8 * nb * 128);
-                    if (pr.lane == 1) pr.copy(st + static_cast<size_t>(ur) * nb * 128, w0 + plane * 128 + rb * 64, rows8 * nb * 64);
-                    if (pr.lane == 2) pr.copy(st + static_cast<size_t>(ur) * nb * 192, w0 + plane * 192 + rb * 16, rows8 * nb * 16);
-                    if (pr.lane == 3) pr.copy(st + static_cast<size_t>(ur) * nb * 208, w0 + plane * 208 + rb * 2, rows8 * nb * 2);
-                } else {
-                    pr.expect(static_cast<unsigned>(rows) * kbs * 208u + static_cast<unsigned>(rows8) * nb * 2u);
-                    for (int i = pr.lane; i < 3 * rows + 1; i += 32) {
-                        if (i == 3 * rows) {
-                            pr.copy(st + static_cast<size_t>(ur) * kbs * 208, w0 + plane * 208 + rb * 2, rows8 * nb * 2);
-                            continue;
-                        }
-                        const int part = i / rows, r = i - part * rows;
-                        const size_t rk = static_cast<size_t>(row0 + r) * nb + b0;
-                        if (part == 0)
-                            pr.copy(st + static_cast<size_t>(r) * kbs * 128, w0 + rk * 128, kbs * 128);
-                        else if (part == 1)
-                            pr.copy(st + static_cast<size_t>(ur) * kbs * 128 + static_cast<size_t>(r) * kbs * 64,
-                                    w0 + plane * 128 + rk * 64, kbs * 64);
-                        else
-                            pr.copy(st + static_cast<size_t>(ur) * kbs * 192 + static_cast<size_t>(r) * kbs * 16,
-                                    w0 + plane * 192 + rk * 16, kbs * 16);
-                    }
-                }
-            }
-            ++pr.R.q;
-        }
-    }
-    return true;
-}
+// The whole producer warp runs these (lane-uniform control flow); the pipe's
+// lane 0 owns the mbarrier protocol, the lanes issue a stage's copies in
+// parallel.  Weight stages come from the GEMV engine's gemv_produce.
 
 // DeltaNet state rows: item = (value head h, 32 rows), one 16 KB stage.
-__device__ bool produce_delta(Producer& pr, const StepParams& P, const StepLayer& L) {
+__device__ bool produce_delta(Pipe& pr, const StepParams& P, const StepLayer& L) {
     const int per_head = P.dv / 32, items = P.nv * per_head;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int h = it / per_head, jb = (it - h * per_head) * 32;
-        if (!pr.acquire(P)) return false;
+        if (!pr.acquire()) return false;
         pr.expect(32u * kDk * 4u);
-        if (pr.lane == 0) pr.copy(pr.R.cur(), L.ssm + (static_cast<size_t>(h) * P.dv + jb) * kDk, 32u * kDk * 4u);
-        ++pr.R.q;
+        if (pr.lane == 0) pr.copy(pr.cur(), L.ssm + (static_cast<size_t>(h) * P.dv + jb) * kDk, 32u * kDk * 4u);
+        pr.commit();
     }
     return true;
 }
 
 // K/V rows of earlier positions: item = (kv group, split), 8 keys per stage;
 // row pos (appended by this step) is read by the consumers themselves.
-__device__ bool produce_attn(Producer& pr, const StepParams& P, const StepLayer& L, int pos) {
+__device__ bool produce_attn(Pipe& pr, const StepParams& P, const StepLayer& L, int pos) {
     const int n_act = (pos + P.T) / P.T, items = P.n_kv * n_act;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int g = it % P.n_kv, s = it / P.n_kv;
         const int t0 = s * P.T, t1 = min(t0 + P.T, pos + 1);
         for (int k0 = t0; k0 < t1; k0 += kKeysPerStage) {
             const int k1 = min(k0 + kKeysPerStage, t1);
-            if (!pr.acquire(P)) return false;
+            if (!pr.acquire()) return false;
             const int nk = k1 - k0 - ((pos >= k0 && pos < k1) ? 1 : 0);
             pr.expect(static_cast<unsigned>(nk) * 2u * kHd * 4u);
-            float* st = reinterpret_cast<float*>(pr.R.cur());
+            float* st = reinterpret_cast<float*>(pr.cur());
             for (int i = pr.lane; i < 2 * (k1 - k0); i += 32) {
                 const int t = k0 + (i >> 1), which = i & 1;
                 if (t == pos) continue;
                 const size_t off = static_cast<size_t>(t) * P.kv_dim + g * kHd;
                 pr.copy(st + (t - k0) * 2 * kHd + which * kHd, (which ? L.vc : L.kc) + off, kHd * 4u);
             }
-            ++pr.R.q;
+            pr.commit();
         }
     }
     return true;
 }
 
-__device__ void producer_main(Producer& pr, const StepParams& P, int pos) {
-    for (int il = 0; il < P.n_layers && pr.ok; ++il) {
+template <int QT, bool DUAL>
+__device__ bool produce_gemv(Pipe& pr, const GemvShape& g, const uint8_t* w0, const uint8_t* w1) {
+    int r0, r1;
+    cta_rows(g.units, g.n, r0, r1);
+    return gemv_produce<QT, LAYOUT_GROUPED, DUAL>(pr, g, w0, w1, r0, r1, nullptr);
+}
+
+__device__ void producer_main(Pipe& pr, const StepParams& P, int pos) {
+    bool ok = true;
+    for (int il = 0; il < P.n_layers && ok; ++il) {
         const StepLayer& L = P.L[il];
-        bool ok;
         if (L.kind == QG_LAYER_DELTANET) {
-            ok = produce_gemv<QT_Q4K, false>(pr, P, P.geo[SG_DN_IN], L.w_in, nullptr) && produce_delta(pr, P, L) &&
-                 produce_gemv<QT_Q4K, false>(pr, P, P.geo[SG_SSM_OUT], L.w_out, nullptr);
+            ok = produce_gemv<QT_Q4K, false>(pr, P.geo[SG_DN_IN], L.w_in, nullptr) && produce_delta(pr, P, L) &&
+                 produce_gemv<QT_Q4K, false>(pr, P.geo[SG_SSM_OUT], L.w_out, nullptr);
         } else {
-            ok = produce_gemv<QT_Q4K, false>(pr, P, P.geo[SG_ATTN_IN], L.w_in, nullptr) &&
-                 produce_attn(pr, P, L, pos) && produce_gemv<QT_Q4K, false>(pr, P, P.geo[SG_ATTN_OUT], L.w_out, nullptr);
+            ok = produce_gemv<QT_Q4K, false>(pr, P.geo[SG_ATTN_IN], L.w_in, nullptr) && produce_attn(pr, P, L, pos) &&
+                 produce_gemv<QT_Q4K, false>(pr, P.geo[SG_ATTN_OUT], L.w_out, nullptr);
         }
-        ok = ok && produce_gemv<QT_Q4K, true>(pr, P, P.geo[SG_FFN_UP], L.w_gate, L.w_up) &&
-             produce_gemv<QT_Q6K, false>(pr, P, P.geo[SG_FFN_DOWN], L.w_down, nullptr);
-        if (!ok) break;
+        ok = ok && produce_gemv<QT_Q4K, true>(pr, P.geo[SG_FFN_UP], L.w_gate, L.w_up) &&
+             produce_gemv<QT_Q6K, false>(pr, P.geo[SG_FFN_DOWN], L.w_down, nullptr);
     }
-    if (pr.ok) produce_gemv<QT_Q6K, false>(pr, P, P.geo[SG_LMHEAD], P.lm_head, nullptr);
-    if (!pr.ok) pr.drain(P);
+    if (ok) ok = produce_gemv<QT_Q6K, false>(pr, P.geo[SG_LMHEAD], P.lm_head, nullptr);
+    if (!ok) pr.drain();
 }
 
 // ============================================================== consumers
@@ -238,19 +108,13 @@ __device__ void producer_main(Producer& pr, const StepParams& P, int pos) {
 // later wait then returns at once) up to the next grid barrier, which every
 // CTA leaves through its abort exit.
 struct Consumer {
-    Ring R;
+    Pipe R;
     uint8_t* smem;  // dynamic shared memory base (scratch at off_dig())
     int tid, warp, lane;
     int* flag;      // shared int for CTA-wide decisions
     bool ok;        // false once the step is aborted (uniform after a grid barrier)
-    __device__ void wait_full(const StepParams& P) {
-        if (!step_wait(R.cur_full(), R.parity(), P) && lane == 0) raise_abort(P, DEVERR_FULL_WAIT);
-    }
-    __device__ void release() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(R.cur_empty());
-        ++R.q;
-    }
+    __device__ void wait_full() const { R.wait_full(); }
+    __device__ void release() { R.release(); }
 };
 
 // Grid-wide barrier number `nbar` (1-based) among the consumer groups.
@@ -286,59 +150,11 @@ __device__ bool grid_sync(Consumer& c, const StepParams& P, unsigned nbar) {
 }
 
 template <int QT, bool DUAL, class Pro, class Epi>
-__device__ void consume_gemv(Consumer& c, const StepParams& P, const StepGeo& g, Pro pro, Epi epi) {
+__device__ void consume_gemv(Consumer& c, const GemvShape& g, Pro pro, Epi epi) {
     int r0, r1;
     cta_rows(g.units, g.n, r0, r1);
-    const int k = g.k;
-    uint8_t* dig = c.smem + off_dig();
-    uint8_t* aux = c.smem + off_aux(k);
-    float* psm = reinterpret_cast<float*>(c.smem + off_pro(QT, k));
-    float* ys = reinterpret_cast<float*>(c.smem + off_ys(QT, k, pro.floats(k)));
     epi.pre(r0, r1, c.tid);
-    pro.prepare(psm, k, c.tid);
-    bar_sync(1, kConsumers);
-    build_xrep<QT>(pro, psm, dig, aux, k, c.warp, c.lane);
-    epi.start();
-    bar_sync(1, kConsumers);
-
-    const int G = 1 << g.lg, rw = 32 / G;
-    const int grp = c.lane >> g.lg, lg0 = c.lane & (G - 1);
-    const int lr = c.warp * rw + grp;
-    for (int row0 = r0; row0 < r1; row0 += g.ur) {
-        const int rows = min(g.ur, r1 - row0);
-        const bool valid = lr < rows;
-        float v0 = 0.0f, v1 = 0.0f;
-        for (int b0 = 0; b0 < g.nb; b0 += g.kb) {
-            const int kbs = min(g.kb, g.nb - b0);
-            c.wait_full(P);
-            const uint8_t* st = c.R.cur();
-            if (valid) {
-                v0 = row_acc_slice<QT>(st, g.ur, lr, kbs, b0, g.nb, G, lg0, dig, aux, k, v0);
-                if constexpr (DUAL)
-                    v1 = row_acc_slice<QT>(st + static_cast<size_t>(g.ur) * kbs * 144, g.ur, lr, kbs, b0, g.nb, G,
-                                           lg0, dig, aux, k, v1);
-            }
-            c.release();
-        }
-        for (int o = G >> 1; o > 0; o >>= 1) {
-            v0 += __shfl_xor_sync(FULL, v0, o);
-            if constexpr (DUAL) v1 += __shfl_xor_sync(FULL, v1, o);
-        }
-        if (valid && lg0 == 0) {
-            if constexpr (Epi::kDeferred) {
-                ys[row0 + lr - r0] = v0;
-                if constexpr (DUAL) ys[g.rows_cta + row0 + lr - r0] = v1;
-            } else {
-                if constexpr (DUAL) epi.row2(row0 + lr, v0, v1);
-                else epi.row(row0 + lr, v0);
-            }
-        }
-    }
-    if constexpr (Epi::kDeferred) {
-        bar_sync(1, kConsumers);
-        epi.apply(r0, r1, ys, ys + g.rows_cta, c.tid);
-    }
-    epi.finish(psm, c.tid);
+    gemv_consume<QT, LAYOUT_GROUPED, DUAL>(c.R, g, r0, r1, pro, epi, c.smem, c.tid);
 }
 
 // Delta rule, item = (value head h, rows jb..jb+31), four rows per warp; the
@@ -365,7 +181,7 @@ __device__ void consume_delta(Consumer& c, const StepParams& P, const StepLayer&
         const float vl = c.lane < 4 ? __ldcg(P.conv_out + 2 * P.k_dim + h * P.dv + j + c.lane) : 0.0f;
         const float g = expf(__ldcg(P.dt + h)), be = __ldcg(P.beta + h);
         bar_sync(1, kConsumers);
-        c.wait_full(P);
+        c.wait_full();
         const float* st = reinterpret_cast<const float*>(c.R.cur());
         const float4 kk = *reinterpret_cast<const float4*>(ks + 4 * c.lane);
         const float4 qq = *reinterpret_cast<const float4*>(qs + 4 * c.lane);
@@ -446,7 +262,7 @@ __device__ void consume_attn(Consumer& c, const StepParams& P, const StepLayer& 
         }
         const float scale = 1.0f / sqrtf(static_cast<float>(kHd));
         for (int stg = 0; stg < nst; ++stg) {
-            c.wait_full(P);
+            c.wait_full();
             const int t = t0 + stg * kKeysPerStage + warp;
             if (t < t1) {
                 const float* kv_row = reinterpret_cast<const float*>(c.R.cur()) + warp * 2 * kHd;
@@ -585,7 +401,7 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
             ei.dt = P.dt;
             ei.beta = P.beta;
             ei.z = P.z;
-            consume_gemv<QT_Q4K, false>(c, P, P.geo[SG_DN_IN], in_norm, ei);
+            consume_gemv<QT_Q4K, false>(c, P.geo[SG_DN_IN], in_norm, ei);
             if (!grid_sync(c, P, ++nbar)) return;
             consume_delta(c, P, L);
             if (!grid_sync(c, P, ++nbar)) return;
@@ -598,7 +414,7 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
             gn.eps = P.eps;
             EpiStore ey{};
             ey.y = P.y;
-            consume_gemv<QT_Q4K, false>(c, P, P.geo[SG_SSM_OUT], gn, ey);
+            consume_gemv<QT_Q4K, false>(c, P.geo[SG_SSM_OUT], gn, ey);
         } else {
             EpiAttnIn ea{};
             ea.qf = P.qf;
@@ -607,7 +423,7 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
             ea.slots = P.slots;
             ea.qd2 = 2 * P.q_dim;
             ea.kvd = P.kv_dim;
-            consume_gemv<QT_Q4K, false>(c, P, P.geo[SG_ATTN_IN], in_norm, ea);
+            consume_gemv<QT_Q4K, false>(c, P.geo[SG_ATTN_IN], in_norm, ea);
             if (!grid_sync(c, P, ++nbar)) return;
             switch (P.gs) {
                 case 1: consume_attn<1>(c, P, L, pos); break;
@@ -617,16 +433,16 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
             if (!grid_sync(c, P, ++nbar)) return;
             EpiStore ey{};
             ey.y = P.y;
-            consume_gemv<QT_Q4K, false>(c, P, P.geo[SG_ATTN_OUT], ProPlainG{P.attn}, ey);
+            consume_gemv<QT_Q4K, false>(c, P.geo[SG_ATTN_OUT], ProPlainG{P.attn}, ey);
         }
         if (!grid_sync(c, P, ++nbar)) return;
         EpiSwiGlu sw{};
         sw.act = P.act;
-        consume_gemv<QT_Q4K, true>(c, P, P.geo[SG_FFN_UP], step_norm(B, P.y, L.post_norm, nullptr, A, P), sw);
+        consume_gemv<QT_Q4K, true>(c, P.geo[SG_FFN_UP], step_norm(B, P.y, L.post_norm, nullptr, A, P), sw);
         if (!grid_sync(c, P, ++nbar)) return;
         EpiStore ey{};
         ey.y = P.y;
-        consume_gemv<QT_Q6K, false>(c, P, P.geo[SG_FFN_DOWN], ProPlainG{P.act}, ey);
+        consume_gemv<QT_Q6K, false>(c, P.geo[SG_FFN_DOWN], ProPlainG{P.act}, ey);
         if (!grid_sync(c, P, ++nbar)) return;
     }
     EpiArgmaxStep ea{};
@@ -635,7 +451,7 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
     ea.hist = P.hist;
     ea.err = P.err;
     ea.advance = P.advance;
-    consume_gemv<QT_Q6K, false>(c, P, P.geo[SG_LMHEAD], step_norm(A, P.y, P.out_norm, nullptr, P.h, P), ea);
+    consume_gemv<QT_Q6K, false>(c, P.geo[SG_LMHEAD], step_norm(A, P.y, P.out_norm, nullptr, P.h, P), ea);
     // the last CTA out re-arms the barrier words for the next step
     bar_sync(1, kConsumers);
     if (c.tid == 0) {
@@ -663,10 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
         fence_mbar_init();
     }
     __syncthreads();
-    Ring R{full, empty, smem + P.ring_off, P.nslots, 0u};
+    Pipe R{full, empty, smem + P.ring_off, P.nslots, kSlotBytes, 0u, P.err, P.gbar + 2, lane, 0ull};
     if (warp == kConsumerWarps) {
-        Producer pr{R, policy_evict_first(), lane, true};
-        producer_main(pr, P, pos);
+        R.pol = policy_evict_first();
+        producer_main(R, P, pos);
         return;
     }
     Consumer c{R, smem, tid, warp, lane, &flag, true};
@@ -674,34 +490,16 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 }
 
 // ================================================================== host
-static int pick_kb(int qt, bool dual, int ur, int nb, int G) {
-    const int per_block = (qt == QT_Q4K ? 144 : 208) * (dual ? 2 : 1);
-    const int fixed = qt == QT_Q6K ? ur * nb * 2 : 0;  // Q6_K: whole-row D region
-    if (ur * nb * (qt == QT_Q4K ? 144 : 210) * (dual ? 2 : 1) <= kSlotBytes) return nb;
-    int kb = (kSlotBytes - fixed) / (ur * per_block);
-    if (kb < 1) return 0;
-    const int bal = G / 4 > 1 ? G / 4 : 1;  // whole rounds of the row's lanes where possible
-    if (kb >= bal) kb -= kb % bal;
-    return kb;
-}
+static_assert(stage_bytes_of(QT_Q6K) <= kSlotBytes && stage_bytes_of(QT_Q4K) <= kSlotBytes,
+              "a GEMV stage must fit one ring slot");
 
-static int make_geo(StepGeo* g, int qt, bool dual, int n, int k, int pro_floats, int grid, int* scratch) {
-    int dummy = 0;
-    const GemvShape sh = gemv_geometry(qt, dual, nullptr, nullptr, n, k, pro_floats, grid, nullptr, &dummy);
-    g->n = n;
-    g->n8 = sh.n8;
-    g->k = k;
-    g->nb = sh.nb;
-    g->cr = sh.cr;
-    g->lg = sh.lg;
-    g->ur = 8 * (32 >> sh.lg);
-    g->units = sh.units;
-    g->rows_cta = 8 * ((sh.units + grid - 1) / grid);
-    g->kb = pick_kb(qt, dual, g->ur, g->nb, 1 << sh.lg);
-    if (g->kb < 1) return set_err(QG_ERR_SHAPE, "step kernel: a row pass of %d x %d does not fit a ring slot", n, k);
-    if (g->kb < g->nb && g->ur != 8)
-        return set_err(QG_ERR_SHAPE, "step kernel: %d x %d would split rows of a multi-row pass", n, k);
-    const int need = off_ys(qt, k, pro_floats) + 4 * (dual ? 2 : 1) * g->rows_cta;
+static int make_geo(GemvShape* g, int qt, bool dual, int n, int k, int pro_floats, int grid, int* scratch) {
+    if (!gemv_k_served(k)) return set_err(QG_ERR_SHAPE, "step kernel: k=%d", k);
+    int used = 0;
+    *g = gemv_geometry(qt, dual, nullptr, nullptr, n, k, pro_floats, grid, nullptr, &used);
+    // every CTA of the step runs every phase: rows split over the whole grid
+    g->rows_cta = 8 * ((g->units + grid - 1) / grid);
+    const int need = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * g->rows_cta);
     *scratch = std::max(*scratch, need);
     return QG_OK;
 }
@@ -744,11 +542,11 @@ int step_setup(const qg_model* m, qg_state* s) {
             const qg_layer_dev* L = nullptr;
             for (const auto& l : m->layers) if (l.kind == QG_LAYER_ATTENTION) { L = &l; break; }
             if ((rc = make_geo(&P.geo[SG_ATTN_IN], QT_Q4K, false, L->n_in, H, pn.floats(H), grid, &sc)) ||
-                (rc = make_geo(&P.geo[SG_ATTN_OUT], QT_Q4K, false, H, m->q_dim, 0, grid, &sc)))
+                (rc = make_geo(&P.geo[SG_ATTN_OUT], QT_Q4K, false, H, m->q_dim, ProPlainG{}.floats(0), grid, &sc)))
                 return rc;
         }
         if ((rc = make_geo(&P.geo[SG_FFN_UP], QT_Q4K, true, c.ffn, H, pn.floats(H), grid, &sc)) ||
-            (rc = make_geo(&P.geo[SG_FFN_DOWN], QT_Q6K, false, H, c.ffn, 0, grid, &sc)) ||
+            (rc = make_geo(&P.geo[SG_FFN_DOWN], QT_Q6K, false, H, c.ffn, ProPlainG{}.floats(0), grid, &sc)) ||
             (rc = make_geo(&P.geo[SG_LMHEAD], QT_Q6K, false, c.vocab, H, pn.floats(H), grid, &sc)))
             return rc;
         P.ring_off = (sc + 127) & ~127;

@@ -113,25 +113,33 @@ def test_gemv_sweep_shapes(qtype, n, k):
 
 
 def test_q6k_planar_roundtrip_bytes():
-    t = synth.q6k_tensor(3, 13, 512)
+    """The planar (8-row grouped) Q6_K layout of qg.h, byte by byte: for group
+    g and super-block b a 1680-byte group-block [QL 8x128 | QH 8x64 | scales
+    8x16 | d 8x2]; padding rows are zero."""
+    n, nb = 13, 2
+    t = synth.q6k_tensor(3, n, 512)
     p = planar(t).cpu().numpy()
-    n8, nb = 16, 2
+    n8 = 16
     assert p.size == n8 * nb * 210
-    blocks = t.data.reshape(13 * nb, 210)
-    ql = p[:n8 * nb * 128].reshape(n8 * nb, 128)
-    qh = p[n8 * nb * 128:n8 * nb * 192].reshape(n8 * nb, 64)
-    sc = p[n8 * nb * 192:n8 * nb * 208].reshape(n8 * nb, 16)
-    dd = p[n8 * nb * 208:].reshape(n8 * nb, 2)
-    for i in range(13 * nb):
-        b = blocks[i]
-        for c in range(4):
-            half, part = c >> 1, c & 1
-            assert np.array_equal(ql[i, 32 * c:32 * c + 16], b[64 * half + 16 * part:64 * half + 16 * part + 16])
-            assert np.array_equal(ql[i, 32 * c + 16:32 * c + 32],
-                                  b[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
-        assert np.array_equal(qh[i], b[128:192]) and np.array_equal(sc[i], b[192:208])
-        assert np.array_equal(dd[i], b[208:210])
-    assert not np.any(ql[13 * nb:]) and not np.any(dd[13 * nb:])
+    blocks = t.data.reshape(n, nb, 210)
+    for g in range(n8 // 8):
+        for b in range(nb):
+            gb = p[(g * nb + b) * 1680:(g * nb + b + 1) * 1680]
+            for rr in range(8):
+                r = 8 * g + rr
+                ql, qh = gb[rr * 128:(rr + 1) * 128], gb[1024 + rr * 64:1024 + (rr + 1) * 64]
+                sc, dd = gb[1536 + rr * 16:1536 + (rr + 1) * 16], gb[1664 + rr * 2:1664 + (rr + 1) * 2]
+                if r >= n:
+                    assert not np.any(ql) and not np.any(qh) and not np.any(sc) and not np.any(dd)
+                    continue
+                blk = blocks[r, b]
+                for c in range(4):
+                    half, part = c >> 1, c & 1
+                    assert np.array_equal(ql[32 * c:32 * c + 16], blk[64 * half + 16 * part:64 * half + 16 * part + 16])
+                    assert np.array_equal(ql[32 * c + 16:32 * c + 32],
+                                          blk[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
+                assert np.array_equal(qh, blk[128:192]) and np.array_equal(sc, blk[192:208])
+                assert np.array_equal(dd, blk[208:210])
 
 
 # ------------------------------------------------------------------ argmax
