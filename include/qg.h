@@ -193,13 +193,16 @@ int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg
 
 /* Planar Q6_K (the layout the GEMV engine streams): n8 = n rounded up to 8
  * rows, nb = k/256.  For every 8-row group g and super-block b one 1680-byte
- * group-block at ((g*nb) + b)*1680 holding exactly the GGUF bytes of those 8
- * blocks: QL [8][128] (per row, for quarter-chunk c = 2*half + part (0..3),
- * the 16 low-4-bit bytes ql[64*half + 16*part ..] followed by
- * ql[64*half + 32 + 16*part ..]), QH [8][64] (as in GGUF), SC [8][16] int8
- * scales, D [8] fp16.  Rows n..n8-1 are zero.  qg_q6k_planar_bytes gives the
- * size (n8*nb*210); src is the raw GGUF tensor and both are device pointers,
- * 16-byte aligned. */
+ * group-block holding exactly the GGUF bytes of those 8 blocks: QL [8][128]
+ * (per row, for quarter-chunk c = 2*half + part (0..3), the 16 low-4-bit
+ * bytes ql[64*half + 16*part ..] followed by ql[64*half + 32 + 16*part ..]),
+ * QH [8][64] (as in GGUF), SC [8][16] int8 scales, D [8] fp16.  Group-blocks
+ * are stored slice-major: K splits into slices of 8 super-blocks, then of 4,
+ * 2 and 1 for the remainder (its binary digits, in that order); slice
+ * [b0, b0 + kb) takes (n8/8)*kb group-blocks from offset (n8/8)*b0*1680, with
+ * group-block (g, b) at ((n8/8)*b0 + g*kb + (b - b0))*1680.  Rows n..n8-1 are
+ * zero.  qg_q6k_planar_bytes gives the size (n8*nb*210); src is the raw GGUF
+ * tensor and both are device pointers, 16-byte aligned. */
 size_t qg_q6k_planar_bytes(int n, int k);
 int qg_q6k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream);
 

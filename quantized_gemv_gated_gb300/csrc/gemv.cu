@@ -72,8 +72,8 @@ static int lmhead_scratch(unsigned long long** out) {
 }
 
 // ------------------------------------------------- grouped weight layouts
-// One thread per (8-row group, super-block) of the padded matrix; rows n..n8-1
-// are zero.  Q6_K: [QL 8 x 128 | QH 8 x 64 | scales 8 x 16 | d 8 x 2] with each
+// One thread per (8-row group, super-block) of the padded matrix, stored at
+// its slice-major place (grouped_offset); rows n..n8-1 are zero.  Q6_K: [QL 8 x 128 | QH 8 x 64 | scales 8 x 16 | d 8 x 2] with each
 // row's QL reordered so that the two 16-byte halves of every 64-weight
 // quarter cq = 2 half + part are adjacent (ql[64 half + 16 part ..] then
 // ql[64 half + 32 + 16 part ..]).  Q4_K: the 8 rows' 144-byte blocks.
@@ -82,7 +82,7 @@ __global__ void q6k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __r
     const long long total = static_cast<long long>(n8 / 8) * nb;
     if (idx >= total) return;
     const long long g = idx / nb, b = idx - g * nb;
-    uint8_t* gb = dst + idx * 1680;
+    uint8_t* gb = dst + grouped_offset(n8, nb, static_cast<int>(g), static_cast<int>(b), 1680);
     for (int rr = 0; rr < 8; ++rr) {
         const long long r = 8 * g + rr;
         uint8_t* ql = gb + rr * 128;
@@ -116,7 +116,7 @@ __global__ void q4k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __r
     const long long total = static_cast<long long>(n8 / 8) * nb;
     if (idx >= total) return;
     const long long g = idx / nb, b = idx - g * nb;
-    uint4* gb = reinterpret_cast<uint4*>(dst + idx * 1152);
+    uint4* gb = reinterpret_cast<uint4*>(dst + grouped_offset(n8, nb, static_cast<int>(g), static_cast<int>(b), 1152));
     for (int rr = 0; rr < 8; ++rr) {
         const long long r = 8 * g + rr;
         for (int i = 0; i < 9; ++i)

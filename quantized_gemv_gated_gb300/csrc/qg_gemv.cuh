@@ -49,10 +49,13 @@ constexpr int kMaxSlices = 12;             // K <= 16384
 constexpr int QT_Q4K = 12;
 constexpr int QT_Q6K = 14;
 // Weight layouts.  RAW: GGUF Q4_K rows.  GROUPED: rows padded to a multiple
-// of 8; for every 8-row group g and super-block b one contiguous group-block
-// at ((g * nb) + b) * GB: Q4_K: the 8 rows' 144-byte blocks (GB = 1152);
-// Q6_K: [QL 8 x 128 | QH 8 x 64 | scales 8 x 16 | d 8 x 2] (GB = 1680), QL
-// with the two 16-byte halves of each 64-weight quarter adjacent.
+// of 8; for every 8-row group g and super-block b one group-block of GB
+// bytes: Q4_K: the 8 rows' 144-byte blocks (GB = 1152); Q6_K: [QL 8 x 128 |
+// QH 8 x 64 | scales 8 x 16 | d 8 x 2] (GB = 1680), QL with the two 16-byte
+// halves of each 64-weight quarter adjacent.  Group-blocks are stored
+// slice-major: the K slices (8 super-blocks each, then 4, 2, 1 for the rest)
+// one after the other, inside a slice group by group, so that any run of
+// consecutive groups of one slice is one contiguous piece.
 constexpr int LAYOUT_RAW = 0;
 constexpr int LAYOUT_GROUPED = 1;
 constexpr int kStageBlockRows = 64;        // super-block rows per stage
@@ -61,6 +64,34 @@ constexpr long long kAbortPollCycles = 100000;  // ~50 us between reads of the a
 __host__ __device__ constexpr int block_bytes(int qt) { return qt == QT_Q4K ? 144 : 210; }
 __host__ __device__ constexpr int group_block_bytes(int qt) { return 8 * block_bytes(qt); }
 __host__ __device__ constexpr int stage_bytes_of(int qt) { return kStageBlockRows * block_bytes(qt); }
+
+// The K slice holding super-block b: its first block b0 and its width kb.
+__host__ __device__ inline void block_slice(int nb, int b, int& b0, int& kb) {
+    const int full = nb / 8;
+    if (b < 8 * full) {
+        b0 = b & ~7;
+        kb = 8;
+        return;
+    }
+    int c = 8 * full;
+    for (int w = 4; w >= 1; w >>= 1)
+        if ((nb - 8 * full) & w) {
+            if (b < c + w) {
+                b0 = c;
+                kb = w;
+                return;
+            }
+            c += w;
+        }
+    b0 = c;
+    kb = 1;
+}
+// Byte offset of group-block (g, b) in the grouped layout of n8 rows.
+__host__ __device__ inline size_t grouped_offset(int n8, int nb, int g, int b, int GB) {
+    int b0, kb;
+    block_slice(nb, b, b0, kb);
+    return (static_cast<size_t>(n8 / 8) * b0 + static_cast<size_t>(g) * kb + (b - b0)) * GB;
+}
 
 // Geometry of one launch (identical on host and device).
 struct GemvShape {
@@ -71,6 +102,7 @@ struct GemvShape {
     int sl_c0[kMaxSlices];     // first chunk of each slice
     int sl_lg[kMaxSlices];     // log2(chunks) of each slice (lanes per row)
     int units;                 // ceil(n / 8)
+    int pp;                    // row passes per stage (a stage: pp * 64 super-block rows)
     int stages;                // ring depth
     int pro_floats;            // prologue scratch floats
     int rows_cta;              // most rows one CTA owns (row-result buffer)
@@ -429,7 +461,7 @@ __device__ bool gemv_produce(Pipe& p, const GemvShape& sh, const uint8_t* w0, co
     const int nb = sh.nb;
     bool first = true;
     for (int s = 0; s < sh.nsl; ++s) {
-        const int lg = sh.sl_lg[s], kb = (1 << lg) >> 2, U = 256 >> lg, b0 = sh.sl_c0[s] >> 2;
+        const int lg = sh.sl_lg[s], kb = (1 << lg) >> 2, U = (256 >> lg) * sh.pp, b0 = sh.sl_c0[s] >> 2;
         for (int row0 = r0; row0 < r1; row0 += U) {
             const int rows = min(U, r1 - row0);
 #pragma unroll
@@ -438,12 +470,12 @@ __device__ bool gemv_produce(Pipe& p, const GemvShape& sh, const uint8_t* w0, co
                 const uint8_t* w = m ? w1 : w0;
                 uint8_t* st = p.cur();
                 if constexpr (LAYOUT == LAYOUT_GROUPED) {
-                    const int g0 = row0 >> 3, ng = (rows + 7) >> 3;
-                    const unsigned piece = static_cast<unsigned>(kb) * GB;
-                    p.expect(ng * piece);
-                    if (p.lane < ng)
-                        p.copy(st + static_cast<size_t>(p.lane) * piece,
-                               w + (static_cast<size_t>(g0 + p.lane) * nb + b0) * GB, piece);
+                    // consecutive groups of one slice: one contiguous piece
+                    const unsigned bytes = static_cast<unsigned>((rows + 7) >> 3) * kb * GB;
+                    p.expect(bytes);
+                    if (p.lane == 0)
+                        p.copy(st, w + (static_cast<size_t>(sh.n8 / 8) * b0 + static_cast<size_t>(row0 >> 3) * kb) * GB,
+                               bytes);
                 } else {  // raw Q4_K rows
                     if (kb == nb) {
                         const unsigned bytes = static_cast<unsigned>(rows) * nb * 144u;
@@ -501,34 +533,37 @@ __device__ void gemv_consume(Pipe& p, const GemvShape& sh, int r0, int r1, Pro& 
         DigQ6 d6;
         if constexpr (QT == QT_Q4K) load_dig_q4(d4, 4 * b + q, dig, aux, k);
         else load_dig_q6(d6, b, q, dig, aux, k);
-        for (int row0 = r0; row0 < r1; row0 += U) {
-            const int row = row0 + rl;
-            const bool valid = row < r1;
+        for (int row0 = r0; row0 < r1; row0 += U * sh.pp) {
 #pragma unroll
             for (int m = 0; m < (DUAL ? 2 : 1); ++m) {
                 p.wait_full();
                 const uint8_t* st = p.cur();
-                float v = 0.0f;
-                if (valid) {
-                    if constexpr (QT == QT_Q4K) {
-                        const uint8_t* blk = LAYOUT == LAYOUT_GROUPED
-                                                 ? st + ((rl >> 3) * kb + bl) * GB + (rl & 7) * 144
-                                                 : st + (rl * kb + bl) * 144;
-                        v = dot_q4k(blk, q, d4);
-                    } else {
-                        const uint8_t* base = st + ((rl >> 3) * kb + bl) * GB;
-                        const int rr = rl & 7;
-                        v = dot_q6k(base + rr * 128 + 32 * q, base + 1024 + rr * 64 + 16 * q,
-                                    base + 1536 + rr * 16 + 8 * (q >> 1),
-                                    reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
+                for (int pass = 0; pass < sh.pp; ++pass) {
+                    const int sl = pass * U + rl;  // row within the stage
+                    const int row = row0 + sl;
+                    const bool valid = row < r1;
+                    float v = 0.0f;
+                    if (valid) {
+                        if constexpr (QT == QT_Q4K) {
+                            const uint8_t* blk = LAYOUT == LAYOUT_GROUPED
+                                                     ? st + ((sl >> 3) * kb + bl) * GB + (sl & 7) * 144
+                                                     : st + (sl * kb + bl) * 144;
+                            v = dot_q4k(blk, q, d4);
+                        } else {
+                            const uint8_t* base = st + ((sl >> 3) * kb + bl) * GB;
+                            const int rr = sl & 7;
+                            v = dot_q6k(base + rr * 128 + 32 * q, base + 1024 + rr * 64 + 16 * q,
+                                        base + 1536 + rr * 16 + 8 * (q >> 1),
+                                        reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
+                        }
+                    }
+                    for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+                    if (valid && j == 0) {
+                        float* y = m ? ys2 : ys;
+                        y[row - r0] = s ? y[row - r0] + v : v;
                     }
                 }
                 p.release();
-                for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-                if (valid && j == 0) {
-                    float* y = m ? ys2 : ys;
-                    y[row - r0] = s ? y[row - r0] + v : v;
-                }
             }
         }
         bar_sync(1, kConsumers);  // this slice's row sums are in before the next adds to them
@@ -557,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
     __syncthreads();
     // the kernel's error word doubles as its abort flag
     Pipe p{full, empty, smem + off_ring(QT, sh.k, sh.pro_floats, (DUAL ? 2 : 1) * sh.rows_cta), sh.stages,
-           stage_bytes_of(QT), 0u, sh.err, sh.err, lane, 0ull};
+           sh.pp * stage_bytes_of(QT), 0u, sh.err, sh.err, lane, 0ull};
     if (warp == kConsumerWarps) {
         p.pol = policy_evict_first();
         if (!gemv_produce<QT, LAYOUT, DUAL>(p, sh, sh.w0, sh.w1, r0, r1, &sh.next)) p.drain();

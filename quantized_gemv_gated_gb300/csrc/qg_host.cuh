@@ -22,12 +22,14 @@ int device_sms();
     } while (0)
 
 constexpr int kCtaSmemBytes = 110 * 1024;  // per CTA: two CTAs per SM fit in 228 KB
+constexpr int kStageTargetBytes = 27 * 1024;  // bulk copies of 13-27 KB stream at full rate
 
 // Geometry for n rows of k weights (dual: two matrices streamed together)
-// over at most max_ctas CTAs (0: two per SM).  K is cut into slices of 32
-// chunks, then the binary digits of the remainder (16, 8, 4 chunks).
+// over at most max_ctas CTAs (0: two per SM), stages of at most max_pp row
+// passes.  K is cut into slices of 32 chunks, then the binary digits of the
+// remainder (16, 8, 4 chunks).
 inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1, int n, int k, int pro_floats,
-                               int max_ctas, unsigned* err, int* grid_out) {
+                               int max_ctas, unsigned* err, int* grid_out, int max_pp = 0) {
     GemvShape sh{};
     sh.w0 = static_cast<const uint8_t*>(w0);
     sh.w1 = static_cast<const uint8_t*>(w1);
@@ -57,7 +59,12 @@ inline GemvShape gemv_geometry(int qt, bool dual, const void* w0, const void* w1
     if (grid < 1) grid = 1;
     sh.rows_cta = 8 * ((sh.units + grid - 1) / grid);
     const int fixed = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * sh.rows_cta);
-    int stages = (kCtaSmemBytes - fixed) / stage_bytes_of(qt);
+    int pp = kStageTargetBytes / stage_bytes_of(qt);
+    if (max_pp > 0 && pp > max_pp) pp = max_pp;
+    if (pp < 1) pp = 1;
+    while (pp > 1 && (kCtaSmemBytes - fixed) / (pp * stage_bytes_of(qt)) < 3) --pp;  // keep three stages in flight
+    sh.pp = pp;
+    int stages = (kCtaSmemBytes - fixed) / (pp * stage_bytes_of(qt));
     if (stages > kMaxStages) stages = kMaxStages;
     sh.stages = stages < 1 ? 1 : stages;
     *grid_out = grid;
@@ -69,7 +76,7 @@ inline bool gemv_k_served(int k) { return k > 0 && k % 256 == 0 && k <= 16384; }
 
 // Bytes of dynamic shared memory one GEMV launch needs.
 inline int gemv_smem(const GemvShape& sh, int qt, bool dual) {
-    return off_ring(qt, sh.k, sh.pro_floats, (dual ? 2 : 1) * sh.rows_cta) + sh.stages * stage_bytes_of(qt);
+    return off_ring(qt, sh.k, sh.pro_floats, (dual ? 2 : 1) * sh.rows_cta) + sh.stages * sh.pp * stage_bytes_of(qt);
 }
 
 // Launch one GEMV-engine kernel on `st` (with programmatic stream

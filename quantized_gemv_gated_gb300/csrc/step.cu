@@ -496,7 +496,7 @@ static_assert(stage_bytes_of(QT_Q6K) <= kSlotBytes && stage_bytes_of(QT_Q4K) <= 
 static int make_geo(GemvShape* g, int qt, bool dual, int n, int k, int pro_floats, int grid, int* scratch) {
     if (!gemv_k_served(k)) return set_err(QG_ERR_SHAPE, "step kernel: k=%d", k);
     int used = 0;
-    *g = gemv_geometry(qt, dual, nullptr, nullptr, n, k, pro_floats, grid, nullptr, &used);
+    *g = gemv_geometry(qt, dual, nullptr, nullptr, n, k, pro_floats, grid, nullptr, &used, 1);  // stage = one slot
     // every CTA of the step runs every phase: rows split over the whole grid
     g->rows_cta = 8 * ((g->units + grid - 1) / grid);
     const int need = off_ring(qt, k, pro_floats, (dual ? 2 : 1) * g->rows_cta);

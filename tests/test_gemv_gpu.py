@@ -112,19 +112,39 @@ def test_gemv_sweep_shapes(qtype, n, k):
     check_against_oracle(sub, x, y[rows])
 
 
-def test_q6k_planar_roundtrip_bytes():
-    """The planar (8-row grouped) Q6_K layout of qg.h, byte by byte: for group
-    g and super-block b a 1680-byte group-block [QL 8x128 | QH 8x64 | scales
-    8x16 | d 8x2]; padding rows are zero."""
-    n, nb = 13, 2
-    t = synth.q6k_tensor(3, n, 512)
+def _planar_slice(nb, b):
+    """(first block, width) of the K slice holding super-block b: slices of 8
+    blocks, then 4, 2 and 1 for the remainder (qg.h, planar Q6_K)."""
+    full = nb // 8
+    if b < 8 * full:
+        return b - b % 8, 8
+    c = 8 * full
+    for w in (4, 2, 1):
+        if (nb - 8 * full) & w:
+            if b < c + w:
+                return c, w
+            c += w
+    raise AssertionError(b)
+
+
+@pytest.mark.parametrize("n,k", [(13, 512), (13, 2560), (21, 3584)])
+def test_q6k_planar_roundtrip_bytes(n, k):
+    """The planar (8-row grouped, slice-major) Q6_K layout of qg.h, byte by
+    byte: 1680-byte group-blocks [QL 8x128 | QH 8x64 | scales 8x16 | d 8x2];
+    padding rows are zero."""
+    nb = k // 256
+    t = synth.q6k_tensor(3 + k, n, k)
     p = planar(t).cpu().numpy()
-    n8 = 16
+    n8 = (n + 7) // 8 * 8
     assert p.size == n8 * nb * 210
     blocks = t.data.reshape(n, nb, 210)
+    seen = set()
     for g in range(n8 // 8):
         for b in range(nb):
-            gb = p[(g * nb + b) * 1680:(g * nb + b + 1) * 1680]
+            b0, kb = _planar_slice(nb, b)
+            off = ((n8 // 8) * b0 + g * kb + (b - b0)) * 1680
+            seen.add(off)
+            gb = p[off:off + 1680]
             for rr in range(8):
                 r = 8 * g + rr
                 ql, qh = gb[rr * 128:(rr + 1) * 128], gb[1024 + rr * 64:1024 + (rr + 1) * 64]
@@ -140,6 +160,7 @@ def test_q6k_planar_roundtrip_bytes():
                                           blk[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
                 assert np.array_equal(qh, blk[128:192]) and np.array_equal(sc, blk[192:208])
                 assert np.array_equal(dd, blk[208:210])
+    assert len(seen) == (n8 // 8) * nb  # every group-block has its own place
 
 
 # ------------------------------------------------------------------ argmax
