@@ -434,6 +434,19 @@ static ProRmsNorm norm_pro(const float* h, const float* y, const float* w, const
     return pn;
 }
 
+// y = W x for the projections back to the hidden size (ssm_out, attn_output,
+// ffn_down): split-K over (slice, 8-row group) tasks when K has several
+// slices (the same floats as the one-CTA-per-row path), else the plain engine.
+template <int QT>
+static int out_gemv(qg_state* s, const uint8_t* w, int n, int k, const float* x, cudaStream_t st,
+                    const L2Prefetch& next) {
+    if (gemv_slices(k) > 1)
+        return launch_gemv_split<QT>(w, n, k, ProPlainG{x}, s->y, st, true, s->err, s->kpart, s->kcnt, next);
+    EpiStore ey{};
+    ey.y = s->y;
+    return launch_gemv<QT, false>(w, nullptr, n, k, ProPlainG{x}, ey, st, true, s->err, next);
+}
+
 static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
@@ -443,10 +456,7 @@ static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cud
                                        norm_pro(io.b, s->y, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
                                        s->err, prefetch_of(L.w_down, q6_bytes(c.hidden, c.ffn)));
     if (rc) return rc;
-    EpiStore ey{};
-    ey.y = s->y;
-    return launch_gemv<QT_Q6K, false>(L.w_down, nullptr, c.hidden, c.ffn, ProPlainG{s->act}, ey, st, true, s->err,
-                                      next_layer_prefetch(m, s, il));
+    return out_gemv<QT_Q6K>(s, L.w_down, c.hidden, c.ffn, s->act, st, next_layer_prefetch(m, s, il));
 }
 
 static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev& L, const ResidualIO& io) {
@@ -497,10 +507,8 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
         rc = launch_pdl(delta_kernel, dim3(c.n_v_heads), dim3(256), smem, st, true, da);
         if (rc) return rc;
     }
-    EpiStore ey{};
-    ey.y = s->y;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->v_dim, ProPlainG{s->o}, ey, st, true, s->err,
-                                    prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
+    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->v_dim, s->o, st,
+                          prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);
 }
@@ -558,10 +566,8 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
         default: return set_err(QG_ERR_SHAPE, "attention: %d query heads per kv head", c.n_heads / c.n_kv_heads);
     }
     if (rc) return rc;
-    EpiStore ey{};
-    ey.y = s->y;
-    rc = launch_gemv<QT_Q4K, false>(L.w_out, nullptr, c.hidden, m->q_dim, ProPlainG{s->attn}, ey, st, true, s->err,
-                                    prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
+    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, s->attn, st,
+                          prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);
 }

@@ -2,6 +2,7 @@
 // building blocks and the whole-token step replayed as one CUDA graph
 // (forward_qwen35_cuda.rs forward_single / forward_single_greedy; memra
 // decode.rs GraphSession: device token and position slots, 4-byte readback).
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -410,7 +411,13 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                (rc = dalloc(s->allocs, &s->attn_count, c.n_kv_heads + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->am_ws, 2, cnt)) || (rc = dalloc(s->allocs, &s->slots, 4, cnt)) ||
                (rc = dalloc(s->allocs, &s->hist, max_seq_len, cnt)) || (rc = dalloc(s->allocs, &s->err, 1, cnt)) ||
-               (rc = dalloc(s->allocs, &s->gbar, 4, cnt)));
+               (rc = dalloc(s->allocs, &s->gbar, 4, cnt)) ||
+               (rc = dalloc(s->allocs, &s->kpart,
+                            static_cast<size_t>(std::max({gemv_slices(c.ffn), gemv_slices(m->v_dim > 0 ? m->v_dim : 256),
+                                                          gemv_slices(m->q_dim > 0 ? m->q_dim : 256)})) *
+                                ((H + 7) & ~size_t(7)),
+                            cnt)) ||
+               (rc = dalloc(s->allocs, &s->kcnt, (H + 7) / 8, cnt)));
     }
     if (!rc) {
         void* p = nullptr;
@@ -477,6 +484,7 @@ int qg_state_reset(qg_state* s) {
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
     QG_CUDA(cudaMemset(s->err, 0, sizeof(unsigned)));
     QG_CUDA(cudaMemset(s->gbar, 0, 4 * sizeof(unsigned)));
+    QG_CUDA(cudaMemset(s->kcnt, 0, sizeof(unsigned) * ((c.hidden + 7) / 8)));
     QG_CUDA(cudaDeviceSynchronize());
     s->kv_len = 0;
     return QG_OK;

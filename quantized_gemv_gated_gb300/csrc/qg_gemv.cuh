@@ -106,6 +106,8 @@ struct GemvShape {
     int stages;                // ring depth
     int pro_floats;            // prologue scratch floats
     int rows_cta;              // most rows one CTA owns (row-result buffer)
+    float* part;               // split-K mode: slice sums [nsl][n8] (global scratch)
+    unsigned* cnt;             // split-K mode: per-group arrival counts [units] (left at 0)
     unsigned* err;
     L2Prefetch next;           // operands of the next kernel, pulled into L2 by the producer
 };
@@ -603,6 +605,153 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
     epi.pre(r0, r1, tid);  // inputs of the epilogue that no earlier kernel of this step writes
     pdl_wait();
     gemv_consume<QT, LAYOUT, DUAL>(p, sh, r0, r1, pro, epi, smem, tid);
+}
+
+// ------------------------------------------------------------ split-K mode
+// For GEMVs with few rows and several K slices (ffn_down, the output
+// projections) one CTA per row group would run its slices one after another.
+// Here the work is (slice, 8-row group) tasks, slice-major, spread evenly over
+// the CTAs; a CTA's consecutive tasks of one slice stream as contiguous
+// stages.  Each task writes its rows' slice sums to part[slice][row]; the last
+// task of a group to arrive adds them in slice order -- the order of the
+// one-CTA-per-row path, so both give the same floats -- and stores y.
+__device__ __forceinline__ void split_range(const GemvShape& sh, long long& t0, long long& t1) {
+    const long long T = static_cast<long long>(sh.units) * sh.nsl;
+    t0 = static_cast<long long>(blockIdx.x) * T / gridDim.x;
+    t1 = static_cast<long long>(blockIdx.x + 1) * T / gridDim.x;
+}
+
+template <int QT>
+__device__ bool gemv_split_produce(Pipe& p, const GemvShape& sh, const L2Prefetch* next) {
+    constexpr int GB = group_block_bytes(QT);
+    long long t0, t1;
+    split_range(sh, t0, t1);
+    bool first = true;
+    for (long long t = t0; t < t1;) {
+        const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
+        const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
+        const int lg = sh.sl_lg[s], kb = (1 << lg) >> 2, U = (256 >> lg) * sh.pp, b0 = sh.sl_c0[s] >> 2;
+        const int ra = 8 * g, rb = min(8 * ge, sh.n);
+        for (int row0 = ra; row0 < rb; row0 += U) {
+            const int rows = min(U, rb - row0);
+            if (!p.acquire()) return false;
+            const unsigned bytes = static_cast<unsigned>((rows + 7) >> 3) * kb * GB;
+            p.expect(bytes);
+            if (p.lane == 0)
+                p.copy(p.cur(), sh.w0 + (static_cast<size_t>(sh.n8 / 8) * b0 + static_cast<size_t>(row0 >> 3) * kb) * GB,
+                       bytes);
+            p.commit();
+            if (first && next && p.lane == 0) next->issue();
+            first = false;
+        }
+        t += ge - g;
+    }
+    if (first && next && p.lane == 0) next->issue();
+    return true;
+}
+
+template <int QT, class Pro>
+__device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, float* y, uint8_t* smem, int tid,
+                                   int* lastf) {
+    constexpr int GB = group_block_bytes(QT);
+    const int warp = tid >> 5, lane = tid & 31, k = sh.k;
+    uint8_t* dig = smem + off_dig();
+    uint8_t* aux = smem + off_aux(k);
+    float* psm = reinterpret_cast<float*>(smem + off_pro(QT, k));
+    pro.prepare(psm, k, tid);
+    bar_sync(1, kConsumers);
+    build_xrep<QT>(pro, psm, dig, aux, k, warp, lane);
+    bar_sync(1, kConsumers);
+    long long t0, t1;
+    split_range(sh, t0, t1);
+    for (long long t = t0; t < t1;) {
+        const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
+        const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
+        const int lg = sh.sl_lg[s], G = 1 << lg, rpw = 32 >> lg, kb = G >> 2, U = 8 * rpw;
+        const int ra = 8 * g, rb = min(8 * ge, sh.n);
+        const int j = lane & (G - 1), rl = warp * rpw + (lane >> lg);
+        int bl, q;
+        lane_chunk<QT>(j, lg, bl, q);
+        const int b = (sh.sl_c0[s] >> 2) + bl;
+        DigQ4 d4;
+        DigQ6 d6;
+        if constexpr (QT == QT_Q4K) load_dig_q4(d4, 4 * b + q, dig, aux, k);
+        else load_dig_q6(d6, b, q, dig, aux, k);
+        float* ps = sh.part + static_cast<size_t>(s) * sh.n8;
+        for (int row0 = ra; row0 < rb; row0 += U * sh.pp) {
+            p.wait_full();
+            const uint8_t* st = p.cur();
+            for (int pass = 0; pass < sh.pp; ++pass) {
+                const int sl = pass * U + rl;
+                const int row = row0 + sl;
+                const bool valid = row < rb;
+                float v = 0.0f;
+                if (valid) {
+                    if constexpr (QT == QT_Q4K) {
+                        v = dot_q4k(st + ((sl >> 3) * kb + bl) * GB + (sl & 7) * 144, q, d4);
+                    } else {
+                        const uint8_t* base = st + ((sl >> 3) * kb + bl) * GB;
+                        const int rr = sl & 7;
+                        v = dot_q6k(base + rr * 128 + 32 * q, base + 1024 + rr * 64 + 16 * q,
+                                    base + 1536 + rr * 16 + 8 * (q >> 1),
+                                    reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
+                    }
+                }
+                for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+                if (valid && j == 0) ps[row] = v;
+            }
+            p.release();
+        }
+        // this run's groups are done for slice s: count them; the last task of
+        // a group adds its slice sums in slice order
+        __threadfence();
+        bar_sync(1, kConsumers);
+        for (int c0 = g; c0 < ge; c0 += 32) {
+            const int nc = min(32, ge - c0);
+            if (tid < nc) lastf[tid] = atomicAdd(sh.cnt + c0 + tid, 1u) == static_cast<unsigned>(sh.nsl - 1);
+            bar_sync(1, kConsumers);
+            for (int e = tid; e < 8 * nc; e += kConsumers) {
+                const int row = 8 * (c0 + (e >> 3)) + (e & 7);
+                if (lastf[e >> 3] && row < sh.n) {
+                    __threadfence();
+                    float v = __ldcg(sh.part + row);
+                    for (int s2 = 1; s2 < sh.nsl; ++s2) v += __ldcg(sh.part + static_cast<size_t>(s2) * sh.n8 + row);
+                    y[row] = v;
+                }
+            }
+            bar_sync(1, kConsumers);
+            if (tid < nc && lastf[tid]) sh.cnt[c0 + tid] = 0u;
+        }
+        t += ge - g;
+    }
+}
+
+template <int QT, class Pro>
+__global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape sh, const Pro pro_in, float* y) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int lastf[32];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < sh.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Pipe p{full, empty, smem + off_ring(QT, sh.k, sh.pro_floats, 0), sh.stages, sh.pp * stage_bytes_of(QT), 0u,
+           sh.err, sh.err, lane, 0ull};
+    if (warp == kConsumerWarps) {
+        p.pol = policy_evict_first();
+        if (!gemv_split_produce<QT>(p, sh, &sh.next)) p.drain();
+        return;
+    }
+    Pro pro = pro_in;
+    pdl_wait();
+    gemv_split_consume<QT>(p, sh, pro, y, smem, tid, lastf);
 }
 
 // ------------------------------------------------------------- prologues

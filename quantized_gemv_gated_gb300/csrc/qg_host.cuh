@@ -115,6 +115,53 @@ int launch_gemv(const void* w0, const void* w1, int n, int k, const Pro& pro, co
     return QG_OK;
 }
 
+// Number of K slices of a k-wide GEMV (32-chunk slices, then 16, 8, 4).
+inline int gemv_slices(int k) {
+    const int cr = k / 64;
+    return cr / 32 + ((cr >> 4) & 1) + ((cr >> 3) & 1) + ((cr >> 2) & 1);
+}
+
+// Split-K launch (gemv_split_kernel): y = W x with EpiStore semantics, for a
+// weight matrix in the grouped layout; part: nsl * n8 floats, cnt: units
+// unsigned, both device scratch, cnt all zero (left zero).
+template <int QT, class Pro>
+int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, float* y, cudaStream_t st, bool pdl, unsigned* err,
+                      float* part, unsigned* cnt, const L2Prefetch& next = L2Prefetch{}) {
+    if (!err || !part || !cnt) return set_err(QG_ERR_CUDA, "gemv_split: missing scratch");
+    int grid = 1;
+    GemvShape sh = gemv_geometry(QT, false, w0, nullptr, n, k, pro.floats(k), 0, err, &grid);
+    const long long tasks = static_cast<long long>(sh.units) * sh.nsl;
+    grid = static_cast<int>(tasks < 2LL * device_sms() ? tasks : 2LL * device_sms());
+    sh.rows_cta = 0;
+    const int fixed = off_ring(QT, k, sh.pro_floats, 0);
+    int stages = (kCtaSmemBytes - fixed) / (sh.pp * stage_bytes_of(QT));
+    sh.stages = stages < 1 ? 1 : (stages > kMaxStages ? kMaxStages : stages);
+    sh.part = part;
+    sh.cnt = cnt;
+    sh.next = next;
+    const int smem = fixed + sh.stages * sh.pp * stage_bytes_of(QT);
+    auto kern = gemv_split_kernel<QT, Pro>;
+    static int configured = 0;
+    if (smem > configured) {
+        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     static_cast<int>(cudaSharedmemCarveoutMaxShared)));
+        configured = smem;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    QG_CUDA(cudaLaunchKernelEx(&cfg, kern, sh, pro, y));
+    return QG_OK;
+}
+
 // Plain launch of a non-engine kernel with the PDL attribute.
 template <class... KArgs, class... Args>
 int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

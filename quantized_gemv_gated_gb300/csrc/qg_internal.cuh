@@ -52,6 +52,8 @@ struct qg_state {
     float *h, *hres, *y, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *attn;
     float *part_acc, *part_ml;
     unsigned* attn_count;       // [n_kv_heads] split arrivals (left at 0)
+    float* kpart;               // split-K GEMV slice sums [max slices][hidden8]
+    unsigned* kcnt;             // split-K GEMV group arrivals [hidden/8] (left at 0)
     unsigned long long* am_ws;  // lm_head argmax workspace (left at 0)
     int* slots;                 // device: [0] token in, [1] position, [2] token out (bit 31: device error)
     uint32_t* hist;             // device: greedy token per position [max_seq]
