@@ -28,36 +28,37 @@
 namespace qg {
 
 // ------------------------------------------------------------ delta rule
-// One CTA per value head h (gdn_delta_rule_into + gdn_gated_rmsnorm_into),
-// head_k_dim = 128 (4 per lane), dv/8 rows per warp.  The head's state tile
-// (dv rows of 128, s[j*128 + i] == S[i][j]) arrives in shared memory with one
-// bulk copy issued before the dependency wait; rows are processed four at a
-// time so that their warp reductions overlap; the gated RMSNorm of the head
-// (a sum of o^2 over its dv rows) is reduced inside the CTA in warp order and
-// the kernel writes u = rmsnorm(o_h) * w * silu(z_h), the ssm_out input.
+// gdn_delta_rule_into over items of 32 state rows of one value head (four
+// rows per warp, head_k_dim = 128: 4 per lane): the item's 16 KB of state
+// arrives in shared memory with one bulk copy issued before the dependency
+// wait; each warp runs decay, read, rank-1 update and query on its rows
+// (delta_rows4), writes them back and stores the rows' o (before the gated
+// RMSNorm, which needs the whole head and is applied by the ssm_out GEMV's
+// prologue, ProGatedNorm).
 struct DeltaArgs {
     const float* conv_out;  // [q | k | v] after conv + SiLU
     const float* dt;        // log-decay per value head
     const float* beta;
     float* S;               // [nv][dv][128]
-    const float* z;         // gate [v_dim]
-    const float* w_norm;    // [dv]
-    float* u;               // [v_dim]
+    float* o;               // [v_dim]
     unsigned* err;
     L2Prefetch next;
     int nk, dv, kdim;
     float eps;
 };
 
+constexpr int kDeltaRows = 32;  // state rows per CTA (one item)
+
 __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
-    extern __shared__ __align__(16) float st[];  // [dv][128]
+    __shared__ __align__(128) float st[kDeltaRows * kDk];
     __shared__ __align__(16) float qs[kDk];
     __shared__ __align__(16) float ks[kDk];
-    __shared__ float wss[8];
     __shared__ __align__(8) uint64_t bar;
-    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per_head = a.dv / kDeltaRows;
+    const int h = blockIdx.x / per_head, jb = (blockIdx.x - h * per_head) * kDeltaRows;
     const int kh = h % a.nk;  // value head h reads key head h % nk (check_head_grouping)
-    const int rpw = a.dv / 8, j0 = warp * rpw;
+    const int j = jb + 4 * warp;  // this warp's first row
     pdl_launch_dependents();
     if (tid == 0) {
         mbar_init(&bar, 1);
@@ -65,15 +66,14 @@ __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
     }
     __syncthreads();
     if (tid == 0) {  // the state does not depend on the previous kernel
-        const unsigned bytes = static_cast<unsigned>(a.dv) * kDk * 4u;
+        const unsigned bytes = kDeltaRows * kDk * 4u;
         mbar_arrive_expect_tx(&bar, bytes);
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(st)),
-            "l"(a.S + static_cast<size_t>(h) * a.dv * kDk), "r"(bytes), "r"(smem_u32(&bar))
+            "l"(a.S + (static_cast<size_t>(h) * a.dv + jb) * kDk), "r"(bytes), "r"(smem_u32(&bar))
             : "memory");
         a.next.issue();
     }
-    float wn = lane < rpw ? __ldg(a.w_norm + j0 + lane) : 0.0f;
     pdl_wait();
     if (warp < 2) {  // per-head L2 norm of q (warp 0) and k (warp 1) (gdn_per_head_l2_norm_into)
         const float4 v = ldcg4(a.conv_out + (warp ? a.kdim : 0) + kh * kDk + 4 * lane);
@@ -86,9 +86,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
         float* dst = warp ? ks : qs;
         *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(v.x * r, v.y * r, v.z * r, v.w * r);
     }
-    // lane i < rpw holds v and z of row j0 + i
-    const float vl = lane < rpw ? __ldcg(a.conv_out + 2 * a.kdim + h * a.dv + j0 + lane) : 0.0f;
-    const float zl = lane < rpw ? __ldcg(a.z + h * a.dv + j0 + lane) : 0.0f;
+    const float vl = lane < 4 ? __ldcg(a.conv_out + 2 * a.kdim + h * a.dv + j + lane) : 0.0f;
     const float g = expf(__ldcg(a.dt + h)), be = __ldcg(a.beta + h);
     __syncthreads();
     if (!mbar_wait(&bar, 0)) {
@@ -98,35 +96,24 @@ __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
     }
     const float4 kk = *reinterpret_cast<const float4*>(ks + 4 * lane);
     const float4 qq = *reinterpret_cast<const float4*>(qs + 4 * lane);
-    float o[kMaxRowsPerWarp];
-#pragma unroll
-    for (int i0 = 0; i0 < kMaxRowsPerWarp; i0 += 4) {
-        if (i0 >= rpw) break;
-        delta_rows4(st + (j0 + i0) * kDk, a.S + (static_cast<size_t>(h) * a.dv + j0 + i0) * kDk, kk, qq, vl, i0, g, be,
-                    lane, o + i0);
-    }
-    // gated RMSNorm over the head's dv rows (warp partials in order)
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i)
-        if (i < rpw) ss = fmaf(o[i], o[i], ss);
-    if (lane == 0) wss[warp] = ss;
-    __syncthreads();
-    float tot = 0.0f;
-    for (int w = 0; w < 8; ++w) tot += wss[w];
-    const float rn = 1.0f / sqrtf(tot / static_cast<float>(a.dv) + a.eps);
+    float o[4];
+    delta_rows4(st + 4 * warp * kDk, a.S + (static_cast<size_t>(h) * a.dv + j) * kDk, kk, qq, vl, 0, g, be, lane, o);
     float mine = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i)
-        if (lane == i) mine = o[i];
-    if (lane < rpw) a.u[h * a.dv + j0 + lane] = ((mine * rn) * wn) * silu(zl);
+    for (int t = 0; t < 4; ++t)
+        if (lane == t) mine = o[t];
+    if (lane < 4) a.o[h * a.dv + j + lane] = mine;
 }
 
-__global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y, int n) {
+// h += y, y given as `parts` vectors `stride` floats apart added in order.
+__global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y, int parts, int stride, int n) {
     pdl_launch_dependents();
     pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) h[i] = __ldcg(h + i) + __ldcg(y + i);
+    if (i >= n) return;
+    float v = __ldcg(y + i);
+    for (int p = 1; p < parts; ++p) v += __ldcg(y + static_cast<size_t>(p) * stride + i);
+    h[i] = __ldcg(h + i) + v;
 }
 
 struct AttnArgs {
@@ -421,11 +408,13 @@ static L2Prefetch next_layer_prefetch(const qg_model* m, const qg_state* s, int 
 // Residual stream: a layer maps (A, pending y) -> (A, pending y') with B as
 // the temporary: its first kernel stores A + y (or the embedding row) to B,
 // its ffn_up stores B + y_mixer to A; the output GEMVs only store y.
-static ProRmsNorm norm_pro(const float* h, const float* y, const float* w, const int* tok, float* h_out, float eps,
-                           int k) {
+static ProRmsNorm norm_pro(const float* h, const qg_state* s, bool with_y, const float* w, const int* tok,
+                           float* h_out, float eps, int k) {
     ProRmsNorm pn{};
     pn.h = h;
-    pn.y = y;
+    pn.y = with_y ? s->ycur : nullptr;
+    pn.y_parts = s->ycur_parts;
+    pn.y_stride = s->ycur_stride;
     pn.w = w;
     pn.tok = tok;
     pn.h_out = h_out;
@@ -437,14 +426,21 @@ static ProRmsNorm norm_pro(const float* h, const float* y, const float* w, const
 // y = W x for the projections back to the hidden size (ssm_out, attn_output,
 // ffn_down): split-K over (slice, 8-row group) tasks when K has several
 // slices (the same floats as the one-CTA-per-row path), else the plain engine.
-template <int QT>
-static int out_gemv(qg_state* s, const uint8_t* w, int n, int k, const float* x, cudaStream_t st,
+template <int QT, class Pro>
+static int out_gemv(qg_state* s, const uint8_t* w, int n, int k, const Pro& pro, cudaStream_t st,
                     const L2Prefetch& next) {
-    if (gemv_slices(k) > 1)
-        return launch_gemv_split<QT>(w, n, k, ProPlainG{x}, s->y, st, true, s->err, s->kpart, s->kcnt, next);
+    if (gemv_slices(k) > 1) {
+        s->ycur = s->kpart;
+        s->ycur_parts = gemv_slices(k);
+        s->ycur_stride = (n + 7) & ~7;
+        return launch_gemv_split<QT>(w, n, k, pro, st, true, s->err, s->kpart, next);
+    }
+    s->ycur = s->y;
+    s->ycur_parts = 1;
+    s->ycur_stride = 0;
     EpiStore ey{};
     ey.y = s->y;
-    return launch_gemv<QT, false>(w, nullptr, n, k, ProPlainG{x}, ey, st, true, s->err, next);
+    return launch_gemv<QT, false>(w, nullptr, n, k, pro, ey, st, true, s->err, next);
 }
 
 static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st) {
@@ -453,15 +449,15 @@ static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cud
     EpiSwiGlu sw{};
     sw.act = s->act;
     int rc = launch_gemv<QT_Q4K, true>(L.w_gate, L.w_up, c.ffn, c.hidden,
-                                       norm_pro(io.b, s->y, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
+                                       norm_pro(io.b, s, true, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
                                        s->err, prefetch_of(L.w_down, q6_bytes(c.hidden, c.ffn)));
     if (rc) return rc;
-    return out_gemv<QT_Q6K>(s, L.w_down, c.hidden, c.ffn, s->act, st, next_layer_prefetch(m, s, il));
+    return out_gemv<QT_Q6K>(s, L.w_down, c.hidden, c.ffn, ProPlainG{s->act}, st, next_layer_prefetch(m, s, il));
 }
 
 static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev& L, const ResidualIO& io) {
-    if (io.embed) return norm_pro(m->embd, nullptr, L.attn_norm, s->slots, io.b, m->cfg.eps, m->cfg.hidden);
-    return norm_pro(io.a, io.y_pending ? s->y : nullptr, L.attn_norm, nullptr, io.b, m->cfg.eps, m->cfg.hidden);
+    if (io.embed) return norm_pro(m->embd, s, false, L.attn_norm, s->slots, io.b, m->cfg.eps, m->cfg.hidden);
+    return norm_pro(io.a, s, io.y_pending, L.attn_norm, nullptr, io.b, m->cfg.eps, m->cfg.hidden);
 }
 
 int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first) {
@@ -489,25 +485,24 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
         da.dt = s->dt;
         da.beta = s->beta;
         da.S = s->ssm[il];
-        da.z = s->z;
-        da.w_norm = L.ssm_norm;
-        da.u = s->o;
+        da.o = s->o;
         da.err = s->err;
         da.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->v_dim));
         da.nk = c.n_k_heads;
         da.dv = c.head_v_dim;
         da.kdim = m->k_dim;
         da.eps = c.eps;
-        const int smem = c.head_v_dim * kDk * 4;
-        static int configured = 0;
-        if (smem > configured) {
-            QG_CUDA(cudaFuncSetAttribute(delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-            configured = smem;
-        }
-        rc = launch_pdl(delta_kernel, dim3(c.n_v_heads), dim3(256), smem, st, true, da);
+        rc = launch_pdl(delta_kernel, dim3(c.n_v_heads * (c.head_v_dim / kDeltaRows)), dim3(256), 0, st, true, da);
         if (rc) return rc;
     }
-    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->v_dim, s->o, st,
+    ProGatedNorm gn{};
+    gn.o = s->o;
+    gn.z = s->z;
+    gn.w = L.ssm_norm;
+    gn.nv = c.n_v_heads;
+    gn.dv = c.head_v_dim;
+    gn.eps = c.eps;
+    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->v_dim, gn, st,
                           prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);
@@ -566,14 +561,15 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
         default: return set_err(QG_ERR_SHAPE, "attention: %d query heads per kv head", c.n_heads / c.n_kv_heads);
     }
     if (rc) return rc;
-    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, s->attn, st,
+    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, ProPlainG{s->attn}, st,
                           prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
     if (rc) return rc;
     return ffn(m, s, il, io, st);
 }
 
-int run_residual(float* h, const float* y, int n, cudaStream_t st) {
-    return launch_pdl(residual_add_kernel, dim3((n + 255) / 256), dim3(256), 0, st, true, h, y, n);
+int run_residual(qg_state* s, float* h, int n, cudaStream_t st) {
+    return launch_pdl(residual_add_kernel, dim3((n + 255) / 256), dim3(256), 0, st, true, h, s->ycur, s->ycur_parts,
+                      s->ycur_stride, n);
 }
 
 int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance) {
@@ -585,7 +581,7 @@ int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, c
     ea.err = s->err;
     ea.advance = advance ? 1 : 0;
     return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden,
-                                      norm_pro(a, s->y, m->out_norm, nullptr, h_final, c.eps, c.hidden), ea, st, true,
+                                      norm_pro(a, s, true, m->out_norm, nullptr, h_final, c.eps, c.hidden), ea, st, true,
                                       s->err);
 }
 

@@ -132,6 +132,7 @@ int check_config(const qg_config* c) {
         if (c->head_v_dim > 128)
             return set_err(QG_ERR_SHAPE, "config: head_v_dim %d (served: up to 128)", c->head_v_dim);
         if (c->head_v_dim % 32) return set_err(QG_ERR_SHAPE, "config: head_v_dim %d is not a multiple of 32", c->head_v_dim);
+        if (c->n_v_heads > 64) return set_err(QG_ERR_SHAPE, "config: %d value heads (served: up to 64)", c->n_v_heads);
     }
     if (has_attn) {
         if (c->head_dim != 256) return set_err(QG_ERR_SHAPE, "config: head_dim %d (served: 256)", c->head_dim);
@@ -417,7 +418,7 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                                                           gemv_slices(m->q_dim > 0 ? m->q_dim : 256)})) *
                                 ((H + 7) & ~size_t(7)),
                             cnt)) ||
-               (rc = dalloc(s->allocs, &s->kcnt, (H + 7) / 8, cnt)));
+               (rc = (s->ycur = s->y, s->ycur_parts = 1, s->ycur_stride = 0, QG_OK)));
     }
     if (!rc) {
         void* p = nullptr;
@@ -484,7 +485,6 @@ int qg_state_reset(qg_state* s) {
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
     QG_CUDA(cudaMemset(s->err, 0, sizeof(unsigned)));
     QG_CUDA(cudaMemset(s->gbar, 0, 4 * sizeof(unsigned)));
-    QG_CUDA(cudaMemset(s->kcnt, 0, sizeof(unsigned) * ((c.hidden + 7) / 8)));
     QG_CUDA(cudaDeviceSynchronize());
     s->kv_len = 0;
     return QG_OK;
@@ -609,7 +609,7 @@ int qg_deltanet_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, 
     const ResidualIO io{hidden_dev, s->h, false, false};
     int rc = run_deltanet_layer(m, s, il, io, st, true);
     if (rc) return rc;
-    return run_residual(hidden_dev, s->y, m->cfg.hidden, st);
+    return run_residual(s, hidden_dev, m->cfg.hidden, st);
 }
 
 int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_dev, int pos, qg_stream stream) {
@@ -626,7 +626,7 @@ int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_de
     QG_CUDA(cudaMemcpyAsync(s->slots + 1, &p, sizeof(int), cudaMemcpyHostToDevice, st));
     const ResidualIO io{hidden_dev, s->h, false, false};
     int rc = run_attention_layer(m, s, il, io, st, false);
-    if (!rc) rc = run_residual(hidden_dev, s->y, m->cfg.hidden, st);
+    if (!rc) rc = run_residual(s, hidden_dev, m->cfg.hidden, st);
     if (rc) return rc;
     if (s->kv_len < pos + 1) s->kv_len = pos + 1;
     return QG_OK;

@@ -107,7 +107,6 @@ struct GemvShape {
     int pro_floats;            // prologue scratch floats
     int rows_cta;              // most rows one CTA owns (row-result buffer)
     float* part;               // split-K mode: slice sums [nsl][n8] (global scratch)
-    unsigned* cnt;             // split-K mode: per-group arrival counts [units] (left at 0)
     unsigned* err;
     L2Prefetch next;           // operands of the next kernel, pulled into L2 by the producer
 };
@@ -502,7 +501,9 @@ __device__ bool gemv_produce(Pipe& p, const GemvShape& sh, const uint8_t* w0, co
 }
 
 // --------------------------------------------------------------- consumer
-// Pro: prepare(float* sm, int k, int tid) fills its scratch (consumers only),
+// Pro: pre(float* sm, int k, int tid) before the dependency wait (inputs no
+//      earlier kernel of the step writes; called by the kernel),
+//      prepare(float* sm, int k, int tid) fills the rest of its scratch,
 //      value8(const float* sm, int i0, float* v) gives x_i0 .. x_i0+7 (i0 % 8 == 0).
 // Epi: pre(r0, r1, tid) before the dependency wait (loads of data no kernel of
 //      the current step writes; called by the kernel), start() after the
@@ -602,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
     }
     Pro pro = pro_in;
     Epi epi = epi_in;
-    epi.pre(r0, r1, tid);  // inputs of the epilogue that no earlier kernel of this step writes
+    epi.pre(r0, r1, tid);  // inputs that no earlier kernel of this step writes
+    pro.pre(reinterpret_cast<float*>(smem + off_pro(QT, sh.k)), sh.k, tid);
     pdl_wait();
     gemv_consume<QT, LAYOUT, DUAL>(p, sh, r0, r1, pro, epi, smem, tid);
 }
@@ -612,9 +614,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
 // projections) one CTA per row group would run its slices one after another.
 // Here the work is (slice, 8-row group) tasks, slice-major, spread evenly over
 // the CTAs; a CTA's consecutive tasks of one slice stream as contiguous
-// stages.  Each task writes its rows' slice sums to part[slice][row]; the last
-// task of a group to arrive adds them in slice order -- the order of the
-// one-CTA-per-row path, so both give the same floats -- and stores y.
+// stages.  Each task writes its rows' slice sums to part[slice][row]; the
+// consumer of y (the next RMSNorm prologue, or the residual add) adds the
+// slices in slice order -- the order of the one-CTA-per-row path, so both give
+// the same floats -- which saves this kernel an arrival count and a second
+// pass over the sums.
 __device__ __forceinline__ void split_range(const GemvShape& sh, long long& t0, long long& t1) {
     const long long T = static_cast<long long>(sh.units) * sh.nsl;
     t0 = static_cast<long long>(blockIdx.x) * T / gridDim.x;
@@ -651,8 +655,7 @@ __device__ bool gemv_split_produce(Pipe& p, const GemvShape& sh, const L2Prefetc
 }
 
 template <int QT, class Pro>
-__device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, float* y, uint8_t* smem, int tid,
-                                   int* lastf) {
+__device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8_t* smem, int tid) {
     constexpr int GB = group_block_bytes(QT);
     const int warp = tid >> 5, lane = tid & 31, k = sh.k;
     uint8_t* dig = smem + off_dig();
@@ -702,34 +705,13 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, float
             }
             p.release();
         }
-        // this run's groups are done for slice s: count them; the last task of
-        // a group adds its slice sums in slice order
-        __threadfence();
-        bar_sync(1, kConsumers);
-        for (int c0 = g; c0 < ge; c0 += 32) {
-            const int nc = min(32, ge - c0);
-            if (tid < nc) lastf[tid] = atomicAdd(sh.cnt + c0 + tid, 1u) == static_cast<unsigned>(sh.nsl - 1);
-            bar_sync(1, kConsumers);
-            for (int e = tid; e < 8 * nc; e += kConsumers) {
-                const int row = 8 * (c0 + (e >> 3)) + (e & 7);
-                if (lastf[e >> 3] && row < sh.n) {
-                    __threadfence();
-                    float v = __ldcg(sh.part + row);
-                    for (int s2 = 1; s2 < sh.nsl; ++s2) v += __ldcg(sh.part + static_cast<size_t>(s2) * sh.n8 + row);
-                    y[row] = v;
-                }
-            }
-            bar_sync(1, kConsumers);
-            if (tid < nc && lastf[tid]) sh.cnt[c0 + tid] = 0u;
-        }
         t += ge - g;
     }
 }
 
 template <int QT, class Pro>
-__global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape sh, const Pro pro_in, float* y) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape sh, const Pro pro_in) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int lastf[32];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -750,8 +732,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape
         return;
     }
     Pro pro = pro_in;
+    pro.pre(reinterpret_cast<float*>(smem + off_pro(QT, sh.k)), sh.k, tid);
     pdl_wait();
-    gemv_split_consume<QT>(p, sh, pro, y, smem, tid, lastf);
+    gemv_split_consume<QT>(p, sh, pro, smem, tid);
 }
 
 // ------------------------------------------------------------- prologues
@@ -761,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape
 struct ProPlainG {
     const float* x;
     __host__ __device__ int floats(int) const { return 16; }
+    __device__ void pre(float*, int, int) {}
     __device__ void prepare(float*, int, int) {}
     __device__ void value8(const float*, int i0, float* v) const {
         const float4 a = ldcg4(x + i0), b = ldcg4(x + i0 + 4);
@@ -770,20 +754,29 @@ struct ProPlainG {
 };
 
 // x = RMSNorm(h + y) * w (residual_add_into then rmsnorm_into): the residual
-// add of the previous GEMV is done here, by every CTA on its own copy, and
+// add of the previous GEMV is done here (y given as the previous GEMV's
+// slice sums when it ran split-K: summed first, in slice order), by every
+// CTA on its own copy, and
 // CTA 0 stores h + y to h_out (the residual stream, double-buffered so that
 // no CTA of this kernel reads what CTA 0 writes).  y may be null.  With
 // `tok` set, h is row *tok of the embedding table (the step's first layer).
 struct ProRmsNorm {
     const float* h;
-    const float* y;
+    const float* y;    // y_parts vectors y_stride floats apart, added in order (split-K slice sums)
     const float* w;
     const int* tok;
     float* h_out;
     float eps;
     int kdim;  // = k
+    int y_parts, y_stride;
     float r;
     __host__ __device__ int floats(int k) const { return 2 * k + 32; }
+    // the norm weights do not depend on the previous kernel: staged before its wait
+    __device__ void pre(float* sm, int k, int tid) {
+#pragma unroll 4
+        for (int i = 4 * tid; i < k; i += 4 * kConsumers)
+            *reinterpret_cast<float4*>(sm + k + i) = __ldg(reinterpret_cast<const float4*>(w + i));
+    }
     __device__ void prepare(float* sm, int k, int tid) {
         const float* src = h;
         if (tok) src = h + static_cast<size_t>(__ldcg(tok)) * k;
@@ -792,15 +785,20 @@ struct ProRmsNorm {
         for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
             float4 v = ldcg4(src + i);
             if (y) {
-                const float4 a = ldcg4(y + i);
+                float4 a = ldcg4(y + i);
+                for (int p = 1; p < y_parts; ++p) {
+                    const float4 b = ldcg4(y + static_cast<size_t>(p) * y_stride + i);
+                    a.x += b.x;
+                    a.y += b.y;
+                    a.z += b.z;
+                    a.w += b.w;
+                }
                 v.x += a.x;
                 v.y += a.y;
                 v.z += a.z;
                 v.w += a.w;
             }
-            const float4 ww = __ldg(reinterpret_cast<const float4*>(w + i));
             *reinterpret_cast<float4*>(sm + i) = v;
-            *reinterpret_cast<float4*>(sm + k + i) = ww;
             if (h_out && blockIdx.x == 0) *reinterpret_cast<float4*>(h_out + i) = v;
             ss = fmaf(v.x, v.x, ss);
             ss = fmaf(v.y, v.y, ss);

@@ -121,13 +121,13 @@ inline int gemv_slices(int k) {
     return cr / 32 + ((cr >> 4) & 1) + ((cr >> 3) & 1) + ((cr >> 2) & 1);
 }
 
-// Split-K launch (gemv_split_kernel): y = W x with EpiStore semantics, for a
-// weight matrix in the grouped layout; part: nsl * n8 floats, cnt: units
-// unsigned, both device scratch, cnt all zero (left zero).
+// Split-K launch (gemv_split_kernel): the slice sums of y = W x go to
+// part[slice][row] (nsl * n8 floats of device scratch); the reader of y adds
+// them in slice order.  W in the grouped layout.
 template <int QT, class Pro>
-int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, float* y, cudaStream_t st, bool pdl, unsigned* err,
-                      float* part, unsigned* cnt, const L2Prefetch& next = L2Prefetch{}) {
-    if (!err || !part || !cnt) return set_err(QG_ERR_CUDA, "gemv_split: missing scratch");
+int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, cudaStream_t st, bool pdl, unsigned* err,
+                      float* part, const L2Prefetch& next = L2Prefetch{}) {
+    if (!err || !part) return set_err(QG_ERR_CUDA, "gemv_split: missing scratch");
     int grid = 1;
     GemvShape sh = gemv_geometry(QT, false, w0, nullptr, n, k, pro.floats(k), 0, err, &grid);
     const long long tasks = static_cast<long long>(sh.units) * sh.nsl;
@@ -137,7 +137,6 @@ int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, float* y, cu
     int stages = (kCtaSmemBytes - fixed) / (sh.pp * stage_bytes_of(QT));
     sh.stages = stages < 1 ? 1 : (stages > kMaxStages ? kMaxStages : stages);
     sh.part = part;
-    sh.cnt = cnt;
     sh.next = next;
     const int smem = fixed + sh.stages * sh.pp * stage_bytes_of(QT);
     auto kern = gemv_split_kernel<QT, Pro>;
@@ -158,7 +157,7 @@ int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, float* y, cu
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    QG_CUDA(cudaLaunchKernelEx(&cfg, kern, sh, pro, y));
+    QG_CUDA(cudaLaunchKernelEx(&cfg, kern, sh, pro));
     return QG_OK;
 }
 

@@ -53,7 +53,10 @@ struct qg_state {
     float *part_acc, *part_ml;
     unsigned* attn_count;       // [n_kv_heads] split arrivals (left at 0)
     float* kpart;               // split-K GEMV slice sums [max slices][hidden8]
-    unsigned* kcnt;             // split-K GEMV group arrivals [hidden/8] (left at 0)
+    // the pending GEMV output y: ycur_parts vectors ycur_stride floats apart
+    // (split-K slice sums), summed in order by its reader
+    const float* ycur;
+    int ycur_parts, ycur_stride;
     unsigned long long* am_ws;  // lm_head argmax workspace (left at 0)
     int* slots;                 // device: [0] token in, [1] position, [2] token out (bit 31: device error)
     uint32_t* hist;             // device: greedy token per position [max_seq]
@@ -90,8 +93,8 @@ struct ResidualIO {
 int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first);
 int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
                         bool pdl_first);
-// h += y (closes a layer run on its own).
-int run_residual(float* h, const float* y, int n, cudaStream_t st);
+// h += the pending y (closes a layer run on its own).
+int run_residual(qg_state* s, float* h, int n, cudaStream_t st);
 // Output norm of a + y (stored to h_final) + fused lm_head GEMV + argmax ->
 // slots[0] / slots[2]; `advance` also records hist[pos] and moves slots[1].
 int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance);

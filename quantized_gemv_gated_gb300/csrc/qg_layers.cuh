@@ -159,12 +159,15 @@ struct ProGatedNorm {
     const float* w;
     int nv, dv, vk;
     float eps;
-    // [rn per head | run partials | o | z]
-    __host__ __device__ int floats(int k) const { return kMaxGatedHeads * 9 + 2 * k; }
+    // [rn per head | run partials | w (dv <= 128) | o | z]
+    __host__ __device__ int floats(int k) const { return kMaxGatedHeads * 9 + 128 + 2 * k; }
+    __device__ void pre(float* sm, int, int tid) {  // the norm weights: before the dependency wait
+        for (int i = tid; i < dv; i += kConsumers) sm[9 * kMaxGatedHeads + i] = __ldg(w + i);
+    }
     __device__ void prepare(float* sm, int k, int tid) {
         vk = k;
         float* part = sm + kMaxGatedHeads;
-        float* os = sm + 9 * kMaxGatedHeads;
+        float* os = sm + 9 * kMaxGatedHeads + 128;
         float* zs = os + k;
 #pragma unroll 4
         for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
@@ -188,10 +191,11 @@ struct ProGatedNorm {
     }
     __device__ void value8(const float* sm, int i0, float* v) const {
         const int h = i0 / dv, j0 = i0 - h * dv;  // dv % 8 == 0: the 8 elements share a head
-        const float* os = sm + 9 * kMaxGatedHeads;
+        const float* ws = sm + 9 * kMaxGatedHeads;
+        const float* os = ws + 128;
         const float rn = sm[h];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = ((os[i0 + t] * rn) * __ldg(w + j0 + t)) * silu(os[vk + i0 + t]);
+        for (int t = 0; t < 8; ++t) v[t] = ((os[i0 + t] * rn) * ws[j0 + t]) * silu(os[vk + i0 + t]);
     }
 };
 

@@ -154,6 +154,7 @@ __device__ void consume_gemv(Consumer& c, const GemvShape& g, Pro pro, Epi epi) 
     int r0, r1;
     cta_rows(g.units, g.n, r0, r1);
     epi.pre(r0, r1, c.tid);
+    pro.pre(reinterpret_cast<float*>(c.smem + off_pro(QT, g.k)), g.k, c.tid);
     gemv_consume<QT, LAYOUT_GROUPED, DUAL>(c.R, g, r0, r1, pro, epi, c.smem, c.tid);
 }
 
@@ -375,6 +376,8 @@ __device__ ProRmsNorm step_norm(const float* h, const float* y, const float* w, 
     pn.h_out = h_out;
     pn.eps = P.eps;
     pn.kdim = P.hidden;
+    pn.y_parts = 1;
+    pn.y_stride = 0;
     return pn;
 }
 
