@@ -285,14 +285,18 @@ __device__ __forceinline__ float dot_q4k(const uint8_t* blk, int g, const DigQ4&
     // scale / min of sub-blocks j = 2g (low nibbles) and 2g+1 (high nibbles)
     const float d = f16_to_f32(static_cast<uint16_t>(hdr.x & 0xffffu));
     const float dmin = f16_to_f32(static_cast<uint16_t>(hdr.x >> 16));
+    // the 6-bit scale/min of sub-blocks j = 2g, 2g + 1 as shifts and masks:
+    // j < 4 (g < 2) is byte j of the scale and min words; j >= 4 is the low /
+    // high nibble of byte j + 4 plus the top two bits of byte j - 4
     int sc[2], mn[2];
+    const bool low = g < 2;
+    const unsigned asc = low ? hdr.y : hdr.w, amn = low ? hdr.z : hdr.w;
+    const unsigned msk = low ? 63u : 15u, mhi = low ? 0u : 0x30u, sm4 = low ? 0u : 4u;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int j = 2 * g + t, sh = 8 * (j & 3);
-        const unsigned by = (hdr.y >> sh) & 0xffu, bz = (hdr.z >> sh) & 0xffu, bw = (hdr.w >> sh) & 0xffu;
-        const bool low = j < 4;
-        sc[t] = static_cast<int>(low ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4)));
-        mn[t] = static_cast<int>(low ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4)));
+        const unsigned sh = 16u * static_cast<unsigned>(g & 1) + 8u * t;
+        sc[t] = static_cast<int>(((asc >> sh) & msk) | ((hdr.y >> (sh + 2u)) & mhi));
+        mn[t] = static_cast<int>(((amn >> (sh + sm4)) & msk) | ((hdr.z >> (sh + 2u)) & mhi));
     }
     // |sc * sum| < 63 * 15 * 255 * 32 per sub-block: the weighted sums fit in int32
     const int I0 = sc[0] * static_cast<int>(a0) + sc[1] * static_cast<int>(b0);
@@ -378,12 +382,21 @@ struct Pipe {
     uint8_t* base;
     int ns;
     int slot_bytes;
-    unsigned q;
+    unsigned q;        // stages taken so far
     unsigned* err;
     unsigned* abort;
     int lane;
     uint64_t pol;
-    __device__ uint8_t* cur() const { return base + static_cast<size_t>(q % ns) * slot_bytes; }
+    int slot = 0;      // q % ns, kept incrementally (no division on the hot path)
+    unsigned ph = 0;   // (q / ns) & 1
+    __device__ uint8_t* cur() const { return base + static_cast<size_t>(slot) * slot_bytes; }
+    __device__ void advance() {
+        ++q;
+        if (++slot == ns) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
     // The abort word is read only once a wait has lasted ~50 us (then every
     // ~50 us): a load of it on every missed poll would put an L2 round trip on
     // the critical path of each stage that lands just in time.
@@ -407,27 +420,27 @@ struct Pipe {
     }
     // consumer side (every lane of every consumer warp)
     __device__ void wait_full() const {
-        if (!wait_bar(&full[q % ns], (q / ns) & 1u) && lane == 0) fail(DEVERR_FULL_WAIT);
+        if (!wait_bar(&full[slot], ph) && lane == 0) fail(DEVERR_FULL_WAIT);
     }
     __device__ void release() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[q % ns]);
-        ++q;
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        advance();
     }
     // producer side (the whole producer warp)
     __device__ bool acquire() {
         int good = 1;
-        if (lane == 0 && q >= static_cast<unsigned>(ns)) good = wait_bar(&empty[q % ns], ((q / ns) - 1u) & 1u) ? 1 : 0;
+        if (lane == 0 && q >= static_cast<unsigned>(ns)) good = wait_bar(&empty[slot], ph ^ 1u) ? 1 : 0;
         good = __shfl_sync(FULL, good, 0);
         if (!good && lane == 0) fail(DEVERR_EMPTY_WAIT);
         return good != 0;
     }
     __device__ void expect(unsigned bytes) {
-        if (lane == 0) mbar_arrive_expect_tx(&full[q % ns], bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
         __syncwarp();
     }
-    __device__ void copy(void* dst, const void* src, unsigned bytes) { bulk_g2s(dst, src, bytes, &full[q % ns], pol); }
-    __device__ void commit() { ++q; }
+    __device__ void copy(void* dst, const void* src, unsigned bytes) { bulk_g2s(dst, src, bytes, &full[slot], pol); }
+    __device__ void commit() { advance(); }
     // error exit: wait (bounded) for this CTA's copies still in flight
     __device__ void drain() {
         if (lane != 0) return;
@@ -442,6 +455,14 @@ struct Pipe {
         }
     }
 };
+
+// Sum of v over the G lanes of its row group (xor tree, G a power of two <= 32).
+__device__ __forceinline__ float group_sum(float v, int G) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        if (o < G) v += __shfl_xor_sync(FULL, v, o);
+    return v;
+}
 
 // Rows [r0, r1) of a launch with `units` 8-row units over gridDim.x CTAs.
 __device__ __forceinline__ void cta_rows(int units, int n, int& r0, int& r1) {
@@ -560,7 +581,7 @@ __device__ void gemv_consume(Pipe& p, const GemvShape& sh, int r0, int r1, Pro& 
                                         reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
                         }
                     }
-                    for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+                    v = group_sum(v, G);
                     if (valid && j == 0) {
                         float* y = m ? ys2 : ys;
                         y[row - r0] = s ? y[row - r0] + v : v;
@@ -700,7 +721,7 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8
                                     reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
                     }
                 }
-                for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+                v = group_sum(v, G);
                 if (valid && j == 0) ps[row] = v;
             }
             p.release();
