@@ -148,14 +148,15 @@ __device__ __forceinline__ int dp4a_su(unsigned a, unsigned b, int c) {
 // One warp per 256-element super-block, 8 consecutive elements per lane:
 // n_i = rint(x_i * 2^(22-e)) with 2^e <= max|x| over the super-block
 // (clamped to |n| < 2^23), stored as three byte planes.
+// Blocks [b_lo, b_hi) only (default: all), for a CTA that uses just some slices.
 template <int QT, class Pro>
 __device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, uint8_t* aux, int k, int warp,
-                           int lane) {
-    const int nsb = k >> 8;
+                           int lane, int b_lo = 0, int b_hi = -1) {
+    const int nsb = b_hi < 0 ? (k >> 8) : b_hi;
     float* units = reinterpret_cast<float*>(aux);
     // a warp's blocks in batches of 4 whose loads are all issued first, so a
     // prologue that reads x from global memory pays one round trip per batch
-    for (int bb = warp; bb < nsb; bb += 4 * kConsumerWarps) {
+    for (int bb = b_lo + warp; bb < nsb; bb += 4 * kConsumerWarps) {
         float xb[4][8];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -682,12 +683,16 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8
     uint8_t* dig = smem + off_dig();
     uint8_t* aux = smem + off_aux(k);
     float* psm = reinterpret_cast<float*>(smem + off_pro(QT, k));
-    pro.prepare(psm, k, tid);
-    bar_sync(1, kConsumers);
-    build_xrep<QT>(pro, psm, dig, aux, k, warp, lane);
-    bar_sync(1, kConsumers);
     long long t0, t1;
     split_range(sh, t0, t1);
+    pro.prepare(psm, k, tid);
+    bar_sync(1, kConsumers);
+    if (t1 > t0) {  // digits of the slices this CTA's tasks use
+        const int s0 = static_cast<int>(t0 / sh.units), s1 = static_cast<int>((t1 - 1) / sh.units);
+        build_xrep<QT>(pro, psm, dig, aux, k, warp, lane, sh.sl_c0[s0] >> 2,
+                       (sh.sl_c0[s1] + (1 << sh.sl_lg[s1])) >> 2);
+    }
+    bar_sync(1, kConsumers);
     for (long long t = t0; t < t1;) {
         const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
         const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
