@@ -458,11 +458,55 @@ struct Pipe {
 };
 
 // Sum of v over the G lanes of its row group (xor tree, G a power of two <= 32).
-__device__ __forceinline__ float group_sum(float v, int G) {
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         if (o < G) v += __shfl_xor_sync(FULL, v, o);
     return v;
+}
+
+// The lane's share of one stage row pass in a slice of G = 2^LG chunks: its
+// byte offsets inside the stage (constant for the slice: row rl of the pass,
+// block bl of the slice, quarter q), and one pass's bytes (64 block-rows).
+template <int QT, int LAYOUT, int LG>
+struct LaneRow {
+    static constexpr int kb = (1 << LG) >> 2;
+    static constexpr int GB = group_block_bytes(QT);
+    static constexpr int pass_bytes = kStageBlockRows * block_bytes(QT);
+    int o0, o1, o2, o3;  // Q4_K: block; Q6_K: QL, QH, scales, d
+    int q;
+    __device__ __forceinline__ LaneRow(int rl, int bl, int q_) : q(q_) {
+        if constexpr (QT == QT_Q4K) {
+            o0 = LAYOUT == LAYOUT_GROUPED ? ((rl >> 3) * kb + bl) * GB + (rl & 7) * 144 : (rl * kb + bl) * 144;
+            o1 = o2 = o3 = 0;
+        } else {
+            const int base = ((rl >> 3) * kb + bl) * GB, rr = rl & 7;
+            o0 = base + rr * 128 + 32 * q;
+            o1 = base + 1024 + rr * 64 + 16 * q;
+            o2 = base + 1536 + rr * 16 + 8 * (q >> 1);
+            o3 = base + 1664 + 2 * rr;
+        }
+    }
+    // the lane's chunk value of its row in the pass starting at ps, summed
+    // over the row's G lanes (lanes of rows past the range read stale bytes
+    // inside the slot; their sums are not stored)
+    __device__ __forceinline__ float value(const uint8_t* ps, const DigQ4& d4, const DigQ6& d6) const {
+        float v;
+        if constexpr (QT == QT_Q4K) v = dot_q4k(ps + o0, q, d4);
+        else v = dot_q6k(ps + o0, ps + o1, ps + o2, reinterpret_cast<const uint16_t*>(ps + o3), q & 1, d6);
+        return group_sum<(1 << LG)>(v);
+    }
+};
+
+// The lane's chunk digits for slice s (lanes per row 2^LG).
+template <int QT, int LG>
+__device__ __forceinline__ void slice_lane(const GemvShape& sh, int s, int lane, const uint8_t* dig, const uint8_t* aux,
+                                           int k, int& bl, int& q, DigQ4& d4, DigQ6& d6) {
+    lane_chunk<QT>(lane & ((1 << LG) - 1), LG, bl, q);
+    const int b = (sh.sl_c0[s] >> 2) + bl;
+    if constexpr (QT == QT_Q4K) load_dig_q4(d4, 4 * b + q, dig, aux, k);
+    else load_dig_q6(d6, b, q, dig, aux, k);
 }
 
 // Rows [r0, r1) of a launch with `units` 8-row units over gridDim.x CTAs.
@@ -523,6 +567,37 @@ __device__ bool gemv_produce(Pipe& p, const GemvShape& sh, const uint8_t* w0, co
 }
 
 // --------------------------------------------------------------- consumer
+// Slice s (2^LG lanes per row) of the rows [r0, r1): every stage of pp passes
+// of U rows; lane j == 0 of each row adds the row's slice sum to ys (ys2 for
+// the second matrix of a dual launch), in slice order.
+template <int QT, int LAYOUT, bool DUAL, int LG>
+__device__ void consume_slice(Pipe& p, const GemvShape& sh, int s, int r0, int r1, float* ys, float* ys2,
+                              const uint8_t* dig, const uint8_t* aux, int warp, int lane) {
+    constexpr int rpw = 32 >> LG, U = 8 * rpw;
+    const int rl = warp * rpw + (lane >> LG);
+    const bool lead = (lane & ((1 << LG) - 1)) == 0;
+    int bl, q;
+    DigQ4 d4;
+    DigQ6 d6;
+    slice_lane<QT, LG>(sh, s, lane, dig, aux, sh.k, bl, q, d4, d6);
+    const LaneRow<QT, LAYOUT, LG> lr(rl, bl, q);
+    const int pp = sh.pp;
+    for (int row0 = r0; row0 < r1; row0 += U * pp) {
+        const int npass = min(pp, (r1 - row0 + U - 1) / U);  // passes holding rows of the range
+#pragma unroll
+        for (int m = 0; m < (DUAL ? 2 : 1); ++m) {
+            p.wait_full();
+            const uint8_t* ps = p.cur();
+            float* y = (m ? ys2 : ys) + (row0 - r0) + rl;
+            for (int pass = 0; pass < npass; ++pass, ps += lr.pass_bytes, y += U) {
+                const float v = lr.value(ps, d4, d6);
+                if (lead && row0 + pass * U + rl < r1) *y = s ? *y + v : v;
+            }
+            p.release();
+        }
+    }
+}
+
 // Pro: pre(float* sm, int k, int tid) before the dependency wait (inputs no
 //      earlier kernel of the step writes; called by the kernel),
 //      prepare(float* sm, int k, int tid) fills the rest of its scratch,
@@ -534,7 +609,6 @@ __device__ bool gemv_produce(Pipe& p, const GemvShape& sh, const uint8_t* w0, co
 template <int QT, int LAYOUT, bool DUAL, class Pro, class Epi>
 __device__ void gemv_consume(Pipe& p, const GemvShape& sh, int r0, int r1, Pro& pro, Epi& epi, uint8_t* smem,
                              int tid) {
-    constexpr int GB = group_block_bytes(QT);
     const int warp = tid >> 5, lane = tid & 31, k = sh.k;
     uint8_t* dig = smem + off_dig();
     uint8_t* aux = smem + off_aux(k);
@@ -548,48 +622,11 @@ __device__ void gemv_consume(Pipe& p, const GemvShape& sh, int r0, int r1, Pro& 
     bar_sync(1, kConsumers);
 
     for (int s = 0; s < sh.nsl; ++s) {
-        const int lg = sh.sl_lg[s], G = 1 << lg, rpw = 32 >> lg, kb = G >> 2, U = 8 * rpw;
-        const int j = lane & (G - 1), rl = warp * rpw + (lane >> lg);
-        int bl, q;
-        lane_chunk<QT>(j, lg, bl, q);
-        const int b = (sh.sl_c0[s] >> 2) + bl;
-        // the lane's chunk digits, in registers for every row of the slice
-        DigQ4 d4;
-        DigQ6 d6;
-        if constexpr (QT == QT_Q4K) load_dig_q4(d4, 4 * b + q, dig, aux, k);
-        else load_dig_q6(d6, b, q, dig, aux, k);
-        for (int row0 = r0; row0 < r1; row0 += U * sh.pp) {
-#pragma unroll
-            for (int m = 0; m < (DUAL ? 2 : 1); ++m) {
-                p.wait_full();
-                const uint8_t* st = p.cur();
-                for (int pass = 0; pass < sh.pp; ++pass) {
-                    const int sl = pass * U + rl;  // row within the stage
-                    const int row = row0 + sl;
-                    const bool valid = row < r1;
-                    float v = 0.0f;
-                    if (valid) {
-                        if constexpr (QT == QT_Q4K) {
-                            const uint8_t* blk = LAYOUT == LAYOUT_GROUPED
-                                                     ? st + ((sl >> 3) * kb + bl) * GB + (sl & 7) * 144
-                                                     : st + (sl * kb + bl) * 144;
-                            v = dot_q4k(blk, q, d4);
-                        } else {
-                            const uint8_t* base = st + ((sl >> 3) * kb + bl) * GB;
-                            const int rr = sl & 7;
-                            v = dot_q6k(base + rr * 128 + 32 * q, base + 1024 + rr * 64 + 16 * q,
-                                        base + 1536 + rr * 16 + 8 * (q >> 1),
-                                        reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
-                        }
-                    }
-                    v = group_sum(v, G);
-                    if (valid && j == 0) {
-                        float* y = m ? ys2 : ys;
-                        y[row - r0] = s ? y[row - r0] + v : v;
-                    }
-                }
-                p.release();
-            }
+        switch (sh.sl_lg[s]) {
+            case 5: consume_slice<QT, LAYOUT, DUAL, 5>(p, sh, s, r0, r1, ys, ys2, dig, aux, warp, lane); break;
+            case 4: consume_slice<QT, LAYOUT, DUAL, 4>(p, sh, s, r0, r1, ys, ys2, dig, aux, warp, lane); break;
+            case 3: consume_slice<QT, LAYOUT, DUAL, 3>(p, sh, s, r0, r1, ys, ys2, dig, aux, warp, lane); break;
+            default: consume_slice<QT, LAYOUT, DUAL, 2>(p, sh, s, r0, r1, ys, ys2, dig, aux, warp, lane); break;
         }
         bar_sync(1, kConsumers);  // this slice's row sums are in before the next adds to them
     }
@@ -676,9 +713,34 @@ __device__ bool gemv_split_produce(Pipe& p, const GemvShape& sh, const L2Prefetc
     return true;
 }
 
+// Rows [ra, rb) of slice s (2^LG lanes per row): their slice sums to part[s].
+template <int QT, int LG>
+__device__ void split_slice(Pipe& p, const GemvShape& sh, int s, int ra, int rb, const uint8_t* dig,
+                            const uint8_t* aux, int warp, int lane) {
+    constexpr int rpw = 32 >> LG, U = 8 * rpw;
+    const int rl = warp * rpw + (lane >> LG);
+    const bool lead = (lane & ((1 << LG) - 1)) == 0;
+    int bl, q;
+    DigQ4 d4;
+    DigQ6 d6;
+    slice_lane<QT, LG>(sh, s, lane, dig, aux, sh.k, bl, q, d4, d6);
+    const LaneRow<QT, LAYOUT_GROUPED, LG> lr(rl, bl, q);
+    const int pp = sh.pp;
+    for (int row0 = ra; row0 < rb; row0 += U * pp) {
+        const int npass = min(pp, (rb - row0 + U - 1) / U);
+        p.wait_full();
+        const uint8_t* ps = p.cur();
+        float* y = sh.part + static_cast<size_t>(s) * sh.n8 + row0 + rl;
+        for (int pass = 0; pass < npass; ++pass, ps += lr.pass_bytes, y += U) {
+            const float v = lr.value(ps, d4, d6);
+            if (lead && row0 + pass * U + rl < rb) *y = v;
+        }
+        p.release();
+    }
+}
+
 template <int QT, class Pro>
 __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8_t* smem, int tid) {
-    constexpr int GB = group_block_bytes(QT);
     const int warp = tid >> 5, lane = tid & 31, k = sh.k;
     uint8_t* dig = smem + off_dig();
     uint8_t* aux = smem + off_aux(k);
@@ -696,40 +758,12 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8
     for (long long t = t0; t < t1;) {
         const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
         const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
-        const int lg = sh.sl_lg[s], G = 1 << lg, rpw = 32 >> lg, kb = G >> 2, U = 8 * rpw;
         const int ra = 8 * g, rb = min(8 * ge, sh.n);
-        const int j = lane & (G - 1), rl = warp * rpw + (lane >> lg);
-        int bl, q;
-        lane_chunk<QT>(j, lg, bl, q);
-        const int b = (sh.sl_c0[s] >> 2) + bl;
-        DigQ4 d4;
-        DigQ6 d6;
-        if constexpr (QT == QT_Q4K) load_dig_q4(d4, 4 * b + q, dig, aux, k);
-        else load_dig_q6(d6, b, q, dig, aux, k);
-        float* ps = sh.part + static_cast<size_t>(s) * sh.n8;
-        for (int row0 = ra; row0 < rb; row0 += U * sh.pp) {
-            p.wait_full();
-            const uint8_t* st = p.cur();
-            for (int pass = 0; pass < sh.pp; ++pass) {
-                const int sl = pass * U + rl;
-                const int row = row0 + sl;
-                const bool valid = row < rb;
-                float v = 0.0f;
-                if (valid) {
-                    if constexpr (QT == QT_Q4K) {
-                        v = dot_q4k(st + ((sl >> 3) * kb + bl) * GB + (sl & 7) * 144, q, d4);
-                    } else {
-                        const uint8_t* base = st + ((sl >> 3) * kb + bl) * GB;
-                        const int rr = sl & 7;
-                        v = dot_q6k(base + rr * 128 + 32 * q, base + 1024 + rr * 64 + 16 * q,
-                                    base + 1536 + rr * 16 + 8 * (q >> 1),
-                                    reinterpret_cast<const uint16_t*>(base + 1664) + rr, q & 1, d6);
-                    }
-                }
-                v = group_sum(v, G);
-                if (valid && j == 0) ps[row] = v;
-            }
-            p.release();
+        switch (sh.sl_lg[s]) {
+            case 5: split_slice<QT, 5>(p, sh, s, ra, rb, dig, aux, warp, lane); break;
+            case 4: split_slice<QT, 4>(p, sh, s, ra, rb, dig, aux, warp, lane); break;
+            case 3: split_slice<QT, 3>(p, sh, s, ra, rb, dig, aux, warp, lane); break;
+            default: split_slice<QT, 2>(p, sh, s, ra, rb, dig, aux, warp, lane); break;
         }
         t += ge - g;
     }
