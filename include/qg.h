@@ -193,10 +193,12 @@ int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg
 
 /* Planar Q6_K (the layout the GEMV engine streams): n8 = n rounded up to 8
  * rows, nb = k/256.  For every 8-row group g and super-block b one 1680-byte
- * group-block holding exactly the GGUF bytes of those 8 blocks: QL [8][128]
- * (per row, for quarter-chunk c = 2*half + part (0..3), the 16 low-4-bit
- * bytes ql[64*half + 16*part ..] followed by ql[64*half + 32 + 16*part ..]),
- * QH [8][64] (as in GGUF), SC [8][16] int8 scales, D [8] fp16.  Group-blocks
+ * group-block holding exactly the GGUF bytes of those 8 blocks, rearranged:
+ * for row rr (0..7) and 64-weight quarter cq = 2*half + part (0..3), u =
+ * 4*rr + cq, a 48-byte record at 48*u: ql[64*half + 16*part .. +16],
+ * ql[64*half + 32 + 16*part .. +16], qh[16*cq .. +16]; the quarter's four
+ * int8 scales sc[8*half + part + 2*s], s = 0..3, at 1536 + 4*u; the row's
+ * fp16 d at 1664 + 2*rr.  Group-blocks
  * are stored slice-major: K splits into slices of 8 super-blocks, then of 4,
  * 2 and 1 for the remainder (its binary digits, in that order); slice
  * [b0, b0 + kb) takes (n8/8)*kb group-blocks from offset (n8/8)*b0*1680, with

@@ -73,10 +73,11 @@ static int lmhead_scratch(unsigned long long** out) {
 
 // ------------------------------------------------- grouped weight layouts
 // One thread per (8-row group, super-block) of the padded matrix, stored at
-// its slice-major place (grouped_offset); rows n..n8-1 are zero.  Q6_K: [QL 8 x 128 | QH 8 x 64 | scales 8 x 16 | d 8 x 2] with each
-// row's QL reordered so that the two 16-byte halves of every 64-weight
-// quarter cq = 2 half + part are adjacent (ql[64 half + 16 part ..] then
-// ql[64 half + 32 + 16 part ..]).  Q4_K: the 8 rows' 144-byte blocks.
+// its slice-major place (grouped_offset); rows n..n8-1 are zero.  Q6_K: for
+// row rr and quarter cq = 2 half + part (u = 4 rr + cq) the 48-byte record
+// [ql[64 half + 16 part ..16] | ql[64 half + 32 + 16 part ..16] | qh[16 cq ..16]]
+// at 48u, the quarter's scales sc[8 half + part + 2s] (s = 0..3) at 1536 + 4u,
+// d at 1664 + 2 rr.  Q4_K: the 8 rows' 144-byte blocks.
 __global__ void q6k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n, int n8, int nb) {
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long total = static_cast<long long>(n8 / 8) * nb;
@@ -85,29 +86,20 @@ __global__ void q6k_grouped_kernel(const uint8_t* __restrict__ src, uint8_t* __r
     uint8_t* gb = dst + grouped_offset(n8, nb, static_cast<int>(g), static_cast<int>(b), 1680);
     for (int rr = 0; rr < 8; ++rr) {
         const long long r = 8 * g + rr;
-        uint8_t* ql = gb + rr * 128;
-        uint8_t* qh = gb + 1024 + rr * 64;
-        uint8_t* sc = gb + 1536 + rr * 16;
-        uint8_t* dd = gb + 1664 + rr * 2;
-        if (r >= n) {
-            for (int i = 0; i < 128; ++i) ql[i] = 0;
-            for (int i = 0; i < 64; ++i) qh[i] = 0;
-            for (int i = 0; i < 16; ++i) sc[i] = 0;
-            dd[0] = dd[1] = 0;
-            continue;
-        }
-        const uint8_t* blk = src + (r * nb + b) * 210;
-        for (int c = 0; c < 4; ++c) {
-            const int half = c >> 1, part = c & 1;
+        const uint8_t* blk = r < n ? src + (r * nb + b) * 210 : nullptr;
+        for (int cq = 0; cq < 4; ++cq) {
+            const int half = cq >> 1, part = cq & 1, u = 4 * rr + cq;
+            uint8_t* rec = gb + 48 * u;
+            uint8_t* sc = gb + 1536 + 4 * u;
             for (int i = 0; i < 16; ++i) {
-                ql[32 * c + i] = blk[64 * half + 16 * part + i];
-                ql[32 * c + 16 + i] = blk[64 * half + 32 + 16 * part + i];
+                rec[i] = blk ? blk[64 * half + 16 * part + i] : 0;
+                rec[16 + i] = blk ? blk[64 * half + 32 + 16 * part + i] : 0;
+                rec[32 + i] = blk ? blk[128 + 16 * cq + i] : 0;
             }
+            for (int s = 0; s < 4; ++s) sc[s] = blk ? blk[192 + 8 * half + part + 2 * s] : 0;
         }
-        for (int i = 0; i < 64; ++i) qh[i] = blk[128 + i];
-        for (int i = 0; i < 16; ++i) sc[i] = blk[192 + i];
-        dd[0] = blk[208];
-        dd[1] = blk[209];
+        gb[1664 + 2 * rr] = blk ? blk[208] : 0;
+        gb[1665 + 2 * rr] = blk ? blk[209] : 0;
     }
 }
 

@@ -50,9 +50,12 @@ constexpr int QT_Q4K = 12;
 constexpr int QT_Q6K = 14;
 // Weight layouts.  RAW: GGUF Q4_K rows.  GROUPED: rows padded to a multiple
 // of 8; for every 8-row group g and super-block b one group-block of GB
-// bytes: Q4_K: the 8 rows' 144-byte blocks (GB = 1152); Q6_K: [QL 8 x 128 |
-// QH 8 x 64 | scales 8 x 16 | d 8 x 2] (GB = 1680), QL with the two 16-byte
-// halves of each 64-weight quarter adjacent.  Group-blocks are stored
+// bytes: Q4_K: the 8 rows' 144-byte blocks (GB = 1152); Q6_K (GB = 1680):
+// for row rr and 64-weight quarter cq = 2 half + part (u = 4 rr + cq) a
+// 48-byte record at 48u [ql[64 half + 16 part ..16] | ql[64 half + 32 + 16
+// part ..16] | qh[16 cq ..16]], the quarter's four scales sc[8 half + part +
+// 2s] (s = 0..3) at 1536 + 4u, and the row's fp16 d at 1664 + 2 rr: every
+// lane's bytes of a row sit at three fixed offsets.  Group-blocks are stored
 // slice-major: the K slices (8 super-blocks each, then 4, 2, 1 for the rest)
 // one after the other, inside a slice group by group, so that any run of
 // consecutive groups of one slice is one contiguous piece.
@@ -113,9 +116,9 @@ struct GemvShape {
 
 // Shared-memory layout offsets.  aux: per 256-element super-block the unit
 // 2^(e-22) (float), then Q4_K: per 32-element sub-block the sum of n (float);
-// Q6_K: per 16-element group {-32*N0, -32*N1, -32*N2, 0} (digit-plane sums).
+// Q6_K: per 16-element group -32 * (sum of n) (float), ordered [block][cq][s].
 __host__ __device__ inline int xaux_bytes(int qt, int k) {
-    return ((4 * (k / 256) + 15) & ~15) + (qt == QT_Q4K ? 4 * (k / 32) : k);
+    return ((4 * (k / 256) + 15) & ~15) + (qt == QT_Q4K ? 4 * (k / 32) : 4 * (k / 16));
 }
 __host__ __device__ inline int aux_tail(int k) { return (4 * (k / 256) + 15) & ~15; }
 __host__ __device__ inline int off_dig() { return 16 * kMaxStages; }
@@ -205,14 +208,13 @@ __device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, uint8_
                 if ((lane & 3) == 0)
                     reinterpret_cast<float*>(aux + aux_tail(k))[8 * b + (lane >> 2)] = static_cast<float>(nsum);
             } else {
-                int n0 = static_cast<int>(dp4a_uu(w0[0], 0x01010101u, dp4a_uu(w0[1], 0x01010101u, 0u)));
-                int n1 = static_cast<int>(dp4a_uu(w1[0], 0x01010101u, dp4a_uu(w1[1], 0x01010101u, 0u)));
-                int n2 = dp4a_su(w2[0], 0x01010101u, dp4a_su(w2[1], 0x01010101u, 0));
-                n0 += __shfl_xor_sync(FULL, n0, 1);
-                n1 += __shfl_xor_sync(FULL, n1, 1);
-                n2 += __shfl_xor_sync(FULL, n2, 1);
-                if ((lane & 1) == 0)
-                    reinterpret_cast<int4*>(aux + aux_tail(k))[swz(QT, u)] = make_int4(-32 * n0, -32 * n1, -32 * n2, 0);
+                // the 16-element group of lanes (2i, 2i+1) is group s = (lane & 15) >> 2
+                // of quarter cq = 2 half + part of block b: nf at [b][cq][s]
+                nsum += __shfl_xor_sync(FULL, nsum, 1);
+                if ((lane & 1) == 0) {
+                    const int cq = 2 * (lane >> 4) + ((lane >> 1) & 1), sg = (lane & 15) >> 2;
+                    reinterpret_cast<float*>(aux + aux_tail(k))[16 * b + 4 * cq + sg] = -32.0f * static_cast<float>(nsum);
+                }
             }
         }
     }
@@ -310,43 +312,45 @@ __device__ __forceinline__ float dot_q4k(const uint8_t* blk, int g, const DigQ4&
 
 // x digits of one Q6_K quarter (block b, cq = 2 half + part): the four
 // 16-element groups x[256b + 128 half + 32 s + 16 part ..], s = 0..3, and
-// their -32 * plane sums.
+// nf[s] = -32 * (sum of n over group s) as a float (the -32 offset of the
+// quants, applied once per group instead of per weight).
 struct DigQ6 {
     uint4 d[4][3];
-    int gc[4][3];
+    float nf[4];
     float unit;
 };
 __device__ __forceinline__ void load_dig_q6(DigQ6& D, int b, int cq, const uint8_t* dig, const uint8_t* aux, int k) {
     const int half = cq >> 1, part = cq & 1;
-    const int4* gcp = reinterpret_cast<const int4*>(aux + aux_tail(k));
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int pos = 256 * b + 128 * half + 32 * s + 16 * part;
         const unsigned u = swz(QT_Q6K, static_cast<unsigned>(pos) >> 4);
 #pragma unroll
         for (int p = 0; p < 3; ++p) D.d[s][p] = *reinterpret_cast<const uint4*>(dig + p * k + (u << 4));
-        const int4 g = gcp[u];
-        D.gc[s][0] = g.x;
-        D.gc[s][1] = g.y;
-        D.gc[s][2] = g.z;
     }
+    const float4 nf = reinterpret_cast<const float4*>(aux + aux_tail(k))[4 * b + cq];
+    D.nf[0] = nf.x;
+    D.nf[1] = nf.y;
+    D.nf[2] = nf.z;
+    D.nf[3] = nf.w;
     D.unit = reinterpret_cast<const float*>(aux)[b];
 }
 
-// One row's Q6_K quarter: ql = its 32 QL bytes (A: ql[64 half + 16 part ..],
-// B: ql[64 half + 32 + 16 part ..]), qh = its 16 QH bytes, sc8 = the 8 scales
-// of its half, dp = its fp16 d.
-__device__ __forceinline__ float dot_q6k(const uint8_t* ql, const uint8_t* qh, const uint8_t* sc8, const uint16_t* dp,
-                                         int part, const DigQ6& D) {
-    const uint4 A = *reinterpret_cast<const uint4*>(ql);
-    const uint4 B = *reinterpret_cast<const uint4*>(ql + 16);
-    const uint4 H = *reinterpret_cast<const uint4*>(qh);
-    const uint2 S = *reinterpret_cast<const uint2*>(sc8);
-    const float d = f16_to_f32(*dp);
+// One row's Q6_K quarter.  rec: its 48-byte record [A | B | H] (A = ql[64
+// half + 16 part ..], B = ql[64 half + 32 + 16 part ..], H = qh[16 cq ..]);
+// S: its four int8 scales (group s in byte s); dbits: its fp16 d.
+// value = d * unit * sum_s sc_s * (sum_i q_i n_i - 32 * sum_i n_i), the first
+// sum exact in integers per digit plane, the second from nf.
+__device__ __forceinline__ float dot_q6k(const uint8_t* rec, unsigned S, uint16_t dbits, const DigQ6& D) {
+    const uint4 A = *reinterpret_cast<const uint4*>(rec);
+    const uint4 B = *reinterpret_cast<const uint4*>(rec + 16);
+    const uint4 H = *reinterpret_cast<const uint4*>(rec + 32);
     int I0 = 0, I1 = 0, I2 = 0;
+    float C = 0.0f;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-        int t0 = D.gc[s][0], t1 = D.gc[s][1], t2 = D.gc[s][2];
+        unsigned t0 = 0u, t1 = 0u;
+        int t2 = 0;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const unsigned a = u4w(A, w), bb = u4w(B, w), hh = u4w(H, w);
@@ -355,19 +359,19 @@ __device__ __forceinline__ float dot_q6k(const uint8_t* ql, const uint8_t* qh, c
             else if (s == 1) q = (bb & 0x0f0f0f0fu) | ((hh << 2) & 0x30303030u);
             else if (s == 2) q = ((a >> 4) & 0x0f0f0f0fu) | (hh & 0x30303030u);
             else q = ((bb >> 4) & 0x0f0f0f0fu) | ((hh >> 2) & 0x30303030u);
-            t0 = static_cast<int>(dp4a_uu(q, u4w(D.d[s][0], w), static_cast<unsigned>(t0)));
-            t1 = static_cast<int>(dp4a_uu(q, u4w(D.d[s][1], w), static_cast<unsigned>(t1)));
+            t0 = dp4a_uu(q, u4w(D.d[s][0], w), t0);
+            t1 = dp4a_uu(q, u4w(D.d[s][1], w), t1);
             t2 = dp4a_us(q, u4w(D.d[s][2], w), t2);
         }
-        const int si = part + 2 * s;
-        const int sc = static_cast<int>(static_cast<int8_t>(((si < 4 ? S.x : S.y) >> (8 * (si & 3))) & 0xffu));
-        // |sc * t| <= 128 * 32 * 255 * 16 per group, four groups: fits in int32
-        I0 += sc * t0;
-        I1 += sc * t1;
+        const int sc = static_cast<int>(S << (24 - 8 * s)) >> 24;  // byte s, sign-extended
+        // |sc * t| <= 128 * 63 * 255 * 16 per group, four groups: fits in int32
+        I0 += sc * static_cast<int>(t0);
+        I1 += sc * static_cast<int>(t1);
         I2 += sc * t2;
+        C = fmaf(static_cast<float>(sc), D.nf[s], C);
     }
-    const float F = fmaf(static_cast<float>(I2), 65536.0f, fmaf(static_cast<float>(I1), 256.0f, static_cast<float>(I0)));
-    return (d * D.unit) * F;
+    const float F = fmaf(static_cast<float>(I2), 65536.0f, fmaf(static_cast<float>(I1), 256.0f, static_cast<float>(I0))) + C;
+    return (f16_to_f32(dbits) * D.unit) * F;
 }
 
 // ----------------------------------------------------------------- pipe
@@ -474,18 +478,18 @@ struct LaneRow {
     static constexpr int kb = (1 << LG) >> 2;
     static constexpr int GB = group_block_bytes(QT);
     static constexpr int pass_bytes = kStageBlockRows * block_bytes(QT);
-    int o0, o1, o2, o3;  // Q4_K: block; Q6_K: QL, QH, scales, d
+    int o0, o1, o2, o3;  // Q4_K: block; Q6_K: [A | B | H] record, scale record, d
     int q;
     __device__ __forceinline__ LaneRow(int rl, int bl, int q_) : q(q_) {
         if constexpr (QT == QT_Q4K) {
             o0 = LAYOUT == LAYOUT_GROUPED ? ((rl >> 3) * kb + bl) * GB + (rl & 7) * 144 : (rl * kb + bl) * 144;
             o1 = o2 = o3 = 0;
-        } else {
-            const int base = ((rl >> 3) * kb + bl) * GB, rr = rl & 7;
-            o0 = base + rr * 128 + 32 * q;
-            o1 = base + 1024 + rr * 64 + 16 * q;
-            o2 = base + 1536 + rr * 16 + 8 * (q >> 1);
-            o3 = base + 1664 + 2 * rr;
+        } else {  // records of the planar Q6_K group-block (see the layout note at the top)
+            const int base = ((rl >> 3) * kb + bl) * GB, rr = rl & 7, u = 4 * rr + q;
+            o0 = base + 48 * u;
+            o1 = base + 1536 + 4 * u;
+            o2 = base + 1664 + 2 * rr;
+            o3 = 0;
         }
     }
     // the lane's chunk value of its row in the pass starting at ps, summed
@@ -494,7 +498,7 @@ struct LaneRow {
     __device__ __forceinline__ float value(const uint8_t* ps, const DigQ4& d4, const DigQ6& d6) const {
         float v;
         if constexpr (QT == QT_Q4K) v = dot_q4k(ps + o0, q, d4);
-        else v = dot_q6k(ps + o0, ps + o1, ps + o2, reinterpret_cast<const uint16_t*>(ps + o3), q & 1, d6);
+        else v = dot_q6k(ps + o0, *reinterpret_cast<const unsigned*>(ps + o1), *reinterpret_cast<const uint16_t*>(ps + o2), d6);
         return group_sum<(1 << LG)>(v);
     }
 };
@@ -678,21 +682,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
 // slices in slice order -- the order of the one-CTA-per-row path, so both give
 // the same floats -- which saves this kernel an arrival count and a second
 // pass over the sums.
-__device__ __forceinline__ void split_range(const GemvShape& sh, long long& t0, long long& t1) {
-    const long long T = static_cast<long long>(sh.units) * sh.nsl;
-    t0 = static_cast<long long>(blockIdx.x) * T / gridDim.x;
-    t1 = static_cast<long long>(blockIdx.x + 1) * T / gridDim.x;
+// (units * nsl < 2^21 for n <= 2^20 rows and K <= 16384: the products fit in 32 bits)
+__device__ __forceinline__ void split_range(const GemvShape& sh, int& t0, int& t1) {
+    const unsigned T = static_cast<unsigned>(sh.units) * sh.nsl;
+    t0 = static_cast<int>(blockIdx.x * T / gridDim.x);
+    t1 = static_cast<int>((blockIdx.x + 1) * T / gridDim.x);
 }
 
 template <int QT>
 __device__ bool gemv_split_produce(Pipe& p, const GemvShape& sh, const L2Prefetch* next) {
     constexpr int GB = group_block_bytes(QT);
-    long long t0, t1;
+    int t0, t1;
     split_range(sh, t0, t1);
     bool first = true;
-    for (long long t = t0; t < t1;) {
-        const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
-        const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
+    for (int t = t0; t < t1;) {
+        const int s = t / sh.units, g = t - s * sh.units;
+        const int ge = min(sh.units, g + (t1 - t));
         const int lg = sh.sl_lg[s], kb = (1 << lg) >> 2, U = (256 >> lg) * sh.pp, b0 = sh.sl_c0[s] >> 2;
         const int ra = 8 * g, rb = min(8 * ge, sh.n);
         for (int row0 = ra; row0 < rb; row0 += U) {
@@ -745,19 +750,19 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8
     uint8_t* dig = smem + off_dig();
     uint8_t* aux = smem + off_aux(k);
     float* psm = reinterpret_cast<float*>(smem + off_pro(QT, k));
-    long long t0, t1;
+    int t0, t1;
     split_range(sh, t0, t1);
     pro.prepare(psm, k, tid);
     bar_sync(1, kConsumers);
     if (t1 > t0) {  // digits of the slices this CTA's tasks use
-        const int s0 = static_cast<int>(t0 / sh.units), s1 = static_cast<int>((t1 - 1) / sh.units);
+        const int s0 = t0 / sh.units, s1 = (t1 - 1) / sh.units;
         build_xrep<QT>(pro, psm, dig, aux, k, warp, lane, sh.sl_c0[s0] >> 2,
                        (sh.sl_c0[s1] + (1 << sh.sl_lg[s1])) >> 2);
     }
     bar_sync(1, kConsumers);
-    for (long long t = t0; t < t1;) {
-        const int s = static_cast<int>(t / sh.units), g = static_cast<int>(t % sh.units);
-        const int ge = static_cast<int>(min(static_cast<long long>(sh.units), g + (t1 - t)));
+    for (int t = t0; t < t1;) {
+        const int s = t / sh.units, g = t - s * sh.units;
+        const int ge = min(sh.units, g + (t1 - t));
         const int ra = 8 * g, rb = min(8 * ge, sh.n);
         switch (sh.sl_lg[s]) {
             case 5: split_slice<QT, 5>(p, sh, s, ra, rb, dig, aux, warp, lane); break;

@@ -128,6 +128,8 @@ template <int QT, class Pro>
 int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, cudaStream_t st, bool pdl, unsigned* err,
                       float* part, const L2Prefetch& next = L2Prefetch{}) {
     if (!err || !part) return set_err(QG_ERR_CUDA, "gemv_split: missing scratch");
+    // the kernel splits its tasks with 32-bit products (blockIdx + 1) * tasks
+    if (n <= 0 || n > (1 << 20)) return set_err(QG_ERR_SHAPE, "gemv_split: n must be in [1, 2^20]");
     int grid = 1;
     GemvShape sh = gemv_geometry(QT, false, w0, nullptr, n, k, pro.floats(k), 0, err, &grid);
     const long long tasks = static_cast<long long>(sh.units) * sh.nsl;

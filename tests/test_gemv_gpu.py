@@ -130,8 +130,9 @@ def _planar_slice(nb, b):
 @pytest.mark.parametrize("n,k", [(13, 512), (13, 2560), (21, 3584)])
 def test_q6k_planar_roundtrip_bytes(n, k):
     """The planar (8-row grouped, slice-major) Q6_K layout of qg.h, byte by
-    byte: 1680-byte group-blocks [QL 8x128 | QH 8x64 | scales 8x16 | d 8x2];
-    padding rows are zero."""
+    byte: in each 1680-byte group-block, per row rr and quarter cq (u = 4 rr
+    + cq) a 48-byte record [ql A | ql B | qh] at 48u, the quarter's four
+    scales at 1536 + 4u, d at 1664 + 2 rr; padding rows are zero."""
     nb = k // 256
     t = synth.q6k_tensor(3 + k, n, k)
     p = planar(t).cpu().numpy()
@@ -147,18 +148,21 @@ def test_q6k_planar_roundtrip_bytes(n, k):
             gb = p[off:off + 1680]
             for rr in range(8):
                 r = 8 * g + rr
-                ql, qh = gb[rr * 128:(rr + 1) * 128], gb[1024 + rr * 64:1024 + (rr + 1) * 64]
-                sc, dd = gb[1536 + rr * 16:1536 + (rr + 1) * 16], gb[1664 + rr * 2:1664 + (rr + 1) * 2]
+                recs = [gb[48 * (4 * rr + cq):48 * (4 * rr + cq + 1)] for cq in range(4)]
+                scs = [gb[1536 + 4 * (4 * rr + cq):1536 + 4 * (4 * rr + cq + 1)] for cq in range(4)]
+                dd = gb[1664 + 2 * rr:1666 + 2 * rr]
                 if r >= n:
-                    assert not np.any(ql) and not np.any(qh) and not np.any(sc) and not np.any(dd)
+                    assert not any(np.any(x) for x in recs + scs) and not np.any(dd)
                     continue
                 blk = blocks[r, b]
-                for c in range(4):
-                    half, part = c >> 1, c & 1
-                    assert np.array_equal(ql[32 * c:32 * c + 16], blk[64 * half + 16 * part:64 * half + 16 * part + 16])
-                    assert np.array_equal(ql[32 * c + 16:32 * c + 32],
-                                          blk[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
-                assert np.array_equal(qh, blk[128:192]) and np.array_equal(sc, blk[192:208])
+                ql, qh, sc = blk[:128], blk[128:192], blk[192:208]
+                for cq in range(4):
+                    half, part = cq >> 1, cq & 1
+                    rec = recs[cq]
+                    assert np.array_equal(rec[:16], ql[64 * half + 16 * part:64 * half + 16 * part + 16])
+                    assert np.array_equal(rec[16:32], ql[64 * half + 32 + 16 * part:64 * half + 48 + 16 * part])
+                    assert np.array_equal(rec[32:48], qh[16 * cq:16 * cq + 16])
+                    assert np.array_equal(scs[cq], sc[[8 * half + part + 2 * s for s in range(4)]])
                 assert np.array_equal(dd, blk[208:210])
     assert len(seen) == (n8 // 8) * nb  # every group-block has its own place
 
