@@ -51,7 +51,7 @@ enum { QG_LAYER_DELTANET = 0, QG_LAYER_ATTENTION = 1 };
 /* Shapes of the model (forward_qwen35_cuda.rs, struct Qwen35CudaDims).
  * conv_dim = 2 * n_k_heads * head_k_dim + n_v_heads * head_v_dim.
  * Served: hidden, ffn, n_v_heads*head_v_dim and n_heads*head_dim multiples of
- * 256; head_k_dim == 128; head_v_dim a multiple of 32 up to 128; conv_kernel
+ * 256; head_k_dim == 128; head_v_dim 32, 64 or 128; conv_kernel
  * 2..8; head_dim == 256;
  * n_rot even and <= head_dim; n_v_heads % n_k_heads == 0; n_heads % n_kv_heads
  * == 0 with at most 8 query heads per kv head. */

@@ -129,9 +129,10 @@ int check_config(const qg_config* c) {
             return set_err(QG_ERR_SHAPE, "config: n_v_heads*head_v_dim must be a multiple of 256");
         if (c->conv_kernel < 2 || c->conv_kernel > 8)
             return set_err(QG_ERR_SHAPE, "config: conv_kernel %d (served: 2..8)", c->conv_kernel);
-        if (c->head_v_dim > 128)
-            return set_err(QG_ERR_SHAPE, "config: head_v_dim %d (served: up to 128)", c->head_v_dim);
-        if (c->head_v_dim % 32) return set_err(QG_ERR_SHAPE, "config: head_v_dim %d is not a multiple of 32", c->head_v_dim);
+        // the delta kernel takes 32 value rows per item; the ssm_out prologue
+        // needs whole heads inside each 256-element super-block
+        if (c->head_v_dim != 32 && c->head_v_dim != 64 && c->head_v_dim != 128)
+            return set_err(QG_ERR_SHAPE, "config: head_v_dim %d (served: 32, 64, 128)", c->head_v_dim);
         if (c->n_v_heads > 64) return set_err(QG_ERR_SHAPE, "config: %d value heads (served: up to 64)", c->n_v_heads);
     }
     if (has_attn) {

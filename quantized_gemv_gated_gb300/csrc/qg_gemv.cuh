@@ -157,28 +157,28 @@ __device__ void build_xrep(const Pro& pro, const float* sm, uint8_t* dig, uint8_
                            int lane, int b_lo = 0, int b_hi = -1) {
     const int nsb = b_hi < 0 ? (k >> 8) : b_hi;
     float* units = reinterpret_cast<float*>(aux);
-    // a warp's blocks in batches of 4 whose loads are all issued first, so a
-    // prologue that reads x from global memory pays one round trip per batch
-    for (int bb = b_lo + warp; bb < nsb; bb += 4 * kConsumerWarps) {
-        float xb[4][8];
+    // a warp's blocks in batches of Pro::kBatch whose global loads are all
+    // issued first (load8), so a prologue that reads x from global memory pays
+    // one round trip per batch; value8 then turns them into x (every lane of
+    // the warp calls it: it may reduce across lanes)
+    constexpr int NB = Pro::kBatch;
+    for (int bb = b_lo + warp; bb < nsb; bb += NB * kConsumerWarps) {
+        typename Pro::Raw raw[NB];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < NB; ++t) {
             const int b = bb + t * kConsumerWarps;
-            if (b < nsb)
-                pro.value8(sm, 256 * b + 8 * lane, xb[t]);
+            if (b < nsb) pro.load8(256 * b + 8 * lane, raw[t]);
         }
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < NB; ++t) {
             const int b = bb + t * kConsumerWarps;
             if (b >= nsb) break;
             const int i0 = 256 * b + 8 * lane;
             float x[8];
+            pro.value8(sm, i0, raw[t], x);
             unsigned am = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                x[j] = xb[t][j];
-                am = max(am, __float_as_uint(x[j]) & 0x7fffffffu);
-            }
+            for (int j = 0; j < 8; ++j) am = max(am, __float_as_uint(x[j]) & 0x7fffffffu);
             am = __reduce_max_sync(FULL, am);
             int e = static_cast<int>(am >> 23) - 127;
             e = e < -100 ? -100 : e;
@@ -605,7 +605,9 @@ __device__ void consume_slice(Pipe& p, const GemvShape& sh, int s, int r0, int r
 // Pro: pre(float* sm, int k, int tid) before the dependency wait (inputs no
 //      earlier kernel of the step writes; called by the kernel),
 //      prepare(float* sm, int k, int tid) fills the rest of its scratch,
-//      value8(const float* sm, int i0, float* v) gives x_i0 .. x_i0+7 (i0 % 8 == 0).
+//      load8(i0, Raw&) issues the global loads behind x_i0 .. x_i0+7 (i0 % 8
+//      == 0) and value8(sm, i0, const Raw&, float* v) gives those 8 values;
+//      kBatch: blocks whose loads build_xrep keeps in flight per warp.
 // Epi: pre(r0, r1, tid) before the dependency wait (loads of data no kernel of
 //      the current step writes; called by the kernel), start() after the
 //      prologue, apply(r0, r1, ys, ys2, tid) once over the CTA's row results
@@ -808,13 +810,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape
 // Its 16 scratch floats are the epilogue's reduction space (finish).
 struct ProPlainG {
     const float* x;
+    struct Raw {
+        float4 a, b;
+    };
+    static constexpr int kBatch = 4;
     __host__ __device__ int floats(int) const { return 16; }
     __device__ void pre(float*, int, int) {}
     __device__ void prepare(float*, int, int) {}
-    __device__ void value8(const float*, int i0, float* v) const {
-        const float4 a = ldcg4(x + i0), b = ldcg4(x + i0 + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    __device__ void load8(int i0, Raw& r) const {
+        r.a = ldcg4(x + i0);
+        r.b = ldcg4(x + i0 + 4);
+    }
+    __device__ void value8(const float*, int, const Raw& r, float* v) const {
+        v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+        v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
     }
 };
 
@@ -835,6 +844,8 @@ struct ProRmsNorm {
     int kdim;  // = k
     int y_parts, y_stride;
     float r;
+    struct Raw {};  // x is staged in shared memory by prepare
+    static constexpr int kBatch = 4;
     __host__ __device__ int floats(int k) const { return 2 * k + 32; }
     // the norm weights do not depend on the previous kernel: staged before its wait
     __device__ void pre(float* sm, int k, int tid) {
@@ -879,7 +890,8 @@ struct ProRmsNorm {
         for (int i = 0; i < kConsumerWarps; ++i) tot += red[i];
         r = 1.0f / sqrtf(tot / static_cast<float>(k) + eps);
     }
-    __device__ void value8(const float* sm, int i0, float* v) const {
+    __device__ void load8(int, Raw&) const {}
+    __device__ void value8(const float* sm, int i0, const Raw&, float* v) const {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const float4 a = *reinterpret_cast<const float4*>(sm + i0 + 4 * h);

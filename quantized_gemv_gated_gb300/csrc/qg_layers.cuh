@@ -148,54 +148,45 @@ struct EpiArgmaxStep : EpiBase {
 // ------------------------------------------------------------ prologues
 // x = gated RMSNorm of the delta-rule output (gdn_gated_rmsnorm_into):
 // u_i = (o_i * rn_h) * w_j * silu(z_i), i = h dv + j, with rn_h = 1 /
-// sqrt(mean_j o^2 + eps).  o and z are staged in shared memory; the sum of
-// squares of a head is taken in the order of the per-head delta kernel:
-// eight partial sums over consecutive runs of dv/8 rows, each a sequential
-// fma chain, then added in run order.
-constexpr int kMaxGatedHeads = 64;
+// sqrt(mean_j o^2 + eps).  dv divides 256, so a super-block holds whole heads:
+// the warp that turns a super-block into digits loads its o and z itself and
+// the dv/8 lanes of a head (8 values each) reduce the head's sum of squares
+// with an xor tree.  Only the norm weights are staged (before the wait).
 struct ProGatedNorm {
     const float* o;
     const float* z;
     const float* w;
-    int nv, dv, vk;
+    int nv, dv;
     float eps;
-    // [rn per head | run partials | w (dv <= 128) | o | z]
-    __host__ __device__ int floats(int k) const { return kMaxGatedHeads * 9 + 128 + 2 * k; }
+    struct Raw {
+        float4 oa, ob, za, zb;
+    };
+    static constexpr int kBatch = 2;
+    __host__ __device__ int floats(int) const { return 128 + 16; }  // w (dv <= 128); scratch
     __device__ void pre(float* sm, int, int tid) {  // the norm weights: before the dependency wait
-        for (int i = tid; i < dv; i += kConsumers) sm[9 * kMaxGatedHeads + i] = __ldg(w + i);
+        for (int i = tid; i < dv; i += kConsumers) sm[i] = __ldg(w + i);
     }
-    __device__ void prepare(float* sm, int k, int tid) {
-        vk = k;
-        float* part = sm + kMaxGatedHeads;
-        float* os = sm + 9 * kMaxGatedHeads + 128;
-        float* zs = os + k;
-#pragma unroll 4
-        for (int i = 4 * tid; i < k; i += 4 * kConsumers) {
-            *reinterpret_cast<float4*>(os + i) = ldcg4(o + i);
-            *reinterpret_cast<float4*>(zs + i) = ldcg4(z + i);
-        }
-        bar_sync(1, kConsumers);
-        const int rpw = dv / 8;
-        for (int r = tid; r < 8 * nv; r += kConsumers) {
-            const float* v = os + (r >> 3) * dv + (r & 7) * rpw;
-            float ss = 0.0f;
-            for (int i = 0; i < rpw; ++i) ss = fmaf(v[i], v[i], ss);
-            part[r] = ss;
-        }
-        bar_sync(1, kConsumers);
-        for (int h = tid; h < nv; h += kConsumers) {
-            float tot = 0.0f;
-            for (int r = 0; r < 8; ++r) tot += part[8 * h + r];
-            sm[h] = 1.0f / sqrtf(tot / static_cast<float>(dv) + eps);
-        }
+    __device__ void prepare(float*, int, int) {}
+    __device__ void load8(int i0, Raw& r) const {
+        r.oa = ldcg4(o + i0);
+        r.ob = ldcg4(o + i0 + 4);
+        r.za = ldcg4(z + i0);
+        r.zb = ldcg4(z + i0 + 4);
     }
-    __device__ void value8(const float* sm, int i0, float* v) const {
-        const int h = i0 / dv, j0 = i0 - h * dv;  // dv % 8 == 0: the 8 elements share a head
-        const float* ws = sm + 9 * kMaxGatedHeads;
-        const float* os = ws + 128;
-        const float rn = sm[h];
+    __device__ void value8(const float* sm, int i0, const Raw& r, float* v) const {
+        const float ov[8] = {r.oa.x, r.oa.y, r.oa.z, r.oa.w, r.ob.x, r.ob.y, r.ob.z, r.ob.w};
+        const float zv[8] = {r.za.x, r.za.y, r.za.z, r.za.w, r.zb.x, r.zb.y, r.zb.z, r.zb.w};
+        float ss = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = ((os[i0 + t] * rn) * ws[j0 + t]) * silu(os[vk + i0 + t]);
+        for (int j = 0; j < 8; ++j) ss = fmaf(ov[j], ov[j], ss);
+        const int lanes = dv >> 3;  // lanes per head
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            if (off < lanes) ss += __shfl_xor_sync(FULL, ss, off);
+        const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
+        const int j0 = i0 & (dv - 1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = ((ov[j] * rn) * sm[j0 + j]) * silu(zv[j]);
     }
 };
 

@@ -517,8 +517,6 @@ int step_setup(const qg_model* m, qg_state* s) {
     for (int il = 0; il < c.n_layers; ++il) (m->kinds[il] == QG_LAYER_DELTANET ? has_dn : has_attn) = true;
     if (has_attn && gs != 1 && gs != 2 && gs != 4)
         return set_err(QG_ERR_SHAPE, "step kernel: %d query heads per kv head (served: 1, 2, 4)", gs);
-    if (has_dn && c.n_v_heads > kMaxGatedHeads)
-        return set_err(QG_ERR_SHAPE, "step kernel: %d value heads (at most %d)", c.n_v_heads, kMaxGatedHeads);
     int dev = 0, sms = 0, coop = 0;
     QG_CUDA(cudaGetDevice(&dev));
     QG_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
