@@ -66,3 +66,17 @@ def test_ctypes_structs_match_header_layout(tmp_path):
             assert getattr(py[s], f).offset == int(val), key
         else:
             assert ctypes.sizeof(py[key]) == int(val), key
+
+
+def test_config_rejects_value_heads_straddling_superblocks():
+    """head_v_dim must divide 256 (the ssm_out prologue reduces each head's
+    sum of squares inside one 256-element super-block): 96 is refused by the
+    host-side check before any device work."""
+    import dataclasses
+    import synth
+    import quantized_gemv_gated_gb300 as qg
+    cfg = dataclasses.replace(synth.CFG_TINY, name="tiny-dv96", head_v_dim=96, n_v_heads=8)
+    w = synth.make_model_weights(cfg)
+    with pytest.raises(qg.QgError) as e:
+        qg.Model(w)
+    assert e.value.code == qg.QG_ERR_SHAPE and "head_v_dim" in qg.qg_last_error()
