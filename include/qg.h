@@ -161,6 +161,20 @@ int qg_state_kv_len(const qg_state* s, int* kv_len);
  * state), e.g. to record timing events around qg_decode_greedy. */
 int qg_state_stream(const qg_state* s, qg_stream* out);
 int qg_state_stats(const qg_state* s, qg_stats* out);
+/* Token mask of the whole-token calls (the decode session's grammar mask,
+ * applied between the lm_head GEMV and the in-graph argmax): `allow` is a
+ * packed bitset of ceil(vocab/32) words, HOST memory; token i may be chosen
+ * iff bit (i & 31) of allow[i >> 5] is set.  The logit of every other token
+ * is replaced by -FLT_MAX before the first-index argmax (so with every token
+ * banned the result is 0).  The mask lives in the state at a fixed device
+ * address that the captured step reads on every replay: setting it takes
+ * effect from the next step, needs no recapture and allocates nothing; the
+ * copy is ordered with the state's steps and complete when the call returns.
+ * n_words = 0 (allow may be NULL) clears the mask; qg_state_create and
+ * qg_state_reset start with no mask.  Errors: QG_ERR_SHAPE when n_words is
+ * neither 0 nor ceil(vocab/32), QG_ERR_ARG for a NULL state or mask. */
+int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
+
 /* How the whole-token calls (qg_decode_token, qg_decode_greedy) run a step:
  * QG_STEP_KERNELS (the default): one kernel per fused op, chained with
  * programmatic dependent launch inside the step's CUDA graph;

@@ -293,6 +293,19 @@ def argmax(x) -> int:
     return int(lib().or_argmax(ptr(x), x.size))
 
 
+def argmax_masked(x, allow_words) -> int:
+    """First-index argmax under the decode session's grammar mask (memra
+    decode.rs, GraphSession mask_dev / decode_step_dc_cap_masked): a token
+    whose bit (i & 31 of word i >> 5) is unset in the packed allow bitset has
+    its logit replaced by -FLT_MAX before the argmax reads the row."""
+    x = f32(x).copy()
+    words = np.asarray(allow_words, dtype=np.uint32)
+    i = np.arange(x.size)
+    allowed = (words[i >> 5] >> (i & 31).astype(np.uint32)) & np.uint32(1)
+    x[allowed == 0] = -np.finfo(np.float32).max
+    return argmax(x)
+
+
 def top2(x):
     x = f32(x)
     a, b = ctypes.c_float(), ctypes.c_float()

@@ -27,7 +27,8 @@ ERROR_NAMES = {0: "QG_OK", -1: "QG_ERR_SHAPE", -2: "QG_ERR_QTYPE", -3: "QG_ERR_E
 EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
-    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_step_mode", "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
+    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_step_mode", "qg_state_set_token_mask",
+    "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
     "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
@@ -109,6 +110,7 @@ def lib():
             "qg_state_stream": [p, ctypes.POINTER(p)],
             "qg_state_stats": [p, ctypes.POINTER(QgStats)],
             "qg_state_set_step_mode": [p, i],
+            "qg_state_set_token_mask": [p, p, i],
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
             "qg_q6k_to_planar": [p, p, i, i, p],
@@ -347,6 +349,16 @@ class State:
     def set_step_mode(self, mode):
         """STEP_KERNELS (default) or STEP_PERSISTENT (qg_state_set_step_mode)."""
         _check(lib().qg_state_set_step_mode(self.handle, int(mode)))
+
+    def set_token_mask(self, allow_words=None):
+        """Token mask of the whole-token calls (qg_state_set_token_mask):
+        `allow_words` a uint32 array of ceil(vocab/32) words, bit i & 31 of
+        word i >> 5 set = token i allowed; None clears it."""
+        if allow_words is None:
+            _check(lib().qg_state_set_token_mask(self.handle, None, 0))
+            return
+        a = np.ascontiguousarray(allow_words, dtype=np.uint32)
+        _check(lib().qg_state_set_token_mask(self.handle, a.ctypes.data, int(a.size)))
 
 
 def qg_deltanet_step(model, state, il, hidden, stream=None):

@@ -579,6 +579,7 @@ int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, c
     ea.slots = s->slots;
     ea.hist = s->hist;
     ea.err = s->err;
+    ea.allow = s->allow;
     ea.advance = advance ? 1 : 0;
     return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden,
                                       norm_pro(a, s, true, m->out_norm, nullptr, h_final, c.eps, c.hidden), ea, st, true,

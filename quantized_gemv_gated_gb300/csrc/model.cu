@@ -413,6 +413,7 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                (rc = dalloc(s->allocs, &s->attn_count, c.n_kv_heads + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->am_ws, 2, cnt)) || (rc = dalloc(s->allocs, &s->slots, 4, cnt)) ||
                (rc = dalloc(s->allocs, &s->hist, max_seq_len, cnt)) || (rc = dalloc(s->allocs, &s->err, 1, cnt)) ||
+               (rc = dalloc(s->allocs, &s->allow, (static_cast<size_t>(c.vocab) + 31) / 32, cnt)) ||
                (rc = dalloc(s->allocs, &s->gbar, 4, cnt)) ||
                (rc = dalloc(s->allocs, &s->kpart,
                             static_cast<size_t>(std::max({gemv_slices(c.ffn), gemv_slices(m->v_dim > 0 ? m->v_dim : 256),
@@ -486,6 +487,7 @@ int qg_state_reset(qg_state* s) {
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
     QG_CUDA(cudaMemset(s->err, 0, sizeof(unsigned)));
     QG_CUDA(cudaMemset(s->gbar, 0, 4 * sizeof(unsigned)));
+    QG_CUDA(cudaMemset(s->allow, 0xff, sizeof(uint32_t) * ((static_cast<size_t>(c.vocab) + 31) / 32)));  // no mask
     QG_CUDA(cudaDeviceSynchronize());
     s->kv_len = 0;
     return QG_OK;
@@ -560,6 +562,23 @@ int qg_state_download_hidden(qg_state* s, float* hidden_host) {
 int qg_state_kv_len(const qg_state* s, int* kv_len) {
     if (!s || !kv_len) return set_err(QG_ERR_ARG, "kv_len: NULL argument");
     *kv_len = s->kv_len;
+    return QG_OK;
+}
+
+int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words) {
+    if (!s) return set_err(QG_ERR_ARG, "set_token_mask: NULL state");
+    const int words = (s->m->cfg.vocab + 31) / 32;
+    if (n_words != 0 && n_words != words)
+        return set_err(QG_ERR_SHAPE, "set_token_mask: %d words (the vocabulary needs %d, or 0 to clear)", n_words,
+                       words);
+    if (n_words && !allow) return set_err(QG_ERR_ARG, "set_token_mask: NULL mask");
+    DeviceGuard dg(s->m->device);
+    // in stream order with the steps, and done before returning: the caller may free `allow`
+    if (n_words)
+        QG_CUDA(cudaMemcpyAsync(s->allow, allow, sizeof(uint32_t) * words, cudaMemcpyHostToDevice, s->stream));
+    else
+        QG_CUDA(cudaMemsetAsync(s->allow, 0xff, sizeof(uint32_t) * words, s->stream));
+    QG_CUDA(cudaStreamSynchronize(s->stream));
     return QG_OK;
 }
 

@@ -60,6 +60,7 @@ struct qg_state {
     unsigned long long* am_ws;  // lm_head argmax workspace (left at 0)
     int* slots;                 // device: [0] token in, [1] position, [2] token out (bit 31: device error)
     uint32_t* hist;             // device: greedy token per position [max_seq]
+    uint32_t* allow;            // device: token mask, ceil(vocab/32) words, bit set = allowed (all set: none)
     unsigned* err;              // device error word
     int* pinned;                // pinned host: [0] token, [1] position, [2] token out
     int keys_per_split, max_splits;

@@ -2,6 +2,8 @@
 // kernel: the epilogues of the fused input projections and of the lm_head
 // argmax, the delta-rule row update, and the attention row helpers.
 #pragma once
+#include <cfloat>
+
 #include "qg_internal.cuh"
 
 namespace qg {
@@ -101,18 +103,23 @@ struct EpiAttnIn : EpiBase {
 
 // lm_head argmax of the whole-token step: publishes the token to slots[0]
 // (the next step's embedding input) and slots[2] (the host readback, with
-// bit 31 set when any kernel of the step set the device error word).
+// bit 31 set when any kernel of the step set the device error word).  allow:
+// the token mask (bit i & 31 of word i >> 5 set = token i allowed); a banned
+// token's logit is replaced by -FLT_MAX before the first-index argmax, as
+// the decode session's grammar mask does before its in-graph argmax.
 struct EpiArgmaxStep : EpiBase {
     unsigned long long* ws;
     int* slots;
     uint32_t* hist;
     const unsigned* err;
+    const uint32_t* allow;
     int advance;
     unsigned long long best;
     __device__ void start() { best = 0ull; }
     __device__ void apply(int r0, int r1, const float* ys, const float*, int tid) {
         for (int r = r0 + tid; r < r1; r += kConsumers) {
-            const unsigned long long key = argmax_key(ys[r - r0], static_cast<unsigned>(r));
+            const bool ok = (__ldcg(allow + (r >> 5)) >> (r & 31)) & 1u;
+            const unsigned long long key = argmax_key(ok ? ys[r - r0] : -FLT_MAX, static_cast<unsigned>(r));
             best = key > best ? key : best;
         }
     }

@@ -50,6 +50,7 @@ struct StepParams {
     unsigned long long* am_ws;
     int* slots;
     uint32_t* hist;
+    const uint32_t* allow;
     unsigned* err;
     unsigned* gbar;  // [0] barrier arrivals, [1] CTAs finished, [2] abort (all zero between steps)
     int advance;     // greedy: record hist[pos] and move the position slot

@@ -453,6 +453,7 @@ __device__ void consumer_main(Consumer& c, const StepParams& P, int pos) {
     ea.slots = P.slots;
     ea.hist = P.hist;
     ea.err = P.err;
+    ea.allow = P.allow;
     ea.advance = P.advance;
     consume_gemv<QT_Q6K, false>(c, P.geo[SG_LMHEAD], step_norm(A, P.y, P.out_norm, nullptr, P.h, P), ea);
     // the last CTA out re-arms the barrier words for the next step
@@ -634,6 +635,7 @@ int step_setup(const qg_model* m, qg_state* s) {
     P.am_ws = s->am_ws;
     P.slots = s->slots;
     P.hist = s->hist;
+    P.allow = s->allow;
     P.err = s->err;
     P.gbar = s->gbar;
     return QG_OK;

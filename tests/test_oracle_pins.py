@@ -500,6 +500,46 @@ def test_argmax_inf_nan_and_signed_zero():
     assert (a, b) == (5.0, 5.0)
 
 
+def _allow(n, allowed):
+    """Packed allow bitset of n tokens with exactly the ids in `allowed` set."""
+    w = np.zeros((n + 31) // 32, np.uint32)
+    for i in allowed:
+        w[i >> 5] |= np.uint32(1) << np.uint32(i & 31)
+    return w
+
+
+def test_masked_argmax_hand_cases():
+    """The grammar mask: banned logits become -FLT_MAX before the first-index
+    argmax (values worked by hand)."""
+    x = np.array([3.0, 1.0, 3.0, 2.0], np.float32)
+    assert oracle.argmax_masked(x, _allow(4, range(4))) == 0   # no ban: first of the tied maxima
+    assert oracle.argmax_masked(x, _allow(4, [1, 2, 3])) == 2  # the first maximum banned
+    assert oracle.argmax_masked(x, _allow(4, [1, 3])) == 3     # both maxima banned
+    assert oracle.argmax_masked(x, _allow(4, [1])) == 1        # one token allowed
+    assert oracle.argmax_masked(x, _allow(4, [])) == 0         # all banned: all -FLT_MAX, first index
+    # -FLT_MAX (a banned id) is above -inf: an allowed -inf logit loses to the first banned id
+    assert oracle.argmax_masked(np.array([5.0, -np.inf], np.float32), _allow(2, [1])) == 0
+    # an allowed NaN never wins; ids beyond n in the last word are ignored
+    y = np.full(40, -1.0, np.float32)
+    y[33], y[38] = np.nan, 0.5
+    assert oracle.argmax_masked(y, _allow(40, [33, 38])) == 38
+    assert oracle.argmax_masked(y, _allow(40, [33, 38]) | np.array([0, 0xFFFFFF00], np.uint32)) == 38
+
+
+def test_masked_argmax_equals_argmax_over_allowed_ids():
+    """On finite logits the mask is the argmax over the allowed ids alone
+    (brute force on random cases)."""
+    rng = np.random.default_rng(71)
+    for _ in range(50):
+        n = int(rng.integers(1, 300))
+        x = rng.standard_normal(n).astype(np.float32)
+        keep = np.flatnonzero(rng.random(n) < 0.3)
+        if keep.size == 0:
+            continue
+        want = keep[np.argmax(x[keep])]  # numpy's argmax is first-index too
+        assert oracle.argmax_masked(x, _allow(n, keep)) == want
+
+
 # ---------------------------------------------------- layers and whole token
 
 def _zero(t):
