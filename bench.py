@@ -17,6 +17,7 @@ the chosen workload.  Default workload: the 0.8B-shaped hybrid (24 layers,
 
   python bench.py [--workload 0.8b|4b|4b-long] [--steps K] [--warmup W]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+  python bench.py --kernels              (GEMV building blocks, one line per shape)
 Multi-GPU: torchrun --nproc-per-node N bench.py --gpus N: N independent
 replicas (weak scaling, no collective on the data path).
 """
@@ -354,6 +355,79 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+# GEMV shapes of the kernel mode: the building blocks at the model's shapes
+# (planar layouts, the layers' own path), lm_head with its fused argmax.
+KERNEL_SHAPES = [
+    ("q4k", 1024, 1024), ("q4k", 6144, 1024), ("q4k", 8224, 1024), ("q4k", 7168, 1024),
+    ("q4k", 12352, 2560), ("q4k", 9216, 2560), ("q6k", 1024, 3584), ("q6k", 2560, 9216),
+    ("lmhead", 248320, 1024), ("lmhead", 248320, 2560),
+]
+
+
+def run_kernels(args):
+    """One JSON line per GEMV shape: device time per launch in a graph of
+    back-to-back launches (chained by programmatic dependent launch, as in the
+    decode step) that rotate through enough weight copies to exceed 3x the
+    129 MB L2, so every launch streams its weights from HBM."""
+    import torch
+    import quantized_gemv_gated_gb300 as qg
+    peak, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    for kind, n, k in KERNEL_SHAPES:
+        make = synth.q4k_tensor if kind == "q4k" else synth.q6k_tensor
+        t = make(synth.subseed(synth.MASTER_SEED, f"kernel.{kind}.{n}.{k}"), n, k)
+        src = torch.from_numpy(t.data).cuda()
+        nbytes = (qg.qg_q4k_planar_bytes if kind == "q4k" else qg.qg_q6k_planar_bytes)(n, k)
+        copies = max(2, -(-3 * 129 * 2 ** 20 // nbytes))
+        ws = []
+        for _ in range(copies):
+            w = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            (qg.qg_q4k_to_planar if kind == "q4k" else qg.qg_q6k_to_planar)(src, w, n, k)
+            ws.append(w)
+        del src
+        x = torch.from_numpy(synth.normal(synth.subseed(synth.MASTER_SEED, f"kernel.x.{k}"), k)).cuda()
+        y = torch.empty(n, dtype=torch.float32, device="cuda")
+        tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsp = torch.zeros(2, dtype=torch.int64, device="cuda")
+
+        def launch(w, st):
+            if kind == "q4k":
+                qg.qg_gemv_q4k_planar(w, x, y, n, k, st)
+            elif kind == "q6k":
+                qg.qg_gemv_q6k(w, x, y, n, k, st)
+            else:
+                qg.qg_lmhead_argmax(w, x, n, k, wsp, tok, st)
+
+        with torch.cuda.stream(stream):
+            for w in ws[:3]:
+                launch(w, stream.cuda_stream)  # eager first launches set the kernels' attributes
+        stream.synchronize()
+        reps = max(copies, 64)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                launch(ws[r % copies], stream.cuda_stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(max(1, args.steps // 16)):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        qg.qg_device_status()
+        us = e0.elapsed_time(e1) * 1e3 / (max(1, args.steps // 16) * reps)
+        algo = nbytes + 4 * k + (4 if kind == "lmhead" else 4 * n)
+        gbs = algo / us / 1e3
+        print(json.dumps({"kernel": f"{kind} {n}x{k}", "layout": "planar (grouped, slice-major)",
+                          "us_per_launch": round(us, 3), "bytes_per_launch": algo, "GB/s": round(gbs, 1),
+                          "frac_of_peak": round(gbs / peak, 4), "peak_GB/s": peak, "peak_kind": peak_kind,
+                          "weight_copies": copies, "launches_per_graph": reps}), flush=True)
+        del ws, g
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,11 +441,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
     ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
                     help="whole-token step: one kernel per fused op, or one persistent launch")
+    ap.add_argument("--kernels", action="store_true",
+                    help="instead of the decode step: one JSON line per GEMV building block at the model's shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         args.steps = min(args.steps, 16)  # bounded sample of the CPU oracle
+    if args.kernels:
+        run_kernels(args)
+        return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, rank, world)

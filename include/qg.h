@@ -202,6 +202,20 @@ int qg_state_set_step_mode(qg_state* s, int mode);
  * QG_ERR_EMPTY. */
 int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream stream);
 
+/* Planar Q4_K, the layout the model's Q4_K projections are streamed from:
+ * n8 = n rounded up to 8 rows, nb = k/256; for every 8-row group g and
+ * super-block b one 1152-byte group-block holding the 8 rows' GGUF blocks of
+ * super-block b in row order (144 bytes each; rows n..n8-1 zero), stored
+ * slice-major as the planar Q6_K below: group-block (g, b) at
+ * ((n8/8)*b0 + g*kb + (b - b0))*1152 for the slice [b0, b0 + kb) holding b.
+ * qg_q4k_planar_bytes gives the size (n8*nb*144, 0 for a bad shape);
+ * qg_q4k_to_planar repacks a raw GGUF tensor (both device pointers, dst
+ * 16-byte aligned); qg_gemv_q4k_planar is qg_gemv_q4k on that layout, the
+ * model's own GEMV path. */
+size_t qg_q4k_planar_bytes(int n, int k);
+int qg_q4k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream);
+int qg_gemv_q4k_planar(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream);
+
 /* The same for Q6_K in the library's planar layout (made by qg_q6k_to_planar). */
 int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream);
 

@@ -28,7 +28,8 @@ EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
     "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_step_mode", "qg_state_set_token_mask",
-    "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes",
+    "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes", "qg_q4k_planar_bytes", "qg_q4k_to_planar",
+    "qg_gemv_q4k_planar",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
     "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
@@ -114,6 +115,8 @@ def lib():
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
             "qg_q6k_to_planar": [p, p, i, i, p],
+            "qg_q4k_to_planar": [p, p, i, i, p],
+            "qg_gemv_q4k_planar": [p, p, p, i, i, p],
             "qg_lmhead_argmax": [p, p, i, i, p, p, p],
             "qg_lmhead_argmax_noalloc": [p, p, i, i, p, p],
             "qg_argmax_f32": [p, i, p, p],
@@ -132,6 +135,8 @@ def lib():
             fn.restype = i
         L.qg_q6k_planar_bytes.argtypes = [i, i]
         L.qg_q6k_planar_bytes.restype = sz
+        L.qg_q4k_planar_bytes.argtypes = [i, i]
+        L.qg_q4k_planar_bytes.restype = sz
         L.qg_lmhead_argmax_workspace_bytes.argtypes = []
         L.qg_lmhead_argmax_workspace_bytes.restype = sz
         L.qg_last_error.argtypes = []
@@ -182,6 +187,18 @@ def qg_gemv_q4k(w, x, y, n, k, stream=None):
 
 def qg_gemv_q6k(w_planar, x, y, n, k, stream=None):
     return _check(lib().qg_gemv_q6k(_dev(w_planar), _dev(x), _dev(y), n, k, _stream(stream)))
+
+
+def qg_gemv_q4k_planar(w_planar, x, y, n, k, stream=None):
+    return _check(lib().qg_gemv_q4k_planar(_dev(w_planar), _dev(x), _dev(y), n, k, _stream(stream)))
+
+
+def qg_q4k_planar_bytes(n, k):
+    return int(lib().qg_q4k_planar_bytes(n, k))
+
+
+def qg_q4k_to_planar(src, dst, n, k, stream=None):
+    return _check(lib().qg_q4k_to_planar(_dev(src), _dev(dst), n, k, _stream(stream)))
 
 
 def qg_q6k_planar_bytes(n, k):

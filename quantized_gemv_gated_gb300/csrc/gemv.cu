@@ -227,6 +227,28 @@ int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg
                                       reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 
+int qg_gemv_q4k_planar(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream) {
+    int rc = check_gemv_args(w_planar, x, y, n, k);
+    if (rc) return rc;
+    EpiStore epi{};
+    epi.y = y;
+    return launch_gemv<QT_Q4K, false>(w_planar, nullptr, n, k, ProPlainG{x}, epi,
+                                      reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
+}
+
+size_t qg_q4k_planar_bytes(int n, int k) {
+    if (n <= 0 || k <= 0 || k % 256) return 0;
+    return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 144;
+}
+
+int qg_q4k_to_planar(const void* src, void* dst, int n, int k, qg_stream stream) {
+    if (!src || !dst) return set_err(QG_ERR_ARG, "q4k_to_planar: NULL pointer");
+    if (n <= 0 || k <= 0) return set_err(QG_ERR_EMPTY, "q4k_to_planar: empty tensor n=%d k=%d", n, k);
+    if (k % 256) return set_err(QG_ERR_SHAPE, "q4k_to_planar: k=%d is not a multiple of 256", k);
+    if (!aligned16(dst)) return set_err(QG_ERR_ARG, "q4k_to_planar: dst must be 16-byte aligned");
+    return q4k_to_grouped(src, dst, n, k, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t qg_q6k_planar_bytes(int n, int k) {
     if (n <= 0 || k <= 0 || k % 256) return 0;
     return static_cast<size_t>((n + 7) & ~7) * (k / 256) * 210;

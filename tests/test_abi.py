@@ -38,6 +38,8 @@ def test_host_only_entry_points_without_gpu():
     import quantized_gemv_gated_gb300 as qg
     assert qg.qg_q6k_planar_bytes(13, 512) == 16 * 2 * 210
     assert qg.qg_q6k_planar_bytes(8, 300) == 0
+    assert qg.qg_q4k_planar_bytes(13, 512) == 16 * 2 * 144
+    assert qg.qg_q4k_planar_bytes(8, 300) == 0
     assert qg.qg_lmhead_argmax_workspace_bytes() == 16
     with pytest.raises(qg.QgError) as e:
         qg.qg_gemv_q4k(0, 0, 0, 4, 256)

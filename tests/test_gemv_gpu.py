@@ -251,3 +251,54 @@ def test_gemv_argument_errors():
     with pytest.raises(qg.QgError) as e:
         qg.qg_gemv_q4k(w.data_ptr() + 4, x, y, 1, 256)
     assert e.value.code == qg.QG_ERR_ARG
+
+
+def planar4(t):
+    """Device planar copy of a synth Q4_K tensor (through the library's repack)."""
+    src = dev(t.data)
+    dst = torch.empty(qg.qg_q4k_planar_bytes(t.n, t.k), dtype=torch.uint8, device="cuda")
+    qg.qg_q4k_to_planar(src, dst, t.n, t.k)
+    return dst
+
+
+@pytest.mark.parametrize("n,k", [(13, 512), (13, 2560), (21, 3584)])
+def test_q4k_planar_roundtrip_bytes(n, k):
+    """The planar Q4_K layout of qg.h byte by byte: 1152-byte group-blocks of
+    the 8 rows' GGUF blocks in row order, slice-major; padding rows zero."""
+    nb = k // 256
+    t = synth.q4k_tensor(5 + k, n, k)
+    p = planar4(t).cpu().numpy()
+    n8 = (n + 7) // 8 * 8
+    assert p.size == n8 * nb * 144 == qg.qg_q4k_planar_bytes(n, k)
+    blocks = t.data.reshape(n, nb, 144)
+    seen = set()
+    for g in range(n8 // 8):
+        for b in range(nb):
+            b0, kb = _planar_slice(nb, b)
+            off = ((n8 // 8) * b0 + g * kb + (b - b0)) * 1152
+            seen.add(off)
+            for rr in range(8):
+                r = 8 * g + rr
+                got = p[off + 144 * rr:off + 144 * (rr + 1)]
+                if r >= n:
+                    assert not np.any(got)
+                else:
+                    assert np.array_equal(got, blocks[r, b])
+    assert len(seen) == (n8 // 8) * nb
+
+
+@pytest.mark.parametrize("n,k", SMALL + [(6144, 1024), (9216, 2560)])
+def test_gemv_q4k_planar_matches_raw_and_oracle(n, k):
+    """The model's Q4_K GEMV path (planar layout) inside the oracle's error
+    bound, and bitwise equal to the raw-layout building block (the same
+    arithmetic in the same order, only the bytes' placement differs)."""
+    t = synth.q4k_tensor(synth.subseed(synth.MASTER_SEED, f"q4p.{n}.{k}"), n, k)
+    x = synth.normal(synth.subseed(synth.MASTER_SEED, f"q4p.x.{k}"), k)
+    y = torch.empty(n, dtype=torch.float32, device="cuda")
+    qg.qg_gemv_q4k_planar(planar4(t), dev(x), y, n, k)
+    torch.cuda.synchronize()
+    qg.qg_device_status()
+    yp = y.cpu().numpy()
+    assert np.array_equal(yp, run_gemv(t, x))
+    if n * k <= 4_000_000:
+        check_against_oracle(t, x, yp)
