@@ -641,6 +641,12 @@ __device__ void gemv_consume(Pipe& p, const GemvShape& sh, int r0, int r1, Pro& 
 }
 
 // ------------------------------------------------------------- the kernel
+// The two engine kernels (and their launchers) have internal linkage: every
+// translation unit registers its own device copy of a kernel it instantiates,
+// so an instantiation shared by two units must not be merged into one host
+// stub whose shared-memory attribute was set on the other unit's copy.
+namespace {
+
 template <int QT, int LAYOUT, bool DUAL, class Pro, class Epi>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, const Pro pro_in, const Epi epi_in) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -673,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvShape sh, c
     pdl_wait();
     gemv_consume<QT, LAYOUT, DUAL>(p, sh, r0, r1, pro, epi, smem, tid);
 }
+
+}  // namespace
 
 // ------------------------------------------------------------ split-K mode
 // For GEMVs with few rows and several K slices (ffn_down, the output
@@ -776,6 +784,8 @@ __device__ void gemv_split_consume(Pipe& p, const GemvShape& sh, Pro& pro, uint8
     }
 }
 
+namespace {
+
 template <int QT, class Pro>
 __global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape sh, const Pro pro_in) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -803,6 +813,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_split_kernel(const GemvShape
     pdl_wait();
     gemv_split_consume<QT>(p, sh, pro, smem, tid);
 }
+
+}  // namespace
 
 // ------------------------------------------------------------- prologues
 // x read straight from global memory by build_xrep (written by an earlier

@@ -79,6 +79,8 @@ inline int gemv_smem(const GemvShape& sh, int qt, bool dual) {
     return off_ring(qt, sh.k, sh.pro_floats, (dual ? 2 : 1) * sh.rows_cta) + sh.stages * sh.pp * stage_bytes_of(qt);
 }
 
+namespace {  // per translation unit, like the kernels they launch and configure
+
 // Launch one GEMV-engine kernel on `st` (with programmatic stream
 // serialisation when `pdl`, so the weights of this launch stream in while the
 // previous kernel on the stream finishes).  err: the device error word, which
@@ -162,6 +164,8 @@ int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, cudaStream_t
     QG_CUDA(cudaLaunchKernelEx(&cfg, kern, sh, pro));
     return QG_OK;
 }
+
+}  // namespace
 
 // Plain launch of a non-engine kernel with the PDL attribute.
 template <class... KArgs, class... Args>

@@ -135,6 +135,33 @@ def test_attention_layer_positions(base, max_seq, positions):
     qg.qg_device_status()
 
 
+def test_public_gemv_then_attention_layer():
+    """The public planar Q4_K GEMV and the attention output projection run the
+    same engine kernel template (Q4_K, plain x, stored y).  A large public call
+    first (a deep ring: more than the default 48 KB of dynamic shared memory),
+    then the single-slice output projection of a small attention layer: each
+    caller launches the kernel copy it configured, whatever ran before."""
+    n, k = 9216, 2560
+    t = synth.q4k_tensor(synth.subseed(synth.MASTER_SEED, "order.q4k"), n, k)
+    src = dev(t.data)
+    wp = torch.empty(qg.qg_q4k_planar_bytes(n, k), dtype=torch.uint8, device="cuda")
+    qg.qg_q4k_to_planar(src, wp, n, k)
+    x = dev(synth.normal(synth.subseed(synth.MASTER_SEED, "order.x"), k))
+    y = torch.empty(n, device="cuda")
+    qg.qg_gemv_q4k_planar(wp, x, y, n, k)
+    torch.cuda.synchronize()
+    cfg = _attn_cfg(synth.CFG_TINY, 96)
+    w = synth.make_model_weights(cfg)
+    m, om = qg.Model(w), oracle.Model(w)
+    st, ost = qg.State(m, 96), oracle.State(om)
+    xa = synth.normal(synth.subseed(synth.MASTER_SEED, "order.h"), cfg.hidden)
+    h = dev(xa)
+    qg.qg_attn_decode_step(m, st, 0, h, 0)
+    assert rel(h.cpu().numpy(), oracle.attention_layer(om, ost, 0, xa, 0)) <= TOL
+    st.close()
+    qg.qg_device_status()
+
+
 @pytest.fixture(scope="module")
 def tiny():
     cfg = synth.CFG_TINY
