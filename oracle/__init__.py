@@ -69,7 +69,9 @@ class OrModel(ctypes.Structure):
 
 class OrState(ctypes.Structure):
     _fields_ = [("conv", ctypes.POINTER(_FP)), ("ssm", ctypes.POINTER(_FP)),
-                ("kc", ctypes.POINTER(_FP)), ("vc", ctypes.POINTER(_FP)), ("kv_len", ctypes.c_int)]
+                ("kc", ctypes.POINTER(_FP)), ("vc", ctypes.POINTER(_FP)), ("kv_len", ctypes.c_int),
+                ("kv_format", ctypes.c_int), ("kq", ctypes.POINTER(ctypes.c_void_p)),
+                ("vq", ctypes.POINTER(ctypes.c_void_p))]
 
 
 def lib():
@@ -105,6 +107,13 @@ def lib():
             "or_rope_neox": (None, [p, i, i, i, i, f]),
             "or_attention": (None, [p, p, p, p, i, i, i, i]),
             "or_sigmoid_gate": (None, [p, p, i]),
+            "or_f32_to_f16": (ctypes.c_uint16, [f]),
+            "or_f32_to_f16_n": (None, [p, i, p]),
+            "or_kv_prescaled": (None, [p, i, i, p]),
+            "or_quantize_q8_0": (None, [p, i, p]),
+            "or_dequantize_q8_0": (None, [p, i, p]),
+            "or_quantize_q5_1": (None, [p, i, p]),
+            "or_dequantize_q5_1": (None, [p, i, p]),
             "or_argmax": (i, [p, i]),
             "or_top2": (None, [p, i, p, p]),
             "or_deltanet_layer": (None, [ctypes.POINTER(OrModel), ctypes.POINTER(OrState), i, p]),
@@ -281,6 +290,58 @@ def attention(q, kc, vc, nh, nkv, hd, t_len):
     return out
 
 
+# ------------------------------------------------- quantized KV cache blocks
+KV_F32, KV_Q8_0_Q5_1 = 0, 1
+Q8_0_BYTES, Q5_1_BYTES = 34, 24  # per 32 values
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    x = f32(np.atleast_1d(x)).copy()
+    out = np.empty(x.size, np.uint16)
+    lib().or_f32_to_f16_n(ptr(x), x.size, ptr(out))
+    return out
+
+
+def kv_prescaled(x, which: int) -> np.ndarray:
+    """The f32 values the codes round (which: 0 = q8_0, 1 = q5_1)."""
+    x = f32(x).copy()
+    pre = np.empty_like(x)
+    lib().or_kv_prescaled(ptr(x), x.size, int(which), ptr(pre))
+    return pre
+
+
+def _kvq(fn, x, nbytes):
+    x = f32(x).copy()
+    assert x.size % 32 == 0
+    out = np.empty(x.size // 32 * nbytes, np.uint8)
+    fn(ptr(x), x.size, ptr(out))
+    return out
+
+
+def _kvd(fn, b, nbytes):
+    b = np.ascontiguousarray(b, np.uint8)
+    n = b.size // nbytes * 32
+    out = np.empty(n, np.float32)
+    fn(ptr(b), n, ptr(out))
+    return out
+
+
+def quantize_q8_0(x) -> np.ndarray:
+    return _kvq(lib().or_quantize_q8_0, x, Q8_0_BYTES)
+
+
+def dequantize_q8_0(b) -> np.ndarray:
+    return _kvd(lib().or_dequantize_q8_0, b, Q8_0_BYTES)
+
+
+def quantize_q5_1(x) -> np.ndarray:
+    return _kvq(lib().or_quantize_q5_1, x, Q5_1_BYTES)
+
+
+def dequantize_q5_1(b) -> np.ndarray:
+    return _kvd(lib().or_dequantize_q5_1, b, Q5_1_BYTES)
+
+
 def sigmoid_gate(x, gate):
     x = f32(x).copy()
     gate = f32(gate)
@@ -358,11 +419,14 @@ class Model:
 class State:
     """Oracle decode state: conv windows, recurrent states, K/V caches."""
 
-    def __init__(self, model: Model):
+    def __init__(self, model: Model, kv_format: int = KV_F32):
         c = model.cfg
         self.cfg = c
+        self.kv_format = int(kv_format)
+        assert self.kv_format in (KV_F32, KV_Q8_0_Q5_1)
         n = c.n_layers
         self.conv, self.ssm, self.kc, self.vc = [None] * n, [None] * n, [None] * n, [None] * n
+        self.kq, self.vq = [None] * n, [None] * n
         for il, kind in enumerate(c.kinds()):
             if kind == DELTANET:
                 self.conv[il] = np.zeros((c.conv_dim, c.conv_kernel - 1), np.float32)
@@ -370,8 +434,29 @@ class State:
             else:
                 self.kc[il] = np.zeros((c.max_seq_len, c.kv_dim), np.float32)
                 self.vc[il] = np.zeros((c.max_seq_len, c.kv_dim), np.float32)
+                if self.kv_format == KV_Q8_0_Q5_1:
+                    self.kq[il] = np.zeros((c.max_seq_len, c.kv_dim // 32 * Q8_0_BYTES), np.uint8)
+                    self.vq[il] = np.zeros((c.max_seq_len, c.kv_dim // 32 * Q5_1_BYTES), np.uint8)
         arr = lambda lst: (_FP * n)(*[fptr(a) if a is not None else None for a in lst])  # noqa: E731
-        self._s = OrState(arr(self.conv), arr(self.ssm), arr(self.kc), arr(self.vc), 0)
+        barr = lambda lst: (ctypes.c_void_p * n)(*[a.ctypes.data if a is not None else None for a in lst])  # noqa
+        self._s = OrState(arr(self.conv), arr(self.ssm), arr(self.kc), arr(self.vc), 0, self.kv_format,
+                          barr(self.kq), barr(self.vq))
+
+    def set_kv_rows(self, il: int, k, v):
+        """Rows 0..len(k)-1 of layer il's cache from f32 K/V rows: stored as
+        they are (f32 cache), or quantized to q8_0 / q5_1 blocks with the
+        dequantized values as the rows the attention reads."""
+        k, v = f32(k), f32(v)
+        t = k.shape[0]
+        if self.kv_format == KV_F32:
+            self.kc[il][:t] = k
+            self.vc[il][:t] = v
+            return
+        kb, vb = quantize_q8_0(k.reshape(-1)), quantize_q5_1(v.reshape(-1))
+        self.kq[il][:t] = kb.reshape(t, -1)
+        self.vq[il][:t] = vb.reshape(t, -1)
+        self.kc[il][:t] = dequantize_q8_0(kb).reshape(t, -1)
+        self.vc[il][:t] = dequantize_q5_1(vb).reshape(t, -1)
 
     @property
     def kv_len(self):

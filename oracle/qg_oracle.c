@@ -30,6 +30,7 @@
  *
  * Readings taken where the pages are silent are listed beside each function.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -76,12 +77,18 @@ typedef struct {
     const or_layer* layers;
 } or_model;
 
+enum { OR_KV_F32 = 0, OR_KV_Q8_0_Q5_1 = 1 };
+
 typedef struct {
     float** conv; /* per layer: [conv_dim][conv_kernel-1], or NULL */
     float** ssm;  /* per layer: [n_v_heads][head_v_dim][head_k_dim], or NULL */
-    float** kc;   /* per layer: [max_seq_len][n_kv_heads*head_dim], or NULL */
+    float** kc;   /* per layer: [max_seq_len][n_kv_heads*head_dim], or NULL; with a
+                     quantized cache, the dequantized values of kq */
     float** vc;
     int kv_len;
+    int kv_format; /* OR_KV_F32, or OR_KV_Q8_0_Q5_1 (q8_0 K, q5_1 V) */
+    uint8_t** kq;  /* per layer, quantized cache only: [max_seq_len][kvd/32] q8_0 blocks */
+    uint8_t** vq;  /* per layer, quantized cache only: [max_seq_len][kvd/32] q5_1 blocks */
 } or_state;
 
 void or_set_threads(int n) {
@@ -439,6 +446,140 @@ void or_attention(const float* q, const float* kc, const float* vc, float* out, 
     free(sc);
 }
 
+/* ---------------------------------------------------- quantized KV cache */
+/*
+ * The decode session's quantized KV cache (forward_qwen35_cuda.rs, full
+ * attention layer: "q8_0 K / q5_1 V" appended by an on-device quantize
+ * kernel, attention over the resident byte K/V).  The pages name the two
+ * GGML block types and nothing more; their contents here are what those
+ * names denote in GGUF (reading):
+ *   q8_0, 34 bytes per 32 values: f16 d, int8 q[32];            x = d*q
+ *   q5_1, 24 bytes per 32 values: f16 d, f16 m, u32 qh, u8 qs[16];
+ *         q_j = (qs nibble) | (bit j of qh) << 4, the low nibble of qs[j]
+ *         holding q_j and the high nibble q_{j+16};            x = d*q + m
+ * The quantizer (reading): d from the block's f32 statistics (q8_0:
+ * max|x| / 127; q5_1: (max - min) / 31 with m = min), each code
+ * roundf(x * (1/d)) -- q5_1: roundf((x - min) * (1/d)) -- in f32 with the
+ * f32 d (half away from zero), clamped to the code range; a d below the
+ * smallest normal f32 gives zero codes.  d and m are stored as f16 (round to
+ * nearest even) and dequantization uses the stored values.  Every row the
+ * attention reads, the appended one included, is the dequantized row.
+ */
+
+/* IEEE 754 binary32 -> binary16, round to nearest, ties to even. */
+uint16_t or_f32_to_f16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t sign = (u >> 16) & 0x8000u, a = u & 0x7fffffffu;
+    if (a >= 0x7f800000u) return (uint16_t)(sign | (a > 0x7f800000u ? 0x7e00u : 0x7c00u));
+    if (a >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u); /* >= 65520: past the largest finite half */
+    int e = (int)(a >> 23) - 127;
+    uint32_t h, rem, half;
+    if (e >= -14) { /* a normal half: keep 10 of the 23 fraction bits */
+        h = ((uint32_t)(e + 15) << 10) | ((a & 0x7fffffu) >> 13);
+        rem = a & 0x1fffu;
+        half = 0x1000u;
+    } else { /* a subnormal half (units of 2^-24), or zero */
+        if (e < -25) return (uint16_t)sign;
+        uint32_t m = (a & 0x7fffffu) | 0x800000u; /* value = m * 2^(e-23) */
+        int shift = -e - 1;                       /* 14 .. 24 */
+        h = m >> shift;
+        rem = m & ((1u << shift) - 1u);
+        half = 1u << (shift - 1);
+    }
+    if (rem > half || (rem == half && (h & 1u))) h++; /* a carry moves into the exponent correctly */
+    return (uint16_t)(sign | h);
+}
+
+void or_f32_to_f16_n(const float* x, int n, uint16_t* out) {
+    for (int i = 0; i < n; i++) out[i] = or_f32_to_f16(x[i]);
+}
+
+static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (uint8_t)(v >> 8); }
+
+/* The f32 values each code rounds: x/d for q8_0, (x - min)/d for q5_1, both
+ * taken as a product with the f32 reciprocal of the f32 d (0 when d is below
+ * the smallest normal f32).  which: 0 = q8_0, 1 = q5_1.  n a multiple of 32. */
+void or_kv_prescaled(const float* x, int n, int which, float* pre) {
+    for (int b = 0; b < n / 32; b++) {
+        const float* xb = x + 32 * b;
+        float lo = xb[0], hi = xb[0], amax = 0.0f;
+        for (int j = 0; j < 32; j++) {
+            lo = fminf(lo, xb[j]);
+            hi = fmaxf(hi, xb[j]);
+            amax = fmaxf(amax, fabsf(xb[j]));
+        }
+        float d = which == 0 ? amax / 127.0f : (hi - lo) / 31.0f;
+        float id = d >= FLT_MIN ? 1.0f / d : 0.0f;
+        for (int j = 0; j < 32; j++) pre[32 * b + j] = which == 0 ? xb[j] * id : (xb[j] - lo) * id;
+    }
+}
+
+/* n values (a multiple of 32) -> n/32 q8_0 blocks of 34 bytes. */
+void or_quantize_q8_0(const float* x, int n, uint8_t* out) {
+    float pre[32];
+    for (int b = 0; b < n / 32; b++) {
+        const float* xb = x + 32 * b;
+        uint8_t* ob = out + 34 * (size_t)b;
+        float amax = 0.0f;
+        for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(xb[j]));
+        wr16(ob, or_f32_to_f16(amax / 127.0f));
+        or_kv_prescaled(xb, 32, 0, pre);
+        for (int j = 0; j < 32; j++) {
+            float v = roundf(pre[j]);
+            int q = v >= 127.0f ? 127 : v <= -127.0f ? -127 : (int)v;
+            ob[2 + j] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
+void or_dequantize_q8_0(const uint8_t* in, int n, float* x) {
+    for (int b = 0; b < n / 32; b++) {
+        const uint8_t* ib = in + 34 * (size_t)b;
+        float d = or_f16(rd16(ib));
+        for (int j = 0; j < 32; j++) x[32 * b + j] = d * (float)(int8_t)ib[2 + j];
+    }
+}
+
+/* n values (a multiple of 32) -> n/32 q5_1 blocks of 24 bytes. */
+void or_quantize_q5_1(const float* x, int n, uint8_t* out) {
+    float pre[32];
+    for (int b = 0; b < n / 32; b++) {
+        const float* xb = x + 32 * b;
+        uint8_t* ob = out + 24 * (size_t)b;
+        float lo = xb[0], hi = xb[0];
+        for (int j = 0; j < 32; j++) {
+            lo = fminf(lo, xb[j]);
+            hi = fmaxf(hi, xb[j]);
+        }
+        wr16(ob, or_f32_to_f16((hi - lo) / 31.0f));
+        wr16(ob + 2, or_f32_to_f16(lo));
+        or_kv_prescaled(xb, 32, 1, pre);
+        uint8_t q[32];
+        uint32_t qh = 0;
+        for (int j = 0; j < 32; j++) {
+            float v = roundf(pre[j]);
+            q[j] = (uint8_t)(v >= 31.0f ? 31 : v <= 0.0f ? 0 : (int)v);
+            qh |= (uint32_t)((q[j] >> 4) & 1) << j;
+        }
+        for (int i = 0; i < 4; i++) ob[4 + i] = (uint8_t)(qh >> (8 * i));
+        for (int j = 0; j < 16; j++) ob[8 + j] = (uint8_t)((q[j] & 15) | ((q[j + 16] & 15) << 4));
+    }
+}
+
+void or_dequantize_q5_1(const uint8_t* in, int n, float* x) {
+    for (int b = 0; b < n / 32; b++) {
+        const uint8_t* ib = in + 24 * (size_t)b;
+        float d = or_f16(rd16(ib)), m = or_f16(rd16(ib + 2));
+        uint32_t qh = (uint32_t)ib[4] | ((uint32_t)ib[5] << 8) | ((uint32_t)ib[6] << 16) | ((uint32_t)ib[7] << 24);
+        for (int j = 0; j < 32; j++) {
+            int nib = j < 16 ? (ib[8 + j] & 15) : (ib[8 + j - 16] >> 4);
+            int q = nib | (int)(((qh >> j) & 1u) << 4);
+            x[32 * b + j] = d * (float)q + m;
+        }
+    }
+}
+
 /* x *= sigmoid(gate) (gdn_sigmoid_gate_into). */
 void or_sigmoid_gate(float* x, const float* gate, int n) {
     for (int i = 0; i < n; i++) x[i] = x[i] * or_sigmoid(gate[i]);
@@ -536,6 +677,16 @@ void or_attention_layer(const or_model* M, or_state* st, int il, float* h, int p
     or_rmsnorm_heads(kraw, L->k_norm, krow, hd, nkv, c->eps);
     or_rope_neox(qn, nh, hd, c->n_rot, pos, ts);
     or_rope_neox(krow, nkv, hd, c->n_rot, pos, ts);
+    if (st->kv_format == OR_KV_Q8_0_Q5_1) {
+        /* quantize-on-append: row pos becomes its q8_0 (K) / q5_1 (V) blocks, and
+           the attention reads it, like every older row, dequantized */
+        uint8_t* kb = st->kq[il] + (size_t)pos * (size_t)(kvd / 32) * 34;
+        uint8_t* vb = st->vq[il] + (size_t)pos * (size_t)(kvd / 32) * 24;
+        or_quantize_q8_0(krow, kvd, kb);
+        or_dequantize_q8_0(kb, kvd, krow);
+        or_quantize_q5_1(vrow, kvd, vb);
+        or_dequantize_q5_1(vb, kvd, vrow);
+    }
     or_attention(qn, st->kc[il], st->vc[il], att, nh, nkv, hd, pos + 1);
     or_sigmoid_gate(att, gate, qd);
     or_gemv(L->wo, att, y);
