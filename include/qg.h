@@ -138,6 +138,28 @@ int qg_model_destroy(qg_model* m);
  * slots, pinned host slots and its own CUDA stream.  Allocates everything a
  * decode needs up front.  Errors: QG_ERR_SHAPE (max_seq_len < 1), QG_ERR_OOM. */
 int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out);
+
+/* KV cache formats.  QG_KV_F32: f32 rows, as qg_state_create makes them.
+ * QG_KV_Q8_0_Q5_1: the decode session's quantized cache (forward_qwen35_cuda.rs,
+ * full-attention layer: q8_0 K / q5_1 V, quantized on append by the attention
+ * kernel, attention over the dequantized rows, this token's included).  Blocks
+ * of 32 values with the GGUF block contents -- q8_0: f16 d, int8 q, x = d*q;
+ * q5_1: f16 d, f16 m, 5-bit q, x = d*q + m -- stored per (kv head, position)
+ * as one record with the 8 blocks' scales first (head_dim 256):
+ *   K record, 272 bytes: d[8] (f16) | q[256] (int8)
+ *   V record, 192 bytes: (d, m)[8] (f16 pairs) | qh[8] (u32, bit j = bit 4 of
+ *     value j's code) | qs[8][16] (byte i: code i & 15 low, code i+16 & 15 high)
+ * One layer's cache is [n_kv_heads][max_seq_len][record].  The quantizer: d from
+ * the block's f32 statistics (q8_0: max|x|/127; q5_1: (max-min)/31, m = min),
+ * code = roundf(x * (1/d)) (q5_1: roundf((x-min) * (1/d))), IEEE f32 operations,
+ * clamped to the code range (zero codes when d is below FLT_MIN); d and m rounded
+ * to f16 (nearest even), and every reader uses the stored f16 values. */
+enum { QG_KV_F32 = 0, QG_KV_Q8_0_Q5_1 = 1 };
+/* qg_state_create with the KV cache in `kv_format`.  A quantized cache holds
+ * 464 bytes per (position, kv head) instead of 2048.  Errors: those of
+ * qg_state_create, QG_ERR_ARG (unknown format). */
+int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_state** out);
+int qg_state_kv_format(const qg_state* s, int* kv_format);
 int qg_state_destroy(qg_state* s);
 /* Zero every window, state and cache; kv_len = 0. */
 int qg_state_reset(qg_state* s);
@@ -145,15 +167,27 @@ int qg_state_reset(qg_state* s);
 /* Teacher forcing (forward_qwen35_cuda.rs upload_layer, upload_attention_kv,
  * download_layer).  HOST buffers.  upload_layer: conv [conv_dim*(conv_kernel-1)]
  * and ssm [n_v_heads*head_v_dim*head_k_dim] of DeltaNet layer il.
- * upload_kv: `rows` whole K and V rows of attention layer il, sets kv_len = rows.
+ * upload_kv: `rows` whole K and V rows of attention layer il (f32,
+ * [rows][n_kv_heads*head_dim]), sets kv_len = rows; a quantized cache stores
+ * them through the append's quantizer on the device (it allocates and frees a
+ * device staging buffer of 2*rows*kv_row floats).
  * download_layer: DeltaNet -> (conv, ssm), *n = max of the two lengths written
  * as (conv_len, ssm_len) into a and b; attention -> the kv_len*kv_row K and V
  * values written so far (*n = kv_len * n_kv_heads*head_dim; 0 on a fresh
  * state).  Pass a == b == NULL to query *n (DeltaNet: *n = ssm_len).
+ * A quantized cache is read with qg_state_download_kv_records instead
+ * (download_layer of its attention layers gives QG_ERR_ARG).
  * Errors: QG_ERR_LAYER_KIND, QG_ERR_SHAPE, QG_ERR_ARG, QG_ERR_CUDA. */
 int qg_state_upload_layer(qg_state* s, int il, const float* conv, const float* ssm);
 int qg_state_upload_kv(qg_state* s, int il, const float* k, const float* v, int rows);
 int qg_state_download_layer(qg_state* s, int il, float* a, float* b, size_t* n);
+/* Quantized cache of attention layer il as written so far: the first kv_len
+ * K records of every kv head into k ([n_kv_heads][kv_len][272 bytes], HOST)
+ * and the V records into v ([n_kv_heads][kv_len][192]); *k_bytes / *v_bytes
+ * receive the sizes (pass k == v == NULL to query them).  Errors:
+ * QG_ERR_LAYER_KIND, QG_ERR_ARG (NULL size pointers, or an f32 cache),
+ * QG_ERR_CUDA. */
+int qg_state_download_kv_records(qg_state* s, int il, void* k, void* v, size_t* k_bytes, size_t* v_bytes);
 /* The residual stream after the last completed step ([hidden], host). */
 int qg_state_download_hidden(qg_state* s, float* hidden_host);
 int qg_state_kv_len(const qg_state* s, int* kv_len);
@@ -185,7 +219,8 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
  * next call).  Errors: QG_ERR_ARG (unknown mode), QG_ERR_SHAPE (the model's
  * shape is not served by the persistent kernel: more than 64 layers, a GQA
  * group other than 1, 2 or 4, more than 64 value heads, or no cooperative
- * launch on the device). */
+ * launch on the device); QG_ERR_ARG also for QG_STEP_PERSISTENT on a state
+ * with a quantized KV cache (the persistent kernel reads f32 caches only). */
 enum { QG_STEP_KERNELS = 0, QG_STEP_PERSISTENT = 1 };
 int qg_state_set_step_mode(qg_state* s, int mode);
 

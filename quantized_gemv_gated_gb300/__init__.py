@@ -34,10 +34,13 @@ EXPORTS = [
     "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
+    "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records",
 ]
 
 
 STEP_KERNELS, STEP_PERSISTENT = 0, 1  # qg_state_set_step_mode
+KV_F32, KV_Q8_0_Q5_1 = 0, 1  # qg_state_create_kv
+K_RECORD_BYTES, V_RECORD_BYTES = 272, 192  # per (kv head, position) of a quantized cache
 
 
 class QgError(RuntimeError):
@@ -101,6 +104,9 @@ def lib():
             "qg_model_create": [ctypes.POINTER(QgConfig), ctypes.POINTER(QgHostWeights), i, ctypes.POINTER(p)],
             "qg_model_destroy": [p],
             "qg_state_create": [p, i, ctypes.POINTER(p)],
+            "qg_state_create_kv": [p, i, i, ctypes.POINTER(p)],
+            "qg_state_kv_format": [p, ctypes.POINTER(i)],
+            "qg_state_download_kv_records": [p, i, p, p, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "qg_state_destroy": [p],
             "qg_state_reset": [p],
             "qg_state_upload_layer": [p, i, p, p],
@@ -291,12 +297,13 @@ class Model:
 class State:
     """Per-sequence decode state (qg_state)."""
 
-    def __init__(self, model: Model, max_seq_len: int):
+    def __init__(self, model: Model, max_seq_len: int, kv_format: int = KV_F32):
         self.model = model
         self.cfg = model.cfg
         self.max_seq_len = max_seq_len
+        self.kv_format = kv_format
         h = ctypes.c_void_p()
-        _check(lib().qg_state_create(model.handle, max_seq_len, ctypes.byref(h)))
+        _check(lib().qg_state_create_kv(model.handle, max_seq_len, kv_format, ctypes.byref(h)))
         self.handle = h
 
     def close(self):
@@ -339,6 +346,19 @@ class State:
         if n.value:
             _check(lib().qg_state_download_layer(self.handle, il, _host(k), _host(v), ctypes.byref(n)))
         return k.reshape(-1, c.kv_dim), v.reshape(-1, c.kv_dim)
+
+    def download_kv_records(self, il):
+        """Quantized cache of attention layer il: (K records [n_kv][kv_len][272],
+        V records [n_kv][kv_len][192]) as uint8 arrays."""
+        kb, vb = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().qg_state_download_kv_records(self.handle, il, None, None, ctypes.byref(kb), ctypes.byref(vb)))
+        k = np.empty(kb.value, np.uint8)
+        v = np.empty(vb.value, np.uint8)
+        if kb.value:
+            _check(lib().qg_state_download_kv_records(self.handle, il, _host(k), _host(v), ctypes.byref(kb),
+                                                      ctypes.byref(vb)))
+        nkv = self.cfg.n_kv_heads
+        return k.reshape(nkv, -1, K_RECORD_BYTES), v.reshape(nkv, -1, V_RECORD_BYTES)
 
     def download_hidden(self):
         h = np.empty(self.cfg.hidden, np.float32)

@@ -119,8 +119,9 @@ __global__ void residual_add_kernel(float* __restrict__ h, const float* __restri
 struct AttnArgs {
     const float* qf;     // [nh][2*hd]: q then gate per head
     const float* kraw;   // [nkv*hd]
-    float* kc;           // K cache [max_seq][kvd]
-    const float* vc;     // V cache
+    float* kc;           // K cache: f32 [max_seq][kvd], or q8_0 records [nkv][max_seq][kKRec bytes]
+    float* vc;           // V cache: f32 [max_seq][kvd], or q5_1 records [nkv][max_seq][kVRec bytes]
+    const float* vraw;   // quantized cache: this token's V row [nkv*hd] (the input GEMV's output)
     const float* q_norm;
     const float* k_norm;
     const int* slots;
@@ -130,25 +131,39 @@ struct AttnArgs {
     float* out;          // [nh*hd], gated
     unsigned* err;
     L2Prefetch next;
-    int kvd, T, max_splits, n_rot;
+    int kvd, T, max_splits, n_rot, max_seq;
     float theta_scale, eps;
 };
 
-template <int GS>
+// Bytes of one ring stage: kKeysPerStage keys' K and V rows (f32), or their
+// K records then their V records (quantized cache).
+template <bool KVQ>
+__host__ __device__ constexpr int attn_stage_bytes() {
+    return KVQ ? kKeysPerStage * (kKRec + kVRec) : kKeysPerStage * 2 * kHd * 4;
+}
+
+template <int GS, bool KVQ>
 __host__ __device__ inline int attn_smem_floats() {
-    return GS * kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd + 64 * GS * 2 + kAttnStages * kKeysPerStage * 2 * kHd;
+    return GS * kHd + kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd + 64 * GS * 2 +
+           kAttnStages * attn_stage_bytes<KVQ>() / 4;
 }
 
 
-template <int GS>
+// KVQ: the cache holds q8_0 K / q5_1 V records (the layout above kvq_put_q8_0):
+// the split holding row pos quantizes this token's K (after its norm and
+// rope) and V rows into the cache, and every key, this one included, is read
+// back dequantized.
+template <int GS, bool KVQ>
 __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
     extern __shared__ __align__(128) float sm[];
     __shared__ uint64_t full[kAttnStages], empty[kAttnStages];
     __shared__ int last_flag;
-    float* ring = sm;                                        // [stages][8 keys][K row | V row]
-    float* q_s = ring + kAttnStages * kKeysPerStage * 2 * kHd;  // [GS][hd]
+    float* ring = sm;                                        // [stages][8 keys][K row | V row] (f32), or
+                                                             // [stages][8 K records | 8 V records]
+    float* q_s = ring + kAttnStages * attn_stage_bytes<KVQ>() / 4;  // [GS][hd]
     float* k_s = q_s + GS * kHd;                             // [hd]
-    float* cs = k_s + kHd;                                   // [hd/2]
+    float* v_s = k_s + kHd;                                  // [hd] this token's V, dequantized (KVQ)
+    float* cs = v_s + kHd;                                   // [hd/2]
     float* sn = cs + kHd / 2;                                // [hd/2]
     float* wml = sn + kHd / 2;                               // [8][GS][2]
     float* wacc = wml + 8 * GS * 2;                          // [8][GS][hd]
@@ -190,19 +205,34 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
                     break;
                 }
                 const int k0 = t0 + st * kKeysPerStage, k1 = min(k0 + kKeysPerStage, t1);
-                if (!waited && k1 > pos) {
-                    pdl_wait();  // V[pos] is written by the previous kernel
-                    waited = true;
-                }
-                unsigned bytes = 0;
-                for (int t = k0; t < k1; ++t) bytes += (t == pos ? 1u : 2u) * kHd * 4u;
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                float* st_base = ring + static_cast<size_t>(slot) * kKeysPerStage * 2 * kHd;
-                for (int t = k0; t < k1; ++t) {
-                    float* dst = st_base + (t - k0) * 2 * kHd;
-                    const size_t off = static_cast<size_t>(t) * a.kvd + g * kHd;
-                    if (t != pos) bulk_g2s(dst, a.kc + off, kHd * 4, &full[slot], pol);
-                    bulk_g2s(dst + kHd, a.vc + off, kHd * 4, &full[slot], pol);
+                if constexpr (KVQ) {
+                    // rows before pos were written by earlier steps; row pos is made here
+                    const int n_old = min(k1, pos) - k0;
+                    const unsigned kb = static_cast<unsigned>(n_old > 0 ? n_old : 0) * kKRec;
+                    const unsigned vb = static_cast<unsigned>(n_old > 0 ? n_old : 0) * kVRec;
+                    mbar_arrive_expect_tx(&full[slot], kb + vb);
+                    uint8_t* st_base = reinterpret_cast<uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true>();
+                    const size_t rec0 = static_cast<size_t>(g) * a.max_seq + k0;
+                    if (kb) {
+                        bulk_g2s(st_base, reinterpret_cast<const uint8_t*>(a.kc) + rec0 * kKRec, kb, &full[slot], pol);
+                        bulk_g2s(st_base + kKeysPerStage * kKRec, reinterpret_cast<const uint8_t*>(a.vc) + rec0 * kVRec,
+                                 vb, &full[slot], pol);
+                    }
+                } else {
+                    if (!waited && k1 > pos) {
+                        pdl_wait();  // V[pos] is written by the previous kernel
+                        waited = true;
+                    }
+                    unsigned bytes = 0;
+                    for (int t = k0; t < k1; ++t) bytes += (t == pos ? 1u : 2u) * kHd * 4u;
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    float* st_base = ring + static_cast<size_t>(slot) * kKeysPerStage * 2 * kHd;
+                    for (int t = k0; t < k1; ++t) {
+                        float* dst = st_base + (t - k0) * 2 * kHd;
+                        const size_t off = static_cast<size_t>(t) * a.kvd + g * kHd;
+                        if (t != pos) bulk_g2s(dst, a.kc + off, kHd * 4, &full[slot], pol);
+                        bulk_g2s(dst + kHd, a.vc + off, kHd * 4, &full[slot], pol);
+                    }
                 }
                 issued = st + 1;
                 if (st == 0) a.next.issue();
@@ -251,7 +281,18 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
         vec[i + half] = x0 * sn[i] + x1 * cs[i];
     }
     bar_sync(1, 256);
-    if (has_new) a.kc[static_cast<size_t>(pos) * a.kvd + g * kHd + tid] = k_s[tid];  // K append at pos
+    if constexpr (KVQ) {
+        if (has_new) {  // quantize-on-append: warp w makes block w of the K and the V record at pos
+            const size_t rec = static_cast<size_t>(g) * a.max_seq + pos;
+            const int e = 32 * warp + lane;
+            k_s[e] = kvq_put_q8_0(k_s[e], lane, warp, reinterpret_cast<uint8_t*>(a.kc) + rec * kKRec);
+            v_s[e] = kvq_put_q5_1(__ldcg(a.vraw + g * kHd + e), lane, warp,
+                                  reinterpret_cast<uint8_t*>(a.vc) + rec * kVRec);
+            bar_sync(1, 256);
+        }
+    } else {
+        if (has_new) a.kc[static_cast<size_t>(pos) * a.kvd + g * kHd + tid] = k_s[tid];  // K append at pos
+    }
 
     float q[GS][8];
 #pragma unroll
@@ -275,10 +316,21 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
         }
         const int t = t0 + st * kKeysPerStage + warp;
         if (t < t1) {
-            const float* kv_row = ring + (static_cast<size_t>(slot) * kKeysPerStage + warp) * 2 * kHd;
             float kv[8], vv[8];
-            row8(t == pos ? k_s : kv_row, lane, kv);
-            row8(kv_row + kHd, lane, vv);
+            if constexpr (KVQ) {
+                const uint8_t* sb = reinterpret_cast<const uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true>();
+                if (t == pos) {
+                    row8(k_s, lane, kv);
+                    row8(v_s, lane, vv);
+                } else {
+                    kvq_k8(sb + warp * kKRec, lane, kv);
+                    kvq_v8(sb + kKeysPerStage * kKRec + warp * kVRec, lane, vv);
+                }
+            } else {
+                const float* kv_row = ring + (static_cast<size_t>(slot) * kKeysPerStage + warp) * 2 * kHd;
+                row8(t == pos ? k_s : kv_row, lane, kv);
+                row8(kv_row + kHd, lane, vv);
+            }
 #pragma unroll
             for (int i = 0; i < GS; ++i) {
                 float dot = 0.0f;
@@ -508,15 +560,47 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
     return ffn(m, s, il, io, st);
 }
 
-template <int GS>
-static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
-    const int smem = attn_smem_floats<GS>() * 4;
+// Grid (rows, n_kv): one CTA per (position, kv head), warp w makes block w
+// of its K and V records with the append's quantizer.
+__global__ void __launch_bounds__(256) kv_quantize_kernel(const float* __restrict__ k, const float* __restrict__ v,
+                                                          int n_kv, int max_seq, uint8_t* kq, uint8_t* vq) {
+    const int t = blockIdx.x, g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t src = (static_cast<size_t>(t) * n_kv + g) * kHd + 32 * warp + lane;
+    const size_t rec = static_cast<size_t>(g) * max_seq + t;
+    kvq_put_q8_0(k[src], lane, warp, kq + rec * kKRec);
+    kvq_put_q5_1(v[src], lane, warp, vq + rec * kVRec);
+}
+
+int kv_quantize_rows(const float* k, const float* v, int rows, int n_kv, int max_seq, uint8_t* kq, uint8_t* vq,
+                     cudaStream_t st) {
+    if (rows <= 0) return QG_OK;
+    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, kq, vq);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+size_t kv_cache_bytes(const qg_state* s, int which) {
+    const qg_model* m = s->m;
+    if (s->kv_format == QG_KV_Q8_0_Q5_1)
+        return static_cast<size_t>(m->cfg.n_kv_heads) * s->max_seq * (which == 0 ? kKRec : kVRec);
+    return sizeof(float) * static_cast<size_t>(s->max_seq) * m->kv_dim;
+}
+
+template <int GS, bool KVQ>
+static int launch_attn_as(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
+    const int smem = attn_smem_floats<GS, KVQ>() * 4;
     static int configured = 0;
     if (smem > configured) {
-        QG_CUDA(cudaFuncSetAttribute(attn_kernel<GS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        QG_CUDA(cudaFuncSetAttribute(attn_kernel<GS, KVQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         configured = smem;
     }
-    return launch_pdl(attn_kernel<GS>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
+    return launch_pdl(attn_kernel<GS, KVQ>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
+}
+
+template <int GS>
+static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
+    return s->kv_format == QG_KV_Q8_0_Q5_1 ? launch_attn_as<GS, true>(m, s, a, st)
+                                           : launch_attn_as<GS, false>(m, s, a, st);
 }
 
 int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
@@ -527,6 +611,7 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
     ea.qf = s->qf;
     ea.kraw = s->kraw;
     ea.vcache = s->vc[il];
+    ea.vraw = s->kv_format == QG_KV_Q8_0_Q5_1 ? s->vraw : nullptr;
     ea.slots = s->slots;
     ea.qd2 = 2 * m->q_dim;
     ea.kvd = m->kv_dim;
@@ -539,6 +624,8 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
     a.kraw = s->kraw;
     a.kc = s->kc[il];
     a.vc = s->vc[il];
+    a.vraw = s->vraw;
+    a.max_seq = s->max_seq;
     a.q_norm = L.q_norm;
     a.k_norm = L.k_norm;
     a.slots = s->slots;

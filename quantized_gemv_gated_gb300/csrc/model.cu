@@ -354,6 +354,12 @@ int qg_model_destroy(qg_model* m) {
 }
 
 int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
+    return qg_state_create_kv(m, max_seq_len, QG_KV_F32, out);
+}
+
+int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_state** out) {
+    if (kv_format != QG_KV_F32 && kv_format != QG_KV_Q8_0_Q5_1)
+        return set_err(QG_ERR_ARG, "state_create: unknown KV cache format %d", kv_format);
     if (!m || !out) return set_err(QG_ERR_ARG, "state_create: NULL argument");
     *out = nullptr;
     if (max_seq_len < 1) return set_err(QG_ERR_SHAPE, "state_create: max_seq_len must be at least 1");
@@ -362,6 +368,7 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
     if (!s) return set_err(QG_ERR_OOM, "state_create: host allocation");
     s->m = m;
     s->max_seq = max_seq_len;
+    s->kv_format = kv_format;
     s->kv_len = 0;
     s->exec_step = nullptr;
     s->exec_greedy = nullptr;
@@ -392,8 +399,9 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                 break;
             rc = dalloc(s->allocs, &s->ssm[il], static_cast<size_t>(c.n_v_heads) * c.head_v_dim * c.head_k_dim, cnt);
         } else {
-            if ((rc = dalloc(s->allocs, &s->kc[il], static_cast<size_t>(max_seq_len) * m->kv_dim, cnt))) break;
-            rc = dalloc(s->allocs, &s->vc[il], static_cast<size_t>(max_seq_len) * m->kv_dim, cnt);
+            // f32 rows, or (quantized cache) records of bytes, allocated as whole floats
+            if ((rc = dalloc(s->allocs, &s->kc[il], kv_cache_bytes(s, 0) / sizeof(float), cnt))) break;
+            rc = dalloc(s->allocs, &s->vc[il], kv_cache_bytes(s, 1) / sizeof(float), cnt);
         }
     }
     if (!rc) {
@@ -405,6 +413,7 @@ int qg_state_create(const qg_model* m, int max_seq_len, qg_state** out) {
                (rc = dalloc(s->allocs, &s->z, m->v_dim + 1, cnt)) || (rc = dalloc(s->allocs, &s->o, m->v_dim + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->act, c.ffn, cnt)) || (rc = dalloc(s->allocs, &s->qf, 2 * m->q_dim + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->kraw, m->kv_dim + 1, cnt)) ||
+               (rc = dalloc(s->allocs, &s->vraw, m->kv_dim + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->attn, m->q_dim + 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->part_acc,
                             static_cast<size_t>(c.n_kv_heads) * s->max_splits * gs * 256 + 1, cnt)) ||
@@ -476,8 +485,8 @@ int qg_state_reset(qg_state* s) {
         if (s->conv[il]) QG_CUDA(cudaMemset(s->conv[il], 0, sizeof(float) * m->conv_dim * (c.conv_kernel - 1)));
         if (s->ssm[il])
             QG_CUDA(cudaMemset(s->ssm[il], 0, sizeof(float) * static_cast<size_t>(c.n_v_heads) * c.head_v_dim * c.head_k_dim));
-        if (s->kc[il]) QG_CUDA(cudaMemset(s->kc[il], 0, sizeof(float) * static_cast<size_t>(s->max_seq) * m->kv_dim));
-        if (s->vc[il]) QG_CUDA(cudaMemset(s->vc[il], 0, sizeof(float) * static_cast<size_t>(s->max_seq) * m->kv_dim));
+        if (s->kc[il]) QG_CUDA(cudaMemset(s->kc[il], 0, kv_cache_bytes(s, 0)));
+        if (s->vc[il]) QG_CUDA(cudaMemset(s->vc[il], 0, kv_cache_bytes(s, 1)));
     }
     QG_CUDA(cudaMemset(s->h, 0, sizeof(float) * c.hidden));
     QG_CUDA(cudaMemset(s->hres, 0, sizeof(float) * c.hidden));
@@ -520,11 +529,58 @@ int qg_state_upload_kv(qg_state* s, int il, const float* k, const float* v, int 
     DeviceGuard dg(m->device);
     QG_CUDA(cudaStreamSynchronize(s->stream));
     const size_t bytes = sizeof(float) * static_cast<size_t>(rows) * m->kv_dim;
-    if (rows > 0) {
+    if (rows > 0 && s->kv_format == QG_KV_Q8_0_Q5_1) {
+        // quantized cache: the f32 rows go through the append's quantizer on the device
+        float* tmp = nullptr;
+        QG_CUDA(cudaMalloc(&tmp, 2 * bytes));
+        int rc = QG_OK;
+        cudaError_t e = cudaMemcpy(tmp, k, bytes, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaMemcpy(tmp + bytes / sizeof(float), v, bytes, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) rc = cuda_err(e, "upload_kv: cudaMemcpy");
+        if (!rc)
+            rc = kv_quantize_rows(tmp, tmp + bytes / sizeof(float), rows, m->cfg.n_kv_heads, s->max_seq,
+                                  reinterpret_cast<uint8_t*>(s->kc[il]), reinterpret_cast<uint8_t*>(s->vc[il]),
+                                  s->stream);
+        if (!rc && (e = cudaStreamSynchronize(s->stream)) != cudaSuccess) rc = cuda_err(e, "upload_kv: quantize");
+        cudaFree(tmp);
+        if (rc) return rc;
+    } else if (rows > 0) {
         QG_CUDA(cudaMemcpy(s->kc[il], k, bytes, cudaMemcpyHostToDevice));
         QG_CUDA(cudaMemcpy(s->vc[il], v, bytes, cudaMemcpyHostToDevice));
     }
     s->kv_len = rows;
+    return QG_OK;
+}
+
+int qg_state_download_kv_records(qg_state* s, int il, void* k, void* v, size_t* k_bytes, size_t* v_bytes) {
+    if (!s || !k_bytes || !v_bytes) return set_err(QG_ERR_ARG, "download_kv_records: NULL argument");
+    const qg_model* m = s->m;
+    if (il < 0 || il >= m->cfg.n_layers || m->kinds[il] != QG_LAYER_ATTENTION)
+        return set_err(QG_ERR_LAYER_KIND, "download_kv_records: layer %d is not a full-attention layer", il);
+    if (s->kv_format != QG_KV_Q8_0_Q5_1)
+        return set_err(QG_ERR_ARG, "download_kv_records: the state's KV cache is f32 (use qg_state_download_layer)");
+    DeviceGuard dg(m->device);
+    QG_CUDA(cudaStreamSynchronize(s->stream));
+    QG_CUDA(cudaDeviceSynchronize());
+    const int nkv = m->cfg.n_kv_heads;
+    const size_t kr = kv_cache_bytes(s, 0) / (static_cast<size_t>(nkv) * s->max_seq);
+    const size_t vr = kv_cache_bytes(s, 1) / (static_cast<size_t>(nkv) * s->max_seq);
+    *k_bytes = static_cast<size_t>(nkv) * s->kv_len * kr;
+    *v_bytes = static_cast<size_t>(nkv) * s->kv_len * vr;
+    if (s->kv_len == 0) return QG_OK;
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(s->kc[il]);
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(s->vc[il]);
+    for (int g = 0; g < nkv; ++g) {  // head g's first kv_len records, packed
+        const size_t at = static_cast<size_t>(g) * s->max_seq, to = static_cast<size_t>(g) * s->kv_len;
+        if (k) QG_CUDA(cudaMemcpy(static_cast<uint8_t*>(k) + to * kr, kc + at * kr, s->kv_len * kr, cudaMemcpyDeviceToHost));
+        if (v) QG_CUDA(cudaMemcpy(static_cast<uint8_t*>(v) + to * vr, vc + at * vr, s->kv_len * vr, cudaMemcpyDeviceToHost));
+    }
+    return QG_OK;
+}
+
+int qg_state_kv_format(const qg_state* s, int* kv_format) {
+    if (!s || !kv_format) return set_err(QG_ERR_ARG, "state_kv_format: NULL argument");
+    *kv_format = s->kv_format;
     return QG_OK;
 }
 
@@ -544,6 +600,8 @@ int qg_state_download_layer(qg_state* s, int il, float* a, float* b, size_t* n) 
         if (b) QG_CUDA(cudaMemcpy(b, s->ssm[il], sl * sizeof(float), cudaMemcpyDeviceToHost));
         return QG_OK;
     }
+    if (s->kv_format != QG_KV_F32)
+        return set_err(QG_ERR_ARG, "download_layer: layer %d holds a quantized cache (use qg_state_download_kv_records)", il);
     const size_t cnt = static_cast<size_t>(s->kv_len) * m->kv_dim;
     *n = cnt;
     if (cnt && a) QG_CUDA(cudaMemcpy(a, s->kc[il], cnt * sizeof(float), cudaMemcpyDeviceToHost));
@@ -593,6 +651,8 @@ int qg_state_set_step_mode(qg_state* s, int mode) {
     if (mode != QG_STEP_KERNELS && mode != QG_STEP_PERSISTENT)
         return set_err(QG_ERR_ARG, "set_step_mode: unknown mode %d", mode);
     if (mode == s->step_mode) return QG_OK;
+    if (mode == QG_STEP_PERSISTENT && s->kv_format != QG_KV_F32)
+        return set_err(QG_ERR_ARG, "set_step_mode: the persistent step kernel reads an f32 KV cache only");
     DeviceGuard dg(s->m->device);
     QG_CUDA(cudaStreamSynchronize(s->stream));
     if (mode == QG_STEP_PERSISTENT && !s->step) {

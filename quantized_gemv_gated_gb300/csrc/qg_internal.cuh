@@ -45,11 +45,13 @@ struct qg_state {
     int max_seq;
     int kv_len;
     cudaStream_t stream;
-    std::vector<float*> conv, ssm, kc, vc;  // per layer, null for the other kind
+    int kv_format;                          // QG_KV_F32 or QG_KV_Q8_0_Q5_1, fixed at creation
+    std::vector<float*> conv, ssm, kc, vc;  // per layer, null for the other kind; with a quantized
+                                            // cache kc / vc hold q8_0 / q5_1 records (bytes)
     // scratch; h: the residual stream after the last step (the lm_head input
     // plus the last pending y), hres: the residual stream between layers, y:
     // the output of the last GEMV, not yet added
-    float *h, *hres, *y, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *attn;
+    float *h, *hres, *y, *conv_out, *dt, *beta, *z, *o, *act, *qf, *kraw, *vraw, *attn;
     float *part_acc, *part_ml;
     unsigned* attn_count;       // [n_kv_heads] split arrivals (left at 0)
     float* kpart;               // split-K GEMV slice sums [max slices][hidden8]
@@ -104,6 +106,12 @@ int step_setup(const qg_model* m, qg_state* s);
 int run_step(qg_state* s, cudaStream_t st, bool advance);
 // Raw GGUF Q4_K rows -> the engine's grouped layout ((n+7)/8*8 x k/256 x 144 bytes).
 int q4k_to_grouped(const void* src, void* dst, int n, int k, cudaStream_t st);
+// Quantized-cache rows from f32 K/V rows ([rows][n_kv*256] each): the records
+// of positions 0..rows-1 of every kv head, made by the append's quantizer.
+int kv_quantize_rows(const float* k, const float* v, int rows, int n_kv, int max_seq, uint8_t* kq, uint8_t* vq,
+                     cudaStream_t st);
+// Bytes of one layer's K or V cache (which: 0 = K, 1 = V).
+size_t kv_cache_bytes(const qg_state* s, int which);
 // a = -exp(A_log) on the device.
 int run_neg_exp(const float* src, float* dst, int n, cudaStream_t st);
 

@@ -82,11 +82,13 @@ struct EpiDnIn : EpiBase {
 
 // Attention input projection rows: [0, 2qd) [q | gate] per head; [2qd,
 // 2qd+kvd) k before its norm; [2qd+kvd, 2qd+2kvd) v, straight into the V
-// cache row at the position in slots[1] (the cache append).
+// cache row at the position in slots[1] (the cache append), or, with a
+// quantized cache, into a scratch row that the attention kernel quantizes.
 struct EpiAttnIn : EpiBase {
     float* qf;
     float* kraw;
-    float* vcache;
+    float* vcache;  // f32 cache: the V row goes straight to row pos
+    float* vraw;    // quantized cache: the V row goes here, the attention kernel quantizes it
     const int* slots;
     int qd2, kvd;
     int pos;
@@ -96,6 +98,7 @@ struct EpiAttnIn : EpiBase {
             const float v = ys[r - r0];
             if (r < qd2) qf[r] = v;
             else if (r < qd2 + kvd) kraw[r - qd2] = v;
+            else if (vraw) vraw[r - qd2 - kvd] = v;
             else vcache[static_cast<size_t>(pos) * kvd + (r - qd2 - kvd)] = v;
         }
     }
@@ -271,5 +274,91 @@ __device__ __forceinline__ void load_row8(const float* p, int lane, float* v) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 __device__ __forceinline__ int dim8(int lane, int j) { return j < 4 ? 4 * lane + j : 128 + 4 * lane + j - 4; }
+
+// ------------------------------------------------- quantized KV cache records
+// The decode session's quantized cache (forward_qwen35_cuda.rs, full
+// attention layer): K as q8_0 blocks, V as q5_1 blocks of 32 values, the GGUF
+// block contents (q8_0: f16 d, int8 q, x = d*q; q5_1: f16 d, f16 m, 5-bit q
+// as a nibble plus one bit of qh, x = d*q + m), laid out per (kv head,
+// position) record with the 8 blocks' scales first:
+//   K record, 272 bytes: d[8] (f16) | q[256] (int8)
+//   V record, 192 bytes: (d, m)[8] (f16 pairs) | qh[8] (u32) | qs[8][16]
+//   (qs byte i of a block: q_i & 15 in the low nibble, q_{i+16} & 15 high)
+// The cache of one layer is [n_kv_heads][max_seq][record], so the keys of one
+// head are contiguous and a stage of them is one bulk copy.
+// Quantizer: the block's f32 statistics give d (q8_0: max|x| / 127; q5_1:
+// (max - min) / 31, m = min); each code is roundf(x * (1/d)) (q5_1:
+// roundf((x - min) * (1/d))) with IEEE-rounded f32 operations, clamped to the
+// code range; d below the smallest normal float gives zero codes; d and m are
+// stored as f16 (round to nearest even), and every reader uses the stored
+// values.
+constexpr int kKRec = 272;
+constexpr int kVRec = 192;
+
+// One warp quantizes one 32-value q8_0 block of a K record: lane holds value
+// `lane` of block b.  Returns the lane's dequantized value.
+__device__ __forceinline__ float kvq_put_q8_0(float x, int lane, int b, uint8_t* rec) {
+    const float amax = warp_max(fabsf(x));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d >= FLT_MIN ? __frcp_rn(d) : 0.0f;
+    const float r = fminf(fmaxf(roundf(__fmul_rn(x, id)), -127.0f), 127.0f);
+    const int q = static_cast<int>(r);
+    const __half dh = __float2half_rn(d);
+    rec[16 + 32 * b + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    if (lane == 0) *reinterpret_cast<uint16_t*>(rec + 2 * b) = __half_as_ushort(dh);
+    return __fmul_rn(__half2float(dh), static_cast<float>(q));
+}
+
+// One warp quantizes one 32-value q5_1 block of a V record (lane = value).
+__device__ __forceinline__ float kvq_put_q5_1(float x, int lane, int b, uint8_t* rec) {
+    const float lo = -warp_max(-x), hi = warp_max(x);
+    const float d = __fdiv_rn(__fsub_rn(hi, lo), 31.0f);
+    const float id = d >= FLT_MIN ? __frcp_rn(d) : 0.0f;
+    const float r = fminf(fmaxf(roundf(__fmul_rn(__fsub_rn(x, lo), id)), 0.0f), 31.0f);
+    const int q = static_cast<int>(r);
+    const unsigned qh = __ballot_sync(0xffffffffu, (q >> 4) & 1);
+    const int q_hi = __shfl_down_sync(0xffffffffu, q, 16);
+    const __half dh = __float2half_rn(d), mh = __float2half_rn(lo);
+    if (lane < 16) rec[64 + 16 * b + lane] = static_cast<uint8_t>((q & 15) | ((q_hi & 15) << 4));
+    if (lane == 0) {
+        *reinterpret_cast<uint32_t*>(rec + 4 * b) =
+            static_cast<uint32_t>(__half_as_ushort(dh)) | (static_cast<uint32_t>(__half_as_ushort(mh)) << 16);
+        *reinterpret_cast<uint32_t*>(rec + 32 + 4 * b) = qh;
+    }
+    return __fadd_rn(__fmul_rn(__half2float(dh), static_cast<float>(q)), __half2float(mh));
+}
+
+// The lane's 8 dims (dim8 order) of a K record, dequantized.
+__device__ __forceinline__ void kvq_k8(const uint8_t* rec, int lane, float* v) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = 4 * h + (lane >> 3);
+        const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + 2 * b)));
+        const uint32_t c = *reinterpret_cast<const uint32_t*>(rec + 16 + 128 * h + 4 * lane);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[4 * h + j] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>((c >> (8 * j)) & 0xffu)));
+    }
+}
+
+// The lane's 8 dims (dim8 order) of a V record, dequantized.
+__device__ __forceinline__ void kvq_v8(const uint8_t* rec, int lane, float* v) {
+    const int j0 = 4 * (lane & 7);  // the lane's first value inside its blocks
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = 4 * h + (lane >> 3);
+        const uint32_t dm = *reinterpret_cast<const uint32_t*>(rec + 4 * b);
+        const float d = __half2float(__ushort_as_half(static_cast<uint16_t>(dm & 0xffffu)));
+        const float m = __half2float(__ushort_as_half(static_cast<uint16_t>(dm >> 16)));
+        const uint32_t qh = *reinterpret_cast<const uint32_t*>(rec + 32 + 4 * b);
+        const uint32_t qs = *reinterpret_cast<const uint32_t*>(rec + 64 + 16 * b + (j0 & 15));
+        const int sh = j0 < 16 ? 0 : 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = static_cast<int>((qs >> (8 * j + sh)) & 15u) | static_cast<int>(((qh >> (j0 + j)) & 1u) << 4);
+            v[4 * h + j] = __fadd_rn(__fmul_rn(d, static_cast<float>(q)), m);
+        }
+    }
+}
 
 }  // namespace qg
