@@ -46,16 +46,21 @@ WORKLOADS = {
     "4b": (synth.CFG_4B, "random-init 4B-shaped hybrid: 32 layers (24 Gated DeltaNet + 8 full attention), "
                          "hidden 2560, FFN 9216, vocab 248320, 32 v-heads over 16 k-heads; "
                          "850 seeded prompt tokens then greedy decode"),
-    "4b-long": (synth.CFG_4B_LONG, "4B-shaped hybrid, f32 KV cache of 8192 positions prefilled with N(0,1) rows "
+    "4b-long": (synth.CFG_4B_LONG, "4B-shaped hybrid, KV cache of 8192 positions prefilled with N(0,1) rows "
                                    "0..7999, greedy decode from position 8000"),
 }
 
 
-def algorithmic_bytes(cfg, t_rows):
+KV_FORMATS = {"f32": 0, "q8_0-q5_1": 1}  # qg_state_create_kv formats
+KV_DESC = {"f32": "f32 K/V cache", "q8_0-q5_1": "q8_0 K / q5_1 V cache (272 + 192 bytes per position and kv head)"}
+
+
+def algorithmic_bytes(cfg, t_rows, kv="f32"):
     """HBM bytes one token must move at KV length t_rows (rows read, incl. the
     new one): every weight as stored (Q4_K 144 B / Q6_K 210 B per 256), the f32
     vectors the kernels read, DeltaNet state and conv window read + write, the
-    KV rows read plus the K/V row written, the embedding row."""
+    KV rows read plus the K/V row written (f32 rows, or the quantized records
+    plus the f32 V row the quantizer reads), the embedding row."""
     H, F = cfg.hidden, cfg.ffn
     q4 = lambda n, k: n * k // 256 * 144  # noqa: E731
     q6 = lambda n, k: n * k // 256 * 210  # noqa: E731
@@ -69,7 +74,11 @@ def algorithmic_bytes(cfg, t_rows):
             total += 2 * cfg.conv_dim * (cfg.conv_kernel - 1) * 4              # window r + w
         else:
             total += q4(2 * cfg.q_dim + 2 * cfg.kv_dim, H) + q4(H, cfg.q_dim) + 2 * cfg.head_dim * 4
-            total += 2 * t_rows * cfg.kv_dim * 4 + 2 * cfg.kv_dim * 4            # KV read + row write
+            if kv == "f32":
+                total += 2 * t_rows * cfg.kv_dim * 4 + 2 * cfg.kv_dim * 4        # KV read + row write
+            else:
+                rec = cfg.n_kv_heads * (272 + 192)
+                total += t_rows * rec + rec + 2 * cfg.kv_dim * 4                 # records r/w, V row w + r
     total += q6(cfg.vocab, H) + H * 4 + H * 4                                   # lm_head, out norm, embed row
     return total
 
@@ -200,13 +209,13 @@ def prefill(qg, m, st, cfg, long_ctx, n_prompt=synth.PROMPT_LEN):
     return len(toks), tok
 
 
-def cpu_baseline(cfg, budget_s=12.0):
+def cpu_baseline(cfg, budget_s=12.0, kv="f32"):
     """The oracle as it stands, on the host cores, decoding the workload's prompt
     from position 0 until the time budget is spent."""
     import oracle
     w = synth.make_model_weights(cfg)
     om = oracle.Model(w)
-    ost = oracle.State(om)
+    ost = oracle.State(om, KV_FORMATS[kv])
     toks = synth.prompt_tokens(cfg)
     n, t0 = 0, time.perf_counter()
     while n < len(toks) and (n < 2 or time.perf_counter() - t0 < budget_s):
@@ -228,7 +237,8 @@ def run_ours(args, rank, world, local):
     w = synth.make_model_weights(cfg)
     m = qg.Model(w, device=local)
     mode = qg.STEP_PERSISTENT if args.step_mode == "persistent" else qg.STEP_KERNELS
-    st = qg.State(m, cfg.max_seq_len)
+    kvf = KV_FORMATS[args.kv_format]
+    st = qg.State(m, cfg.max_seq_len, kvf)
     st.set_step_mode(mode)
     # warm up (graph capture, clocks), then restart the sequence for the timed run
     pos, _ = prefill(qg, m, st, cfg, long_ctx, args.prompt)
@@ -255,7 +265,7 @@ def run_ours(args, rank, world, local):
     # e2e: the host API, one decode_token per step on a second state
     dt2 = None
     if not args.no_e2e:
-        st2 = qg.State(m, cfg.max_seq_len)
+        st2 = qg.State(m, cfg.max_seq_len, kvf)
         st2.set_step_mode(mode)
         p2, tok = prefill(qg, m, st2, cfg, long_ctx, args.prompt)
         ext2 = torch.cuda.ExternalStream(st2.stream)
@@ -296,14 +306,15 @@ def run_ours(args, rank, world, local):
 
     tokps = world * K / dt
     mean_t = pos0 + (K + 1) / 2.0  # KV rows read, averaged over the timed steps
-    bpt = algorithmic_bytes(cfg, mean_t)
+    bpt = algorithmic_bytes(cfg, mean_t, args.kv_format)
     step_gbs = bpt * K / dt / 1e9 * world
     out = {
         "metric": METRIC, "value": round(tokps, 3), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(1000.0 * dt / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
         "config": {"workload": f"{args.workload}: {desc}", "global_batch": world, "seq_len": cfg.max_seq_len,
-                   "parallelism": f"replicas x{world}", "step_mode": args.step_mode, "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
+                   "parallelism": f"replicas x{world}", "step_mode": args.step_mode,
+                   "kv_cache": KV_DESC[args.kv_format], "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
                    "l2": f"no flush: {bpt / 1e6:.1f} MB of weights and state per token > 129 MB L2",
                    "greedy_tokens_head": [int(t) for t in toks[:4]]},
         "bytes_per_token": int(bpt),
@@ -320,7 +331,7 @@ def run_ours(args, rank, world, local):
         "kernels_per_token": int(nodes),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg)
+        out["cpu_baseline"] = cpu_baseline(cfg, kv=args.kv_format)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -333,7 +344,7 @@ def run_reference(args, rank, world):
     K, W = args.steps, args.warmup
     w = synth.make_model_weights(cfg)
     om = oracle.Model(w)
-    ost = oracle.State(om)
+    ost = oracle.State(om, KV_FORMATS[args.kv_format])
     toks = synth.prompt_tokens(cfg)
     for i in range(W):
         oracle.forward_token(om, ost, int(toks[i]), i)
@@ -348,7 +359,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(1000.0 * dt / K, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
-        "config": {"workload": f"{args.workload}: {desc}", "global_batch": 1, "seq_len": cfg.max_seq_len},
+        "config": {"workload": f"{args.workload}: {desc}", "global_batch": 1, "seq_len": cfg.max_seq_len,
+                   "kv_cache": KV_DESC[args.kv_format]},
         "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -438,6 +450,8 @@ def main():
     ap.add_argument("--prompt", type=int, default=synth.PROMPT_LEN,
                     help="prompt tokens fed before the timed decode (default 850)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", choices=sorted(KV_FORMATS), default="f32",
+                    help="KV cache format of the decode state (and of the oracle's, on the reference arm)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
     ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
                     help="whole-token step: one kernel per fused op, or one persistent launch")
