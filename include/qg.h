@@ -209,6 +209,26 @@ int qg_state_stats(const qg_state* s, qg_stats* out);
  * neither 0 nor ceil(vocab/32), QG_ERR_ARG for a NULL state or mask. */
 int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
 
+/* Batched prompt prefill (the decode session's batched prefill,
+ * forward_qwen35_cuda.rs): tokens[0..n_tokens) (HOST) at positions
+ * pos0..pos0+n_tokens-1 go through the layers in chunks of up to 256 tokens,
+ * each projection one multi-token GEMM (weights read once per chunk), the conv
+ * and delta-rule recurrences token by token inside one kernel per layer, and
+ * causal attention over cache rows 0..pos for each token.  It leaves the state
+ * a token-by-token decode of the same tokens leaves (conv windows, recurrent
+ * states, K/V rows in the state's cache format, the residual stream of the
+ * last token, kv_len >= pos0 + n_tokens) and writes to *next_token the argmax
+ * of the last token's logits (under the state's token mask): the first
+ * generated token, to be fed to qg_decode_token at position pos0 + n_tokens.
+ * The first call on a state allocates its scratch (about 256 x (hidden x 3 +
+ * 8 x hidden + 3 x ffn + the input projection's width) floats), kept until
+ * qg_state_destroy; later calls allocate nothing.  Synchronous.
+ * Errors: QG_ERR_ARG (NULL, or a state of another model), QG_ERR_SHAPE
+ * (n_tokens < 1, head_k_dim != 128, a GQA group other than 1, 2, 4),
+ * QG_ERR_POS (positions past the cache), QG_ERR_TOKEN, QG_ERR_OOM,
+ * QG_ERR_CUDA, QG_ERR_TIMEOUT. */
+int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int n_tokens, int pos0, uint32_t* next_token);
+
 /* How the whole-token calls (qg_decode_token, qg_decode_greedy) run a step:
  * QG_STEP_KERNELS (the default): one kernel per fused op, chained with
  * programmatic dependent launch inside the step's CUDA graph;

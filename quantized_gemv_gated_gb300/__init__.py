@@ -34,7 +34,7 @@ EXPORTS = [
     "qg_argmax_f32",
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
-    "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records",
+    "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records", "qg_prefill",
 ]
 
 
@@ -105,6 +105,7 @@ def lib():
             "qg_model_destroy": [p],
             "qg_state_create": [p, i, ctypes.POINTER(p)],
             "qg_state_create_kv": [p, i, i, ctypes.POINTER(p)],
+            "qg_prefill": [p, p, p, i, i, ctypes.POINTER(ctypes.c_uint32)],
             "qg_state_kv_format": [p, ctypes.POINTER(i)],
             "qg_state_download_kv_records": [p, i, p, p, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "qg_state_destroy": [p],
@@ -409,6 +410,15 @@ def qg_attn_decode_step(model, state, il, hidden, pos, stream=None):
 def qg_decode_token(model, state, token, pos):
     out = ctypes.c_uint32()
     _check(lib().qg_decode_token(model.handle, state.handle, int(token), int(pos), ctypes.byref(out)))
+    return out.value
+
+
+def qg_prefill(model, state, tokens, pos0=0):
+    """Batched prompt prefill of `tokens` at positions pos0.. (qg_prefill);
+    returns the first generated token."""
+    t = np.ascontiguousarray(tokens, np.uint32).reshape(-1)
+    out = ctypes.c_uint32()
+    _check(lib().qg_prefill(model.handle, state.handle, _host(t), int(t.size), int(pos0), ctypes.byref(out)))
     return out.value
 
 

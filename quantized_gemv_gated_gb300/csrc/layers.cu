@@ -563,18 +563,24 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
 // Grid (rows, n_kv): one CTA per (position, kv head), warp w makes block w
 // of its K and V records with the append's quantizer.
 __global__ void __launch_bounds__(256) kv_quantize_kernel(const float* __restrict__ k, const float* __restrict__ v,
-                                                          int n_kv, int max_seq, uint8_t* kq, uint8_t* vq) {
+                                                          int n_kv, int max_seq, int pos0, uint8_t* kq, uint8_t* vq) {
     const int t = blockIdx.x, g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t src = (static_cast<size_t>(t) * n_kv + g) * kHd + 32 * warp + lane;
-    const size_t rec = static_cast<size_t>(g) * max_seq + t;
+    const size_t rec = static_cast<size_t>(g) * max_seq + pos0 + t;
     kvq_put_q8_0(k[src], lane, warp, kq + rec * kKRec);
     kvq_put_q5_1(v[src], lane, warp, vq + rec * kVRec);
 }
 
 int kv_quantize_rows(const float* k, const float* v, int rows, int n_kv, int max_seq, uint8_t* kq, uint8_t* vq,
                      cudaStream_t st) {
+    return kv_quantize_rows_at(k, v, rows, 0, n_kv, max_seq, kq, vq, st);
+}
+
+int kv_quantize_rows_at(const float* k, const float* v, int rows, int pos0, int n_kv, int max_seq, uint8_t* kq,
+                        uint8_t* vq, cudaStream_t st) {
     if (rows <= 0) return QG_OK;
-    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, kq, vq);
+    if (pos0 < 0 || pos0 + rows > max_seq) return set_err(QG_ERR_POS, "kv_quantize: rows past the cache");
+    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, pos0, kq, vq);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
@@ -671,6 +677,22 @@ int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, c
     return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden,
                                       norm_pro(a, s, true, m->out_norm, nullptr, h_final, c.eps, c.hidden), ea, st, true,
                                       s->err);
+}
+
+// Output norm of a (no pending y; stored to s->h) + fused lm_head GEMV + argmax
+// -> slots[0] / slots[2]; no history, no position move (the end of a prefill).
+int run_lmhead_of(const qg_model* m, qg_state* s, const float* a, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    EpiArgmaxStep ea{};
+    ea.ws = s->am_ws;
+    ea.slots = s->slots;
+    ea.hist = s->hist;
+    ea.err = s->err;
+    ea.allow = s->allow;
+    ea.advance = 0;
+    return launch_gemv<QT_Q6K, false>(m->lm_head, nullptr, c.vocab, c.hidden,
+                                      norm_pro(a, s, false, m->out_norm, nullptr, s->h, c.eps, c.hidden), ea, st,
+                                      false, s->err);
 }
 
 }  // namespace qg

@@ -13,17 +13,6 @@ using namespace qg;
 
 namespace {
 
-struct DeviceGuard {
-    int prev = -1;
-    explicit DeviceGuard(int dev) {
-        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
-        if (prev != dev) cudaSetDevice(dev);
-    }
-    ~DeviceGuard() {
-        int cur = -1;
-        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-    }
-};
 
 template <class T>
 int dalloc(std::vector<void*>& list, T** p, size_t count, uint64_t* counter = nullptr) {
@@ -372,6 +361,7 @@ int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_sta
     s->kv_len = 0;
     s->exec_step = nullptr;
     s->exec_greedy = nullptr;
+    s->pf = nullptr;
     s->step = nullptr;
     s->step_mode = QG_STEP_KERNELS;
     s->step_grid = s->step_smem = 0;
@@ -468,6 +458,7 @@ int qg_state_destroy(qg_state* s) {
     if (s->exec_greedy) cudaGraphExecDestroy(s->exec_greedy);
     if (s->stream) cudaStreamDestroy(s->stream);
     if (s->pinned) cudaFreeHost(s->pinned);
+    prefill_release(s);
     free_all(s->allocs);
     delete s->step;
     delete s;

@@ -1,0 +1,680 @@
+// Batched prompt prefill: a chunk of prompt tokens goes through every layer
+// together, so each projection is one multi-token GEMM that reads its weights
+// once per chunk instead of once per token (the decode session's batched
+// prefill, forward_qwen35_cuda.rs).  The recurrences stay exact token-by-token
+// recurrences inside one kernel per layer: the causal conv scans each channel
+// over the chunk, the delta rule walks the chunk with each warp's four state
+// rows in registers, and the attention of token p reads the cache rows
+// 0..pos0+p (causal).  The state it leaves (conv windows, recurrent states, K/V
+// rows, the residual stream) is the state the token-by-token decode leaves,
+// and the lm_head argmax of the last token is the first generated token.
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "qg_layers.cuh"
+
+namespace qg {
+namespace {
+
+constexpr int kPfRows = 64;    // weight rows per GEMM tile
+constexpr int kPfTok = 64;     // tokens per GEMM tile
+constexpr int kPfLd = 260;     // shared-memory row stride of the tiles (floats; 16-byte aligned rows)
+constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
+constexpr int kPfMaxSplit = 8; // K splits of the projections back to the hidden size
+
+__device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return static_cast<uint16_t>(p[0] | (p[1] << 8)); }
+
+// Weights [64 c, 64 c + 64) of one 144-byte GGUF Q4_K block (sub-blocks 2c and
+// 2c + 1: the low then the high nibbles of bytes 32c..32c+31), as f32:
+// d * scale_j * q - dmin * min_j with the 6-bit scales and mins of sub-block j.
+__device__ void q4k_piece(const uint8_t* blk, int c, float* out) {
+    const float d = f16_to_f32(ld16(blk)), dmin = f16_to_f32(ld16(blk + 2));
+    const uint8_t* sc = blk + 4;
+    const uint8_t* q = blk + 16 + 32 * c;
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+        const int j = 2 * c + hi;
+        int s, m;
+        if (j < 4) {
+            s = sc[j] & 63;
+            m = sc[j + 4] & 63;
+        } else {
+            s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+            m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+        }
+        const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
+        for (int i = 0; i < 32; ++i) {
+            const int v = hi ? (q[i] >> 4) : (q[i] & 15);
+            out[32 * hi + i] = ds * static_cast<float>(v) - dm;
+        }
+    }
+}
+
+// The 64 weights of record (rr, cq = 2 half + part) of a planar Q6_K
+// group-block (the layout of qg_q6k_to_planar), written at their places in the
+// row's 256: 128 half + 16 part + i + 32 s, s = 0..3, i < 16, each
+// d * scale_s * (6-bit code - 32).
+__device__ void q6k_piece(const uint8_t* gb, int rr, int cq, float* row) {
+    const int u = 4 * rr + cq, half = cq >> 1, part = cq & 1;
+    const uint8_t* rec = gb + 48 * u;
+    const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
+    float ds[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) ds[s] = d * static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + s]));
+    float* o = row + 128 * half + 16 * part;
+    for (int i = 0; i < 16; ++i) {
+        const int a = rec[i], b = rec[16 + i], h = rec[32 + i];
+        o[i] = ds[0] * static_cast<float>(((a & 15) | ((h & 3) << 4)) - 32);
+        o[32 + i] = ds[1] * static_cast<float>(((b & 15) | (((h >> 2) & 3) << 4)) - 32);
+        o[64 + i] = ds[2] * static_cast<float>(((a >> 4) | (((h >> 4) & 3) << 4)) - 32);
+        o[96 + i] = ds[3] * static_cast<float>(((b >> 4) | (((h >> 6) & 3) << 4)) - 32);
+    }
+}
+
+// Y[z][t][row] = sum over the super-blocks of split z of W[row] . X[t], for a
+// planar Q4_K / Q6_K W [n x k] and f32 X [P][ldx].  Grid (ceil(n/64),
+// ceil(P/64), splits), 256 threads: per super-block the CTA dequantizes its 64
+// rows (one 64-weight piece per thread) and loads its 64 tokens' 256 inputs
+// into shared memory, then each thread accumulates 4 rows x 4 tokens (rows
+// rg + 16 i, tokens tg + 16 j) in k order.
+template <int QT>
+__global__ void __launch_bounds__(256) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                      const float* __restrict__ X, int ldx, float* __restrict__ Y,
+                                                      int ldy, size_t split_stride, int P, int sb_per_split) {
+    extern __shared__ __align__(16) float smf[];
+    float* Ws = smf;                   // [64 rows][kPfLd]
+    float* Xs = smf + kPfRows * kPfLd; // [64 tokens][kPfLd]
+    const int tid = threadIdx.x, rg = tid & 15, tg = tid >> 4;
+    const int row0 = blockIdx.x * kPfRows, tok0 = blockIdx.y * kPfTok;
+    const int nb = k / 256, n8 = (n + 7) & ~7;
+    const int b0 = blockIdx.z * sb_per_split, b1 = min(nb, b0 + sb_per_split);
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int b = b0; b < b1; ++b) {
+        {
+            const int gl = tid >> 5, u = tid & 31, rr = u >> 2, c = u & 3;  // group, row in group, piece
+            const int gi = row0 / 8 + gl;
+            float* wrow = Ws + (gl * 8 + rr) * kPfLd;
+            if (gi < n8 / 8) {
+                const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, QT == QT_Q6K ? 1680 : 1152);
+                if (QT == QT_Q6K) q6k_piece(gb, rr, c, wrow);
+                else q4k_piece(gb + 144 * rr, c, wrow + 64 * c);
+            } else {
+                for (int i = 0; i < 64; ++i) wrow[64 * c + i] = 0.0f;
+            }
+        }
+        for (int e = tid; e < kPfTok * 64; e += 256) {
+            const int t = e >> 6, q4 = e & 63;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (tok0 + t < P) v = *reinterpret_cast<const float4*>(X + static_cast<size_t>(tok0 + t) * ldx + 256 * b + 4 * q4);
+            *reinterpret_cast<float4*>(Xs + t * kPfLd + 4 * q4) = v;
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int kk = 0; kk < 256; kk += 4) {
+            float4 w[4], x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4*>(Ws + (rg + 16 * i) * kPfLd + kk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(Xs + (tg + 16 * j) * kPfLd + kk);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float a = fmaf(w[i].x, x[j].x, acc[i][j]);
+                    a = fmaf(w[i].y, x[j].y, a);
+                    a = fmaf(w[i].z, x[j].z, a);
+                    acc[i][j] = fmaf(w[i].w, x[j].w, a);
+                }
+        }
+        __syncthreads();
+    }
+    float* Yz = Y + blockIdx.z * split_stride;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = row0 + rg + 16 * i, t = tok0 + tg + 16 * j;
+            if (r < n && t < P) Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
+        }
+}
+
+// X[p] = E[tok[p]].  Grid P.
+__global__ void pf_embed_kernel(const float* __restrict__ E, const int* __restrict__ tok, int H, float* __restrict__ X) {
+    const int p = blockIdx.x;
+    const float* src = E + static_cast<size_t>(tok[p]) * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) X[static_cast<size_t>(p) * H + i] = src[i];
+}
+
+// X[p] += the `parts` split sums (in split order); then, when w is given,
+// Xn[p] = RMSNorm(X[p]) * w.  Grid P, 256 threads.
+__global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts,
+                                                          size_t split_stride, const float* __restrict__ w,
+                                                          float* __restrict__ Xn, int H, float eps) {
+    __shared__ float red[8];
+    const int p = blockIdx.x, tid = threadIdx.x;
+    float* x = X + static_cast<size_t>(p) * H;
+    float ss = 0.0f;
+    for (int i = tid; i < H; i += 256) {
+        float v = x[i];
+        if (parts > 0) {
+            float y = Yp[static_cast<size_t>(p) * H + i];
+            for (int z = 1; z < parts; ++z) y += Yp[z * split_stride + static_cast<size_t>(p) * H + i];
+            v += y;
+            x[i] = v;
+        }
+        ss = fmaf(v, v, ss);
+    }
+    if (!w) return;
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i];
+    const float r = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
+    for (int i = tid; i < H; i += 256) Xn[static_cast<size_t>(p) * H + i] = (x[i] * r) * w[i];
+}
+
+// Causal conv1d + SiLU of the qkv rows over the chunk, one thread per channel
+// scanning the tokens (window carried in registers, written back at the end),
+// and the alpha/beta gates of every token.  Z rows [qkv C | alpha nv | beta nv | z].
+__global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P, int C, int nv, int K,
+                                     float* __restrict__ win, const float* __restrict__ wconv,
+                                     const float* __restrict__ dt_bias, const float* __restrict__ a,
+                                     float* __restrict__ Cq, float* __restrict__ dt, float* __restrict__ beta) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c < C) {
+        float wv[kMaxConvTaps], kw[kMaxConvTaps];
+        for (int t = 0; t < K; ++t) kw[t] = wconv[static_cast<size_t>(c) * K + t];
+        for (int t = 0; t < K - 1; ++t) wv[t] = win[static_cast<size_t>(c) * (K - 1) + t];
+        for (int p = 0; p < P; ++p) {
+            const float v = Z[static_cast<size_t>(p) * ldz + c];
+            float acc = 0.0f;
+            for (int t = 0; t < K - 1; ++t) acc += kw[t] * wv[t];
+            acc += kw[K - 1] * v;
+            Cq[static_cast<size_t>(p) * C + c] = silu(acc);
+            for (int t = 1; t < K - 1; ++t) wv[t - 1] = wv[t];
+            wv[K - 2] = v;
+        }
+        for (int t = 0; t < K - 1; ++t) win[static_cast<size_t>(c) * (K - 1) + t] = wv[t];
+    } else if (c < C + nv) {
+        const int h = c - C;
+        for (int p = 0; p < P; ++p) {
+            dt[p * nv + h] = softplus(Z[static_cast<size_t>(p) * ldz + C + h] + dt_bias[h]) * a[h];
+            beta[p * nv + h] = sigmoid(Z[static_cast<size_t>(p) * ldz + C + nv + h]);
+        }
+    }
+}
+
+// Per-head L2 norm of each token's q and k (head_k_dim 128): one warp per
+// (token, q|k, key head); QKn [P][2][nk][128].
+__global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, int nk, int P, float eps,
+                                 float* __restrict__ QKn) {
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (wid >= P * 2 * nk) return;
+    const int p = wid / (2 * nk), r = wid - p * 2 * nk, which = r / nk, kh = r - which * nk;
+    const float4 v = *reinterpret_cast<const float4*>(Cq + static_cast<size_t>(p) * C + which * kdim + kh * kDk + 4 * lane);
+    float ss = v.x * v.x;
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+    ss = warp_sum(ss);
+    const float rr = 1.0f / sqrtf(ss + eps);
+    *reinterpret_cast<float4*>(QKn + (static_cast<size_t>(wid)) * kDk + 4 * lane) =
+        make_float4(v.x * rr, v.y * rr, v.z * rr, v.w * rr);
+}
+
+// The delta rule over the chunk: CTA = 32 state rows of one value head, each
+// warp 4 rows held in registers (lane: dims 4 lane..+3) for the whole chunk;
+// per token decay, read, rank-1 update and query as the decode step does
+// (delta_rows4), with the next token's inputs loaded ahead.  O [P][v_dim].
+__global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq, int C, int kdim,
+                                                       const float* __restrict__ QKn, const float* __restrict__ dt,
+                                                       const float* __restrict__ beta, float* __restrict__ S,
+                                                       float* __restrict__ O, int P, int nk, int nv, int dv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_head = dv / 32;
+    const int h = blockIdx.x / per_head, j = (blockIdx.x - h * per_head) * 32 + 4 * warp;
+    const int kh = h % nk;
+    const int vd = nv * dv;
+    float4 st[4];
+    float* Sg = S + (static_cast<size_t>(h) * dv + j) * kDk;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) st[t] = *reinterpret_cast<const float4*>(Sg + t * kDk + 4 * lane);
+    const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
+    auto load = [&](int p, float4& kk, float4& qq, float& vl, float& g, float& be) {
+        const float* base = QKn + static_cast<size_t>(p) * 2 * nk * kDk;
+        qq = *reinterpret_cast<const float4*>(base + kh * kDk + 4 * lane);
+        kk = *reinterpret_cast<const float4*>(base + (nk + kh) * kDk + 4 * lane);
+        vl = lane < 4 ? Cq[static_cast<size_t>(p) * C + 2 * kdim + h * dv + j + lane] : 0.0f;
+        g = dt[p * nv + h];
+        be = beta[p * nv + h];
+    };
+    float4 kk, qq, kn, qn;
+    float vl, g, be, vn = 0.0f, gn = 0.0f, ben = 0.0f;
+    load(0, kk, qq, vl, g, be);
+    for (int p = 0; p < P; ++p) {
+        if (p + 1 < P) load(p + 1, kn, qn, vn, gn, ben);
+        const float gd = expf(g);
+        float4 rr[4];
+        float dot[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            rr[t] = make_float4(gd * st[t].x, gd * st[t].y, gd * st[t].z, gd * st[t].w);  // decay
+            float d = rr[t].x * kk.x;
+            d = fmaf(rr[t].y, kk.y, d);
+            d = fmaf(rr[t].z, kk.z, d);
+            dot[t] = fmaf(rr[t].w, kk.w, d);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) dot[t] += __shfl_xor_sync(0xffffffffu, dot[t], off);  // read
+        float oq[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float d = be * (__shfl_sync(0xffffffffu, vl, t) - dot[t]);
+            st[t] = make_float4(fmaf(kk.x, d, rr[t].x), fmaf(kk.y, d, rr[t].y), fmaf(kk.z, d, rr[t].z),
+                                fmaf(kk.w, d, rr[t].w));  // rank-1 update
+            float q = st[t].x * qq.x;
+            q = fmaf(st[t].y, qq.y, q);
+            q = fmaf(st[t].z, qq.z, q);
+            oq[t] = fmaf(st[t].w, qq.w, q);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) oq[t] += __shfl_xor_sync(0xffffffffu, oq[t], off);  // query
+        float mine = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (lane == t) mine = oq[t] * scale;
+        if (lane < 4) O[static_cast<size_t>(p) * vd + h * dv + j + lane] = mine;
+        kk = kn;
+        qq = qn;
+        vl = vn;
+        g = gn;
+        be = ben;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) *reinterpret_cast<float4*>(Sg + t * kDk + 4 * lane) = st[t];
+}
+
+// Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h).  Grid P,
+// one warp per head (head_v_dim 32/64/128: 1, 2 or 4 values per lane).
+__global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restrict__ O, const float* __restrict__ Z,
+                                                            int ldz, int zoff, const float* __restrict__ w, int nv,
+                                                            int dv, float eps, float* __restrict__ U) {
+    const int p = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = dv / 32;
+    for (int h = warp; h < nv; h += 8) {
+        const float* o = O + static_cast<size_t>(p) * nv * dv + h * dv;
+        const float* z = Z + static_cast<size_t>(p) * ldz + zoff + h * dv;
+        float ov[4], ss = 0.0f;
+        for (int e = 0; e < per; ++e) {
+            ov[e] = o[lane + 32 * e];
+            ss = fmaf(ov[e], ov[e], ss);
+        }
+        ss = warp_sum(ss);
+        const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
+        for (int e = 0; e < per; ++e) {
+            const int i = lane + 32 * e;
+            U[static_cast<size_t>(p) * nv * dv + h * dv + i] = ((ov[e] * rn) * w[i]) * silu(z[i]);
+        }
+    }
+}
+
+// Attention inputs of token p (position pos0 + p): per-head RMSNorm and
+// partial NEOX rope of q (to Qn [P][nh][256]) and k, and the K and V rows
+// (to the f32 cache rows, or to staging rows for the quantizer).  Grid P.
+__global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restrict__ Z, int ldz, int nh, int nkv,
+                                                           const float* __restrict__ q_norm,
+                                                           const float* __restrict__ k_norm, int pos0, int n_rot,
+                                                           float theta_scale, float eps, float* __restrict__ Qn,
+                                                           float* __restrict__ Krow, float* __restrict__ Vrow,
+                                                           size_t row_stride) {
+    __shared__ float cs[kHd / 2], sn[kHd / 2];
+    __shared__ __align__(16) float vec[8][kHd];
+    const int p = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = n_rot / 2, qd = nh * kHd, kvd = nkv * kHd;
+    const int pos = pos0 + p;
+    if (tid < half) {  // theta_0 = pos, theta_{i+1} = theta_i * theta_scale (f32 running product)
+        float th = static_cast<float>(pos);
+        for (int i = 0; i < tid; ++i) th = th * theta_scale;
+        float sv, cv;
+        sincosf(th, &sv, &cv);
+        cs[tid] = cv;
+        sn[tid] = sv;
+    }
+    const float* z = Z + static_cast<size_t>(p) * ldz;
+    for (int i = tid; i < kvd; i += 256) Vrow[static_cast<size_t>(p) * row_stride + i] = z[2 * qd + kvd + i];
+    __syncthreads();
+    for (int job0 = 0; job0 < nh + nkv; job0 += 8) {
+        const int job = job0 + warp;
+        if (job < nh + nkv) {
+            const float* src = job < nh ? z + static_cast<size_t>(job) * 2 * kHd : z + 2 * qd + (job - nh) * kHd;
+            const float* w = job < nh ? q_norm : k_norm;
+            float v[8];
+            row8(src, lane, v);
+            float ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+            ss = warp_sum(ss);
+            const float r = 1.0f / sqrtf(ss / static_cast<float>(kHd) + eps);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vec[warp][dim8(lane, i)] = (v[i] * r) * w[dim8(lane, i)];
+            __syncwarp();
+            for (int i = lane; i < half; i += 32) {
+                const float x0 = vec[warp][i], x1 = vec[warp][i + half];
+                vec[warp][i] = x0 * cs[i] - x1 * sn[i];
+                vec[warp][i + half] = x0 * sn[i] + x1 * cs[i];
+            }
+            __syncwarp();
+            float* dst = job < nh ? Qn + (static_cast<size_t>(p) * nh + job) * kHd
+                                  : Krow + static_cast<size_t>(p) * row_stride + (job - nh) * kHd;
+            for (int i = lane; i < kHd; i += 32) dst[i] = vec[warp][i];
+            __syncwarp();
+        }
+    }
+}
+
+// Causal GQA attention of the chunk's tokens: CTA (p, g) for the GS query
+// heads of kv group g of token p over cache rows 0..pos0+p (f32 rows, or
+// quantized records read dequantized), 8 warps taking keys t = warp mod 8 with
+// an online softmax each, then combined; the output is gated by
+// sigmoid(gate) and stored to Att [P][nh*256].
+template <int GS, bool KVQ>
+__global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
+                                                             int ldz, const float* __restrict__ kc,
+                                                             const float* __restrict__ vc, int kvd, int max_seq,
+                                                             int pos0, float* __restrict__ Att) {
+    __shared__ float wml[8][GS][2];
+    __shared__ __align__(16) float wacc[8][GS][kHd];
+    const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nh = gridDim.y * GS, t_len = pos0 + p + 1;
+    float q[GS][8], m[GS], l[GS], acc[GS][8];
+#pragma unroll
+    for (int i = 0; i < GS; ++i) {
+        row8(Qn + (static_cast<size_t>(p) * nh + g * GS + i) * kHd, lane, q[i]);
+        m[i] = -INFINITY;
+        l[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    }
+    const float scale = 1.0f / sqrtf(static_cast<float>(kHd));
+    for (int t = warp; t < t_len; t += 8) {
+        float kv[8], vv[8];
+        if constexpr (KVQ) {
+            const size_t rec = static_cast<size_t>(g) * max_seq + t;
+            kvq_k8(reinterpret_cast<const uint8_t*>(kc) + rec * kKRec, lane, kv);
+            kvq_v8(reinterpret_cast<const uint8_t*>(vc) + rec * kVRec, lane, vv);
+        } else {
+            load_row8(kc + static_cast<size_t>(t) * kvd + g * kHd, lane, kv);
+            load_row8(vc + static_cast<size_t>(t) * kvd + g * kHd, lane, vv);
+        }
+#pragma unroll
+        for (int i = 0; i < GS; ++i) {
+            float dot = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dot = fmaf(q[i][j], kv[j], dot);
+            const float sc = warp_sum(dot) * scale;
+            const float mn = fmaxf(m[i], sc);
+            const float c = expf(m[i] - mn), pr = expf(sc - mn);
+            l[i] = fmaf(l[i], c, pr);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(acc[i][j], c, pr * vv[j]);
+            m[i] = mn;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < GS; ++i) {
+        if (lane == 0) {
+            wml[warp][i][0] = m[i];
+            wml[warp][i][1] = l[i];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wacc[warp][i][dim8(lane, j)] = acc[i][j];
+    }
+    __syncthreads();
+    for (int i = 0; i < GS; ++i) {  // thread tid owns dim tid of every head
+        float M = -INFINITY;
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, wml[w][i][0]);
+        float L = 0.0f, A = 0.0f;
+        for (int w = 0; w < 8; ++w) {
+            const float mw = wml[w][i][0];
+            const float f = mw == -INFINITY ? 0.0f : expf(mw - M);
+            L = fmaf(wml[w][i][1], f, L);
+            A = fmaf(wacc[w][i][tid], f, A);
+        }
+        const int h = g * GS + i;
+        const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
+        Att[static_cast<size_t>(p) * nh * kHd + h * kHd + tid] = (A / L) * sigmoid(gt);
+    }
+}
+
+// A = silu(G) * U, elementwise.
+__global__ void pf_swiglu_kernel(const float* __restrict__ G, const float* __restrict__ U, float* __restrict__ A,
+                                 size_t n) {
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n) A[i] = silu(G[i]) * U[i];
+}
+
+// ------------------------------------------------------------ host side
+struct Scratch {
+    int chunk;
+    int* tok;
+    float *X, *Xn, *Z, *Yp, *G, *Uf, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
+};
+
+template <class T>
+int pf_alloc(qg_state* s, T** p, size_t count) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, (count ? count : 1) * sizeof(T));
+    if (e != cudaSuccess) return set_err(QG_ERR_OOM, "prefill: cudaMalloc of %zu bytes: %s", count * sizeof(T),
+                                         cudaGetErrorString(e));
+    s->allocs.push_back(q);
+    s->stats.device_allocs++;
+    *p = static_cast<T*>(q);
+    return QG_OK;
+}
+
+int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
+    if (s->pf) {
+        *out = static_cast<Scratch*>(s->pf);
+        return QG_OK;
+    }
+    const qg_config& c = m->cfg;
+    const size_t P = kPfChunk, H = c.hidden;
+    size_t n_in = 0;
+    for (int il = 0; il < c.n_layers; ++il) n_in = std::max(n_in, static_cast<size_t>(m->layers[il].n_in));
+    const size_t mid = std::max({static_cast<size_t>(m->v_dim), static_cast<size_t>(m->q_dim), size_t(1)});
+    Scratch* sc = new (std::nothrow) Scratch();
+    if (!sc) return set_err(QG_ERR_OOM, "prefill: host allocation");
+    sc->chunk = kPfChunk;
+    int rc = QG_OK;
+    (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H)) ||
+           (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, kPfMaxSplit * P * H)) ||
+           (rc = pf_alloc(s, &sc->G, P * c.ffn)) || (rc = pf_alloc(s, &sc->Uf, P * c.ffn)) ||
+           (rc = pf_alloc(s, &sc->A, P * c.ffn)) || (rc = pf_alloc(s, &sc->Cq, P * std::max(m->conv_dim, 1))) ||
+           (rc = pf_alloc(s, &sc->dt, P * (c.n_v_heads + 1))) || (rc = pf_alloc(s, &sc->beta, P * (c.n_v_heads + 1))) ||
+           (rc = pf_alloc(s, &sc->QKn, P * 2 * std::max(m->k_dim, 1))) ||
+           (rc = pf_alloc(s, &sc->O, P * std::max(m->v_dim, 1))) || (rc = pf_alloc(s, &sc->Uin, P * mid)) ||
+           (rc = pf_alloc(s, &sc->Qn, P * std::max(m->q_dim, 1))) || (rc = pf_alloc(s, &sc->Ks, P * std::max(m->kv_dim, 1))) ||
+           (rc = pf_alloc(s, &sc->Vs, P * std::max(m->kv_dim, 1))));
+    if (rc) {
+        delete sc;
+        return rc;
+    }
+    s->pf = sc;
+    *out = sc;
+    return QG_OK;
+}
+
+template <int QT>
+int gemm(const uint8_t* W, int n, int k, const float* X, int ldx, float* Y, int ldy, int P, int splits, cudaStream_t st,
+         int* used_splits) {
+    const int nb = k / 256;
+    if (splits > nb) splits = nb;
+    if (splits < 1) splits = 1;
+    const int per = (nb + splits - 1) / splits;
+    const int z = (nb + per - 1) / per;
+    if (used_splits) *used_splits = z;
+    const int smem = 2 * kPfRows * kPfLd * static_cast<int>(sizeof(float));
+    static bool configured = false;
+    if (!configured) {
+        QG_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        configured = true;
+    }
+    const dim3 grid((n + kPfRows - 1) / kPfRows, (P + kPfTok - 1) / kPfTok, z);
+    pf_gemm_kernel<QT><<<grid, 256, smem, st>>>(W, n, k, X, ldx, Y, ldy, static_cast<size_t>(P) * ldy, P, per);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+// Splits of a projection back to the hidden size: enough CTAs for two per SM.
+int splits_for(int n, int k, int P) {
+    const int ctas = ((n + kPfRows - 1) / kPfRows) * ((P + kPfTok - 1) / kPfTok);
+    int z = (2 * device_sms() + ctas - 1) / ctas;
+    return std::max(1, std::min({z, kPfMaxSplit, k / 256}));
+}
+
+template <bool KVQ>
+int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const float* kc,
+                  const float* vc, int kvd, int max_seq, int pos0, float* att) {
+    switch (gs) {
+        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
+        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
+        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
+        default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
+    }
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+// One chunk of P tokens at positions pos0.. through every layer; X holds the
+// residual stream of each token at the end (the last layer's output added).
+int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const int H = c.hidden;
+    const size_t part = static_cast<size_t>(P) * H;
+    pf_embed_kernel<<<P, 256, 0, st>>>(m->embd, sc->tok, H, sc->X);
+    QG_CUDA(cudaGetLastError());
+    int pending = 0;  // split sums of the last projection not yet added to X
+    int rc = QG_OK;
+    for (int il = 0; il < c.n_layers && !rc; ++il) {
+        const qg_layer_dev& L = m->layers[il];
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, H, c.eps);
+        QG_CUDA(cudaGetLastError());
+        if ((rc = gemm<QT_Q4K>(L.w_in, L.n_in, H, sc->Xn, H, sc->Z, L.n_in, P, 1, st, nullptr))) break;
+        int k_out;
+        if (m->kinds[il] == QG_LAYER_DELTANET) {
+            const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
+            pf_conv_gates_kernel<<<(C + 2 * nv + 127) / 128, 128, 0, st>>>(sc->Z, L.n_in, P, C, nv, c.conv_kernel,
+                                                                         s->conv[il], L.conv_w, L.dt_bias, L.a, sc->Cq,
+                                                                         sc->dt, sc->beta);
+            QG_CUDA(cudaGetLastError());
+            const int warps = P * 2 * c.n_k_heads;
+            pf_l2norm_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(sc->Cq, C, m->k_dim, c.n_k_heads, P, c.eps,
+                                                                      sc->QKn);
+            QG_CUDA(cudaGetLastError());
+            pf_delta_kernel<<<nv * dv / 32, 256, 0, st>>>(sc->Cq, C, m->k_dim, sc->QKn, sc->dt, sc->beta, s->ssm[il],
+                                                         sc->O, P, c.n_k_heads, nv, dv);
+            QG_CUDA(cudaGetLastError());
+            pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, sc->Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
+                                                    sc->Uin);
+            QG_CUDA(cudaGetLastError());
+            k_out = m->v_dim;
+        } else {
+            const int nkv = c.n_kv_heads, kvd = m->kv_dim;
+            const bool kvq = s->kv_format == QG_KV_Q8_0_Q5_1;
+            float* Kdst = kvq ? sc->Ks : s->kc[il] + static_cast<size_t>(pos0) * kvd;
+            float* Vdst = kvq ? sc->Vs : s->vc[il] + static_cast<size_t>(pos0) * kvd;
+            pf_attn_prep_kernel<<<P, 256, 0, st>>>(sc->Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, pos0, c.n_rot,
+                                                   m->theta_scale, c.eps, sc->Qn, Kdst, Vdst, kvd);
+            QG_CUDA(cudaGetLastError());
+            if (kvq && (rc = kv_quantize_rows_at(sc->Ks, sc->Vs, P, pos0, nkv, s->max_seq,
+                                                 reinterpret_cast<uint8_t*>(s->kc[il]),
+                                                 reinterpret_cast<uint8_t*>(s->vc[il]), st)))
+                break;
+            const dim3 grid(P, nkv);
+            const int gs = c.n_heads / nkv;
+            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, s->kc[il], s->vc[il], kvd, s->max_seq,
+                                           pos0, sc->Uin)
+                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, s->kc[il], s->vc[il], kvd, s->max_seq,
+                                            pos0, sc->Uin);
+            if (rc) break;
+            k_out = m->q_dim;
+        }
+        if ((rc = gemm<QT_Q4K>(L.w_out, H, k_out, sc->Uin, k_out, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending)))
+            break;
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, H, c.eps);
+        QG_CUDA(cudaGetLastError());
+        if ((rc = gemm<QT_Q4K>(L.w_gate, c.ffn, H, sc->Xn, H, sc->G, c.ffn, P, 1, st, nullptr))) break;
+        if ((rc = gemm<QT_Q4K>(L.w_up, c.ffn, H, sc->Xn, H, sc->Uf, c.ffn, P, 1, st, nullptr))) break;
+        const size_t na = static_cast<size_t>(P) * c.ffn;
+        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(sc->G, sc->Uf, sc->A, na);
+        QG_CUDA(cudaGetLastError());
+        rc = gemm<QT_Q6K>(L.w_down, H, c.ffn, sc->A, c.ffn, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
+    }
+    if (rc) return rc;
+    pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, nullptr, nullptr, H, c.eps);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+}  // namespace
+
+void prefill_release(qg_state* s) {  // the device buffers belong to s->allocs
+    delete static_cast<Scratch*>(s->pf);
+    s->pf = nullptr;
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int n_tokens, int pos0,
+                          uint32_t* next_token) {
+    if (!m || !s || !next_token) return set_err(QG_ERR_ARG, "prefill: NULL argument");
+    if (s->m != m) return set_err(QG_ERR_ARG, "prefill: state belongs to another model");
+    if (n_tokens < 1) return set_err(QG_ERR_SHAPE, "prefill: %d tokens", n_tokens);
+    if (!tokens) return set_err(QG_ERR_ARG, "prefill: NULL tokens");
+    if (pos0 < 0 || pos0 + n_tokens > s->max_seq)
+        return set_err(QG_ERR_POS, "prefill: positions %d..%d are past the KV cache (%d rows)", pos0,
+                       pos0 + n_tokens - 1, s->max_seq);
+    const qg_config& c = m->cfg;
+    for (int i = 0; i < n_tokens; ++i)
+        if (tokens[i] >= static_cast<uint32_t>(c.vocab))
+            return set_err(QG_ERR_TOKEN, "prefill: token %u is outside the %d-row embedding table", tokens[i], c.vocab);
+    if (c.head_k_dim != kDk) return set_err(QG_ERR_SHAPE, "prefill: head_k_dim %d is not served", c.head_k_dim);
+    DeviceGuard dg(m->device);
+    Scratch* sc = nullptr;
+    int rc = scratch_of(m, s, &sc);
+    if (rc) return rc;
+    cudaStream_t st = s->stream;
+    QG_CUDA(cudaStreamSynchronize(st));
+    for (int c0 = 0; c0 < n_tokens && !rc; c0 += sc->chunk) {
+        const int P = std::min(sc->chunk, n_tokens - c0);
+        QG_CUDA(cudaMemcpyAsync(sc->tok, tokens + c0, sizeof(int) * P, cudaMemcpyHostToDevice, st));
+        rc = run_chunk(m, s, sc, P, pos0 + c0, st);
+        if (!rc && c0 + P >= n_tokens)
+            rc = run_lmhead_of(m, s, sc->X + static_cast<size_t>(P - 1) * c.hidden, st);
+        if (!rc) QG_CUDA(cudaStreamSynchronize(st));  // the token copy of the next chunk reuses sc->tok
+    }
+    if (rc) return rc;
+    unsigned out = 0;
+    QG_CUDA(cudaMemcpy(&out, s->slots + 2, sizeof out, cudaMemcpyDeviceToHost));
+    if (out & 0x80000000u) {
+        unsigned e = 0;
+        cudaMemcpy(&e, s->err, sizeof e, cudaMemcpyDeviceToHost);
+        return set_err(QG_ERR_TIMEOUT, "prefill: a kernel gave up on a bounded wait (flags 0x%x)", e);
+    }
+    *next_token = out;
+    if (s->kv_len < pos0 + n_tokens) s->kv_len = pos0 + n_tokens;
+    return QG_OK;
+}

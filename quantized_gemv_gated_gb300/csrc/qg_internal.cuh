@@ -65,6 +65,7 @@ struct qg_state {
     uint32_t* allow;            // device: token mask, ceil(vocab/32) words, bit set = allowed (all set: none)
     unsigned* err;              // device error word
     int* pinned;                // pinned host: [0] token, [1] position, [2] token out
+    void* pf;                   // batched prefill scratch (made by the first qg_prefill call), or null
     int keys_per_split, max_splits;
     cudaGraphExec_t exec_step;
     cudaGraphExec_t exec_greedy;
@@ -79,6 +80,19 @@ struct qg_state {
 };
 
 namespace qg {
+
+// Makes `dev` current for a scope and restores the caller's device after it.
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
 
 // Residual-stream buffers of one layer: the layer reads a (+ the pending
 // state y when y_pending, or the embedding row of slots[0] when embed), keeps
@@ -101,6 +115,13 @@ int run_residual(qg_state* s, float* h, int n, cudaStream_t st);
 // Output norm of a + y (stored to h_final) + fused lm_head GEMV + argmax ->
 // slots[0] / slots[2]; `advance` also records hist[pos] and moves slots[1].
 int run_lmhead(const qg_model* m, qg_state* s, const float* a, float* h_final, cudaStream_t st, bool advance);
+// Output norm of a + fused lm_head GEMV + argmax, no pending y, no advance.
+int run_lmhead_of(const qg_model* m, qg_state* s, const float* a, cudaStream_t st);
+// Quantized-cache records of positions pos0..pos0+rows-1 (see kv_quantize_rows).
+int kv_quantize_rows_at(const float* k, const float* v, int rows, int pos0, int n_kv, int max_seq, uint8_t* kq,
+                        uint8_t* vq, cudaStream_t st);
+// Free the batched-prefill scratch descriptor (its device buffers are in s->allocs).
+void prefill_release(qg_state* s);
 // Persistent step kernel: fill s->step (once per state), launch one step.
 int step_setup(const qg_model* m, qg_state* s);
 int run_step(qg_state* s, cudaStream_t st, bool advance);

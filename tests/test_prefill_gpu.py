@@ -1,0 +1,146 @@
+"""Batched prompt prefill (qg_prefill) on the GPU through the C ABI, against
+the oracle decoding the same prompt token by token.
+
+Bars: the returned token equals the oracle's argmax at the last prompt
+position (exact where its top-2 margin is decisive); the residual stream of
+the last token within 1e-3 normwise; the recurrent states, conv windows and
+K/V rows the prefill leaves within the f32 bars of the layer tests; decoding
+on from the prefilled state gives the oracle's tokens; prefilling in two calls
+agrees with one call.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+qg = pytest.importorskip("quantized_gemv_gated_gb300")
+
+TOL = 1e-3
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def _oracle_prompt(om, ost, toks, pos0=0):
+    tok = hid = logits = None
+    for i, t in enumerate(toks):
+        tok, hid, logits = oracle.forward_token(om, ost, int(t), pos0 + i, want_logits=True)
+    return tok, hid, logits
+
+
+def _token_ok(got, want, logits):
+    top = np.sort(logits.astype(np.float64))[::-1]
+    tol = 1e-3 * max(1.0, float(np.max(np.abs(logits))))
+    if top[0] - top[1] > tol:
+        return got == want
+    return logits[got] >= top[0] - tol
+
+
+def _check_states(cfg, st, ost, n):
+    for il, kind in enumerate(cfg.kinds()):
+        if kind == synth.DELTANET:
+            conv, ssm = st.download_layer(il)
+            assert rel(conv, ost.conv[il]) <= 1e-4, f"layer {il}: conv window"
+            assert rel(ssm, ost.ssm[il]) <= 1e-3, f"layer {il}: recurrent state"
+        else:
+            k, v = st.download_layer(il)
+            assert k.shape[0] == n
+            assert rel(k, ost.kc[il][:n]) <= 1e-4 and rel(v, ost.vc[il][:n]) <= 1e-4, f"layer {il}: K/V rows"
+
+
+@pytest.mark.parametrize("n_prompt", [1, 37, 300])
+def test_prefill_tiny_matches_oracle(n_prompt):
+    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=320)
+    w = synth.make_model_weights(cfg)
+    m, om = qg.Model(w), oracle.Model(w)
+    toks = synth.prompt_tokens(cfg, n_prompt)
+    st, ost = qg.State(m, cfg.max_seq_len), oracle.State(om)
+    got = qg.qg_prefill(m, st, toks)
+    want, hid, logits = _oracle_prompt(om, ost, toks)
+    assert _token_ok(got, want, logits), f"token {got} vs oracle {want}"
+    assert rel(st.download_hidden(), hid) <= TOL
+    assert st.kv_len == n_prompt
+    _check_states(cfg, st, ost, n_prompt)
+    # decoding on from the prefilled state
+    tok = want
+    for i in range(6):
+        a = qg.qg_decode_token(m, st, tok, n_prompt + i)
+        tok, h2, lg = oracle.forward_token(om, ost, tok, n_prompt + i, want_logits=True)
+        assert _token_ok(a, tok, lg)
+    assert rel(st.download_hidden(), h2) <= TOL
+    qg.qg_device_status()
+
+
+def test_prefill_0p8b_shapes_and_split_calls():
+    cfg = synth.CFG_0P8B
+    w = synth.make_model_weights(cfg, dmax=5e-5)  # the varied workload: margins of order 0.03-1 logit
+    m, om = qg.Model(w), oracle.Model(w)
+    toks = synth.prompt_tokens(cfg, 48)
+    ost = oracle.State(om)
+    want, hid, logits = _oracle_prompt(om, ost, toks)
+    one = qg.State(m, cfg.max_seq_len)
+    a = qg.qg_prefill(m, one, toks)
+    assert _token_ok(a, want, logits)
+    assert rel(one.download_hidden(), hid) <= TOL
+    _check_states(cfg, one, ost, len(toks))
+    two = qg.State(m, cfg.max_seq_len)
+    qg.qg_prefill(m, two, toks[:20])
+    b = qg.qg_prefill(m, two, toks[20:], 20)
+    assert _token_ok(b, want, logits)
+    assert rel(two.download_hidden(), hid) <= TOL
+    assert rel(two.download_hidden(), one.download_hidden()) <= TOL
+    qg.qg_device_status()
+
+
+def test_prefill_quantized_cache():
+    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=128)
+    w = synth.make_model_weights(cfg)
+    m, om = qg.Model(w), oracle.Model(w)
+    toks = synth.prompt_tokens(cfg, 40)
+    st, ost = qg.State(m, cfg.max_seq_len, qg.KV_Q8_0_Q5_1), oracle.State(om, oracle.KV_Q8_0_Q5_1)
+    got = qg.qg_prefill(m, st, toks)
+    want, hid, logits = _oracle_prompt(om, ost, toks)
+    assert _token_ok(got, want, logits)
+    # every cache row is quantized on each side from its own f32 rows, so a code
+    # within ~1e-5 of a rounding boundary may differ by one step (each such code
+    # moves the residual stream by well under 1e-3, see the decode-step test)
+    assert rel(st.download_hidden(), hid) <= 5e-3
+    il = cfg.kinds().index(synth.ATTENTION)
+    K, V = st.download_kv_records(il)
+    nkv = cfg.n_kv_heads
+    Ko = np.ascontiguousarray(ost.kq[il][:40].reshape(40, nkv, 8, 34)[..., 2:]).view(np.int8).astype(np.int32)
+    Kq = np.ascontiguousarray(K.transpose(1, 0, 2)[..., 16:]).view(np.int8).reshape(40, nkv, 8, 32).astype(np.int32)
+    assert np.max(np.abs(Kq - Ko)) <= 1 and np.mean(Kq != Ko) < 1e-2
+    tok = want
+    for i in range(4):
+        a = qg.qg_decode_token(m, st, tok, 40 + i)
+        tok, _, lg = oracle.forward_token(om, ost, tok, 40 + i, want_logits=True)
+        assert _token_ok(a, tok, lg)
+
+
+def test_prefill_arguments():
+    cfg = synth.CFG_TINY
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    st = qg.State(m, cfg.max_seq_len)
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_prefill(m, st, np.zeros(0, np.uint32))
+    assert e.value.code == qg.QG_ERR_SHAPE
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_prefill(m, st, [1, 2, 3], cfg.max_seq_len - 2)
+    assert e.value.code == qg.QG_ERR_POS
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_prefill(m, st, [1, cfg.vocab])
+    assert e.value.code == qg.QG_ERR_TOKEN
+    a0 = st.stats()["device_allocs"]
+    qg.qg_prefill(m, st, [1, 2, 3])
+    a1 = st.stats()["device_allocs"]
+    qg.qg_prefill(m, st, [4, 5], 3)
+    assert st.stats()["device_allocs"] == a1 > a0  # scratch made once, then reused
