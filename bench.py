@@ -367,6 +367,68 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def run_prefill(args):
+    """One JSON line: the workload's seeded prompt prefilled in one qg_prefill
+    call (timed with CUDA events on the state's stream, the state reset
+    between runs outside the timed region) against the same prompt decoded
+    token by token (one captured-graph step per token), and the FLOP rate of
+    the prefill's projections (2 x the projection weights x tokens)."""
+    import torch
+    import quantized_gemv_gated_gb300 as qg
+    cfg, desc = WORKLOADS[args.workload]
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    kvf = KV_FORMATS[args.kv_format]
+    st = qg.State(m, cfg.max_seq_len, kvf)
+    toks = synth.prompt_tokens(cfg, args.prompt)
+    n = len(toks)
+    ext = torch.cuda.ExternalStream(st.stream)
+    first = None
+    for _ in range(max(1, args.warmup)):
+        st.reset()
+        first = qg.qg_prefill(m, st, toks)
+    times = []
+    for _ in range(max(1, args.steps // 16)):
+        st.reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ext)
+        tok = qg.qg_prefill(m, st, toks)
+        e1.record(ext)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1000.0)
+        assert tok == first
+    t_pf = sorted(times)[len(times) // 2]
+    # token by token through the decode step
+    st.reset()
+    qg.qg_decode_token(m, st, int(toks[0]), 0)
+    st.reset()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(ext)
+    for pos, t in enumerate(toks):
+        tok2 = qg.qg_decode_token(m, st, int(t), pos)
+    f1.record(ext)
+    f1.synchronize()
+    t_tw = f0.elapsed_time(f1) / 1000.0
+    qg.qg_device_status()
+    H, F = cfg.hidden, cfg.ffn
+    params = 0
+    for kind in cfg.kinds():
+        params += 3 * F * H
+        if kind == synth.DELTANET:
+            params += (cfg.conv_dim + 2 * cfg.n_v_heads + cfg.v_dim) * H + H * cfg.v_dim
+        else:
+            params += (2 * cfg.q_dim + 2 * cfg.kv_dim) * H + H * cfg.q_dim
+    flops = 2.0 * params * n
+    print(json.dumps({
+        "mode": "prefill", "workload": f"{args.workload}: {desc}", "kv_cache": KV_DESC[args.kv_format],
+        "prompt_tokens": n, "prefill_ms": round(t_pf * 1e3, 3), "prefill_tok_s": round(n / t_pf, 1),
+        "tokenwise_ms": round(t_tw * 1e3, 3), "tokenwise_tok_s": round(n / t_tw, 1),
+        "speedup": round(t_tw / t_pf, 2), "projection_tflops": round(flops / t_pf / 1e12, 2),
+        "same_first_token": bool(tok == tok2), "runs": len(times),
+        "arith": "f32 FMA on CUDA cores (dequantized Q4_K/Q6_K tiles in shared memory)",
+    }), flush=True)
+
+
 # GEMV shapes of the kernel mode: the building blocks at the model's shapes
 # (planar layouts, the layers' own path), lm_head with its fused argmax.
 KERNEL_SHAPES = [
@@ -455,6 +517,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
     ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
                     help="whole-token step: one kernel per fused op, or one persistent launch")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time qg_prefill of the workload's prompt against token-by-token decode (one JSON line)")
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the decode step: one JSON line per GEMV building block at the model's shapes")
     args = ap.parse_args()
@@ -464,6 +528,9 @@ def main():
         args.steps = min(args.steps, 16)  # bounded sample of the CPU oracle
     if args.kernels:
         run_kernels(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
