@@ -220,9 +220,11 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
  * last token, kv_len >= pos0 + n_tokens) and writes to *next_token the argmax
  * of the last token's logits (under the state's token mask): the first
  * generated token, to be fed to qg_decode_token at position pos0 + n_tokens.
- * The first call on a state allocates its scratch (about 256 x (hidden x 3 +
- * 8 x hidden + 3 x ffn + the input projection's width) floats), kept until
- * qg_state_destroy; later calls allocate nothing.  Synchronous.
+ * The first call on a state allocates its scratch, kept until
+ * qg_state_destroy (later calls allocate nothing): about 256 x (19 hidden +
+ * 17 ffn + 17 max(ffn, w) + w + q_dim + 2 kv_dim + ...) floats, w the widest
+ * fused input projection (16 of those terms hold the K-split partial sums;
+ * ~0.4 GB at the 4B shape).  Synchronous.
  * Errors: QG_ERR_ARG (NULL, or a state of another model), QG_ERR_SHAPE
  * (n_tokens < 1, head_k_dim != 128, a GQA group other than 1, 2, 4),
  * QG_ERR_POS (positions past the cache), QG_ERR_TOKEN, QG_ERR_OOM,

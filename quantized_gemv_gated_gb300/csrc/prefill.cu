@@ -17,130 +17,149 @@
 namespace qg {
 namespace {
 
-constexpr int kPfRows = 64;    // weight rows per GEMM tile
-constexpr int kPfTok = 64;     // tokens per GEMM tile
-constexpr int kPfLd = 260;     // shared-memory row stride of the tiles (floats; 16-byte aligned rows)
+constexpr int kGR = 128;       // weight rows per GEMM tile
+constexpr int kGT = 128;       // tokens per GEMM tile
+constexpr int kGK = 64;        // k per shared-memory stage (a quarter super-block)
 constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
-constexpr int kPfMaxSplit = 8; // K splits of the projections back to the hidden size
+constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
 
 __device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return static_cast<uint16_t>(p[0] | (p[1] << 8)); }
 
-// Weights [64 c, 64 c + 64) of one 144-byte GGUF Q4_K block (sub-blocks 2c and
-// 2c + 1: the low then the high nibbles of bytes 32c..32c+31), as f32:
-// d * scale_j * q - dmin * min_j with the 6-bit scales and mins of sub-block j.
-__device__ void q4k_piece(const uint8_t* blk, int c, float* out) {
+// Sub-block j (32 weights) of one 144-byte GGUF Q4_K block, as f32:
+// d * scale_j * q - dmin * min_j, q the low (j even) or high (j odd) nibbles
+// of bytes 32 (j/2) .. +31, with the 6-bit scale and min of sub-block j.
+__device__ __forceinline__ void q4k_sub(const uint8_t* blk, int j, float* v) {
     const float d = f16_to_f32(ld16(blk)), dmin = f16_to_f32(ld16(blk + 2));
     const uint8_t* sc = blk + 4;
-    const uint8_t* q = blk + 16 + 32 * c;
-#pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-        const int j = 2 * c + hi;
-        int s, m;
-        if (j < 4) {
-            s = sc[j] & 63;
-            m = sc[j + 4] & 63;
-        } else {
-            s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
-            m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-        }
-        const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
-        for (int i = 0; i < 32; ++i) {
-            const int v = hi ? (q[i] >> 4) : (q[i] & 15);
-            out[32 * hi + i] = ds * static_cast<float>(v) - dm;
-        }
+    int s, m;
+    if (j < 4) {
+        s = sc[j] & 63;
+        m = sc[j + 4] & 63;
+    } else {
+        s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+        m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
     }
+    const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
+    const uint8_t* q = blk + 16 + 32 * (j >> 1);
+    const int sh = (j & 1) * 4;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = ds * static_cast<float>((q[i] >> sh) & 15) - dm;
 }
 
-// The 64 weights of record (rr, cq = 2 half + part) of a planar Q6_K
-// group-block (the layout of qg_q6k_to_planar), written at their places in the
-// row's 256: 128 half + 16 part + i + 32 s, s = 0..3, i < 16, each
-// d * scale_s * (6-bit code - 32).
-__device__ void q6k_piece(const uint8_t* gb, int rr, int cq, float* row) {
-    const int u = 4 * rr + cq, half = cq >> 1, part = cq & 1;
-    const uint8_t* rec = gb + 48 * u;
+// Weights 64 q + 32 hf .. +31 of row rr of a planar Q6_K group-block (the
+// layout of qg_q6k_to_planar), as f32 d * scale * (6-bit code - 32).  They are
+// 128 h + 32 s + 16 p + i with h = q/2, s = 2 (q&1) + hf, p = 0, 1, i < 16:
+// bytes i of the records (rr, 2h + p) and their scale s.
+__device__ __forceinline__ void q6k_sub(const uint8_t* gb, int rr, int q, int hf, float* v) {
+    const int h = q >> 1, s = 2 * (q & 1) + hf;
     const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
-    float ds[4];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) ds[s] = d * static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + s]));
-    float* o = row + 128 * half + 16 * part;
-    for (int i = 0; i < 16; ++i) {
-        const int a = rec[i], b = rec[16 + i], h = rec[32 + i];
-        o[i] = ds[0] * static_cast<float>(((a & 15) | ((h & 3) << 4)) - 32);
-        o[32 + i] = ds[1] * static_cast<float>(((b & 15) | (((h >> 2) & 3) << 4)) - 32);
-        o[64 + i] = ds[2] * static_cast<float>(((a >> 4) | (((h >> 4) & 3) << 4)) - 32);
-        o[96 + i] = ds[3] * static_cast<float>(((b >> 4) | (((h >> 6) & 3) << 4)) - 32);
+    for (int p = 0; p < 2; ++p) {
+        const int u = 4 * rr + 2 * h + p;
+        const uint8_t* rec = gb + 48 * u;
+        const float ds = d * static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + s]));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int a = rec[i], b = rec[16 + i], hb = rec[32 + i];
+            int code;
+            if (s == 0) code = (a & 15) | ((hb & 3) << 4);
+            else if (s == 1) code = (b & 15) | (((hb >> 2) & 3) << 4);
+            else if (s == 2) code = (a >> 4) | (((hb >> 4) & 3) << 4);
+            else code = (b >> 4) | (((hb >> 6) & 3) << 4);
+            v[16 * p + i] = ds * static_cast<float>(code - 32);
+        }
     }
 }
 
-// Y[z][t][row] = sum over the super-blocks of split z of W[row] . X[t], for a
-// planar Q4_K / Q6_K W [n x k] and f32 X [P][ldx].  Grid (ceil(n/64),
-// ceil(P/64), splits), 256 threads: per super-block the CTA dequantizes its 64
-// rows (one 64-weight piece per thread) and loads its 64 tokens' 256 inputs
-// into shared memory, then each thread accumulates 4 rows x 4 tokens (rows
-// rg + 16 i, tokens tg + 16 j) in k order.
+// Y[z][t][row] = sum over the 64-weight quarters of split z of W[row] . X[t],
+// for a planar Q4_K / Q6_K W [n x k] and f32 X [P][ldx].  Grid (ceil(n/128),
+// ceil(P/128), splits), 256 threads.  Per 64-weight quarter of a super-block
+// the CTA dequantizes its 128 rows (thread: 32 weights of one row) into
+// Ws[k][row] and stages its 128 tokens' inputs as Xs[k][token]; each thread then
+// accumulates 8 rows x 8 tokens as outer products, in k order: rows 4 ty..+3
+// and 64 + 4 ty..+3, tokens likewise with tx, so that eight consecutive lanes
+// read 128 contiguous bytes (no bank conflicts).
 template <int QT>
-__global__ void __launch_bounds__(256) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
-                                                      const float* __restrict__ X, int ldx, float* __restrict__ Y,
-                                                      int ldy, size_t split_stride, int P, int sb_per_split) {
+__global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                         const float* __restrict__ X, int ldx, float* __restrict__ Y,
+                                                         int ldy, size_t split_stride, int P, int q_per_split) {
     extern __shared__ __align__(16) float smf[];
-    float* Ws = smf;                   // [64 rows][kPfLd]
-    float* Xs = smf + kPfRows * kPfLd; // [64 tokens][kPfLd]
-    const int tid = threadIdx.x, rg = tid & 15, tg = tid >> 4;
-    const int row0 = blockIdx.x * kPfRows, tok0 = blockIdx.y * kPfTok;
+    float* Ws = smf;              // [kGK][kGR]
+    float* Xs = smf + kGK * kGR;  // [kGK][kGT]
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int row0 = blockIdx.x * kGR, tok0 = blockIdx.y * kGT;
     const int nb = k / 256, n8 = (n + 7) & ~7;
-    const int b0 = blockIdx.z * sb_per_split, b1 = min(nb, b0 + sb_per_split);
-    float acc[4][4];
+    const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split);
+    const int dr = tid & (kGR - 1), hf = tid >> 7;  // dequantization role: row, half of the quarter
+    const int grow = row0 + dr;
+    const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
+    float acc[8][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-    for (int b = b0; b < b1; ++b) {
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int qi = q0; qi < q1; ++qi) {
+        const int b = qi >> 2, q = qi & 3;
+        const uint8_t* gb = row_ok ? W + grouped_offset(n8, nb, grow >> 3, b, QT == QT_Q6K ? 1680 : 1152) : nullptr;
         {
-            const int gl = tid >> 5, u = tid & 31, rr = u >> 2, c = u & 3;  // group, row in group, piece
-            const int gi = row0 / 8 + gl;
-            float* wrow = Ws + (gl * 8 + rr) * kPfLd;
-            if (gi < n8 / 8) {
-                const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, QT == QT_Q6K ? 1680 : 1152);
-                if (QT == QT_Q6K) q6k_piece(gb, rr, c, wrow);
-                else q4k_piece(gb + 144 * rr, c, wrow + 64 * c);
+            float v[32];
+            if (row_ok) {
+                if (QT == QT_Q6K) q6k_sub(gb, grow & 7, q, hf, v);
+                else q4k_sub(gb + 144 * (grow & 7), 2 * q + hf, v);
             } else {
-                for (int i = 0; i < 64; ++i) wrow[64 * c + i] = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
             }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Ws[(32 * hf + i) * kGR + dr] = v[i];
+            for (int e = tid; e < kGT * (kGK / 4); e += 256) {
+                const int t = e & (kGT - 1), c4 = e >> 7;
+                float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (tok0 + t < P)
+                    x = *reinterpret_cast<const float4*>(X + static_cast<size_t>(tok0 + t) * ldx + 256 * b + 64 * q + 4 * c4);
+                Xs[(4 * c4 + 0) * kGT + t] = x.x;
+                Xs[(4 * c4 + 1) * kGT + t] = x.y;
+                Xs[(4 * c4 + 2) * kGT + t] = x.z;
+                Xs[(4 * c4 + 3) * kGT + t] = x.w;
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int kk = 0; kk < kGK; ++kk) {
+                const float4 a0 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 4 * ty);
+                const float4 a1 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 64 + 4 * ty);
+                const float4 c0 = *reinterpret_cast<const float4*>(Xs + kk * kGT + 4 * tx);
+                const float4 c1 = *reinterpret_cast<const float4*>(Xs + kk * kGT + 64 + 4 * tx);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+            }
+            __syncthreads();
         }
-        for (int e = tid; e < kPfTok * 64; e += 256) {
-            const int t = e >> 6, q4 = e & 63;
-            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (tok0 + t < P) v = *reinterpret_cast<const float4*>(X + static_cast<size_t>(tok0 + t) * ldx + 256 * b + 4 * q4);
-            *reinterpret_cast<float4*>(Xs + t * kPfLd + 4 * q4) = v;
-        }
-        __syncthreads();
-#pragma unroll 2
-        for (int kk = 0; kk < 256; kk += 4) {
-            float4 w[4], x[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4*>(Ws + (rg + 16 * i) * kPfLd + kk);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(Xs + (tg + 16 * j) * kPfLd + kk);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float a = fmaf(w[i].x, x[j].x, acc[i][j]);
-                    a = fmaf(w[i].y, x[j].y, a);
-                    a = fmaf(w[i].z, x[j].z, a);
-                    acc[i][j] = fmaf(w[i].w, x[j].w, a);
-                }
-        }
-        __syncthreads();
     }
     float* Yz = Y + blockIdx.z * split_stride;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i) {
+        const int r = row0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+        if (r >= n) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = row0 + rg + 16 * i, t = tok0 + tg + 16 * j;
-            if (r < n && t < P) Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
+        for (int j = 0; j < 8; ++j) {
+            const int t = tok0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
+            if (t < P) Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
         }
+    }
+}
+
+// Z = the `parts` split sums of a projection, added in split order.
+__global__ void pf_sum_parts_kernel(const float* __restrict__ Yp, int parts, size_t stride, float* __restrict__ Z,
+                                    size_t count) {
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    float v = Yp[i];
+    for (int z = 1; z < parts; ++z) v += Yp[z * stride + i];
+    Z[i] = v;
 }
 
 // X[p] = E[tok[p]].  Grid P.
@@ -180,35 +199,48 @@ __global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X,
     for (int i = tid; i < H; i += 256) Xn[static_cast<size_t>(p) * H + i] = (x[i] * r) * w[i];
 }
 
-// Causal conv1d + SiLU of the qkv rows over the chunk, one thread per channel
-// scanning the tokens (window carried in registers, written back at the end),
-// and the alpha/beta gates of every token.  Z rows [qkv C | alpha nv | beta nv | z].
+// Causal conv1d + SiLU of the qkv rows and the alpha/beta gates, one thread
+// per (token, row): the conv of token p reads inputs p-K+1..p (older ones from
+// the window of the previous call), taps in the decode step's order; no
+// recurrence, so the whole chunk runs at once.  Z rows [qkv C | alpha nv |
+// beta nv | z].  The window moves afterwards (pf_conv_window_kernel).
 __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P, int C, int nv, int K,
-                                     float* __restrict__ win, const float* __restrict__ wconv,
+                                     const float* __restrict__ win, const float* __restrict__ wconv,
                                      const float* __restrict__ dt_bias, const float* __restrict__ a,
                                      float* __restrict__ Cq, float* __restrict__ dt, float* __restrict__ beta) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int W = C + nv;
+    if (idx >= static_cast<long long>(P) * W) return;
+    const int p = static_cast<int>(idx / W), c = static_cast<int>(idx - static_cast<long long>(p) * W);
     if (c < C) {
-        float wv[kMaxConvTaps], kw[kMaxConvTaps];
-        for (int t = 0; t < K; ++t) kw[t] = wconv[static_cast<size_t>(c) * K + t];
-        for (int t = 0; t < K - 1; ++t) wv[t] = win[static_cast<size_t>(c) * (K - 1) + t];
-        for (int p = 0; p < P; ++p) {
-            const float v = Z[static_cast<size_t>(p) * ldz + c];
-            float acc = 0.0f;
-            for (int t = 0; t < K - 1; ++t) acc += kw[t] * wv[t];
-            acc += kw[K - 1] * v;
-            Cq[static_cast<size_t>(p) * C + c] = silu(acc);
-            for (int t = 1; t < K - 1; ++t) wv[t - 1] = wv[t];
-            wv[K - 2] = v;
+        const float* kw = wconv + static_cast<size_t>(c) * K;
+        float acc = 0.0f;
+        for (int t = 0; t < K - 1; ++t) {
+            const int i = p - (K - 1) + t;
+            const float x = i >= 0 ? Z[static_cast<size_t>(i) * ldz + c] : win[static_cast<size_t>(c) * (K - 1) + (K - 1) + i];
+            acc += kw[t] * x;
         }
-        for (int t = 0; t < K - 1; ++t) win[static_cast<size_t>(c) * (K - 1) + t] = wv[t];
-    } else if (c < C + nv) {
-        const int h = c - C;
-        for (int p = 0; p < P; ++p) {
-            dt[p * nv + h] = softplus(Z[static_cast<size_t>(p) * ldz + C + h] + dt_bias[h]) * a[h];
-            beta[p * nv + h] = sigmoid(Z[static_cast<size_t>(p) * ldz + C + nv + h]);
-        }
+        acc += kw[K - 1] * Z[static_cast<size_t>(p) * ldz + c];
+        Cq[static_cast<size_t>(p) * C + c] = silu(acc);
+    } else {
+        const int h = c - C;  // dt = softplus(alpha + dt_bias) * a, beta = sigmoid(beta_raw)
+        dt[p * nv + h] = softplus(Z[static_cast<size_t>(p) * ldz + C + h] + dt_bias[h]) * a[h];
+        beta[p * nv + h] = sigmoid(Z[static_cast<size_t>(p) * ldz + C + nv + h]);
     }
+}
+
+// The conv window after the chunk: the last K-1 inputs, oldest first (from
+// the old window where the chunk is shorter than that).  One thread per row.
+__global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int P, int C, int K, float* __restrict__ win) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float nw[kMaxConvTaps];
+    float* wc = win + static_cast<size_t>(c) * (K - 1);
+    for (int t = 0; t < K - 1; ++t) {
+        const int i = P - (K - 1) + t;
+        nw[t] = i >= 0 ? Z[static_cast<size_t>(i) * ldz + c] : wc[(K - 1) + i];
+    }
+    for (int t = 0; t < K - 1; ++t) wc[t] = nw[t];
 }
 
 // Per-head L2 norm of each token's q and k (head_k_dim 128): one warp per
@@ -232,14 +264,21 @@ __global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, 
 // The delta rule over the chunk: CTA = 32 state rows of one value head, each
 // warp 4 rows held in registers (lane: dims 4 lane..+3) for the whole chunk;
 // per token decay, read, rank-1 update and query as the decode step does
-// (delta_rows4), with the next token's inputs loaded ahead.  O [P][v_dim].
+// (delta_rows4).  The inputs of 32 tokens at a time (the head's normalised q
+// and k, the CTA's v values, the gates) are staged in shared memory by the
+// whole CTA, so the token loop reads shared memory only.  O [P][v_dim].
+constexpr int kDeltaStage = 32;
 __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq, int C, int kdim,
                                                        const float* __restrict__ QKn, const float* __restrict__ dt,
                                                        const float* __restrict__ beta, float* __restrict__ S,
                                                        float* __restrict__ O, int P, int nk, int nv, int dv) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ __align__(16) float sq[kDeltaStage][kDk];
+    __shared__ __align__(16) float sk[kDeltaStage][kDk];
+    __shared__ float sv[kDeltaStage][32];
+    __shared__ float sg[kDeltaStage], sb[kDeltaStage];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_head = dv / 32;
-    const int h = blockIdx.x / per_head, j = (blockIdx.x - h * per_head) * 32 + 4 * warp;
+    const int h = blockIdx.x / per_head, jb = (blockIdx.x - h * per_head) * 32, j = jb + 4 * warp;
     const int kh = h % nk;
     const int vd = nv * dv;
     float4 st[4];
@@ -247,62 +286,67 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
 #pragma unroll
     for (int t = 0; t < 4; ++t) st[t] = *reinterpret_cast<const float4*>(Sg + t * kDk + 4 * lane);
     const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
-    auto load = [&](int p, float4& kk, float4& qq, float& vl, float& g, float& be) {
-        const float* base = QKn + static_cast<size_t>(p) * 2 * nk * kDk;
-        qq = *reinterpret_cast<const float4*>(base + kh * kDk + 4 * lane);
-        kk = *reinterpret_cast<const float4*>(base + (nk + kh) * kDk + 4 * lane);
-        vl = lane < 4 ? Cq[static_cast<size_t>(p) * C + 2 * kdim + h * dv + j + lane] : 0.0f;
-        g = dt[p * nv + h];
-        be = beta[p * nv + h];
-    };
-    float4 kk, qq, kn, qn;
-    float vl, g, be, vn = 0.0f, gn = 0.0f, ben = 0.0f;
-    load(0, kk, qq, vl, g, be);
-    for (int p = 0; p < P; ++p) {
-        if (p + 1 < P) load(p + 1, kn, qn, vn, gn, ben);
-        const float gd = expf(g);
-        float4 rr[4];
-        float dot[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            rr[t] = make_float4(gd * st[t].x, gd * st[t].y, gd * st[t].z, gd * st[t].w);  // decay
-            float d = rr[t].x * kk.x;
-            d = fmaf(rr[t].y, kk.y, d);
-            d = fmaf(rr[t].z, kk.z, d);
-            dot[t] = fmaf(rr[t].w, kk.w, d);
+    for (int p0 = 0; p0 < P; p0 += kDeltaStage) {
+        const int np = min(kDeltaStage, P - p0);
+        __syncthreads();  // the previous block's inputs are consumed
+        for (int e = tid; e < np * 64; e += 256) {
+            const int t = e >> 6, r = e & 63, which = r >> 5, c4 = r & 31;
+            const float4 v = *reinterpret_cast<const float4*>(
+                QKn + (static_cast<size_t>(p0 + t) * 2 * nk + which * nk + kh) * kDk + 4 * c4);
+            *reinterpret_cast<float4*>((which ? &sk[t][0] : &sq[t][0]) + 4 * c4) = v;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) dot[t] += __shfl_xor_sync(0xffffffffu, dot[t], off);  // read
-        float oq[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float d = be * (__shfl_sync(0xffffffffu, vl, t) - dot[t]);
-            st[t] = make_float4(fmaf(kk.x, d, rr[t].x), fmaf(kk.y, d, rr[t].y), fmaf(kk.z, d, rr[t].z),
-                                fmaf(kk.w, d, rr[t].w));  // rank-1 update
-            float q = st[t].x * qq.x;
-            q = fmaf(st[t].y, qq.y, q);
-            q = fmaf(st[t].z, qq.z, q);
-            oq[t] = fmaf(st[t].w, qq.w, q);
+        for (int e = tid; e < np * 32; e += 256) {
+            const int t = e >> 5, jj = e & 31;
+            sv[t][jj] = Cq[static_cast<size_t>(p0 + t) * C + 2 * kdim + h * dv + jb + jj];
         }
+        if (tid < np) {
+            sg[tid] = dt[(p0 + tid) * nv + h];
+            sb[tid] = beta[(p0 + tid) * nv + h];
+        }
+        __syncthreads();
+        for (int t = 0; t < np; ++t) {
+            const float4 kk = *reinterpret_cast<const float4*>(&sk[t][4 * lane]);
+            const float4 qq = *reinterpret_cast<const float4*>(&sq[t][4 * lane]);
+            const float vl = lane < 4 ? sv[t][4 * warp + lane] : 0.0f;
+            const float gd = expf(sg[t]), be = sb[t];
+            float4 rr[4];
+            float dot[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
+            for (int u = 0; u < 4; ++u) {
+                rr[u] = make_float4(gd * st[u].x, gd * st[u].y, gd * st[u].z, gd * st[u].w);  // decay
+                float d = rr[u].x * kk.x;
+                d = fmaf(rr[u].y, kk.y, d);
+                d = fmaf(rr[u].z, kk.z, d);
+                dot[u] = fmaf(rr[u].w, kk.w, d);
+            }
 #pragma unroll
-            for (int t = 0; t < 4; ++t) oq[t] += __shfl_xor_sync(0xffffffffu, oq[t], off);  // query
-        float mine = 0.0f;
+            for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-            if (lane == t) mine = oq[t] * scale;
-        if (lane < 4) O[static_cast<size_t>(p) * vd + h * dv + j + lane] = mine;
-        kk = kn;
-        qq = qn;
-        vl = vn;
-        g = gn;
-        be = ben;
+                for (int u = 0; u < 4; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], off);  // read
+            float oq[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float d = be * (__shfl_sync(0xffffffffu, vl, u) - dot[u]);
+                st[u] = make_float4(fmaf(kk.x, d, rr[u].x), fmaf(kk.y, d, rr[u].y), fmaf(kk.z, d, rr[u].z),
+                                    fmaf(kk.w, d, rr[u].w));  // rank-1 update
+                float q = st[u].x * qq.x;
+                q = fmaf(st[u].y, qq.y, q);
+                q = fmaf(st[u].z, qq.z, q);
+                oq[u] = fmaf(st[u].w, qq.w, q);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) oq[u] += __shfl_xor_sync(0xffffffffu, oq[u], off);  // query
+            float mine = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (lane == u) mine = oq[u] * scale;
+            if (lane < 4) O[static_cast<size_t>(p0 + t) * vd + h * dv + j + lane] = mine;
+        }
     }
 #pragma unroll
-    for (int t = 0; t < 4; ++t) *reinterpret_cast<float4*>(Sg + t * kDk + 4 * lane) = st[t];
+    for (int u = 0; u < 4; ++u) *reinterpret_cast<float4*>(Sg + u * kDk + 4 * lane) = st[u];
 }
 
 // Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h).  Grid P,
@@ -457,18 +501,22 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
     }
 }
 
-// A = silu(G) * U, elementwise.
-__global__ void pf_swiglu_kernel(const float* __restrict__ G, const float* __restrict__ U, float* __restrict__ A,
-                                 size_t n) {
+// A = silu(G) * U, elementwise, G and U given as split sums (added in order).
+__global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
+                                 size_t stride, float* __restrict__ A, size_t n) {
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < n) A[i] = silu(G[i]) * U[i];
+    if (i >= n) return;
+    float g = Gp[i], u = Up[i];
+    for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
+    for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
+    A[i] = silu(g) * u;
 }
 
 // ------------------------------------------------------------ host side
 struct Scratch {
     int chunk;
     int* tok;
-    float *X, *Xn, *Z, *Yp, *G, *Uf, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
+    float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
 };
 
 template <class T>
@@ -499,7 +547,8 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     int rc = QG_OK;
     (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H)) ||
            (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, kPfMaxSplit * P * H)) ||
-           (rc = pf_alloc(s, &sc->G, P * c.ffn)) || (rc = pf_alloc(s, &sc->Uf, P * c.ffn)) ||
+           (rc = pf_alloc(s, &sc->Zp, kPfMaxSplit * P * std::max(n_in, static_cast<size_t>(c.ffn)))) ||
+           (rc = pf_alloc(s, &sc->Up, kPfMaxSplit * P * c.ffn)) ||
            (rc = pf_alloc(s, &sc->A, P * c.ffn)) || (rc = pf_alloc(s, &sc->Cq, P * std::max(m->conv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->dt, P * (c.n_v_heads + 1))) || (rc = pf_alloc(s, &sc->beta, P * (c.n_v_heads + 1))) ||
            (rc = pf_alloc(s, &sc->QKn, P * 2 * std::max(m->k_dim, 1))) ||
@@ -518,29 +567,29 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
 template <int QT>
 int gemm(const uint8_t* W, int n, int k, const float* X, int ldx, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits) {
-    const int nb = k / 256;
-    if (splits > nb) splits = nb;
+    const int nq = k / 64;
+    if (splits > nq) splits = nq;
     if (splits < 1) splits = 1;
-    const int per = (nb + splits - 1) / splits;
-    const int z = (nb + per - 1) / per;
+    const int per = (nq + splits - 1) / splits;
+    const int z = (nq + per - 1) / per;
     if (used_splits) *used_splits = z;
-    const int smem = 2 * kPfRows * kPfLd * static_cast<int>(sizeof(float));
+    const int smem = kGK * (kGR + kGT) * static_cast<int>(sizeof(float));
     static bool configured = false;
     if (!configured) {
         QG_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         configured = true;
     }
-    const dim3 grid((n + kPfRows - 1) / kPfRows, (P + kPfTok - 1) / kPfTok, z);
+    const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
     pf_gemm_kernel<QT><<<grid, 256, smem, st>>>(W, n, k, X, ldx, Y, ldy, static_cast<size_t>(P) * ldy, P, per);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
 
-// Splits of a projection back to the hidden size: enough CTAs for two per SM.
+// K splits of a projection: enough CTAs for two per SM (at most kPfMaxSplit).
 int splits_for(int n, int k, int P) {
-    const int ctas = ((n + kPfRows - 1) / kPfRows) * ((P + kPfTok - 1) / kPfTok);
+    const int ctas = ((n + kGR - 1) / kGR) * ((P + kGT - 1) / kGT);
     int z = (2 * device_sms() + ctas - 1) / ctas;
-    return std::max(1, std::min({z, kPfMaxSplit, k / 256}));
+    return std::max(1, std::min({z, kPfMaxSplit, k / 64}));
 }
 
 template <bool KVQ>
@@ -570,13 +619,22 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
         const qg_layer_dev& L = m->layers[il];
         pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, H, c.eps);
         QG_CUDA(cudaGetLastError());
-        if ((rc = gemm<QT_Q4K>(L.w_in, L.n_in, H, sc->Xn, H, sc->Z, L.n_in, P, 1, st, nullptr))) break;
+        int zin = 1;
+        if ((rc = gemm<QT_Q4K>(L.w_in, L.n_in, H, sc->Xn, H, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
+            break;
+        {
+            const size_t cnt = static_cast<size_t>(P) * L.n_in;
+            pf_sum_parts_kernel<<<static_cast<unsigned>((cnt + 255) / 256), 256, 0, st>>>(sc->Zp, zin, cnt, sc->Z, cnt);
+            QG_CUDA(cudaGetLastError());
+        }
         int k_out;
         if (m->kinds[il] == QG_LAYER_DELTANET) {
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
-            pf_conv_gates_kernel<<<(C + 2 * nv + 127) / 128, 128, 0, st>>>(sc->Z, L.n_in, P, C, nv, c.conv_kernel,
-                                                                         s->conv[il], L.conv_w, L.dt_bias, L.a, sc->Cq,
-                                                                         sc->dt, sc->beta);
+            const long long cg = static_cast<long long>(P) * (C + nv);
+            pf_conv_gates_kernel<<<static_cast<unsigned>((cg + 255) / 256), 256, 0, st>>>(
+                sc->Z, L.n_in, P, C, nv, c.conv_kernel, s->conv[il], L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
+            QG_CUDA(cudaGetLastError());
+            pf_conv_window_kernel<<<(C + 255) / 256, 256, 0, st>>>(sc->Z, L.n_in, P, C, c.conv_kernel, s->conv[il]);
             QG_CUDA(cudaGetLastError());
             const int warps = P * 2 * c.n_k_heads;
             pf_l2norm_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(sc->Cq, C, m->k_dim, c.n_k_heads, P, c.eps,
@@ -614,10 +672,12 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
             break;
         pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, H, c.eps);
         QG_CUDA(cudaGetLastError());
-        if ((rc = gemm<QT_Q4K>(L.w_gate, c.ffn, H, sc->Xn, H, sc->G, c.ffn, P, 1, st, nullptr))) break;
-        if ((rc = gemm<QT_Q4K>(L.w_up, c.ffn, H, sc->Xn, H, sc->Uf, c.ffn, P, 1, st, nullptr))) break;
+        const int zf = splits_for(c.ffn, H, P);
+        int zg = 1, zu = 1;
+        if ((rc = gemm<QT_Q4K>(L.w_gate, c.ffn, H, sc->Xn, H, sc->Zp, c.ffn, P, zf, st, &zg))) break;
+        if ((rc = gemm<QT_Q4K>(L.w_up, c.ffn, H, sc->Xn, H, sc->Up, c.ffn, P, zf, st, &zu))) break;
         const size_t na = static_cast<size_t>(P) * c.ffn;
-        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(sc->G, sc->Uf, sc->A, na);
+        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(sc->Zp, zg, sc->Up, zu, na, sc->A, na);
         QG_CUDA(cudaGetLastError());
         rc = gemm<QT_Q6K>(L.w_down, H, c.ffn, sc->A, c.ffn, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
     }
