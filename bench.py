@@ -96,10 +96,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# The translation unit of the lm_head GEMV + argmax building block whose DRAM
+# counters profiles/traffic.json records: gemv.cu and the headers it includes.
+LMHEAD_SOURCES = ("gemv.cu", "qg_host.cuh", "qg_gemv.cuh", "qg_common.cuh")
+
+
 def kernel_sources_hash():
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in LMHEAD_SOURCES:
+        with open(os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <type_traits>
 
 #include "qg_layers.cuh"
 
@@ -25,42 +26,79 @@ constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarte
 
 __device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return static_cast<uint16_t>(p[0] | (p[1] << 8)); }
 
-// Sub-block j (32 weights) of one 144-byte GGUF Q4_K block, as f32:
-// d * scale_j * q - dmin * min_j, q the low (j even) or high (j odd) nibbles
-// of bytes 32 (j/2) .. +31, with the 6-bit scale and min of sub-block j.
-__device__ __forceinline__ void q4k_sub(const uint8_t* blk, int j, float* v) {
-    const float d = f16_to_f32(ld16(blk)), dmin = f16_to_f32(ld16(blk + 2));
-    const uint8_t* sc = blk + 4;
-    int s, m;
-    if (j < 4) {
-        s = sc[j] & 63;
-        m = sc[j + 4] & 63;
-    } else {
-        s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
-        m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-    }
-    const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
-    const uint8_t* q = blk + 16 + 32 * (j >> 1);
-    const int sh = (j & 1) * 4;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = ds * static_cast<float>((q[i] >> sh) & 15) - dm;
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
+__device__ __forceinline__ int byte_of(const uint4& v, int b) { return (word_of(v, b >> 2) >> (8 * (b & 3))) & 0xff; }
 
-// Weights 64 q + 32 hf .. +31 of row rr of a planar Q6_K group-block (the
-// layout of qg_q6k_to_planar), as f32 d * scale * (6-bit code - 32).  They are
-// 128 h + 32 s + 16 p + i with h = q/2, s = 2 (q&1) + hf, p = 0, 1, i < 16:
-// bytes i of the records (rr, 2h + p) and their scale s.
-__device__ __forceinline__ void q6k_sub(const uint8_t* gb, int rr, int q, int hf, float* v) {
-    const int h = q >> 1, s = 2 * (q & 1) + hf;
-    const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
+// Raw bytes one thread dequantizes per 64-weight quarter, loaded a quarter
+// ahead.  Q4_K: the 16-byte head of the row's 144-byte block (d, dmin, the 12
+// bytes of 6-bit scales and mins) and the quarter's 32 bytes of nibbles.
+// Q6_K: the row's two 48-byte records of the quarter, their 4 scales each, d.
+struct RawQ4 {
+    uint4 h, q0, q1;
+};
+struct RawQ6 {
+    uint4 r[2][3];
+    uint32_t sc[2];
+    uint32_t d;
+};
+
+__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, RawQ4& r) {
+    const uint8_t* blk = gb + 144 * rr;
+    r.h = *reinterpret_cast<const uint4*>(blk);
+    r.q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
+    r.q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+}
+__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, RawQ6& r) {
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const int u = 4 * rr + 2 * h + p;
-        const uint8_t* rec = gb + 48 * u;
-        const float ds = d * static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + s]));
+        const int u = 4 * rr + 2 * (q >> 1) + p;
+#pragma unroll
+        for (int w = 0; w < 3; ++w) r.r[p][w] = *reinterpret_cast<const uint4*>(gb + 48 * u + 16 * w);
+        r.sc[p] = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
+    }
+    r.d = *reinterpret_cast<const uint16_t*>(gb + 1664 + 2 * rr);
+}
+
+// Weights 64 q + 32 hf .. +31 of the row (sub-block j = 2q + hf of the GGUF
+// Q4_K block): d * scale_j * nibble - dmin * min_j, the low nibbles for hf = 0.
+__device__ __forceinline__ void raw_decode(const RawQ4& r, int q, int hf, float* v) {
+    const int j = 2 * q + hf;
+    const float d = f16_to_f32(static_cast<uint16_t>(r.h.x & 0xffffu));
+    const float dmin = f16_to_f32(static_cast<uint16_t>(r.h.x >> 16));
+    int s, m;  // 6-bit scale and min of sub-block j from the 12 bytes at 4..15
+    if (j < 4) {
+        s = byte_of(r.h, 4 + j) & 63;
+        m = byte_of(r.h, 8 + j) & 63;
+    } else {
+        s = (byte_of(r.h, 8 + j) & 15) | ((byte_of(r.h, j) >> 6) << 4);
+        m = (byte_of(r.h, 8 + j) >> 4) | ((byte_of(r.h, 4 + j) >> 6) << 4);
+    }
+    const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
+    const int sh = 4 * hf;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint4& w = i < 16 ? r.q0 : r.q1;
+        const int nib = (word_of(w, (i & 15) >> 2) >> (8 * (i & 3) + sh)) & 15;
+        v[i] = ds * static_cast<float>(nib) - dm;
+    }
+}
+
+// Weights 64 q + 32 hf .. +31 of the row in the planar Q6_K layout: they are
+// 128 h + 32 s + 16 p + i (h = q/2, s = 2 (q&1) + hf, p = 0, 1, i < 16), byte
+// i of record (rr, 2h + p) with its scale s: d * scale * (6-bit code - 32).
+__device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int hf, float* v) {
+    const int s = 2 * (q & 1) + hf;
+    const float d = f16_to_f32(static_cast<uint16_t>(r.d & 0xffffu));
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const float ds = d * static_cast<float>(static_cast<int8_t>((r.sc[p] >> (8 * s)) & 0xffu));
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int a = rec[i], b = rec[16 + i], hb = rec[32 + i];
+            const int a = (word_of(r.r[p][0], i >> 2) >> (8 * (i & 3))) & 0xff;
+            const int b = (word_of(r.r[p][1], i >> 2) >> (8 * (i & 3))) & 0xff;
+            const int hb = (word_of(r.r[p][2], i >> 2) >> (8 * (i & 3))) & 0xff;
             int code;
             if (s == 0) code = (a & 15) | ((hb & 3) << 4);
             else if (s == 1) code = (b & 15) | (((hb >> 2) & 3) << 4);
@@ -71,21 +109,31 @@ __device__ __forceinline__ void q6k_sub(const uint8_t* gb, int rr, int q, int hf
     }
 }
 
-// Y[z][t][row] = sum over the 64-weight quarters of split z of W[row] . X[t],
-// for a planar Q4_K / Q6_K W [n x k] and f32 X [P][ldx].  Grid (ceil(n/128),
-// ceil(P/128), splits), 256 threads.  Per 64-weight quarter of a super-block
-// the CTA dequantizes its 128 rows (thread: 32 weights of one row) into
-// Ws[k][row] and stages its 128 tokens' inputs as Xs[k][token]; each thread then
-// accumulates 8 rows x 8 tokens as outer products, in k order: rows 4 ty..+3
-// and 64 + 4 ty..+3, tokens likewise with tx, so that eight consecutive lanes
-// read 128 contiguous bytes (no bank conflicts).
-template <int QT>
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Y = W X over the 64-weight quarters of split z, for a planar Q4_K / Q6_K W
+// [n x k] and k-major f32 inputs X[k][ldx] (token t of the chunk in column t).
+// Grid (ceil(n/128), ceil(P/128), splits), 256 threads.  Per quarter the CTA
+// dequantizes its 128 rows (thread: 32 weights of one row, from raw bytes
+// loaded while the previous quarter computed) into Ws[k][row], while the next quarter's inputs
+// stream into the other half of the double-buffered Xs[k][token] by 16-byte
+// async copies; each thread accumulates 8 rows x 8 tokens as outer products in
+// k order (rows 4 ty..+3 and 64 + 4 ty..+3, tokens likewise with tx, so eight
+// consecutive lanes read 128 contiguous bytes).  Output: split z at
+// Y + z split_stride, token-major (Y[t ldy + row]) or, when ROW_MAJOR,
+// Y[row ldy + t] (k-major for a following GEMM).
+template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                          const float* __restrict__ X, int ldx, float* __restrict__ Y,
                                                          int ldy, size_t split_stride, int P, int q_per_split) {
+    using Raw = typename std::conditional<QT == QT_Q6K, RawQ6, RawQ4>::type;
     extern __shared__ __align__(16) float smf[];
-    float* Ws = smf;              // [kGK][kGR]
-    float* Xs = smf + kGK * kGR;  // [kGK][kGT]
+    float* Ws = smf;                  // [kGK][kGR]
+    float* Xs = smf + kGK * kGR;      // [2][kGK][kGT]
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int row0 = blockIdx.x * kGR, tok0 = blockIdx.y * kGT;
     const int nb = k / 256, n8 = (n + 7) & ~7;
@@ -93,51 +141,61 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
     const int dr = tid & (kGR - 1), hf = tid >> 7;  // dequantization role: row, half of the quarter
     const int grow = row0 + dr;
     const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
+    const int GB = QT == QT_Q6K ? 1680 : 1152;
+    auto issue_x = [&](int qi, int buf) {  // the quarter's 64 k-rows x 128 tokens, 16 bytes per copy
+        float* xs = Xs + buf * kGK * kGT;
+        const float* xg = X + static_cast<size_t>(64 * qi) * ldx + tok0;
+        for (int e = tid; e < kGK * (kGT / 4); e += 256) {
+            const int kk = e >> 5, c4 = e & 31;
+            cp_async16(xs + kk * kGT + 4 * c4, xg + static_cast<size_t>(kk) * ldx + 4 * c4);
+        }
+    };
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    Raw cur{};
+    if (q0 < q1) {
+        if (row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, cur);
+        issue_x(q0, 0);
+    }
+    cp_async_commit();
     for (int qi = q0; qi < q1; ++qi) {
-        const int b = qi >> 2, q = qi & 3;
-        const uint8_t* gb = row_ok ? W + grouped_offset(n8, nb, grow >> 3, b, QT == QT_Q6K ? 1680 : 1152) : nullptr;
+        const int buf = (qi - q0) & 1;
+        if (qi + 1 < q1) issue_x(qi + 1, buf ^ 1);
+        cp_async_commit();
         {
             float v[32];
             if (row_ok) {
-                if (QT == QT_Q6K) q6k_sub(gb, grow & 7, q, hf, v);
-                else q4k_sub(gb + 144 * (grow & 7), 2 * q + hf, v);
+                raw_decode(cur, qi & 3, hf, v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.0f;
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) Ws[(32 * hf + i) * kGR + dr] = v[i];
-            for (int e = tid; e < kGT * (kGK / 4); e += 256) {
-                const int t = e & (kGT - 1), c4 = e >> 7;
-                float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (tok0 + t < P)
-                    x = *reinterpret_cast<const float4*>(X + static_cast<size_t>(tok0 + t) * ldx + 256 * b + 64 * q + 4 * c4);
-                Xs[(4 * c4 + 0) * kGT + t] = x.x;
-                Xs[(4 * c4 + 1) * kGT + t] = x.y;
-                Xs[(4 * c4 + 2) * kGT + t] = x.z;
-                Xs[(4 * c4 + 3) * kGT + t] = x.w;
-            }
-            __syncthreads();
-#pragma unroll 4
-            for (int kk = 0; kk < kGK; ++kk) {
-                const float4 a0 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 4 * ty);
-                const float4 a1 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 64 + 4 * ty);
-                const float4 c0 = *reinterpret_cast<const float4*>(Xs + kk * kGT + 4 * tx);
-                const float4 c1 = *reinterpret_cast<const float4*>(Xs + kk * kGT + 64 + 4 * tx);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
-            }
-            __syncthreads();
         }
+        // the next quarter's raw bytes, into the registers just decoded (one set live)
+        if (qi + 1 < q1 && row_ok)
+            raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, cur);
+        cp_async_wait1();  // this quarter's inputs have landed (the next quarter's may be in flight)
+        __syncthreads();
+        const float* xs = Xs + buf * kGK * kGT;
+#pragma unroll 4
+        for (int kk = 0; kk < kGK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 4 * ty);
+            const float4 a1 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 64 + 4 * ty);
+            const float4 c0 = *reinterpret_cast<const float4*>(xs + kk * kGT + 4 * tx);
+            const float4 c1 = *reinterpret_cast<const float4*>(xs + kk * kGT + 64 + 4 * tx);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+        }
+        __syncthreads();
     }
     float* Yz = Y + blockIdx.z * split_stride;
 #pragma unroll
@@ -147,7 +205,10 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = tok0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
-            if (t < P) Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
+            if (t < P) {
+                if (ROW_MAJOR) Yz[static_cast<size_t>(r) * ldy + t] = acc[i][j];
+                else Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
+            }
         }
     }
 }
@@ -170,10 +231,10 @@ __global__ void pf_embed_kernel(const float* __restrict__ E, const int* __restri
 }
 
 // X[p] += the `parts` split sums (in split order); then, when w is given,
-// Xn[p] = RMSNorm(X[p]) * w.  Grid P, 256 threads.
+// RMSNorm(X[p]) * w into column p of the k-major Xn[H][ldn].  Grid P.
 __global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts,
                                                           size_t split_stride, const float* __restrict__ w,
-                                                          float* __restrict__ Xn, int H, float eps) {
+                                                          float* __restrict__ Xn, int ldn, int H, float eps) {
     __shared__ float red[8];
     const int p = blockIdx.x, tid = threadIdx.x;
     float* x = X + static_cast<size_t>(p) * H;
@@ -196,7 +257,7 @@ __global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X,
 #pragma unroll
     for (int i = 0; i < 8; ++i) t += red[i];
     const float r = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
-    for (int i = tid; i < H; i += 256) Xn[static_cast<size_t>(p) * H + i] = (x[i] * r) * w[i];
+    for (int i = tid; i < H; i += 256) Xn[static_cast<size_t>(i) * ldn + p] = (x[i] * r) * w[i];
 }
 
 // Causal conv1d + SiLU of the qkv rows and the alpha/beta gates, one thread
@@ -349,11 +410,12 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
     for (int u = 0; u < 4; ++u) *reinterpret_cast<float4*>(Sg + u * kDk + 4 * lane) = st[u];
 }
 
-// Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h).  Grid P,
-// one warp per head (head_v_dim 32/64/128: 1, 2 or 4 values per lane).
+// Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h), into column
+// p of the k-major U[v_dim][ldu].  Grid P, one warp per head (head_v_dim
+// 32/64/128: 1, 2 or 4 values per lane).
 __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restrict__ O, const float* __restrict__ Z,
                                                             int ldz, int zoff, const float* __restrict__ w, int nv,
-                                                            int dv, float eps, float* __restrict__ U) {
+                                                            int dv, float eps, float* __restrict__ U, int ldu) {
     const int p = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per = dv / 32;
     for (int h = warp; h < nv; h += 8) {
@@ -368,7 +430,7 @@ __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restr
         const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
         for (int e = 0; e < per; ++e) {
             const int i = lane + 32 * e;
-            U[static_cast<size_t>(p) * nv * dv + h * dv + i] = ((ov[e] * rn) * w[i]) * silu(z[i]);
+            U[static_cast<size_t>(h * dv + i) * ldu + p] = ((ov[e] * rn) * w[i]) * silu(z[i]);
         }
     }
 }
@@ -431,12 +493,12 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
 // heads of kv group g of token p over cache rows 0..pos0+p (f32 rows, or
 // quantized records read dequantized), 8 warps taking keys t = warp mod 8 with
 // an online softmax each, then combined; the output is gated by
-// sigmoid(gate) and stored to Att [P][nh*256].
+// sigmoid(gate) and stored to column p of the k-major Att[nh*256][lda].
 template <int GS, bool KVQ>
 __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
                                                              int ldz, const float* __restrict__ kc,
                                                              const float* __restrict__ vc, int kvd, int max_seq,
-                                                             int pos0, float* __restrict__ Att) {
+                                                             int pos0, float* __restrict__ Att, int lda) {
     __shared__ float wml[8][GS][2];
     __shared__ __align__(16) float wacc[8][GS][kHd];
     const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -497,11 +559,12 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
         }
         const int h = g * GS + i;
         const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
-        Att[static_cast<size_t>(p) * nh * kHd + h * kHd + tid] = (A / L) * sigmoid(gt);
+        Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
     }
 }
 
-// A = silu(G) * U, elementwise, G and U given as split sums (added in order).
+// A = silu(G) * U, elementwise (k-major [ffn][chunk] arrays), G and U given as
+// split sums (added in order).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
                                  size_t stride, float* __restrict__ A, size_t n) {
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -564,8 +627,10 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     return QG_OK;
 }
 
-template <int QT>
-int gemm(const uint8_t* W, int n, int k, const float* X, int ldx, float* Y, int ldy, int P, int splits, cudaStream_t st,
+// Y = W X with X k-major [k][kPfChunk]; ROW_MAJOR: Y[row][ldy] per split
+// (split stride n * ldy), else Y[token][ldy] (split stride P * ldy).
+template <int QT, bool ROW_MAJOR>
+int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits) {
     const int nq = k / 64;
     if (splits > nq) splits = nq;
@@ -573,14 +638,15 @@ int gemm(const uint8_t* W, int n, int k, const float* X, int ldx, float* Y, int 
     const int per = (nq + splits - 1) / splits;
     const int z = (nq + per - 1) / per;
     if (used_splits) *used_splits = z;
-    const int smem = kGK * (kGR + kGT) * static_cast<int>(sizeof(float));
+    const int smem = kGK * (kGR + 2 * kGT) * static_cast<int>(sizeof(float));
     static bool configured = false;
     if (!configured) {
-        QG_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        QG_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT, ROW_MAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
         configured = true;
     }
     const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
-    pf_gemm_kernel<QT><<<grid, 256, smem, st>>>(W, n, k, X, ldx, Y, ldy, static_cast<size_t>(P) * ldy, P, per);
+    const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
+    pf_gemm_kernel<QT, ROW_MAJOR><<<grid, 256, smem, st>>>(W, n, k, X, kPfChunk, Y, ldy, split_stride, P, per);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
@@ -596,9 +662,9 @@ template <bool KVQ>
 int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const float* kc,
                   const float* vc, int kvd, int max_seq, int pos0, float* att) {
     switch (gs) {
-        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
-        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
-        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att); break;
+        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
+        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
+        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
         default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
     }
     QG_CUDA(cudaGetLastError());
@@ -617,10 +683,10 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
     int rc = QG_OK;
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, H, c.eps);
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, kPfChunk, H, c.eps);
         QG_CUDA(cudaGetLastError());
         int zin = 1;
-        if ((rc = gemm<QT_Q4K>(L.w_in, L.n_in, H, sc->Xn, H, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
+        if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
             break;
         {
             const size_t cnt = static_cast<size_t>(P) * L.n_in;
@@ -644,7 +710,7 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
                                                          sc->O, P, c.n_k_heads, nv, dv);
             QG_CUDA(cudaGetLastError());
             pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, sc->Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
-                                                    sc->Uin);
+                                                    sc->Uin, kPfChunk);
             QG_CUDA(cudaGetLastError());
             k_out = m->v_dim;
         } else {
@@ -668,21 +734,21 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
             if (rc) break;
             k_out = m->q_dim;
         }
-        if ((rc = gemm<QT_Q4K>(L.w_out, H, k_out, sc->Uin, k_out, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending)))
+        if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending)))
             break;
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, H, c.eps);
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, kPfChunk, H, c.eps);
         QG_CUDA(cudaGetLastError());
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
-        if ((rc = gemm<QT_Q4K>(L.w_gate, c.ffn, H, sc->Xn, H, sc->Zp, c.ffn, P, zf, st, &zg))) break;
-        if ((rc = gemm<QT_Q4K>(L.w_up, c.ffn, H, sc->Xn, H, sc->Up, c.ffn, P, zf, st, &zu))) break;
-        const size_t na = static_cast<size_t>(P) * c.ffn;
+        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, kPfChunk, P, zf, st, &zg))) break;
+        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, kPfChunk, P, zf, st, &zu))) break;
+        const size_t na = static_cast<size_t>(c.ffn) * kPfChunk;  // k-major [ffn][chunk], columns >= P unused
         pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(sc->Zp, zg, sc->Up, zu, na, sc->A, na);
         QG_CUDA(cudaGetLastError());
-        rc = gemm<QT_Q6K>(L.w_down, H, c.ffn, sc->A, c.ffn, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
+        rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
     }
     if (rc) return rc;
-    pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, nullptr, nullptr, H, c.eps);
+    pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, nullptr, nullptr, kPfChunk, H, c.eps);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
