@@ -231,6 +231,22 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
  * QG_ERR_CUDA, QG_ERR_TIMEOUT. */
 int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int n_tokens, int pos0, uint32_t* next_token);
 
+/* Batched decode of n sequences in lockstep (the decode session's batched
+ * decode, forward_qwen35_cuda.rs): token tokens[i] of the sequence held by
+ * states[i] at position positions[i], for n distinct states of this model with
+ * one KV cache format; writes each sequence's next token (the argmax of its
+ * logits under its own token mask) to next_tokens[i] and leaves each state as
+ * qg_decode_token would.  The projections read every weight once per step for
+ * all n sequences (n <= 4: a small-batch dequantizing GEMV, 4 multiply-adds per
+ * weight read; more: the prefill GEMM); the conv, delta rule and attention run
+ * per sequence on its own state; the lm_head runs once per sequence.  Runs on
+ * states[0]'s stream with its prefill scratch (made by the first call).
+ * Synchronous.  Errors: QG_ERR_ARG (NULL, a state of another model, one state
+ * twice, KV formats that differ), QG_ERR_SHAPE (n outside 1..16, head_k_dim !=
+ * 128), QG_ERR_TOKEN, QG_ERR_POS, QG_ERR_OOM, QG_ERR_CUDA, QG_ERR_TIMEOUT. */
+int qg_decode_batch(qg_model* m, qg_state* const* states, int n, const uint32_t* tokens, const int* positions,
+                    uint32_t* next_tokens);
+
 /* How the whole-token calls (qg_decode_token, qg_decode_greedy) run a step:
  * QG_STEP_KERNELS (the default): one kernel per fused op, chained with
  * programmatic dependent launch inside the step's CUDA graph;

@@ -35,6 +35,7 @@ EXPORTS = [
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
     "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records", "qg_prefill",
+    "qg_decode_batch",
 ]
 
 
@@ -106,6 +107,7 @@ def lib():
             "qg_state_create": [p, i, ctypes.POINTER(p)],
             "qg_state_create_kv": [p, i, i, ctypes.POINTER(p)],
             "qg_prefill": [p, p, p, i, i, ctypes.POINTER(ctypes.c_uint32)],
+            "qg_decode_batch": [p, p, i, p, p, p],
             "qg_state_kv_format": [p, ctypes.POINTER(i)],
             "qg_state_download_kv_records": [p, i, p, p, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "qg_state_destroy": [p],
@@ -420,6 +422,19 @@ def qg_prefill(model, state, tokens, pos0=0):
     out = ctypes.c_uint32()
     _check(lib().qg_prefill(model.handle, state.handle, _host(t), int(t.size), int(pos0), ctypes.byref(out)))
     return out.value
+
+
+def qg_decode_batch(model, states, tokens, positions):
+    """One lockstep decode step of len(states) sequences (qg_decode_batch);
+    returns their next tokens."""
+    n = len(states)
+    hs = (ctypes.c_void_p * n)(*[st.handle.value for st in states])
+    t = np.ascontiguousarray(tokens, np.uint32).reshape(-1)
+    p = np.ascontiguousarray(positions, np.int32).reshape(-1)
+    assert t.size == n and p.size == n
+    out = np.zeros(n, np.uint32)
+    _check(lib().qg_decode_batch(model.handle, ctypes.cast(hs, ctypes.c_void_p), n, _host(t), _host(p), _host(out)))
+    return [int(x) for x in out]
 
 
 def qg_decode_token_eager(model, state, token, pos):

@@ -26,6 +26,28 @@ constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarte
 
 __device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return static_cast<uint16_t>(p[0] | (p[1] << 8)); }
 
+// The columns of one pass split into segments: segment s is one sequence's
+// run of consecutive positions pos0[s].. in columns col0[s]..col0[s+1]-1, with
+// that sequence's state of the current layer (conv window and recurrent
+// state, or K/V cache).  A prefill is one segment; a batched decode step is
+// one single-column segment per sequence.
+constexpr int kMaxSeg = 16;
+struct Segs {
+    int n;
+    int col0[kMaxSeg + 1];
+    int pos0[kMaxSeg];
+    int max_seq[kMaxSeg];  // the sequence's cache length (the record stride of a quantized cache)
+    float* conv[kMaxSeg];
+    float* ssm[kMaxSeg];
+    float* kc[kMaxSeg];
+    float* vc[kMaxSeg];
+};
+__device__ __forceinline__ int seg_of(const Segs& sg, int p) {
+    int s = 0;
+    while (s + 1 < sg.n && p >= sg.col0[s + 1]) ++s;
+    return s;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
@@ -213,6 +235,90 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
     }
 }
 
+// Y = W X for at most 4 columns (a batched decode step): the weights are read
+// once and each is multiplied against the 4 columns' inputs.  X k-major
+// [k][kPfChunk] (the 4 columns of one k are one float4), staged in shared
+// memory; one warp per row, lane l dequantizing weights 8 l..8 l+7 of each
+// super-block from 8-byte loads of the planar layout, 4 accumulators, a warp
+// sum at the row's end.  Output token-major Y[t][ldy] or, ROW_MAJOR,
+// Y[row][ldy]; columns >= nm are not stored.  Grid: rows / 16 (capped), 512
+// threads, dynamic shared memory 16 k bytes.
+template <int QT, bool ROW_MAJOR>
+__global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                      const float* __restrict__ X, float* __restrict__ Y, int ldy,
+                                                      int nm) {
+    extern __shared__ __align__(16) float4 xs4[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < k; i += 512) xs4[i] = *reinterpret_cast<const float4*>(X + static_cast<size_t>(i) * kPfChunk);
+    __syncthreads();
+    const int nb = k / 256, n8 = (n + 7) & ~7;
+    const int GB = QT == QT_Q6K ? 1680 : 1152;
+    for (int row = blockIdx.x * 16 + warp; row < n; row += gridDim.x * 16) {
+        const int gi = row >> 3, rr = row & 7;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, GB);
+            float w[8];
+            if (QT == QT_Q4K) {
+                const uint8_t* blk = gb + 144 * rr;
+                const uint4 h = *reinterpret_cast<const uint4*>(blk);
+                const int j = lane >> 2, c = lane >> 3, o = 8 * (lane & 7);
+                const float d = f16_to_f32(static_cast<uint16_t>(h.x & 0xffffu));
+                const float dmin = f16_to_f32(static_cast<uint16_t>(h.x >> 16));
+                int sc, mn;
+                if (j < 4) {
+                    sc = byte_of(h, 4 + j) & 63;
+                    mn = byte_of(h, 8 + j) & 63;
+                } else {
+                    sc = (byte_of(h, 8 + j) & 15) | ((byte_of(h, j) >> 6) << 4);
+                    mn = (byte_of(h, 8 + j) >> 4) | ((byte_of(h, 4 + j) >> 6) << 4);
+                }
+                const float ds = d * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
+                const uint2 q = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + (o & 31));
+                const int sh = o < 32 ? 0 : 4;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t word = i < 4 ? q.x : q.y;
+                    w[i] = ds * static_cast<float>((word >> (8 * (i & 3) + sh)) & 15u) - dm;
+                }
+            } else {
+                // weights 8 lane.. = 128 h + 32 s + 16 p + i0.. of record (rr, 2h + p), scale s
+                const int hh = lane >> 4, sidx = (lane >> 2) & 3, pp = (lane >> 1) & 1, i0 = 8 * (lane & 1);
+                const int u = 4 * rr + 2 * hh + pp;
+                const uint8_t* rec = gb + 48 * u;
+                const uint2 nb8 = *reinterpret_cast<const uint2*>(rec + 16 * (sidx & 1) + i0);
+                const uint2 hb8 = *reinterpret_cast<const uint2*>(rec + 32 + i0);
+                const float ds = f16_to_f32(ld16(gb + 1664 + 2 * rr)) *
+                                 static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + sidx]));
+                const int nsh = 4 * (sidx >> 1), hsh = 2 * sidx;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t nw = i < 4 ? nb8.x : nb8.y, hw = i < 4 ? hb8.x : hb8.y;
+                    const int code = static_cast<int>((nw >> (8 * (i & 3) + nsh)) & 15u) |
+                                     (static_cast<int>((hw >> (8 * (i & 3) + hsh)) & 3u) << 4);
+                    w[i] = ds * static_cast<float>(code - 32);
+                }
+            }
+            const float4* xb = xs4 + 256 * b + 8 * lane;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 xv = xb[i];
+                acc[0] = fmaf(w[i], xv.x, acc[0]);
+                acc[1] = fmaf(w[i], xv.y, acc[1]);
+                acc[2] = fmaf(w[i], xv.z, acc[2]);
+                acc[3] = fmaf(w[i], xv.w, acc[3]);
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) acc[mm] = warp_sum(acc[mm]);
+        if (lane < nm) {
+            const float v = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+            if (ROW_MAJOR) Y[static_cast<size_t>(row) * ldy + lane] = v;
+            else Y[static_cast<size_t>(lane) * ldy + row] = v;
+        }
+    }
+}
+
 // Z = the `parts` split sums of a projection, added in split order.
 __global__ void pf_sum_parts_kernel(const float* __restrict__ Yp, int parts, size_t stride, float* __restrict__ Z,
                                     size_t count) {
@@ -266,7 +372,7 @@ __global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X,
 // recurrence, so the whole chunk runs at once.  Z rows [qkv C | alpha nv |
 // beta nv | z].  The window moves afterwards (pf_conv_window_kernel).
 __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P, int C, int nv, int K,
-                                     const float* __restrict__ win, const float* __restrict__ wconv,
+                                     const Segs sg, const float* __restrict__ wconv,
                                      const float* __restrict__ dt_bias, const float* __restrict__ a,
                                      float* __restrict__ Cq, float* __restrict__ dt, float* __restrict__ beta) {
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -274,11 +380,14 @@ __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P
     if (idx >= static_cast<long long>(P) * W) return;
     const int p = static_cast<int>(idx / W), c = static_cast<int>(idx - static_cast<long long>(p) * W);
     if (c < C) {
+        const int s = seg_of(sg, p), c0 = sg.col0[s];  // inputs before the segment's first column: its window
+        const float* win = sg.conv[s];
         const float* kw = wconv + static_cast<size_t>(c) * K;
         float acc = 0.0f;
         for (int t = 0; t < K - 1; ++t) {
             const int i = p - (K - 1) + t;
-            const float x = i >= 0 ? Z[static_cast<size_t>(i) * ldz + c] : win[static_cast<size_t>(c) * (K - 1) + (K - 1) + i];
+            const float x = i >= c0 ? Z[static_cast<size_t>(i) * ldz + c]
+                                    : win[static_cast<size_t>(c) * (K - 1) + (K - 1) + (i - c0)];
             acc += kw[t] * x;
         }
         acc += kw[K - 1] * Z[static_cast<size_t>(p) * ldz + c];
@@ -290,16 +399,18 @@ __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P
     }
 }
 
-// The conv window after the chunk: the last K-1 inputs, oldest first (from
-// the old window where the chunk is shorter than that).  One thread per row.
-__global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int P, int C, int K, float* __restrict__ win) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+// Each segment's conv window after the pass: its last K-1 inputs, oldest
+// first (from the old window where the segment is shorter than that).  Grid
+// (rows / 256, segments).
+__global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int C, int K, const Segs sg) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x, s = blockIdx.y;
     if (c >= C) return;
+    const int c0 = sg.col0[s], P = sg.col0[s + 1] - c0;
     float nw[kMaxConvTaps];
-    float* wc = win + static_cast<size_t>(c) * (K - 1);
+    float* wc = sg.conv[s] + static_cast<size_t>(c) * (K - 1);
     for (int t = 0; t < K - 1; ++t) {
         const int i = P - (K - 1) + t;
-        nw[t] = i >= 0 ? Z[static_cast<size_t>(i) * ldz + c] : wc[(K - 1) + i];
+        nw[t] = i >= 0 ? Z[static_cast<size_t>(c0 + i) * ldz + c] : wc[(K - 1) + i];
     }
     for (int t = 0; t < K - 1; ++t) wc[t] = nw[t];
 }
@@ -329,10 +440,19 @@ __global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, 
 // and k, the CTA's v values, the gates) are staged in shared memory by the
 // whole CTA, so the token loop reads shared memory only.  O [P][v_dim].
 constexpr int kDeltaStage = 32;
-__global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq, int C, int kdim,
-                                                       const float* __restrict__ QKn, const float* __restrict__ dt,
-                                                       const float* __restrict__ beta, float* __restrict__ S,
-                                                       float* __restrict__ O, int P, int nk, int nv, int dv) {
+__global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq_all, int C, int kdim,
+                                                       const float* __restrict__ QKn_all,
+                                                       const float* __restrict__ dt_all,
+                                                       const float* __restrict__ beta_all, const Segs sgs,
+                                                       float* __restrict__ O_all, int nk, int nv, int dv) {
+    // segment blockIdx.y: its columns c0.. and its recurrent state
+    const int c0 = sgs.col0[blockIdx.y], P = sgs.col0[blockIdx.y + 1] - c0;
+    float* __restrict__ S = sgs.ssm[blockIdx.y];
+    const float* Cq = Cq_all + static_cast<size_t>(c0) * C;
+    const float* QKn = QKn_all + static_cast<size_t>(c0) * 2 * nk * kDk;
+    const float* dt = dt_all + c0 * nv;
+    const float* beta = beta_all + c0 * nv;
+    float* O = O_all + static_cast<size_t>(c0) * nv * dv;
     __shared__ __align__(16) float sq[kDeltaStage][kDk];
     __shared__ __align__(16) float sk[kDeltaStage][kDk];
     __shared__ float sv[kDeltaStage][32];
@@ -440,15 +560,19 @@ __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restr
 // (to the f32 cache rows, or to staging rows for the quantizer).  Grid P.
 __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restrict__ Z, int ldz, int nh, int nkv,
                                                            const float* __restrict__ q_norm,
-                                                           const float* __restrict__ k_norm, int pos0, int n_rot,
+                                                           const float* __restrict__ k_norm, const Segs sg, int n_rot,
                                                            float theta_scale, float eps, float* __restrict__ Qn,
-                                                           float* __restrict__ Krow, float* __restrict__ Vrow,
-                                                           size_t row_stride) {
+                                                           float* __restrict__ Kst, float* __restrict__ Vst) {
     __shared__ float cs[kHd / 2], sn[kHd / 2];
     __shared__ __align__(16) float vec[8][kHd];
     const int p = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = n_rot / 2, qd = nh * kHd, kvd = nkv * kHd;
-    const int pos = pos0 + p;
+    const int s = seg_of(sg, p);
+    const int pos = sg.pos0[s] + (p - sg.col0[s]);
+    // K/V rows: straight into the sequence's f32 cache row pos, or (staging
+    // given) into column p of the staging rows for the quantizer
+    float* Krow = Kst ? Kst + static_cast<size_t>(p) * kvd : sg.kc[s] + static_cast<size_t>(pos) * kvd;
+    float* Vrow = Vst ? Vst + static_cast<size_t>(p) * kvd : sg.vc[s] + static_cast<size_t>(pos) * kvd;
     if (tid < half) {  // theta_0 = pos, theta_{i+1} = theta_i * theta_scale (f32 running product)
         float th = static_cast<float>(pos);
         for (int i = 0; i < tid; ++i) th = th * theta_scale;
@@ -458,7 +582,7 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
         sn[tid] = sv;
     }
     const float* z = Z + static_cast<size_t>(p) * ldz;
-    for (int i = tid; i < kvd; i += 256) Vrow[static_cast<size_t>(p) * row_stride + i] = z[2 * qd + kvd + i];
+    for (int i = tid; i < kvd; i += 256) Vrow[i] = z[2 * qd + kvd + i];
     __syncthreads();
     for (int job0 = 0; job0 < nh + nkv; job0 += 8) {
         const int job = job0 + warp;
@@ -481,8 +605,7 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
                 vec[warp][i + half] = x0 * sn[i] + x1 * cs[i];
             }
             __syncwarp();
-            float* dst = job < nh ? Qn + (static_cast<size_t>(p) * nh + job) * kHd
-                                  : Krow + static_cast<size_t>(p) * row_stride + (job - nh) * kHd;
+            float* dst = job < nh ? Qn + (static_cast<size_t>(p) * nh + job) * kHd : Krow + (job - nh) * kHd;
             for (int i = lane; i < kHd; i += 32) dst[i] = vec[warp][i];
             __syncwarp();
         }
@@ -496,13 +619,16 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
 // sigmoid(gate) and stored to column p of the k-major Att[nh*256][lda].
 template <int GS, bool KVQ>
 __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
-                                                             int ldz, const float* __restrict__ kc,
-                                                             const float* __restrict__ vc, int kvd, int max_seq,
-                                                             int pos0, float* __restrict__ Att, int lda) {
+                                                             int ldz, const Segs sg, int kvd,
+                                                             float* __restrict__ Att, int lda) {
     __shared__ float wml[8][GS][2];
     __shared__ __align__(16) float wacc[8][GS][kHd];
     const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nh = gridDim.y * GS, t_len = pos0 + p + 1;
+    const int sq = seg_of(sg, p);
+    const float* __restrict__ kc = sg.kc[sq];
+    const float* __restrict__ vc = sg.vc[sq];
+    const int max_seq = sg.max_seq[sq];
+    const int nh = gridDim.y * GS, t_len = sg.pos0[sq] + (p - sg.col0[sq]) + 1;
     float q[GS][8], m[GS], l[GS], acc[GS][8];
 #pragma unroll
     for (int i = 0; i < GS; ++i) {
@@ -632,6 +758,20 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits) {
+    if (P <= 4 && k * 16 <= 200 * 1024) {  // a batched decode step: the small-batch GEMV
+        if (used_splits) *used_splits = 1;
+        const int bsmem = k * 16;
+        static int bconfigured = 0;
+        if (bsmem > bconfigured) {
+            QG_CUDA(cudaFuncSetAttribute(bm_gemv_kernel<QT, ROW_MAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bsmem));
+            bconfigured = bsmem;
+        }
+        const int blocks = std::min((n + 15) / 16, 4 * device_sms());
+        bm_gemv_kernel<QT, ROW_MAJOR><<<blocks, 512, bsmem, st>>>(W, n, k, X, Y, ldy, P);
+        QG_CUDA(cudaGetLastError());
+        return QG_OK;
+    }
     const int nq = k / 64;
     if (splits > nq) splits = nq;
     if (splits < 1) splits = 1;
@@ -659,30 +799,56 @@ int splits_for(int n, int k, int P) {
 }
 
 template <bool KVQ>
-int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const float* kc,
-                  const float* vc, int kvd, int max_seq, int pos0, float* att) {
+int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const Segs& sg, int kvd,
+                  float* att) {
     switch (gs) {
-        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
-        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
-        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, kc, vc, kvd, max_seq, pos0, att, kPfChunk); break;
+        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
+        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
+        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
         default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
     }
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }
 
-// One chunk of P tokens at positions pos0.. through every layer; X holds the
-// residual stream of each token at the end (the last layer's output added).
-int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cudaStream_t st) {
+// One pass of columns through every layer: segment i is sequence ss[i]'s
+// tokens at positions pos0[i].. in columns col0[i]..col0[i+1]-1 (token ids in
+// sc->tok).  X holds each column's residual stream at the end.
+struct Pass {
+    int n;
+    qg_state* ss[kMaxSeg];
+    int pos0[kMaxSeg];
+    int col0[kMaxSeg + 1];
+};
+
+Segs segs_of(const Pass& ps, int il) {
+    Segs sg{};
+    sg.n = ps.n;
+    for (int i = 0; i < ps.n; ++i) {
+        sg.col0[i] = ps.col0[i];
+        sg.pos0[i] = ps.pos0[i];
+        sg.max_seq[i] = ps.ss[i]->max_seq;
+        sg.conv[i] = ps.ss[i]->conv[il];
+        sg.ssm[i] = ps.ss[i]->ssm[il];
+        sg.kc[i] = ps.ss[i]->kc[il];
+        sg.vc[i] = ps.ss[i]->vc[il];
+    }
+    sg.col0[ps.n] = ps.col0[ps.n];
+    return sg;
+}
+
+int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
     const qg_config& c = m->cfg;
-    const int H = c.hidden;
+    const int H = c.hidden, P = ps.col0[ps.n];
     const size_t part = static_cast<size_t>(P) * H;
+    const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
     pf_embed_kernel<<<P, 256, 0, st>>>(m->embd, sc->tok, H, sc->X);
     QG_CUDA(cudaGetLastError());
     int pending = 0;  // split sums of the last projection not yet added to X
     int rc = QG_OK;
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
+        const Segs sg = segs_of(ps, il);
         pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, kPfChunk, H, c.eps);
         QG_CUDA(cudaGetLastError());
         int zin = 1;
@@ -698,16 +864,16 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
             const long long cg = static_cast<long long>(P) * (C + nv);
             pf_conv_gates_kernel<<<static_cast<unsigned>((cg + 255) / 256), 256, 0, st>>>(
-                sc->Z, L.n_in, P, C, nv, c.conv_kernel, s->conv[il], L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
+                sc->Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
             QG_CUDA(cudaGetLastError());
-            pf_conv_window_kernel<<<(C + 255) / 256, 256, 0, st>>>(sc->Z, L.n_in, P, C, c.conv_kernel, s->conv[il]);
+            pf_conv_window_kernel<<<dim3((C + 255) / 256, ps.n), 256, 0, st>>>(sc->Z, L.n_in, C, c.conv_kernel, sg);
             QG_CUDA(cudaGetLastError());
             const int warps = P * 2 * c.n_k_heads;
             pf_l2norm_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(sc->Cq, C, m->k_dim, c.n_k_heads, P, c.eps,
                                                                       sc->QKn);
             QG_CUDA(cudaGetLastError());
-            pf_delta_kernel<<<nv * dv / 32, 256, 0, st>>>(sc->Cq, C, m->k_dim, sc->QKn, sc->dt, sc->beta, s->ssm[il],
-                                                         sc->O, P, c.n_k_heads, nv, dv);
+            pf_delta_kernel<<<dim3(nv * dv / 32, ps.n), 256, 0, st>>>(sc->Cq, C, m->k_dim, sc->QKn, sc->dt, sc->beta,
+                                                                     sg, sc->O, c.n_k_heads, nv, dv);
             QG_CUDA(cudaGetLastError());
             pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, sc->Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
                                                     sc->Uin, kPfChunk);
@@ -715,22 +881,22 @@ int run_chunk(const qg_model* m, qg_state* s, Scratch* sc, int P, int pos0, cuda
             k_out = m->v_dim;
         } else {
             const int nkv = c.n_kv_heads, kvd = m->kv_dim;
-            const bool kvq = s->kv_format == QG_KV_Q8_0_Q5_1;
-            float* Kdst = kvq ? sc->Ks : s->kc[il] + static_cast<size_t>(pos0) * kvd;
-            float* Vdst = kvq ? sc->Vs : s->vc[il] + static_cast<size_t>(pos0) * kvd;
-            pf_attn_prep_kernel<<<P, 256, 0, st>>>(sc->Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, pos0, c.n_rot,
-                                                   m->theta_scale, c.eps, sc->Qn, Kdst, Vdst, kvd);
+            pf_attn_prep_kernel<<<P, 256, 0, st>>>(sc->Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, sg, c.n_rot,
+                                                   m->theta_scale, c.eps, sc->Qn, kvq ? sc->Ks : nullptr,
+                                                   kvq ? sc->Vs : nullptr);
             QG_CUDA(cudaGetLastError());
-            if (kvq && (rc = kv_quantize_rows_at(sc->Ks, sc->Vs, P, pos0, nkv, s->max_seq,
-                                                 reinterpret_cast<uint8_t*>(s->kc[il]),
-                                                 reinterpret_cast<uint8_t*>(s->vc[il]), st)))
-                break;
+            for (int i = 0; kvq && i < ps.n && !rc; ++i) {
+                const qg_state* si = ps.ss[i];
+                const size_t off = static_cast<size_t>(ps.col0[i]) * kvd;
+                rc = kv_quantize_rows_at(sc->Ks + off, sc->Vs + off, ps.col0[i + 1] - ps.col0[i], ps.pos0[i], nkv,
+                                         si->max_seq, reinterpret_cast<uint8_t*>(si->kc[il]),
+                                         reinterpret_cast<uint8_t*>(si->vc[il]), st);
+            }
+            if (rc) break;
             const dim3 grid(P, nkv);
             const int gs = c.n_heads / nkv;
-            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, s->kc[il], s->vc[il], kvd, s->max_seq,
-                                           pos0, sc->Uin)
-                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, s->kc[il], s->vc[il], kvd, s->max_seq,
-                                            pos0, sc->Uin);
+            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin)
+                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin);
             if (rc) break;
             k_out = m->q_dim;
         }
@@ -787,7 +953,13 @@ extern "C" int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int 
     for (int c0 = 0; c0 < n_tokens && !rc; c0 += sc->chunk) {
         const int P = std::min(sc->chunk, n_tokens - c0);
         QG_CUDA(cudaMemcpyAsync(sc->tok, tokens + c0, sizeof(int) * P, cudaMemcpyHostToDevice, st));
-        rc = run_chunk(m, s, sc, P, pos0 + c0, st);
+        Pass ps{};
+        ps.n = 1;
+        ps.ss[0] = s;
+        ps.pos0[0] = pos0 + c0;
+        ps.col0[0] = 0;
+        ps.col0[1] = P;
+        rc = run_pass(m, ps, sc, st);
         if (!rc && c0 + P >= n_tokens)
             rc = run_lmhead_of(m, s, sc->X + static_cast<size_t>(P - 1) * c.hidden, st);
         if (!rc) QG_CUDA(cudaStreamSynchronize(st));  // the token copy of the next chunk reuses sc->tok
@@ -802,5 +974,56 @@ extern "C" int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int 
     }
     *next_token = out;
     if (s->kv_len < pos0 + n_tokens) s->kv_len = pos0 + n_tokens;
+    return QG_OK;
+}
+
+extern "C" int qg_decode_batch(qg_model* m, qg_state* const* states, int n, const uint32_t* tokens,
+                               const int* positions, uint32_t* next_tokens) {
+    if (!m || !states || !tokens || !positions || !next_tokens) return set_err(QG_ERR_ARG, "decode_batch: NULL argument");
+    if (n < 1 || n > kMaxSeg) return set_err(QG_ERR_SHAPE, "decode_batch: %d sequences (served: 1..%d)", n, kMaxSeg);
+    const qg_config& c = m->cfg;
+    if (c.head_k_dim != kDk) return set_err(QG_ERR_SHAPE, "decode_batch: head_k_dim %d is not served", c.head_k_dim);
+    for (int i = 0; i < n; ++i) {
+        qg_state* si = states[i];
+        if (!si || si->m != m) return set_err(QG_ERR_ARG, "decode_batch: state %d is NULL or of another model", i);
+        if (si->kv_format != states[0]->kv_format)
+            return set_err(QG_ERR_ARG, "decode_batch: the states' KV cache formats differ");
+        for (int j = 0; j < i; ++j)
+            if (states[j] == si) return set_err(QG_ERR_ARG, "decode_batch: state %d appears twice", i);
+        if (tokens[i] >= static_cast<uint32_t>(c.vocab))
+            return set_err(QG_ERR_TOKEN, "decode_batch: token %u is outside the %d-row embedding table", tokens[i], c.vocab);
+        if (positions[i] < 0 || positions[i] >= si->max_seq)
+            return set_err(QG_ERR_POS, "decode_batch: position %d is past the KV cache (%d rows)", positions[i], si->max_seq);
+    }
+    DeviceGuard dg(m->device);
+    Scratch* sc = nullptr;
+    int rc = scratch_of(m, states[0], &sc);
+    if (rc) return rc;
+    for (int i = 0; i < n; ++i) QG_CUDA(cudaStreamSynchronize(states[i]->stream));
+    cudaStream_t st = states[0]->stream;
+    QG_CUDA(cudaMemcpyAsync(sc->tok, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, st));
+    Pass ps{};
+    ps.n = n;
+    for (int i = 0; i < n; ++i) {
+        ps.ss[i] = states[i];
+        ps.pos0[i] = positions[i];
+        ps.col0[i] = i;
+    }
+    ps.col0[n] = n;
+    rc = run_pass(m, ps, sc, st);
+    for (int i = 0; i < n && !rc; ++i) rc = run_lmhead_of(m, states[i], sc->X + static_cast<size_t>(i) * c.hidden, st);
+    if (rc) return rc;
+    QG_CUDA(cudaStreamSynchronize(st));
+    for (int i = 0; i < n; ++i) {
+        unsigned out = 0;
+        QG_CUDA(cudaMemcpy(&out, states[i]->slots + 2, sizeof out, cudaMemcpyDeviceToHost));
+        if (out & 0x80000000u) {
+            unsigned e = 0;
+            cudaMemcpy(&e, states[i]->err, sizeof e, cudaMemcpyDeviceToHost);
+            return set_err(QG_ERR_TIMEOUT, "decode_batch: a kernel gave up on a bounded wait (flags 0x%x)", e);
+        }
+        next_tokens[i] = out;
+        if (states[i]->kv_len < positions[i] + 1) states[i]->kv_len = positions[i] + 1;
+    }
     return QG_OK;
 }
