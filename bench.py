@@ -434,6 +434,72 @@ def run_prefill(args):
     }), flush=True)
 
 
+def run_batch(args):
+    """One JSON line: --batch B sequences decoded in lockstep (qg_decode_batch),
+    each prefilled with its own seeded prompt, for K steps (the synchronous
+    calls timed by CUDA events on the first state's stream, host copies of the
+    B tokens and positions included), against one sequence through the
+    captured single-sequence step over the same K steps."""
+    import torch
+    import quantized_gemv_gated_gb300 as qg
+    cfg, desc = WORKLOADS[args.workload]
+    B, K = args.batch, args.steps
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    kvf = KV_FORMATS[args.kv_format]
+    states = [qg.State(m, cfg.max_seq_len, kvf) for _ in range(B)]
+
+    def prefill_all():
+        toks, pos = [], []
+        for i, st in enumerate(states):
+            st.reset()
+            prompt = synth.tokens(synth.subseed(synth.MASTER_SEED, f"batch.bench.{i}"), cfg.vocab, args.prompt)
+            toks.append(qg.qg_prefill(m, st, prompt))
+            pos.append(len(prompt))
+        return toks, pos
+
+    toks, pos = prefill_all()
+    for _ in range(args.warmup):
+        toks = qg.qg_decode_batch(m, states, toks, pos)
+        pos = [p + 1 for p in pos]
+    toks, pos = prefill_all()
+    assert pos[0] + K <= cfg.max_seq_len
+    ext = torch.cuda.ExternalStream(states[0].stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(ext)
+    for _ in range(K):
+        toks = qg.qg_decode_batch(m, states, toks, pos)
+        pos = [p + 1 for p in pos]
+    e1.record(ext)
+    e1.synchronize()
+    dt = e0.elapsed_time(e1) / 1000.0
+    # one sequence through the captured single-sequence step
+    one = states[0]
+    one.reset()
+    prompt = synth.tokens(synth.subseed(synth.MASTER_SEED, "batch.bench.0"), cfg.vocab, args.prompt)
+    t1 = qg.qg_prefill(m, one, prompt)
+    p1 = len(prompt)
+    t1 = qg.qg_decode_token(m, one, t1, p1)
+    ext1 = torch.cuda.ExternalStream(one.stream)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(ext1)
+    for i in range(K):
+        t1 = qg.qg_decode_token(m, one, t1, p1 + 1 + i)
+    f1.record(ext1)
+    f1.synchronize()
+    d1 = f0.elapsed_time(f1) / 1000.0
+    qg.qg_device_status()
+    print(json.dumps({
+        "mode": "batch", "workload": f"{args.workload}: {desc}", "kv_cache": KV_DESC[args.kv_format],
+        "sequences": B, "steps": K, "prompt_tokens_each": args.prompt,
+        "batch_tok_s": round(B * K / dt, 1), "batch_ms_per_step": round(1e3 * dt / K, 3),
+        "single_tok_s": round(K / d1, 1), "single_ms_per_step": round(1e3 * d1 / K, 3),
+        "ratio": round((B * K / dt) / (K / d1), 2),
+        "path": "small-batch GEMV (4 multiply-adds per weight read)" if B <= 4 else "prefill GEMM tiles",
+    }), flush=True)
+
+
 # GEMV shapes of the kernel mode: the building blocks at the model's shapes
 # (planar layouts, the layers' own path), lm_head with its fused argmax.
 KERNEL_SHAPES = [
@@ -522,6 +588,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
     ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
                     help="whole-token step: one kernel per fused op, or one persistent launch")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="decode this many sequences in lockstep (qg_decode_batch) against one sequence (one JSON line)")
     ap.add_argument("--prefill", action="store_true",
                     help="time qg_prefill of the workload's prompt against token-by-token decode (one JSON line)")
     ap.add_argument("--kernels", action="store_true",
@@ -536,6 +604,9 @@ def main():
         return
     if args.prefill:
         run_prefill(args)
+        return
+    if args.batch:
+        run_batch(args)
         return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":

@@ -238,71 +238,75 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
 // Y = W X for at most 4 columns (a batched decode step): the weights are read
 // once and each is multiplied against the 4 columns' inputs.  X k-major
 // [k][kPfChunk] (the 4 columns of one k are one float4), staged in shared
-// memory; one warp per row, lane l dequantizing weights 8 l..8 l+7 of each
-// super-block from 8-byte loads of the planar layout, 4 accumulators, a warp
-// sum at the row's end.  Output token-major Y[t][ldy] or, ROW_MAJOR,
-// Y[row][ldy]; columns >= nm are not stored.  Grid: rows / 16 (capped), 512
-// threads, dynamic shared memory 16 k bytes.
+// memory.  One CTA per 8-row group, two warps per row taking alternate
+// super-blocks; lane l dequantizes weights l, l + 32, .., l + 224 of a
+// super-block (one of each 32-weight sub-block: the warp's loads of the
+// weight bytes and of the staged inputs are consecutive, no bank conflicts)
+// into 4 accumulators; the two warps' sums meet in shared memory.  Output token-major Y[t][ldy] or, ROW_MAJOR,
+// Y[row][ldy]; columns >= nm are not stored.  Grid ceil(n/8), 512 threads,
+// dynamic shared memory 16 k bytes.
 template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                       const float* __restrict__ X, float* __restrict__ Y, int ldy,
                                                       int nm) {
     extern __shared__ __align__(16) float4 xs4[];
+    __shared__ float red[16][4];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < k; i += 512) xs4[i] = *reinterpret_cast<const float4*>(X + static_cast<size_t>(i) * kPfChunk);
     __syncthreads();
     const int nb = k / 256, n8 = (n + 7) & ~7;
     const int GB = QT == QT_Q6K ? 1680 : 1152;
-    for (int row = blockIdx.x * 16 + warp; row < n; row += gridDim.x * 16) {
-        const int gi = row >> 3, rr = row & 7;
+    const int gi = blockIdx.x, rr = warp & 7, half = warp >> 3;
+    {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int b = 0; b < nb; ++b) {
+#pragma unroll 2
+        for (int b = half; b < nb; b += 2) {
             const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, GB);
-            float w[8];
+            float w[8];  // weights lane + 32 i of the super-block (sub-block i)
             if (QT == QT_Q4K) {
                 const uint8_t* blk = gb + 144 * rr;
                 const uint4 h = *reinterpret_cast<const uint4*>(blk);
-                const int j = lane >> 2, c = lane >> 3, o = 8 * (lane & 7);
                 const float d = f16_to_f32(static_cast<uint16_t>(h.x & 0xffffu));
                 const float dmin = f16_to_f32(static_cast<uint16_t>(h.x >> 16));
-                int sc, mn;
-                if (j < 4) {
-                    sc = byte_of(h, 4 + j) & 63;
-                    mn = byte_of(h, 8 + j) & 63;
-                } else {
-                    sc = (byte_of(h, 8 + j) & 15) | ((byte_of(h, j) >> 6) << 4);
-                    mn = (byte_of(h, 8 + j) >> 4) | ((byte_of(h, 4 + j) >> 6) << 4);
-                }
-                const float ds = d * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
-                const uint2 q = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + (o & 31));
-                const int sh = o < 32 ? 0 : 4;
+                int qb[4];  // byte lane of each 64-weight chunk: the low nibble for sub-block 2c, the high for 2c + 1
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) qb[c4] = blk[16 + 32 * c4 + lane];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t word = i < 4 ? q.x : q.y;
-                    w[i] = ds * static_cast<float>((word >> (8 * (i & 3) + sh)) & 15u) - dm;
+                    int sc, mn;
+                    if (i < 4) {
+                        sc = byte_of(h, 4 + i) & 63;
+                        mn = byte_of(h, 8 + i) & 63;
+                    } else {
+                        sc = (byte_of(h, 8 + i) & 15) | ((byte_of(h, i) >> 6) << 4);
+                        mn = (byte_of(h, 8 + i) >> 4) | ((byte_of(h, 4 + i) >> 6) << 4);
+                    }
+                    const int nib = (i & 1) ? (qb[i >> 1] >> 4) : (qb[i >> 1] & 15);
+                    w[i] = (d * static_cast<float>(sc)) * static_cast<float>(nib) - dmin * static_cast<float>(mn);
                 }
             } else {
-                // weights 8 lane.. = 128 h + 32 s + 16 p + i0.. of record (rr, 2h + p), scale s
-                const int hh = lane >> 4, sidx = (lane >> 2) & 3, pp = (lane >> 1) & 1, i0 = 8 * (lane & 1);
-                const int u = 4 * rr + 2 * hh + pp;
-                const uint8_t* rec = gb + 48 * u;
-                const uint2 nb8 = *reinterpret_cast<const uint2*>(rec + 16 * (sidx & 1) + i0);
-                const uint2 hb8 = *reinterpret_cast<const uint2*>(rec + 32 + i0);
-                const float ds = f16_to_f32(ld16(gb + 1664 + 2 * rr)) *
-                                 static_cast<float>(static_cast<int8_t>(gb[1536 + 4 * u + sidx]));
-                const int nsh = 4 * (sidx >> 1), hsh = 2 * sidx;
+                // weight lane + 32 i = 128 hh + 32 s + 16 p + idx: byte idx of record (rr, 2 hh + p), scale s
+                const int pp = lane >> 4, idx = lane & 15;
+                const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t nw = i < 4 ? nb8.x : nb8.y, hw = i < 4 ? hb8.x : hb8.y;
-                    const int code = static_cast<int>((nw >> (8 * (i & 3) + nsh)) & 15u) |
-                                     (static_cast<int>((hw >> (8 * (i & 3) + hsh)) & 3u) << 4);
-                    w[i] = ds * static_cast<float>(code - 32);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int u = 4 * rr + 2 * hh + pp;
+                    const uint8_t* rec = gb + 48 * u;
+                    const int a = rec[idx], bq = rec[16 + idx], hb = rec[32 + idx];
+                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
+#pragma unroll
+                    for (int sidx = 0; sidx < 4; ++sidx) {
+                        const int nib = ((sidx & 1) ? bq : a) >> (4 * (sidx >> 1)) & 15;
+                        const int code = nib | (((hb >> (2 * sidx)) & 3) << 4);
+                        const float ds = d * static_cast<float>(static_cast<int8_t>((sw >> (8 * sidx)) & 0xffu));
+                        w[4 * hh + sidx] = ds * static_cast<float>(code - 32);
+                    }
                 }
             }
-            const float4* xb = xs4 + 256 * b + 8 * lane;
+            const float4* xb = xs4 + 256 * b + lane;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 xv = xb[i];
+                const float4 xv = xb[32 * i];
                 acc[0] = fmaf(w[i], xv.x, acc[0]);
                 acc[1] = fmaf(w[i], xv.y, acc[1]);
                 acc[2] = fmaf(w[i], xv.z, acc[2]);
@@ -311,10 +315,15 @@ __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict_
         }
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) acc[mm] = warp_sum(acc[mm]);
-        if (lane < nm) {
-            const float v = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
-            if (ROW_MAJOR) Y[static_cast<size_t>(row) * ldy + lane] = v;
-            else Y[static_cast<size_t>(lane) * ldy + row] = v;
+        if (lane < 4) red[warp][lane] = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int r = tid >> 2, mm = tid & 3, row = 8 * gi + r;
+        if (row < n && mm < nm) {
+            const float v = red[r][mm] + red[r + 8][mm];
+            if (ROW_MAJOR) Y[static_cast<size_t>(row) * ldy + mm] = v;
+            else Y[static_cast<size_t>(mm) * ldy + row] = v;
         }
     }
 }
@@ -689,12 +698,13 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
     }
 }
 
-// A = silu(G) * U, elementwise (k-major [ffn][chunk] arrays), G and U given as
-// split sums (added in order).
+// A = silu(G) * U, elementwise over the first P columns of k-major [ffn][chunk]
+// arrays, G and U given as split sums (added in order).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
-                                 size_t stride, float* __restrict__ A, size_t n) {
-    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= n) return;
+                                 size_t stride, float* __restrict__ A, int ffn, int P) {
+    const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= static_cast<size_t>(ffn) * P) return;
+    const size_t i = (e / P) * kPfChunk + (e % P);
     float g = Gp[i], u = Up[i];
     for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
     for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
@@ -767,8 +777,7 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
                                          bsmem));
             bconfigured = bsmem;
         }
-        const int blocks = std::min((n + 15) / 16, 4 * device_sms());
-        bm_gemv_kernel<QT, ROW_MAJOR><<<blocks, 512, bsmem, st>>>(W, n, k, X, Y, ldy, P);
+        bm_gemv_kernel<QT, ROW_MAJOR><<<(n + 7) / 8, 512, bsmem, st>>>(W, n, k, X, Y, ldy, P);
         QG_CUDA(cudaGetLastError());
         return QG_OK;
     }
@@ -908,8 +917,9 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
         int zg = 1, zu = 1;
         if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, kPfChunk, P, zf, st, &zg))) break;
         if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, kPfChunk, P, zf, st, &zu))) break;
-        const size_t na = static_cast<size_t>(c.ffn) * kPfChunk;  // k-major [ffn][chunk], columns >= P unused
-        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(sc->Zp, zg, sc->Up, zu, na, sc->A, na);
+        const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
+        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(
+            sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * kPfChunk, sc->A, c.ffn, P);
         QG_CUDA(cudaGetLastError());
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
     }
