@@ -71,3 +71,31 @@ def test_reference_arm_torchrun_world2_rank0_prints_only():
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
     assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_byte_model_of_the_kv_formats():
+    """Per token at KV length t, an attention layer moves 2 t kvd f32 values
+    plus the new row (f32 cache), or t n_kv (272 + 192) bytes of records, the
+    new row's records and its f32 V row written then read (quantized cache);
+    everything else is the same."""
+    import bench
+    import synth
+    cfg = synth.CFG_4B_LONG
+    n_attn = sum(1 for k in cfg.kinds() if k == synth.ATTENTION)
+    for t in (1, 8000):
+        f = bench.algorithmic_bytes(cfg, t)
+        q = bench.algorithmic_bytes(cfg, t, "q8_0-q5_1")
+        per_f = 2 * t * cfg.kv_dim * 4 + 2 * cfg.kv_dim * 4
+        per_q = t * cfg.n_kv_heads * 464 + cfg.n_kv_heads * 464 + 2 * cfg.kv_dim * 4
+        assert f - q == n_attn * (per_f - per_q)
+    assert bench.KV_FORMATS == {"f32": 0, "q8_0-q5_1": 1}
+
+
+def test_bench_modes_are_registered():
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, "bench.py", "--help"], capture_output=True, text=True, timeout=120,
+                         cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert out.returncode == 0
+    for flag in ("--kv-format", "--prefill", "--batch", "--kernels", "--impl"):
+        assert flag in out.stdout
