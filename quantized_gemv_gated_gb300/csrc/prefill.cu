@@ -236,24 +236,21 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
 }
 
 // Y = W X for at most 4 columns (a batched decode step): the weights are read
-// once and each is multiplied against the 4 columns' inputs.  X k-major
-// [k][kPfChunk] (the 4 columns of one k are one float4), staged in shared
-// memory.  One CTA per 8-row group, two warps per row taking alternate
+// once and each is multiplied against the 4 columns' inputs.  X packed
+// [k][4] (the 4 columns of one k are one float4), read straight from L1/L2 (a
+// warp's reads are 32 consecutive float4).  One CTA per 8-row group, two warps per row taking alternate
 // super-blocks; lane l dequantizes weights l, l + 32, .., l + 224 of a
 // super-block (one of each 32-weight sub-block: the warp's loads of the
 // weight bytes and of the staged inputs are consecutive, no bank conflicts)
 // into 4 accumulators; the two warps' sums meet in shared memory.  Output token-major Y[t][ldy] or, ROW_MAJOR,
-// Y[row][ldy]; columns >= nm are not stored.  Grid ceil(n/8), 512 threads,
-// dynamic shared memory 16 k bytes.
+// Y[row][ldy]; columns >= nm are not stored.  Grid ceil(n/8), 512 threads.
 template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                       const float* __restrict__ X, float* __restrict__ Y, int ldy,
                                                       int nm) {
-    extern __shared__ __align__(16) float4 xs4[];
     __shared__ float red[16][4];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < k; i += 512) xs4[i] = *reinterpret_cast<const float4*>(X + static_cast<size_t>(i) * kPfChunk);
-    __syncthreads();
+    const float4* __restrict__ xs4 = reinterpret_cast<const float4*>(X);
     const int nb = k / 256, n8 = (n + 7) & ~7;
     const int GB = QT == QT_Q6K ? 1680 : 1152;
     const int gi = blockIdx.x, rr = warp & 7, half = warp >> 3;
@@ -306,7 +303,7 @@ __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict_
             const float4* xb = xs4 + 256 * b + lane;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 xv = xb[32 * i];
+                const float4 xv = __ldg(xb + 32 * i);
                 acc[0] = fmaf(w[i], xv.x, acc[0]);
                 acc[1] = fmaf(w[i], xv.y, acc[1]);
                 acc[2] = fmaf(w[i], xv.z, acc[2]);
@@ -698,13 +695,13 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
     }
 }
 
-// A = silu(G) * U, elementwise over the first P columns of k-major [ffn][chunk]
+// A = silu(G) * U, elementwise over the first P columns of k-major [ffn][ldk]
 // arrays, G and U given as split sums (added in order).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
-                                 size_t stride, float* __restrict__ A, int ffn, int P) {
+                                 size_t stride, float* __restrict__ A, int ffn, int P, int ldk) {
     const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= static_cast<size_t>(ffn) * P) return;
-    const size_t i = (e / P) * kPfChunk + (e % P);
+    const size_t i = (e / P) * ldk + (e % P);
     float g = Gp[i], u = Up[i];
     for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
     for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
@@ -763,21 +760,15 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     return QG_OK;
 }
 
-// Y = W X with X k-major [k][kPfChunk]; ROW_MAJOR: Y[row][ldy] per split
-// (split stride n * ldy), else Y[token][ldy] (split stride P * ldy).
+// Y = W X with X k-major [k][ldk]: ldk = 4 (a pass of at most 4 columns, the
+// small-batch GEMV), else kPfChunk (the tiled GEMM).  ROW_MAJOR: Y[row][ldy]
+// per split (split stride n * ldy), else Y[token][ldy] (split stride P * ldy).
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits) {
-    if (P <= 4 && k * 16 <= 200 * 1024) {  // a batched decode step: the small-batch GEMV
+    if (P <= 4) {  // a batched decode step: the small-batch GEMV over packed [k][4] inputs
         if (used_splits) *used_splits = 1;
-        const int bsmem = k * 16;
-        static int bconfigured = 0;
-        if (bsmem > bconfigured) {
-            QG_CUDA(cudaFuncSetAttribute(bm_gemv_kernel<QT, ROW_MAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         bsmem));
-            bconfigured = bsmem;
-        }
-        bm_gemv_kernel<QT, ROW_MAJOR><<<(n + 7) / 8, 512, bsmem, st>>>(W, n, k, X, Y, ldy, P);
+        bm_gemv_kernel<QT, ROW_MAJOR><<<(n + 7) / 8, 512, 0, st>>>(W, n, k, X, Y, ldy, P);
         QG_CUDA(cudaGetLastError());
         return QG_OK;
     }
@@ -809,11 +800,11 @@ int splits_for(int n, int k, int P) {
 
 template <bool KVQ>
 int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const Segs& sg, int kvd,
-                  float* att) {
+                  float* att, int ldk) {
     switch (gs) {
-        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
-        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
-        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, kPfChunk); break;
+        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
+        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
+        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
         default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
     }
     QG_CUDA(cudaGetLastError());
@@ -849,6 +840,7 @@ Segs segs_of(const Pass& ps, int il) {
 int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
     const qg_config& c = m->cfg;
     const int H = c.hidden, P = ps.col0[ps.n];
+    const int ldk = P <= 4 ? 4 : kPfChunk;  // stride of the k-major GEMM inputs (packed for the small batch)
     const size_t part = static_cast<size_t>(P) * H;
     const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
     pf_embed_kernel<<<P, 256, 0, st>>>(m->embd, sc->tok, H, sc->X);
@@ -858,7 +850,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
         const Segs sg = segs_of(ps, il);
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, kPfChunk, H, c.eps);
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, ldk, H, c.eps);
         QG_CUDA(cudaGetLastError());
         int zin = 1;
         if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
@@ -885,7 +877,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
                                                                      sg, sc->O, c.n_k_heads, nv, dv);
             QG_CUDA(cudaGetLastError());
             pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, sc->Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
-                                                    sc->Uin, kPfChunk);
+                                                    sc->Uin, ldk);
             QG_CUDA(cudaGetLastError());
             k_out = m->v_dim;
         } else {
@@ -904,22 +896,22 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
             if (rc) break;
             const dim3 grid(P, nkv);
             const int gs = c.n_heads / nkv;
-            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin)
-                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin);
+            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin, ldk)
+                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin, ldk);
             if (rc) break;
             k_out = m->q_dim;
         }
         if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending)))
             break;
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, kPfChunk, H, c.eps);
+        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldk, H, c.eps);
         QG_CUDA(cudaGetLastError());
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
-        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, kPfChunk, P, zf, st, &zg))) break;
-        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, kPfChunk, P, zf, st, &zu))) break;
+        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg))) break;
+        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu))) break;
         const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
         pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(
-            sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * kPfChunk, sc->A, c.ffn, P);
+            sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk);
         QG_CUDA(cudaGetLastError());
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
     }
