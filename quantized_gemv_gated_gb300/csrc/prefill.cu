@@ -244,6 +244,69 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
 // weight bytes and of the staged inputs are consecutive, no bank conflicts)
 // into 4 accumulators; the two warps' sums meet in shared memory.  Output token-major Y[t][ldy] or, ROW_MAJOR,
 // Y[row][ldy]; columns >= nm are not stored.  Grid ceil(n/8), 512 threads.
+// One warp's part of row (gi, rr) of a small-batch GEMV: the super-blocks
+// b = half, half + 2, .. of the row, lane l taking weights l + 32 i of each,
+// multiplied against the 4 packed input columns xs4[k] into acc[4].
+template <int QT>
+__device__ __forceinline__ void bm_row_acc(const uint8_t* __restrict__ W, int n8, int nb, int gi, int rr, int half,
+                                           int lane, const float4* __restrict__ xs4, float* acc) {
+    const int GB = QT == QT_Q6K ? 1680 : 1152;
+#pragma unroll 2
+    for (int b = half; b < nb; b += 2) {
+        const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, GB);
+        float w[8];  // weights lane + 32 i of the super-block (sub-block i)
+        if (QT == QT_Q4K) {
+            const uint8_t* blk = gb + 144 * rr;
+            const uint4 h = *reinterpret_cast<const uint4*>(blk);
+            const float d = f16_to_f32(static_cast<uint16_t>(h.x & 0xffffu));
+            const float dmin = f16_to_f32(static_cast<uint16_t>(h.x >> 16));
+            int qb[4];  // byte lane of each 64-weight chunk: the low nibble for sub-block 2c, the high for 2c + 1
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) qb[c4] = blk[16 + 32 * c4 + lane];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                int sc, mn;
+                if (i < 4) {
+                    sc = byte_of(h, 4 + i) & 63;
+                    mn = byte_of(h, 8 + i) & 63;
+                } else {
+                    sc = (byte_of(h, 8 + i) & 15) | ((byte_of(h, i) >> 6) << 4);
+                    mn = (byte_of(h, 8 + i) >> 4) | ((byte_of(h, 4 + i) >> 6) << 4);
+                }
+                const int nib = (i & 1) ? (qb[i >> 1] >> 4) : (qb[i >> 1] & 15);
+                w[i] = (d * static_cast<float>(sc)) * static_cast<float>(nib) - dmin * static_cast<float>(mn);
+            }
+        } else {
+            // weight lane + 32 i = 128 hh + 32 s + 16 p + idx: byte idx of record (rr, 2 hh + p), scale s
+            const int pp = lane >> 4, idx = lane & 15;
+            const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int u = 4 * rr + 2 * hh + pp;
+                const uint8_t* rec = gb + 48 * u;
+                const int a = rec[idx], bq = rec[16 + idx], hb = rec[32 + idx];
+                const uint32_t sw = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
+#pragma unroll
+                for (int sidx = 0; sidx < 4; ++sidx) {
+                    const int nib = ((sidx & 1) ? bq : a) >> (4 * (sidx >> 1)) & 15;
+                    const int code = nib | (((hb >> (2 * sidx)) & 3) << 4);
+                    const float ds = d * static_cast<float>(static_cast<int8_t>((sw >> (8 * sidx)) & 0xffu));
+                    w[4 * hh + sidx] = ds * static_cast<float>(code - 32);
+                }
+            }
+        }
+        const float4* xb = xs4 + 256 * b + lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 xv = __ldg(xb + 32 * i);
+            acc[0] = fmaf(w[i], xv.x, acc[0]);
+            acc[1] = fmaf(w[i], xv.y, acc[1]);
+            acc[2] = fmaf(w[i], xv.z, acc[2]);
+            acc[3] = fmaf(w[i], xv.w, acc[3]);
+        }
+    }
+}
+
 template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                       const float* __restrict__ X, float* __restrict__ Y, int ldy,
@@ -252,64 +315,10 @@ __global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float4* __restrict__ xs4 = reinterpret_cast<const float4*>(X);
     const int nb = k / 256, n8 = (n + 7) & ~7;
-    const int GB = QT == QT_Q6K ? 1680 : 1152;
     const int gi = blockIdx.x, rr = warp & 7, half = warp >> 3;
     {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 2
-        for (int b = half; b < nb; b += 2) {
-            const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, GB);
-            float w[8];  // weights lane + 32 i of the super-block (sub-block i)
-            if (QT == QT_Q4K) {
-                const uint8_t* blk = gb + 144 * rr;
-                const uint4 h = *reinterpret_cast<const uint4*>(blk);
-                const float d = f16_to_f32(static_cast<uint16_t>(h.x & 0xffffu));
-                const float dmin = f16_to_f32(static_cast<uint16_t>(h.x >> 16));
-                int qb[4];  // byte lane of each 64-weight chunk: the low nibble for sub-block 2c, the high for 2c + 1
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) qb[c4] = blk[16 + 32 * c4 + lane];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    int sc, mn;
-                    if (i < 4) {
-                        sc = byte_of(h, 4 + i) & 63;
-                        mn = byte_of(h, 8 + i) & 63;
-                    } else {
-                        sc = (byte_of(h, 8 + i) & 15) | ((byte_of(h, i) >> 6) << 4);
-                        mn = (byte_of(h, 8 + i) >> 4) | ((byte_of(h, 4 + i) >> 6) << 4);
-                    }
-                    const int nib = (i & 1) ? (qb[i >> 1] >> 4) : (qb[i >> 1] & 15);
-                    w[i] = (d * static_cast<float>(sc)) * static_cast<float>(nib) - dmin * static_cast<float>(mn);
-                }
-            } else {
-                // weight lane + 32 i = 128 hh + 32 s + 16 p + idx: byte idx of record (rr, 2 hh + p), scale s
-                const int pp = lane >> 4, idx = lane & 15;
-                const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int u = 4 * rr + 2 * hh + pp;
-                    const uint8_t* rec = gb + 48 * u;
-                    const int a = rec[idx], bq = rec[16 + idx], hb = rec[32 + idx];
-                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
-#pragma unroll
-                    for (int sidx = 0; sidx < 4; ++sidx) {
-                        const int nib = ((sidx & 1) ? bq : a) >> (4 * (sidx >> 1)) & 15;
-                        const int code = nib | (((hb >> (2 * sidx)) & 3) << 4);
-                        const float ds = d * static_cast<float>(static_cast<int8_t>((sw >> (8 * sidx)) & 0xffu));
-                        w[4 * hh + sidx] = ds * static_cast<float>(code - 32);
-                    }
-                }
-            }
-            const float4* xb = xs4 + 256 * b + lane;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 xv = __ldg(xb + 32 * i);
-                acc[0] = fmaf(w[i], xv.x, acc[0]);
-                acc[1] = fmaf(w[i], xv.y, acc[1]);
-                acc[2] = fmaf(w[i], xv.z, acc[2]);
-                acc[3] = fmaf(w[i], xv.w, acc[3]);
-            }
-        }
+        bm_row_acc<QT>(W, n8, nb, gi, rr, half, lane, xs4, acc);
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) acc[mm] = warp_sum(acc[mm]);
         if (lane < 4) red[warp][lane] = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
@@ -855,19 +864,21 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
         int zin = 1;
         if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
             break;
-        {
+        const float* Z = sc->Zp;  // the input projection's output [P][n_in]: one split is already the sum
+        if (zin > 1) {
             const size_t cnt = static_cast<size_t>(P) * L.n_in;
             pf_sum_parts_kernel<<<static_cast<unsigned>((cnt + 255) / 256), 256, 0, st>>>(sc->Zp, zin, cnt, sc->Z, cnt);
             QG_CUDA(cudaGetLastError());
+            Z = sc->Z;
         }
         int k_out;
         if (m->kinds[il] == QG_LAYER_DELTANET) {
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
             const long long cg = static_cast<long long>(P) * (C + nv);
             pf_conv_gates_kernel<<<static_cast<unsigned>((cg + 255) / 256), 256, 0, st>>>(
-                sc->Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
+                Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
             QG_CUDA(cudaGetLastError());
-            pf_conv_window_kernel<<<dim3((C + 255) / 256, ps.n), 256, 0, st>>>(sc->Z, L.n_in, C, c.conv_kernel, sg);
+            pf_conv_window_kernel<<<dim3((C + 255) / 256, ps.n), 256, 0, st>>>(Z, L.n_in, C, c.conv_kernel, sg);
             QG_CUDA(cudaGetLastError());
             const int warps = P * 2 * c.n_k_heads;
             pf_l2norm_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(sc->Cq, C, m->k_dim, c.n_k_heads, P, c.eps,
@@ -876,13 +887,13 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
             pf_delta_kernel<<<dim3(nv * dv / 32, ps.n), 256, 0, st>>>(sc->Cq, C, m->k_dim, sc->QKn, sc->dt, sc->beta,
                                                                      sg, sc->O, c.n_k_heads, nv, dv);
             QG_CUDA(cudaGetLastError());
-            pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, sc->Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
+            pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
                                                     sc->Uin, ldk);
             QG_CUDA(cudaGetLastError());
             k_out = m->v_dim;
         } else {
             const int nkv = c.n_kv_heads, kvd = m->kv_dim;
-            pf_attn_prep_kernel<<<P, 256, 0, st>>>(sc->Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, sg, c.n_rot,
+            pf_attn_prep_kernel<<<P, 256, 0, st>>>(Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, sg, c.n_rot,
                                                    m->theta_scale, c.eps, sc->Qn, kvq ? sc->Ks : nullptr,
                                                    kvq ? sc->Vs : nullptr);
             QG_CUDA(cudaGetLastError());
@@ -896,8 +907,8 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
             if (rc) break;
             const dim3 grid(P, nkv);
             const int gs = c.n_heads / nkv;
-            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin, ldk)
-                     : launch_causal<false>(gs, grid, st, sc->Qn, sc->Z, L.n_in, sg, kvd, sc->Uin, ldk);
+            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk)
+                     : launch_causal<false>(gs, grid, st, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk);
             if (rc) break;
             k_out = m->q_dim;
         }

@@ -127,3 +127,40 @@ def test_batch_arguments():
     with pytest.raises(qg.QgError) as e:
         qg.qg_decode_batch(m, many, [1] * 17, [0] * 17)
     assert e.value.code == qg.QG_ERR_SHAPE
+
+
+def test_batch_token_masks_per_sequence():
+    """The batched lm_head keeps each sequence's own token mask: sequence 0
+    unmasked, sequence 1 under a random allow set, sequence 2 allowed one id."""
+    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=64)
+    w = synth.make_model_weights(cfg)
+    m, om = qg.Model(w), oracle.Model(w)
+    V = cfg.vocab
+    rng = np.random.default_rng(synth.subseed(synth.MASTER_SEED, "batch.masks"))
+
+    def allow(ids):
+        words = np.zeros((V + 31) // 32, np.uint32)
+        for i in ids:
+            words[i >> 5] |= np.uint32(1) << np.uint32(i & 31)
+        return words
+
+    masks = [None, allow(np.flatnonzero(rng.random(V) < 0.2)), allow([int(rng.integers(V))])]
+    states = [qg.State(m, cfg.max_seq_len) for _ in range(3)]
+    ostates = [oracle.State(om) for _ in range(3)]
+    for st, mk in zip(states, masks):
+        st.set_token_mask(mk)
+    toks, pos = [11, 12, 13], [0, 0, 0]
+    for step in range(5):
+        got = qg.qg_decode_batch(m, states, toks, pos)
+        for i in range(3):
+            ref, _, lg = oracle.forward_token(om, ostates[i], toks[i], pos[i], want_logits=True)
+            want = ref if masks[i] is None else oracle.argmax_masked(lg, masks[i])
+            if masks[i] is not None:
+                assert (masks[i][got[i] >> 5] >> np.uint32(got[i] & 31)) & 1, f"seq {i}: banned id {got[i]}"
+                x = lg.astype(np.float64).copy()
+                ids = np.arange(V)
+                x[((masks[i][ids >> 5] >> (ids & 31).astype(np.uint32)) & 1) == 0] = -np.finfo(np.float32).max
+                assert _token_ok(got[i], want, x.astype(np.float32))
+            else:
+                assert _token_ok(got[i], want, lg)
+            toks[i], pos[i] = want, pos[i] + 1
