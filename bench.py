@@ -435,7 +435,8 @@ def run_prefill(args):
 
 
 def run_batch(args):
-    """One JSON line: --batch B sequences decoded in lockstep (qg_decode_batch),
+    """One JSON line: --batch B sequences decoded in lockstep (qg_batch_step:
+    the step as one captured graph),
     each prefilled with its own seeded prompt, for K steps (the synchronous
     calls timed by CUDA events on the first state's stream, host copies of the
     B tokens and positions included), against one sequence through the
@@ -458,9 +459,10 @@ def run_batch(args):
             pos.append(len(prompt))
         return toks, pos
 
+    bt = qg.Batch(m, states)  # one captured graph per step (qg_batch_step)
     toks, pos = prefill_all()
     for _ in range(args.warmup):
-        toks = qg.qg_decode_batch(m, states, toks, pos)
+        toks = bt.step(toks, pos)
         pos = [p + 1 for p in pos]
     toks, pos = prefill_all()
     assert pos[0] + K <= cfg.max_seq_len
@@ -469,11 +471,12 @@ def run_batch(args):
     torch.cuda.synchronize()
     e0.record(ext)
     for _ in range(K):
-        toks = qg.qg_decode_batch(m, states, toks, pos)
+        toks = bt.step(toks, pos)
         pos = [p + 1 for p in pos]
     e1.record(ext)
     e1.synchronize()
     dt = e0.elapsed_time(e1) / 1000.0
+    bt.close()
     # one sequence through the captured single-sequence step
     one = states[0]
     one.reset()

@@ -247,6 +247,19 @@ int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int n_tokens, i
 int qg_decode_batch(qg_model* m, qg_state* const* states, int n, const uint32_t* tokens, const int* positions,
                     uint32_t* next_tokens);
 
+/* The same lockstep decode for a fixed set of sequences through one captured
+ * CUDA graph: qg_batch_create records the states (n distinct states of m, one
+ * KV format; they must outlive the batch, and their streams are not used
+ * meanwhile by other calls); each qg_batch_step copies the n tokens and
+ * positions in from pinned memory, replays the step (captured on the first
+ * call; positions are read on the device, so any valid positions replay) and
+ * copies the n tokens out.  Results are those of qg_decode_batch.  Errors: as
+ * qg_decode_batch. */
+typedef struct qg_batch qg_batch;
+int qg_batch_create(qg_model* m, qg_state* const* states, int n, qg_batch** out);
+int qg_batch_step(qg_batch* b, const uint32_t* tokens, const int* positions, uint32_t* next_tokens);
+int qg_batch_destroy(qg_batch* b);
+
 /* How the whole-token calls (qg_decode_token, qg_decode_greedy) run a step:
  * QG_STEP_KERNELS (the default): one kernel per fused op, chained with
  * programmatic dependent launch inside the step's CUDA graph;

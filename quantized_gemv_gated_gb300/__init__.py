@@ -35,7 +35,7 @@ EXPORTS = [
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
     "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records", "qg_prefill",
-    "qg_decode_batch",
+    "qg_decode_batch", "qg_batch_create", "qg_batch_step", "qg_batch_destroy",
 ]
 
 
@@ -108,6 +108,9 @@ def lib():
             "qg_state_create_kv": [p, i, i, ctypes.POINTER(p)],
             "qg_prefill": [p, p, p, i, i, ctypes.POINTER(ctypes.c_uint32)],
             "qg_decode_batch": [p, p, i, p, p, p],
+            "qg_batch_create": [p, p, i, ctypes.POINTER(p)],
+            "qg_batch_step": [p, p, p, p],
+            "qg_batch_destroy": [p],
             "qg_state_kv_format": [p, ctypes.POINTER(i)],
             "qg_state_download_kv_records": [p, i, p, p, ctypes.POINTER(sz), ctypes.POINTER(sz)],
             "qg_state_destroy": [p],
@@ -435,6 +438,39 @@ def qg_decode_batch(model, states, tokens, positions):
     out = np.zeros(n, np.uint32)
     _check(lib().qg_decode_batch(model.handle, ctypes.cast(hs, ctypes.c_void_p), n, _host(t), _host(p), _host(out)))
     return [int(x) for x in out]
+
+
+class Batch:
+    """A fixed set of sequences decoded in lockstep through one captured graph
+    (qg_batch_create / qg_batch_step / qg_batch_destroy)."""
+
+    def __init__(self, model, states):
+        self.model, self.states = model, list(states)
+        hs = (ctypes.c_void_p * len(self.states))(*[st.handle.value for st in self.states])
+        h = ctypes.c_void_p()
+        _check(lib().qg_batch_create(model.handle, ctypes.cast(hs, ctypes.c_void_p), len(self.states),
+                                     ctypes.byref(h)))
+        self.handle = h
+
+    def step(self, tokens, positions):
+        n = len(self.states)
+        t = np.ascontiguousarray(tokens, np.uint32).reshape(-1)
+        p = np.ascontiguousarray(positions, np.int32).reshape(-1)
+        assert t.size == n and p.size == n
+        out = np.zeros(n, np.uint32)
+        _check(lib().qg_batch_step(self.handle, _host(t), _host(p), _host(out)))
+        return [int(x) for x in out]
+
+    def close(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            lib().qg_batch_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def qg_decode_token_eager(model, state, token, pos):

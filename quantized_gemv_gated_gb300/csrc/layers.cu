@@ -563,10 +563,12 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
 // Grid (rows, n_kv): one CTA per (position, kv head), warp w makes block w
 // of its K and V records with the append's quantizer.
 __global__ void __launch_bounds__(256) kv_quantize_kernel(const float* __restrict__ k, const float* __restrict__ v,
-                                                          int n_kv, int max_seq, int pos0, uint8_t* kq, uint8_t* vq) {
+                                                          int n_kv, int max_seq, int pos0, const int* pos0_dev,
+                                                          uint8_t* kq, uint8_t* vq) {
     const int t = blockIdx.x, g = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t src = (static_cast<size_t>(t) * n_kv + g) * kHd + 32 * warp + lane;
-    const size_t rec = static_cast<size_t>(g) * max_seq + pos0 + t;
+    const int base = pos0_dev ? *pos0_dev : pos0;  // first position: an argument, or read on the device
+    const size_t rec = static_cast<size_t>(g) * max_seq + base + t;
     kvq_put_q8_0(k[src], lane, warp, kq + rec * kKRec);
     kvq_put_q5_1(v[src], lane, warp, vq + rec * kVRec);
 }
@@ -580,7 +582,15 @@ int kv_quantize_rows_at(const float* k, const float* v, int rows, int pos0, int 
                         uint8_t* vq, cudaStream_t st) {
     if (rows <= 0) return QG_OK;
     if (pos0 < 0 || pos0 + rows > max_seq) return set_err(QG_ERR_POS, "kv_quantize: rows past the cache");
-    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, pos0, kq, vq);
+    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, pos0, nullptr, kq, vq);
+    QG_CUDA(cudaGetLastError());
+    return QG_OK;
+}
+
+int kv_quantize_rows_dev(const float* k, const float* v, int rows, const int* pos0_dev, int n_kv, int max_seq,
+                         uint8_t* kq, uint8_t* vq, cudaStream_t st) {
+    if (rows <= 0) return QG_OK;
+    kv_quantize_kernel<<<dim3(rows, n_kv), 256, 0, st>>>(k, v, n_kv, max_seq, 0, pos0_dev, kq, vq);
     QG_CUDA(cudaGetLastError());
     return QG_OK;
 }

@@ -35,7 +35,7 @@ constexpr int kMaxSeg = 16;
 struct Segs {
     int n;
     int col0[kMaxSeg + 1];
-    int pos0[kMaxSeg];
+    const int* pos0;       // device: first position of each segment (so a captured pass replays with new ones)
     int max_seq[kMaxSeg];  // the sequence's cache length (the record stride of a quantized cache)
     float* conv[kMaxSeg];
     float* ssm[kMaxSeg];
@@ -722,6 +722,7 @@ struct Scratch {
     int chunk;
     int* tok;
     float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
+    int* pos;  // device: the pass's first position per segment [kMaxSeg]
 };
 
 template <class T>
@@ -750,7 +751,7 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     if (!sc) return set_err(QG_ERR_OOM, "prefill: host allocation");
     sc->chunk = kPfChunk;
     int rc = QG_OK;
-    (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H)) ||
+    (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->pos, kMaxSeg)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H)) ||
            (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, kPfMaxSplit * P * H)) ||
            (rc = pf_alloc(s, &sc->Zp, kPfMaxSplit * P * std::max(n_in, static_cast<size_t>(c.ffn)))) ||
            (rc = pf_alloc(s, &sc->Up, kPfMaxSplit * P * c.ffn)) ||
@@ -826,7 +827,7 @@ int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const flo
 struct Pass {
     int n;
     qg_state* ss[kMaxSeg];
-    int pos0[kMaxSeg];
+    const int* pos_dev;  // device: first position of each segment
     int col0[kMaxSeg + 1];
 };
 
@@ -835,7 +836,6 @@ Segs segs_of(const Pass& ps, int il) {
     sg.n = ps.n;
     for (int i = 0; i < ps.n; ++i) {
         sg.col0[i] = ps.col0[i];
-        sg.pos0[i] = ps.pos0[i];
         sg.max_seq[i] = ps.ss[i]->max_seq;
         sg.conv[i] = ps.ss[i]->conv[il];
         sg.ssm[i] = ps.ss[i]->ssm[il];
@@ -843,6 +843,7 @@ Segs segs_of(const Pass& ps, int il) {
         sg.vc[i] = ps.ss[i]->vc[il];
     }
     sg.col0[ps.n] = ps.col0[ps.n];
+    sg.pos0 = ps.pos_dev;
     return sg;
 }
 
@@ -900,9 +901,9 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
             for (int i = 0; kvq && i < ps.n && !rc; ++i) {
                 const qg_state* si = ps.ss[i];
                 const size_t off = static_cast<size_t>(ps.col0[i]) * kvd;
-                rc = kv_quantize_rows_at(sc->Ks + off, sc->Vs + off, ps.col0[i + 1] - ps.col0[i], ps.pos0[i], nkv,
-                                         si->max_seq, reinterpret_cast<uint8_t*>(si->kc[il]),
-                                         reinterpret_cast<uint8_t*>(si->vc[il]), st);
+                rc = kv_quantize_rows_dev(sc->Ks + off, sc->Vs + off, ps.col0[i + 1] - ps.col0[i], ps.pos_dev + i,
+                                          nkv, si->max_seq, reinterpret_cast<uint8_t*>(si->kc[il]),
+                                          reinterpret_cast<uint8_t*>(si->vc[il]), st);
             }
             if (rc) break;
             const dim3 grid(P, nkv);
@@ -966,10 +967,13 @@ extern "C" int qg_prefill(qg_model* m, qg_state* s, const uint32_t* tokens, int 
     for (int c0 = 0; c0 < n_tokens && !rc; c0 += sc->chunk) {
         const int P = std::min(sc->chunk, n_tokens - c0);
         QG_CUDA(cudaMemcpyAsync(sc->tok, tokens + c0, sizeof(int) * P, cudaMemcpyHostToDevice, st));
+        const int p0 = pos0 + c0;
+        QG_CUDA(cudaMemcpyAsync(sc->pos, &p0, sizeof(int), cudaMemcpyHostToDevice, st));
+        QG_CUDA(cudaStreamSynchronize(st));  // p0 lives on this frame
         Pass ps{};
         ps.n = 1;
         ps.ss[0] = s;
-        ps.pos0[0] = pos0 + c0;
+        ps.pos_dev = sc->pos;
         ps.col0[0] = 0;
         ps.col0[1] = P;
         rc = run_pass(m, ps, sc, st);
@@ -1015,11 +1019,12 @@ extern "C" int qg_decode_batch(qg_model* m, qg_state* const* states, int n, cons
     for (int i = 0; i < n; ++i) QG_CUDA(cudaStreamSynchronize(states[i]->stream));
     cudaStream_t st = states[0]->stream;
     QG_CUDA(cudaMemcpyAsync(sc->tok, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, st));
+    QG_CUDA(cudaMemcpyAsync(sc->pos, positions, sizeof(int) * n, cudaMemcpyHostToDevice, st));
     Pass ps{};
     ps.n = n;
+    ps.pos_dev = sc->pos;
     for (int i = 0; i < n; ++i) {
         ps.ss[i] = states[i];
-        ps.pos0[i] = positions[i];
         ps.col0[i] = i;
     }
     ps.col0[n] = n;
@@ -1037,6 +1042,145 @@ extern "C" int qg_decode_batch(qg_model* m, qg_state* const* states, int n, cons
         }
         next_tokens[i] = out;
         if (states[i]->kv_len < positions[i] + 1) states[i]->kv_len = positions[i] + 1;
+    }
+    return QG_OK;
+}
+
+// ----------------------------------------------------------- batch graphs
+// A fixed set of sequences decoded in lockstep through one captured CUDA graph:
+// per step, the tokens and positions go in from pinned host memory, the pass
+// and each sequence's lm_head argmax run, and the n token words come back.
+struct qg_batch {
+    qg_model* m;
+    int n;
+    qg_state* ss[kMaxSeg];
+    int* pinned;  // [0, 16) tokens, [16, 32) positions, [32, 48) token words out
+    cudaGraphExec_t exec;
+};
+
+namespace {
+
+int batch_check(const qg_model* m, qg_state* const* states, int n) {
+    if (n < 1 || n > kMaxSeg) return set_err(QG_ERR_SHAPE, "batch: %d sequences (served: 1..%d)", n, kMaxSeg);
+    if (m->cfg.head_k_dim != kDk) return set_err(QG_ERR_SHAPE, "batch: head_k_dim %d is not served", m->cfg.head_k_dim);
+    for (int i = 0; i < n; ++i) {
+        qg_state* si = states[i];
+        if (!si || si->m != m) return set_err(QG_ERR_ARG, "batch: state %d is NULL or of another model", i);
+        if (si->kv_format != states[0]->kv_format) return set_err(QG_ERR_ARG, "batch: the states' KV cache formats differ");
+        for (int j = 0; j < i; ++j)
+            if (states[j] == si) return set_err(QG_ERR_ARG, "batch: state %d appears twice", i);
+    }
+    return QG_OK;
+}
+
+int batch_inputs_check(const qg_model* m, qg_state* const* states, int n, const uint32_t* tokens,
+                       const int* positions) {
+    for (int i = 0; i < n; ++i) {
+        if (tokens[i] >= static_cast<uint32_t>(m->cfg.vocab))
+            return set_err(QG_ERR_TOKEN, "batch: token %u is outside the %d-row embedding table", tokens[i], m->cfg.vocab);
+        if (positions[i] < 0 || positions[i] >= states[i]->max_seq)
+            return set_err(QG_ERR_POS, "batch: position %d is past the KV cache (%d rows)", positions[i],
+                           states[i]->max_seq);
+    }
+    return QG_OK;
+}
+
+}  // namespace
+
+extern "C" int qg_batch_create(qg_model* m, qg_state* const* states, int n, qg_batch** out) {
+    if (!m || !states || !out) return set_err(QG_ERR_ARG, "batch_create: NULL argument");
+    int rc = batch_check(m, states, n);
+    if (rc) return rc;
+    DeviceGuard dg(m->device);
+    Scratch* sc = nullptr;
+    if ((rc = scratch_of(m, states[0], &sc))) return rc;
+    qg_batch* b = new (std::nothrow) qg_batch();
+    if (!b) return set_err(QG_ERR_OOM, "batch_create: host allocation");
+    b->m = m;
+    b->n = n;
+    for (int i = 0; i < n; ++i) b->ss[i] = states[i];
+    b->exec = nullptr;
+    void* p = nullptr;
+    const cudaError_t e = cudaHostAlloc(&p, 48 * sizeof(int), cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+        delete b;
+        return cuda_err(e, "batch_create: cudaHostAlloc");
+    }
+    b->pinned = static_cast<int*>(p);
+    std::memset(b->pinned, 0, 48 * sizeof(int));
+    *out = b;
+    return QG_OK;
+}
+
+extern "C" int qg_batch_destroy(qg_batch* b) {
+    if (!b) return QG_OK;
+    DeviceGuard dg(b->m->device);
+    cudaStreamSynchronize(b->ss[0]->stream);
+    if (b->exec) cudaGraphExecDestroy(b->exec);
+    if (b->pinned) cudaFreeHost(b->pinned);
+    delete b;
+    return QG_OK;
+}
+
+extern "C" int qg_batch_step(qg_batch* b, const uint32_t* tokens, const int* positions, uint32_t* next_tokens) {
+    if (!b || !tokens || !positions || !next_tokens) return set_err(QG_ERR_ARG, "batch_step: NULL argument");
+    qg_model* m = b->m;
+    const int n = b->n;
+    int rc = batch_inputs_check(m, b->ss, n, tokens, positions);
+    if (rc) return rc;
+    DeviceGuard dg(m->device);
+    for (int i = 1; i < n; ++i) QG_CUDA(cudaStreamSynchronize(b->ss[i]->stream));
+    cudaStream_t st = b->ss[0]->stream;
+    QG_CUDA(cudaStreamSynchronize(st));
+    Scratch* sc = static_cast<Scratch*>(b->ss[0]->pf);
+    for (int i = 0; i < n; ++i) {
+        b->pinned[i] = static_cast<int>(tokens[i]);
+        b->pinned[16 + i] = positions[i];
+    }
+    if (!b->exec) {  // capture once: copies in, the pass, each lm_head, the token words out
+        cudaGraph_t g = nullptr;
+        QG_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed));
+        cudaError_t e = cudaMemcpyAsync(sc->tok, b->pinned, sizeof(int) * n, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(sc->pos, b->pinned + 16, sizeof(int) * n, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) rc = cuda_err(e, "batch_step: capture H2D");
+        Pass ps{};
+        ps.n = n;
+        ps.pos_dev = sc->pos;
+        for (int i = 0; i < n; ++i) {
+            ps.ss[i] = b->ss[i];
+            ps.col0[i] = i;
+        }
+        ps.col0[n] = n;
+        if (!rc) rc = run_pass(m, ps, sc, st);
+        for (int i = 0; i < n && !rc; ++i)
+            rc = run_lmhead_of(m, b->ss[i], sc->X + static_cast<size_t>(i) * m->cfg.hidden, st);
+        for (int i = 0; i < n && !rc; ++i) {
+            e = cudaMemcpyAsync(b->pinned + 32 + i, b->ss[i]->slots + 2, sizeof(int), cudaMemcpyDeviceToHost, st);
+            if (e != cudaSuccess) rc = cuda_err(e, "batch_step: capture D2H");
+        }
+        const cudaError_t ee = cudaStreamEndCapture(st, &g);
+        if (!rc && ee != cudaSuccess) rc = cuda_err(ee, "batch_step: cudaStreamEndCapture");
+        if (!rc) {
+            e = cudaGraphInstantiate(&b->exec, g, 0);
+            if (e != cudaSuccess) {
+                rc = cuda_err(e, "batch_step: cudaGraphInstantiate");
+                b->exec = nullptr;
+            }
+        }
+        if (g) cudaGraphDestroy(g);
+        if (rc) return rc;
+    }
+    QG_CUDA(cudaGraphLaunch(b->exec, st));
+    QG_CUDA(cudaStreamSynchronize(st));
+    for (int i = 0; i < n; ++i) {
+        const unsigned w = static_cast<unsigned>(b->pinned[32 + i]);
+        if (w & 0x80000000u) {
+            unsigned e = 0;
+            cudaMemcpy(&e, b->ss[i]->err, sizeof e, cudaMemcpyDeviceToHost);
+            return set_err(QG_ERR_TIMEOUT, "batch_step: a kernel gave up on a bounded wait (flags 0x%x)", e);
+        }
+        next_tokens[i] = w;
+        if (b->ss[i]->kv_len < positions[i] + 1) b->ss[i]->kv_len = positions[i] + 1;
     }
     return QG_OK;
 }

@@ -122,6 +122,10 @@ int kv_quantize_rows_at(const float* k, const float* v, int rows, int pos0, int 
                         uint8_t* vq, cudaStream_t st);
 // Free the batched-prefill scratch descriptor (its device buffers are in s->allocs).
 void prefill_release(qg_state* s);
+// The same with the first position read on the device (*pos0_dev; rows must be
+// within the cache, which the caller checks on the host).
+int kv_quantize_rows_dev(const float* k, const float* v, int rows, const int* pos0_dev, int n_kv, int max_seq,
+                         uint8_t* kq, uint8_t* vq, cudaStream_t st);
 // Persistent step kernel: fill s->step (once per state), launch one step.
 int step_setup(const qg_model* m, qg_state* s);
 int run_step(qg_state* s, cudaStream_t st, bool advance);

@@ -164,3 +164,36 @@ def test_batch_token_masks_per_sequence():
             else:
                 assert _token_ok(got[i], want, lg)
             toks[i], pos[i] = want, pos[i] + 1
+
+
+@pytest.mark.parametrize("kv_format", [qg.KV_F32, qg.KV_Q8_0_Q5_1])
+def test_batch_graph_matches_eager_bitwise(kv_format):
+    """qg_batch_step (one captured graph, positions read on the device) against
+    qg_decode_batch on twin states: the same kernels in the same order, so the
+    same tokens and bitwise the same residual streams, step after step."""
+    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=64)
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    n = 3
+    ea = [qg.State(m, cfg.max_seq_len, kv_format) for _ in range(n)]
+    gr = [qg.State(m, cfg.max_seq_len, kv_format) for _ in range(n)]
+    toks, pos = [], []
+    for i in range(n):
+        prompt = synth.tokens(synth.subseed(synth.MASTER_SEED, f"batch.graph.{i}"), cfg.vocab, 3 + 2 * i)
+        a = qg.qg_prefill(m, ea[i], prompt)
+        b = qg.qg_prefill(m, gr[i], prompt)
+        assert a == b
+        toks.append(a)
+        pos.append(len(prompt))
+    bt = qg.Batch(m, gr)
+    for step in range(6):
+        te = qg.qg_decode_batch(m, ea, toks, pos)
+        tg = bt.step(toks, pos)
+        assert te == tg, f"step {step}: eager {te} graph {tg}"
+        for i in range(n):
+            assert np.array_equal(ea[i].download_hidden(), gr[i].download_hidden())
+        toks, pos = te, [p + 1 for p in pos]
+    for i in range(n):
+        assert gr[i].kv_len == pos[i]
+    bt.close()
+    qg.qg_device_status()
