@@ -8,6 +8,13 @@
 // 0..pos0+p (causal).  The state it leaves (conv windows, recurrent states, K/V
 // rows, the residual stream) is the state the token-by-token decode leaves,
 // and the lm_head argmax of the last token is the first generated token.
+//
+// The same pass runs the batched decode (the decode session's batched decode):
+// its columns are split into segments, one per sequence, each with that
+// sequence's state and positions, so a lockstep step of n sequences is n
+// single-column segments; with at most 4 columns the projections use a
+// small-batch GEMV that reads each weight once for all of them, and a fixed set
+// of sequences can replay the whole step as one captured graph (qg_batch_*).
 #include <algorithm>
 #include <cstring>
 #include <new>
