@@ -197,3 +197,27 @@ def test_batch_graph_matches_eager_bitwise(kv_format):
         assert gr[i].kv_len == pos[i]
     bt.close()
     qg.qg_device_status()
+
+
+def test_batch_graph_arguments():
+    cfg = synth.CFG_TINY
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    s1, s2 = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
+    with pytest.raises(qg.QgError) as e:
+        qg.Batch(m, [s1, s1])
+    assert e.value.code == qg.QG_ERR_ARG
+    with pytest.raises(qg.QgError) as e:
+        qg.Batch(m, [s1, qg.State(m, cfg.max_seq_len, qg.KV_Q8_0_Q5_1)])
+    assert e.value.code == qg.QG_ERR_ARG
+    bt = qg.Batch(m, [s1, s2])
+    with pytest.raises(qg.QgError) as e:
+        bt.step([1, cfg.vocab], [0, 0])
+    assert e.value.code == qg.QG_ERR_TOKEN
+    with pytest.raises(qg.QgError) as e:
+        bt.step([1, 2], [0, cfg.max_seq_len])
+    assert e.value.code == qg.QG_ERR_POS
+    # refused inputs change nothing: the first real step still matches the eager call
+    t3, t4 = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
+    assert bt.step([1, 2], [0, 0]) == qg.qg_decode_batch(m, [t3, t4], [1, 2], [0, 0])
+    bt.close()
