@@ -18,12 +18,12 @@
  *     -> attn_output GEMV -> residual -> post_attention_norm -> SwiGLU FFN
  *     -> residual
  *   token: embedding row -> every layer -> output rms_norm -> lm_head GEMV
- *     (no bias) -> argmax, first index of the maximum (aprender PR #4332,
- *     "Greedy GPU argmax").
+ *     (no bias) -> argmax, first index of the maximum (aprender PR #4332, the
+ *     greedy argmax on the GPU).
  *
  * Precision is the page's: weights dequantized to f32, f32 accumulation in
- * natural index order ("The CPU reference dequantizes to f32 and accumulates
- * in f32", forward_qwen35_cuda.rs, pin_reference_gemv).  An f64-accumulating
+ * natural index order (the CPU reference of forward_qwen35_cuda.rs,
+ * pin_reference_gemv, dequantizes to f32 and sums in f32).  An f64-accumulating
  * GEMV is kept for the error-bound pins (attn_q_gemv_of_host_input there).
  * Row loops may run on several OpenMP threads; each row's sum stays
  * sequential, so the thread count never changes a result.
@@ -349,7 +349,7 @@ void or_delta_rule(const float* q, const float* k, const float* v, const float* 
 }
 
 /* Per value head: u = rmsnorm(o_h) * w * silu(z_h), w shared by the heads
- * (gdn_gated_rmsnorm_into; memra gated_rmsnorm "PER d_state-ROW").  Reading:
+ * (gdn_gated_rmsnorm_into; memra gated_rmsnorm normalises each value-head row).  Reading:
  * the gate activation is SiLU. */
 void or_gated_rmsnorm(const float* o, const float* z, const float* w, float* u, int dv, int nv,
                       float eps) {
@@ -449,9 +449,9 @@ void or_attention(const float* q, const float* kc, const float* vc, float* out, 
 /* ---------------------------------------------------- quantized KV cache */
 /*
  * The decode session's quantized KV cache (forward_qwen35_cuda.rs, full
- * attention layer: "q8_0 K / q5_1 V" appended by an on-device quantize
- * kernel, attention over the resident byte K/V).  The pages name the two
- * GGML block types and nothing more; their contents here are what those
+ * attention layer: K as q8_0 blocks and V as q5_1 blocks, appended by a
+ * quantize kernel on the device, the attention reading the quantized bytes).
+ * That source names the two GGML block types and nothing more; their contents here are what those
  * names denote in GGUF (reading):
  *   q8_0, 34 bytes per 32 values: f16 d, int8 q[32];            x = d*q
  *   q5_1, 24 bytes per 32 values: f16 d, f16 m, u32 qh, u8 qs[16];
@@ -586,7 +586,7 @@ void or_sigmoid_gate(float* x, const float* gate, int n) {
 }
 
 /* First index of the maximum (the CPU argmax of aprender PR #4332; qualia
- * merges candidates with "v > max || v == max && id < best").  NaN never
+ * merges candidates by value, the smaller index winning a tie).  NaN never
  * wins; an all-NaN vector gives 0. */
 int or_argmax(const float* x, int n) {
     int best = -1;
