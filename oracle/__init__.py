@@ -6,8 +6,11 @@ import it.  The arithmetic lives in qg_oracle.c (plain C, f32 as the pages fix
 it); this module compiles it, marshals numpy arrays into its structs and
 keeps the model/state objects alive.
 
-Every function of qg_oracle.c is pinned by tests/test_oracle_pins.py against
-closed forms, invariants, hand-worked examples or brute force.
+Every function of qg_oracle.c is pinned by tests/test_oracle_pins.py and
+tests/test_oracle_kvq.py against closed forms, invariants, hand-worked
+examples or brute force; the layer and whole-token compositions are pinned by
+tests/test_oracle_compose.py, which restates them from those primitives and
+checks that planted wiring mistakes are detected.
 """
 import ctypes
 import os
