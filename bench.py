@@ -2,30 +2,37 @@
 """Batch-1 decode benchmark of the hybrid Gated-DeltaNet / attention model on GB300.
 
 One step = one whole token (every layer, output norm, lm_head + argmax) of
-the chosen workload.  Default workload: the 0.8B-shaped hybrid (24 layers,
-850 prompt tokens fed one per step, then greedy tokens).  Prints ONE JSON line.
+the chosen workload.  Default workload: the 4B-shaped hybrid (32 layers,
+850 prompt tokens fed one per step, then greedy tokens), the largest
+single-GPU configuration.  Prints ONE JSON line.
 
   value      tokens/s of the device-resident greedy loop (qg_decode_greedy: one
              CUDA-graph replay per token, token and position stay on the GPU),
              timed with CUDA events on the state's stream, max over ranks.
   e2e        tokens/s through qg_decode_token: per token an 8-byte H2D of
              (token, position) from pinned memory and a 4-byte D2H of the id.
-  roofline   the dominant kernel (fused lm_head GEMV + argmax over the
-             248,320-row Q6_K table) timed live with CUDA events on its stream,
-             algorithmic bytes per launch / duration vs the measured HBM peak.
-  cpu_baseline  the CPU oracle on a bounded sample of the same workload.
+  kernels    every kernel kind of the step timed live with CUDA events: a CUDA
+             graph of PDL-chained launches of that exact kernel over the
+             model's layers (qg_bench_kernel), per-launch time, algorithmic
+             bytes, HBM rate and share of the step (launches per token x time).
+  roofline   the kernel with the largest share: algorithmic bytes per launch /
+             its CUDA-event duration vs the measured HBM peak.
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload, at the
+             same positions (the state before them synthetic), all host cores
+             and one core.
 
-  python bench.py [--workload 0.8b|4b|4b-long] [--steps K] [--warmup W]
+  python bench.py [--workload 4b|0.8b|4b-long] [--steps K] [--warmup W]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+  python bench.py --layer                (one DeltaNet layer step, us per step)
   python bench.py --kernels              (GEMV building blocks, one line per shape)
 Multi-GPU: torchrun --nproc-per-node N bench.py --gpus N: N independent
 replicas (weak scaling, no collective on the data path).
 """
 import argparse
-import glob
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import tempfile
@@ -87,6 +94,111 @@ def lmhead_bytes(cfg):
     return cfg.vocab * cfg.hidden // 256 * 210 + cfg.hidden * 4
 
 
+DTYPE = ("f32 (GEMV: each activation a 24-bit block-fixed-point integer per 256-element block, exact integer "
+         "sub-block sums with dp4a, f32 accumulation; norms, recurrences and attention in f32)")
+
+# kernel kinds of the step (qg_bench_kernel): name, launches per token
+KERNEL_KINDS = [("dn_in", 0), ("delta", 1), ("ssm_out", 2), ("attn_in", 3), ("attn", 4), ("attn_out", 5),
+                ("ffn_up", 6), ("ffn_down", 7), ("lmhead", 8)]
+
+
+def kernel_bytes(cfg, kind, t_rows, kv="f32"):
+    """Algorithmic HBM bytes of one launch of a kernel kind: its weights as
+    stored, the state it reads and writes (DeltaNet state and conv window, KV
+    rows), the f32 vectors it reads or writes; the same accounting as
+    algorithmic_bytes, split by kernel (the per-layer sums add up to it)."""
+    H, F = cfg.hidden, cfg.ffn
+    q4 = lambda n, k: n * k // 256 * 144  # noqa: E731
+    q6 = lambda n, k: n * k // 256 * 210  # noqa: E731
+    if kind == "dn_in":
+        return (q4(cfg.conv_dim + 2 * cfg.n_v_heads + cfg.v_dim, H) + cfg.conv_dim * cfg.conv_kernel * 4
+                + 2 * cfg.conv_dim * (cfg.conv_kernel - 1) * 4 + 2 * cfg.n_v_heads * 4 + H * 4)
+    if kind == "delta":
+        return 2 * cfg.n_v_heads * cfg.head_v_dim * cfg.head_k_dim * 4
+    if kind == "ssm_out":
+        return q4(H, cfg.v_dim) + cfg.head_v_dim * 4
+    if kind == "attn_in":
+        return q4(2 * cfg.q_dim + 2 * cfg.kv_dim, H) + H * 4
+    if kind == "attn":
+        if kv == "f32":
+            return 2 * t_rows * cfg.kv_dim * 4 + 2 * cfg.kv_dim * 4 + 2 * cfg.head_dim * 4
+        rec = cfg.n_kv_heads * (272 + 192)
+        return t_rows * rec + rec + 2 * cfg.kv_dim * 4 + 2 * cfg.head_dim * 4
+    if kind == "attn_out":
+        return q4(H, cfg.q_dim)
+    if kind == "ffn_up":
+        return 2 * q4(F, H) + H * 4
+    if kind == "ffn_down":
+        return q6(H, F)
+    return q6(cfg.vocab, H) + H * 4 + H * 4  # + the output norm and the embedding row
+
+
+def kernel_launches(cfg, kind):
+    """Launches of a kernel kind per token."""
+    kinds = cfg.kinds()
+    n_dn = sum(1 for k in kinds if k == synth.DELTANET)
+    return {"dn_in": n_dn, "delta": n_dn, "ssm_out": n_dn, "attn_in": len(kinds) - n_dn, "attn": len(kinds) - n_dn,
+            "attn_out": len(kinds) - n_dn, "ffn_up": len(kinds), "ffn_down": len(kinds), "lmhead": 1}[kind]
+
+
+def time_kernels(qg, m, cfg, kvf, kv_name, pos, long_ctx, peak, reps=4):
+    """Each kernel kind of the step timed with CUDA events: a CUDA graph of
+    PDL-chained launches of that kernel over the model's layers (qg_bench_kernel,
+    on a separate state brought to the timed position), replayed `reps` times;
+    per-launch time = graph time / launches.  Weights rotate over the layers, so
+    every launch streams from HBM as in the step (the lm_head's 208-521 MB
+    exceed the L2 by themselves)."""
+    import torch
+    st = qg.State(m, cfg.max_seq_len, kvf)
+    prefill_synthetic(qg, st, cfg, pos)
+    stream = torch.cuda.Stream()
+    out, total = [], 0.0
+    t_rows = pos + 1
+    for name, kind in KERNEL_KINDS:
+        n_per_tok = kernel_launches(cfg, name)
+        if n_per_tok == 0:
+            continue
+        launches = 4 if name == "lmhead" else max(2 * n_per_tok, 16)
+        with torch.cuda.stream(stream):
+            qg.qg_bench_kernel(m, st, kind, launches, stream.cuda_stream)  # eager: grants shared memory
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            qg.qg_bench_kernel(m, st, kind, launches, stream.cuda_stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * launches)
+        b = kernel_bytes(cfg, name, t_rows, kv_name)
+        gbs = b / us / 1e3
+        out.append({"kernel": name, "launches_per_token": n_per_tok, "us_per_launch": round(us, 3),
+                    "bytes_per_launch": int(b), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        total += n_per_tok * us
+        del g
+    qg.qg_device_status()
+    st.close()
+    for k in out:
+        k["share"] = round(k["launches_per_token"] * k["us_per_launch"] / total, 4)
+    return out
+
+
+def prefill_synthetic(qg, st, cfg, pos):
+    """A state at position `pos` with synthetic contents: every attention
+    layer's K/V rows 0..pos-1 N(0,1), every DeltaNet window and state
+    N(0,0.1) (the same recipe as the long-context workload)."""
+    for il, kind in enumerate(cfg.kinds()):
+        if kind == synth.DELTANET:
+            st.upload_layer(il, *synth.initial_deltanet_state(cfg, il))
+        elif pos > 0:
+            st.upload_kv(il, *synth.long_context_kv(cfg, il, pos))
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -96,16 +208,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# The translation unit of the lm_head GEMV + argmax building block whose DRAM
-# counters profiles/traffic.json records: gemv.cu and the headers it includes.
-LMHEAD_SOURCES = ("gemv.cu", "qg_host.cuh", "qg_gemv.cuh", "qg_common.cuh")
-
-
+# profiles/traffic.json records ncu DRAM bytes per launch of the step's kernels,
+# keyed by kernel kind, with a hash of the CUDA sources they were taken from:
+# a record taken from other sources reads as unknown (null).
 def kernel_sources_hash():
     h = hashlib.sha256()
-    for name in LMHEAD_SOURCES:
-        with open(os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -214,22 +327,98 @@ def prefill(qg, m, st, cfg, long_ctx, n_prompt=synth.PROMPT_LEN):
     return len(toks), tok
 
 
-def cpu_baseline(cfg, budget_s=12.0, kv="f32"):
-    """The oracle as it stands, on the host cores, decoding the workload's prompt
-    from position 0 until the time budget is spent."""
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_at(cfg, pos0, kv="f32"):
+    """The oracle's model and a state at position pos0 with synthetic contents
+    (K/V rows 0..pos0-1 N(0,1), DeltaNet windows and states N(0,0.1)): a token
+    at pos0.. then costs what it costs in the decode being timed."""
     import oracle
     w = synth.make_model_weights(cfg)
     om = oracle.Model(w)
     ost = oracle.State(om, KV_FORMATS[kv])
-    toks = synth.prompt_tokens(cfg)
+    for il, kind in enumerate(cfg.kinds()):
+        if kind == synth.DELTANET:
+            c, s_ = synth.initial_deltanet_state(cfg, il)
+            ost.conv[il][:] = c
+            ost.ssm[il][:] = s_
+        elif pos0 > 0:
+            ost.set_kv_rows(il, *synth.long_context_kv(cfg, il, pos0))
+    ost.kv_len = pos0
+    return om, ost
+
+
+def time_oracle(om, ost, pos0, n_max, budget_s, threads):
+    """Tokens per second of oracle.forward_token at positions pos0.. on
+    `threads` host threads (0: all), at least one token, stopping when the
+    budget is spent."""
+    import oracle
+    oracle.set_threads(threads if threads else os.cpu_count() or 1)
+    tok = int(synth.tokens(synth.subseed(synth.MASTER_SEED, "bench.oracle"), om.cfg.vocab, 1)[0])
     n, t0 = 0, time.perf_counter()
-    while n < len(toks) and (n < 2 or time.perf_counter() - t0 < budget_s):
-        oracle.forward_token(om, ost, int(toks[n]), n)
+    while n < n_max and (n < 1 or time.perf_counter() - t0 < budget_s):
+        tok, _, _ = oracle.forward_token(om, ost, tok, pos0 + n)
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 4), "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{n} prompt tokens decoded from position 0 by the f32 C oracle (OpenMP over GEMV rows), "
-                      f"{dt:.1f} s"}
+    used = oracle.max_threads()
+    oracle.set_threads(os.cpu_count() or 1)
+    return n, dt, used
+
+
+def time_oracle_layer(budget_s, threads):
+    """Microseconds per step of the oracle's single DeltaNet layer (the
+    one-layer workload: 8 steps, fresh N(0,1) hidden each step)."""
+    import oracle
+    cfg = synth.CFG_LAYER
+    w = synth.make_model_weights(cfg)
+    om = oracle.Model(w)
+    ost = oracle.State(om)
+    c, s_ = synth.initial_deltanet_state(cfg, 0)
+    ost.conv[0][:] = c
+    ost.ssm[0][:] = s_
+    hs = synth.layer_inputs(cfg, 8)
+    oracle.set_threads(threads if threads else os.cpu_count() or 1)
+    n, t0 = 0, time.perf_counter()
+    while n < 8 or time.perf_counter() - t0 < min(budget_s, 2.0):
+        oracle.deltanet_layer(om, ost, 0, hs[n % 8])
+        n += 1
+        if n >= 400:
+            break
+    dt = time.perf_counter() - t0
+    used = oracle.max_threads()
+    oracle.set_threads(os.cpu_count() or 1)
+    return round(1e6 * dt / n, 1), n, used
+
+
+def cpu_baseline(cfg, pos0, n_max, kv="f32", budget_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    timed workload: tokens at the GPU arm's positions pos0.. from a synthetic
+    state at pos0, on all cores (the value) and on one core; plus the
+    one-layer step in microseconds."""
+    om, ost = oracle_at(cfg, pos0, kv)
+    n, dt, used = time_oracle(om, ost, pos0, n_max, budget_s, 0)
+    om1, ost1 = oracle_at(cfg, pos0, kv)
+    n1, dt1, _ = time_oracle(om1, ost1, pos0, max(1, min(n_max, 2)), budget_s / 3, 1)
+    layer_all, nl, _ = time_oracle_layer(budget_s, 0)
+    layer_one, _, _ = time_oracle_layer(budget_s, 1)
+    return {"value": round(n / dt, 4), "unit": "tok/s", "cores": used, "kind": "oracle",
+            "cpu": cpu_model(), "host_cores": os.cpu_count(),
+            "sample": f"{n} tokens at positions {pos0}..{pos0 + n - 1} (the GPU arm's timed positions) by the f32 C "
+                      f"oracle with OpenMP over GEMV rows on {used} threads, from a synthetic state at position "
+                      f"{pos0} (K/V rows N(0,1), DeltaNet windows and states N(0,0.1)), {dt:.1f} s",
+            "single_core": {"value": round(n1 / dt1, 4), "unit": "tok/s", "cores": 1,
+                            "sample": f"{n1} tokens at positions {pos0}.., {dt1:.1f} s"},
+            "layer_step_us": {"all_cores": layer_all, "one_core": layer_one,
+                              "workload": "one Gated DeltaNet layer (hidden 1024, FFN 3072, 16 heads x 128)"}}
 
 
 def run_ours(args, rank, world, local):
@@ -285,38 +474,20 @@ def run_ours(args, rank, world, local):
         dt2 = max_over_ranks(f0.elapsed_time(f1) / 1000.0, world)
         st2.close()
 
-    # dominant kernel: fused lm_head GEMV + argmax, timed alone on its stream
-    wl = torch.from_numpy(w.lm_head.data).cuda()
-    wp = torch.empty(qg.qg_q6k_planar_bytes(cfg.vocab, cfg.hidden), dtype=torch.uint8, device="cuda")
-    qg.qg_q6k_to_planar(wl, wp, cfg.vocab, cfg.hidden)
-    del wl
-    x = torch.from_numpy(synth.normal(7, cfg.hidden)).cuda()
-    ws = torch.zeros(2, dtype=torch.int64, device="cuda")
-    tk = torch.zeros(1, dtype=torch.int32, device="cuda")
-    s3 = torch.cuda.Stream()
-    with torch.cuda.stream(s3):
-        for _ in range(3):
-            qg.qg_lmhead_argmax(wp, x, cfg.vocab, cfg.hidden, ws, tk, s3)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 20
-        g0.record(s3)
-        for _ in range(reps):
-            qg.qg_lmhead_argmax(wp, x, cfg.vocab, cfg.hidden, ws, tk, s3)
-        g1.record(s3)
-    g1.synchronize()
-    t_lm = g0.elapsed_time(g1) / 1000.0 / reps
     peak, peak_kind = measured_peaks()
-    lm_gbs = lmhead_bytes(cfg) / t_lm / 1e9
-    qg.qg_device_status()
-
     tokps = world * K / dt
     mean_t = pos0 + (K + 1) / 2.0  # KV rows read, averaged over the timed steps
     bpt = algorithmic_bytes(cfg, mean_t, args.kv_format)
     step_gbs = bpt * K / dt / 1e9 * world
+    # every kernel kind of the step, timed with CUDA events (PDL-chained graphs
+    # of that kernel over the layers); the largest share is the roofline kernel
+    kernels = time_kernels(qg, m, cfg, kvf, args.kv_format, pos0 + K // 2, long_ctx, peak)
+    dom = max(kernels, key=lambda k: k["share"])
+    lm = next(k for k in kernels if k["kernel"] == "lmhead")
     out = {
         "metric": METRIC, "value": round(tokps, 3), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(1000.0 * dt / K, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic (seeded random-init weights and prompt)",
         "config": {"workload": f"{args.workload}: {desc}", "global_batch": world, "seq_len": cfg.max_seq_len,
                    "parallelism": f"replicas x{world}", "step_mode": args.step_mode,
                    "kv_cache": KV_DESC[args.kv_format], "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
@@ -325,10 +496,15 @@ def run_ours(args, rank, world, local):
         "bytes_per_token": int(bpt),
         "step_roofline": {"achieved": round(step_gbs / world, 1), "peak": peak, "unit": "GB/s",
                           "frac": round(step_gbs / world / peak, 4), "peak_kind": peak_kind},
-        "roofline": {"bound": "hbm", "kernel": "lm_head GEMV + argmax (Q6_K, vocab x hidden)",
-                     "achieved": round(lm_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(lm_gbs / peak, 4),
-                     "traffic": ncu_traffic("lmhead_argmax"), "bytes_per_launch": lmhead_bytes(cfg),
-                     "launch_us": round(t_lm * 1e6, 2), "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
+                     "frac": dom["frac"], "traffic": ncu_traffic(dom["kernel"]),
+                     "bytes_per_launch": dom["bytes_per_launch"], "launch_us": dom["us_per_launch"],
+                     "share_of_step": dom["share"], "peak_kind": peak_kind,
+                     "how": "CUDA events around a graph of PDL-chained launches of this kernel over the model's "
+                            "layers (qg_bench_kernel), on the launching stream"},
+        "roofline_lmhead": {"achieved": lm["GB/s"], "frac": lm["frac"], "launch_us": lm["us_per_launch"],
+                            "bytes_per_launch": lm["bytes_per_launch"], "traffic": ncu_traffic("lmhead")},
+        "kernels": kernels,
         "clocks": clocks,
         "e2e": ({"value": round(world * K / dt2, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
                  "d2h_bytes_per_step": 4} if dt2 else None),
@@ -336,40 +512,96 @@ def run_ours(args, rank, world, local):
         "kernels_per_token": int(nodes),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, kv=args.kv_format)
+        out["cpu_baseline"] = cpu_baseline(cfg, pos0, K, kv=args.kv_format)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
 def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: the workload's decode timed at the
+    positions the GPU arm times (pos0.. after the prompt, or 8000.. for the
+    long context), from a synthetic state at pos0, on all host cores; K steps
+    of a bounded sample after W warm-up tokens."""
     if rank != 0:
         return
-    import oracle
     cfg, desc = WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    w = synth.make_model_weights(cfg)
-    om = oracle.Model(w)
-    ost = oracle.State(om, KV_FORMATS[args.kv_format])
-    toks = synth.prompt_tokens(cfg)
-    for i in range(W):
-        oracle.forward_token(om, ost, int(toks[i]), i)
-    t0 = time.perf_counter()
-    for i in range(W, W + K):
-        oracle.forward_token(om, ost, int(toks[i % len(toks)]), i)
-    dt = time.perf_counter() - t0
-    v = round(K / dt, 4)
-    sample = (f"{K} tokens of the workload's prompt decoded at positions {W}..{W + K - 1} by the f32 C oracle "
-              f"(OpenMP over GEMV rows) after {W} warm-up tokens")
+    pos0 = synth.LONG_PREFILL + 1 if args.workload == "4b-long" else args.prompt
+    om, ost = oracle_at(cfg, pos0 - W, args.kv_format)
+    time_oracle(om, ost, pos0 - W, W, 1e9, 0)  # warm-up tokens at pos0 - W .. pos0 - 1
+    n, dt, used = time_oracle(om, ost, pos0, K, 1e9, 0)
+    v = round(n / dt, 4)
+    sample = (f"{n} tokens at positions {pos0}..{pos0 + n - 1} (the GPU arm's timed positions) by the f32 C oracle "
+              f"with OpenMP over GEMV rows on {used} threads, after {W} warm-up tokens, from a synthetic state "
+              f"(K/V rows N(0,1), DeltaNet windows and states N(0,0.1))")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": round(1000.0 * dt / K, 3), "higher_is_better": True, "scaling": "weak",
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": n,
+        "warmup": W, "ms_per_step": round(1000.0 * dt / n, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and prompt)",
         "config": {"workload": f"{args.workload}: {desc}", "global_batch": 1, "seq_len": cfg.max_seq_len,
-                   "kv_cache": KV_DESC[args.kv_format]},
-        "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
-                         "sample": sample},
+                   "kv_cache": KV_DESC[args.kv_format], "timed_positions": [pos0, pos0 + n - 1]},
+        "cpu_baseline": {"value": v, "unit": "tok/s", "cores": used, "kind": "oracle", "cpu": cpu_model(),
+                         "host_cores": os.cpu_count(), "sample": sample},
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def run_layer(args):
+    """One JSON line: the one-layer workload (one Gated DeltaNet layer,
+    hidden 1024, FFN 3072, 16 heads x 128, 8 steps from seeded state) through
+    qg_deltanet_step, microseconds per step (CUDA events around a graph of the
+    steps on one stream, each step on a fresh N(0,1) hidden), against the
+    oracle's layer step on all host cores and on one."""
+    import torch
+    import quantized_gemv_gated_gb300 as qg
+    cfg = synth.CFG_LAYER
+    w = synth.make_model_weights(cfg)
+    m = qg.Model(w)
+    st = qg.State(m, cfg.max_seq_len)
+    st.upload_layer(0, *synth.initial_deltanet_state(cfg, 0))
+    hs = torch.from_numpy(synth.layer_inputs(cfg, 8)).cuda()
+    hbuf = torch.empty(cfg.hidden, device="cuda")
+    stream = torch.cuda.Stream()
+    n_steps = 8
+    with torch.cuda.stream(stream):
+        for i in range(n_steps):
+            hbuf.copy_(hs[i])
+            qg.qg_deltanet_step(m, st, 0, hbuf, stream.cuda_stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_steps):
+            hbuf.copy_(hs[i])
+            qg.qg_deltanet_step(m, st, 0, hbuf, stream.cuda_stream)
+    reps = max(4, args.steps // 8)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    qg.qg_device_status()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_steps)
+    q4 = lambda n, k: n * k // 256 * 144  # noqa: E731
+    H, F = cfg.hidden, cfg.ffn
+    b = (kernel_bytes(cfg, "dn_in", 0) + kernel_bytes(cfg, "delta", 0) + kernel_bytes(cfg, "ssm_out", 0)
+         + kernel_bytes(cfg, "ffn_up", 0) + kernel_bytes(cfg, "ffn_down", 0))
+    peak, peak_kind = measured_peaks()
+    line = {"mode": "layer", "workload": "one Gated DeltaNet layer, hidden 1024, FFN 3072, 16 k-heads / 16 v-heads "
+                                         "x 128, conv 4, 8 steps from seeded state",
+            "us_per_step": round(us, 3), "bytes_per_step": int(b), "GB/s": round(b / us / 1e3, 1),
+            "frac": round(b / us / 1e3 / peak, 4), "peak_kind": peak_kind,
+            "how": "CUDA events around a graph of 8 qg_deltanet_step calls (5 layer kernels + the residual add each)"}
+    if not args.no_cpu_baseline:
+        a, n, used = time_oracle_layer(10.0, 0)
+        one, _, _ = time_oracle_layer(10.0, 1)
+        line["cpu_baseline"] = {"us_per_step": a, "cores": used, "one_core_us_per_step": one, "cpu": cpu_model(),
+                                "kind": "oracle", "sample": f"{n} layer steps"}
+    del q4, H, F
+    print(json.dumps(line), flush=True)
 
 
 def run_prefill(args):
@@ -582,7 +814,7 @@ def main():
     ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="0.8b")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="4b")
     ap.add_argument("--prompt", type=int, default=synth.PROMPT_LEN,
                     help="prompt tokens fed before the timed decode (default 850)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -597,11 +829,14 @@ def main():
                     help="time qg_prefill of the workload's prompt against token-by-token decode (one JSON line)")
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the decode step: one JSON line per GEMV building block at the model's shapes")
+    ap.add_argument("--layer", action="store_true",
+                    help="the one-layer workload through qg_deltanet_step: us per step (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
-        args.steps = min(args.steps, 16)  # bounded sample of the CPU oracle
+    if args.layer:
+        run_layer(args)
+        return
     if args.kernels:
         run_kernels(args)
         return

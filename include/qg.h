@@ -161,7 +161,9 @@ enum { QG_KV_F32 = 0, QG_KV_Q8_0_Q5_1 = 1 };
 int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_state** out);
 int qg_state_kv_format(const qg_state* s, int* kv_format);
 int qg_state_destroy(qg_state* s);
-/* Zero every window, state and cache; kv_len = 0. */
+/* Zero every window, state and cache; kv_len = 0; clear the token mask: the
+ * state a fresh forward_qwen35_cuda.rs new_state gives, without reallocating
+ * (the captured graph and scratch are kept). */
 int qg_state_reset(qg_state* s);
 
 /* Teacher forcing (forward_qwen35_cuda.rs upload_layer, upload_attention_kv,
@@ -339,17 +341,21 @@ int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, v
  * must not allocate (device memory reserved up front by a pool; a loop on a
  * latency budget, where an allocation call can synchronise the device).  The
  * first call on each device (the device current at the call) resolves the
- * scratch address and zeroes it, synchronously: make that first call before
- * any stream capture.  Every call leaves the scratch zeroed.  There is one
- * scratch per device, so calls on one device must not overlap on the GPU
- * (two streams at once race on it).  The pages have no counterpart of this
- * entry point.  Errors: those of qg_lmhead_argmax, QG_ERR_CUDA when the
- * scratch cannot be resolved, QG_ERR_SHAPE if the kernel's workspace ever
- * outgrew the static area. */
+ * scratch address (cudaGetSymbolAddress, which may load the library's device
+ * code): make that first call before any stream capture.  The scratch is zero
+ * when the library loads and every call leaves it zeroed, so no call clears it
+ * first.  There is one scratch per device, so calls on one device must not
+ * overlap on the GPU (two streams at once race on it).  The pages have no
+ * counterpart of this entry point.  Errors: those of qg_lmhead_argmax,
+ * QG_ERR_CUDA when the scratch cannot be resolved, QG_ERR_SHAPE if the
+ * kernel's workspace ever outgrew the static area. */
 int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, int k, uint32_t* tok_dev,
                              qg_stream stream);
 
-/* First index of the maximum of x[n] (NaN never wins) -> *idx_dev. */
+/* First index of the maximum of x[n] (NaN never wins; all NaN gives 0) ->
+ * *idx_dev: the device argmax of aprender PR #4332 ("Greedy GPU argmax",
+ * first index on ties) over logits the caller already holds.  x and idx_dev
+ * 4-byte aligned device pointers.  Errors: QG_ERR_ARG, QG_ERR_EMPTY. */
 int qg_argmax_f32(const float* x, int n, uint32_t* idx_dev, qg_stream stream);
 
 /* One Gated DeltaNet layer (forward_qwen35_cuda.rs forward_deltanet_layer)
@@ -386,9 +392,40 @@ int qg_decode_token_eager(qg_model* m, qg_state* s, uint32_t token, int pos, uin
  * receives the ids at the end.  Errors as qg_decode_token. */
 int qg_decode_greedy(qg_model* m, qg_state* s, int pos0, int n_steps, uint32_t* tokens_host);
 
+/* ----------------------------------------------------------- measurement */
+
+/* The kernels of the decode step, one launch each per layer of their kind
+ * (the lm_head once per token). */
+enum {
+    QG_KERNEL_DN_IN = 0,     /* DeltaNet: RMSNorm + fused qkv/alpha/beta/gate GEMV + conv/gates */
+    QG_KERNEL_DELTA = 1,     /* DeltaNet: per-head L2 norm + gated delta rule */
+    QG_KERNEL_SSM_OUT = 2,   /* DeltaNet: gated RMSNorm + ssm_out GEMV */
+    QG_KERNEL_ATTN_IN = 3,   /* attention: RMSNorm + fused q|gate/k/v GEMV + V append */
+    QG_KERNEL_ATTN = 4,      /* attention: q/k norm, rope, K append, split-K GQA attention, gate */
+    QG_KERNEL_ATTN_OUT = 5,  /* attention: attn_output GEMV */
+    QG_KERNEL_FFN_UP = 6,    /* every layer: RMSNorm + ffn_gate/ffn_up dual GEMV + SwiGLU */
+    QG_KERNEL_FFN_DOWN = 7,  /* every layer: ffn_down (Q6_K) GEMV */
+    QG_KERNEL_LMHEAD = 8     /* output RMSNorm + lm_head GEMV + first-index argmax */
+};
+
+/* Measurement hook (the pages have no counterpart): enqueue `launches`
+ * launches of one kernel kind of the decode step on `stream`, chained by
+ * programmatic dependent launch as inside the step, walking the layers that
+ * have that kernel in index order, so that consecutive launches stream
+ * different layers' weights from HBM as the step does.  Each launch runs with
+ * exactly the arguments it has inside the step; the state's buffers are its
+ * inputs and outputs, so the state's contents (windows, recurrent states, the
+ * cache rows at its position, scratch) are meaningless afterwards: reset or
+ * re-prefill it before decoding again.  Allocates nothing and can be captured
+ * in a CUDA graph, which is how a caller times one kernel with events on
+ * `stream`.  Errors: QG_ERR_ARG (NULL, launches < 1, or a kind the model does
+ * not have), QG_ERR_CUDA. */
+int qg_bench_kernel(const qg_model* m, qg_state* s, int kind, int launches, qg_stream stream);
+
 /* Error word of the building blocks on the current device: QG_OK, or
  * QG_ERR_TIMEOUT when a building-block kernel gave up on a bounded wait since
- * the last check (the word is cleared).  Synchronous. */
+ * the last check (the word is cleared).  Synchronous.  The pages have no
+ * counterpart: their kernels do not wait on device flags. */
 int qg_device_status(void);
 
 /* Message of the last failed call on this thread ("" if none). */

@@ -12,11 +12,12 @@ tests/golden/stream_<workload>.json.
               drawn below 5e-5 instead of 0.02: the residual stream stays
               near unit scale, so the argmax follows the token (at 0.02 one
               token wins every step by a margin of ~50 logits).
+  4b-varied : the same for the 4b workload.
   4b-long   : every attention layer's K/V rows 0..7999 ~ N(0,1), DeltaNet
               windows and states ~ N(0,0.1), a seeded first token at
               position 8000, then 63 greedy tokens (64 steps in all).
 
-  python oracle/make_golden.py 0.8b [0.8b-varied 4b 4b-long] [--threads N]
+  python oracle/make_golden.py 0.8b [0.8b-varied 4b 4b-varied 4b-long] [--threads N]
 """
 import argparse
 import base64
@@ -34,8 +35,9 @@ import oracle  # noqa: E402
 import synth  # noqa: E402
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
-CFGS = {"0.8b": synth.CFG_0P8B, "0.8b-varied": synth.CFG_0P8B, "4b": synth.CFG_4B, "4b-long": synth.CFG_4B_LONG}
-DMAX = {"0.8b-varied": 5e-5}  # quantized-scale bound per workload (default 0.02)
+CFGS = {"0.8b": synth.CFG_0P8B, "0.8b-varied": synth.CFG_0P8B, "4b": synth.CFG_4B, "4b-varied": synth.CFG_4B,
+        "4b-long": synth.CFG_4B_LONG}
+DMAX = {"0.8b-varied": 5e-5, "4b-varied": 5e-5}  # quantized-scale bound per workload (default 0.02)
 
 
 def b64(a):

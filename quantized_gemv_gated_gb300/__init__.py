@@ -35,11 +35,16 @@ EXPORTS = [
     "qg_deltanet_step", "qg_attn_decode_step", "qg_decode_token", "qg_decode_token_eager",
     "qg_decode_greedy", "qg_device_status", "qg_last_error",
     "qg_state_create_kv", "qg_state_kv_format", "qg_state_download_kv_records", "qg_prefill",
-    "qg_decode_batch", "qg_batch_create", "qg_batch_step", "qg_batch_destroy",
+    "qg_decode_batch", "qg_batch_create", "qg_batch_step", "qg_batch_destroy", "qg_bench_kernel",
 ]
 
 
 STEP_KERNELS, STEP_PERSISTENT = 0, 1  # qg_state_set_step_mode
+# kernel kinds of the decode step (qg_bench_kernel)
+KERNEL_DN_IN, KERNEL_DELTA, KERNEL_SSM_OUT, KERNEL_ATTN_IN, KERNEL_ATTN, KERNEL_ATTN_OUT = 0, 1, 2, 3, 4, 5
+KERNEL_FFN_UP, KERNEL_FFN_DOWN, KERNEL_LMHEAD = 6, 7, 8
+KERNEL_NAMES = {0: "dn_in", 1: "delta", 2: "ssm_out", 3: "attn_in", 4: "attn", 5: "attn_out", 6: "ffn_up",
+                7: "ffn_down", 8: "lmhead"}
 KV_F32, KV_Q8_0_Q5_1 = 0, 1  # qg_state_create_kv
 K_RECORD_BYTES, V_RECORD_BYTES = 272, 192  # per (kv head, position) of a quantized cache
 
@@ -134,6 +139,7 @@ def lib():
             "qg_argmax_f32": [p, i, p, p],
             "qg_deltanet_step": [p, p, i, p, p],
             "qg_attn_decode_step": [p, p, i, p, i, p],
+            "qg_bench_kernel": [p, p, i, i, p],
             "qg_decode_token": [p, p, ctypes.c_uint32, i, ctypes.POINTER(ctypes.c_uint32)],
             "qg_decode_token_eager": [p, p, ctypes.c_uint32, i, ctypes.POINTER(ctypes.c_uint32)],
             "qg_decode_greedy": [p, p, i, i, p],
@@ -410,6 +416,12 @@ def qg_deltanet_step(model, state, il, hidden, stream=None):
 
 def qg_attn_decode_step(model, state, il, hidden, pos, stream=None):
     return _check(lib().qg_attn_decode_step(model.handle, state.handle, il, _dev(hidden), pos, _stream(stream)))
+
+
+def qg_bench_kernel(model, state, kind, launches, stream=None):
+    """`launches` PDL-chained launches of one kernel kind of the decode step
+    (KERNEL_*), over the layers that have it; leaves the state meaningless."""
+    return _check(lib().qg_bench_kernel(model.handle, state.handle, int(kind), int(launches), _stream(stream)))
 
 
 def qg_decode_token(model, state, token, pos):

@@ -2,7 +2,9 @@
 // fused lm_head GEMV + argmax and a plain argmax; plus the error plumbing
 // shared by the whole library.
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "qg_host.cuh"
 
@@ -34,23 +36,43 @@ int device_sms() {
     return v;
 }
 
+int grant_smem(const void* kern, int smem) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> granted;  // (kernel, device) -> bytes
+    int dev = 0;
+    QG_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lock(mu);
+    int& have = granted[std::make_pair(kern, dev)];
+    if (smem > have) {
+        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     static_cast<int>(cudaSharedmemCarveoutMaxShared)));
+        have = smem;
+    }
+    return QG_OK;
+}
+
 // Error word of the building blocks (one per device that loads the library).
 __device__ unsigned g_block_err;
 
 static unsigned* block_err_ptr() {
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static std::mutex mu;
     static unsigned* cache[64] = {nullptr};
-    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
-    unsigned* p = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_block_err) != cudaSuccess) return nullptr;
-    if (dev >= 0 && dev < 64) cache[dev] = p;
-    return p;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        unsigned* p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_block_err) != cudaSuccess) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
 }
 
 // Static scratch of qg_lmhead_argmax_noalloc: the fused argmax's workspace
-// (best key, arrival count), 16 of its 256 bytes in use.  Every call leaves it
-// zeroed again; it is zeroed once per device before the first call.
+// (best key, arrival count), 16 of its 256 bytes in use.  A __device__ array
+// without an initializer is zero when the module loads, and every call leaves
+// it zeroed again (the last CTA clears it), so no call needs to clear it first.
 static __device__ __align__(256) unsigned long long g_lmhead_scratch[32];
 
 static int lmhead_scratch(unsigned long long** out) {
@@ -63,8 +85,6 @@ static int lmhead_scratch(unsigned long long** out) {
     if (!cache[dev]) {
         unsigned long long* p = nullptr;
         QG_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_lmhead_scratch));
-        QG_CUDA(cudaMemset(p, 0, sizeof(g_lmhead_scratch)));
-        QG_CUDA(cudaDeviceSynchronize());
         cache[dev] = p;
     }
     *out = cache[dev];
@@ -196,12 +216,15 @@ using namespace qg;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// y (an f32 vector, or the 4-byte token slot of the fused argmax) is written
+// with 4-byte stores: a misaligned pointer is refused here, before any launch.
 static int check_gemv_args(const void* w, const float* x, const void* y, int n, int k) {
     if (!w || !x || !y) return set_err(QG_ERR_ARG, "gemv: NULL pointer");
     if (n < 0 || k < 0) return set_err(QG_ERR_ARG, "gemv: negative size n=%d k=%d", n, k);
     if (n == 0 || k == 0) return set_err(QG_ERR_EMPTY, "gemv: empty tensor n=%d k=%d", n, k);
     if (!gemv_k_served(k)) return set_err(QG_ERR_SHAPE, "gemv: k=%d is not a multiple of 256 up to 16384", k);
     if (!aligned16(w) || !aligned16(x)) return set_err(QG_ERR_ARG, "gemv: w and x must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(y) & 3u) return set_err(QG_ERR_ARG, "gemv: y / tok_dev must be 4-byte aligned");
     return QG_OK;
 }
 
@@ -283,7 +306,8 @@ int qg_lmhead_argmax(const void* w_planar, const float* x, int n_vocab, int k, v
 // loop on a latency budget, where an allocation call can synchronise the
 // device.  Nothing here calls cudaMalloc / cudaFree or an allocating library
 // routine; the first call on a device resolves the scratch address with
-// cudaGetSymbolAddress and zeroes it, later calls only launch.
+// cudaGetSymbolAddress (nothing is copied or synchronised), later calls only
+// launch.
 int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, int k, uint32_t* tok_dev,
                              qg_stream stream) {
     int rc = check_gemv_args(w_planar, x, tok_dev, n_vocab, k);
@@ -303,6 +327,8 @@ int qg_lmhead_argmax_noalloc(const void* w_planar, const float* x, int n_vocab, 
 
 int qg_argmax_f32(const float* x, int n, uint32_t* idx_dev, qg_stream stream) {
     if (!x || !idx_dev) return set_err(QG_ERR_ARG, "argmax_f32: NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(idx_dev)) & 3u)
+        return set_err(QG_ERR_ARG, "argmax_f32: x and idx_dev must be 4-byte aligned");
     if (n <= 0) return set_err(QG_ERR_EMPTY, "argmax_f32: n=%d", n);
     argmax_f32_kernel<<<1, 1024, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, n, idx_dev);
     QG_CUDA(cudaGetLastError());

@@ -495,16 +495,39 @@ static int out_gemv(qg_state* s, const uint8_t* w, int n, int k, const Pro& pro,
     return launch_gemv<QT, false>(w, nullptr, n, k, pro, ey, st, true, s->err, next);
 }
 
-static int ffn(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st) {
+// The pending output of a projection back to the hidden size (ssm_out,
+// attn_output, ffn_down) of k inputs, as out_gemv leaves it for the next
+// reader: split-K slice sums, or one vector.
+static void pending_y(qg_state* s, int n, int k) {
+    if (gemv_slices(k) > 1) {
+        s->ycur = s->kpart;
+        s->ycur_parts = gemv_slices(k);
+        s->ycur_stride = (n + 7) & ~7;
+    } else {
+        s->ycur = s->y;
+        s->ycur_parts = 1;
+        s->ycur_stride = 0;
+    }
+}
+
+// ----------------------------------------------- the kernels of one layer
+// FFN gate/up: RMSNorm prologue of io.b + the pending y (the mixer's output),
+// storing the stream to io.a; dual GEMV with the SwiGLU epilogue.
+static int launch_ffn_up(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
     EpiSwiGlu sw{};
     sw.act = s->act;
-    int rc = launch_gemv<QT_Q4K, true>(L.w_gate, L.w_up, c.ffn, c.hidden,
-                                       norm_pro(io.b, s, true, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
-                                       s->err, prefetch_of(L.w_down, q6_bytes(c.hidden, c.ffn)));
-    if (rc) return rc;
-    return out_gemv<QT_Q6K>(s, L.w_down, c.hidden, c.ffn, ProPlainG{s->act}, st, next_layer_prefetch(m, s, il));
+    return launch_gemv<QT_Q4K, true>(L.w_gate, L.w_up, c.ffn, c.hidden,
+                                     norm_pro(io.b, s, true, L.post_norm, nullptr, io.a, c.eps, c.hidden), sw, st, true,
+                                     s->err, prefetch_of(L.w_down, q6_bytes(c.hidden, c.ffn)));
+}
+
+// FFN down (Q6_K, split-K over the hidden rows): y pending for the next layer.
+static int launch_ffn_down(const qg_model* m, qg_state* s, int il, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    return out_gemv<QT_Q6K>(s, m->layers[il].w_down, c.hidden, c.ffn, ProPlainG{s->act}, st,
+                            next_layer_prefetch(m, s, il));
 }
 
 static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev& L, const ResidualIO& io) {
@@ -512,7 +535,9 @@ static ProRmsNorm input_norm(const qg_model* m, qg_state* s, const qg_layer_dev&
     return norm_pro(io.a, s, io.y_pending, L.attn_norm, nullptr, io.b, m->cfg.eps, m->cfg.hidden);
 }
 
-int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first) {
+// DeltaNet input: RMSNorm prologue + the fused [qkv | alpha | beta | gate]
+// GEMV with the conv / gates / z epilogue.
+static int launch_dn_in(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
     EpiDnIn ei{};
@@ -527,26 +552,32 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
     ei.dt = s->dt;
     ei.beta = s->beta;
     ei.z = s->z;
-    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ei, st, pdl_first,
-                                        s->err,
-                                        prefetch_of(s->ssm[il], sizeof(float) * c.n_v_heads * c.head_v_dim * kDk));
-    if (rc) return rc;
-    {
-        DeltaArgs da{};
-        da.conv_out = s->conv_out;
-        da.dt = s->dt;
-        da.beta = s->beta;
-        da.S = s->ssm[il];
-        da.o = s->o;
-        da.err = s->err;
-        da.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->v_dim));
-        da.nk = c.n_k_heads;
-        da.dv = c.head_v_dim;
-        da.kdim = m->k_dim;
-        da.eps = c.eps;
-        rc = launch_pdl(delta_kernel, dim3(c.n_v_heads * (c.head_v_dim / kDeltaRows)), dim3(256), 0, st, true, da);
-        if (rc) return rc;
-    }
+    return launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ei, st, pdl, s->err,
+                                      prefetch_of(s->ssm[il], sizeof(float) * c.n_v_heads * c.head_v_dim * kDk));
+}
+
+static int launch_delta(const qg_model* m, qg_state* s, int il, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const qg_layer_dev& L = m->layers[il];
+    DeltaArgs da{};
+    da.conv_out = s->conv_out;
+    da.dt = s->dt;
+    da.beta = s->beta;
+    da.S = s->ssm[il];
+    da.o = s->o;
+    da.err = s->err;
+    da.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->v_dim));
+    da.nk = c.n_k_heads;
+    da.dv = c.head_v_dim;
+    da.kdim = m->k_dim;
+    da.eps = c.eps;
+    return launch_pdl(delta_kernel, dim3(c.n_v_heads * (c.head_v_dim / kDeltaRows)), dim3(256), 0, st, true, da);
+}
+
+// ssm_out: gated-RMSNorm prologue (per value head, on o and z) + GEMV.
+static int launch_ssm_out(const qg_model* m, qg_state* s, int il, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const qg_layer_dev& L = m->layers[il];
     ProGatedNorm gn{};
     gn.o = s->o;
     gn.z = s->z;
@@ -554,10 +585,16 @@ int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO&
     gn.nv = c.n_v_heads;
     gn.dv = c.head_v_dim;
     gn.eps = c.eps;
-    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->v_dim, gn, st,
-                          prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
-    if (rc) return rc;
-    return ffn(m, s, il, io, st);
+    return out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->v_dim, gn, st,
+                            prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
+}
+
+int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first) {
+    int rc;
+    if ((rc = launch_dn_in(m, s, il, io, st, pdl_first)) || (rc = launch_delta(m, s, il, st)) ||
+        (rc = launch_ssm_out(m, s, il, st)) || (rc = launch_ffn_up(m, s, il, io, st)))
+        return rc;
+    return launch_ffn_down(m, s, il, st);
 }
 
 // Grid (rows, n_kv): one CTA per (position, kv head), warp w makes block w
@@ -605,11 +642,7 @@ size_t kv_cache_bytes(const qg_state* s, int which) {
 template <int GS, bool KVQ>
 static int launch_attn_as(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
     const int smem = attn_smem_floats<GS, KVQ>() * 4;
-    static int configured = 0;
-    if (smem > configured) {
-        QG_CUDA(cudaFuncSetAttribute(attn_kernel<GS, KVQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        configured = smem;
-    }
+    if (int rc = grant_smem(reinterpret_cast<const void*>(attn_kernel<GS, KVQ>), smem)) return rc;
     return launch_pdl(attn_kernel<GS, KVQ>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
 }
 
@@ -619,8 +652,9 @@ static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaSt
                                            : launch_attn_as<GS, false>(m, s, a, st);
 }
 
-int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
-                        bool pdl_first) {
+// Attention input: RMSNorm prologue + the fused [q|gate | k | v] GEMV; v rows
+// land in the V cache row at the step's position.
+static int launch_attn_in(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl) {
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
     EpiAttnIn ea{};
@@ -631,9 +665,12 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
     ea.slots = s->slots;
     ea.qd2 = 2 * m->q_dim;
     ea.kvd = m->kv_dim;
-    int rc = launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ea, st, pdl_first,
-                                        s->err);
-    if (rc) return rc;
+    return launch_gemv<QT_Q4K, false>(L.w_in, nullptr, L.n_in, c.hidden, input_norm(m, s, L, io), ea, st, pdl, s->err);
+}
+
+static int launch_attention(const qg_model* m, qg_state* s, int il, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const qg_layer_dev& L = m->layers[il];
     AttnArgs a{};
     a.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->q_dim));
     a.qf = s->qf;
@@ -657,17 +694,75 @@ int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO
     a.theta_scale = m->theta_scale;
     a.eps = c.eps;
     switch (c.n_heads / c.n_kv_heads) {
-        case 1: rc = launch_attn<1>(m, s, a, st); break;
-        case 2: rc = launch_attn<2>(m, s, a, st); break;
-        case 4: rc = launch_attn<4>(m, s, a, st); break;
-        case 8: rc = launch_attn<8>(m, s, a, st); break;
+        case 1: return launch_attn<1>(m, s, a, st);
+        case 2: return launch_attn<2>(m, s, a, st);
+        case 4: return launch_attn<4>(m, s, a, st);
+        case 8: return launch_attn<8>(m, s, a, st);
         default: return set_err(QG_ERR_SHAPE, "attention: %d query heads per kv head", c.n_heads / c.n_kv_heads);
     }
-    if (rc) return rc;
-    rc = out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, ProPlainG{s->attn}, st,
-                          prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
-    if (rc) return rc;
-    return ffn(m, s, il, io, st);
+}
+
+static int launch_attn_out(const qg_model* m, qg_state* s, int il, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    const qg_layer_dev& L = m->layers[il];
+    return out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, ProPlainG{s->attn}, st,
+                            prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
+}
+
+int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
+                        bool pdl_first) {
+    int rc;
+    if ((rc = launch_attn_in(m, s, il, io, st, pdl_first)) || (rc = launch_attention(m, s, il, st)) ||
+        (rc = launch_attn_out(m, s, il, st)) || (rc = launch_ffn_up(m, s, il, io, st)))
+        return rc;
+    return launch_ffn_down(m, s, il, st);
+}
+
+// Measurement: `launches` launches of one kernel kind, PDL-chained on st,
+// walking the layers that have it (for kernels that read the previous
+// kernel's pending output, the bookkeeping of that predecessor is set first,
+// so every launch runs exactly the configuration it has inside the step).
+int run_kernel_kind(const qg_model* m, qg_state* s, int kind, int launches, cudaStream_t st) {
+    const qg_config& c = m->cfg;
+    std::vector<int> layers;
+    for (int il = 0; il < c.n_layers; ++il) {
+        const bool dn = m->kinds[il] == QG_LAYER_DELTANET;
+        const bool has = kind == QG_KERNEL_FFN_UP || kind == QG_KERNEL_FFN_DOWN ||
+                         ((kind == QG_KERNEL_DN_IN || kind == QG_KERNEL_DELTA || kind == QG_KERNEL_SSM_OUT) && dn) ||
+                         ((kind == QG_KERNEL_ATTN_IN || kind == QG_KERNEL_ATTN || kind == QG_KERNEL_ATTN_OUT) && !dn);
+        if (has) layers.push_back(il);
+    }
+    if (kind == QG_KERNEL_LMHEAD) layers.push_back(c.n_layers - 1);
+    if (layers.empty() || kind < 0 || kind > QG_KERNEL_LMHEAD)
+        return set_err(QG_ERR_ARG, "bench_kernel: kernel kind %d does not occur in this model", kind);
+    const ResidualIO io{s->hres, s->h, true, false};
+    for (int i = 0; i < launches; ++i) {
+        const int il = layers[static_cast<size_t>(i) % layers.size()];
+        const bool dn = m->kinds[il] == QG_LAYER_DELTANET;
+        int rc = QG_OK;
+        switch (kind) {
+            case QG_KERNEL_DN_IN:
+            case QG_KERNEL_ATTN_IN:
+                pending_y(s, c.hidden, c.ffn);  // after the previous layer's ffn_down
+                rc = dn ? launch_dn_in(m, s, il, io, st, true) : launch_attn_in(m, s, il, io, st, true);
+                break;
+            case QG_KERNEL_DELTA: rc = launch_delta(m, s, il, st); break;
+            case QG_KERNEL_SSM_OUT: rc = launch_ssm_out(m, s, il, st); break;
+            case QG_KERNEL_ATTN: rc = launch_attention(m, s, il, st); break;
+            case QG_KERNEL_ATTN_OUT: rc = launch_attn_out(m, s, il, st); break;
+            case QG_KERNEL_FFN_UP:
+                pending_y(s, c.hidden, dn ? m->v_dim : m->q_dim);  // after the mixer's output projection
+                rc = launch_ffn_up(m, s, il, io, st);
+                break;
+            case QG_KERNEL_FFN_DOWN: rc = launch_ffn_down(m, s, il, st); break;
+            default:
+                pending_y(s, c.hidden, c.ffn);
+                rc = run_lmhead(m, s, s->hres, s->h, st, false);
+                break;
+        }
+        if (rc) return rc;
+    }
+    return QG_OK;
 }
 
 int run_residual(qg_state* s, float* h, int n, cudaStream_t st) {

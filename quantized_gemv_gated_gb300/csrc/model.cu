@@ -703,6 +703,14 @@ int qg_attn_decode_step(const qg_model* m, qg_state* s, int il, float* hidden_de
     return QG_OK;
 }
 
+int qg_bench_kernel(const qg_model* m, qg_state* s, int kind, int launches, qg_stream stream) {
+    if (!m || !s) return set_err(QG_ERR_ARG, "bench_kernel: NULL argument");
+    if (s->m != m) return set_err(QG_ERR_ARG, "bench_kernel: the state belongs to another model");
+    if (launches < 1) return set_err(QG_ERR_ARG, "bench_kernel: %d launches", launches);
+    DeviceGuard dg(m->device);
+    return run_kernel_kind(m, s, kind, launches, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int qg_decode_token(qg_model* m, qg_state* s, uint32_t token, int pos, uint32_t* next_token) {
     int rc = check_step(m, s, token, pos, next_token);
     if (rc) return rc;

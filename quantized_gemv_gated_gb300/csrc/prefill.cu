@@ -796,11 +796,7 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     const int z = (nq + per - 1) / per;
     if (used_splits) *used_splits = z;
     const int smem = kGK * (kGR + 2 * kGT) * static_cast<int>(sizeof(float));
-    static bool configured = false;
-    if (!configured) {
-        QG_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT, ROW_MAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        configured = true;
-    }
+    if (int rc = grant_smem(reinterpret_cast<const void*>(pf_gemm_kernel<QT, ROW_MAJOR>), smem)) return rc;
     const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
     const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
     pf_gemm_kernel<QT, ROW_MAJOR><<<grid, 256, smem, st>>>(W, n, k, X, kPfChunk, Y, ldy, split_stride, P, per);

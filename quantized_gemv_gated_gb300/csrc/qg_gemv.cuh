@@ -240,10 +240,14 @@ __device__ __forceinline__ unsigned u4w(const uint4& v, int w) { return w == 0 ?
 
 // x digits of one Q4_K chunk (x[64c, 64c + 64)): planes of the low-nibble
 // sub-block (x[64c + 16h ..]) and of the high-nibble one (x[64c + 32 + 16h ..]).
+// The dot takes the high nibbles in place (16 x their value: one mask instead
+// of a shift and a mask), so every integer sum it forms is 16 x the plain one;
+// the sums of n and the unit are kept pre-scaled to match (x16, /16: powers of
+// two, so the row value is bit for bit the one of the plain form).
 struct DigQ4 {
     uint4 lo[2][3], hi[2][3];
-    float ns0, ns1;  // sums of n over the two sub-blocks
-    float unit;      // 2^(e-22) of the super-block
+    float ns0, ns1;  // 16 x the sums of n over the two sub-blocks
+    float unit;      // 2^(e-22) / 16 of the super-block
 };
 __device__ __forceinline__ void load_dig_q4(DigQ4& D, int c, const uint8_t* dig, const uint8_t* aux, int k) {
     const int xo = 64 * c;
@@ -258,9 +262,9 @@ __device__ __forceinline__ void load_dig_q4(DigQ4& D, int c, const uint8_t* dig,
         }
     }
     const float2 ns = *reinterpret_cast<const float2*>(aux + aux_tail(k) + 4 * (xo >> 5));
-    D.ns0 = ns.x;
-    D.ns1 = ns.y;
-    D.unit = reinterpret_cast<const float*>(aux)[xo >> 8];
+    D.ns0 = 16.0f * ns.x;
+    D.ns1 = 16.0f * ns.y;
+    D.unit = 0.0625f * reinterpret_cast<const float*>(aux)[xo >> 8];
 }
 
 // One row's Q4_K chunk g of the 144-byte block at blk against the lane's digits.
@@ -276,7 +280,7 @@ __device__ __forceinline__ float dot_q4k(const uint8_t* blk, int g, const DigQ4&
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const unsigned qw = u4w(q, w);
-            const unsigned lo = qw & 0x0f0f0f0fu, hi = (qw >> 4) & 0x0f0f0f0fu;
+            const unsigned lo = qw & 0x0f0f0f0fu, hi = qw & 0xf0f0f0f0u;  // hi: 16 x the high nibbles
             a0 = dp4a_uu(lo, u4w(D.lo[h][0], w), a0);
             a1 = dp4a_uu(lo, u4w(D.lo[h][1], w), a1);
             a2 = dp4a_us(lo, u4w(D.lo[h][2], w), a2);
@@ -301,10 +305,13 @@ __device__ __forceinline__ float dot_q4k(const uint8_t* blk, int g, const DigQ4&
         sc[t] = static_cast<int>(((asc >> sh) & msk) | ((hdr.y >> (sh + 2u)) & mhi));
         mn[t] = static_cast<int>(((amn >> (sh + sm4)) & msk) | ((hdr.z >> (sh + 2u)) & mhi));
     }
-    // |sc * sum| < 63 * 15 * 255 * 32 per sub-block: the weighted sums fit in int32
-    const int I0 = sc[0] * static_cast<int>(a0) + sc[1] * static_cast<int>(b0);
-    const int I1 = sc[0] * static_cast<int>(a1) + sc[1] * static_cast<int>(b1);
-    const int I2 = sc[0] * a2 + sc[1] * b2;
+    // the low sub-block's scale x16 matches the in-place high nibbles: I = 16 x
+    // the plain weighted sum, |I| < 2 * 16 * 63 * 15 * 255 * 32 < 2^31, and each
+    // I is 16 x an integer below 2^24 in magnitude, so it converts to f32 exactly
+    const int s0 = sc[0] << 4;
+    const int I0 = s0 * static_cast<int>(a0) + sc[1] * static_cast<int>(b0);
+    const int I1 = s0 * static_cast<int>(a1) + sc[1] * static_cast<int>(b1);
+    const int I2 = s0 * a2 + sc[1] * b2;
     const float F = fmaf(static_cast<float>(I2), 65536.0f, fmaf(static_cast<float>(I1), 256.0f, static_cast<float>(I0)));
     const float M = fmaf(static_cast<float>(mn[0]), D.ns0, static_cast<float>(mn[1]) * D.ns1);
     return D.unit * fmaf(d, F, -(dmin * M));

@@ -14,6 +14,11 @@ namespace qg {
 int set_err(int code, const char* fmt, ...);
 int cuda_err(cudaError_t e, const char* what);
 int device_sms();
+// Raise `kern`'s dynamic shared-memory limit to at least `smem` bytes (and
+// prefer the largest carveout) on the current device, once per (kernel,
+// device) and size: the attribute is per device, so a kernel configured on
+// one device is configured again on the next.  Thread-safe.
+int grant_smem(const void* kern, int smem);
 
 #define QG_CUDA(call)                                              \
     do {                                                           \
@@ -96,13 +101,7 @@ int launch_gemv(const void* w0, const void* w1, int n, int k, const Pro& pro, co
     if (smem > 227 * 1024)
         return set_err(QG_ERR_SHAPE, "gemv: %d x %d needs %d bytes of shared memory per CTA", n, k, smem);
     auto kern = gemv_kernel<QT, LAYOUT, DUAL, Pro, Epi>;
-    static int configured = 0;  // per instantiation: largest dynamic smem granted so far
-    if (smem > configured) {
-        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     static_cast<int>(cudaSharedmemCarveoutMaxShared)));
-        configured = smem;
-    }
+    if (int rc = grant_smem(reinterpret_cast<const void*>(kern), smem)) return rc;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -144,13 +143,7 @@ int launch_gemv_split(const void* w0, int n, int k, const Pro& pro, cudaStream_t
     sh.next = next;
     const int smem = fixed + sh.stages * sh.pp * stage_bytes_of(QT);
     auto kern = gemv_split_kernel<QT, Pro>;
-    static int configured = 0;
-    if (smem > configured) {
-        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-        QG_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     static_cast<int>(cudaSharedmemCarveoutMaxShared)));
-        configured = smem;
-    }
+    if (int rc = grant_smem(reinterpret_cast<const void*>(kern), smem)) return rc;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

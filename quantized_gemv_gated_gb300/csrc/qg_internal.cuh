@@ -110,6 +110,10 @@ struct ResidualIO {
 int run_deltanet_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st, bool pdl_first);
 int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,
                         bool pdl_first);
+// `launches` PDL-chained launches of one kernel kind of the step (QG_KERNEL_*),
+// round robin over the layers that have it (measurement; the state's contents
+// become meaningless).
+int run_kernel_kind(const qg_model* m, qg_state* s, int kind, int launches, cudaStream_t st);
 // h += the pending y (closes a layer run on its own).
 int run_residual(qg_state* s, float* h, int n, cudaStream_t st);
 // Output norm of a + y (stored to h_final) + fused lm_head GEMV + argmax ->

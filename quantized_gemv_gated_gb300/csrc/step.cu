@@ -556,13 +556,7 @@ int step_setup(const qg_model* m, qg_state* s) {
         P.nslots = std::min(kStepMaxSlots, (per_cta - P.ring_off) / kSlotBytes);
         if (P.nslots < 2) return set_err(QG_ERR_SHAPE, "step kernel: %d bytes of phase scratch leave no ring", sc);
         s->step_smem = P.ring_off + P.nslots * kSlotBytes;
-        static bool configured = false;
-        if (!configured) {
-            QG_CUDA(cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStepSmemPerCta));
-            QG_CUDA(cudaFuncSetAttribute(step_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         static_cast<int>(cudaSharedmemCarveoutMaxShared)));
-            configured = true;
-        }
+        if ((rc = grant_smem(reinterpret_cast<const void*>(step_kernel), kStepSmemPerCta))) return rc;
         int per_sm = 0;
         QG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_kernel, kThreads, s->step_smem));
         if (per_sm < 1) return set_err(QG_ERR_SHAPE, "step kernel: no CTA fits an SM");

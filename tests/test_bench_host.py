@@ -52,25 +52,41 @@ def test_bytes_per_token_closed_forms():
 
 @pytest.mark.slow
 def test_reference_arm_json_line():
-    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
-                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "0.8b",
+                          "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr
     lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "tok/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # timed at the GPU arm's positions: right after the 850-token prompt
+    assert d["config"]["timed_positions"] == [850, 851] and d["steps"] == 2
+    assert d["cpu_baseline"]["cpu"] and d["cpu_baseline"]["cores"] >= 1
 
 
 @pytest.mark.slow
 def test_reference_arm_torchrun_world2_rank0_prints_only():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(29700 + os.getpid() % 200),
-           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"]
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "0.8b", "--gpus", "2", "--steps", "2",
+           "--warmup", "3"]
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
     assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_kernel_bytes_add_up_to_the_token():
+    """The per-kernel byte counts of the roofline, times their launches per
+    token, add up to the whole token's algorithmic bytes."""
+    for cfg in (synth.CFG_0P8B, synth.CFG_4B, synth.CFG_TINY):
+        for kv in ("f32", "q8_0-q5_1"):
+            for t in (1, 900):
+                tot = sum(bench.kernel_launches(cfg, k) * bench.kernel_bytes(cfg, k, t, kv)
+                          for k, _ in bench.KERNEL_KINDS)
+                assert tot == bench.algorithmic_bytes(cfg, t, kv)
+    assert [k for k, _ in bench.KERNEL_KINDS][-1] == "lmhead"
 
 
 def test_byte_model_of_the_kv_formats():
@@ -97,5 +113,5 @@ def test_bench_modes_are_registered():
     out = subprocess.run([sys.executable, "bench.py", "--help"], capture_output=True, text=True, timeout=120,
                          cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert out.returncode == 0
-    for flag in ("--kv-format", "--prefill", "--batch", "--kernels", "--impl"):
+    for flag in ("--kv-format", "--prefill", "--batch", "--kernels", "--impl", "--layer"):
         assert flag in out.stdout
