@@ -15,6 +15,7 @@ import pytest
 
 import oracle
 import synth
+from kvq_sync import sync_rows
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -100,29 +101,36 @@ def test_prefill_0p8b_shapes_and_split_calls():
 
 
 def test_prefill_quantized_cache():
+    """The prefill against the oracle's token-by-token forward, teacher-forced:
+    after each oracle token its new cache row is set to the GPU's record of
+    that row (each side quantizes its own f32 row, and a code within ~1e-6
+    of a rounding boundary may come out one step apart), so the oracle
+    attends over the GPU's cache and near-tie codes do not accumulate."""
     cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=128)
     w = synth.make_model_weights(cfg)
     m, om = qg.Model(w), oracle.Model(w)
     toks = synth.prompt_tokens(cfg, 40)
     st, ost = qg.State(m, cfg.max_seq_len, qg.KV_Q8_0_Q5_1), oracle.State(om, oracle.KV_Q8_0_Q5_1)
     got = qg.qg_prefill(m, st, toks)
-    want, hid, logits = _oracle_prompt(om, ost, toks)
+    attn = [il for il, k in enumerate(cfg.kinds()) if k == synth.ATTENTION]
+    flips = 0
+    for pos, t in enumerate(toks):
+        want, hid, logits = oracle.forward_token(om, ost, int(t), pos, want_logits=True)
+        for il in attn:
+            diff, step, scales = sync_rows(st, ost, il, pos, pos + 1, cfg.n_kv_heads)
+            assert scales <= 1 and step <= 1, f"row {pos} layer {il}: a value moved {scales:.3g} steps or a code {step}"
+            flips += diff
     assert _token_ok(got, want, logits)
-    # every cache row is quantized on each side from its own f32 rows, so a code
-    # within ~1e-5 of a rounding boundary may differ by one step (each such code
-    # moves the residual stream by well under 1e-3, see the decode-step test)
-    assert rel(st.download_hidden(), hid) <= 5e-3
-    il = cfg.kinds().index(synth.ATTENTION)
-    K, V = st.download_kv_records(il)
-    nkv = cfg.n_kv_heads
-    Ko = np.ascontiguousarray(ost.kq[il][:40].reshape(40, nkv, 8, 34)[..., 2:]).view(np.int8).astype(np.int32)
-    Kq = np.ascontiguousarray(K.transpose(1, 0, 2)[..., 16:]).view(np.int8).reshape(40, nkv, 8, 32).astype(np.int32)
-    assert np.max(np.abs(Kq - Ko)) <= 1 and np.mean(Kq != Ko) < 1e-2
+    assert rel(st.download_hidden(), hid) <= TOL
     tok = want
     for i in range(4):
         a = qg.qg_decode_token(m, st, tok, 40 + i)
-        tok, _, lg = oracle.forward_token(om, ost, tok, 40 + i, want_logits=True)
+        tok, hid, lg = oracle.forward_token(om, ost, tok, 40 + i, want_logits=True)
         assert _token_ok(a, tok, lg)
+        assert rel(st.download_hidden(), hid) <= TOL
+        for il in attn:
+            sync_rows(st, ost, il, 40 + i, 41 + i, cfg.n_kv_heads)
+    print(f"prefill of 40 tokens, quantized cache: {flips} near-tie codes synced")
 
 
 def test_prefill_arguments():
