@@ -151,6 +151,10 @@ def time_kernels(qg, m, cfg, kvf, kv_name, pos, long_ctx, peak, reps=4):
     import torch
     st = qg.State(m, cfg.max_seq_len, kvf)
     prefill_synthetic(qg, st, cfg, pos)
+    # one step at `pos`: its position is in the state's device slot, where the
+    # attention kernel reads it, so the timed attention covers pos + 1 rows
+    qg.qg_decode_token(m, st, int(synth.tokens(synth.subseed(synth.MASTER_SEED, "bench.kernels"), cfg.vocab, 1)[0]),
+                       pos)
     stream = torch.cuda.Stream()
     out, total = [], 0.0
     t_rows = pos + 1

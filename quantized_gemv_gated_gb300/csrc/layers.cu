@@ -117,6 +117,10 @@ __global__ void residual_add_kernel(float* __restrict__ h, const float* __restri
 }
 
 struct AttnArgs {
+    // f32 cache: 2-D tensor maps of the layer's K and V caches ([max_seq] rows
+    // of kvd floats; box: 256 floats x the keys of a stage), so a stage of one
+    // kv head's keys is one tensor copy for K and one for V
+    CUtensorMap kmap, vmap;
     const float* qf;     // [nh][2*hd]: q then gate per head
     const float* kraw;   // [nkv*hd]
     float* kc;           // K cache: f32 [max_seq][kvd], or q8_0 records [nkv][max_seq][kKRec bytes]
@@ -135,17 +139,25 @@ struct AttnArgs {
     float theta_scale, eps;
 };
 
-// Bytes of one ring stage: kKeysPerStage keys' K and V rows (f32), or their
-// K records then their V records (quantized cache).
-template <bool KVQ>
+// Consumer warps CW of the attention kernel, which is also its keys per ring
+// stage (one key per consumer warp per stage): 16 for up to 4 query heads per
+// kv head, twice the keys in flight per SM of 8 warps (measured on the 4B
+// step: 26 instead of ~35 us per launch at t ~ 8000, and no slower at t ~
+// 900); 8 above that, where the per-warp accumulators of 8 heads need the
+// registers.
+inline int attn_warps(int gs) { return gs <= 4 ? 16 : 8; }
+
+// Bytes of one ring stage: its keys' K rows then V rows (f32), or their K
+// records then their V records (quantized cache).
+template <bool KVQ, int CW>
 __host__ __device__ constexpr int attn_stage_bytes() {
-    return KVQ ? kKeysPerStage * (kKRec + kVRec) : kKeysPerStage * 2 * kHd * 4;
+    return KVQ ? CW * (kKRec + kVRec) : CW * 2 * kHd * 4;
 }
 
-template <int GS, bool KVQ>
+template <int GS, bool KVQ, int CW>
 __host__ __device__ inline int attn_smem_floats() {
-    return GS * kHd + kHd + kHd + kHd + 8 * GS * 2 + 8 * GS * kHd + 64 * GS * 2 +
-           kAttnStages * attn_stage_bytes<KVQ>() / 4;
+    return GS * kHd + kHd + kHd + kHd + CW * GS * 2 + CW * GS * kHd + 64 * GS * 2 +
+           kAttnStages * attn_stage_bytes<KVQ, CW>() / 4;
 }
 
 
@@ -153,21 +165,22 @@ __host__ __device__ inline int attn_smem_floats() {
 // the split holding row pos quantizes this token's K (after its norm and
 // rope) and V rows into the cache, and every key, this one included, is read
 // back dequantized.
-template <int GS, bool KVQ>
-__global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
+template <int GS, bool KVQ, int CW>
+__global__ void __launch_bounds__(32 * (CW + 1)) attn_kernel(const __grid_constant__ AttnArgs a) {
+    constexpr int KS = CW, NC = 32 * CW;  // keys per stage, consumer threads
     extern __shared__ __align__(128) float sm[];
     __shared__ uint64_t full[kAttnStages], empty[kAttnStages];
     __shared__ int last_flag;
-    float* ring = sm;                                        // [stages][8 keys][K row | V row] (f32), or
-                                                             // [stages][8 K records | 8 V records]
-    float* q_s = ring + kAttnStages * attn_stage_bytes<KVQ>() / 4;  // [GS][hd]
+    float* ring = sm;                                        // [stages][KS K rows | KS V rows] (f32), or
+                                                             // [stages][KS K records | KS V records]
+    float* q_s = ring + kAttnStages * attn_stage_bytes<KVQ, CW>() / 4;  // [GS][hd]
     float* k_s = q_s + GS * kHd;                             // [hd]
     float* v_s = k_s + kHd;                                  // [hd] this token's V, dequantized (KVQ)
     float* cs = v_s + kHd;                                   // [hd/2]
     float* sn = cs + kHd / 2;                                // [hd/2]
-    float* wml = sn + kHd / 2;                               // [8][GS][2]
-    float* wacc = wml + 8 * GS * 2;                          // [8][GS][hd]
-    float* cml = wacc + 8 * GS * kHd;                        // [64][GS][2] split (m, l) of the combine
+    float* wml = sn + kHd / 2;                               // [CW][GS][2]
+    float* wacc = wml + CW * GS * 2;                         // [CW][GS][hd]
+    float* cml = wacc + CW * GS * kHd;                       // [64][GS][2] split (m, l) of the combine
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x, g = blockIdx.y;
@@ -179,19 +192,19 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
     if (s >= n_act) return;
     const bool has_new = (s == n_act - 1);  // the split holding row pos
     const int t0 = s * a.T, t1 = min(t0 + a.T, t_len);
-    const int nst = (t1 - t0 + kKeysPerStage - 1) / kKeysPerStage;
+    const int nst = (t1 - t0 + KS - 1) / KS;
     const int half = a.n_rot / 2;
 
     if (tid == 0) {
         for (int i = 0; i < kAttnStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 8);
+            mbar_init(&empty[i], CW);
         }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == 8) {
+    if (warp == CW) {
         // ----------------------------------------------------------- producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
@@ -204,18 +217,18 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
                     ok = false;
                     break;
                 }
-                const int k0 = t0 + st * kKeysPerStage, k1 = min(k0 + kKeysPerStage, t1);
+                const int k0 = t0 + st * KS, k1 = min(k0 + KS, t1);
                 if constexpr (KVQ) {
                     // rows before pos were written by earlier steps; row pos is made here
                     const int n_old = min(k1, pos) - k0;
                     const unsigned kb = static_cast<unsigned>(n_old > 0 ? n_old : 0) * kKRec;
                     const unsigned vb = static_cast<unsigned>(n_old > 0 ? n_old : 0) * kVRec;
                     mbar_arrive_expect_tx(&full[slot], kb + vb);
-                    uint8_t* st_base = reinterpret_cast<uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true>();
+                    uint8_t* st_base = reinterpret_cast<uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true, CW>();
                     const size_t rec0 = static_cast<size_t>(g) * a.max_seq + k0;
                     if (kb) {
                         bulk_g2s(st_base, reinterpret_cast<const uint8_t*>(a.kc) + rec0 * kKRec, kb, &full[slot], pol);
-                        bulk_g2s(st_base + kKeysPerStage * kKRec, reinterpret_cast<const uint8_t*>(a.vc) + rec0 * kVRec,
+                        bulk_g2s(st_base + KS * kKRec, reinterpret_cast<const uint8_t*>(a.vc) + rec0 * kVRec,
                                  vb, &full[slot], pol);
                     }
                 } else {
@@ -223,16 +236,14 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
                         pdl_wait();  // V[pos] is written by the previous kernel
                         waited = true;
                     }
-                    unsigned bytes = 0;
-                    for (int t = k0; t < k1; ++t) bytes += (t == pos ? 1u : 2u) * kHd * 4u;
-                    mbar_arrive_expect_tx(&full[slot], bytes);
-                    float* st_base = ring + static_cast<size_t>(slot) * kKeysPerStage * 2 * kHd;
-                    for (int t = k0; t < k1; ++t) {
-                        float* dst = st_base + (t - k0) * 2 * kHd;
-                        const size_t off = static_cast<size_t>(t) * a.kvd + g * kHd;
-                        if (t != pos) bulk_g2s(dst, a.kc + off, kHd * 4, &full[slot], pol);
-                        bulk_g2s(dst + kHd, a.vc + off, kHd * 4, &full[slot], pol);
-                    }
+                    // one tensor copy of kv head g's K rows k0..k0+KS-1 and one of its V
+                    // rows (K[pos] is replaced by this kernel's own row; rows past the
+                    // split are read and not used, rows past the cache read as zeros)
+                    constexpr unsigned box = KS * kHd * 4u;
+                    mbar_arrive_expect_tx(&full[slot], 2u * box);
+                    float* st_base = ring + static_cast<size_t>(slot) * KS * 2 * kHd;
+                    tma_load_2d(st_base, &a.kmap, g * kHd, k0, &full[slot], pol);
+                    tma_load_2d(st_base + KS * kHd, &a.vmap, g * kHd, k0, &full[slot], pol);
                 }
                 issued = st + 1;
                 if (st == 0) a.next.issue();
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
         sn[tid] = sv;
     }
     // per-head RMSNorm of q (and of this token's k) (per_head_rmsnorm_into)
-    for (int job = warp; job < GS + (has_new ? 1 : 0); job += 8) {
+    for (int job = warp; job < GS + (has_new ? 1 : 0); job += CW) {
         const float* src = job < GS ? a.qf + static_cast<size_t>(g * GS + job) * 2 * kHd : a.kraw + g * kHd;
         const float* w = job < GS ? a.q_norm : a.k_norm;
         float* dst = job < GS ? q_s + job * kHd : k_s;
@@ -270,28 +281,30 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[dim8(lane, i)] = (v[i] * r) * __ldg(w + dim8(lane, i));
     }
-    bar_sync(1, 256);
+    bar_sync(1, NC);
     // partial NEOX rope on pairs (i, i + n_rot/2), i < n_rot/2 (gdn_partial_neox_rope_into)
     const int jobs = GS + (has_new ? 1 : 0);
-    for (int p = tid; p < jobs * half; p += 256) {
+    for (int p = tid; p < jobs * half; p += NC) {
         const int job = p / half, i = p - job * half;
         float* vec = job < GS ? q_s + job * kHd : k_s;
         const float x0 = vec[i], x1 = vec[i + half];
         vec[i] = x0 * cs[i] - x1 * sn[i];
         vec[i + half] = x0 * sn[i] + x1 * cs[i];
     }
-    bar_sync(1, 256);
+    bar_sync(1, NC);
     if constexpr (KVQ) {
-        if (has_new) {  // quantize-on-append: warp w makes block w of the K and the V record at pos
+        if (has_new) {  // quantize-on-append: warp w < 8 makes block w of the K and the V record at pos
             const size_t rec = static_cast<size_t>(g) * a.max_seq + pos;
             const int e = 32 * warp + lane;
-            k_s[e] = kvq_put_q8_0(k_s[e], lane, warp, reinterpret_cast<uint8_t*>(a.kc) + rec * kKRec);
-            v_s[e] = kvq_put_q5_1(__ldcg(a.vraw + g * kHd + e), lane, warp,
-                                  reinterpret_cast<uint8_t*>(a.vc) + rec * kVRec);
-            bar_sync(1, 256);
+            if (warp < 8) {
+                k_s[e] = kvq_put_q8_0(k_s[e], lane, warp, reinterpret_cast<uint8_t*>(a.kc) + rec * kKRec);
+                v_s[e] = kvq_put_q5_1(__ldcg(a.vraw + g * kHd + e), lane, warp,
+                                      reinterpret_cast<uint8_t*>(a.vc) + rec * kVRec);
+            }
+            bar_sync(1, NC);
         }
     } else {
-        if (has_new) a.kc[static_cast<size_t>(pos) * a.kvd + g * kHd + tid] = k_s[tid];  // K append at pos
+        if (has_new && tid < kHd) a.kc[static_cast<size_t>(pos) * a.kvd + g * kHd + tid] = k_s[tid];  // K append at pos
     }
 
     float q[GS][8];
@@ -314,22 +327,22 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
             atomicOr(a.err, DEVERR_FULL_WAIT);
             break;
         }
-        const int t = t0 + st * kKeysPerStage + warp;
+        const int t = t0 + st * KS + warp;
         if (t < t1) {
             float kv[8], vv[8];
             if constexpr (KVQ) {
-                const uint8_t* sb = reinterpret_cast<const uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true>();
+                const uint8_t* sb = reinterpret_cast<const uint8_t*>(ring) + static_cast<size_t>(slot) * attn_stage_bytes<true, CW>();
                 if (t == pos) {
                     row8(k_s, lane, kv);
                     row8(v_s, lane, vv);
                 } else {
                     kvq_k8(sb + warp * kKRec, lane, kv);
-                    kvq_v8(sb + kKeysPerStage * kKRec + warp * kVRec, lane, vv);
+                    kvq_v8(sb + KS * kKRec + warp * kVRec, lane, vv);
                 }
             } else {
-                const float* kv_row = ring + (static_cast<size_t>(slot) * kKeysPerStage + warp) * 2 * kHd;
-                row8(t == pos ? k_s : kv_row, lane, kv);
-                row8(kv_row + kHd, lane, vv);
+                const float* k_row = ring + static_cast<size_t>(slot) * KS * 2 * kHd + warp * kHd;
+                row8(t == pos ? k_s : k_row, lane, kv);
+                row8(k_row + KS * kHd, lane, vv);
             }
 #pragma unroll
             for (int i = 0; i < GS; ++i) {
@@ -357,36 +370,38 @@ __global__ void __launch_bounds__(288) attn_kernel(const AttnArgs a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) wacc[(warp * GS + i) * kHd + dim8(lane, j)] = acc[i][j];
     }
-    bar_sync(1, 256);
-    // combine the 8 warps: thread tid owns dim tid of every head
+    bar_sync(1, NC);
+    // combine the CW warps in warp order: thread tid owns dim tid % 256 of
+    // heads tid / 256, tid / 256 + NC / 256, ...
     const size_t pbase = (static_cast<size_t>(g) * a.max_splits + s) * GS;
-    for (int i = 0; i < GS; ++i) {
+    const int dd = tid & (kHd - 1);
+    for (int i = tid / kHd; i < GS; i += NC / kHd) {
         float M = -INFINITY;
-        for (int w = 0; w < 8; ++w) M = fmaxf(M, wml[(w * GS + i) * 2]);
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, wml[(w * GS + i) * 2]);
         float L = 0.0f, A = 0.0f;
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < CW; ++w) {
             const float mw = wml[(w * GS + i) * 2];
             const float f = mw == -INFINITY ? 0.0f : expf(mw - M);
             L = fmaf(wml[(w * GS + i) * 2 + 1], f, L);
-            A = fmaf(wacc[(w * GS + i) * kHd + tid], f, A);
+            A = fmaf(wacc[(w * GS + i) * kHd + dd], f, A);
         }
-        a.part_acc[(pbase + i) * kHd + tid] = A;
-        if (tid == 0) {
+        a.part_acc[(pbase + i) * kHd + dd] = A;
+        if (dd == 0) {
             a.part_ml[(pbase + i) * 2 + 0] = M;
             a.part_ml[(pbase + i) * 2 + 1] = L;
         }
     }
     __threadfence();
-    bar_sync(1, 256);
+    bar_sync(1, NC);
     if (tid == 0) last_flag = (atomicAdd(a.count + g, 1u) == static_cast<unsigned>(n_act - 1));
-    bar_sync(1, 256);
+    bar_sync(1, NC);
     if (!last_flag) return;
     __threadfence();
     // last CTA of group g: combine the splits in order, then the sigmoid gate
     const size_t hb = static_cast<size_t>(g) * a.max_splits * GS;
-    for (int e = tid; e < n_act * GS * 2; e += 256) cml[e] = __ldcg(a.part_ml + hb * 2 + e);
-    bar_sync(1, 256);
-    for (int job = tid; job < GS * (kHd / 4); job += 256) {
+    for (int e = tid; e < n_act * GS * 2; e += NC) cml[e] = __ldcg(a.part_ml + hb * 2 + e);
+    bar_sync(1, NC);
+    for (int job = tid; job < GS * (kHd / 4); job += NC) {
         const int i = job / (kHd / 4), d4 = 4 * (job - i * (kHd / 4));
         float M = -INFINITY;
         for (int sp = 0; sp < n_act; ++sp) M = fmaxf(M, cml[(sp * GS + i) * 2]);
@@ -639,17 +654,23 @@ size_t kv_cache_bytes(const qg_state* s, int which) {
     return sizeof(float) * static_cast<size_t>(s->max_seq) * m->kv_dim;
 }
 
-template <int GS, bool KVQ>
+template <int GS, bool KVQ, int CW>
 static int launch_attn_as(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
-    const int smem = attn_smem_floats<GS, KVQ>() * 4;
-    if (int rc = grant_smem(reinterpret_cast<const void*>(attn_kernel<GS, KVQ>), smem)) return rc;
-    return launch_pdl(attn_kernel<GS, KVQ>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(288), smem, st, true, a);
+    const int smem = attn_smem_floats<GS, KVQ, CW>() * 4;
+    if (int rc = grant_smem(reinterpret_cast<const void*>(attn_kernel<GS, KVQ, CW>), smem)) return rc;
+    return launch_pdl(attn_kernel<GS, KVQ, CW>, dim3(s->max_splits, m->cfg.n_kv_heads), dim3(32 * (CW + 1)), smem, st,
+                      true, a);
+}
+
+template <int GS, bool KVQ>
+static int launch_attn_w(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
+    if constexpr (GS <= 4) return launch_attn_as<GS, KVQ, 16>(m, s, a, st);
+    else return launch_attn_as<GS, KVQ, 8>(m, s, a, st);
 }
 
 template <int GS>
 static int launch_attn(const qg_model* m, qg_state* s, const AttnArgs& a, cudaStream_t st) {
-    return s->kv_format == QG_KV_Q8_0_Q5_1 ? launch_attn_as<GS, true>(m, s, a, st)
-                                           : launch_attn_as<GS, false>(m, s, a, st);
+    return s->kv_format == QG_KV_Q8_0_Q5_1 ? launch_attn_w<GS, true>(m, s, a, st) : launch_attn_w<GS, false>(m, s, a, st);
 }
 
 // Attention input: RMSNorm prologue + the fused [q|gate | k | v] GEMV; v rows
@@ -672,6 +693,8 @@ static int launch_attention(const qg_model* m, qg_state* s, int il, cudaStream_t
     const qg_config& c = m->cfg;
     const qg_layer_dev& L = m->layers[il];
     AttnArgs a{};
+    a.kmap = s->kmap[il];
+    a.vmap = s->vmap[il];
     a.next = prefetch_of(L.w_out, q4_bytes(c.hidden, m->q_dim));
     a.qf = s->qf;
     a.kraw = s->kraw;
@@ -707,6 +730,42 @@ static int launch_attn_out(const qg_model* m, qg_state* s, int il, cudaStream_t 
     const qg_layer_dev& L = m->layers[il];
     return out_gemv<QT_Q4K>(s, L.w_out, c.hidden, m->q_dim, ProPlainG{s->attn}, st,
                             prefetch_of(L.w_gate, q4_bytes(c.ffn, c.hidden), L.w_up, q4_bytes(c.ffn, c.hidden)));
+}
+
+int encode_kv_maps(qg_state* s) {
+    const qg_model* m = s->m;
+    const int n = m->cfg.n_layers;
+    s->kmap.assign(n, CUtensorMap{});
+    s->vmap.assign(n, CUtensorMap{});
+    if (s->kv_format != QG_KV_F32) return QG_OK;
+    using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Encode encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        QG_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || !fn)
+            return set_err(QG_ERR_CUDA, "the driver has no cuTensorMapEncodeTiled");
+        encode = reinterpret_cast<Encode>(fn);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(m->kv_dim), static_cast<cuuint64_t>(s->max_seq)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(m->kv_dim) * sizeof(float)};
+    const int gs = m->cfg.n_kv_heads > 0 ? m->cfg.n_heads / m->cfg.n_kv_heads : 1;
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHd), static_cast<cuuint32_t>(attn_warps(gs))};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int il = 0; il < n; ++il) {
+        if (m->kinds[il] != QG_LAYER_ATTENTION) continue;
+        for (int which = 0; which < 2; ++which) {
+            CUtensorMap* map = which ? &s->vmap[il] : &s->kmap[il];
+            const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, which ? s->vc[il] : s->kc[il], dims,
+                                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return set_err(QG_ERR_CUDA, "cuTensorMapEncodeTiled: error %d (layer %d)", r, il);
+        }
+    }
+    return QG_OK;
 }
 
 int run_attention_layer(const qg_model* m, qg_state* s, int il, const ResidualIO& io, cudaStream_t st,

@@ -421,6 +421,7 @@ int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_sta
                             cnt)) ||
                (rc = (s->ycur = s->y, s->ycur_parts = 1, s->ycur_stride = 0, QG_OK)));
     }
+    if (!rc) rc = encode_kv_maps(s);
     if (!rc) {
         void* p = nullptr;
         cudaError_t e = cudaHostAlloc(&p, 4 * sizeof(int), cudaHostAllocDefault);

@@ -95,6 +95,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
+// Tiled 2-D tensor copy (TMA) of the box at element coordinates (x, y) of the
+// tensor map at `tmap` (a __grid_constant__ kernel parameter) into shared
+// memory at dst (128-byte aligned), completing on `bar`.  x times the element
+// size must be a multiple of 16 bytes; rows past the tensor read as zeros and
+// still count toward the box's bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Hint the TMA engine to pull [src, src + bytes) into L2 (no shared memory
 // involved); src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {

@@ -1,5 +1,7 @@
 // Internal layout of qg_model / qg_state and the per-layer launchers.
 #pragma once
+#include <cuda.h>
+
 #include <vector>
 
 #include "qg_host.cuh"
@@ -48,6 +50,7 @@ struct qg_state {
     int kv_format;                          // QG_KV_F32 or QG_KV_Q8_0_Q5_1, fixed at creation
     std::vector<float*> conv, ssm, kc, vc;  // per layer, null for the other kind; with a quantized
                                             // cache kc / vc hold q8_0 / q5_1 records (bytes)
+    std::vector<CUtensorMap> kmap, vmap;    // f32 cache: 2-D tensor maps of kc / vc (attention layers)
     // scratch; h: the residual stream after the last step (the lm_head input
     // plus the last pending y), hres: the residual stream between layers, y:
     // the output of the last GEMV, not yet added
@@ -130,6 +133,10 @@ void prefill_release(qg_state* s);
 // within the cache, which the caller checks on the host).
 int kv_quantize_rows_dev(const float* k, const float* v, int rows, const int* pos0_dev, int n_kv, int max_seq,
                          uint8_t* kq, uint8_t* vq, cudaStream_t st);
+// f32 cache: the 2-D tensor maps of every attention layer's K and V cache
+// ([max_seq] rows of kv_dim floats; box: one head's 256 floats x the
+// attention's keys per stage), for its tensor copies.
+int encode_kv_maps(qg_state* s);
 // Persistent step kernel: fill s->step (once per state), launch one step.
 int step_setup(const qg_model* m, qg_state* s);
 int run_step(qg_state* s, cudaStream_t st, bool advance);

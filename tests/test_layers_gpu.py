@@ -171,8 +171,11 @@ def tiny():
 
 @pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
 def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
-    """The graph step (per-kernel or persistent) against the kernel-by-kernel
-    eager step (bitwise) and the oracle (tolerance, exact token)."""
+    """The graph step against the kernel-by-kernel eager step and the oracle
+    (tolerance, exact token).  The per-kernel graph replays the eager step's
+    kernels, so the two agree bitwise; the persistent kernel folds the
+    attention's keys over 8 warps where the per-kernel attention uses 16, so
+    it agrees with both within the tolerance only."""
     cfg, w, m, om = tiny
     sg, se = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
     sg.set_step_mode(mode)
@@ -184,7 +187,10 @@ def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
         b = qg.qg_decode_token_eager(m, se, int(t), pos)
         ref, ref_h, logits = oracle.forward_token(om, ost, int(t), pos, want_logits=True)
         hg, he = sg.download_hidden(), se.download_hidden()
-        assert np.array_equal(hg, he) and a == b, f"pos {pos}: graph and eager differ"
+        if mode == qg.STEP_KERNELS:
+            assert np.array_equal(hg, he) and a == b, f"pos {pos}: graph and eager differ"
+        else:
+            assert rel(hg, he) <= TOL, f"pos {pos}: persistent and eager differ by {rel(hg, he):.3g}"
         e = rel(hg, ref_h)
         worst = max(worst, e)
         assert e <= TOL, f"pos {pos}: hidden {e:.3g}"

@@ -78,11 +78,13 @@ def test_masked_tokens_match_oracle_graph_and_eager(tiny, mode):
             s.set_token_mask(words)
         a = qg.qg_decode_token(m, sg, int(t), pos)
         b = qg.qg_decode_token_eager(m, se, int(t), pos)
-        assert a == b, f"pos {pos}: graph {a} != eager {b}"
+        if mode == qg.STEP_KERNELS:  # the same kernels: the same token (the persistent one: the oracle's, below)
+            assert a == b, f"pos {pos}: graph {a} != eager {b}"
         if words is not None:
             assert (words[a >> 5] >> np.uint32(a & 31)) & 1, f"pos {pos}: banned id {a} chosen"
         exact += _check(a, logits, words, want)
-        assert np.array_equal(sg.download_hidden(), se.download_hidden())
+        if mode == qg.STEP_KERNELS:
+            assert np.array_equal(sg.download_hidden(), se.download_hidden())
     assert exact >= len(toks) - 2
     st = sg.stats()
     assert st["graph_captures"] == 1 and st["graph_launches"] == len(toks)
