@@ -391,9 +391,11 @@ __global__ void __launch_bounds__(32 * (CW + 1)) attn_kernel(const __grid_consta
             a.part_ml[(pbase + i) * 2 + 1] = L;
         }
     }
-    __threadfence();
-    bar_sync(1, NC);
-    if (tid == 0) last_flag = (atomicAdd(a.count + g, 1u) == static_cast<unsigned>(n_act - 1));
+    bar_sync(1, NC);  // every thread's partials are written ...
+    if (tid == 0) {
+        __threadfence();  // ... and released at gpu scope (cumulative over the barrier), before the arrival
+        last_flag = (atomicAdd(a.count + g, 1u) == static_cast<unsigned>(n_act - 1));
+    }
     bar_sync(1, NC);
     if (!last_flag) return;
     __threadfence();
@@ -401,19 +403,26 @@ __global__ void __launch_bounds__(32 * (CW + 1)) attn_kernel(const __grid_consta
     const size_t hb = static_cast<size_t>(g) * a.max_splits * GS;
     for (int e = tid; e < n_act * GS * 2; e += NC) cml[e] = __ldcg(a.part_ml + hb * 2 + e);
     bar_sync(1, NC);
-    for (int job = tid; job < GS * (kHd / 4); job += NC) {
+    // one float4 of a head per job; when the CTA has two threads per job
+    // (adjacent lanes), each folds every other split in split order and the
+    // pair adds the two sums: half the dependent L2 round trips per thread
+    constexpr int JOBS = GS * (kHd / 4);
+    constexpr int R = NC >= 2 * JOBS ? 2 : 1;
+    for (int jt = tid; jt < R * JOBS; jt += NC) {
+        const int job = jt / R, half = jt % R;
         const int i = job / (kHd / 4), d4 = 4 * (job - i * (kHd / 4));
         float M = -INFINITY;
         for (int sp = 0; sp < n_act; ++sp) M = fmaxf(M, cml[(sp * GS + i) * 2]);
         float L = 0.0f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp0 = 0; sp0 < n_act; sp0 += 8) {
+        for (int sp0 = half; sp0 < n_act; sp0 += 8 * R) {
             float4 v[8];
             float f[8], lw[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const bool in = sp0 + u < n_act;
-                const int sp = in ? sp0 + u : sp0;
+                const int spu = sp0 + R * u;
+                const bool in = spu < n_act;
+                const int sp = in ? spu : 0;  // split 0 always exists; its term is weighted 0
                 v[u] = __ldcg(reinterpret_cast<const float4*>(a.part_acc + (hb + sp * GS + i) * kHd + d4));
                 f[u] = in ? expf(cml[(sp * GS + i) * 2] - M) : 0.0f;
                 lw[u] = cml[(sp * GS + i) * 2 + 1];
@@ -426,6 +435,14 @@ __global__ void __launch_bounds__(32 * (CW + 1)) attn_kernel(const __grid_consta
                 A.z = fmaf(v[u].z, f[u], A.z);
                 A.w = fmaf(v[u].w, f[u], A.w);
             }
+        }
+        if constexpr (R == 2) {  // the pair's two sums (every lane of the warp takes part)
+            L += __shfl_xor_sync(FULL, L, 1);
+            A.x += __shfl_xor_sync(FULL, A.x, 1);
+            A.y += __shfl_xor_sync(FULL, A.y, 1);
+            A.z += __shfl_xor_sync(FULL, A.z, 1);
+            A.w += __shfl_xor_sync(FULL, A.w, 1);
+            if (half) continue;
         }
         const int h = g * GS + i;
         const float4 gt = __ldcg(reinterpret_cast<const float4*>(a.qf + static_cast<size_t>(h) * 2 * kHd + kHd + d4));
