@@ -434,10 +434,8 @@ def run_ours(args, rank, world, local):
     K, W = args.steps, args.warmup
     w = synth.make_model_weights(cfg)
     m = qg.Model(w, device=local)
-    mode = qg.STEP_PERSISTENT if args.step_mode == "persistent" else qg.STEP_KERNELS
     kvf = KV_FORMATS[args.kv_format]
     st = qg.State(m, cfg.max_seq_len, kvf)
-    st.set_step_mode(mode)
     # warm up (graph capture, clocks), then restart the sequence for the timed run
     pos, _ = prefill(qg, m, st, cfg, long_ctx, args.prompt)
     qg.qg_decode_greedy(m, st, pos, W)
@@ -464,7 +462,6 @@ def run_ours(args, rank, world, local):
     dt2 = None
     if not args.no_e2e:
         st2 = qg.State(m, cfg.max_seq_len, kvf)
-        st2.set_step_mode(mode)
         p2, tok = prefill(qg, m, st2, cfg, long_ctx, args.prompt)
         ext2 = torch.cuda.ExternalStream(st2.stream)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -493,7 +490,7 @@ def run_ours(args, rank, world, local):
         "ms_per_step": round(1000.0 * dt / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE, "data": "synthetic (seeded random-init weights and prompt)",
         "config": {"workload": f"{args.workload}: {desc}", "global_batch": world, "seq_len": cfg.max_seq_len,
-                   "parallelism": f"replicas x{world}", "step_mode": args.step_mode,
+                   "parallelism": f"replicas x{world}",
                    "kv_cache": KV_DESC[args.kv_format], "prompt_tokens": pos0, "timed_positions": [pos0, pos0 + K - 1],
                    "l2": f"no flush: {bpt / 1e6:.1f} MB of weights and state per token > 129 MB L2",
                    "greedy_tokens_head": [int(t) for t in toks[:4]]},
@@ -825,8 +822,6 @@ def main():
     ap.add_argument("--kv-format", choices=sorted(KV_FORMATS), default="f32",
                     help="KV cache format of the decode state (and of the oracle's, on the reference arm)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-API (e2e) measurement")
-    ap.add_argument("--step-mode", choices=["kernels", "persistent"], default="kernels",
-                    help="whole-token step: one kernel per fused op, or one persistent launch")
     ap.add_argument("--batch", type=int, default=0,
                     help="decode this many sequences in lockstep (qg_decode_batch) against one sequence (one JSON line)")
     ap.add_argument("--prefill", action="store_true",

@@ -262,20 +262,6 @@ int qg_batch_create(qg_model* m, qg_state* const* states, int n, qg_batch** out)
 int qg_batch_step(qg_batch* b, const uint32_t* tokens, const int* positions, uint32_t* next_tokens);
 int qg_batch_destroy(qg_batch* b);
 
-/* How the whole-token calls (qg_decode_token, qg_decode_greedy) run a step:
- * QG_STEP_KERNELS (the default): one kernel per fused op, chained with
- * programmatic dependent launch inside the step's CUDA graph;
- * QG_STEP_PERSISTENT: one cooperative launch per token whose CTAs stay
- * resident and separate the phases with grid-wide barriers, while a producer
- * warp per CTA streams the weights ahead across them.  Both give bit-identical
- * results.  Changing the mode drops the captured graphs (recaptured on the
- * next call).  Errors: QG_ERR_ARG (unknown mode), QG_ERR_SHAPE (the model's
- * shape is not served by the persistent kernel: more than 64 layers, a GQA
- * group other than 1, 2 or 4, more than 64 value heads, or no cooperative
- * launch on the device); QG_ERR_ARG also for QG_STEP_PERSISTENT on a state
- * with a quantized KV cache (the persistent kernel reads f32 caches only). */
-enum { QG_STEP_KERNELS = 0, QG_STEP_PERSISTENT = 1 };
-int qg_state_set_step_mode(qg_state* s, int mode);
 
 /* ------------------------------------------------------- building blocks
  * Device pointers, the caller's stream, no allocation, no synchronisation. */

@@ -27,7 +27,7 @@ ERROR_NAMES = {0: "QG_OK", -1: "QG_ERR_SHAPE", -2: "QG_ERR_QTYPE", -3: "QG_ERR_E
 EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
-    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_step_mode", "qg_state_set_token_mask",
+    "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_token_mask",
     "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes", "qg_q4k_planar_bytes", "qg_q4k_to_planar",
     "qg_gemv_q4k_planar",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
@@ -39,7 +39,6 @@ EXPORTS = [
 ]
 
 
-STEP_KERNELS, STEP_PERSISTENT = 0, 1  # qg_state_set_step_mode
 # kernel kinds of the decode step (qg_bench_kernel)
 KERNEL_DN_IN, KERNEL_DELTA, KERNEL_SSM_OUT, KERNEL_ATTN_IN, KERNEL_ATTN, KERNEL_ATTN_OUT = 0, 1, 2, 3, 4, 5
 KERNEL_FFN_UP, KERNEL_FFN_DOWN, KERNEL_LMHEAD = 6, 7, 8
@@ -127,7 +126,6 @@ def lib():
             "qg_state_kv_len": [p, ctypes.POINTER(i)],
             "qg_state_stream": [p, ctypes.POINTER(p)],
             "qg_state_stats": [p, ctypes.POINTER(QgStats)],
-            "qg_state_set_step_mode": [p, i],
             "qg_state_set_token_mask": [p, p, i],
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
@@ -394,10 +392,6 @@ class State:
         st = QgStats()
         _check(lib().qg_state_stats(self.handle, ctypes.byref(st)))
         return st.as_dict()
-
-    def set_step_mode(self, mode):
-        """STEP_KERNELS (default) or STEP_PERSISTENT (qg_state_set_step_mode)."""
-        _check(lib().qg_state_set_step_mode(self.handle, int(mode)))
 
     def set_token_mask(self, allow_words=None):
         """Token mask of the whole-token calls (qg_state_set_token_mask):

@@ -182,7 +182,7 @@ int capture(qg_model* m, qg_state* s, bool greedy, cudaGraphExec_t* exec) {
         cudaError_t e = cudaMemcpyAsync(s->slots, s->pinned, 2 * sizeof(int), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) rc = cuda_err(e, "capture H2D");
     }
-    if (!rc) rc = s->step_mode == QG_STEP_PERSISTENT ? run_step(s, st, greedy) : enqueue_token(m, s, st, greedy);
+    if (!rc) rc = enqueue_token(m, s, st, greedy);
     if (!rc && !greedy) {
         cudaError_t e = cudaMemcpyAsync(s->pinned + 2, s->slots + 2, sizeof(int), cudaMemcpyDeviceToHost, st);
         if (e != cudaSuccess) rc = cuda_err(e, "capture D2H");
@@ -362,10 +362,6 @@ int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_sta
     s->exec_step = nullptr;
     s->exec_greedy = nullptr;
     s->pf = nullptr;
-    s->step = nullptr;
-    s->step_mode = QG_STEP_KERNELS;
-    s->step_grid = s->step_smem = 0;
-    s->gbar = nullptr;
     std::memset(&s->stats, 0, sizeof s->stats);
     const qg_config& c = m->cfg;
     uint64_t* cnt = &s->stats.device_allocs;
@@ -413,7 +409,6 @@ int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_sta
                (rc = dalloc(s->allocs, &s->am_ws, 2, cnt)) || (rc = dalloc(s->allocs, &s->slots, 4, cnt)) ||
                (rc = dalloc(s->allocs, &s->hist, max_seq_len, cnt)) || (rc = dalloc(s->allocs, &s->err, 1, cnt)) ||
                (rc = dalloc(s->allocs, &s->allow, (static_cast<size_t>(c.vocab) + 31) / 32, cnt)) ||
-               (rc = dalloc(s->allocs, &s->gbar, 4, cnt)) ||
                (rc = dalloc(s->allocs, &s->kpart,
                             static_cast<size_t>(std::max({gemv_slices(c.ffn), gemv_slices(m->v_dim > 0 ? m->v_dim : 256),
                                                           gemv_slices(m->q_dim > 0 ? m->q_dim : 256)})) *
@@ -441,7 +436,6 @@ int qg_state_create_kv(const qg_model* m, int max_seq_len, int kv_format, qg_sta
         rc = qg_state_reset(s);
     }
     if (rc) {
-        delete s->step;
         if (s->pinned) cudaFreeHost(s->pinned);
         free_all(s->allocs);
         delete s;
@@ -461,7 +455,6 @@ int qg_state_destroy(qg_state* s) {
     if (s->pinned) cudaFreeHost(s->pinned);
     prefill_release(s);
     free_all(s->allocs);
-    delete s->step;
     delete s;
     return QG_OK;
 }
@@ -487,7 +480,6 @@ int qg_state_reset(qg_state* s) {
     QG_CUDA(cudaMemset(s->am_ws, 0, 2 * sizeof(unsigned long long)));
     QG_CUDA(cudaMemset(s->slots, 0, 4 * sizeof(int)));
     QG_CUDA(cudaMemset(s->err, 0, sizeof(unsigned)));
-    QG_CUDA(cudaMemset(s->gbar, 0, 4 * sizeof(unsigned)));
     QG_CUDA(cudaMemset(s->allow, 0xff, sizeof(uint32_t) * ((static_cast<size_t>(c.vocab) + 31) / 32)));  // no mask
     QG_CUDA(cudaDeviceSynchronize());
     s->kv_len = 0;
@@ -635,32 +627,6 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words) {
 int qg_state_stream(const qg_state* s, qg_stream* out) {
     if (!s || !out) return set_err(QG_ERR_ARG, "state_stream: NULL argument");
     *out = reinterpret_cast<qg_stream>(s->stream);
-    return QG_OK;
-}
-
-int qg_state_set_step_mode(qg_state* s, int mode) {
-    if (!s) return set_err(QG_ERR_ARG, "set_step_mode: NULL state");
-    if (mode != QG_STEP_KERNELS && mode != QG_STEP_PERSISTENT)
-        return set_err(QG_ERR_ARG, "set_step_mode: unknown mode %d", mode);
-    if (mode == s->step_mode) return QG_OK;
-    if (mode == QG_STEP_PERSISTENT && s->kv_format != QG_KV_F32)
-        return set_err(QG_ERR_ARG, "set_step_mode: the persistent step kernel reads an f32 KV cache only");
-    DeviceGuard dg(s->m->device);
-    QG_CUDA(cudaStreamSynchronize(s->stream));
-    if (mode == QG_STEP_PERSISTENT && !s->step) {
-        s->step = new (std::nothrow) StepParams();
-        if (!s->step) return set_err(QG_ERR_OOM, "set_step_mode: host allocation");
-        const int rc = step_setup(s->m, s);
-        if (rc) {
-            delete s->step;
-            s->step = nullptr;
-            return rc;
-        }
-    }
-    if (s->exec_step) cudaGraphExecDestroy(s->exec_step);
-    if (s->exec_greedy) cudaGraphExecDestroy(s->exec_greedy);
-    s->exec_step = s->exec_greedy = nullptr;
-    s->step_mode = mode;
     return QG_OK;
 }
 

@@ -16,7 +16,6 @@ enum : unsigned {
     DEVERR_FULL_WAIT = 1u,    // consumer waited too long for a bulk copy
     DEVERR_EMPTY_WAIT = 2u,   // producer waited too long for a free ring slot
     DEVERR_DRAIN_WAIT = 4u,   // copies still in flight at an error exit
-    DEVERR_GRID_WAIT = 8u,    // a grid-wide barrier of the step kernel waited too long
 };
 
 // ~1-2 s at GB300 clocks: far above any legitimate wait, short enough that a
@@ -65,18 +64,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
     }
     return true;
 }
-
-// Grid-barrier primitives: release-add of an arrival, relaxed polling, and
-// one acquire fence once the count is reached.
-__device__ __forceinline__ void red_release_add_gpu(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ------------------------------------------------------ bulk copy (TMA 1-D)
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -386,8 +386,8 @@ __device__ __forceinline__ float dot_q6k(const uint8_t* rec, unsigned S, uint16_
 // consumer warps: `full` completes when a stage's bulk copies have landed,
 // `empty` when all consumer warps released it.  q counts the stages taken
 // (the same sequence on both sides).  Waits are bounded and also give up
-// once `abort` is non-zero (a per-kernel error word, or the persistent step
-// kernel's step-wide flag), so a failed pipeline ends in about one wait.
+// once `abort` (the kernel's error word) is non-zero, so a failed pipeline
+// ends in about one wait.
 struct Pipe {
     uint64_t* full;
     uint64_t* empty;
@@ -428,7 +428,6 @@ struct Pipe {
     }
     __device__ void fail(unsigned bit) const {
         atomicOr(err, bit);
-        if (abort != err) atomicExch(abort, 1u);
     }
     // consumer side (every lane of every consumer warp)
     __device__ void wait_full() const {

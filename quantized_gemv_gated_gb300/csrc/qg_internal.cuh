@@ -5,7 +5,6 @@
 #include <vector>
 
 #include "qg_host.cuh"
-#include "qg_step.cuh"
 
 // Device-resident weights of one layer.
 struct qg_layer_dev {
@@ -72,12 +71,6 @@ struct qg_state {
     int keys_per_split, max_splits;
     cudaGraphExec_t exec_step;
     cudaGraphExec_t exec_greedy;
-    // persistent whole-step kernel: parameters (null when the model shape is
-    // not served by it) and whether decode calls use it
-    qg::StepParams* step;
-    int step_mode;
-    int step_grid, step_smem;
-    unsigned* gbar;             // device: its barrier words [3] (left at 0)
     qg_stats stats;
     std::vector<void*> allocs;
 };
@@ -137,9 +130,6 @@ int kv_quantize_rows_dev(const float* k, const float* v, int rows, const int* po
 // ([max_seq] rows of kv_dim floats; box: one head's 256 floats x the
 // attention's keys per stage), for its tensor copies.
 int encode_kv_maps(qg_state* s);
-// Persistent step kernel: fill s->step (once per state), launch one step.
-int step_setup(const qg_model* m, qg_state* s);
-int run_step(qg_state* s, cudaStream_t st, bool advance);
 // Raw GGUF Q4_K rows -> the engine's grouped layout ((n+7)/8*8 x k/256 x 144 bytes).
 int q4k_to_grouped(const void* src, void* dst, int n, int k, cudaStream_t st);
 // Quantized-cache rows from f32 K/V rows ([rows][n_kv*256] each): the records

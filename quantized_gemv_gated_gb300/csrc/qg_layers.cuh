@@ -1,12 +1,14 @@
-// Device pieces shared by the per-layer kernels and the persistent step
-// kernel: the epilogues of the fused input projections and of the lm_head
-// argmax, the delta-rule row update, and the attention row helpers.
+// Device pieces shared by the per-layer kernels and the batched prefill: the
+// epilogues of the fused input projections and of the lm_head argmax, the
+// delta-rule row update, and the attention row helpers.
 #pragma once
 #include <cfloat>
 
 #include "qg_internal.cuh"
 
 namespace qg {
+
+constexpr int kHd = 256;  // attention head_dim (the configs the kernels serve)
 
 // ------------------------------------------------------------ epilogues
 // DeltaNet input projection rows: [0, C) qkv -> conv; [C, C+nv) alpha;
@@ -204,7 +206,6 @@ struct ProGatedNorm {
 // gdn_delta_rule_into: per value head a [dv x 128] state, s[j*128 + i] ==
 // S[i][j]; the key head of value head h is h % n_k_heads.
 constexpr int kDk = 128;
-constexpr int kMaxRowsPerWarp = 16;
 
 // Rows t = 0..3 of one value head, one warp (lane owns k-dims 4*lane..+3):
 // decay by g, read S_t . k, rank-1 update S_t += k * beta * (v_t - S_t . k),
@@ -250,16 +251,16 @@ __device__ __forceinline__ void delta_rows4(const float* st, float* Sg, float4 k
 }
 
 // ------------------------------------------------------ GQA decode attention
-// Grid (max_splits, n_kv_heads), 8 consumer warps + 1 producer warp.  CTA
+// Grid (max_splits, n_kv_heads), CW consumer warps + 1 producer warp.  CTA
 // (s, g) covers cache rows [s*T, min((s+1)*T, pos+1)) for the GS query heads
 // of kv group g (contiguous groups).  The producer streams the split's K and V
-// rows of group g (1 KB each) into a shared-memory ring with bulk copies,
-// 8 keys per stage; rows older than pos are fetched before the dependency
-// wait, V[pos] (written by the previous kernel) after it, and K[pos] is
-// computed here.  head_dim = 256: lane owns dims 4*lane..+3 and 128+4*lane..+3.
-constexpr int kHd = 256;
+// rows of head g (1 KB each) into a shared-memory ring, CW keys per stage as
+// one 2-D tensor copy of K rows and one of V rows (f32 cache), or one bulk
+// copy of K records and one of V records (quantized cache); rows older than
+// pos are fetched before the dependency wait, V[pos] (written by the previous
+// kernel) after it, and K[pos] is computed here.  head_dim = 256: lane owns
+// dims 4*lane..+3 and 128+4*lane..+3.
 constexpr int kAttnStages = 4;
-constexpr int kKeysPerStage = 8;
 
 __device__ __forceinline__ void row8(const float* p, int lane, float* v) {
     const float4 a = *reinterpret_cast<const float4*>(p + 4 * lane);

@@ -260,9 +260,6 @@ def test_quantized_cache_arguments():
     fmt = qg.ctypes.c_int()
     qg._check(qg.lib().qg_state_kv_format(st.handle, qg.ctypes.byref(fmt)))
     assert fmt.value == qg.KV_Q8_0_Q5_1
-    with pytest.raises(qg.QgError) as e:
-        st.set_step_mode(qg.STEP_PERSISTENT)
-    assert e.value.code == qg.QG_ERR_ARG
     il = cfg.kinds().index(synth.ATTENTION)
     with pytest.raises(qg.QgError) as e:
         st.download_layer(il)

@@ -169,16 +169,12 @@ def tiny():
     return cfg, w, qg.Model(w), oracle.Model(w)
 
 
-@pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
-def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
+def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny):
     """The graph step against the kernel-by-kernel eager step and the oracle
-    (tolerance, exact token).  The per-kernel graph replays the eager step's
-    kernels, so the two agree bitwise; the persistent kernel folds the
-    attention's keys over 8 warps where the per-kernel attention uses 16, so
-    it agrees with both within the tolerance only."""
+    (tolerance, exact token).  The graph replays the eager step's kernels, so
+    the two agree bitwise."""
     cfg, w, m, om = tiny
     sg, se = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
-    sg.set_step_mode(mode)
     ost = oracle.State(om)
     toks = synth.prompt_tokens(cfg, 40)
     worst = 0.0
@@ -187,10 +183,7 @@ def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
         b = qg.qg_decode_token_eager(m, se, int(t), pos)
         ref, ref_h, logits = oracle.forward_token(om, ost, int(t), pos, want_logits=True)
         hg, he = sg.download_hidden(), se.download_hidden()
-        if mode == qg.STEP_KERNELS:
-            assert np.array_equal(hg, he) and a == b, f"pos {pos}: graph and eager differ"
-        else:
-            assert rel(hg, he) <= TOL, f"pos {pos}: persistent and eager differ by {rel(hg, he):.3g}"
+        assert np.array_equal(hg, he) and a == b, f"pos {pos}: graph and eager differ"
         e = rel(hg, ref_h)
         worst = max(worst, e)
         assert e <= TOL, f"pos {pos}: hidden {e:.3g}"
@@ -199,16 +192,14 @@ def test_decode_token_matches_oracle_graph_and_eager_bitwise(tiny, mode):
             pytest.fail(f"pos {pos}: token {a} != oracle {ref} (oracle top-2 margin {v1 - v2:.4g})")
     st = sg.stats()
     assert st["graph_captures"] == 1 and st["graph_launches"] == len(toks)
-    assert st["graph_kernel_nodes"] == 1 if mode == qg.STEP_PERSISTENT else st["graph_kernel_nodes"] > 1
+    assert st["graph_kernel_nodes"] == 5 * cfg.n_layers + 1
     assert st["d2h_bytes"] == 4 * len(toks) and st["h2d_bytes"] == 8 * len(toks)
     print(f"tiny model, 40 tokens: worst hidden rel err {worst:.3g}, {st['graph_kernel_nodes']} kernel nodes")
 
 
-@pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
-def test_greedy_device_loop_matches_oracle_greedy(tiny, mode):
+def test_greedy_device_loop_matches_oracle_greedy(tiny):
     cfg, w, m, om = tiny
     st = qg.State(m, cfg.max_seq_len)
-    st.set_step_mode(mode)
     ost = oracle.State(om)
     toks = synth.prompt_tokens(cfg, 12)
     for pos, t in enumerate(toks):

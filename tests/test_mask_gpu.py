@@ -4,7 +4,7 @@ against the oracle's masked argmax of its own logits on the same seeded
 model and inputs.
 
 Bars: token ids exact wherever the masked top-2 margin of the oracle's logits
-is decisive; graph (either step mode) and eager replays identical; setting,
+is decisive; graph and eager replays identical; setting,
 changing and clearing the mask between steps needs no recapture.
 """
 import numpy as np
@@ -52,12 +52,10 @@ def _check(got, logits, words, want):
     return False
 
 
-@pytest.mark.parametrize("mode", [qg.STEP_KERNELS, qg.STEP_PERSISTENT])
-def test_masked_tokens_match_oracle_graph_and_eager(tiny, mode):
+def test_masked_tokens_match_oracle_graph_and_eager(tiny):
     cfg, w, m, om = tiny
     V = cfg.vocab
     sg, se = qg.State(m, cfg.max_seq_len), qg.State(m, cfg.max_seq_len)
-    sg.set_step_mode(mode)
     ost = oracle.State(om)
     rng = np.random.default_rng(synth.subseed(synth.MASTER_SEED, "token-mask"))
     toks = synth.prompt_tokens(cfg, 32)
@@ -78,13 +76,11 @@ def test_masked_tokens_match_oracle_graph_and_eager(tiny, mode):
             s.set_token_mask(words)
         a = qg.qg_decode_token(m, sg, int(t), pos)
         b = qg.qg_decode_token_eager(m, se, int(t), pos)
-        if mode == qg.STEP_KERNELS:  # the same kernels: the same token (the persistent one: the oracle's, below)
-            assert a == b, f"pos {pos}: graph {a} != eager {b}"
+        assert a == b, f"pos {pos}: graph {a} != eager {b}"
         if words is not None:
             assert (words[a >> 5] >> np.uint32(a & 31)) & 1, f"pos {pos}: banned id {a} chosen"
         exact += _check(a, logits, words, want)
-        if mode == qg.STEP_KERNELS:
-            assert np.array_equal(sg.download_hidden(), se.download_hidden())
+        assert np.array_equal(sg.download_hidden(), se.download_hidden())
     assert exact >= len(toks) - 2
     st = sg.stats()
     assert st["graph_captures"] == 1 and st["graph_launches"] == len(toks)
