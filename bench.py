@@ -214,12 +214,13 @@ def measured_peaks():
 
 # profiles/traffic.json records ncu DRAM bytes per launch of the step's kernels,
 # keyed by kernel kind, with a hash of the CUDA sources they were taken from:
-# a record taken from other sources reads as unknown (null).
+# a record taken from other sources reads as unknown (null).  The batched
+# prefill's source is not part of any decode-step kernel and is left out.
 def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and name != "prefill.cu":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
