@@ -31,8 +31,6 @@ constexpr int kGK = 64;        // k per shared-memory stage (a quarter super-blo
 constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
 constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
 
-__device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return static_cast<uint16_t>(p[0] | (p[1] << 8)); }
-
 // The columns of one pass split into segments: segment s is one sequence's
 // run of consecutive positions pos0[s].. in columns col0[s]..col0[s+1]-1, with
 // that sequence's state of the current layer (conv window and recurrent
@@ -159,6 +157,8 @@ template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                          const float* __restrict__ X, int ldx, float* __restrict__ Y,
                                                          int ldy, size_t split_stride, int P, int q_per_split) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     using Raw = typename std::conditional<QT == QT_Q6K, RawQ6, RawQ4>::type;
     extern __shared__ __align__(16) float smf[];
     float* Ws = smf;                  // [kGK][kGR]
@@ -242,108 +242,514 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
     }
 }
 
-// Y = W X for at most 4 columns (a batched decode step): the weights are read
-// once and each is multiplied against the 4 columns' inputs.  X packed
-// [k][4] (the 4 columns of one k are one float4), read straight from L1/L2 (a
-// warp's reads are 32 consecutive float4).  One CTA per 8-row group, two warps per row taking alternate
-// super-blocks; lane l dequantizes weights l, l + 32, .., l + 224 of a
-// super-block (one of each 32-weight sub-block: the warp's loads of the
-// weight bytes and of the staged inputs are consecutive, no bank conflicts)
-// into 4 accumulators; the two warps' sums meet in shared memory.  Output token-major Y[t][ldy] or, ROW_MAJOR,
-// Y[row][ldy]; columns >= nm are not stored.  Grid ceil(n/8), 512 threads.
-// One warp's part of row (gi, rr) of a small-batch GEMV: the super-blocks
-// b = half, half + 2, .. of the row, lane l taking weights l + 32 i of each,
-// multiplied against the 4 packed input columns xs4[k] into acc[4].
+// ------------------------------------ small-batch GEMV on the engine's pipeline
+// Y = W X for at most 4 columns (a lockstep decode step of up to 4
+// sequences), W in the engine's grouped, slice-major layout and read once for
+// all columns; X packed [k][4] (the 4 columns of one k are one float4).
+//
+// Work split.  The (K slice, 8-row group) tasks, slice-major and weighted by
+// the slice width, are cut into one contiguous range per CTA (two CTAs per
+// SM).  A task writes its rows' sums over its slice to output part s (s the
+// slice index) and the consumer of Y adds the parts in slice order, so a CTA
+// stages the inputs of one slice (two at a range's seam) once, and its
+// producer warp streams the CTA's rows of that slice into the engine's ring
+// of shared-memory stages (one bulk copy per stage of up to PP row passes).
+//
+// Arithmetic.  In a slice of G = 2^lg chunks of 64 weights, G lanes cover one
+// row (the engine's lane partition), lane j its chunk; a lane takes all the
+// passes of a stage together, so every input float4 it reads serves each of
+// them.  A 4- or 6-bit code c becomes the float 1 + c 2^-e by a shift that
+// puts it into the mantissa of 1.0 and one mask-or, so a lane's sum over a
+// sub-block is sum x + 2^-e sum c x: the plain sum of x over the sub-block
+// (formed once per slice and shared by every lane) is taken off and the rest
+// scaled by 2^e, both exact.  The products keep f32 rounding (2^-24 of
+// sum |x| per sub-block, times 2^e <= 2^8 after the subtraction).  The integer
+// scales and the Q4_K minimum enter once per sub-block, as the GGUF formulas
+// have them, and a transposed xor tree sums the 4 columns over a row's G
+// lanes (lane j ends with column j >> (lg - 2)).
+constexpr int kBmSliceK = 2048;  // inputs staged per slice (the widest slice: 32 chunks of 64)
 template <int QT>
-__device__ __forceinline__ void bm_row_acc(const uint8_t* __restrict__ W, int n8, int nb, int gi, int rr, int half,
-                                           int lane, const float4* __restrict__ xs4, float* acc) {
-    const int GB = QT == QT_Q6K ? 1680 : 1152;
-#pragma unroll 2
-    for (int b = half; b < nb; b += 2) {
-        const uint8_t* gb = W + grouped_offset(n8, nb, gi, b, GB);
-        float w[8];  // weights lane + 32 i of the super-block (sub-block i)
-        if (QT == QT_Q4K) {
-            const uint8_t* blk = gb + 144 * rr;
-            const uint4 h = *reinterpret_cast<const uint4*>(blk);
-            const float d = f16_to_f32(static_cast<uint16_t>(h.x & 0xffffu));
-            const float dmin = f16_to_f32(static_cast<uint16_t>(h.x >> 16));
-            int qb[4];  // byte lane of each 64-weight chunk: the low nibble for sub-block 2c, the high for 2c + 1
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) qb[c4] = blk[16 + 32 * c4 + lane];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                int sc, mn;
-                if (i < 4) {
-                    sc = byte_of(h, 4 + i) & 63;
-                    mn = byte_of(h, 8 + i) & 63;
-                } else {
-                    sc = (byte_of(h, 8 + i) & 15) | ((byte_of(h, i) >> 6) << 4);
-                    mn = (byte_of(h, 8 + i) >> 4) | ((byte_of(h, 4 + i) >> 6) << 4);
-                }
-                const int nib = (i & 1) ? (qb[i >> 1] >> 4) : (qb[i >> 1] & 15);
-                w[i] = (d * static_cast<float>(sc)) * static_cast<float>(nib) - dmin * static_cast<float>(mn);
-            }
+struct BmPasses {
+    static constexpr int value = QT == QT_Q4K ? 3 : 2;  // row passes per stage (27 KB / 26 KB)
+};
+constexpr int kBmXs = kBmSliceK + kBmSliceK / 64 + kBmSliceK / 512;  // staged float4 slots (with the padding)
+
+// Slot of input k in the staged slice: a row's lanes read inputs 64 (Q4_K) or
+// 256 (Q6_K) apart at the same time, which would fall on the same banks; one
+// float4 of padding after every 64 and one more after every 512 puts the 8
+// lanes of a shared-memory phase on 8 different 16-byte bank groups.  A run
+// of 64 inputs from a multiple of 64 stays contiguous, so a lane reads its
+// chunk at fixed offsets from one pointer.
+__device__ __forceinline__ int xs_at(int k) { return k + (k >> 6) + (k >> 9); }
+
+__device__ __forceinline__ void fma4(float4& a, float q, const float4& x) {
+    a.x = fmaf(q, x.x, a.x);
+    a.y = fmaf(q, x.y, a.y);
+    a.z = fmaf(q, x.z, a.z);
+    a.w = fmaf(q, x.w, a.w);
+}
+// Byte b of v moved to bits 15..22 (Q4_K: low nibble at 15, high at 19) or
+// 17..22 (Q6_K codes), the mantissa bits of 1.0 that the mask-or fills.
+template <int B, int AT>
+__device__ __forceinline__ unsigned byte_to(unsigned v) {
+    constexpr int sh = AT - 8 * B;
+    return sh >= 0 ? v << sh : v >> -sh;
+}
+__device__ __forceinline__ float one_plus(unsigned t, unsigned mask) { return __uint_as_float((t & mask) | 0x3F800000u); }
+
+// The 4 columns of v summed over the G = 2^lg lanes of the lane's row: lane j
+// of the row returns column j >> (lg - 2) (a transposed xor tree: two
+// exchanges halve the columns, the rest is a plain tree).
+__device__ __forceinline__ float row_sum4(const float4& v, int lg, int lane) {
+    const int o1 = 1 << (lg - 1), o2 = 1 << (lg - 2);
+    const bool b1 = lane & o1, b2 = lane & o2;
+    float a0 = b1 ? v.z : v.x, a1 = b1 ? v.w : v.y;
+    a0 += __shfl_xor_sync(FULL, b1 ? v.x : v.z, o1);
+    a1 += __shfl_xor_sync(FULL, b1 ? v.y : v.w, o1);
+    float r = b2 ? a1 : a0;
+    r += __shfl_xor_sync(FULL, b2 ? a0 : a1, o2);
+    for (int o = o2 >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(FULL, r, o);
+    return r;
+}
+
+// What a lane needs of its row and chunk in one slice.
+struct BmLane {
+    int lg, rl, j, q;
+    int o0, o1, o2;  // Q4_K: the row's block; Q6_K: [A | B | H] record, scale record, d (as LaneRow)
+    int k0;          // the chunk's first input, relative to the slice
+    int col;         // the column this lane stores
+    bool store;
+};
+template <int QT>
+__device__ __forceinline__ BmLane bm_lane(int lg, int warp, int lane, int nm) {
+    BmLane L;
+    L.lg = lg;
+    const int rpw = 32 >> lg, kbl = (1 << lg) >> 2;
+    L.rl = warp * rpw + (lane >> lg);
+    L.j = lane & ((1 << lg) - 1);
+    int bl;
+    lane_chunk<QT>(L.j, lg, bl, L.q);
+    if constexpr (QT == QT_Q4K) {
+        L.o0 = ((L.rl >> 3) * kbl + bl) * group_block_bytes(QT) + (L.rl & 7) * 144;
+        L.o1 = L.o2 = 0;
+        L.k0 = 256 * bl + 64 * L.q;
+    } else {
+        const int base = ((L.rl >> 3) * kbl + bl) * group_block_bytes(QT), rr = L.rl & 7, u = 4 * rr + L.q;
+        L.o0 = base + 48 * u;
+        L.o1 = base + 1536 + 4 * u;
+        L.o2 = base + 1664 + 2 * rr;
+        L.k0 = 256 * bl + 128 * (L.q >> 1) + 16 * (L.q & 1);
+    }
+    L.col = L.j >> (lg - 2);
+    L.store = (L.j & ((1 << (lg - 2)) - 1)) == 0 && L.col < nm;
+    return L;
+}
+
+// Where a row's slice sums go: output part Yp (token-major Y[t][ldy] or,
+// ROW_MAJOR, Y[row][ldy]), or (AM, the argmax mode) the CTA's row sums ys
+// [row - r0][4] in shared memory, added over the slices in slice order.
+struct BmOut {
+    float* Yp;
+    int ldy;
+    float* ys;
+    int r0;
+    bool first;
+};
+template <bool ROW_MAJOR, bool AM>
+__device__ __forceinline__ void bm_put(const BmLane& L, float v, int row, int rb, const BmOut& o) {
+    if (L.store && row < rb) {
+        if (AM) {
+            float* y = o.ys + 4 * (row - o.r0) + L.col;
+            *y = o.first ? v : *y + v;
+        } else if (ROW_MAJOR) {
+            o.Yp[static_cast<size_t>(row) * o.ldy + L.col] = v;
         } else {
-            // weight lane + 32 i = 128 hh + 32 s + 16 p + idx: byte idx of record (rr, 2 hh + p), scale s
-            const int pp = lane >> 4, idx = lane & 15;
-            const float d = f16_to_f32(ld16(gb + 1664 + 2 * rr));
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int u = 4 * rr + 2 * hh + pp;
-                const uint8_t* rec = gb + 48 * u;
-                const int a = rec[idx], bq = rec[16 + idx], hb = rec[32 + idx];
-                const uint32_t sw = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
-#pragma unroll
-                for (int sidx = 0; sidx < 4; ++sidx) {
-                    const int nib = ((sidx & 1) ? bq : a) >> (4 * (sidx >> 1)) & 15;
-                    const int code = nib | (((hb >> (2 * sidx)) & 3) << 4);
-                    const float ds = d * static_cast<float>(static_cast<int8_t>((sw >> (8 * sidx)) & 0xffu));
-                    w[4 * hh + sidx] = ds * static_cast<float>(code - 32);
-                }
-            }
-        }
-        const float4* xb = xs4 + 256 * b + lane;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 xv = __ldg(xb + 32 * i);
-            acc[0] = fmaf(w[i], xv.x, acc[0]);
-            acc[1] = fmaf(w[i], xv.y, acc[1]);
-            acc[2] = fmaf(w[i], xv.z, acc[2]);
-            acc[3] = fmaf(w[i], xv.w, acc[3]);
+            o.Yp[static_cast<size_t>(L.col) * o.ldy + row] = v;
         }
     }
 }
 
-template <int QT, bool ROW_MAJOR>
-__global__ void __launch_bounds__(512) bm_gemv_kernel(const uint8_t* __restrict__ W, int n, int k,
-                                                      const float* __restrict__ X, float* __restrict__ Y, int ldy,
-                                                      int nm) {
-    __shared__ float red[16][4];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float4* __restrict__ xs4 = reinterpret_cast<const float4*>(X);
-    const int nb = k / 256, n8 = (n + 7) & ~7;
-    const int gi = blockIdx.x, rr = warp & 7, half = warp >> 3;
-    {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        bm_row_acc<QT>(W, n8, nb, gi, rr, half, lane, xs4, acc);
+// NP Q4_K row passes of a stage (the first at ps), rows row, row + U, ...
+template <int NP, bool ROW_MAJOR, bool AM>
+__device__ void bm_q4_passes(const BmLane& L, const uint8_t* ps, const float4* xs, const float4* xsum, int row, int U,
+                             int rb, const BmOut& o) {
+    constexpr int PB = kStageBlockRows * 144;
+    float4 s0[NP], s1[NP];
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) acc[mm] = warp_sum(acc[mm]);
-        if (lane < 4) red[warp][lane] = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+    for (int t = 0; t < NP; ++t) {
+        s0[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        s1[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
-    if (tid < 32) {
-        const int r = tid >> 2, mm = tid & 3, row = 8 * gi + r;
-        if (row < n && mm < nm) {
-            const float v = red[r][mm] + red[r + 8][mm];
-            if (ROW_MAJOR) Y[static_cast<size_t>(row) * ldy + mm] = v;
-            else Y[static_cast<size_t>(mm) * ldy + row] = v;
+    const float4* xc = xs + xs_at(L.k0);  // the chunk's 64 inputs, contiguous
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {  // bytes 16h .. 16h + 15 of the chunk's 32
+        uint4 cw[NP];
+#pragma unroll
+        for (int t = 0; t < NP; ++t) cw[t] = *reinterpret_cast<const uint4*>(ps + t * PB + L.o0 + 16 + 32 * L.q + 16 * h);
+        const float4* xb = xc + 16 * h;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // byte i: low nibble -> input k0 + 16h + i, high -> k0 + 32 + 16h + i
+            const float4 xl = xb[i], xh = xb[32 + i];
+#pragma unroll
+            for (int t = 0; t < NP; ++t) {
+                unsigned v = u4w(cw[t], i >> 2);
+                switch (i & 3) {
+                    case 0: v = byte_to<0, 15>(v); break;
+                    case 1: v = byte_to<1, 15>(v); break;
+                    case 2: v = byte_to<2, 15>(v); break;
+                    default: v = byte_to<3, 15>(v); break;
+                }
+                fma4(s0[t], one_plus(v, 0x00078000u), xl);  // 1 + q / 256
+                fma4(s1[t], one_plus(v, 0x00780000u), xh);  // 1 + q / 16
+            }
         }
     }
+    const float4 X0 = xsum[L.k0 >> 5], X1 = xsum[(L.k0 >> 5) + 1];
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+        const uint4 hdr = *reinterpret_cast<const uint4*>(ps + t * PB + L.o0);
+        const float d = f16_to_f32(static_cast<uint16_t>(hdr.x & 0xffffu));
+        const float dmin = f16_to_f32(static_cast<uint16_t>(hdr.x >> 16));
+        // 6-bit scale / min of sub-blocks 2q (low nibbles) and 2q + 1 (high), as dot_q4k takes them
+        int sc[2], mn[2];
+        const bool low = L.q < 2;
+        const unsigned asc = low ? hdr.y : hdr.w, amn = low ? hdr.z : hdr.w;
+        const unsigned msk = low ? 63u : 15u, mhi = low ? 0u : 0x30u, sm4 = low ? 0u : 4u;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const unsigned sh8 = 16u * static_cast<unsigned>(L.q & 1) + 8u * u;
+            sc[u] = static_cast<int>(((asc >> sh8) & msk) | ((hdr.y >> (sh8 + 2u)) & mhi));
+            mn[u] = static_cast<int>(((amn >> (sh8 + sm4)) & msk) | ((hdr.z >> (sh8 + 2u)) & mhi));
+        }
+        const float a0 = 256.0f * d * static_cast<float>(sc[0]), a1 = 16.0f * d * static_cast<float>(sc[1]);
+        const float b0 = dmin * static_cast<float>(mn[0]), b1 = dmin * static_cast<float>(mn[1]);
+        float4 acc;
+        acc.x = fmaf(a0, s0[t].x - X0.x, fmaf(a1, s1[t].x - X1.x, -fmaf(b0, X0.x, b1 * X1.x)));
+        acc.y = fmaf(a0, s0[t].y - X0.y, fmaf(a1, s1[t].y - X1.y, -fmaf(b0, X0.y, b1 * X1.y)));
+        acc.z = fmaf(a0, s0[t].z - X0.z, fmaf(a1, s1[t].z - X1.z, -fmaf(b0, X0.z, b1 * X1.z)));
+        acc.w = fmaf(a0, s0[t].w - X0.w, fmaf(a1, s1[t].w - X1.w, -fmaf(b0, X0.w, b1 * X1.w)));
+        bm_put<ROW_MAJOR, AM>(L, row_sum4(acc, L.lg, L.j), row + t * U, rb, o);
+    }
+}
+
+// NP Q6_K row passes (planar records): per 16-weight group s4 with int8 scale
+// sc, sc * (sum (c - 32) x) = sc * (64 (sum (1 + c/64) x - X) - 32 X), then d.
+template <int NP, bool ROW_MAJOR, bool AM>
+__device__ void bm_q6_passes(const BmLane& L, const uint8_t* ps, const float4* xs, const float4* xsum, int row, int U,
+                             int rb, const BmOut& o) {
+    constexpr int PB = kStageBlockRows * 210;
+    uint4 A[NP], B[NP], H[NP];
+    unsigned S[NP];
+    float4 acc[NP];
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+        const uint8_t* rec = ps + t * PB + L.o0;
+        A[t] = *reinterpret_cast<const uint4*>(rec);
+        B[t] = *reinterpret_cast<const uint4*>(rec + 16);
+        H[t] = *reinterpret_cast<const uint4*>(rec + 32);
+        S[t] = *reinterpret_cast<const unsigned*>(ps + t * PB + L.o1);
+        acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {  // group s4: inputs k0 + 32 s4 .. + 15
+        const int kk = L.k0 + 32 * s4;
+        const float4* xg = xs + xs_at(kk);  // the group's 16 inputs, contiguous
+        float4 sg[NP];
+#pragma unroll
+        for (int t = 0; t < NP; ++t) sg[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            unsigned c4[NP];  // the 4 codes of inputs 4w .. 4w + 3 of the group (dot_q6k's unpacking)
+#pragma unroll
+            for (int t = 0; t < NP; ++t) {
+                const unsigned a = u4w(A[t], w), bb = u4w(B[t], w), hh = u4w(H[t], w);
+                if (s4 == 0) c4[t] = (a & 0x0f0f0f0fu) | ((hh << 4) & 0x30303030u);
+                else if (s4 == 1) c4[t] = (bb & 0x0f0f0f0fu) | ((hh << 2) & 0x30303030u);
+                else if (s4 == 2) c4[t] = ((a >> 4) & 0x0f0f0f0fu) | (hh & 0x30303030u);
+                else c4[t] = ((bb >> 4) & 0x0f0f0f0fu) | ((hh >> 2) & 0x30303030u);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int i = 4 * w + b;
+                const float4 x = xg[i];
+#pragma unroll
+                for (int t = 0; t < NP; ++t) {
+                    unsigned v;
+                    switch (b) {
+                        case 0: v = byte_to<0, 17>(c4[t]); break;
+                        case 1: v = byte_to<1, 17>(c4[t]); break;
+                        case 2: v = byte_to<2, 17>(c4[t]); break;
+                        default: v = byte_to<3, 17>(c4[t]); break;
+                    }
+                    fma4(sg[t], one_plus(v, 0x007E0000u), x);  // 1 + c / 64
+                }
+            }
+        }
+        const float4 X = xsum[kk >> 4];
+        const float4 m32 = make_float4(-32.0f * X.x, -32.0f * X.y, -32.0f * X.z, -32.0f * X.w);
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
+            const float sc = static_cast<float>(static_cast<int>(S[t] << (24 - 8 * s4)) >> 24);
+            acc[t].x = fmaf(sc, fmaf(64.0f, sg[t].x - X.x, m32.x), acc[t].x);
+            acc[t].y = fmaf(sc, fmaf(64.0f, sg[t].y - X.y, m32.y), acc[t].y);
+            acc[t].z = fmaf(sc, fmaf(64.0f, sg[t].z - X.z, m32.z), acc[t].z);
+            acc[t].w = fmaf(sc, fmaf(64.0f, sg[t].w - X.w, m32.w), acc[t].w);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+        const float d = f16_to_f32(*reinterpret_cast<const uint16_t*>(ps + t * PB + L.o2));
+        const float4 v = make_float4(d * acc[t].x, d * acc[t].y, d * acc[t].z, d * acc[t].w);
+        bm_put<ROW_MAJOR, AM>(L, row_sum4(v, L.lg, L.j), row + t * U, rb, o);
+    }
+}
+
+// Rows [ra, rb) of one slice (2^lg lanes per row), stage by stage.
+template <int QT, bool ROW_MAJOR, bool AM>
+__device__ void bm4_slice(Pipe& p, int lg, int ra, int rb, const float4* xs, const float4* xsum, const BmOut& o, int nm,
+                          int warp, int lane) {
+    constexpr int PP = BmPasses<QT>::value;
+    constexpr int PB = kStageBlockRows * block_bytes(QT);
+    const BmLane L = bm_lane<QT>(lg, warp, lane, nm);
+    const int U = 8 * (32 >> lg);
+    for (int row0 = ra; row0 < rb; row0 += U * PP) {
+        const int npass = min(PP, (rb - row0 + U - 1) / U);  // uniform over the CTA
+        p.wait_full();
+        const uint8_t* ps = p.cur();
+        const int row = row0 + L.rl;
+        if constexpr (QT == QT_Q4K) {
+            if (npass == 3) bm_q4_passes<3, ROW_MAJOR, AM>(L, ps, xs, xsum, row, U, rb, o);
+            else if (npass == 2) bm_q4_passes<2, ROW_MAJOR, AM>(L, ps, xs, xsum, row, U, rb, o);
+            else bm_q4_passes<1, ROW_MAJOR, AM>(L, ps, xs, xsum, row, U, rb, o);
+        } else {
+            if (npass == 2) bm_q6_passes<2, ROW_MAJOR, AM>(L, ps, xs, xsum, row, U, rb, o);
+            else bm_q6_passes<1, ROW_MAJOR, AM>(L, ps, xs, xsum, row, U, rb, o);
+        }
+        p.release();
+    }
+}
+
+// First task (slice-major index s * units + g) that starts at or after weight
+// position pos, a task of slice s weighing 2^lg_s.
+__device__ int bm_task_at(const GemvShape& sh, long long pos) {
+    long long c = 0;
+    for (int s = 0; s < sh.nsl; ++s) {
+        const int lg = sh.sl_lg[s];
+        const long long span = static_cast<long long>(sh.units) << lg;
+        if (pos < c + span) return s * sh.units + static_cast<int>((pos - c + (1LL << lg) - 1) >> lg);
+        c += span;
+    }
+    return sh.nsl * sh.units;
+}
+
+// The CTA's work as a walk over (slice s, rows [ra, rb)) segments.  Parts
+// mode: its range of tasks, a run of consecutive groups of one slice per
+// segment.  AM: its own rows (whole 8-row groups) in every slice, slice by slice.
+template <bool AM>
+struct BmWalk {
+    int it, end, r0, r1;
+    __device__ explicit BmWalk(const GemvShape& sh) {
+        if (AM) {
+            cta_rows(sh.units, sh.n, r0, r1);
+            it = 0;
+            end = sh.nsl;
+        } else {
+            long long tot = 0;
+            for (int s = 0; s < sh.nsl; ++s) tot += static_cast<long long>(sh.units) << sh.sl_lg[s];
+            it = bm_task_at(sh, tot * blockIdx.x / gridDim.x);
+            end = bm_task_at(sh, tot * (blockIdx.x + 1) / gridDim.x);
+            r0 = r1 = 0;
+        }
+    }
+    __device__ bool next(const GemvShape& sh, int& s, int& ra, int& rb) {
+        if (it >= end) return false;
+        if (AM) {
+            s = it++;
+            ra = r0;
+            rb = r1;
+        } else {
+            s = it / sh.units;
+            const int g = it - s * sh.units, ge = min(sh.units, g + (end - it));
+            ra = 8 * g;
+            rb = min(8 * ge, sh.n);
+            it += ge - g;
+        }
+        return true;
+    }
+};
+
+// The producer warp: the CTA's segments in order, each in stages of PP passes
+// (one contiguous piece of the grouped layout per stage).
+template <int QT, bool AM>
+__device__ bool bm_produce(Pipe& p, const GemvShape& sh) {
+    constexpr int GB = group_block_bytes(QT), PP = BmPasses<QT>::value;
+    BmWalk<AM> wk(sh);
+    int s, ra, rb;
+    while (wk.next(sh, s, ra, rb)) {
+        const int lg = sh.sl_lg[s], kbl = (1 << lg) >> 2, U = 8 * (32 >> lg) * PP, b0 = sh.sl_c0[s] >> 2;
+        for (int row0 = ra; row0 < rb; row0 += U) {
+            const int rows = min(U, rb - row0);
+            if (!p.acquire()) return false;
+            const unsigned bytes = static_cast<unsigned>((rows + 7) >> 3) * kbl * GB;
+            p.expect(bytes);
+            if (p.lane == 0)
+                p.copy(p.cur(), sh.w0 + (static_cast<size_t>(sh.n8 / 8) * b0 + static_cast<size_t>(row0 >> 3) * kbl) * GB,
+                       bytes);
+            p.commit();
+        }
+    }
+    return true;
+}
+
+// Per column c < nm of the argmax mode: the sequence's first-index argmax
+// word (two u64: key, arrival count; zero between launches), its token slots
+// (slots[0] = token, slots[2] = token | bit 31 when an error word is set), its
+// allow bitset and error word.
+struct BmArgmax {
+    unsigned long long* ws[4];
+    int* slots[4];
+    const uint32_t* allow[4];
+    const unsigned* err[4];
+};
+
+// Parts mode: output part s (slice s) at Y + s * split_stride, Y[t][ldy]
+// (token-major) or, ROW_MAJOR, Y[row][ldy]; columns >= nm are not stored.
+// AM: the rows' full sums stay in shared memory (ys at ys_off) and each column
+// ends in a masked first-index argmax over all rows (the lm_head of up to 4
+// sequences: EpiArgmaxStep's key and last-arriver protocol per column).
+template <int QT, bool ROW_MAJOR, bool AM>
+__global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, const float* __restrict__ X,
+                                                          float* __restrict__ Y, int ldy, size_t split_stride, int nm,
+                                                          int ring_off, const BmArgmax am) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    float4* xs = reinterpret_cast<float4*>(smem + 16 * kMaxStages);  // [kBmXs]
+    float4* xsum = xs + kBmXs;                                        // [kBmSliceK / 16]: sums of 32 (Q4_K) or 16 inputs
+    float* ys = reinterpret_cast<float*>(xsum + kBmSliceK / 16);     // AM: [rows_cta][4]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int st = 0; st < sh.stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Pipe p{full, empty, smem + ring_off, sh.stages, BmPasses<QT>::value * stage_bytes_of(QT), 0u, sh.err, sh.err, lane,
+           0ull};
+    if (warp == kConsumerWarps) {  // the weights depend on no earlier kernel: they stream in before the wait
+        p.pol = policy_evict_first();
+        if (!bm_produce<QT, AM>(p, sh)) p.drain();
+        return;
+    }
+    pdl_wait();  // X (and the output parts this launch overwrites) belong to the earlier kernels
+    const float4* X4 = reinterpret_cast<const float4*>(X);
+    constexpr int SL = QT == QT_Q4K ? 32 : 16;  // inputs per sub-block sum
+    BmWalk<AM> wk(sh);
+    int s, ra, rb;
+    while (wk.next(sh, s, ra, rb)) {
+        const int lg = sh.sl_lg[s], kn = 64 << lg, kb = 64 * sh.sl_c0[s];
+        // the slice's inputs, four loads in flight per thread (kn is a multiple of kConsumers)
+        for (int i0 = 0; i0 < kn; i0 += 4 * kConsumers) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * kConsumers < kn) v[u] = __ldg(X4 + kb + i0 + u * kConsumers + tid);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * kConsumers < kn) xs[xs_at(i0 + u * kConsumers + tid)] = v[u];
+        }
+        bar_sync(1, kConsumers);
+        for (int e = tid; e < 4 * (kn / SL); e += kConsumers) {  // (sub-block, column) sums
+            const int sb = e >> 2, c = e & 3;
+            float a = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < SL; ++i) a += reinterpret_cast<const float*>(xs + xs_at(SL * sb + i))[c];
+            reinterpret_cast<float*>(xsum)[e] = a;
+        }
+        bar_sync(1, kConsumers);
+        const BmOut o{Y + s * split_stride, ldy, ys, wk.r0, s == 0};
+        bm4_slice<QT, ROW_MAJOR, AM>(p, lg, ra, rb, xs, xsum, o, nm, warp, lane);
+        bar_sync(1, kConsumers);  // xs, xsum (and AM: the slice's row sums) are complete
+    }
+    if constexpr (AM) {
+        unsigned long long best[4] = {0ull, 0ull, 0ull, 0ull};
+        for (int r = wk.r0 + tid; r < wk.r1; r += kConsumers) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c < nm) {
+                    const bool ok = (__ldcg(am.allow[c] + (r >> 5)) >> (r & 31)) & 1u;
+                    const unsigned long long key =
+                        argmax_key(ok ? ys[4 * (r - wk.r0) + c] : -FLT_MAX, static_cast<unsigned>(r));
+                    best[c] = key > best[c] ? key : best[c];
+                }
+            }
+        }
+        unsigned long long* red = reinterpret_cast<unsigned long long*>(xsum);  // [warp][4]
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            best[c] = warp_max_u64(best[c]);
+            if (lane == 0) red[4 * warp + c] = best[c];
+        }
+        bar_sync(1, kConsumers);
+        if (tid < nm) {
+            const int c = tid;
+            unsigned long long m = 0ull;
+            for (int w = 0; w < kConsumerWarps; ++w) m = red[4 * w + c] > m ? red[4 * w + c] : m;
+            atomicMax(am.ws[c], m);
+            __threadfence();
+            const unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(am.ws[c] + 1), 1u);
+            if (prev == gridDim.x - 1) {  // the last CTA for this column publishes
+                __threadfence();
+                const unsigned long long key = atomicExch(am.ws[c], 0ull);
+                atomicExch(reinterpret_cast<unsigned*>(am.ws[c] + 1), 0u);
+                const unsigned tok = key ? argmax_key_index(key) : 0u;
+                const unsigned e = __ldcg(am.err[c]) | __ldcg(sh.err);
+                am.slots[c][0] = static_cast<int>(tok);
+                am.slots[c][2] = static_cast<int>(tok | (e ? 0x80000000u : 0u));
+            }
+        }
+    }
+}
+
+// Launch of bm4_kernel over nm <= 4 columns.  Parts mode: *parts = the K
+// slices (output parts, split_stride apart).  AM: the argmax words of am.
+// err: the device error word of the bounded ring waits.
+template <int QT, bool ROW_MAJOR, bool AM>
+int launch_bm4(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, size_t split_stride, int nm,
+               const BmArgmax& am, unsigned* err, cudaStream_t st, int* parts) {
+    if (!err) return set_err(QG_ERR_CUDA, "small-batch GEMV: no device error word");
+    if (nm < 1 || nm > 4) return set_err(QG_ERR_SHAPE, "small-batch GEMV: %d columns (served: 1..4)", nm);
+    constexpr int PP = BmPasses<QT>::value;
+    int grid = 1;
+    GemvShape sh = gemv_geometry(QT, false, W, nullptr, n, k, 0, 0, err, &grid, PP);  // AM: whole row groups per CTA
+    if (sh.nsl > kPfMaxSplit) return set_err(QG_ERR_SHAPE, "small-batch GEMV: k = %d has %d slices", k, sh.nsl);
+    sh.pp = PP;
+    if (!AM) grid = static_cast<int>(std::min<long long>(2LL * device_sms(), static_cast<long long>(sh.units) * sh.nsl));
+    const int ys_bytes = AM ? 16 * sh.rows_cta : 0;
+    const int ring_off = (16 * kMaxStages + 16 * kBmXs + 16 * (kBmSliceK / 16) + ys_bytes + 127) & ~127;
+    const int slot = PP * stage_bytes_of(QT);
+    int stages = (kCtaSmemBytes - ring_off) / slot;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return set_err(QG_ERR_SHAPE, "small-batch GEMV: %d x %d leaves no ring in shared memory", n, k);
+    sh.stages = stages;
+    const int smem = ring_off + stages * slot;
+    auto kern = bm4_kernel<QT, ROW_MAJOR, AM>;
+    if (int rc = grant_smem(reinterpret_cast<const void*>(kern), smem)) return rc;
+    if (int e_ = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, true, sh, X, Y, ldy, split_stride, nm, ring_off,
+                            am))
+        return e_;
+    if (parts) *parts = sh.nsl;
+    return QG_OK;
 }
 
 // Z = the `parts` split sums of a projection, added in split order.
 __global__ void pf_sum_parts_kernel(const float* __restrict__ Yp, int parts, size_t stride, float* __restrict__ Z,
                                     size_t count) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= count) return;
     float v = Yp[i];
@@ -353,29 +759,73 @@ __global__ void pf_sum_parts_kernel(const float* __restrict__ Yp, int parts, siz
 
 // X[p] = E[tok[p]].  Grid P.
 __global__ void pf_embed_kernel(const float* __restrict__ E, const int* __restrict__ tok, int H, float* __restrict__ X) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const int p = blockIdx.x;
     const float* src = E + static_cast<size_t>(tok[p]) * H;
     for (int i = threadIdx.x; i < H; i += blockDim.x) X[static_cast<size_t>(p) * H + i] = src[i];
 }
 
+// Per column of a batched decode pass, where the final residual stream is
+// also stored (each sequence's state), or null.
+struct HOut {
+    float* h[kMaxSeg];
+};
+
 // X[p] += the `parts` split sums (in split order); then, when w is given,
-// RMSNorm(X[p]) * w into column p of the k-major Xn[H][ldn].  Grid P.
-__global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts,
-                                                          size_t split_stride, const float* __restrict__ w,
-                                                          float* __restrict__ Xn, int ldn, int H, float eps) {
-    __shared__ float red[8];
+// RMSNorm(X[p]) * w into column p of the k-major Xn[H][ldn]; with ho.h[p],
+// X[p] is also stored there.  Grid P, 1024 threads, each holding the
+// elements tid + 1024 e (H <= 16384): every load of a thread is issued before
+// the first sum needs one.
+constexpr int kAddNormThreads = 1024, kAddNormPer = 16;
+__global__ void __launch_bounds__(kAddNormThreads) pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp,
+                                                                      int parts, size_t split_stride,
+                                                                      const float* __restrict__ w, float* __restrict__ Xn,
+                                                                      int ldn, int H, float eps, const HOut ho) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
+    __shared__ float red[kAddNormThreads / 32];
     const int p = blockIdx.x, tid = threadIdx.x;
     float* x = X + static_cast<size_t>(p) * H;
-    float ss = 0.0f;
-    for (int i = tid; i < H; i += 256) {
-        float v = x[i];
-        if (parts > 0) {
-            float y = Yp[static_cast<size_t>(p) * H + i];
-            for (int z = 1; z < parts; ++z) y += Yp[z * split_stride + static_cast<size_t>(p) * H + i];
-            v += y;
-            x[i] = v;
+    const float* yp = Yp + static_cast<size_t>(p) * H;
+    float* hp = p < kMaxSeg ? ho.h[p] : nullptr;
+    float v[kAddNormPer];
+#pragma unroll
+    for (int e = 0; e < kAddNormPer; ++e) {
+        const int i = tid + kAddNormThreads * e;
+        v[e] = i < H ? x[i] : 0.0f;
+    }
+    if (parts > 0) {
+        float y[kAddNormPer];
+#pragma unroll
+        for (int e = 0; e < kAddNormPer; ++e) {
+            const int i = tid + kAddNormThreads * e;
+            y[e] = i < H ? yp[i] : 0.0f;
         }
-        ss = fmaf(v, v, ss);
+        for (int z = 1; z < parts; ++z) {
+#pragma unroll
+            for (int e = 0; e < kAddNormPer; ++e) {
+                const int i = tid + kAddNormThreads * e;
+                if (i < H) y[e] += yp[z * split_stride + i];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kAddNormPer; ++e) {
+            const int i = tid + kAddNormThreads * e;
+            if (i < H) {
+                v[e] += y[e];
+                x[i] = v[e];
+            }
+        }
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kAddNormPer; ++e) {
+        const int i = tid + kAddNormThreads * e;
+        if (i < H) {
+            ss = fmaf(v[e], v[e], ss);
+            if (hp) hp[i] = v[e];
+        }
     }
     if (!w) return;
     ss = warp_sum(ss);
@@ -383,9 +833,13 @@ __global__ void __launch_bounds__(256) pf_add_norm_kernel(float* __restrict__ X,
     __syncthreads();
     float t = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += red[i];
+    for (int i = 0; i < kAddNormThreads / 32; ++i) t += red[i];
     const float r = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
-    for (int i = tid; i < H; i += 256) Xn[static_cast<size_t>(i) * ldn + p] = (x[i] * r) * w[i];
+#pragma unroll
+    for (int e = 0; e < kAddNormPer; ++e) {
+        const int i = tid + kAddNormThreads * e;
+        if (i < H) Xn[static_cast<size_t>(i) * ldn + p] = (v[e] * r) * w[i];
+    }
 }
 
 // Causal conv1d + SiLU of the qkv rows and the alpha/beta gates, one thread
@@ -397,6 +851,8 @@ __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P
                                      const Segs sg, const float* __restrict__ wconv,
                                      const float* __restrict__ dt_bias, const float* __restrict__ a,
                                      float* __restrict__ Cq, float* __restrict__ dt, float* __restrict__ beta) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int W = C + nv;
     if (idx >= static_cast<long long>(P) * W) return;
@@ -425,6 +881,8 @@ __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P
 // first (from the old window where the segment is shorter than that).  Grid
 // (rows / 256, segments).
 __global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int C, int K, const Segs sg) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const int c = blockIdx.x * blockDim.x + threadIdx.x, s = blockIdx.y;
     if (c >= C) return;
     const int c0 = sg.col0[s], P = sg.col0[s + 1] - c0;
@@ -441,6 +899,8 @@ __global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int 
 // (token, q|k, key head); QKn [P][2][nk][128].
 __global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, int nk, int P, float eps,
                                  float* __restrict__ QKn) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (wid >= P * 2 * nk) return;
     const int p = wid / (2 * nk), r = wid - p * 2 * nk, which = r / nk, kh = r - which * nk;
@@ -467,6 +927,8 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
                                                        const float* __restrict__ dt_all,
                                                        const float* __restrict__ beta_all, const Segs sgs,
                                                        float* __restrict__ O_all, int nk, int nv, int dv) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     // segment blockIdx.y: its columns c0.. and its recurrent state
     const int c0 = sgs.col0[blockIdx.y], P = sgs.col0[blockIdx.y + 1] - c0;
     float* __restrict__ S = sgs.ssm[blockIdx.y];
@@ -553,27 +1015,29 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
 }
 
 // Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h), into column
-// p of the k-major U[v_dim][ldu].  Grid P, one warp per head (head_v_dim
-// 32/64/128: 1, 2 or 4 values per lane).
+// p of the k-major U[v_dim][ldu].  Grid (P, ceil(nv / 8)), one warp per head
+// (head_v_dim 32/64/128: 1, 2 or 4 values per lane).
 __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restrict__ O, const float* __restrict__ Z,
                                                             int ldz, int zoff, const float* __restrict__ w, int nv,
                                                             int dv, float eps, float* __restrict__ U, int ldu) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const int p = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per = dv / 32;
-    for (int h = warp; h < nv; h += 8) {
-        const float* o = O + static_cast<size_t>(p) * nv * dv + h * dv;
-        const float* z = Z + static_cast<size_t>(p) * ldz + zoff + h * dv;
-        float ov[4], ss = 0.0f;
-        for (int e = 0; e < per; ++e) {
-            ov[e] = o[lane + 32 * e];
-            ss = fmaf(ov[e], ov[e], ss);
-        }
-        ss = warp_sum(ss);
-        const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
-        for (int e = 0; e < per; ++e) {
-            const int i = lane + 32 * e;
-            U[static_cast<size_t>(h * dv + i) * ldu + p] = ((ov[e] * rn) * w[i]) * silu(z[i]);
-        }
+    const int h = 8 * blockIdx.y + warp;
+    if (h >= nv) return;
+    const float* o = O + static_cast<size_t>(p) * nv * dv + h * dv;
+    const float* z = Z + static_cast<size_t>(p) * ldz + zoff + h * dv;
+    float ov[4], ss = 0.0f;
+    for (int e = 0; e < per; ++e) {
+        ov[e] = o[lane + 32 * e];
+        ss = fmaf(ov[e], ov[e], ss);
+    }
+    ss = warp_sum(ss);
+    const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
+    for (int e = 0; e < per; ++e) {
+        const int i = lane + 32 * e;
+        U[static_cast<size_t>(h * dv + i) * ldu + p] = ((ov[e] * rn) * w[i]) * silu(z[i]);
     }
 }
 
@@ -585,6 +1049,8 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
                                                            const float* __restrict__ k_norm, const Segs sg, int n_rot,
                                                            float theta_scale, float eps, float* __restrict__ Qn,
                                                            float* __restrict__ Kst, float* __restrict__ Vst) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     __shared__ float cs[kHd / 2], sn[kHd / 2];
     __shared__ __align__(16) float vec[8][kHd];
     const int p = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -643,6 +1109,8 @@ template <int GS, bool KVQ>
 __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
                                                              int ldz, const Segs sg, int kvd,
                                                              float* __restrict__ Att, int lda) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     __shared__ float wml[8][GS][2];
     __shared__ __align__(16) float wacc[8][GS][kHd];
     const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -715,6 +1183,8 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
 // arrays, G and U given as split sums (added in order).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
                                  size_t stride, float* __restrict__ A, int ffn, int P, int ldk) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= static_cast<size_t>(ffn) * P) return;
     const size_t i = (e / P) * ldk + (e % P);
@@ -782,12 +1252,13 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
 // per split (split stride n * ldy), else Y[token][ldy] (split stride P * ldy).
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
-         int* used_splits) {
-    if (P <= 4) {  // a batched decode step: the small-batch GEMV over packed [k][4] inputs
-        if (used_splits) *used_splits = 1;
-        bm_gemv_kernel<QT, ROW_MAJOR><<<(n + 7) / 8, 512, 0, st>>>(W, n, k, X, Y, ldy, P);
-        QG_CUDA(cudaGetLastError());
-        return QG_OK;
+         int* used_splits, unsigned* err) {
+    if (P <= 4) {  // a batched decode step: the small-batch GEMV over packed [k][4] inputs, one part per K slice
+        const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
+        int parts = 1;
+        const int rc = launch_bm4<QT, ROW_MAJOR, false>(W, n, k, X, Y, ldy, split_stride, P, BmArgmax{}, err, st, &parts);
+        if (used_splits) *used_splits = parts;
+        return rc;
     }
     const int nq = k / 64;
     if (splits > nq) splits = nq;
@@ -799,8 +1270,9 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     if (int rc = grant_smem(reinterpret_cast<const void*>(pf_gemm_kernel<QT, ROW_MAJOR>), smem)) return rc;
     const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
     const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
-    pf_gemm_kernel<QT, ROW_MAJOR><<<grid, 256, smem, st>>>(W, n, k, X, kPfChunk, Y, ldy, split_stride, P, per);
-    QG_CUDA(cudaGetLastError());
+    if (int e_ = launch_pdl(pf_gemm_kernel<QT, ROW_MAJOR>, dim3(grid), dim3(256), smem, st, true, W, n, k, X, kPfChunk,
+                            Y, ldy, split_stride, P, per))
+        return e_;
     return QG_OK;
 }
 
@@ -815,13 +1287,14 @@ template <bool KVQ>
 int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const Segs& sg, int kvd,
                   float* att, int ldk) {
     switch (gs) {
-        case 1: pf_causal_attn_kernel<1, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
-        case 2: pf_causal_attn_kernel<2, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
-        case 4: pf_causal_attn_kernel<4, KVQ><<<grid, 256, 0, st>>>(Qn, Z, ldz, sg, kvd, att, ldk); break;
+        case 1: return launch_pdl(pf_causal_attn_kernel<1, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
+                                  ldk);
+        case 2: return launch_pdl(pf_causal_attn_kernel<2, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
+                                  ldk);
+        case 4: return launch_pdl(pf_causal_attn_kernel<4, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
+                                  ldk);
         default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
     }
-    QG_CUDA(cudaGetLastError());
-    return QG_OK;
 }
 
 // One pass of columns through every layer: segment i is sequence ss[i]'s
@@ -850,57 +1323,65 @@ Segs segs_of(const Pass& ps, int il) {
     return sg;
 }
 
-int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
+// lm: the pass ends in the output norm of its (at most 4) columns for
+// run_lmhead_batch, each column's stream stored to its state.
+int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bool lm = false) {
     const qg_config& c = m->cfg;
     const int H = c.hidden, P = ps.col0[ps.n];
     const int ldk = P <= 4 ? 4 : kPfChunk;  // stride of the k-major GEMM inputs (packed for the small batch)
     const size_t part = static_cast<size_t>(P) * H;
     const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
-    pf_embed_kernel<<<P, 256, 0, st>>>(m->embd, sc->tok, H, sc->X);
-    QG_CUDA(cudaGetLastError());
+    unsigned* err = ps.ss[0]->err;  // the small-batch GEMV's bounded waits report here
+    if (int e_ = launch_pdl(pf_embed_kernel, dim3(P), dim3(256), 0, st, true, m->embd, sc->tok, H, sc->X))
+        return e_;
     int pending = 0;  // split sums of the last projection not yet added to X
     int rc = QG_OK;
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
         const Segs sg = segs_of(ps, il);
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, ldk, H, c.eps);
-        QG_CUDA(cudaGetLastError());
+        if (int e_ = launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending,
+                                part, L.attn_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+            return e_;
         int zin = 1;
-        if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin)))
+        if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin,
+                                      err)))
             break;
         const float* Z = sc->Zp;  // the input projection's output [P][n_in]: one split is already the sum
         if (zin > 1) {
             const size_t cnt = static_cast<size_t>(P) * L.n_in;
-            pf_sum_parts_kernel<<<static_cast<unsigned>((cnt + 255) / 256), 256, 0, st>>>(sc->Zp, zin, cnt, sc->Z, cnt);
-            QG_CUDA(cudaGetLastError());
+            if (int e_ = launch_pdl(pf_sum_parts_kernel, dim3(static_cast<unsigned>((cnt + 255) / 256)), dim3(256), 0,
+                                    st, true, sc->Zp, zin, cnt, sc->Z, cnt))
+                return e_;
             Z = sc->Z;
         }
         int k_out;
         if (m->kinds[il] == QG_LAYER_DELTANET) {
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
             const long long cg = static_cast<long long>(P) * (C + nv);
-            pf_conv_gates_kernel<<<static_cast<unsigned>((cg + 255) / 256), 256, 0, st>>>(
-                Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta);
-            QG_CUDA(cudaGetLastError());
-            pf_conv_window_kernel<<<dim3((C + 255) / 256, ps.n), 256, 0, st>>>(Z, L.n_in, C, c.conv_kernel, sg);
-            QG_CUDA(cudaGetLastError());
+            if (int e_ = launch_pdl(pf_conv_gates_kernel, dim3(static_cast<unsigned>((cg + 255) / 256)), dim3(256), 0,
+                                    st, true, Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq,
+                                    sc->dt, sc->beta))
+                return e_;
+            if (int e_ = launch_pdl(pf_conv_window_kernel, dim3((C + 255) / 256, ps.n), dim3(256), 0, st, true, Z,
+                                    L.n_in, C, c.conv_kernel, sg))
+                return e_;
             const int warps = P * 2 * c.n_k_heads;
-            pf_l2norm_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(sc->Cq, C, m->k_dim, c.n_k_heads, P, c.eps,
-                                                                      sc->QKn);
-            QG_CUDA(cudaGetLastError());
-            pf_delta_kernel<<<dim3(nv * dv / 32, ps.n), 256, 0, st>>>(sc->Cq, C, m->k_dim, sc->QKn, sc->dt, sc->beta,
-                                                                     sg, sc->O, c.n_k_heads, nv, dv);
-            QG_CUDA(cudaGetLastError());
-            pf_gated_norm_kernel<<<P, 256, 0, st>>>(sc->O, Z, L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps,
-                                                    sc->Uin, ldk);
-            QG_CUDA(cudaGetLastError());
+            if (int e_ = launch_pdl(pf_l2norm_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, true, sc->Cq, C,
+                                    m->k_dim, c.n_k_heads, P, c.eps, sc->QKn))
+                return e_;
+            if (int e_ = launch_pdl(pf_delta_kernel, dim3(nv * dv / 32, ps.n), dim3(256), 0, st, true, sc->Cq, C,
+                                    m->k_dim, sc->QKn, sc->dt, sc->beta, sg, sc->O, c.n_k_heads, nv, dv))
+                return e_;
+            if (int e_ = launch_pdl(pf_gated_norm_kernel, dim3(P, (nv + 7) / 8), dim3(256), 0, st, true, sc->O, Z,
+                                    L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps, sc->Uin, ldk))
+                return e_;
             k_out = m->v_dim;
         } else {
             const int nkv = c.n_kv_heads, kvd = m->kv_dim;
-            pf_attn_prep_kernel<<<P, 256, 0, st>>>(Z, L.n_in, c.n_heads, nkv, L.q_norm, L.k_norm, sg, c.n_rot,
-                                                   m->theta_scale, c.eps, sc->Qn, kvq ? sc->Ks : nullptr,
-                                                   kvq ? sc->Vs : nullptr);
-            QG_CUDA(cudaGetLastError());
+            if (int e_ = launch_pdl(pf_attn_prep_kernel, dim3(P), dim3(256), 0, st, true, Z, L.n_in, c.n_heads, nkv,
+                                    L.q_norm, L.k_norm, sg, c.n_rot, m->theta_scale, c.eps, sc->Qn,
+                                    kvq ? sc->Ks : nullptr, kvq ? sc->Vs : nullptr))
+                return e_;
             for (int i = 0; kvq && i < ps.n && !rc; ++i) {
                 const qg_state* si = ps.ss[i];
                 const size_t off = static_cast<size_t>(ps.col0[i]) * kvd;
@@ -916,24 +1397,47 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
             if (rc) break;
             k_out = m->q_dim;
         }
-        if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending)))
+        if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending,
+                                      err)))
             break;
-        pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldk, H, c.eps);
-        QG_CUDA(cudaGetLastError());
+        if (int e_ = launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending,
+                                part, L.post_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+            return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
-        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg))) break;
-        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu))) break;
+        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
+        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
         const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
-        pf_swiglu_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, st>>>(
-            sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk);
-        QG_CUDA(cudaGetLastError());
-        rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending);
+        if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, true,
+                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk))
+            return e_;
+        rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
     }
     if (rc) return rc;
-    pf_add_norm_kernel<<<P, 256, 0, st>>>(sc->X, sc->Yp, pending, part, nullptr, nullptr, kPfChunk, H, c.eps);
-    QG_CUDA(cudaGetLastError());
-    return QG_OK;
+    if (lm) {  // batched lm_head next: the output norm of every column, each stream to its state
+        HOut ho{};
+        for (int i = 0; i < ps.n; ++i) ho.h[i] = ps.ss[i]->h;
+        return launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending, part,
+                          m->out_norm, sc->Xn, ldk, H, c.eps, ho);
+    }
+    return launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending, part,
+                      static_cast<const float*>(nullptr), static_cast<float*>(nullptr), kPfChunk, H, c.eps, HOut{});
+}
+
+// The lm_head argmax of every column of a batched pass (at most 4, after
+// run_pass with lm): one small-batch GEMV over the output-normed columns in
+// sc->Xn, each column's token into its sequence's slots, masked by its
+// sequence's allow bitset.
+int run_lmhead_batch(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
+    BmArgmax am{};
+    for (int i = 0; i < ps.n; ++i) {
+        am.ws[i] = ps.ss[i]->am_ws;
+        am.slots[i] = ps.ss[i]->slots;
+        am.allow[i] = ps.ss[i]->allow;
+        am.err[i] = ps.ss[i]->err;
+    }
+    return launch_bm4<QT_Q6K, false, true>(m->lm_head, m->cfg.vocab, m->cfg.hidden, sc->Xn, nullptr, 0, 0, ps.n, am,
+                                           ps.ss[0]->err, st, nullptr);
 }
 
 }  // namespace
@@ -1031,8 +1535,11 @@ extern "C" int qg_decode_batch(qg_model* m, qg_state* const* states, int n, cons
         ps.col0[i] = i;
     }
     ps.col0[n] = n;
-    rc = run_pass(m, ps, sc, st);
-    for (int i = 0; i < n && !rc; ++i) rc = run_lmhead_of(m, states[i], sc->X + static_cast<size_t>(i) * c.hidden, st);
+    const bool lm4 = n <= 4;  // one batched lm_head for up to 4 sequences
+    rc = run_pass(m, ps, sc, st, lm4);
+    if (!rc && lm4) rc = run_lmhead_batch(m, ps, sc, st);
+    for (int i = 0; i < n && !rc && !lm4; ++i)
+        rc = run_lmhead_of(m, states[i], sc->X + static_cast<size_t>(i) * c.hidden, st);
     if (rc) return rc;
     QG_CUDA(cudaStreamSynchronize(st));
     for (int i = 0; i < n; ++i) {
@@ -1154,8 +1661,10 @@ extern "C" int qg_batch_step(qg_batch* b, const uint32_t* tokens, const int* pos
             ps.col0[i] = i;
         }
         ps.col0[n] = n;
-        if (!rc) rc = run_pass(m, ps, sc, st);
-        for (int i = 0; i < n && !rc; ++i)
+        const bool lm4 = n <= 4;  // one batched lm_head for up to 4 sequences
+        if (!rc) rc = run_pass(m, ps, sc, st, lm4);
+        if (!rc && lm4) rc = run_lmhead_batch(m, ps, sc, st);
+        for (int i = 0; i < n && !rc && !lm4; ++i)
             rc = run_lmhead_of(m, b->ss[i], sc->X + static_cast<size_t>(i) * m->cfg.hidden, st);
         for (int i = 0; i < n && !rc; ++i) {
             e = cudaMemcpyAsync(b->pinned + 32 + i, b->ss[i]->slots + 2, sizeof(int), cudaMemcpyDeviceToHost, st);
