@@ -30,6 +30,7 @@ constexpr int kGT = 128;       // tokens per GEMM tile
 constexpr int kGK = 64;        // k per shared-memory stage (a quarter super-block)
 constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
 constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
+constexpr int kAttnSplits = 16; // key splits of a batched decode step's attention (up to 4 columns)
 
 // The columns of one pass split into segments: segment s is one sequence's
 // run of consecutive positions pos0[s].. in columns col0[s]..col0[s+1]-1, with
@@ -774,57 +775,73 @@ struct HOut {
 
 // X[p] += the `parts` split sums (in split order); then, when w is given,
 // RMSNorm(X[p]) * w into column p of the k-major Xn[H][ldn]; with ho.h[p],
-// X[p] is also stored there.  Grid P, 1024 threads, each holding the
-// elements tid + 1024 e (H <= 16384): every load of a thread is issued before
-// the first sum needs one.
-constexpr int kAddNormThreads = 1024, kAddNormPer = 16;
-__global__ void __launch_bounds__(kAddNormThreads) pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp,
-                                                                      int parts, size_t split_stride,
-                                                                      const float* __restrict__ w, float* __restrict__ Xn,
-                                                                      int ldn, int H, float eps, const HOut ho) {
+// X[p] is also stored there.  Grid P.  SMALL (a batched decode step, P <= 16):
+// 1024 threads, each holding the elements tid + 1024 e (H <= 16384), every
+// load issued before the first sum needs one; else (a prefill chunk) 256
+// threads striding over H, so that all P CTAs are resident at once.
+constexpr int kAddNormWide = 1024, kAddNormPer = 16;
+template <bool SMALL>
+__global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
+    pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts, size_t split_stride,
+                       const float* __restrict__ w, float* __restrict__ Xn, int ldn, int H, float eps, const HOut ho) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
-    __shared__ float red[kAddNormThreads / 32];
+    constexpr int T = SMALL ? kAddNormWide : 256;
+    __shared__ float red[T / 32];
     const int p = blockIdx.x, tid = threadIdx.x;
     float* x = X + static_cast<size_t>(p) * H;
     const float* yp = Yp + static_cast<size_t>(p) * H;
     float* hp = p < kMaxSeg ? ho.h[p] : nullptr;
-    float v[kAddNormPer];
-#pragma unroll
-    for (int e = 0; e < kAddNormPer; ++e) {
-        const int i = tid + kAddNormThreads * e;
-        v[e] = i < H ? x[i] : 0.0f;
-    }
-    if (parts > 0) {
-        float y[kAddNormPer];
+    float ss = 0.0f;
+    float v[SMALL ? kAddNormPer : 1];
+    if constexpr (SMALL) {
 #pragma unroll
         for (int e = 0; e < kAddNormPer; ++e) {
-            const int i = tid + kAddNormThreads * e;
-            y[e] = i < H ? yp[i] : 0.0f;
+            const int i = tid + T * e;
+            v[e] = i < H ? x[i] : 0.0f;
         }
-        for (int z = 1; z < parts; ++z) {
+        if (parts > 0) {
+            float y[kAddNormPer];
 #pragma unroll
             for (int e = 0; e < kAddNormPer; ++e) {
-                const int i = tid + kAddNormThreads * e;
-                if (i < H) y[e] += yp[z * split_stride + i];
+                const int i = tid + T * e;
+                y[e] = i < H ? yp[i] : 0.0f;
+            }
+            for (int z = 1; z < parts; ++z) {
+#pragma unroll
+                for (int e = 0; e < kAddNormPer; ++e) {
+                    const int i = tid + T * e;
+                    if (i < H) y[e] += yp[z * split_stride + i];
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < kAddNormPer; ++e) {
+                const int i = tid + T * e;
+                if (i < H) {
+                    v[e] += y[e];
+                    x[i] = v[e];
+                }
             }
         }
 #pragma unroll
         for (int e = 0; e < kAddNormPer; ++e) {
-            const int i = tid + kAddNormThreads * e;
+            const int i = tid + T * e;
             if (i < H) {
-                v[e] += y[e];
-                x[i] = v[e];
+                ss = fmaf(v[e], v[e], ss);
+                if (hp) hp[i] = v[e];
             }
         }
-    }
-    float ss = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kAddNormPer; ++e) {
-        const int i = tid + kAddNormThreads * e;
-        if (i < H) {
-            ss = fmaf(v[e], v[e], ss);
-            if (hp) hp[i] = v[e];
+    } else {
+        for (int i = tid; i < H; i += T) {
+            float u = x[i];
+            if (parts > 0) {
+                float y = yp[i];
+                for (int z = 1; z < parts; ++z) y += yp[z * split_stride + i];
+                u += y;
+                x[i] = u;
+            }
+            if (hp) hp[i] = u;
+            ss = fmaf(u, u, ss);
         }
     }
     if (!w) return;
@@ -833,13 +850,29 @@ __global__ void __launch_bounds__(kAddNormThreads) pf_add_norm_kernel(float* __r
     __syncthreads();
     float t = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kAddNormThreads / 32; ++i) t += red[i];
+    for (int i = 0; i < T / 32; ++i) t += red[i];
     const float r = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
+    if constexpr (SMALL) {
 #pragma unroll
-    for (int e = 0; e < kAddNormPer; ++e) {
-        const int i = tid + kAddNormThreads * e;
-        if (i < H) Xn[static_cast<size_t>(i) * ldn + p] = (v[e] * r) * w[i];
+        for (int e = 0; e < kAddNormPer; ++e) {
+            const int i = tid + T * e;
+            if (i < H) Xn[static_cast<size_t>(i) * ldn + p] = (v[e] * r) * w[i];
+        }
+    } else {
+        for (int i = tid; i < H; i += T) Xn[static_cast<size_t>(i) * ldn + p] = (x[i] * r) * w[i];
     }
+}
+
+// One add-norm launch of a pass of P columns (the variant and the PDL flag of
+// the pass: programmatic chaining pays in a batched decode step, and costs a
+// prefill chunk's multi-wave grids more than it saves).
+int add_norm(int P, bool pdl, cudaStream_t st, float* X, const float* Yp, int parts, size_t split_stride,
+             const float* w, float* Xn, int ldn, int H, float eps, const HOut& ho) {
+    if (P <= kMaxSeg)
+        return launch_pdl(pf_add_norm_kernel<true>, dim3(P), dim3(kAddNormWide), 0, st, pdl, X, Yp, parts, split_stride,
+                          w, Xn, ldn, H, eps, ho);
+    return launch_pdl(pf_add_norm_kernel<false>, dim3(P), dim3(256), 0, st, pdl, X, Yp, parts, split_stride, w, Xn, ldn,
+                      H, eps, ho);
 }
 
 // Causal conv1d + SiLU of the qkv rows and the alpha/beta gates, one thread
@@ -1100,15 +1133,20 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
     }
 }
 
-// Causal GQA attention of the chunk's tokens: CTA (p, g) for the GS query
+// Causal GQA attention of the chunk's tokens: CTA (p, g, z) for the GS query
 // heads of kv group g of token p over cache rows 0..pos0+p (f32 rows, or
 // quantized records read dequantized), 8 warps taking keys t = warp mod 8 with
-// an online softmax each, then combined; the output is gated by
-// sigmoid(gate) and stored to column p of the k-major Att[nh*256][lda].
+// an online softmax each, then combined.  Without Part (grid z = 1): the
+// output is gated by sigmoid(gate) and stored to column p of the k-major
+// Att[nh*256][lda].  With Part (a batched decode step, grid z = the key
+// splits): CTA z takes the z-th of gridDim.z equal runs of the rows and stores
+// its running max, sum and unnormalised output per head to Part (merged by
+// pf_attn_merge_kernel).
 template <int GS, bool KVQ>
 __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
                                                              int ldz, const Segs sg, int kvd,
-                                                             float* __restrict__ Att, int lda) {
+                                                             float* __restrict__ Att, int lda,
+                                                             float* __restrict__ Part) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     __shared__ float wml[8][GS][2];
@@ -1129,7 +1167,8 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
     }
     const float scale = 1.0f / sqrtf(static_cast<float>(kHd));
-    for (int t = warp; t < t_len; t += 8) {
+    const int per = (t_len + gridDim.z - 1) / gridDim.z, t_lo = blockIdx.z * per, t_hi = min(t_len, t_lo + per);
+    for (int t = t_lo + warp; t < t_hi; t += 8) {
         float kv[8], vv[8];
         if constexpr (KVQ) {
             const size_t rec = static_cast<size_t>(g) * max_seq + t;
@@ -1174,9 +1213,40 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
             A = fmaf(wacc[w][i][tid], f, A);
         }
         const int h = g * GS + i;
-        const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
-        Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
+        if (Part) {  // [p][h][z]: kHd outputs, then max and sum
+            float* pr = Part + ((static_cast<size_t>(p) * nh + h) * gridDim.z + blockIdx.z) * (kHd + 2);
+            pr[tid] = A;
+            if (tid == 0) {
+                pr[kHd] = M;
+                pr[kHd + 1] = L;
+            }
+        } else {
+            const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
+            Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
+        }
     }
+}
+
+// The key splits of pf_causal_attn_kernel's Part merged (split order) and
+// gated: CTA (p, h), thread tid = output dim.  An empty split has max -inf.
+__global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* __restrict__ Part, int splits,
+                                                            const float* __restrict__ Z, int ldz,
+                                                            float* __restrict__ Att, int lda) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
+    const int p = blockIdx.x, h = blockIdx.y, nh = gridDim.y, tid = threadIdx.x;
+    const float* pr = Part + (static_cast<size_t>(p) * nh + h) * splits * (kHd + 2);
+    float M = -INFINITY;
+    for (int z = 0; z < splits; ++z) M = fmaxf(M, pr[z * (kHd + 2) + kHd]);
+    float L = 0.0f, A = 0.0f;
+    for (int z = 0; z < splits; ++z) {
+        const float mz = pr[z * (kHd + 2) + kHd];
+        const float f = mz == -INFINITY ? 0.0f : expf(mz - M);
+        L = fmaf(pr[z * (kHd + 2) + kHd + 1], f, L);
+        A = fmaf(pr[z * (kHd + 2) + tid], f, A);
+    }
+    const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
+    Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
 }
 
 // A = silu(G) * U, elementwise over the first P columns of k-major [ffn][ldk]
@@ -1199,6 +1269,7 @@ struct Scratch {
     int chunk;
     int* tok;
     float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
+    float* Ap;  // the attention's key-split partials of a batched decode step [4][n_heads][kAttnSplits][kHd + 2]
     int* pos;  // device: the pass's first position per segment [kMaxSeg]
 };
 
@@ -1237,7 +1308,8 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
            (rc = pf_alloc(s, &sc->QKn, P * 2 * std::max(m->k_dim, 1))) ||
            (rc = pf_alloc(s, &sc->O, P * std::max(m->v_dim, 1))) || (rc = pf_alloc(s, &sc->Uin, P * mid)) ||
            (rc = pf_alloc(s, &sc->Qn, P * std::max(m->q_dim, 1))) || (rc = pf_alloc(s, &sc->Ks, P * std::max(m->kv_dim, 1))) ||
-           (rc = pf_alloc(s, &sc->Vs, P * std::max(m->kv_dim, 1))));
+           (rc = pf_alloc(s, &sc->Vs, P * std::max(m->kv_dim, 1))) ||
+           (rc = pf_alloc(s, &sc->Ap, static_cast<size_t>(4) * std::max(c.n_heads, 1) * kAttnSplits * (kHd + 2))));
     if (rc) {
         delete sc;
         return rc;
@@ -1270,7 +1342,7 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     if (int rc = grant_smem(reinterpret_cast<const void*>(pf_gemm_kernel<QT, ROW_MAJOR>), smem)) return rc;
     const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
     const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
-    if (int e_ = launch_pdl(pf_gemm_kernel<QT, ROW_MAJOR>, dim3(grid), dim3(256), smem, st, true, W, n, k, X, kPfChunk,
+    if (int e_ = launch_pdl(pf_gemm_kernel<QT, ROW_MAJOR>, dim3(grid), dim3(256), smem, st, false, W, n, k, X, kPfChunk,
                             Y, ldy, split_stride, P, per))
         return e_;
     return QG_OK;
@@ -1284,15 +1356,18 @@ int splits_for(int n, int k, int P) {
 }
 
 template <bool KVQ>
-int launch_causal(int gs, dim3 grid, cudaStream_t st, const float* Qn, const float* Z, int ldz, const Segs& sg, int kvd,
-                  float* att, int ldk) {
+int launch_causal(int gs, dim3 grid, cudaStream_t st, bool pdl, const float* Qn, const float* Z, int ldz, const Segs& sg,
+                  int kvd, float* att, int ldk, float* part) {
     switch (gs) {
-        case 1: return launch_pdl(pf_causal_attn_kernel<1, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
-                                  ldk);
-        case 2: return launch_pdl(pf_causal_attn_kernel<2, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
-                                  ldk);
-        case 4: return launch_pdl(pf_causal_attn_kernel<4, KVQ>, grid, dim3(256), 0, st, true, Qn, Z, ldz, sg, kvd, att,
-                                  ldk);
+        case 1:
+            return launch_pdl(pf_causal_attn_kernel<1, KVQ>, grid, dim3(256), 0, st, pdl, Qn, Z, ldz, sg, kvd, att, ldk,
+                              part);
+        case 2:
+            return launch_pdl(pf_causal_attn_kernel<2, KVQ>, grid, dim3(256), 0, st, pdl, Qn, Z, ldz, sg, kvd, att, ldk,
+                              part);
+        case 4:
+            return launch_pdl(pf_causal_attn_kernel<4, KVQ>, grid, dim3(256), 0, st, pdl, Qn, Z, ldz, sg, kvd, att, ldk,
+                              part);
         default: return set_err(QG_ERR_SHAPE, "prefill: GQA group of %d query heads is not served", gs);
     }
 }
@@ -1332,15 +1407,15 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
     const size_t part = static_cast<size_t>(P) * H;
     const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
     unsigned* err = ps.ss[0]->err;  // the small-batch GEMV's bounded waits report here
-    if (int e_ = launch_pdl(pf_embed_kernel, dim3(P), dim3(256), 0, st, true, m->embd, sc->tok, H, sc->X))
+    const bool pdl = P <= 4;        // programmatic chaining of the pass's kernels: a batched decode step only
+    if (int e_ = launch_pdl(pf_embed_kernel, dim3(P), dim3(256), 0, st, pdl, m->embd, sc->tok, H, sc->X))
         return e_;
     int pending = 0;  // split sums of the last projection not yet added to X
     int rc = QG_OK;
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
         const Segs sg = segs_of(ps, il);
-        if (int e_ = launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending,
-                                part, L.attn_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, ldk, H, c.eps, HOut{}))
             return e_;
         int zin = 1;
         if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin,
@@ -1350,7 +1425,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
         if (zin > 1) {
             const size_t cnt = static_cast<size_t>(P) * L.n_in;
             if (int e_ = launch_pdl(pf_sum_parts_kernel, dim3(static_cast<unsigned>((cnt + 255) / 256)), dim3(256), 0,
-                                    st, true, sc->Zp, zin, cnt, sc->Z, cnt))
+                                    st, pdl, sc->Zp, zin, cnt, sc->Z, cnt))
                 return e_;
             Z = sc->Z;
         }
@@ -1359,26 +1434,26 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
             const long long cg = static_cast<long long>(P) * (C + nv);
             if (int e_ = launch_pdl(pf_conv_gates_kernel, dim3(static_cast<unsigned>((cg + 255) / 256)), dim3(256), 0,
-                                    st, true, Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq,
+                                    st, pdl, Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq,
                                     sc->dt, sc->beta))
                 return e_;
-            if (int e_ = launch_pdl(pf_conv_window_kernel, dim3((C + 255) / 256, ps.n), dim3(256), 0, st, true, Z,
+            if (int e_ = launch_pdl(pf_conv_window_kernel, dim3((C + 255) / 256, ps.n), dim3(256), 0, st, pdl, Z,
                                     L.n_in, C, c.conv_kernel, sg))
                 return e_;
             const int warps = P * 2 * c.n_k_heads;
-            if (int e_ = launch_pdl(pf_l2norm_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, true, sc->Cq, C,
+            if (int e_ = launch_pdl(pf_l2norm_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, pdl, sc->Cq, C,
                                     m->k_dim, c.n_k_heads, P, c.eps, sc->QKn))
                 return e_;
-            if (int e_ = launch_pdl(pf_delta_kernel, dim3(nv * dv / 32, ps.n), dim3(256), 0, st, true, sc->Cq, C,
+            if (int e_ = launch_pdl(pf_delta_kernel, dim3(nv * dv / 32, ps.n), dim3(256), 0, st, pdl, sc->Cq, C,
                                     m->k_dim, sc->QKn, sc->dt, sc->beta, sg, sc->O, c.n_k_heads, nv, dv))
                 return e_;
-            if (int e_ = launch_pdl(pf_gated_norm_kernel, dim3(P, (nv + 7) / 8), dim3(256), 0, st, true, sc->O, Z,
+            if (int e_ = launch_pdl(pf_gated_norm_kernel, dim3(P, (nv + 7) / 8), dim3(256), 0, st, pdl, sc->O, Z,
                                     L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps, sc->Uin, ldk))
                 return e_;
             k_out = m->v_dim;
         } else {
             const int nkv = c.n_kv_heads, kvd = m->kv_dim;
-            if (int e_ = launch_pdl(pf_attn_prep_kernel, dim3(P), dim3(256), 0, st, true, Z, L.n_in, c.n_heads, nkv,
+            if (int e_ = launch_pdl(pf_attn_prep_kernel, dim3(P), dim3(256), 0, st, pdl, Z, L.n_in, c.n_heads, nkv,
                                     L.q_norm, L.k_norm, sg, c.n_rot, m->theta_scale, c.eps, sc->Qn,
                                     kvq ? sc->Ks : nullptr, kvq ? sc->Vs : nullptr))
                 return e_;
@@ -1390,25 +1465,31 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
                                           reinterpret_cast<uint8_t*>(si->vc[il]), st);
             }
             if (rc) break;
-            const dim3 grid(P, nkv);
             const int gs = c.n_heads / nkv;
-            rc = kvq ? launch_causal<true>(gs, grid, st, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk)
-                     : launch_causal<false>(gs, grid, st, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk);
+            const int zs = pdl ? kAttnSplits : 1;  // a batched decode step: key splits, then a merge
+            float* part = zs > 1 ? sc->Ap : nullptr;
+            const dim3 grid(P, nkv, zs);
+            rc = kvq ? launch_causal<true>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk, part)
+                     : launch_causal<false>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk, part);
             if (rc) break;
+            if (part) {
+                if (int e_ = launch_pdl(pf_attn_merge_kernel, dim3(P, c.n_heads), dim3(kHd), 0, st, pdl, part, zs, Z,
+                                        L.n_in, sc->Uin, ldk))
+                    return e_;
+            }
             k_out = m->q_dim;
         }
         if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending,
                                       err)))
             break;
-        if (int e_ = launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending,
-                                part, L.post_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldk, H, c.eps, HOut{}))
             return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
         if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
         if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
         const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
-        if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, true,
+        if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, pdl,
                                 sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk))
             return e_;
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
@@ -1417,11 +1498,9 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
     if (lm) {  // batched lm_head next: the output norm of every column, each stream to its state
         HOut ho{};
         for (int i = 0; i < ps.n; ++i) ho.h[i] = ps.ss[i]->h;
-        return launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending, part,
-                          m->out_norm, sc->Xn, ldk, H, c.eps, ho);
+        return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, m->out_norm, sc->Xn, ldk, H, c.eps, ho);
     }
-    return launch_pdl(pf_add_norm_kernel, dim3(P), dim3(kAddNormThreads), 0, st, true, sc->X, sc->Yp, pending, part,
-                      static_cast<const float*>(nullptr), static_cast<float*>(nullptr), kPfChunk, H, c.eps, HOut{});
+    return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, nullptr, nullptr, kPfChunk, H, c.eps, HOut{});
 }
 
 // The lm_head argmax of every column of a batched pass (at most 4, after
