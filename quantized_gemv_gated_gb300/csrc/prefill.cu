@@ -1,7 +1,7 @@
 // Batched prompt prefill: a chunk of prompt tokens goes through every layer
-// together, so each projection is one multi-token GEMM that reads its weights
-// once per chunk instead of once per token (the decode session's batched
-// prefill, forward_qwen35_cuda.rs).  The recurrences stay exact token-by-token
+// together, so each projection is one multi-token GEMM on the tensor cores
+// (tcgen05.mma) that reads its weights once per chunk instead of once per
+// token (the decode session's batched prefill, forward_qwen35_cuda.rs).  The recurrences stay exact token-by-token
 // recurrences inside one kernel per layer: the causal conv scans each channel
 // over the chunk, the delta rule walks the chunk with each warp's four state
 // rows in registers, and the attention of token p reads the cache rows
@@ -15,6 +15,8 @@
 // single-column segments; with at most 4 columns the projections use a
 // small-batch GEMV that reads each weight once for all of them, and a fixed set
 // of sequences can replay the whole step as one captured graph (qg_batch_*).
+#include <cuda_bf16.h>
+
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -25,9 +27,6 @@
 namespace qg {
 namespace {
 
-constexpr int kGR = 128;       // weight rows per GEMM tile
-constexpr int kGT = 128;       // tokens per GEMM tile
-constexpr int kGK = 64;        // k per shared-memory stage (a quarter super-block)
 constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
 constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
 constexpr int kAttnSplits = 16; // key splits of a batched decode step's attention (up to 4 columns)
@@ -137,65 +136,123 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int hf, float*
     }
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Y = W X over the 64-weight quarters of split z, for a planar Q4_K / Q6_K W
-// [n x k] and k-major f32 inputs X[k][ldx] (token t of the chunk in column t).
-// Grid (ceil(n/128), ceil(P/128), splits), 256 threads.  Per quarter the CTA
-// dequantizes its 128 rows (thread: 32 weights of one row, from raw bytes
-// loaded while the previous quarter computed) into Ws[k][row], while the next quarter's inputs
-// stream into the other half of the double-buffered Xs[k][token] by 16-byte
-// async copies; each thread accumulates 8 rows x 8 tokens as outer products in
-// k order (rows 4 ty..+3 and 64 + 4 ty..+3, tokens likewise with tx, so eight
-// consecutive lanes read 128 contiguous bytes).  Output: split z at
-// Y + z split_stride, token-major (Y[t ldy + row]) or, when ROW_MAJOR,
-// Y[row ldy + t] (k-major for a following GEMM).
+// ------------------------------------------- prefill GEMM on the tensor cores
+// Y = W X for a chunk of P > 4 tokens with tcgen05.mma: the CTA's 128 weight
+// rows are the A operand (M = 128), its 128 tokens the B operand (N = 128),
+// both K-major bf16 tiles in shared memory, fp32 accumulators in tensor
+// memory (128 lanes x 128 columns).  Each operand value v is split into
+// hi = bf16(v) and lo = bf16(v - hi), and every 16-wide K step issues three
+// products, hi*hi + hi*lo + lo*hi: the dropped lo*lo term and the rounding of
+// lo leave a relative error near 2^-16 per product, against 2^-8 for one bf16
+// product (f32 accumulation throughout).
+//
+// Tiles.  A K step of 64 weights (a quarter super-block) is one 128-byte row
+// per matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16
+// (the 128-byte swizzle; the matrix descriptor's rows of 8 are 1024 bytes
+// apart), four 16 KB tiles per stage (A hi, A lo, B hi, B lo), two stages.
+// All 256 threads build a stage: thread (row r = tid & 127, half hf = tid >>
+// 7) dequantizes 32 weights of weight row r (raw bytes loaded a quarter
+// ahead) and converts 32 inputs of token r (X is k-major, so a warp's loads
+// of one k are 32 consecutive tokens).  Thread 0 then issues the stage's 12
+// MMAs and commits them to the stage's mbarrier, which the threads wait on
+// (bounded) before rebuilding that stage two quarters later.
+constexpr int kMmaTile = 128 * 128;           // bytes of one 128 x 64 bf16 operand tile
+constexpr int kMmaStage = 4 * kMmaTile;       // A hi, A lo, B hi, B lo
+constexpr int kMmaSmem = 2 * kMmaStage + 1024 + 64;  // two stages, 1024-byte alignment, barriers
+// kind::f16 instruction descriptor: f32 accumulator (bits 4-5 = 1), bf16 A and
+// B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kMmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle:
+// start address >> 4, leading offset 16 B (unused by this layout), 8-row
+// groups 1024 B apart, descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t mma_sdesc(uint32_t addr) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+        "l"(a), "l"(b), "r"(kMmaIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// 8 values as 16 bytes of bf16 hi parts, their lo parts to `lo`.
+__device__ __forceinline__ uint4 bf16_hi_lo(const float* v, uint4& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(v[2 * i] - __low2float(hh), v[2 * i + 1] - __high2float(hh));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+// 32 values of row r (chunks 4 hf .. 4 hf + 3) into a hi and a lo tile.
+__device__ __forceinline__ void put_row32(uint8_t* thi, uint8_t* tlo, int r, int hf, const float* v) {
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint4 lo;
+        const uint4 hi = bf16_hi_lo(v + 8 * c4, lo);
+        const int off = r * 128 + (((4 * hf + c4) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(thi + off) = hi;
+        *reinterpret_cast<uint4*>(tlo + off) = lo;
+    }
+}
+
+// Y = W X over the quarters of split z (grid (ceil(n/128), ceil(P/128),
+// splits), 256 threads, kMmaSmem bytes): W planar Q4_K / Q6_K [n x k] in the
+// grouped layout, X k-major f32 [k][ldx].  Output: split z at Y + z
+// split_stride, token-major Y[t ldy + row] or, ROW_MAJOR, Y[row ldy + t] (k-major
+// for a following GEMM).
+// err: a bounded wait that gave up sets DEVERR_FULL_WAIT and the CTA stores nothing.
 template <int QT, bool ROW_MAJOR>
-__global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restrict__ W, int n, int k,
-                                                         const float* __restrict__ X, int ldx, float* __restrict__ Y,
-                                                         int ldy, size_t split_stride, int P, int q_per_split) {
-    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
-    pdl_wait();               // everything earlier in the pass is complete and visible
+__global__ void __launch_bounds__(256, 1) pf_mma_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                        const float* __restrict__ X, int ldx, float* __restrict__ Y,
+                                                        int ldy, size_t split_stride, int P, int q_per_split,
+                                                        unsigned* __restrict__ err) {
     using Raw = typename std::conditional<QT == QT_Q6K, RawQ6, RawQ4>::type;
-    extern __shared__ __align__(16) float smf[];
-    float* Ws = smf;                  // [kGK][kGR]
-    float* Xs = smf + kGK * kGR;      // [2][kGK][kGT]
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int row0 = blockIdx.x * kGR, tok0 = blockIdx.y * kGT;
+    extern __shared__ uint8_t mma_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mma_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kMmaStage);  // [2]: a stage's MMAs have completed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + 2 * kMmaStage + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = blockIdx.x * 128, tok0 = blockIdx.y * 128;
     const int nb = k / 256, n8 = (n + 7) & ~7;
     const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split);
-    const int dr = tid & (kGR - 1), hf = tid >> 7;  // dequantization role: row, half of the quarter
-    const int grow = row0 + dr;
+    const int r = tid & 127, hf = tid >> 7;
+    const int grow = row0 + r;
     const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
     const int GB = QT == QT_Q6K ? 1680 : 1152;
-    auto issue_x = [&](int qi, int buf) {  // the quarter's 64 k-rows x 128 tokens, 16 bytes per copy
-        float* xs = Xs + buf * kGK * kGT;
-        const float* xg = X + static_cast<size_t>(64 * qi) * ldx + tok0;
-        for (int e = tid; e < kGK * (kGT / 4); e += 256) {
-            const int kk = e >> 5, c4 = e & 31;
-            cp_async16(xs + kk * kGT + 4 * c4, xg + static_cast<size_t>(kk) * ldx + 4 * c4);
-        }
-    };
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-    Raw cur{};
-    if (q0 < q1) {
-        if (row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, cur);
-        issue_x(q0, 0);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
     }
-    cp_async_commit();
+    if (warp == 0) {  // 128 columns of tensor memory: the 128 x 128 f32 accumulator
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(128)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tslot;
+    Raw cur{};
+    if (q0 < q1 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, cur);
+    bool ok = true;
     for (int qi = q0; qi < q1; ++qi) {
-        const int buf = (qi - q0) & 1;
-        if (qi + 1 < q1) issue_x(qi + 1, buf ^ 1);
-        cp_async_commit();
-        {
+        const int j = qi - q0, st = j & 1;
+        uint8_t* sb = sm + st * kMmaStage;
+        const bool free = j < 2 || mbar_wait(&bar[st], ((j - 2) >> 1) & 1);  // the MMAs that read this stage are done
+        if (free) {
             float v[32];
             if (row_ok) {
                 raw_decode(cur, qi & 3, hf, v);
@@ -203,43 +260,75 @@ __global__ void __launch_bounds__(256, 2) pf_gemm_kernel(const uint8_t* __restri
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.0f;
             }
+            put_row32(sb, sb + kMmaTile, r, hf, v);
+            if (qi + 1 < q1 && row_ok)
+                raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, cur);
+            const float* xg = X + static_cast<size_t>(64 * qi + 32 * hf) * ldx + tok0 + r;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) Ws[(32 * hf + i) * kGR + dr] = v[i];
+            for (int i = 0; i < 32; ++i) v[i] = __ldg(xg + static_cast<size_t>(i) * ldx);
+            put_row32(sb + 2 * kMmaTile, sb + 3 * kMmaTile, r, hf, v);
         }
-        // the next quarter's raw bytes, into the registers just decoded (one set live)
-        if (qi + 1 < q1 && row_ok)
-            raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, cur);
-        cp_async_wait1();  // this quarter's inputs have landed (the next quarter's may be in flight)
-        __syncthreads();
-        const float* xs = Xs + buf * kGK * kGT;
-#pragma unroll 4
-        for (int kk = 0; kk < kGK; ++kk) {
-            const float4 a0 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 4 * ty);
-            const float4 a1 = *reinterpret_cast<const float4*>(Ws + kk * kGR + 64 + 4 * ty);
-            const float4 c0 = *reinterpret_cast<const float4*>(xs + kk * kGT + 4 * tx);
-            const float4 c1 = *reinterpret_cast<const float4*>(xs + kk * kGT + 64 + 4 * tx);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tiles, visible to the tensor core
+        if (!__syncthreads_and(free)) {  // every thread leaves together when a wait gave up
+            ok = false;
+            break;
         }
-        __syncthreads();
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t a_hi = smem_u32(sb), a_lo = a_hi + kMmaTile, b_hi = a_hi + 2 * kMmaTile,
+                           b_lo = a_hi + 3 * kMmaTile;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
+                const uint32_t o = 32 * s;
+                mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
+                mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
+                mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+            }
+            mma_commit(&bar[st]);
+        }
     }
-    float* Yz = Y + blockIdx.z * split_stride;
+    const int nq = q1 - q0;
+    if (ok && nq > 0) ok = mbar_wait(&bar[(nq - 1) & 1], ((nq - 1) >> 1) & 1);  // every MMA of the CTA is done
+    ok = __syncthreads_and(ok);  // uniform: the accumulator loads are warp-collective
+    if (!ok && tid == 0) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {  // warp w: accumulator lanes 32 (w & 3) .., columns 64 (w >> 2) ..
+        const int lq = warp & 3, ch = warp >> 2;
+        const int row = row0 + 32 * lq + lane;
+        float* Yz = Y + blockIdx.z * split_stride;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+            uint32_t v[16];
+            if (nq > 0) {
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(64 * ch + c);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                    : "r"(ta));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = row0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
-        if (r >= n) continue;
+                for (int i = 0; i < 16; ++i) v[i] = 0u;
+            }
+            if (row < n) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int t = tok0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
-            if (t < P) {
-                if (ROW_MAJOR) Yz[static_cast<size_t>(r) * ldy + t] = acc[i][j];
-                else Yz[static_cast<size_t>(t) * ldy + r] = acc[i][j];
+                for (int i = 0; i < 16; ++i) {
+                    const int t = tok0 + 64 * ch + c + i;
+                    if (t < P) {
+                        if (ROW_MAJOR) Yz[static_cast<size_t>(row) * ldy + t] = __uint_as_float(v[i]);
+                        else Yz[static_cast<size_t>(t) * ldy + row] = __uint_as_float(v[i]);
+                    }
+                }
             }
         }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
     }
 }
 
@@ -1338,20 +1427,19 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     const int per = (nq + splits - 1) / splits;
     const int z = (nq + per - 1) / per;
     if (used_splits) *used_splits = z;
-    const int smem = kGK * (kGR + 2 * kGT) * static_cast<int>(sizeof(float));
-    if (int rc = grant_smem(reinterpret_cast<const void*>(pf_gemm_kernel<QT, ROW_MAJOR>), smem)) return rc;
-    const dim3 grid((n + kGR - 1) / kGR, (P + kGT - 1) / kGT, z);
+    if (int rc = grant_smem(reinterpret_cast<const void*>(pf_mma_kernel<QT, ROW_MAJOR>), kMmaSmem)) return rc;
+    const dim3 grid((n + 127) / 128, (P + 127) / 128, z);
     const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
-    if (int e_ = launch_pdl(pf_gemm_kernel<QT, ROW_MAJOR>, dim3(grid), dim3(256), smem, st, false, W, n, k, X, kPfChunk,
-                            Y, ldy, split_stride, P, per))
+    if (int e_ = launch_pdl(pf_mma_kernel<QT, ROW_MAJOR>, grid, dim3(256), kMmaSmem, st, false, W, n, k, X, kPfChunk, Y,
+                            ldy, split_stride, P, per, err))
         return e_;
     return QG_OK;
 }
 
-// K splits of a projection: enough CTAs for two per SM (at most kPfMaxSplit).
+// K splits of a projection: enough CTAs for one per SM (at most kPfMaxSplit).
 int splits_for(int n, int k, int P) {
-    const int ctas = ((n + kGR - 1) / kGR) * ((P + kGT - 1) / kGT);
-    int z = (2 * device_sms() + ctas - 1) / ctas;
+    const int ctas = ((n + 127) / 128) * ((P + 127) / 128);
+    const int z = device_sms() / ctas;
     return std::max(1, std::min({z, kPfMaxSplit, k / 64}));
 }
 
