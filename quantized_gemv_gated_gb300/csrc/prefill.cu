@@ -58,40 +58,37 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
 }
 __device__ __forceinline__ int byte_of(const uint4& v, int b) { return (word_of(v, b >> 2) >> (8 * (b & 3))) & 0xff; }
 
-// Raw bytes one thread dequantizes per 64-weight quarter, loaded a quarter
-// ahead.  Q4_K: the 16-byte head of the row's 144-byte block (d, dmin, the 12
-// bytes of 6-bit scales and mins) and the quarter's 32 bytes of nibbles.
-// Q6_K: the row's two 48-byte records of the quarter, their 4 scales each, d.
+// Raw bytes one thread dequantizes: 16 weights of a 64-weight quarter q of a
+// row, part (0..3) = 2 hf + p: weights 64 q + 32 hf + 16 p .. + 15, loaded a
+// quarter ahead.  Q4_K: the row's 16-byte block head (d, dmin, the 12 bytes of
+// 6-bit scales and mins) and the 16 bytes of nibbles holding those weights
+// (low nibbles for hf = 0, high for hf = 1).  Q6_K: the row's 48-byte planar
+// record of those weights, its 4 scales and d.
 struct RawQ4 {
-    uint4 h, q0, q1;
+    uint4 h, q;
 };
 struct RawQ6 {
-    uint4 r[2][3];
-    uint32_t sc[2];
+    uint4 r[3];
+    uint32_t sc;
     uint32_t d;
 };
 
-__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, RawQ4& r) {
+__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, int part, RawQ4& r) {
     const uint8_t* blk = gb + 144 * rr;
     r.h = *reinterpret_cast<const uint4*>(blk);
-    r.q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
-    r.q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+    r.q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q + 16 * (part & 1));
 }
-__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, RawQ6& r) {
+__device__ __forceinline__ void raw_load(const uint8_t* gb, int rr, int q, int part, RawQ6& r) {
+    const int u = 4 * rr + 2 * (q >> 1) + (part & 1);
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const int u = 4 * rr + 2 * (q >> 1) + p;
-#pragma unroll
-        for (int w = 0; w < 3; ++w) r.r[p][w] = *reinterpret_cast<const uint4*>(gb + 48 * u + 16 * w);
-        r.sc[p] = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
-    }
+    for (int w = 0; w < 3; ++w) r.r[w] = *reinterpret_cast<const uint4*>(gb + 48 * u + 16 * w);
+    r.sc = *reinterpret_cast<const uint32_t*>(gb + 1536 + 4 * u);
     r.d = *reinterpret_cast<const uint16_t*>(gb + 1664 + 2 * rr);
 }
 
-// Weights 64 q + 32 hf .. +31 of the row (sub-block j = 2q + hf of the GGUF
-// Q4_K block): d * scale_j * nibble - dmin * min_j, the low nibbles for hf = 0.
-__device__ __forceinline__ void raw_decode(const RawQ4& r, int q, int hf, float* v) {
-    const int j = 2 * q + hf;
+// Q4_K: d * scale_j * nibble - dmin * min_j for sub-block j = 2 q + hf.
+__device__ __forceinline__ void raw_decode(const RawQ4& r, int q, int part, float* v) {
+    const int hf = part >> 1, j = 2 * q + hf;
     const float d = f16_to_f32(static_cast<uint16_t>(r.h.x & 0xffffu));
     const float dmin = f16_to_f32(static_cast<uint16_t>(r.h.x >> 16));
     int s, m;  // 6-bit scale and min of sub-block j from the 12 bytes at 4..15
@@ -105,37 +102,32 @@ __device__ __forceinline__ void raw_decode(const RawQ4& r, int q, int hf, float*
     const float ds = d * static_cast<float>(s), dm = dmin * static_cast<float>(m);
     const int sh = 4 * hf;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint4& w = i < 16 ? r.q0 : r.q1;
-        const int nib = (word_of(w, (i & 15) >> 2) >> (8 * (i & 3) + sh)) & 15;
+    for (int i = 0; i < 16; ++i) {
+        const int nib = (word_of(r.q, i >> 2) >> (8 * (i & 3) + sh)) & 15;
         v[i] = ds * static_cast<float>(nib) - dm;
     }
 }
 
-// Weights 64 q + 32 hf .. +31 of the row in the planar Q6_K layout: they are
-// 128 h + 32 s + 16 p + i (h = q/2, s = 2 (q&1) + hf, p = 0, 1, i < 16), byte
-// i of record (rr, 2h + p) with its scale s: d * scale * (6-bit code - 32).
-__device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int hf, float* v) {
-    const int s = 2 * (q & 1) + hf;
+// Q6_K (planar): weights 128 h + 32 s + 16 p + i (h = q / 2, s = 2 (q & 1) +
+// hf, i < 16) are byte i of record (rr, 2 h + p) with its scale s:
+// d * scale * (6-bit code - 32).
+__device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int part, float* v) {
+    const int s = 2 * (q & 1) + (part >> 1);
     const float d = f16_to_f32(static_cast<uint16_t>(r.d & 0xffffu));
+    const float ds = d * static_cast<float>(static_cast<int8_t>((r.sc >> (8 * s)) & 0xffu));
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const float ds = d * static_cast<float>(static_cast<int8_t>((r.sc[p] >> (8 * s)) & 0xffu));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int a = (word_of(r.r[p][0], i >> 2) >> (8 * (i & 3))) & 0xff;
-            const int b = (word_of(r.r[p][1], i >> 2) >> (8 * (i & 3))) & 0xff;
-            const int hb = (word_of(r.r[p][2], i >> 2) >> (8 * (i & 3))) & 0xff;
-            int code;
-            if (s == 0) code = (a & 15) | ((hb & 3) << 4);
-            else if (s == 1) code = (b & 15) | (((hb >> 2) & 3) << 4);
-            else if (s == 2) code = (a >> 4) | (((hb >> 4) & 3) << 4);
-            else code = (b >> 4) | (((hb >> 6) & 3) << 4);
-            v[16 * p + i] = ds * static_cast<float>(code - 32);
-        }
+    for (int i = 0; i < 16; ++i) {
+        const int a = (word_of(r.r[0], i >> 2) >> (8 * (i & 3))) & 0xff;
+        const int b = (word_of(r.r[1], i >> 2) >> (8 * (i & 3))) & 0xff;
+        const int hb = (word_of(r.r[2], i >> 2) >> (8 * (i & 3))) & 0xff;
+        int code;
+        if (s == 0) code = (a & 15) | ((hb & 3) << 4);
+        else if (s == 1) code = (b & 15) | (((hb >> 2) & 3) << 4);
+        else if (s == 2) code = (a >> 4) | (((hb >> 4) & 3) << 4);
+        else code = (b >> 4) | (((hb >> 6) & 3) << 4);
+        v[i] = ds * static_cast<float>(code - 32);
     }
 }
-
 
 // ------------------------------------------- prefill GEMM on the tensor cores
 // Y = W X for a chunk of P > 4 tokens with tcgen05.mma: the CTA's 128 weight
@@ -147,19 +139,22 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int hf, float*
 // lo leave a relative error near 2^-16 per product, against 2^-8 for one bf16
 // product (f32 accumulation throughout).
 //
-// Tiles.  A K step of 64 weights (a quarter super-block) is one 128-byte row
-// per matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16
-// (the 128-byte swizzle; the matrix descriptor's rows of 8 are 1024 bytes
-// apart), four 16 KB tiles per stage (A hi, A lo, B hi, B lo), two stages.
-// All 256 threads build a stage: thread (row r = tid & 127, half hf = tid >>
-// 7) dequantizes 32 weights of weight row r (raw bytes loaded a quarter
-// ahead) and converts 32 inputs of token r (X is k-major, so a warp's loads
-// of one k are 32 consecutive tokens).  Thread 0 then issues the stage's 12
-// MMAs and commits them to the stage's mbarrier, which the threads wait on
-// (bounded) before rebuilding that stage two quarters later.
-constexpr int kMmaTile = 128 * 128;           // bytes of one 128 x 64 bf16 operand tile
-constexpr int kMmaStage = 4 * kMmaTile;       // A hi, A lo, B hi, B lo
+// Tiles.  A K step of 64 (a quarter super-block) is one 128-byte row per
+// matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16 (the
+// 128-byte swizzle; the matrix descriptor's groups of 8 rows are 1024 bytes
+// apart).  A stage holds four 16 KB tiles (A hi, A lo, B hi, B lo); two
+// stages.  The inputs arrive already in this form: the kernels that produce
+// a GEMM input write it as (quarter, 128-token tile) pairs of hi and lo tiles
+// (put_xt), and one bulk copy per stage brings the pair in.  The 512 threads
+// build the A tiles: thread (row r = tid & 127, part = tid >> 7) dequantizes
+// 16 weights of weight row r (raw bytes loaded a quarter ahead).  Thread 0
+// then issues the stage's 12 MMAs and commits them to the stage's mbarrier,
+// which the threads wait on (bounded) before rebuilding that stage two
+// quarters later.
+constexpr int kMmaTile = 128 * 128;                  // bytes of one 128 x 64 bf16 operand tile
+constexpr int kMmaStage = 4 * kMmaTile;              // A hi, A lo, B hi, B lo
 constexpr int kMmaSmem = 2 * kMmaStage + 1024 + 64;  // two stages, 1024-byte alignment, barriers
+constexpr int kMmaThreads = 512;
 // kind::f16 instruction descriptor: f32 accumulator (bits 4-5 = 1), bf16 A and
 // B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t kMmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -195,45 +190,64 @@ __device__ __forceinline__ uint4 bf16_hi_lo(const float* v, uint4& lo) {
     lo = make_uint4(l[0], l[1], l[2], l[3]);
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
-// 32 values of row r (chunks 4 hf .. 4 hf + 3) into a hi and a lo tile.
-__device__ __forceinline__ void put_row32(uint8_t* thi, uint8_t* tlo, int r, int hf, const float* v) {
+// 16 values of row r (chunks c0, c0 + 1) into a hi and a lo tile.
+__device__ __forceinline__ void put_row16(uint8_t* thi, uint8_t* tlo, int r, int c0, const float* v) {
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
+    for (int c = 0; c < 2; ++c) {
         uint4 lo;
-        const uint4 hi = bf16_hi_lo(v + 8 * c4, lo);
-        const int off = r * 128 + (((4 * hf + c4) ^ (r & 7)) << 4);
+        const uint4 hi = bf16_hi_lo(v + 8 * c, lo);
+        const int off = r * 128 + (((c0 + c) ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(thi + off) = hi;
         *reinterpret_cast<uint4*>(tlo + off) = lo;
     }
 }
+// A GEMM input value (k, token p) of a prefill chunk in the tensor-core form:
+// the (quarter k / 64, token tile p / 128) pair of tiles [hi | lo], 32 KB each,
+// row p % 128, element k % 64.  Tokens P..255 of a chunk are never read back.
+__device__ __forceinline__ void put_xt(uint8_t* xt, int k, int p, float v) {
+    uint8_t* t = xt + static_cast<size_t>((k >> 6) * 2 + (p >> 7)) * (2 * kMmaTile);
+    const int row = p & 127;
+    const int off = row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + 2 * (k & 7);
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    *reinterpret_cast<__nv_bfloat16*>(t + off) = h;
+    *reinterpret_cast<__nv_bfloat16*>(t + kMmaTile + off) = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+// A GEMM input of a pass: k-major f32 [k][ld], or (ld == 0) the tiles of put_xt.
+__device__ __forceinline__ void put_in(float* out, int ld, int k, int p, float v) {
+    if (ld == 0) put_xt(reinterpret_cast<uint8_t*>(out), k, p, v);
+    else out[static_cast<size_t>(k) * ld + p] = v;
+}
 
 // Y = W X over the quarters of split z (grid (ceil(n/128), ceil(P/128),
-// splits), 256 threads, kMmaSmem bytes): W planar Q4_K / Q6_K [n x k] in the
-// grouped layout, X k-major f32 [k][ldx].  Output: split z at Y + z
-// split_stride, token-major Y[t ldy + row] or, ROW_MAJOR, Y[row ldy + t] (k-major
-// for a following GEMM).
-// err: a bounded wait that gave up sets DEVERR_FULL_WAIT and the CTA stores nothing.
+// splits), kMmaThreads threads, kMmaSmem bytes): W planar Q4_K / Q6_K [n x k]
+// in the grouped layout, XT the inputs as put_xt tiles.  Output: split z at
+// Y + z split_stride, token-major Y[t ldy + row] or, ROW_MAJOR, Y[row ldy + t]
+// (k-major for a following GEMM).  err: a bounded wait that gave up sets
+// DEVERR_FULL_WAIT and the CTA stores nothing.
 template <int QT, bool ROW_MAJOR>
-__global__ void __launch_bounds__(256, 1) pf_mma_kernel(const uint8_t* __restrict__ W, int n, int k,
-                                                        const float* __restrict__ X, int ldx, float* __restrict__ Y,
-                                                        int ldy, size_t split_stride, int P, int q_per_split,
-                                                        unsigned* __restrict__ err) {
+__global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                                const uint8_t* __restrict__ XT, float* __restrict__ Y,
+                                                                int ldy, size_t split_stride, int P, int q_per_split,
+                                                                unsigned* __restrict__ err) {
     using Raw = typename std::conditional<QT == QT_Q6K, RawQ6, RawQ4>::type;
     extern __shared__ uint8_t mma_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mma_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kMmaStage);  // [2]: a stage's MMAs have completed
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + 2 * kMmaStage + 16);
+    uint64_t* done = reinterpret_cast<uint64_t*>(sm + 2 * kMmaStage);  // [2]: a stage's MMAs have completed
+    uint64_t* full = done + 2;                                          // [2]: a stage's input tiles have landed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * 128, tok0 = blockIdx.y * 128;
     const int nb = k / 256, n8 = (n + 7) & ~7;
     const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split);
-    const int r = tid & 127, hf = tid >> 7;
+    const int r = tid & 127, part = tid >> 7;
     const int grow = row0 + r;
     const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
     const int GB = QT == QT_Q6K ? 1680 : 1152;
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&done[i], 1);
+            mbar_init(&full[i], 1);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {  // 128 columns of tensor memory: the 128 x 128 f32 accumulator
@@ -246,61 +260,66 @@ __global__ void __launch_bounds__(256, 1) pf_mma_kernel(const uint8_t* __restric
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tslot;
     Raw cur{};
-    if (q0 < q1 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, cur);
+    if (q0 < q1 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, part, cur);
     bool ok = true;
     for (int qi = q0; qi < q1; ++qi) {
         const int j = qi - q0, st = j & 1;
         uint8_t* sb = sm + st * kMmaStage;
-        const bool free = j < 2 || mbar_wait(&bar[st], ((j - 2) >> 1) & 1);  // the MMAs that read this stage are done
+        const bool free = j < 2 || mbar_wait(&done[st], ((j - 2) >> 1) & 1);  // the MMAs that read this stage are done
         if (free) {
-            float v[32];
+            if (tid == 0) {  // this quarter's input tiles [hi | lo] of the CTA's token tile
+                mbar_arrive_expect_tx(&full[st], 2 * kMmaTile);
+                bulk_g2s(sb + 2 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (2 * kMmaTile),
+                         2 * kMmaTile, &full[st], policy_evict_first());
+            }
+            float v[16];
             if (row_ok) {
-                raw_decode(cur, qi & 3, hf, v);
+                raw_decode(cur, qi & 3, part, v);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
             }
-            put_row32(sb, sb + kMmaTile, r, hf, v);
+            put_row16(sb, sb + kMmaTile, r, 2 * part, v);
             if (qi + 1 < q1 && row_ok)
-                raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, cur);
-            const float* xg = X + static_cast<size_t>(64 * qi + 32 * hf) * ldx + tok0 + r;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __ldg(xg + static_cast<size_t>(i) * ldx);
-            put_row32(sb + 2 * kMmaTile, sb + 3 * kMmaTile, r, hf, v);
+                raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, part, cur);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tiles, visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the A tiles, visible to the tensor core
         if (!__syncthreads_and(free)) {  // every thread leaves together when a wait gave up
             ok = false;
             break;
         }
         if (tid == 0) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a_hi = smem_u32(sb), a_lo = a_hi + kMmaTile, b_hi = a_hi + 2 * kMmaTile,
-                           b_lo = a_hi + 3 * kMmaTile;
+            const bool landed = mbar_wait(&full[st], (j >> 1) & 1);
+            if (landed) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a_hi = smem_u32(sb), a_lo = a_hi + kMmaTile, b_hi = a_hi + 2 * kMmaTile,
+                               b_lo = a_hi + 3 * kMmaTile;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
-                const uint32_t o = 32 * s;
-                mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
-                mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
-                mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+                for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
+                    const uint32_t o = 32 * s;
+                    mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
+                    mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
+                    mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+                }
             }
-            mma_commit(&bar[st]);
+            mma_commit(&done[st]);  // also when nothing was issued: the waits stay matched
+            if (!landed) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
         }
     }
     const int nq = q1 - q0;
-    if (ok && nq > 0) ok = mbar_wait(&bar[(nq - 1) & 1], ((nq - 1) >> 1) & 1);  // every MMA of the CTA is done
-    ok = __syncthreads_and(ok);  // uniform: the accumulator loads are warp-collective
+    if (ok && nq > 0) ok = mbar_wait(&done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);  // every MMA of the CTA is done
+    ok = __syncthreads_and(ok && !__ldcg(err)) != 0;  // uniform: the accumulator loads are warp-collective
     if (!ok && tid == 0) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {  // warp w: accumulator lanes 32 (w & 3) .., columns 64 (w >> 2) ..
-        const int lq = warp & 3, ch = warp >> 2;
+    if (ok) {  // warp w: accumulator lanes 32 (w & 3) .., columns 32 (w >> 2) ..
+        const int lq = warp & 3, cb = 32 * (warp >> 2);
         const int row = row0 + 32 * lq + lane;
         float* Yz = Y + blockIdx.z * split_stride;
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < 32; c += 16) {
             uint32_t v[16];
             if (nq > 0) {
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(64 * ch + c);
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(cb + c);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
                     "[%16];"
@@ -315,7 +334,7 @@ __global__ void __launch_bounds__(256, 1) pf_mma_kernel(const uint8_t* __restric
             if (row < n) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int t = tok0 + 64 * ch + c + i;
+                    const int t = tok0 + cb + c + i;
                     if (t < P) {
                         if (ROW_MAJOR) Yz[static_cast<size_t>(row) * ldy + t] = __uint_as_float(v[i]);
                         else Yz[static_cast<size_t>(t) * ldy + row] = __uint_as_float(v[i]);
@@ -863,7 +882,7 @@ struct HOut {
 };
 
 // X[p] += the `parts` split sums (in split order); then, when w is given,
-// RMSNorm(X[p]) * w into column p of the k-major Xn[H][ldn]; with ho.h[p],
+// RMSNorm(X[p]) * w into column p of the GEMM input Xn (put_in); with ho.h[p],
 // X[p] is also stored there.  Grid P.  SMALL (a batched decode step, P <= 16):
 // 1024 threads, each holding the elements tid + 1024 e (H <= 16384), every
 // load issued before the first sum needs one; else (a prefill chunk) 256
@@ -945,10 +964,10 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
 #pragma unroll
         for (int e = 0; e < kAddNormPer; ++e) {
             const int i = tid + T * e;
-            if (i < H) Xn[static_cast<size_t>(i) * ldn + p] = (v[e] * r) * w[i];
+            if (i < H) put_in(Xn, ldn, i, p, (v[e] * r) * w[i]);
         }
     } else {
-        for (int i = tid; i < H; i += T) Xn[static_cast<size_t>(i) * ldn + p] = (x[i] * r) * w[i];
+        for (int i = tid; i < H; i += T) put_in(Xn, ldn, i, p, (x[i] * r) * w[i]);
     }
 }
 
@@ -1137,7 +1156,7 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
 }
 
 // Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h), into column
-// p of the k-major U[v_dim][ldu].  Grid (P, ceil(nv / 8)), one warp per head
+// p of the GEMM input U (put_in).  Grid (P, ceil(nv / 8)), one warp per head
 // (head_v_dim 32/64/128: 1, 2 or 4 values per lane).
 __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restrict__ O, const float* __restrict__ Z,
                                                             int ldz, int zoff, const float* __restrict__ w, int nv,
@@ -1159,7 +1178,7 @@ __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restr
     const float rn = 1.0f / sqrtf(ss / static_cast<float>(dv) + eps);
     for (int e = 0; e < per; ++e) {
         const int i = lane + 32 * e;
-        U[static_cast<size_t>(h * dv + i) * ldu + p] = ((ov[e] * rn) * w[i]) * silu(z[i]);
+        put_in(U, ldu, h * dv + i, p, ((ov[e] * rn) * w[i]) * silu(z[i]));
     }
 }
 
@@ -1226,8 +1245,8 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
 // heads of kv group g of token p over cache rows 0..pos0+p (f32 rows, or
 // quantized records read dequantized), 8 warps taking keys t = warp mod 8 with
 // an online softmax each, then combined.  Without Part (grid z = 1): the
-// output is gated by sigmoid(gate) and stored to column p of the k-major
-// Att[nh*256][lda].  With Part (a batched decode step, grid z = the key
+// output is gated by sigmoid(gate) and stored to column p of the GEMM input
+// Att (put_in).  With Part (a batched decode step, grid z = the key
 // splits): CTA z takes the z-th of gridDim.z equal runs of the rows and stores
 // its running max, sum and unnormalised output per head to Part (merged by
 // pf_attn_merge_kernel).
@@ -1311,7 +1330,7 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
             }
         } else {
             const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
-            Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
+            put_in(Att, lda, h * kHd + tid, p, (A / L) * sigmoid(gt));
         }
     }
 }
@@ -1335,22 +1354,24 @@ __global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* __restr
         A = fmaf(pr[z * (kHd + 2) + tid], f, A);
     }
     const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
-    Att[static_cast<size_t>(h * kHd + tid) * lda + p] = (A / L) * sigmoid(gt);
+    put_in(Att, lda, h * kHd + tid, p, (A / L) * sigmoid(gt));
 }
 
 // A = silu(G) * U, elementwise over the first P columns of k-major [ffn][ldk]
-// arrays, G and U given as split sums (added in order).
+// arrays, G and U given as split sums (added in order); A is a GEMM input
+// (put_in: k-major [ffn][lda], or lda == 0 the tensor-core tiles).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
-                                 size_t stride, float* __restrict__ A, int ffn, int P, int ldk) {
+                                 size_t stride, float* __restrict__ A, int ffn, int P, int ldk, int lda) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= static_cast<size_t>(ffn) * P) return;
-    const size_t i = (e / P) * ldk + (e % P);
+    const int kk = static_cast<int>(e / P), p = static_cast<int>(e % P);
+    const size_t i = static_cast<size_t>(kk) * ldk + p;
     float g = Gp[i], u = Up[i];
     for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
     for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
-    A[i] = silu(g) * u;
+    put_in(A, lda, kk, p, silu(g) * u);
 }
 
 // ------------------------------------------------------------ host side
@@ -1408,9 +1429,10 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     return QG_OK;
 }
 
-// Y = W X with X k-major [k][ldk]: ldk = 4 (a pass of at most 4 columns, the
-// small-batch GEMV), else kPfChunk (the tiled GEMM).  ROW_MAJOR: Y[row][ldy]
-// per split (split stride n * ldy), else Y[token][ldy] (split stride P * ldy).
+// Y = W X: for at most 4 columns (a batched decode step) X packed k-major
+// [k][4] and the small-batch GEMV; else X as the tensor-core tiles of put_xt
+// and pf_mma_kernel.  ROW_MAJOR: Y[row][ldy] per split (split stride n * ldy),
+// else Y[token][ldy] (split stride P * ldy).
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits, unsigned* err) {
@@ -1430,8 +1452,8 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     if (int rc = grant_smem(reinterpret_cast<const void*>(pf_mma_kernel<QT, ROW_MAJOR>), kMmaSmem)) return rc;
     const dim3 grid((n + 127) / 128, (P + 127) / 128, z);
     const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
-    if (int e_ = launch_pdl(pf_mma_kernel<QT, ROW_MAJOR>, grid, dim3(256), kMmaSmem, st, false, W, n, k, X, kPfChunk, Y,
-                            ldy, split_stride, P, per, err))
+    if (int e_ = launch_pdl(pf_mma_kernel<QT, ROW_MAJOR>, grid, dim3(kMmaThreads), kMmaSmem, st, false, W, n, k,
+                            reinterpret_cast<const uint8_t*>(X), Y, ldy, split_stride, P, per, err))
         return e_;
     return QG_OK;
 }
@@ -1491,7 +1513,8 @@ Segs segs_of(const Pass& ps, int il) {
 int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bool lm = false) {
     const qg_config& c = m->cfg;
     const int H = c.hidden, P = ps.col0[ps.n];
-    const int ldk = P <= 4 ? 4 : kPfChunk;  // stride of the k-major GEMM inputs (packed for the small batch)
+    const int ldk = P <= 4 ? 4 : kPfChunk;  // stride of the gate/up outputs, k-major
+    const int ldin = P <= 4 ? 4 : 0;        // GEMM inputs: packed [k][4] columns, or the tensor-core tiles
     const size_t part = static_cast<size_t>(P) * H;
     const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
     unsigned* err = ps.ss[0]->err;  // the small-batch GEMV's bounded waits report here
@@ -1503,7 +1526,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
     for (int il = 0; il < c.n_layers && !rc; ++il) {
         const qg_layer_dev& L = m->layers[il];
         const Segs sg = segs_of(ps, il);
-        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.attn_norm, sc->Xn, ldin, H, c.eps, HOut{}))
             return e_;
         int zin = 1;
         if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin,
@@ -1536,7 +1559,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
                                     m->k_dim, sc->QKn, sc->dt, sc->beta, sg, sc->O, c.n_k_heads, nv, dv))
                 return e_;
             if (int e_ = launch_pdl(pf_gated_norm_kernel, dim3(P, (nv + 7) / 8), dim3(256), 0, st, pdl, sc->O, Z,
-                                    L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps, sc->Uin, ldk))
+                                    L.n_in, C + 2 * nv, L.ssm_norm, nv, dv, c.eps, sc->Uin, ldin))
                 return e_;
             k_out = m->v_dim;
         } else {
@@ -1557,12 +1580,12 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             const int zs = pdl ? kAttnSplits : 1;  // a batched decode step: key splits, then a merge
             float* part = zs > 1 ? sc->Ap : nullptr;
             const dim3 grid(P, nkv, zs);
-            rc = kvq ? launch_causal<true>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk, part)
-                     : launch_causal<false>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldk, part);
+            rc = kvq ? launch_causal<true>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldin, part)
+                     : launch_causal<false>(gs, grid, st, pdl, sc->Qn, Z, L.n_in, sg, kvd, sc->Uin, ldin, part);
             if (rc) break;
             if (part) {
                 if (int e_ = launch_pdl(pf_attn_merge_kernel, dim3(P, c.n_heads), dim3(kHd), 0, st, pdl, part, zs, Z,
-                                        L.n_in, sc->Uin, ldk))
+                                        L.n_in, sc->Uin, ldin))
                     return e_;
             }
             k_out = m->q_dim;
@@ -1570,7 +1593,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
         if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending,
                                       err)))
             break;
-        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldk, H, c.eps, HOut{}))
+        if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldin, H, c.eps, HOut{}))
             return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
@@ -1578,7 +1601,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
         if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
         const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
         if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, pdl,
-                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk))
+                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk, ldin))
             return e_;
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
     }
@@ -1586,7 +1609,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
     if (lm) {  // batched lm_head next: the output norm of every column, each stream to its state
         HOut ho{};
         for (int i = 0; i < ps.n; ++i) ho.h[i] = ps.ss[i]->h;
-        return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, m->out_norm, sc->Xn, ldk, H, c.eps, ho);
+        return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, m->out_norm, sc->Xn, ldin, H, c.eps, ho);
     }
     return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, nullptr, nullptr, kPfChunk, H, c.eps, HOut{});
 }
