@@ -142,19 +142,19 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int part, floa
 // Tiles.  A K step of 64 (a quarter super-block) is one 128-byte row per
 // matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16 (the
 // 128-byte swizzle; the matrix descriptor's groups of 8 rows are 1024 bytes
-// apart).  A stage holds four 16 KB tiles (A hi, A lo, B hi, B lo); two
+// apart).  A stage holds four 16 KB tiles (A hi, A lo, B hi, B lo); three
 // stages.  The inputs arrive already in this form: the kernels that produce
 // a GEMM input write it as (quarter, 128-token tile) pairs of hi and lo tiles
-// (put_xt), and one bulk copy per stage brings the pair in.  The 512 threads
-// build the A tiles: thread (row r = tid & 127, part = tid >> 7) dequantizes
-// 16 weights of weight row r (raw bytes loaded a quarter ahead).  Thread 0
-// then issues the stage's 12 MMAs and commits them to the stage's mbarrier,
-// which the threads wait on (bounded) before rebuilding that stage two
-// quarters later.
-constexpr int kMmaTile = 128 * 128;                  // bytes of one 128 x 64 bf16 operand tile
-constexpr int kMmaStage = 4 * kMmaTile;              // A hi, A lo, B hi, B lo
-constexpr int kMmaSmem = 2 * kMmaStage + 1024 + 64;  // two stages, 1024-byte alignment, barriers
-constexpr int kMmaThreads = 512;
+// (put_xt), and one bulk copy per stage brings the pair in.  512 threads build
+// the A tiles: thread (row r = tid & 127, part = tid >> 7) dequantizes 16
+// weights of weight row r (the next quarter's raw bytes are loaded before this
+// quarter's are decoded).  A 17th warp issues each stage's 12 MMAs.
+constexpr int kMmaTile = 128 * 128;      // bytes of one 128 x 64 bf16 operand tile
+constexpr int kMmaStage = 4 * kMmaTile;  // A hi, A lo, B hi, B lo
+constexpr int kMmaStages = 3;
+constexpr int kMmaSmem = kMmaStages * kMmaStage + 1024 + 128;  // stages, 1024-byte alignment, barriers
+constexpr int kMmaBuilders = 512;                               // 16 warps build the stages
+constexpr int kMmaThreads = kMmaBuilders + 32;                  // + the warp that issues the MMAs
 // kind::f16 instruction descriptor: f32 accumulator (bits 4-5 = 1), bf16 A and
 // B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t kMmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -224,6 +224,11 @@ __device__ __forceinline__ void put_in(float* out, int ld, int k, int p, float v
 // Y + z split_stride, token-major Y[t ldy + row] or, ROW_MAJOR, Y[row ldy + t]
 // (k-major for a following GEMM).  err: a bounded wait that gave up sets
 // DEVERR_FULL_WAIT and the CTA stores nothing.
+//
+// Warps 0..15 build stages (warp-level arrivals on `built`, no CTA barrier in
+// the loop); warp 16 waits for a stage's `built` and `full` (its input tiles'
+// bulk copy), issues its MMAs and commits them to `done`, which the builders
+// wait on before they reuse the stage kMmaStages quarters later.
 template <int QT, bool ROW_MAJOR>
 __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* __restrict__ W, int n, int k,
                                                                 const uint8_t* __restrict__ XT, float* __restrict__ Y,
@@ -232,21 +237,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     using Raw = typename std::conditional<QT == QT_Q6K, RawQ6, RawQ4>::type;
     extern __shared__ uint8_t mma_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mma_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* done = reinterpret_cast<uint64_t*>(sm + 2 * kMmaStage);  // [2]: a stage's MMAs have completed
-    uint64_t* full = done + 2;                                          // [2]: a stage's input tiles have landed
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 2);
+    uint64_t* done = reinterpret_cast<uint64_t*>(sm + kMmaStages * kMmaStage);  // a stage's MMAs have completed
+    uint64_t* full = done + kMmaStages;                                          // a stage's input tiles have landed
+    uint64_t* built = full + kMmaStages;                                         // a stage's weight tiles are written
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(built + kMmaStages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * 128, tok0 = blockIdx.y * 128;
     const int nb = k / 256, n8 = (n + 7) & ~7;
-    const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split);
-    const int r = tid & 127, part = tid >> 7;
-    const int grow = row0 + r;
-    const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
-    const int GB = QT == QT_Q6K ? 1680 : 1152;
+    const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split), nq = q1 - q0;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMmaStages; ++i) {
             mbar_init(&done[i], 1);
             mbar_init(&full[i], 1);
+            mbar_init(&built[i], kMmaBuilders / 32);
         }
         fence_mbar_init();
     }
@@ -259,59 +262,80 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tslot;
-    Raw cur{};
-    if (q0 < q1 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, part, cur);
-    bool ok = true;
-    for (int qi = q0; qi < q1; ++qi) {
-        const int j = qi - q0, st = j & 1;
-        uint8_t* sb = sm + st * kMmaStage;
-        const bool free = j < 2 || mbar_wait(&done[st], ((j - 2) >> 1) & 1);  // the MMAs that read this stage are done
-        if (free) {
-            if (tid == 0) {  // this quarter's input tiles [hi | lo] of the CTA's token tile
-                mbar_arrive_expect_tx(&full[st], 2 * kMmaTile);
-                bulk_g2s(sb + 2 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (2 * kMmaTile),
-                         2 * kMmaTile, &full[st], policy_evict_first());
-            }
-            float v[16];
-            if (row_ok) {
-                raw_decode(cur, qi & 3, part, v);
-            } else {
+    if (warp == kMmaBuilders / 32) {  // the MMA warp
+        if (lane == 0) {
+            for (int j = 0, st = 0, use = 0; j < nq; ++j) {
+                const bool ready = mbar_wait(&built[st], use & 1) && mbar_wait(&full[st], use & 1);
+                if (ready) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a_hi = smem_u32(sm + st * kMmaStage), a_lo = a_hi + kMmaTile,
+                                   b_hi = a_hi + 2 * kMmaTile, b_lo = a_hi + 3 * kMmaTile;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-            }
-            put_row16(sb, sb + kMmaTile, r, 2 * part, v);
-            if (qi + 1 < q1 && row_ok)
-                raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, part, cur);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the A tiles, visible to the tensor core
-        if (!__syncthreads_and(free)) {  // every thread leaves together when a wait gave up
-            ok = false;
-            break;
-        }
-        if (tid == 0) {
-            const bool landed = mbar_wait(&full[st], (j >> 1) & 1);
-            if (landed) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a_hi = smem_u32(sb), a_lo = a_hi + kMmaTile, b_hi = a_hi + 2 * kMmaTile,
-                               b_lo = a_hi + 3 * kMmaTile;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
-                    const uint32_t o = 32 * s;
-                    mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
-                    mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
-                    mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+                    for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
+                        const uint32_t o = 32 * s;
+                        mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
+                        mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
+                        mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+                    }
+                } else {
+                    atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
+                }
+                mma_commit(&done[st]);  // also when nothing was issued: the builders' waits stay matched
+                if (++st == kMmaStages) {
+                    st = 0;
+                    ++use;
                 }
             }
-            mma_commit(&done[st]);  // also when nothing was issued: the waits stay matched
-            if (!landed) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
         }
+        __syncwarp();
+    } else {  // builders: thread (row r = tid & 127, part = tid >> 7)
+        const int r = tid & 127, part = tid >> 7;
+        const int grow = row0 + r;
+        const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
+        const int GB = QT == QT_Q6K ? 1680 : 1152;
+        Raw cur{};
+        if (nq > 0 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, part, cur);
+        bool failed = false;
+        for (int j = 0, st = 0, use = 0; j < nq; ++j) {
+            const int qi = q0 + j;
+            uint8_t* sb = sm + st * kMmaStage;
+            const bool free = use == 0 || mbar_wait(&done[st], (use - 1) & 1);  // the MMAs that read this stage are done
+            if (free) {
+                if (tid == 0) {  // this quarter's input tiles [hi | lo] of the CTA's token tile
+                    mbar_arrive_expect_tx(&full[st], 2 * kMmaTile);
+                    bulk_g2s(sb + 2 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (2 * kMmaTile),
+                             2 * kMmaTile, &full[st], policy_evict_first());
+                }
+                Raw nxt{};  // the next quarter's raw bytes, in flight while this one is decoded
+                if (qi + 1 < q1 && row_ok)
+                    raw_load(W + grouped_offset(n8, nb, grow >> 3, (qi + 1) >> 2, GB), grow & 7, (qi + 1) & 3, part,
+                             nxt);
+                float v[16];
+                if (row_ok) {
+                    raw_decode(cur, qi & 3, part, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                }
+                put_row16(sb, sb + kMmaTile, r, 2 * part, v);
+                cur = nxt;
+            } else {
+                failed = true;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tiles, visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&built[st]);
+            if (++st == kMmaStages) {
+                st = 0;
+                ++use;
+            }
+        }
+        if (failed) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
     }
-    const int nq = q1 - q0;
-    if (ok && nq > 0) ok = mbar_wait(&done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);  // every MMA of the CTA is done
+    bool ok = nq == 0 || mbar_wait(&done[(nq - 1) % kMmaStages], ((nq - 1) / kMmaStages) & 1);  // all MMAs done
     ok = __syncthreads_and(ok && !__ldcg(err)) != 0;  // uniform: the accumulator loads are warp-collective
-    if (!ok && tid == 0) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {  // warp w: accumulator lanes 32 (w & 3) .., columns 32 (w >> 2) ..
+    if (ok && warp < kMmaBuilders / 32) {  // warp w: accumulator lanes 32 (w & 3) .., columns 32 (w >> 2) ..
         const int lq = warp & 3, cb = 32 * (warp >> 2);
         const int row = row0 + 32 * lq + lane;
         float* Yz = Y + blockIdx.z * split_stride;
@@ -1357,8 +1381,11 @@ __global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* __restr
     put_in(Att, lda, h * kHd + tid, p, (A / L) * sigmoid(gt));
 }
 
-// A = silu(G) * U, elementwise over the first P columns of k-major [ffn][ldk]
-// arrays, G and U given as split sums (added in order); A is a GEMM input
+// A = silu(G) * U, elementwise over P columns of ffn values, G and U given as
+// split sums (added in order): ldk > 0, k-major [ffn][ldk] (a batched decode
+// step, thread e on value e / P of column e % P); ldk == 0, token-major [P][ffn]
+// (a prefill chunk: consecutive threads on consecutive values of one token, so
+// the tile stores of put_xt stay within 128-byte rows).  A is a GEMM input
 // (put_in: k-major [ffn][lda], or lda == 0 the tensor-core tiles).
 __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
                                  size_t stride, float* __restrict__ A, int ffn, int P, int ldk, int lda) {
@@ -1366,8 +1393,9 @@ __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const
     pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= static_cast<size_t>(ffn) * P) return;
-    const int kk = static_cast<int>(e / P), p = static_cast<int>(e % P);
-    const size_t i = static_cast<size_t>(kk) * ldk + p;
+    const int kk = ldk ? static_cast<int>(e / P) : static_cast<int>(e % ffn);
+    const int p = ldk ? static_cast<int>(e % P) : static_cast<int>(e / ffn);
+    const size_t i = ldk ? static_cast<size_t>(kk) * ldk + p : static_cast<size_t>(p) * ffn + kk;
     float g = Gp[i], u = Up[i];
     for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
     for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
@@ -1458,11 +1486,23 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     return QG_OK;
 }
 
-// K splits of a projection: enough CTAs for one per SM (at most kPfMaxSplit).
+// K splits of a projection (one CTA per SM at a time): the count whose waves
+// of CTAs leave the fewest SMs idle, each split at least 4 quarters long
+// (at most kPfMaxSplit; ties go to fewer splits).
 int splits_for(int n, int k, int P) {
-    const int ctas = ((n + 127) / 128) * ((P + 127) / 128);
-    const int z = device_sms() / ctas;
-    return std::max(1, std::min({z, kPfMaxSplit, k / 64}));
+    const long long ctas = static_cast<long long>((n + 127) / 128) * ((P + 127) / 128), sms = device_sms();
+    const int zmax = std::max(1, std::min(kPfMaxSplit, k / 256));
+    int best = 1;
+    double best_eff = 0.0;
+    for (int z = 1; z <= zmax; ++z) {
+        const long long c = ctas * z, waves = (c + sms - 1) / sms;
+        const double eff = static_cast<double>(c) / static_cast<double>(waves * sms);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = z;
+        }
+    }
+    return best;
 }
 
 template <bool KVQ>
@@ -1597,11 +1637,17 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
-        if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
-        if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
-        const size_t na = static_cast<size_t>(c.ffn) * P;  // k-major [ffn][chunk]: the first P columns
+        if (P <= 4) {  // row-major [ffn][4] sums for the small-batch SwiGLU
+            if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
+            if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
+        } else {  // token-major [P][ffn]
+            if ((rc = gemm<QT_Q4K, false>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, c.ffn, P, zf, st, &zg, err))) break;
+            if ((rc = gemm<QT_Q4K, false>(L.w_up, c.ffn, H, sc->Xn, sc->Up, c.ffn, P, zf, st, &zu, err))) break;
+        }
+        const size_t na = static_cast<size_t>(c.ffn) * P;  // ffn values of each of the P columns
         if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, pdl,
-                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * ldk, sc->A, c.ffn, P, ldk, ldin))
+                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * (P <= 4 ? ldk : P), sc->A, c.ffn,
+                                P, P <= 4 ? ldk : 0, ldin))
             return e_;
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
     }
