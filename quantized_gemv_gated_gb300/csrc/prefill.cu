@@ -1486,23 +1486,20 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     return QG_OK;
 }
 
-// K splits of a projection (one CTA per SM at a time): the count whose waves
-// of CTAs leave the fewest SMs idle, each split at least 4 quarters long
-// (at most kPfMaxSplit; ties go to fewer splits).
+// K splits of a projection (one CTA per SM at a time).  Fewer row x token
+// tiles than SMs: as many splits as fill one wave (each split at least 4
+// quarters, at most kPfMaxSplit).  Otherwise a second split only where it
+// cuts the SMs left idle by the last wave by 10 points or more and K holds 32
+// quarters: the CTA's fixed costs (tensor memory, pipeline fill, the output
+// tile) stay small against its K loop.
 int splits_for(int n, int k, int P) {
     const long long ctas = static_cast<long long>((n + 127) / 128) * ((P + 127) / 128), sms = device_sms();
-    const int zmax = std::max(1, std::min(kPfMaxSplit, k / 256));
-    int best = 1;
-    double best_eff = 0.0;
-    for (int z = 1; z <= zmax; ++z) {
+    if (ctas < sms) return std::max(1, static_cast<int>(std::min<long long>({sms / ctas, k / 256, kPfMaxSplit})));
+    auto eff = [&](long long z) {
         const long long c = ctas * z, waves = (c + sms - 1) / sms;
-        const double eff = static_cast<double>(c) / static_cast<double>(waves * sms);
-        if (eff > best_eff + 0.02) {
-            best_eff = eff;
-            best = z;
-        }
-    }
-    return best;
+        return static_cast<double>(c) / static_cast<double>(waves * sms);
+    };
+    return (k / 64 >= 32 && eff(2) > eff(1) + 0.1) ? 2 : 1;
 }
 
 template <bool KVQ>
