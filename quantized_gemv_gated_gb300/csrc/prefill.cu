@@ -133,25 +133,33 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int part, floa
 // Y = W X for a chunk of P > 4 tokens with tcgen05.mma: the CTA's 128 weight
 // rows are the A operand (M = 128), its 128 tokens the B operand (N = 128),
 // both K-major bf16 tiles in shared memory, fp32 accumulators in tensor
-// memory (128 lanes x 128 columns).  Each operand value v is split into
-// hi = bf16(v) and lo = bf16(v - hi), and every 16-wide K step issues three
-// products, hi*hi + hi*lo + lo*hi: the dropped lo*lo term and the rounding of
-// lo leave a relative error near 2^-16 per product, against 2^-8 for one bf16
-// product (f32 accumulation throughout).
+// memory.  Each operand value v is split three ways, hi = bf16(v), mid =
+// bf16(v - hi), lo = bf16(v - hi - mid) (24 significant bits, as f32 has), and
+// every 16-wide K step issues six products: hi*hi into one 128 x 128
+// accumulator, hi*mid, mid*hi, hi*lo, lo*hi and mid*mid into a second one
+// (columns 128..255), the two added in f32 when the tile is stored; the
+// dropped terms are below 2^-24 of the product.  Measured on one tile of
+// Q4_K-shaped weights against an fp64 product (K = 2560): 3.3e-6 relative,
+// against 2.2e-6 for an f32 FMA loop, 5.4e-6 for a two-way split (hi, lo; three
+// products) and 2.7e-3 for one bf16 product.  The two-way split's extra error,
+// amplified through 32 layers, put the 4B prefill's deep attention K/V rows
+// past 1e-3 of the oracle's.
 //
 // Tiles.  A K step of 64 (a quarter super-block) is one 128-byte row per
 // matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16 (the
 // 128-byte swizzle; the matrix descriptor's groups of 8 rows are 1024 bytes
-// apart).  A stage holds four 16 KB tiles (A hi, A lo, B hi, B lo); three
+// apart).  A stage holds six 16 KB tiles (A hi, mid, lo, B hi, mid, lo); two
 // stages.  The inputs arrive already in this form: the kernels that produce
-// a GEMM input write it as (quarter, 128-token tile) pairs of hi and lo tiles
-// (put_xt), and one bulk copy per stage brings the pair in.  512 threads build
-// the A tiles: thread (row r = tid & 127, part = tid >> 7) dequantizes 16
-// weights of weight row r (the next quarter's raw bytes are loaded before this
-// quarter's are decoded).  A 17th warp issues each stage's 12 MMAs.
+// a GEMM input write it as (quarter, 128-token tile) triples of hi, mid and
+// lo tiles (put_xt), and one bulk copy per stage brings the triple in.  512
+// threads build the A tiles: thread (row r = tid & 127, part = tid >> 7)
+// dequantizes 16 weights of weight row r (the next quarter's raw bytes are
+// loaded before this quarter's are decoded).  A 17th warp issues each stage's
+// 24 MMAs.
 constexpr int kMmaTile = 128 * 128;      // bytes of one 128 x 64 bf16 operand tile
-constexpr int kMmaStage = 4 * kMmaTile;  // A hi, A lo, B hi, B lo
-constexpr int kMmaStages = 3;
+constexpr int kMmaStage = 6 * kMmaTile;  // A hi, mid, lo, B hi, mid, lo
+constexpr int kMmaStages = 2;
+constexpr int kXtBytesPerValue = 6;      // a GEMM input value as put_xt tiles: hi, mid, lo
 constexpr int kMmaSmem = kMmaStages * kMmaStage + 1024 + 128;  // stages, 1024-byte alignment, barriers
 constexpr int kMmaBuilders = 512;                               // 16 warps build the stages
 constexpr int kMmaThreads = kMmaBuilders + 32;                  // + the warp that issues the MMAs
@@ -177,40 +185,48 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-// 8 values as 16 bytes of bf16 hi parts, their lo parts to `lo`.
-__device__ __forceinline__ uint4 bf16_hi_lo(const float* v, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        const __nv_bfloat162 ll = __floats2bfloat162_rn(v[2 * i] - __low2float(hh), v[2 * i + 1] - __high2float(hh));
-        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
-        l[i] = *reinterpret_cast<const uint32_t*>(&ll);
-    }
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
-    return make_uint4(h[0], h[1], h[2], h[3]);
+// 16 consecutive accumulator columns of the warp's 32 lanes (wait::ld before use).
+__device__ __forceinline__ void tmem_ld16(uint32_t ta, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(ta));
 }
-// 16 values of row r (chunks c0, c0 + 1) into a hi and a lo tile.
-__device__ __forceinline__ void put_row16(uint8_t* thi, uint8_t* tlo, int r, int c0, const float* v) {
+// The three-way split of one value: hi, mid, lo as bf16 (round to nearest).
+__device__ __forceinline__ void bf16_split3(float v, __nv_bfloat16& h, __nv_bfloat16& m, __nv_bfloat16& l) {
+    h = __float2bfloat16_rn(v);
+    const float r = v - __bfloat162float(h);  // exact
+    m = __float2bfloat16_rn(r);
+    l = __float2bfloat16_rn(r - __bfloat162float(m));
+}
+// 16 values of row r (chunks c0, c0 + 1) into the hi, mid and lo tiles t0,
+// t0 + kMmaTile, t0 + 2 kMmaTile.
+__device__ __forceinline__ void put_row16(uint8_t* t0, int r, int c0, const float* v) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        uint4 lo;
-        const uint4 hi = bf16_hi_lo(v + 8 * c, lo);
+        __align__(16) __nv_bfloat16 h[8], m[8], l[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bf16_split3(v[8 * c + i], h[i], m[i], l[i]);
         const int off = r * 128 + (((c0 + c) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(thi + off) = hi;
-        *reinterpret_cast<uint4*>(tlo + off) = lo;
+        *reinterpret_cast<uint4*>(t0 + off) = *reinterpret_cast<const uint4*>(h);
+        *reinterpret_cast<uint4*>(t0 + kMmaTile + off) = *reinterpret_cast<const uint4*>(m);
+        *reinterpret_cast<uint4*>(t0 + 2 * kMmaTile + off) = *reinterpret_cast<const uint4*>(l);
     }
 }
 // A GEMM input value (k, token p) of a prefill chunk in the tensor-core form:
-// the (quarter k / 64, token tile p / 128) pair of tiles [hi | lo], 32 KB each,
-// row p % 128, element k % 64.  Tokens P..255 of a chunk are never read back.
+// the (quarter k / 64, token tile p / 128) triple of tiles [hi | mid | lo], 48 KB
+// each triple, row p % 128, element k % 64.  Tokens P..255 of a chunk are never
+// read back.
 __device__ __forceinline__ void put_xt(uint8_t* xt, int k, int p, float v) {
-    uint8_t* t = xt + static_cast<size_t>((k >> 6) * 2 + (p >> 7)) * (2 * kMmaTile);
+    uint8_t* t = xt + static_cast<size_t>((k >> 6) * 2 + (p >> 7)) * (3 * kMmaTile);
     const int row = p & 127;
     const int off = row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + 2 * (k & 7);
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    __nv_bfloat16 h, m, l;
+    bf16_split3(v, h, m, l);
     *reinterpret_cast<__nv_bfloat16*>(t + off) = h;
-    *reinterpret_cast<__nv_bfloat16*>(t + kMmaTile + off) = __float2bfloat16_rn(v - __bfloat162float(h));
+    *reinterpret_cast<__nv_bfloat16*>(t + kMmaTile + off) = m;
+    *reinterpret_cast<__nv_bfloat16*>(t + 2 * kMmaTile + off) = l;
 }
 // A GEMM input of a pass: k-major f32 [k][ld], or (ld == 0) the tiles of put_xt.
 __device__ __forceinline__ void put_in(float* out, int ld, int k, int p, float v) {
@@ -253,8 +269,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
         }
         fence_mbar_init();
     }
-    if (warp == 0) {  // 128 columns of tensor memory: the 128 x 128 f32 accumulator
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(128)
+    if (warp == 0) {  // 256 columns of tensor memory: two 128 x 128 f32 accumulators
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(256)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -268,14 +284,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
                 const bool ready = mbar_wait(&built[st], use & 1) && mbar_wait(&full[st], use & 1);
                 if (ready) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t a_hi = smem_u32(sm + st * kMmaStage), a_lo = a_hi + kMmaTile,
-                                   b_hi = a_hi + 2 * kMmaTile, b_lo = a_hi + 3 * kMmaTile;
+                    const uint32_t ah = smem_u32(sm + st * kMmaStage), am = ah + kMmaTile, al = ah + 2 * kMmaTile,
+                                   bh = ah + 3 * kMmaTile, bm = ah + 4 * kMmaTile, bl = ah + 5 * kMmaTile;
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
                         const uint32_t o = 32 * s;
-                        mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_hi + o), (j > 0 || s > 0) ? 1u : 0u);
-                        mma_bf16(tmem, mma_sdesc(a_hi + o), mma_sdesc(b_lo + o), 1u);
-                        mma_bf16(tmem, mma_sdesc(a_lo + o), mma_sdesc(b_hi + o), 1u);
+                        const uint32_t acc = (j > 0 || s > 0) ? 1u : 0u;
+                        mma_bf16(tmem, mma_sdesc(ah + o), mma_sdesc(bh + o), acc);  // hi * hi
+                        // the corrections, apart from hi * hi
+                        mma_bf16(tmem + 128, mma_sdesc(ah + o), mma_sdesc(bm + o), acc);
+                        mma_bf16(tmem + 128, mma_sdesc(am + o), mma_sdesc(bh + o), 1u);
+                        mma_bf16(tmem + 128, mma_sdesc(ah + o), mma_sdesc(bl + o), 1u);
+                        mma_bf16(tmem + 128, mma_sdesc(al + o), mma_sdesc(bh + o), 1u);
+                        mma_bf16(tmem + 128, mma_sdesc(am + o), mma_sdesc(bm + o), 1u);
                     }
                 } else {
                     atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
@@ -301,10 +322,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
             uint8_t* sb = sm + st * kMmaStage;
             const bool free = use == 0 || mbar_wait(&done[st], (use - 1) & 1);  // the MMAs that read this stage are done
             if (free) {
-                if (tid == 0) {  // this quarter's input tiles [hi | lo] of the CTA's token tile
-                    mbar_arrive_expect_tx(&full[st], 2 * kMmaTile);
-                    bulk_g2s(sb + 2 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (2 * kMmaTile),
-                             2 * kMmaTile, &full[st], policy_evict_first());
+                if (tid == 0) {  // this quarter's input tiles [hi | mid | lo] of the CTA's token tile
+                    mbar_arrive_expect_tx(&full[st], 3 * kMmaTile);
+                    bulk_g2s(sb + 3 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (3 * kMmaTile),
+                             3 * kMmaTile, &full[st], policy_evict_first());
                 }
                 Raw nxt{};  // the next quarter's raw bytes, in flight while this one is decoded
                 if (qi + 1 < q1 && row_ok)
@@ -317,7 +338,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.0f;
                 }
-                put_row16(sb, sb + kMmaTile, r, 2 * part, v);
+                put_row16(sb, r, 2 * part, v);
                 cur = nxt;
             } else {
                 failed = true;
@@ -341,27 +362,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
         float* Yz = Y + blockIdx.z * split_stride;
 #pragma unroll 1
         for (int c = 0; c < 32; c += 16) {
-            uint32_t v[16];
+            float v[16];
             if (nq > 0) {
                 const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(cb + c);
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-                    "[%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                    : "r"(ta));
+                uint32_t h[16], l[16];
+                tmem_ld16(ta, h);
+                tmem_ld16(ta + 128, l);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(h[i]) + __uint_as_float(l[i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0u;
+                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
             }
             if (row < n) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int t = tok0 + cb + c + i;
                     if (t < P) {
-                        if (ROW_MAJOR) Yz[static_cast<size_t>(row) * ldy + t] = __uint_as_float(v[i]);
-                        else Yz[static_cast<size_t>(t) * ldy + row] = __uint_as_float(v[i]);
+                        if (ROW_MAJOR) Yz[static_cast<size_t>(row) * ldy + t] = v[i];
+                        else Yz[static_cast<size_t>(t) * ldy + row] = v[i];
                     }
                 }
             }
@@ -371,7 +391,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     __syncthreads();
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
     }
 }
 
@@ -1406,6 +1426,8 @@ __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const
 struct Scratch {
     int chunk;
     int* tok;
+    // Xn, Uin and A are GEMM inputs: f32 [k][4] for a batched decode step, the
+    // put_xt tiles (kXtBytesPerValue bytes a value) for a prefill chunk
     float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
     float* Ap;  // the attention's key-split partials of a batched decode step [4][n_heads][kAttnSplits][kHd + 2]
     int* pos;  // device: the pass's first position per segment [kMaxSeg]
@@ -1437,14 +1459,14 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     if (!sc) return set_err(QG_ERR_OOM, "prefill: host allocation");
     sc->chunk = kPfChunk;
     int rc = QG_OK;
-    (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->pos, kMaxSeg)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H)) ||
+    (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->pos, kMaxSeg)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H * kXtBytesPerValue / 4)) ||
            (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, kPfMaxSplit * P * H)) ||
            (rc = pf_alloc(s, &sc->Zp, kPfMaxSplit * P * std::max(n_in, static_cast<size_t>(c.ffn)))) ||
            (rc = pf_alloc(s, &sc->Up, kPfMaxSplit * P * c.ffn)) ||
-           (rc = pf_alloc(s, &sc->A, P * c.ffn)) || (rc = pf_alloc(s, &sc->Cq, P * std::max(m->conv_dim, 1))) ||
+           (rc = pf_alloc(s, &sc->A, P * c.ffn * kXtBytesPerValue / 4)) || (rc = pf_alloc(s, &sc->Cq, P * std::max(m->conv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->dt, P * (c.n_v_heads + 1))) || (rc = pf_alloc(s, &sc->beta, P * (c.n_v_heads + 1))) ||
            (rc = pf_alloc(s, &sc->QKn, P * 2 * std::max(m->k_dim, 1))) ||
-           (rc = pf_alloc(s, &sc->O, P * std::max(m->v_dim, 1))) || (rc = pf_alloc(s, &sc->Uin, P * mid)) ||
+           (rc = pf_alloc(s, &sc->O, P * std::max(m->v_dim, 1))) || (rc = pf_alloc(s, &sc->Uin, P * mid * kXtBytesPerValue / 4)) ||
            (rc = pf_alloc(s, &sc->Qn, P * std::max(m->q_dim, 1))) || (rc = pf_alloc(s, &sc->Ks, P * std::max(m->kv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->Vs, P * std::max(m->kv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->Ap, static_cast<size_t>(4) * std::max(c.n_heads, 1) * kAttnSplits * (kHd + 2))));
