@@ -664,7 +664,7 @@ def run_prefill(args):
         "tokenwise_ms": round(t_tw * 1e3, 3), "tokenwise_tok_s": round(n / t_tw, 1),
         "speedup": round(t_tw / t_pf, 2), "projection_tflops": round(flops / t_pf / 1e12, 2),
         "same_first_token": bool(tok == tok2), "runs": len(times),
-        "arith": "tcgen05.mma bf16 hi/lo split (3 products per K step), f32 accumulators in tensor memory; Q4_K/Q6_K dequantized into shared-memory tiles",
+        "arith": "tcgen05.mma on a three-way bf16 split (hi, mid, lo: 6 products per K step), f32 accumulators in tensor memory; Q4_K/Q6_K dequantized into shared-memory tiles",
     }), flush=True)
 
 
