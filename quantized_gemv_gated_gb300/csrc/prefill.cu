@@ -200,18 +200,29 @@ __device__ __forceinline__ void bf16_split3(float v, __nv_bfloat16& h, __nv_bflo
     m = __float2bfloat16_rn(r);
     l = __float2bfloat16_rn(r - __bfloat162float(m));
 }
+// The three-way split of two values at once (one paired conversion per part),
+// the same values bf16_split3 gives.
+__device__ __forceinline__ void bf16x2_split3(float a, float b, uint32_t& h, uint32_t& m, uint32_t& l) {
+    const __nv_bfloat162 hh = __floats2bfloat162_rn(a, b);
+    const float ra = a - __low2float(hh), rb = b - __high2float(hh);  // exact
+    const __nv_bfloat162 mm = __floats2bfloat162_rn(ra, rb);
+    const __nv_bfloat162 ll = __floats2bfloat162_rn(ra - __low2float(mm), rb - __high2float(mm));
+    h = *reinterpret_cast<const uint32_t*>(&hh);
+    m = *reinterpret_cast<const uint32_t*>(&mm);
+    l = *reinterpret_cast<const uint32_t*>(&ll);
+}
 // 16 values of row r (chunks c0, c0 + 1) into the hi, mid and lo tiles t0,
 // t0 + kMmaTile, t0 + 2 kMmaTile.
 __device__ __forceinline__ void put_row16(uint8_t* t0, int r, int c0, const float* v) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        __align__(16) __nv_bfloat16 h[8], m[8], l[8];
+        uint32_t h[4], m[4], l[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) bf16_split3(v[8 * c + i], h[i], m[i], l[i]);
+        for (int i = 0; i < 4; ++i) bf16x2_split3(v[8 * c + 2 * i], v[8 * c + 2 * i + 1], h[i], m[i], l[i]);
         const int off = r * 128 + (((c0 + c) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(t0 + off) = *reinterpret_cast<const uint4*>(h);
-        *reinterpret_cast<uint4*>(t0 + kMmaTile + off) = *reinterpret_cast<const uint4*>(m);
-        *reinterpret_cast<uint4*>(t0 + 2 * kMmaTile + off) = *reinterpret_cast<const uint4*>(l);
+        *reinterpret_cast<uint4*>(t0 + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(t0 + kMmaTile + off) = make_uint4(m[0], m[1], m[2], m[3]);
+        *reinterpret_cast<uint4*>(t0 + 2 * kMmaTile + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
 }
 // A GEMM input value (k, token p) of a prefill chunk in the tensor-core form:
