@@ -67,7 +67,7 @@ def _check_states(cfg, st, ost, n):
             assert rel(k, ost.kc[il][:n]) <= row_bar(il) and rel(v, ost.vc[il][:n]) <= row_bar(il), f"layer {il}: K/V rows"
 
 
-@pytest.mark.parametrize("n_prompt", [1, 37, 300])
+@pytest.mark.parametrize("n_prompt", [1, 5, 37, 129, 300])
 def test_prefill_tiny_matches_oracle(n_prompt):
     cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=320)
     w = synth.make_model_weights(cfg)
