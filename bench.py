@@ -733,7 +733,8 @@ def run_batch(args):
         "batch_tok_s": round(B * K / dt, 1), "batch_ms_per_step": round(1e3 * dt / K, 3),
         "single_tok_s": round(K / d1, 1), "single_ms_per_step": round(1e3 * d1 / K, 3),
         "ratio": round((B * K / dt) / (K / d1), 2),
-        "path": "small-batch GEMV (4 multiply-adds per weight read)" if B <= 4 else "prefill GEMM tiles",
+        "path": ("small-batch GEMV (4 multiply-adds per weight read)" if B <= 4 else
+                 "small-batch GEMV per group of 4 sequences" if B <= 8 else "prefill tensor-core GEMM tiles"),
     }), flush=True)
 
 

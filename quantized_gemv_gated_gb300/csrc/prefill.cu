@@ -12,8 +12,8 @@
 // The same pass runs the batched decode (the decode session's batched decode):
 // its columns are split into segments, one per sequence, each with that
 // sequence's state and positions, so a lockstep step of n sequences is n
-// single-column segments; with at most 4 columns the projections use a
-// small-batch GEMV that reads each weight once for all of them, and a fixed set
+// single-column segments; with at most 8 columns the projections use a
+// small-batch GEMV that reads each weight once per group of 4, and a fixed set
 // of sequences can replay the whole step as one captured graph (qg_batch_*).
 #include <cuda_bf16.h>
 
@@ -29,7 +29,8 @@ namespace {
 
 constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
 constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
-constexpr int kAttnSplits = 16; // key splits of a batched decode step's attention (up to 4 columns)
+constexpr int kAttnSplits = 16; // key splits of a batched decode step's attention
+constexpr int kSmallBatch = 8;  // columns of a batched decode step on the small-batch GEMV (groups of 4)
 
 // The columns of one pass split into segments: segment s is one sequence's
 // run of consecutive positions pos0[s].. in columns col0[s]..col0[s+1]-1, with
@@ -782,7 +783,7 @@ struct BmArgmax {
 // ends in a masked first-index argmax over all rows (the lm_head of up to 4
 // sequences: EpiArgmaxStep's key and last-arriver protocol per column).
 template <int QT, bool ROW_MAJOR, bool AM>
-__global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, const float* __restrict__ X,
+__global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, const float* __restrict__ X, int xq,
                                                           float* __restrict__ Y, int ldy, size_t split_stride, int nm,
                                                           int ring_off, const BmArgmax am) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -820,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, co
             float4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (i0 + u * kConsumers < kn) v[u] = __ldg(X4 + kb + i0 + u * kConsumers + tid);
+                if (i0 + u * kConsumers < kn) v[u] = __ldg(X4 + static_cast<size_t>(kb + i0 + u * kConsumers + tid) * xq);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (i0 + u * kConsumers < kn) xs[xs_at(i0 + u * kConsumers + tid)] = v[u];
@@ -878,11 +879,13 @@ __global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, co
     }
 }
 
-// Launch of bm4_kernel over nm <= 4 columns.  Parts mode: *parts = the K
-// slices (output parts, split_stride apart).  AM: the argmax words of am.
-// err: the device error word of the bounded ring waits.
+// Launch of bm4_kernel over nm <= 4 columns: input k of the group is the
+// float4 at X + k * xq floats (xq = 4: packed [k][4]; 8: one half of packed
+// [k][8]).  Parts mode: *parts = the K slices (output parts, split_stride
+// apart).  AM: the argmax words of am.  err: the device error word of the
+// bounded ring waits.
 template <int QT, bool ROW_MAJOR, bool AM>
-int launch_bm4(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, size_t split_stride, int nm,
+int launch_bm4(const uint8_t* W, int n, int k, const float* X, int xq, float* Y, int ldy, size_t split_stride, int nm,
                const BmArgmax& am, unsigned* err, cudaStream_t st, int* parts) {
     if (!err) return set_err(QG_ERR_CUDA, "small-batch GEMV: no device error word");
     if (nm < 1 || nm > 4) return set_err(QG_ERR_SHAPE, "small-batch GEMV: %d columns (served: 1..4)", nm);
@@ -902,8 +905,8 @@ int launch_bm4(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy
     const int smem = ring_off + stages * slot;
     auto kern = bm4_kernel<QT, ROW_MAJOR, AM>;
     if (int rc = grant_smem(reinterpret_cast<const void*>(kern), smem)) return rc;
-    if (int e_ = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, true, sh, X, Y, ldy, split_stride, nm, ring_off,
-                            am))
+    if (int e_ = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, true, sh, X, xq / 4, Y, ldy, split_stride, nm,
+                            ring_off, am))
         return e_;
     if (parts) *parts = sh.nsl;
     return QG_OK;
@@ -1440,7 +1443,7 @@ struct Scratch {
     // Xn, Uin and A are GEMM inputs: f32 [k][4] for a batched decode step, the
     // put_xt tiles (kXtBytesPerValue bytes a value) for a prefill chunk
     float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
-    float* Ap;  // the attention's key-split partials of a batched decode step [4][n_heads][kAttnSplits][kHd + 2]
+    float* Ap;  // the attention's key-split partials of a batched decode step [kSmallBatch][n_heads][kAttnSplits][kHd + 2]
     int* pos;  // device: the pass's first position per segment [kMaxSeg]
 };
 
@@ -1480,7 +1483,7 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
            (rc = pf_alloc(s, &sc->O, P * std::max(m->v_dim, 1))) || (rc = pf_alloc(s, &sc->Uin, P * mid * kXtBytesPerValue / 4)) ||
            (rc = pf_alloc(s, &sc->Qn, P * std::max(m->q_dim, 1))) || (rc = pf_alloc(s, &sc->Ks, P * std::max(m->kv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->Vs, P * std::max(m->kv_dim, 1))) ||
-           (rc = pf_alloc(s, &sc->Ap, static_cast<size_t>(4) * std::max(c.n_heads, 1) * kAttnSplits * (kHd + 2))));
+           (rc = pf_alloc(s, &sc->Ap, static_cast<size_t>(kSmallBatch) * std::max(c.n_heads, 1) * kAttnSplits * (kHd + 2))));
     if (rc) {
         delete sc;
         return rc;
@@ -1490,19 +1493,26 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     return QG_OK;
 }
 
-// Y = W X: for at most 4 columns (a batched decode step) X packed k-major
-// [k][4] and the small-batch GEMV; else X as the tensor-core tiles of put_xt
-// and pf_mma_kernel.  ROW_MAJOR: Y[row][ldy] per split (split stride n * ldy),
-// else Y[token][ldy] (split stride P * ldy).
+// Y = W X: for at most kSmallBatch columns (a batched decode step) X packed
+// k-major [k][4] (P <= 4) or [k][8], and the small-batch GEMV once per group of
+// 4 columns; else X as the tensor-core tiles of put_xt and pf_mma_kernel.
+// ROW_MAJOR: Y[row][ldy] per split (split stride n * ldy), else Y[token][ldy]
+// (split stride P * ldy).
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
          int* used_splits, unsigned* err) {
-    if (P <= 4) {  // a batched decode step: the small-batch GEMV over packed [k][4] inputs, one part per K slice
+    if (P <= kSmallBatch) {  // a batched decode step: the small-batch GEMV per 4 columns, one part per K slice
         const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
+        const int xq = P <= 4 ? 4 : 8;
         int parts = 1;
-        const int rc = launch_bm4<QT, ROW_MAJOR, false>(W, n, k, X, Y, ldy, split_stride, P, BmArgmax{}, err, st, &parts);
+        for (int g = 0; 4 * g < P; ++g) {
+            float* Yg = ROW_MAJOR ? Y + 4 * g : Y + static_cast<size_t>(4 * g) * ldy;
+            if (int rc = launch_bm4<QT, ROW_MAJOR, false>(W, n, k, X + 4 * g, xq, Yg, ldy, split_stride,
+                                                          std::min(4, P - 4 * g), BmArgmax{}, err, st, &parts))
+                return rc;
+        }
         if (used_splits) *used_splits = parts;
-        return rc;
+        return QG_OK;
     }
     const int nq = k / 64;
     if (splits > nq) splits = nq;
@@ -1578,17 +1588,18 @@ Segs segs_of(const Pass& ps, int il) {
     return sg;
 }
 
-// lm: the pass ends in the output norm of its (at most 4) columns for
+// lm: the pass ends in the output norm of its (at most kSmallBatch) columns for
 // run_lmhead_batch, each column's stream stored to its state.
 int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bool lm = false) {
     const qg_config& c = m->cfg;
     const int H = c.hidden, P = ps.col0[ps.n];
-    const int ldk = P <= 4 ? 4 : kPfChunk;  // stride of the gate/up outputs, k-major
-    const int ldin = P <= 4 ? 4 : 0;        // GEMM inputs: packed [k][4] columns, or the tensor-core tiles
+    const bool small = P <= kSmallBatch;    // a batched decode step: the small-batch GEMV
+    const int ldk = !small ? kPfChunk : P <= 4 ? 4 : 8;  // stride of the gate/up outputs, k-major
+    const int ldin = small ? ldk : 0;       // GEMM inputs: packed [k][4] or [k][8] columns, or the tensor-core tiles
     const size_t part = static_cast<size_t>(P) * H;
     const bool kvq = ps.ss[0]->kv_format == QG_KV_Q8_0_Q5_1;
     unsigned* err = ps.ss[0]->err;  // the small-batch GEMV's bounded waits report here
-    const bool pdl = P <= 4;        // programmatic chaining of the pass's kernels: a batched decode step only
+    const bool pdl = small;         // programmatic chaining of the pass's kernels: a batched decode step only
     if (int e_ = launch_pdl(pf_embed_kernel, dim3(P), dim3(256), 0, st, pdl, m->embd, sc->tok, H, sc->X))
         return e_;
     int pending = 0;  // split sums of the last projection not yet added to X
@@ -1667,7 +1678,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
-        if (P <= 4) {  // row-major [ffn][4] sums for the small-batch SwiGLU
+        if (small) {  // row-major [ffn][ldk] sums for the small-batch SwiGLU
             if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
             if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
         } else {  // token-major [P][ffn]
@@ -1676,8 +1687,8 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
         }
         const size_t na = static_cast<size_t>(c.ffn) * P;  // ffn values of each of the P columns
         if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, pdl,
-                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * (P <= 4 ? ldk : P), sc->A, c.ffn,
-                                P, P <= 4 ? ldk : 0, ldin))
+                                sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * (small ? ldk : P), sc->A, c.ffn,
+                                P, small ? ldk : 0, ldin))
             return e_;
         rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
     }
@@ -1690,20 +1701,27 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
     return add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, nullptr, nullptr, kPfChunk, H, c.eps, HOut{});
 }
 
-// The lm_head argmax of every column of a batched pass (at most 4, after
-// run_pass with lm): one small-batch GEMV over the output-normed columns in
-// sc->Xn, each column's token into its sequence's slots, masked by its
-// sequence's allow bitset.
+// The lm_head argmax of every column of a batched pass (at most kSmallBatch,
+// after run_pass with lm): one small-batch GEMV per 4 columns over the
+// output-normed columns in sc->Xn, each column's token into its sequence's
+// slots, masked by its sequence's allow bitset.
 int run_lmhead_batch(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st) {
-    BmArgmax am{};
-    for (int i = 0; i < ps.n; ++i) {
-        am.ws[i] = ps.ss[i]->am_ws;
-        am.slots[i] = ps.ss[i]->slots;
-        am.allow[i] = ps.ss[i]->allow;
-        am.err[i] = ps.ss[i]->err;
+    const int xq = ps.n <= 4 ? 4 : 8;
+    for (int g = 0; 4 * g < ps.n; ++g) {
+        BmArgmax am{};
+        const int nm = std::min(4, ps.n - 4 * g);
+        for (int c = 0; c < nm; ++c) {
+            const qg_state* si = ps.ss[4 * g + c];
+            am.ws[c] = si->am_ws;
+            am.slots[c] = si->slots;
+            am.allow[c] = si->allow;
+            am.err[c] = si->err;
+        }
+        if (int rc = launch_bm4<QT_Q6K, false, true>(m->lm_head, m->cfg.vocab, m->cfg.hidden, sc->Xn + 4 * g, xq,
+                                                     nullptr, 0, 0, nm, am, ps.ss[0]->err, st, nullptr))
+            return rc;
     }
-    return launch_bm4<QT_Q6K, false, true>(m->lm_head, m->cfg.vocab, m->cfg.hidden, sc->Xn, nullptr, 0, 0, ps.n, am,
-                                           ps.ss[0]->err, st, nullptr);
+    return QG_OK;
 }
 
 }  // namespace
@@ -1801,10 +1819,10 @@ extern "C" int qg_decode_batch(qg_model* m, qg_state* const* states, int n, cons
         ps.col0[i] = i;
     }
     ps.col0[n] = n;
-    const bool lm4 = n <= 4;  // one batched lm_head for up to 4 sequences
-    rc = run_pass(m, ps, sc, st, lm4);
-    if (!rc && lm4) rc = run_lmhead_batch(m, ps, sc, st);
-    for (int i = 0; i < n && !rc && !lm4; ++i)
+    const bool lmb = n <= kSmallBatch;  // batched lm_head launches, one per 4 sequences
+    rc = run_pass(m, ps, sc, st, lmb);
+    if (!rc && lmb) rc = run_lmhead_batch(m, ps, sc, st);
+    for (int i = 0; i < n && !rc && !lmb; ++i)
         rc = run_lmhead_of(m, states[i], sc->X + static_cast<size_t>(i) * c.hidden, st);
     if (rc) return rc;
     QG_CUDA(cudaStreamSynchronize(st));
@@ -1927,10 +1945,10 @@ extern "C" int qg_batch_step(qg_batch* b, const uint32_t* tokens, const int* pos
             ps.col0[i] = i;
         }
         ps.col0[n] = n;
-        const bool lm4 = n <= 4;  // one batched lm_head for up to 4 sequences
-        if (!rc) rc = run_pass(m, ps, sc, st, lm4);
-        if (!rc && lm4) rc = run_lmhead_batch(m, ps, sc, st);
-        for (int i = 0; i < n && !rc && !lm4; ++i)
+        const bool lmb = n <= kSmallBatch;  // batched lm_head launches, one per 4 sequences
+        if (!rc) rc = run_pass(m, ps, sc, st, lmb);
+        if (!rc && lmb) rc = run_lmhead_batch(m, ps, sc, st);
+        for (int i = 0; i < n && !rc && !lmb; ++i)
             rc = run_lmhead_of(m, b->ss[i], sc->X + static_cast<size_t>(i) * m->cfg.hidden, st);
         for (int i = 0; i < n && !rc; ++i) {
             e = cudaMemcpyAsync(b->pinned + 32 + i, b->ss[i]->slots + 2, sizeof(int), cudaMemcpyDeviceToHost, st);
