@@ -65,7 +65,7 @@ def _run(cfg, n, steps, kv_format=qg.KV_F32, dmax=0.02):
     qg.qg_device_status()
 
 
-@pytest.mark.parametrize("n", [1, 3, 4, 6])
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 6, 8, 9])
 def test_batch_tiny(n):
     _run(dataclasses.replace(synth.CFG_TINY, max_seq_len=64), n, steps=5)
 
