@@ -214,13 +214,17 @@ def measured_peaks():
 
 # profiles/traffic.json records ncu DRAM bytes per launch of the step's kernels,
 # keyed by kernel kind, with a hash of the CUDA sources they were taken from:
-# a record taken from other sources reads as unknown (null).  The batched
-# prefill's source is not part of any decode-step kernel and is left out.
+# a record taken from other sources reads as unknown (null).  Translation
+# units that compile no decode-step kernel are left out: the batched prefill
+# and the standalone building-block entry points with their repacks.
+STEP_FREE_SOURCES = ("prefill.cu", "gemv.cu", "gemv_rows.cu")
+
+
 def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_gemv_gated_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")) and name != "prefill.cu":
+        if name.endswith((".cu", ".cuh")) and name not in STEP_FREE_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
@@ -777,7 +781,7 @@ def run_kernels(args):
             if kind == "q4k":
                 qg.qg_gemv_q4k_planar(w, x, y, n, k, st)
             elif kind == "q6k":
-                qg.qg_gemv_q6k(w, x, y, n, k, st)
+                qg.qg_gemv_q6k_planar(w, x, y, n, k, st)
             else:
                 qg.qg_lmhead_argmax(w, x, n, k, wsp, tok, st)
 

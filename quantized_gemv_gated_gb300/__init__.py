@@ -28,7 +28,7 @@ EXPORTS = [
     "qg_model_create", "qg_model_destroy", "qg_state_create", "qg_state_destroy", "qg_state_reset",
     "qg_state_upload_layer", "qg_state_upload_kv", "qg_state_download_layer", "qg_state_download_hidden",
     "qg_state_kv_len", "qg_state_stream", "qg_state_stats", "qg_state_set_token_mask",
-    "qg_gemv_q4k", "qg_gemv_q6k", "qg_q6k_planar_bytes", "qg_q4k_planar_bytes", "qg_q4k_to_planar",
+    "qg_gemv_q4k", "qg_gemv_q6k", "qg_gemv_q6k_planar", "qg_q6k_planar_bytes", "qg_q4k_planar_bytes", "qg_q4k_to_planar",
     "qg_gemv_q4k_planar",
     "qg_q6k_to_planar", "qg_lmhead_argmax_workspace_bytes", "qg_lmhead_argmax", "qg_lmhead_argmax_noalloc",
     "qg_argmax_f32",
@@ -129,6 +129,7 @@ def lib():
             "qg_state_set_token_mask": [p, p, i],
             "qg_gemv_q4k": [p, p, p, i, i, p],
             "qg_gemv_q6k": [p, p, p, i, i, p],
+            "qg_gemv_q6k_planar": [p, p, p, i, i, p],
             "qg_q6k_to_planar": [p, p, i, i, p],
             "qg_q4k_to_planar": [p, p, i, i, p],
             "qg_gemv_q4k_planar": [p, p, p, i, i, p],
@@ -201,8 +202,12 @@ def qg_gemv_q4k(w, x, y, n, k, stream=None):
     return _check(lib().qg_gemv_q4k(_dev(w), _dev(x), _dev(y), n, k, _stream(stream)))
 
 
-def qg_gemv_q6k(w_planar, x, y, n, k, stream=None):
-    return _check(lib().qg_gemv_q6k(_dev(w_planar), _dev(x), _dev(y), n, k, _stream(stream)))
+def qg_gemv_q6k(w, x, y, n, k, stream=None):
+    return _check(lib().qg_gemv_q6k(_dev(w), _dev(x), _dev(y), n, k, _stream(stream)))
+
+
+def qg_gemv_q6k_planar(w_planar, x, y, n, k, stream=None):
+    return _check(lib().qg_gemv_q6k_planar(_dev(w_planar), _dev(x), _dev(y), n, k, _stream(stream)))
 
 
 def qg_gemv_q4k_planar(w_planar, x, y, n, k, stream=None):

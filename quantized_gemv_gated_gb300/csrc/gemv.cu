@@ -1,4 +1,4 @@
-// Building-block entry points: Q4_K / Q6_K GEMV, the Q6_K planar repack, the
+// Building-block entry points: Q4_K GEMV, planar Q4_K / Q6_K GEMV and repacks, the
 // fused lm_head GEMV + argmax and a plain argmax; plus the error plumbing
 // shared by the whole library.
 #include <cstring>
@@ -241,7 +241,7 @@ int qg_gemv_q4k(const void* w, const float* x, float* y, int n, int k, qg_stream
                                                   reinterpret_cast<cudaStream_t>(stream), true, block_err_ptr());
 }
 
-int qg_gemv_q6k(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream) {
+int qg_gemv_q6k_planar(const void* w_planar, const float* x, float* y, int n, int k, qg_stream stream) {
     int rc = check_gemv_args(w_planar, x, y, n, k);
     if (rc) return rc;
     EpiStore epi{};

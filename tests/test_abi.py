@@ -51,6 +51,15 @@ def test_host_only_entry_points_without_gpu():
         qg.qg_gemv_q6k(16, 16, 16, 0, 256)
     assert e.value.code == qg.QG_ERR_EMPTY
     assert "empty" in qg.qg_last_error()
+    with pytest.raises(qg.QgError) as e:  # raw Q6_K rows: any k multiple of 256, 2-byte aligned rows
+        qg.qg_gemv_q6k(16, 16, 16, 4, 300)
+    assert e.value.code == qg.QG_ERR_SHAPE
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_gemv_q6k(17, 16, 16, 4, 256)
+    assert e.value.code == qg.QG_ERR_ARG
+    with pytest.raises(qg.QgError) as e:
+        qg.qg_gemv_q6k_planar(16, 16, 16, 4, 16640)  # past the engine's K limit
+    assert e.value.code == qg.QG_ERR_SHAPE
 
 
 def test_ctypes_structs_match_header_layout(tmp_path):

@@ -1,13 +1,16 @@
-"""GEMV, Q6_K planar repack, fused lm_head + argmax and argmax on the GPU,
-through the C ABI, against the CPU oracle on the same seeded inputs.
+"""GEMV (Q4_K from raw rows; Q6_K from raw rows and from the planar repack),
+the Q6_K planar repack, fused lm_head + argmax and argmax on the GPU, through
+the C ABI, against the CPU oracle on the same seeded inputs.
 
 Bar (pages' float-GEMV parity, forward_qwen35_cuda.rs pin_reference_gemv):
 the GPU result must sit inside the error bound of the exact (f64) product
-that its arithmetic guarantees -- x held to 2^-23 of each 256-element block's
-largest magnitude M_b, exact integer sub-block sums, f32 accumulation:
-|y - y_exact| <= 2^-23 * sum_k |w_k| M_b(k) + 8 * 2^-24 * sum_k |w_k x_k| --
-and within 1e-5 normwise of the f32 oracle.  Argmax indices are compared
-bit-exactly.
+that its arithmetic guarantees and within 1e-5 normwise of the f32 oracle.
+On the GEMV engine x is held to 2^-23 of each 256-element block's largest
+magnitude M_b, sub-block sums are exact integers, accumulation is f32:
+|y - y_exact| <= 2^-23 * sum_k |w_k| M_b(k) + 8 * 2^-24 * sum_k |w_k x_k|.
+The raw-row Q6_K kernel is plain f32 with at most k/256 + 11 roundings per
+product: |y - y_exact| <= (k/256 + 16) * 2^-24 * sum_k |w_k x_k|.  Argmax
+indices are compared bit-exactly.
 """
 import numpy as np
 import pytest
@@ -35,26 +38,35 @@ def planar(t):
     return dst
 
 
-def run_gemv(t, x):
+def run_gemv(t, x, layout="engine"):
+    """y = W x on the GPU.  layout "engine": Q4_K from raw rows and Q6_K from
+    the planar repack, both on the GEMV engine; "rows": Q6_K straight from raw
+    GGUF rows (qg_gemv_q6k, plain f32 arithmetic)."""
     y = torch.empty(t.n, dtype=torch.float32, device="cuda")
     xd = dev(x)
     if t.qtype == synth.QTYPE_Q4_K:
-        w = dev(t.data)
-        qg.qg_gemv_q4k(w, xd, y, t.n, t.k)
+        assert layout == "engine"
+        qg.qg_gemv_q4k(dev(t.data), xd, y, t.n, t.k)
+    elif layout == "rows":
+        qg.qg_gemv_q6k(dev(t.data), xd, y, t.n, t.k)
     else:
-        w = planar(t)
-        qg.qg_gemv_q6k(w, xd, y, t.n, t.k)
+        qg.qg_gemv_q6k_planar(planar(t), xd, y, t.n, t.k)
     torch.cuda.synchronize()
     qg.qg_device_status()
     return y.cpu().numpy()
 
 
-def check_against_oracle(t, x, y, tight=True):
+def check_against_oracle(t, x, y, tight=True, layout="engine"):
     exact = oracle.gemv_f64(t, x)
     W = np.abs(oracle.dequant(t).astype(np.float64))
     ax = np.abs(x.astype(np.float64))
-    blockmax = np.repeat(ax.reshape(-1, 256).max(axis=1), 256)
-    bound = 2 * F32_EPS * (W @ blockmax) + 8 * F32_EPS * (W @ ax) + 1e-30
+    if layout == "rows":
+        # plain f32: each product passes through at most k/256 + 11 roundings
+        bound = (t.k // 256 + 16) * F32_EPS * (W @ ax) + 1e-30
+        tight = True
+    else:
+        blockmax = np.repeat(ax.reshape(-1, 256).max(axis=1), 256)
+        bound = 2 * F32_EPS * (W @ blockmax) + 8 * F32_EPS * (W @ ax) + 1e-30
     err = np.abs(y.astype(np.float64) - exact)
     assert np.all(err <= bound), f"max err/bound {float(np.max(err / bound)):.3g}"
     ref = oracle.gemv(t, x)
@@ -65,17 +77,21 @@ def check_against_oracle(t, x, y, tight=True):
 SMALL = [(1, 256), (13, 256), (37, 768), (300, 2560), (1000, 1024), (129, 3584), (64, 4096)]
 
 
+# (quant type, layout) of every GEMV entry point: qg_gemv_q4k, qg_gemv_q6k_planar, qg_gemv_q6k
+PATHS = [(synth.QTYPE_Q4_K, "engine"), (synth.QTYPE_Q6_K, "engine"), (synth.QTYPE_Q6_K, "rows")]
+
+
 @pytest.mark.parametrize("n,k", SMALL)
-@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
-def test_gemv_small_shapes(qtype, n, k):
+@pytest.mark.parametrize("qtype,layout", PATHS)
+def test_gemv_small_shapes(qtype, layout, n, k):
     gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
     t = gen(1000 + n + k, n, k)
     x = synth.normal(77 + n, k)
-    check_against_oracle(t, x, run_gemv(t, x))
+    check_against_oracle(t, x, run_gemv(t, x, layout), layout=layout)
 
 
-@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
-def test_gemv_special_inputs(qtype):
+@pytest.mark.parametrize("qtype,layout", PATHS)
+def test_gemv_special_inputs(qtype, layout):
     gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
     t = gen(5, 40, 512)
     cases = [(np.zeros(512, np.float32), True),
@@ -86,11 +102,11 @@ def test_gemv_special_inputs(qtype):
              # largest magnitude, so only the representation bound is promised
              (np.where(np.arange(512) % 256 == 5, 100.0, 1e-3).astype(np.float32), False)]
     for x, tight in cases:
-        y = run_gemv(t, x)
+        y = run_gemv(t, x, layout)
         if not np.any(x):
             assert np.all(y == 0)
         else:
-            check_against_oracle(t, x, y, tight)
+            check_against_oracle(t, x, y, tight, layout)
 
 
 # the standalone-kernel sweep shapes, all rows against the oracle
@@ -98,18 +114,38 @@ SWEEP = [(1024, 1024), (6144, 1024), (9216, 2560), (2560, 9216)]
 
 
 @pytest.mark.parametrize("n,k", SWEEP)
-@pytest.mark.parametrize("qtype", [synth.QTYPE_Q4_K, synth.QTYPE_Q6_K])
-def test_gemv_sweep_shapes(qtype, n, k):
+@pytest.mark.parametrize("qtype,layout", PATHS)
+def test_gemv_sweep_shapes(qtype, layout, n, k):
     gen = synth.q4k_tensor if qtype == synth.QTYPE_Q4_K else synth.q6k_tensor
     t = gen(synth.subseed(synth.MASTER_SEED, f"sweep.{qtype}.{n}x{k}"), n, k)
     x = synth.normal(synth.subseed(synth.MASTER_SEED, f"sweep.x.{k}"), k)
-    y = run_gemv(t, x)
+    y = run_gemv(t, x, layout)
     ref = oracle.gemv(t, x)
     rel = np.max(np.abs(y - ref)) / np.max(np.abs(ref))
     assert rel <= 1e-5, rel
     rows = np.arange(0, n, max(1, n // 97))
     sub = synth.QTensor(t.data.reshape(n, -1)[rows].ravel().copy(), t.qtype, len(rows), k)
-    check_against_oracle(sub, x, y[rows])
+    check_against_oracle(sub, x, y[rows], layout=layout)
+
+
+def test_gemv_q6k_rows_odd_offset_and_long_k():
+    """Raw Q6_K rows start wherever the file puts them: 210-byte blocks leave
+    a row (and a tensor inside a mapped file) only 2-byte aligned, and the
+    row kernel has no K limit.  W at an offset of 2 bytes, k = 16640 (past
+    the engine's 16384)."""
+    n, k = 45, 16640
+    t = synth.q6k_tensor(synth.subseed(synth.MASTER_SEED, "rows.odd"), n, k)
+    x = synth.normal(synth.subseed(synth.MASTER_SEED, "rows.odd.x"), k)
+    buf = torch.zeros(t.data.size + 16, dtype=torch.uint8, device="cuda")
+    buf[2:2 + t.data.size] = dev(t.data)
+    y = torch.empty(n, dtype=torch.float32, device="cuda")
+    qg.qg_gemv_q6k(buf[2:], dev(x), y, n, k)
+    torch.cuda.synchronize()
+    qg.qg_device_status()
+    check_against_oracle(t, x, y.cpu().numpy(), layout="rows")
+    with pytest.raises(qg.QgError) as e:  # odd byte address: refused before any launch
+        qg.qg_gemv_q6k(buf[1:], dev(x), y, n, k)
+    assert e.value.code == qg.QG_ERR_ARG
 
 
 def _planar_slice(nb, b):
