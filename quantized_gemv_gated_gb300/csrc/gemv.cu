@@ -1,6 +1,7 @@
 // Building-block entry points: Q4_K GEMV, planar Q4_K / Q6_K GEMV and repacks, the
 // fused lm_head GEMV + argmax and a plain argmax; plus the error plumbing
 // shared by the whole library.
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -27,12 +28,15 @@ int cuda_err(cudaError_t e, const char* what) {
 int device_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    static int cache[64] = {0};
-    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    static std::atomic<int> cache[64];  // zero-initialised; a racing first call stores the same value
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
     if (v < 1) v = 1;
-    if (dev >= 0 && dev < 64) cache[dev] = v;
+    if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
