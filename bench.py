@@ -743,11 +743,13 @@ def run_batch(args):
 
 
 # GEMV shapes of the kernel mode: the building blocks at the model's shapes
-# (planar layouts, the layers' own path), lm_head with its fused argmax.
+# (planar layouts, the layers' own path), lm_head with its fused argmax, and
+# the Q6_K GEMV on raw rows.
 KERNEL_SHAPES = [
     ("q4k", 1024, 1024), ("q4k", 6144, 1024), ("q4k", 8224, 1024), ("q4k", 7168, 1024),
     ("q4k", 12352, 2560), ("q4k", 9216, 2560), ("q6k", 1024, 3584), ("q6k", 2560, 9216),
     ("lmhead", 248320, 1024), ("lmhead", 248320, 2560),
+    ("q6k-rows", 2560, 9216), ("q6k-rows", 248320, 2560),  # qg_gemv_q6k on raw GGUF rows
 ]
 
 
@@ -760,14 +762,23 @@ def run_kernels(args):
     import quantized_gemv_gated_gb300 as qg
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.Stream()
-    for kind, n, k in KERNEL_SHAPES:
+    shapes = KERNEL_SHAPES
+    if args.shape:
+        shapes = [sh for sh in KERNEL_SHAPES if f"{sh[0]}:{sh[1]}x{sh[2]}" in args.shape]
+        if len(shapes) != len(set(args.shape)):
+            raise SystemExit(f"--shape: not among {[f'{a}:{b}x{c}' for a, b, c in KERNEL_SHAPES]}")
+    for kind, n, k in shapes:
         make = synth.q4k_tensor if kind == "q4k" else synth.q6k_tensor
         t = make(synth.subseed(synth.MASTER_SEED, f"kernel.{kind}.{n}.{k}"), n, k)
         src = torch.from_numpy(t.data).cuda()
-        nbytes = (qg.qg_q4k_planar_bytes if kind == "q4k" else qg.qg_q6k_planar_bytes)(n, k)
+        rows = kind == "q6k-rows"
+        nbytes = t.data.size if rows else (qg.qg_q4k_planar_bytes if kind == "q4k" else qg.qg_q6k_planar_bytes)(n, k)
         copies = max(2, -(-3 * 129 * 2 ** 20 // nbytes))
         ws = []
         for _ in range(copies):
+            if rows:
+                ws.append(src.clone())
+                continue
             w = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
             (qg.qg_q4k_to_planar if kind == "q4k" else qg.qg_q6k_to_planar)(src, w, n, k)
             ws.append(w)
@@ -782,6 +793,8 @@ def run_kernels(args):
                 qg.qg_gemv_q4k_planar(w, x, y, n, k, st)
             elif kind == "q6k":
                 qg.qg_gemv_q6k_planar(w, x, y, n, k, st)
+            elif rows:
+                qg.qg_gemv_q6k(w, x, y, n, k, st)
             else:
                 qg.qg_lmhead_argmax(w, x, n, k, wsp, tok, st)
 
@@ -807,7 +820,8 @@ def run_kernels(args):
         us = e0.elapsed_time(e1) * 1e3 / (max(1, args.steps // 16) * reps)
         algo = nbytes + 4 * k + (4 if kind == "lmhead" else 4 * n)
         gbs = algo / us / 1e3
-        print(json.dumps({"kernel": f"{kind} {n}x{k}", "layout": "planar (grouped, slice-major)",
+        print(json.dumps({"kernel": f"{kind} {n}x{k}",
+                          "layout": "raw GGUF rows" if rows else "planar (grouped, slice-major)",
                           "us_per_launch": round(us, 3), "bytes_per_launch": algo, "GB/s": round(gbs, 1),
                           "frac_of_peak": round(gbs / peak, 4), "peak_GB/s": peak, "peak_kind": peak_kind,
                           "weight_copies": copies, "launches_per_graph": reps}), flush=True)
@@ -834,6 +848,8 @@ def main():
                     help="time qg_prefill of the workload's prompt against token-by-token decode (one JSON line)")
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the decode step: one JSON line per GEMV building block at the model's shapes")
+    ap.add_argument("--shape", action="append", default=None, metavar="KIND:NxK",
+                    help="with --kernels: only these shapes (e.g. q6k-rows:248320x2560); repeatable")
     ap.add_argument("--layer", action="store_true",
                     help="the one-layer workload through qg_deltanet_step: us per step (one JSON line)")
     args = ap.parse_args()

@@ -293,13 +293,13 @@ int qg_gemv_q4k_planar(const void* w_planar, const float* x, float* y, int n, in
 /* y[n] = sum_k deq(W[n][k]) * x[k] for Q6_K (forward_qwen35_cuda.rs
  * gemv_dispatch, float variant), straight from raw GGUF rows: w holds n rows
  * of k/256 210-byte blocks (ql[128], qh[64], int8 scales[16], fp16 d) exactly
- * as the file stores them, 2-byte aligned; x: [k] f32, 8-byte aligned; y: [n]
- * f32, 4-byte aligned.  Plain f32 arithmetic: every product w_k x_k passes
- * through at most k/256 + 11 roundings (products, four-scale block sum, block
- * accumulation, warp tree), so |y - y_exact| <= (k/256 + 16) 2^-24
- * sum_k |w_k x_k|.  k a multiple of 256 else QG_ERR_SHAPE (no upper limit);
- * n == 0 or k == 0 -> QG_ERR_EMPTY; NULL or misaligned pointers ->
- * QG_ERR_ARG. */
+ * as the file stores them, 2-byte aligned; x: [k] f32, 16-byte aligned; y:
+ * [n] f32, 4-byte aligned.  Plain f32 arithmetic: every product w_k x_k
+ * passes through at most k/256 + 13 roundings (an 8-term sum per sub-block
+ * half, the block accumulation, the warp tree; d * scale is exact), so
+ * |y - y_exact| <= (k/256 + 16) 2^-24 sum_k |w_k x_k|.
+ * k a multiple of 256 else QG_ERR_SHAPE (no upper limit); n == 0 or k == 0
+ * -> QG_ERR_EMPTY; NULL or misaligned pointers -> QG_ERR_ARG. */
 int qg_gemv_q6k(const void* w, const float* x, float* y, int n, int k, qg_stream stream);
 
 /* The same product on the library's planar Q6_K layout (made by

@@ -8,7 +8,7 @@ that its arithmetic guarantees and within 1e-5 normwise of the f32 oracle.
 On the GEMV engine x is held to 2^-23 of each 256-element block's largest
 magnitude M_b, sub-block sums are exact integers, accumulation is f32:
 |y - y_exact| <= 2^-23 * sum_k |w_k| M_b(k) + 8 * 2^-24 * sum_k |w_k x_k|.
-The raw-row Q6_K kernel is plain f32 with at most k/256 + 11 roundings per
+The raw-row Q6_K kernel is plain f32 with at most k/256 + 13 roundings per
 product: |y - y_exact| <= (k/256 + 16) * 2^-24 * sum_k |w_k x_k|.  Argmax
 indices are compared bit-exactly.
 """
@@ -61,7 +61,7 @@ def check_against_oracle(t, x, y, tight=True, layout="engine"):
     W = np.abs(oracle.dequant(t).astype(np.float64))
     ax = np.abs(x.astype(np.float64))
     if layout == "rows":
-        # plain f32: each product passes through at most k/256 + 11 roundings
+        # plain f32: each product passes through at most k/256 + 13 roundings
         bound = (t.k // 256 + 16) * F32_EPS * (W @ ax) + 1e-30
         tight = True
     else:
@@ -128,18 +128,21 @@ def test_gemv_sweep_shapes(qtype, layout, n, k):
     check_against_oracle(sub, x, y[rows], layout=layout)
 
 
-def test_gemv_q6k_rows_odd_offset_and_long_k():
+@pytest.mark.parametrize("off", [2, 6, 14])
+def test_gemv_q6k_rows_odd_offset_and_long_k(off):
     """Raw Q6_K rows start wherever the file puts them: 210-byte blocks leave
     a row (and a tensor inside a mapped file) only 2-byte aligned, and the
-    row kernel has no K limit.  W at an offset of 2 bytes, k = 16640 (past
-    the engine's 16384)."""
+    row kernel has no K limit.  W at an offset of `off` bytes from a 16-byte
+    boundary, k = 16640 (past the engine's 16384; 65 blocks, so every row
+    takes four full 16-block chunks and a one-block chunk, each with its own
+    ragged head and tail)."""
     n, k = 45, 16640
     t = synth.q6k_tensor(synth.subseed(synth.MASTER_SEED, "rows.odd"), n, k)
     x = synth.normal(synth.subseed(synth.MASTER_SEED, "rows.odd.x"), k)
     buf = torch.zeros(t.data.size + 16, dtype=torch.uint8, device="cuda")
-    buf[2:2 + t.data.size] = dev(t.data)
+    buf[off:off + t.data.size] = dev(t.data)
     y = torch.empty(n, dtype=torch.float32, device="cuda")
-    qg.qg_gemv_q6k(buf[2:], dev(x), y, n, k)
+    qg.qg_gemv_q6k(buf[off:], dev(x), y, n, k)
     torch.cuda.synchronize()
     qg.qg_device_status()
     check_against_oracle(t, x, y.cpu().numpy(), layout="rows")
