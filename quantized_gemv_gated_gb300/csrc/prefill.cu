@@ -1117,8 +1117,11 @@ __global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, 
 // The delta rule over the chunk: CTA = 32 state rows of one value head, each
 // warp 4 rows held in registers (lane: dims 4 lane..+3) for the whole chunk;
 // per token decay, read, rank-1 update and query as the decode step does
-// (delta_rows4).  The inputs of 32 tokens at a time (the head's normalised q
-// and k, the CTA's v values, the gates) are staged in shared memory by the
+// (delta_rows4), with the decay applied to the read's sum (g (S k)) and each
+// token's query reduced together with the next token's read, so that only
+// the read's reduction lies on the state's chain from token to token.  The
+// inputs of 32 tokens at a time (the head's normalised q and k, the CTA's v
+// values, the decay factors and gates) are staged in shared memory by the
 // whole CTA, so the token loop reads shared memory only.  O [P][v_dim].
 constexpr int kDeltaStage = 32;
 __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq_all, int C, int kdim,
@@ -1138,7 +1141,7 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
     float* O = O_all + static_cast<size_t>(c0) * nv * dv;
     __shared__ __align__(16) float sq[kDeltaStage][kDk];
     __shared__ __align__(16) float sk[kDeltaStage][kDk];
-    __shared__ float sv[kDeltaStage][32];
+    __shared__ __align__(16) float sv[kDeltaStage][32];  // rows read as float4 by each warp
     __shared__ float sg[kDeltaStage], sb[kDeltaStage];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_head = dv / 32;
@@ -1150,6 +1153,8 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
 #pragma unroll
     for (int t = 0; t < 4; ++t) st[t] = *reinterpret_cast<const float4*>(Sg + t * kDk + 4 * lane);
     const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
+    float oq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the pending token's query partial sums
+    int pend = -1;                          // its column, -1: none
     for (int p0 = 0; p0 < P; p0 += kDeltaStage) {
         const int np = min(kDeltaStage, P - p0);
         __syncthreads();  // the previous block's inputs are consumed
@@ -1164,50 +1169,70 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
             sv[t][jj] = Cq[static_cast<size_t>(p0 + t) * C + 2 * kdim + h * dv + jb + jj];
         }
         if (tid < np) {
-            sg[tid] = dt[(p0 + tid) * nv + h];
+            sg[tid] = expf(dt[(p0 + tid) * nv + h]);  // the decay factor, off the token loop's chain
             sb[tid] = beta[(p0 + tid) * nv + h];
         }
         __syncthreads();
         for (int t = 0; t < np; ++t) {
             const float4 kk = *reinterpret_cast<const float4*>(&sk[t][4 * lane]);
             const float4 qq = *reinterpret_cast<const float4*>(&sq[t][4 * lane]);
-            const float vl = lane < 4 ? sv[t][4 * warp + lane] : 0.0f;
-            const float gd = expf(sg[t]), be = sb[t];
-            float4 rr[4];
+            const float4 vv = *reinterpret_cast<const float4*>(&sv[t][4 * warp]);  // the warp's 4 v values
+            const float gd = sg[t], be = sb[t];
+            float a[8];  // the read's partial sums (this token), the query's (the pending token)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // read: (g S) k = g (S k), the decay applied to the sum
+                float d = st[u].x * kk.x;
+                d = fmaf(st[u].y, kk.y, d);
+                d = fmaf(st[u].z, kk.z, d);
+                a[u] = fmaf(st[u].w, kk.w, d);
+                a[4 + u] = oq[u];
+            }
+            // the eight sums over the warp in one transposed xor tree (lanes
+            // paired 16, 8, 4, 2, 1 apart as in a plain tree, the same sums):
+            // each level a lane keeps half of its values and adds the
+            // partner's copy of them; at the end lane l holds sum number
+            // 4 (l >> 4 & 1) + 2 (l >> 3 & 1) + (l >> 2 & 1)
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            float r4[4], r2[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                r4[i] = (b4 ? a[4 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, b4 ? a[i] : a[4 + i], 16);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                r2[i] = (b3 ? r4[2 + i] : r4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? r4[i] : r4[2 + i], 8);
+            float r1 = (b2 ? r2[1] : r2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? r2[0] : r2[1], 4);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+            // read sum u sits in lane 8 (u >> 1) + 4 (u & 1), query sum u 16 lanes on
+            if (pend >= 0 && b4 && (lane & 3) == 0)
+                O[static_cast<size_t>(pend) * vd + h * dv + j + ((lane >> 2) & 3)] = r1 * scale;
             float dot[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                rr[u] = make_float4(gd * st[u].x, gd * st[u].y, gd * st[u].z, gd * st[u].w);  // decay
-                float d = rr[u].x * kk.x;
-                d = fmaf(rr[u].y, kk.y, d);
-                d = fmaf(rr[u].z, kk.z, d);
-                dot[u] = fmaf(rr[u].w, kk.w, d);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], off);  // read
-            float oq[4];
+            for (int u = 0; u < 4; ++u) dot[u] = __shfl_sync(0xffffffffu, r1, 8 * (u >> 1) + 4 * (u & 1));
+            const float vl[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float d = be * (__shfl_sync(0xffffffffu, vl, u) - dot[u]);
-                st[u] = make_float4(fmaf(kk.x, d, rr[u].x), fmaf(kk.y, d, rr[u].y), fmaf(kk.z, d, rr[u].z),
-                                    fmaf(kk.w, d, rr[u].w));  // rank-1 update
+                const float d = be * (vl[u] - gd * dot[u]);
+                st[u] = make_float4(fmaf(kk.x, d, gd * st[u].x), fmaf(kk.y, d, gd * st[u].y),
+                                    fmaf(kk.z, d, gd * st[u].z), fmaf(kk.w, d, gd * st[u].w));  // decay + rank-1 update
                 float q = st[u].x * qq.x;
                 q = fmaf(st[u].y, qq.y, q);
                 q = fmaf(st[u].z, qq.z, q);
-                oq[u] = fmaf(st[u].w, qq.w, q);
+                oq[u] = fmaf(st[u].w, qq.w, q);  // query, reduced with the next token's read
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) oq[u] += __shfl_xor_sync(0xffffffffu, oq[u], off);  // query
-            float mine = 0.0f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (lane == u) mine = oq[u] * scale;
-            if (lane < 4) O[static_cast<size_t>(p0 + t) * vd + h * dv + j + lane] = mine;
+            pend = p0 + t;
         }
+    }
+    if (pend >= 0) {  // the last token's query
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) oq[u] += __shfl_xor_sync(0xffffffffu, oq[u], off);
+        float mine = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (lane == u) mine = oq[u] * scale;
+        if (lane < 4) O[static_cast<size_t>(pend) * vd + h * dv + j + lane] = mine;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) *reinterpret_cast<float4*>(Sg + u * kDk + 4 * lane) = st[u];
