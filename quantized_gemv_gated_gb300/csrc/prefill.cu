@@ -1120,10 +1120,17 @@ __global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, 
 // (delta_rows4), with the decay applied to the read's sum (g (S k)) and each
 // token's query reduced together with the next token's read, so that only
 // the read's reduction lies on the state's chain from token to token.  The
-// inputs of 32 tokens at a time (the head's normalised q and k, the CTA's v
+// inputs of 16 tokens at a time (the head's normalised q and k, the CTA's v
 // values, the decay factors and gates) are staged in shared memory by the
-// whole CTA, so the token loop reads shared memory only.  O [P][v_dim].
-constexpr int kDeltaStage = 32;
+// whole CTA, two stages deep (the next stage's async copies run under this
+// stage's tokens), so the token loop reads shared memory only.  O [P][v_dim].
+constexpr int kDeltaStage = 16;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq_all, int C, int kdim,
                                                        const float* __restrict__ QKn_all,
                                                        const float* __restrict__ dt_all,
@@ -1139,15 +1146,35 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
     const float* dt = dt_all + c0 * nv;
     const float* beta = beta_all + c0 * nv;
     float* O = O_all + static_cast<size_t>(c0) * nv * dv;
-    __shared__ __align__(16) float sq[kDeltaStage][kDk];
-    __shared__ __align__(16) float sk[kDeltaStage][kDk];
-    __shared__ __align__(16) float sv[kDeltaStage][32];  // rows read as float4 by each warp
-    __shared__ float sg[kDeltaStage], sb[kDeltaStage];
+    // two stages: the next one's inputs arrive while this one's tokens run
+    __shared__ __align__(16) float sq[2][kDeltaStage][kDk];
+    __shared__ __align__(16) float sk[2][kDeltaStage][kDk];
+    __shared__ __align__(16) float sv[2][kDeltaStage][32];  // rows read as float4 by each warp
+    __shared__ float sg[2][kDeltaStage], sb[2][kDeltaStage];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_head = dv / 32;
     const int h = blockIdx.x / per_head, jb = (blockIdx.x - h * per_head) * 32, j = jb + 4 * warp;
     const int kh = h % nk;
     const int vd = nv * dv;
+    // async copies of tokens p1 .. p1 + kDeltaStage - 1 (those before P) into stage buffer b:
+    // the head's normalised q and k rows and the CTA's 32 v values (16-byte pieces)
+    auto issue_stage = [&](int p1, int b) {
+        const int n1 = min(kDeltaStage, P - p1);
+        for (int e = tid; e < n1 * 64; e += 256) {
+            const int t = e >> 6, r = e & 63, which = r >> 5, c4 = r & 31;
+            cp_async16((which ? &sk[b][t][0] : &sq[b][t][0]) + 4 * c4,
+                       QKn + (static_cast<size_t>(p1 + t) * 2 * nk + which * nk + kh) * kDk + 4 * c4);
+        }
+        for (int e = tid; e < n1 * 8; e += 256) {
+            const int t = e >> 3, c4 = e & 7;
+            cp_async16(&sv[b][t][4 * c4], Cq + static_cast<size_t>(p1 + t) * C + 2 * kdim + h * dv + jb + 4 * c4);
+        }
+    };
+    issue_stage(0, 0);
+    if (tid < min(kDeltaStage, P)) {
+        sg[0][tid] = expf(dt[tid * nv + h]);  // the decay factor, off the token loop's chain
+        sb[0][tid] = beta[tid * nv + h];
+    }
     float4 st[4];
     float* Sg = S + (static_cast<size_t>(h) * dv + j) * kDk;
 #pragma unroll
@@ -1155,29 +1182,31 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
     const float scale = 1.0f / sqrtf(static_cast<float>(kDk));
     float oq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the pending token's query partial sums
     int pend = -1;                          // its column, -1: none
-    for (int p0 = 0; p0 < P; p0 += kDeltaStage) {
-        const int np = min(kDeltaStage, P - p0);
-        __syncthreads();  // the previous block's inputs are consumed
-        for (int e = tid; e < np * 64; e += 256) {
-            const int t = e >> 6, r = e & 63, which = r >> 5, c4 = r & 31;
-            const float4 v = *reinterpret_cast<const float4*>(
-                QKn + (static_cast<size_t>(p0 + t) * 2 * nk + which * nk + kh) * kDk + 4 * c4);
-            *reinterpret_cast<float4*>((which ? &sk[t][0] : &sq[t][0]) + 4 * c4) = v;
+    cp_async_wait_all();
+    __syncthreads();
+    for (int p0 = 0, cur = 0; p0 < P; p0 += kDeltaStage, cur ^= 1) {
+        const int np = min(kDeltaStage, P - p0), p1 = p0 + kDeltaStage;
+        // the next stage: its copies in flight, its gates in registers (the
+        // exponential taken after this stage's tokens, off their chain)
+        float gn = 0.0f, bn = 0.0f;
+        const bool more = p1 < P;
+        if (more) {
+            issue_stage(p1, cur ^ 1);
+            if (tid < min(kDeltaStage, P - p1)) {
+                gn = dt[(p1 + tid) * nv + h];
+                bn = beta[(p1 + tid) * nv + h];
+            }
         }
-        for (int e = tid; e < np * 32; e += 256) {
-            const int t = e >> 5, jj = e & 31;
-            sv[t][jj] = Cq[static_cast<size_t>(p0 + t) * C + 2 * kdim + h * dv + jb + jj];
-        }
-        if (tid < np) {
-            sg[tid] = expf(dt[(p0 + tid) * nv + h]);  // the decay factor, off the token loop's chain
-            sb[tid] = beta[(p0 + tid) * nv + h];
-        }
-        __syncthreads();
+        const float(*sq_c)[kDk] = sq[cur];
+        const float(*sk_c)[kDk] = sk[cur];
+        const float(*sv_c)[32] = sv[cur];
+        const float* sg_c = sg[cur];
+        const float* sb_c = sb[cur];
         for (int t = 0; t < np; ++t) {
-            const float4 kk = *reinterpret_cast<const float4*>(&sk[t][4 * lane]);
-            const float4 qq = *reinterpret_cast<const float4*>(&sq[t][4 * lane]);
-            const float4 vv = *reinterpret_cast<const float4*>(&sv[t][4 * warp]);  // the warp's 4 v values
-            const float gd = sg[t], be = sb[t];
+            const float4 kk = *reinterpret_cast<const float4*>(&sk_c[t][4 * lane]);
+            const float4 qq = *reinterpret_cast<const float4*>(&sq_c[t][4 * lane]);
+            const float4 vv = *reinterpret_cast<const float4*>(&sv_c[t][4 * warp]);  // the warp's 4 v values
+            const float gd = sg_c[t], be = sb_c[t];
             float a[8];  // the read's partial sums (this token), the query's (the pending token)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {  // read: (g S) k = g (S k), the decay applied to the sum
@@ -1222,6 +1251,12 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
             }
             pend = p0 + t;
         }
+        if (more && tid < min(kDeltaStage, P - p1)) {
+            sg[cur ^ 1][tid] = expf(gn);
+            sb[cur ^ 1][tid] = bn;
+        }
+        cp_async_wait_all();
+        __syncthreads();  // the next stage is in; this one is no longer read (its buffer is refilled next)
     }
     if (pend >= 0) {  // the last token's query
 #pragma unroll
