@@ -447,11 +447,12 @@ constexpr int kBmXs = kBmSliceK + kBmSliceK / 64 + kBmSliceK / 512;  // staged f
 // chunk at fixed offsets from one pointer.
 __device__ __forceinline__ int xs_at(int k) { return k + (k >> 6) + (k >> 9); }
 
+// a += q x, as two packed f32x2 multiply-adds (each half rounds as fmaf does)
 __device__ __forceinline__ void fma4(float4& a, float q, const float4& x) {
-    a.x = fmaf(q, x.x, a.x);
-    a.y = fmaf(q, x.y, a.y);
-    a.z = fmaf(q, x.z, a.z);
-    a.w = fmaf(q, x.w, a.w);
+    const float2 qq = make_float2(q, q);
+    const float2 lo = __ffma2_rn(qq, make_float2(x.x, x.y), make_float2(a.x, a.y));
+    const float2 hi = __ffma2_rn(qq, make_float2(x.z, x.w), make_float2(a.z, a.w));
+    a = make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 // Byte b of v moved to bits 15..22 (Q4_K: low nibble at 15, high at 19) or
 // 17..22 (Q6_K codes), the mantissa bits of 1.0 that the mask-or fills.
