@@ -947,7 +947,7 @@ struct HOut {
 // load issued before the first sum needs one; else (a prefill chunk) 256
 // threads striding over H, so that all P CTAs are resident at once.
 constexpr int kAddNormWide = 1024, kAddNormPer = 16;
-template <bool SMALL>
+template <bool SMALL, int PER = 1>  // PER: values per thread of the wide variant (H <= 1024 PER)
 __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
     pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts, size_t split_stride,
                        const float* __restrict__ w, float* __restrict__ Xn, int ldn, int H, float eps, const HOut ho) {
@@ -960,29 +960,47 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
     const float* yp = Yp + static_cast<size_t>(p) * H;
     float* hp = p < kMaxSeg ? ho.h[p] : nullptr;
     float ss = 0.0f;
-    float v[SMALL ? kAddNormPer : 1];
+    float v[SMALL ? PER : 1];
     if constexpr (SMALL) {
 #pragma unroll
-        for (int e = 0; e < kAddNormPer; ++e) {
+        for (int e = 0; e < PER; ++e) {
             const int i = tid + T * e;
             v[e] = i < H ? x[i] : 0.0f;
         }
         if (parts > 0) {
-            float y[kAddNormPer];
+            float y[PER];
 #pragma unroll
-            for (int e = 0; e < kAddNormPer; ++e) {
+            for (int e = 0; e < PER; ++e) {
                 const int i = tid + T * e;
                 y[e] = i < H ? yp[i] : 0.0f;
             }
-            for (int z = 1; z < parts; ++z) {
+            constexpr int D = PER <= 4 ? 4 : 1;  // parts whose loads are in flight together (registers allowing)
+            if constexpr (D == 1) {
+                for (int z = 1; z < parts; ++z)
 #pragma unroll
-                for (int e = 0; e < kAddNormPer; ++e) {
-                    const int i = tid + T * e;
-                    if (i < H) y[e] += yp[z * split_stride + i];
+                    for (int e = 0; e < PER; ++e) {
+                        const int i = tid + T * e;
+                        if (i < H) y[e] += yp[z * split_stride + i];
+                    }
+            } else {
+                for (int z0 = 1; z0 < parts; z0 += D) {  // added in part order
+                    float tz[D][PER];
+#pragma unroll
+                    for (int zz = 0; zz < D; ++zz)
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) {
+                            const int i = tid + T * e;
+                            tz[zz][e] = (z0 + zz < parts && i < H) ? yp[(z0 + zz) * split_stride + i] : 0.0f;
+                        }
+#pragma unroll
+                    for (int zz = 0; zz < D; ++zz)
+#pragma unroll
+                        for (int e = 0; e < PER; ++e)
+                            if (z0 + zz < parts) y[e] += tz[zz][e];
                 }
             }
 #pragma unroll
-            for (int e = 0; e < kAddNormPer; ++e) {
+            for (int e = 0; e < PER; ++e) {
                 const int i = tid + T * e;
                 if (i < H) {
                     v[e] += y[e];
@@ -991,7 +1009,7 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
             }
         }
 #pragma unroll
-        for (int e = 0; e < kAddNormPer; ++e) {
+        for (int e = 0; e < PER; ++e) {
             const int i = tid + T * e;
             if (i < H) {
                 ss = fmaf(v[e], v[e], ss);
@@ -1003,7 +1021,14 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
             float u = x[i];
             if (parts > 0) {
                 float y = yp[i];
-                for (int z = 1; z < parts; ++z) y += yp[z * split_stride + i];
+                for (int z0 = 1; z0 < parts; z0 += 4) {  // four parts' loads in flight, added in part order
+                    float t4[4];
+#pragma unroll
+                    for (int zz = 0; zz < 4; ++zz) t4[zz] = z0 + zz < parts ? yp[(z0 + zz) * split_stride + i] : 0.0f;
+#pragma unroll
+                    for (int zz = 0; zz < 4; ++zz)
+                        if (z0 + zz < parts) y += t4[zz];
+                }
                 u += y;
                 x[i] = u;
             }
@@ -1021,7 +1046,7 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
     const float r = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
     if constexpr (SMALL) {
 #pragma unroll
-        for (int e = 0; e < kAddNormPer; ++e) {
+        for (int e = 0; e < PER; ++e) {
             const int i = tid + T * e;
             if (i < H) put_in(Xn, ldn, i, p, (v[e] * r) * w[i]);
         }
@@ -1035,9 +1060,12 @@ __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
 // prefill chunk's multi-wave grids more than it saves).
 int add_norm(int P, bool pdl, cudaStream_t st, float* X, const float* Yp, int parts, size_t split_stride,
              const float* w, float* Xn, int ldn, int H, float eps, const HOut& ho) {
+    if (P <= kMaxSeg && H <= 4 * kAddNormWide)  // up to 4 values per thread: the parts' loads stay in registers
+        return launch_pdl(pf_add_norm_kernel<true, 4>, dim3(P), dim3(kAddNormWide), 0, st, pdl, X, Yp, parts,
+                          split_stride, w, Xn, ldn, H, eps, ho);
     if (P <= kMaxSeg)
-        return launch_pdl(pf_add_norm_kernel<true>, dim3(P), dim3(kAddNormWide), 0, st, pdl, X, Yp, parts, split_stride,
-                          w, Xn, ldn, H, eps, ho);
+        return launch_pdl(pf_add_norm_kernel<true, kAddNormPer>, dim3(P), dim3(kAddNormWide), 0, st, pdl, X, Yp, parts,
+                          split_stride, w, Xn, ldn, H, eps, ho);
     return launch_pdl(pf_add_norm_kernel<false>, dim3(P), dim3(256), 0, st, pdl, X, Yp, parts, split_stride, w, Xn, ldn,
                       H, eps, ho);
 }
