@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const DeltaArgs a) {
 }
 
 // h += y, y given as `parts` vectors `stride` floats apart added in order.
-__global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y, int parts, int stride, int n) {
+__global__ void residual_add_kernel(float* h, const float* y, int parts, int stride, int n) {
     pdl_launch_dependents();
     pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;

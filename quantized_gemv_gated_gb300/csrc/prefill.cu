@@ -784,8 +784,8 @@ struct BmArgmax {
 // ends in a masked first-index argmax over all rows (the lm_head of up to 4
 // sequences: EpiArgmaxStep's key and last-arriver protocol per column).
 template <int QT, bool ROW_MAJOR, bool AM>
-__global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, const float* __restrict__ X, int xq,
-                                                          float* __restrict__ Y, int ldy, size_t split_stride, int nm,
+__global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, const float* X, int xq,
+                                                          float* Y, int ldy, size_t split_stride, int nm,
                                                           int ring_off, const BmArgmax am) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, co
             float4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (i0 + u * kConsumers < kn) v[u] = __ldg(X4 + static_cast<size_t>(kb + i0 + u * kConsumers + tid) * xq);
+                if (i0 + u * kConsumers < kn) v[u] = __ldcg(X4 + static_cast<size_t>(kb + i0 + u * kConsumers + tid) * xq);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (i0 + u * kConsumers < kn) xs[xs_at(i0 + u * kConsumers + tid)] = v[u];
@@ -914,19 +914,26 @@ int launch_bm4(const uint8_t* W, int n, int k, const float* X, int xq, float* Y,
 }
 
 // Z = the `parts` split sums of a projection, added in split order.
-__global__ void pf_sum_parts_kernel(const float* __restrict__ Yp, int parts, size_t stride, float* __restrict__ Z,
+__global__ void pf_sum_parts_kernel(const float* Yp, int parts, size_t stride, float* Z,
                                     size_t count) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= count) return;
     float v = Yp[i];
-    for (int z = 1; z < parts; ++z) v += Yp[z * stride + i];
+    for (int z0 = 1; z0 < parts; z0 += 4) {  // four parts' loads in flight, added in part order
+        float t[4];
+#pragma unroll
+        for (int zz = 0; zz < 4; ++zz) t[zz] = z0 + zz < parts ? Yp[(z0 + zz) * stride + i] : 0.0f;
+#pragma unroll
+        for (int zz = 0; zz < 4; ++zz)
+            if (z0 + zz < parts) v += t[zz];
+    }
     Z[i] = v;
 }
 
 // X[p] = E[tok[p]].  Grid P.
-__global__ void pf_embed_kernel(const float* __restrict__ E, const int* __restrict__ tok, int H, float* __restrict__ X) {
+__global__ void pf_embed_kernel(const float* E, const int* tok, int H, float* X) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const int p = blockIdx.x;
@@ -949,8 +956,8 @@ struct HOut {
 constexpr int kAddNormWide = 1024, kAddNormPer = 16;
 template <bool SMALL, int PER = 1>  // PER: values per thread of the wide variant (H <= 1024 PER)
 __global__ void __launch_bounds__(SMALL ? kAddNormWide : 256)
-    pf_add_norm_kernel(float* __restrict__ X, const float* __restrict__ Yp, int parts, size_t split_stride,
-                       const float* __restrict__ w, float* __restrict__ Xn, int ldn, int H, float eps, const HOut ho) {
+    pf_add_norm_kernel(float* X, const float* Yp, int parts, size_t split_stride,
+                       const float* w, float* Xn, int ldn, int H, float eps, const HOut ho) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     constexpr int T = SMALL ? kAddNormWide : 256;
@@ -1075,10 +1082,10 @@ int add_norm(int P, bool pdl, cudaStream_t st, float* X, const float* Yp, int pa
 // the window of the previous call), taps in the decode step's order; no
 // recurrence, so the whole chunk runs at once.  Z rows [qkv C | alpha nv |
 // beta nv | z].  The window moves afterwards (pf_conv_window_kernel).
-__global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P, int C, int nv, int K,
-                                     const Segs sg, const float* __restrict__ wconv,
-                                     const float* __restrict__ dt_bias, const float* __restrict__ a,
-                                     float* __restrict__ Cq, float* __restrict__ dt, float* __restrict__ beta) {
+__global__ void pf_conv_gates_kernel(const float* Z, int ldz, int P, int C, int nv, int K,
+                                     const Segs sg, const float* wconv,
+                                     const float* dt_bias, const float* a,
+                                     float* Cq, float* dt, float* beta) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1108,7 +1115,7 @@ __global__ void pf_conv_gates_kernel(const float* __restrict__ Z, int ldz, int P
 // Each segment's conv window after the pass: its last K-1 inputs, oldest
 // first (from the old window where the segment is shorter than that).  Grid
 // (rows / 256, segments).
-__global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int C, int K, const Segs sg) {
+__global__ void pf_conv_window_kernel(const float* Z, int ldz, int C, int K, const Segs sg) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const int c = blockIdx.x * blockDim.x + threadIdx.x, s = blockIdx.y;
@@ -1125,8 +1132,8 @@ __global__ void pf_conv_window_kernel(const float* __restrict__ Z, int ldz, int 
 
 // Per-head L2 norm of each token's q and k (head_k_dim 128): one warp per
 // (token, q|k, key head); QKn [P][2][nk][128].
-__global__ void pf_l2norm_kernel(const float* __restrict__ Cq, int C, int kdim, int nk, int P, float eps,
-                                 float* __restrict__ QKn) {
+__global__ void pf_l2norm_kernel(const float* Cq, int C, int kdim, int nk, int P, float eps,
+                                 float* QKn) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -1160,11 +1167,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__ Cq_all, int C, int kdim,
-                                                       const float* __restrict__ QKn_all,
-                                                       const float* __restrict__ dt_all,
-                                                       const float* __restrict__ beta_all, const Segs sgs,
-                                                       float* __restrict__ O_all, int nk, int nv, int dv) {
+__global__ void __launch_bounds__(256) pf_delta_kernel(const float* Cq_all, int C, int kdim,
+                                                       const float* QKn_all,
+                                                       const float* dt_all,
+                                                       const float* beta_all, const Segs sgs,
+                                                       float* O_all, int nk, int nv, int dv) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     // segment blockIdx.y: its columns c0.. and its recurrent state
@@ -1305,9 +1312,9 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* __restrict__
 // Gated RMSNorm per value head: U = RMSNorm(o_h) * w * silu(z_h), into column
 // p of the GEMM input U (put_in).  Grid (P, ceil(nv / 8)), one warp per head
 // (head_v_dim 32/64/128: 1, 2 or 4 values per lane).
-__global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restrict__ O, const float* __restrict__ Z,
-                                                            int ldz, int zoff, const float* __restrict__ w, int nv,
-                                                            int dv, float eps, float* __restrict__ U, int ldu) {
+__global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* O, const float* Z,
+                                                            int ldz, int zoff, const float* w, int nv,
+                                                            int dv, float eps, float* U, int ldu) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const int p = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1332,11 +1339,11 @@ __global__ void __launch_bounds__(256) pf_gated_norm_kernel(const float* __restr
 // Attention inputs of token p (position pos0 + p): per-head RMSNorm and
 // partial NEOX rope of q (to Qn [P][nh][256]) and k, and the K and V rows
 // (to the f32 cache rows, or to staging rows for the quantizer).  Grid P.
-__global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restrict__ Z, int ldz, int nh, int nkv,
-                                                           const float* __restrict__ q_norm,
-                                                           const float* __restrict__ k_norm, const Segs sg, int n_rot,
-                                                           float theta_scale, float eps, float* __restrict__ Qn,
-                                                           float* __restrict__ Kst, float* __restrict__ Vst) {
+__global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* Z, int ldz, int nh, int nkv,
+                                                           const float* q_norm,
+                                                           const float* k_norm, const Segs sg, int n_rot,
+                                                           float theta_scale, float eps, float* Qn,
+                                                           float* Kst, float* Vst) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     __shared__ float cs[kHd / 2], sn[kHd / 2];
@@ -1398,10 +1405,10 @@ __global__ void __launch_bounds__(256) pf_attn_prep_kernel(const float* __restri
 // its running max, sum and unnormalised output per head to Part (merged by
 // pf_attn_merge_kernel).
 template <int GS, bool KVQ>
-__global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __restrict__ Qn, const float* __restrict__ Z,
+__global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* Qn, const float* Z,
                                                              int ldz, const Segs sg, int kvd,
-                                                             float* __restrict__ Att, int lda,
-                                                             float* __restrict__ Part) {
+                                                             float* Att, int lda,
+                                                             float* Part) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     __shared__ float wml[8][GS][2];
@@ -1484,21 +1491,33 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* __rest
 
 // The key splits of pf_causal_attn_kernel's Part merged (split order) and
 // gated: CTA (p, h), thread tid = output dim.  An empty split has max -inf.
-__global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* __restrict__ Part, int splits,
-                                                            const float* __restrict__ Z, int ldz,
-                                                            float* __restrict__ Att, int lda) {
+__global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* Part, int splits,
+                                                            const float* Z, int ldz,
+                                                            float* Att, int lda) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const int p = blockIdx.x, h = blockIdx.y, nh = gridDim.y, tid = threadIdx.x;
     const float* pr = Part + (static_cast<size_t>(p) * nh + h) * splits * (kHd + 2);
+    // every split's loads in flight at once (splits <= kAttnSplits), then the
+    // merge in split order
+    float ms[kAttnSplits], ls[kAttnSplits], as[kAttnSplits];
+#pragma unroll
+    for (int z = 0; z < kAttnSplits; ++z) {
+        const bool in = z < splits;
+        ms[z] = in ? pr[z * (kHd + 2) + kHd] : -INFINITY;
+        ls[z] = in ? pr[z * (kHd + 2) + kHd + 1] : 0.0f;
+        as[z] = in ? pr[z * (kHd + 2) + tid] : 0.0f;
+    }
     float M = -INFINITY;
-    for (int z = 0; z < splits; ++z) M = fmaxf(M, pr[z * (kHd + 2) + kHd]);
+#pragma unroll
+    for (int z = 0; z < kAttnSplits; ++z) M = fmaxf(M, ms[z]);
     float L = 0.0f, A = 0.0f;
-    for (int z = 0; z < splits; ++z) {
-        const float mz = pr[z * (kHd + 2) + kHd];
-        const float f = mz == -INFINITY ? 0.0f : expf(mz - M);
-        L = fmaf(pr[z * (kHd + 2) + kHd + 1], f, L);
-        A = fmaf(pr[z * (kHd + 2) + tid], f, A);
+#pragma unroll
+    for (int z = 0; z < kAttnSplits; ++z) {
+        if (z >= splits) break;
+        const float f = ms[z] == -INFINITY ? 0.0f : expf(ms[z] - M);
+        L = fmaf(ls[z], f, L);
+        A = fmaf(as[z], f, A);
     }
     const float gt = Z[static_cast<size_t>(p) * ldz + static_cast<size_t>(h) * 2 * kHd + kHd + tid];
     put_in(Att, lda, h * kHd + tid, p, (A / L) * sigmoid(gt));
@@ -1510,8 +1529,8 @@ __global__ void __launch_bounds__(kHd) pf_attn_merge_kernel(const float* __restr
 // (a prefill chunk: consecutive threads on consecutive values of one token, so
 // the tile stores of put_xt stay within 128-byte rows).  A is a GEMM input
 // (put_in: k-major [ffn][lda], or lda == 0 the tensor-core tiles).
-__global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const float* __restrict__ Up, int uparts,
-                                 size_t stride, float* __restrict__ A, int ffn, int P, int ldk, int lda) {
+__global__ void pf_swiglu_kernel(const float* Gp, int gparts, const float* Up, int uparts,
+                                 size_t stride, float* A, int ffn, int P, int ldk, int lda) {
     pdl_launch_dependents();  // the next kernel of the pass may start its prologue
     pdl_wait();               // everything earlier in the pass is complete and visible
     const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1520,8 +1539,20 @@ __global__ void pf_swiglu_kernel(const float* __restrict__ Gp, int gparts, const
     const int p = ldk ? static_cast<int>(e % P) : static_cast<int>(e / ffn);
     const size_t i = ldk ? static_cast<size_t>(kk) * ldk + p : static_cast<size_t>(p) * ffn + kk;
     float g = Gp[i], u = Up[i];
-    for (int z = 1; z < gparts; ++z) g += Gp[z * stride + i];
-    for (int z = 1; z < uparts; ++z) u += Up[z * stride + i];
+    const int parts = max(gparts, uparts);
+    for (int z0 = 1; z0 < parts; z0 += 4) {  // both sums' loads in flight, each added in part order
+        float tg[4], tu[4];
+#pragma unroll
+        for (int zz = 0; zz < 4; ++zz) {
+            tg[zz] = z0 + zz < gparts ? Gp[(z0 + zz) * stride + i] : 0.0f;
+            tu[zz] = z0 + zz < uparts ? Up[(z0 + zz) * stride + i] : 0.0f;
+        }
+#pragma unroll
+        for (int zz = 0; zz < 4; ++zz) {
+            if (z0 + zz < gparts) g += tg[zz];
+            if (z0 + zz < uparts) u += tu[zz];
+        }
+    }
     put_in(A, lda, kk, p, silu(g) * u);
 }
 
