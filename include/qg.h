@@ -213,7 +213,7 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
 
 /* Batched prompt prefill (the decode session's batched prefill,
  * forward_qwen35_cuda.rs): tokens[0..n_tokens) (HOST) at positions
- * pos0..pos0+n_tokens-1 go through the layers in chunks of up to 256 tokens,
+ * pos0..pos0+n_tokens-1 go through the layers in chunks of up to 1024 tokens,
  * each projection one multi-token GEMM (weights read once per chunk), the conv
  * and delta-rule recurrences token by token inside one kernel per layer, and
  * causal attention over cache rows 0..pos for each token.  It leaves the state
@@ -223,10 +223,10 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
  * of the last token's logits (under the state's token mask): the first
  * generated token, to be fed to qg_decode_token at position pos0 + n_tokens.
  * The first call on a state allocates its scratch, kept until
- * qg_state_destroy (later calls allocate nothing): about 256 x (19 hidden +
+ * qg_state_destroy (later calls allocate nothing): about 1024 x (19 hidden +
  * 17 ffn + 17 max(ffn, w) + w + q_dim + 2 kv_dim + ...) floats, w the widest
  * fused input projection (16 of those terms hold the K-split partial sums;
- * ~0.4 GB at the 4B shape).  Synchronous.
+ * ~1.8 GB at the 4B shape).  Synchronous.
  * Errors: QG_ERR_ARG (NULL, or a state of another model), QG_ERR_SHAPE
  * (n_tokens < 1, head_k_dim != 128, a GQA group other than 1, 2, 4),
  * QG_ERR_POS (positions past the cache), QG_ERR_TOKEN, QG_ERR_OOM,

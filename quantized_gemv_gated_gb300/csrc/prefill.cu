@@ -27,7 +27,7 @@
 namespace qg {
 namespace {
 
-constexpr int kPfChunk = 256;  // prompt tokens per pass through the layers
+constexpr int kPfChunk = 1024;  // prompt tokens per pass through the layers
 constexpr int kPfMaxSplit = 16; // K splits of a projection (in 64-weight quarters)
 constexpr int kAttnSplits = 16; // key splits of a batched decode step's attention
 constexpr int kSmallBatch = 8;  // columns of a batched decode step on the small-batch GEMV (groups of 4)
@@ -161,6 +161,7 @@ constexpr int kMmaTile = 128 * 128;      // bytes of one 128 x 64 bf16 operand t
 constexpr int kMmaStage = 6 * kMmaTile;  // A hi, mid, lo, B hi, mid, lo
 constexpr int kMmaStages = 2;
 constexpr int kXtBytesPerValue = 6;      // a GEMM input value as put_xt tiles: hi, mid, lo
+constexpr int kXtTiles = kPfChunk / 128;  // token tiles of a chunk (input tile triples per quarter)
 constexpr int kMmaSmem = kMmaStages * kMmaStage + 1024 + 128;  // stages, 1024-byte alignment, barriers
 constexpr int kMmaBuilders = 512;                               // 16 warps build the stages
 constexpr int kMmaThreads = kMmaBuilders + 32;                  // + the warp that issues the MMAs
@@ -228,10 +229,10 @@ __device__ __forceinline__ void put_row16(uint8_t* t0, int r, int c0, const floa
 }
 // A GEMM input value (k, token p) of a prefill chunk in the tensor-core form:
 // the (quarter k / 64, token tile p / 128) triple of tiles [hi | mid | lo], 48 KB
-// each triple, row p % 128, element k % 64.  Tokens P..255 of a chunk are never
-// read back.
+// each triple, kXtTiles triples per quarter, row p % 128, element k % 64.
+// Tokens P..kPfChunk-1 of a chunk are never read back.
 __device__ __forceinline__ void put_xt(uint8_t* xt, int k, int p, float v) {
-    uint8_t* t = xt + static_cast<size_t>((k >> 6) * 2 + (p >> 7)) * (3 * kMmaTile);
+    uint8_t* t = xt + static_cast<size_t>((k >> 6) * kXtTiles + (p >> 7)) * (3 * kMmaTile);
     const int row = p & 127;
     const int off = row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + 2 * (k & 7);
     __nv_bfloat16 h, m, l;
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
             if (free) {
                 if (tid == 0) {  // this quarter's input tiles [hi | mid | lo] of the CTA's token tile
                     mbar_arrive_expect_tx(&full[st], 3 * kMmaTile);
-                    bulk_g2s(sb + 3 * kMmaTile, XT + static_cast<size_t>(qi * 2 + blockIdx.y) * (3 * kMmaTile),
+                    bulk_g2s(sb + 3 * kMmaTile, XT + static_cast<size_t>(qi * kXtTiles + blockIdx.y) * (3 * kMmaTile),
                              3 * kMmaTile, &full[st], policy_evict_first());
                 }
                 Raw nxt{};  // the next quarter's raw bytes, in flight while this one is decoded
