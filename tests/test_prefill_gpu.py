@@ -67,9 +67,9 @@ def _check_states(cfg, st, ost, n):
             assert rel(k, ost.kc[il][:n]) <= row_bar(il) and rel(v, ost.vc[il][:n]) <= row_bar(il), f"layer {il}: K/V rows"
 
 
-@pytest.mark.parametrize("n_prompt", [1, 5, 37, 129, 300])
+@pytest.mark.parametrize("n_prompt", [1, 5, 37, 129, 300, 1100])  # 1100: two chunks (1024 + 76 tokens)
 def test_prefill_tiny_matches_oracle(n_prompt):
-    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=320)
+    cfg = dataclasses.replace(synth.CFG_TINY, max_seq_len=max(320, n_prompt + 8))
     w = synth.make_model_weights(cfg)
     m, om = qg.Model(w), oracle.Model(w)
     toks = synth.prompt_tokens(cfg, n_prompt)
