@@ -1565,6 +1565,7 @@ struct Scratch {
     // put_xt tiles (kXtBytesPerValue bytes a value) for a prefill chunk
     float *X, *Xn, *Z, *Yp, *Zp, *Up, *A, *Cq, *dt, *beta, *QKn, *O, *Uin, *Qn, *Ks, *Vs;
     float* Ap;  // the attention's key-split partials of a batched decode step [kSmallBatch][n_heads][kAttnSplits][kHd + 2]
+    size_t cap_yp, cap_zp, cap_up;  // floats of the split-sum buffers Yp, Zp, Up
     int* pos;  // device: the pass's first position per segment [kMaxSeg]
 };
 
@@ -1580,6 +1581,8 @@ int pf_alloc(qg_state* s, T** p, size_t count) {
     return QG_OK;
 }
 
+size_t split_rows(int n, int k, int P);
+
 int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     if (s->pf) {
         *out = static_cast<Scratch*>(s->pf);
@@ -1590,14 +1593,27 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     size_t n_in = 0;
     for (int il = 0; il < c.n_layers; ++il) n_in = std::max(n_in, static_cast<size_t>(m->layers[il].n_in));
     const size_t mid = std::max({static_cast<size_t>(m->v_dim), static_cast<size_t>(m->q_dim), size_t(1)});
+    // the split-sum buffers: as many [n] vectors as the largest split layout
+    // any projection of the model takes for any pass of 1..kPfChunk columns
+    // (the rule of splits_for; gemm refuses a layout past these sizes)
+    size_t rows = 1;
+    for (int il = 0; il < c.n_layers; ++il) {
+        const qg_layer_dev& L = m->layers[il];
+        const int k_out = m->kinds[il] == QG_LAYER_DELTANET ? m->v_dim : m->q_dim;
+        for (int p = 1; p <= kPfChunk; ++p)
+            rows = std::max({rows, split_rows(L.n_in, c.hidden, p), split_rows(c.hidden, k_out, p),
+                             split_rows(c.ffn, c.hidden, p), split_rows(c.hidden, c.ffn, p)});
+    }
     Scratch* sc = new (std::nothrow) Scratch();
     if (!sc) return set_err(QG_ERR_OOM, "prefill: host allocation");
     sc->chunk = kPfChunk;
+    sc->cap_yp = rows * H;
+    sc->cap_zp = rows * std::max(n_in, static_cast<size_t>(c.ffn));
+    sc->cap_up = rows * c.ffn;
     int rc = QG_OK;
     (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->pos, kMaxSeg)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H * kXtBytesPerValue / 4)) ||
-           (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, kPfMaxSplit * P * H)) ||
-           (rc = pf_alloc(s, &sc->Zp, kPfMaxSplit * P * std::max(n_in, static_cast<size_t>(c.ffn)))) ||
-           (rc = pf_alloc(s, &sc->Up, kPfMaxSplit * P * c.ffn)) ||
+           (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, sc->cap_yp)) ||
+           (rc = pf_alloc(s, &sc->Zp, sc->cap_zp)) || (rc = pf_alloc(s, &sc->Up, sc->cap_up)) ||
            (rc = pf_alloc(s, &sc->A, P * c.ffn * kXtBytesPerValue / 4)) || (rc = pf_alloc(s, &sc->Cq, P * std::max(m->conv_dim, 1))) ||
            (rc = pf_alloc(s, &sc->dt, P * (c.n_v_heads + 1))) || (rc = pf_alloc(s, &sc->beta, P * (c.n_v_heads + 1))) ||
            (rc = pf_alloc(s, &sc->QKn, P * 2 * std::max(m->k_dim, 1))) ||
@@ -1614,6 +1630,11 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     return QG_OK;
 }
 
+// An upper bound on the K slices of the small-batch GEMV over k inputs (one
+// output part each): slices of 2048, then at most three for the remainder's
+// binary digits (1024, 512, 256).
+inline int max_slices(int k) { return k / 2048 + 3; }
+
 // Y = W X: for at most kSmallBatch columns (a batched decode step) X packed
 // k-major [k][4] (P <= 4) or [k][8], and the small-batch GEMV once per group of
 // 4 columns; else X as the tensor-core tiles of put_xt and pf_mma_kernel.
@@ -1621,9 +1642,11 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
 // (split stride P * ldy).
 template <int QT, bool ROW_MAJOR>
 int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int P, int splits, cudaStream_t st,
-         int* used_splits, unsigned* err) {
+         int* used_splits, unsigned* err, size_t cap) {
     if (P <= kSmallBatch) {  // a batched decode step: the small-batch GEMV per 4 columns, one part per K slice
         const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
+        if (static_cast<size_t>(max_slices(k)) * split_stride > cap)
+            return set_err(QG_ERR_SHAPE, "prefill: the slice sums of a %d x %d GEMV exceed their buffer", n, k);
         const int xq = P <= 4 ? 4 : 8;
         int parts = 1;
         for (int g = 0; 4 * g < P; ++g) {
@@ -1641,9 +1664,11 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     const int per = (nq + splits - 1) / splits;
     const int z = (nq + per - 1) / per;
     if (used_splits) *used_splits = z;
+    const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
+    if (static_cast<size_t>(z) * split_stride > cap)
+        return set_err(QG_ERR_SHAPE, "prefill: %d K splits of a %d x %d GEMM exceed their buffer", z, n, k);
     if (int rc = grant_smem(reinterpret_cast<const void*>(pf_mma_kernel<QT, ROW_MAJOR>), kMmaSmem)) return rc;
     const dim3 grid((n + 127) / 128, (P + 127) / 128, z);
-    const size_t split_stride = ROW_MAJOR ? static_cast<size_t>(n) * ldy : static_cast<size_t>(P) * ldy;
     if (int e_ = launch_pdl(pf_mma_kernel<QT, ROW_MAJOR>, grid, dim3(kMmaThreads), kMmaSmem, st, false, W, n, k,
                             reinterpret_cast<const uint8_t*>(X), Y, ldy, split_stride, P, per, err))
         return e_;
@@ -1664,6 +1689,18 @@ int splits_for(int n, int k, int P) {
         return static_cast<double>(c) / static_cast<double>(waves * sms);
     };
     return (k / 64 >= 32 && eff(2) > eff(1) + 0.1) ? 2 : 1;
+}
+
+// Columns' worth of split partial sums a projection n x k writes for a pass of
+// P columns (the split buffers hold this many [n] vectors): one part per K
+// slice of [n][8] (row-major) or [P][n] for a batched decode step, else the K
+// splits gemm takes of [P][n] each.
+size_t split_rows(int n, int k, int P) {
+    if (P <= kSmallBatch) return static_cast<size_t>(max_slices(k)) * kSmallBatch;
+    const int nq = k / 64;
+    const int splits = std::min(std::max(splits_for(n, k, P), 1), nq);
+    const int per = (nq + splits - 1) / splits;
+    return static_cast<size_t>((nq + per - 1) / per) * P;
 }
 
 template <bool KVQ>
@@ -1732,7 +1769,7 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             return e_;
         int zin = 1;
         if ((rc = gemm<QT_Q4K, false>(L.w_in, L.n_in, H, sc->Xn, sc->Zp, L.n_in, P, splits_for(L.n_in, H, P), st, &zin,
-                                      err)))
+                                      err, sc->cap_zp)))
             break;
         const float* Z = sc->Zp;  // the input projection's output [P][n_in]: one split is already the sum
         if (zin > 1) {
@@ -1793,25 +1830,26 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
             k_out = m->q_dim;
         }
         if ((rc = gemm<QT_Q4K, false>(L.w_out, H, k_out, sc->Uin, sc->Yp, H, P, splits_for(H, k_out, P), st, &pending,
-                                      err)))
+                                      err, sc->cap_yp)))
             break;
         if (int e_ = add_norm(P, pdl, st, sc->X, sc->Yp, pending, part, L.post_norm, sc->Xn, ldin, H, c.eps, HOut{}))
             return e_;
         const int zf = splits_for(c.ffn, H, P);
         int zg = 1, zu = 1;
         if (small) {  // row-major [ffn][ldk] sums for the small-batch SwiGLU
-            if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err))) break;
-            if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err))) break;
+            if ((rc = gemm<QT_Q4K, true>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, ldk, P, zf, st, &zg, err, sc->cap_zp))) break;
+            if ((rc = gemm<QT_Q4K, true>(L.w_up, c.ffn, H, sc->Xn, sc->Up, ldk, P, zf, st, &zu, err, sc->cap_up))) break;
         } else {  // token-major [P][ffn]
-            if ((rc = gemm<QT_Q4K, false>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, c.ffn, P, zf, st, &zg, err))) break;
-            if ((rc = gemm<QT_Q4K, false>(L.w_up, c.ffn, H, sc->Xn, sc->Up, c.ffn, P, zf, st, &zu, err))) break;
+            if ((rc = gemm<QT_Q4K, false>(L.w_gate, c.ffn, H, sc->Xn, sc->Zp, c.ffn, P, zf, st, &zg, err, sc->cap_zp))) break;
+            if ((rc = gemm<QT_Q4K, false>(L.w_up, c.ffn, H, sc->Xn, sc->Up, c.ffn, P, zf, st, &zu, err, sc->cap_up))) break;
         }
         const size_t na = static_cast<size_t>(c.ffn) * P;  // ffn values of each of the P columns
         if (int e_ = launch_pdl(pf_swiglu_kernel, dim3(static_cast<unsigned>((na + 255) / 256)), dim3(256), 0, st, pdl,
                                 sc->Zp, zg, sc->Up, zu, static_cast<size_t>(c.ffn) * (small ? ldk : P), sc->A, c.ffn,
                                 P, small ? ldk : 0, ldin))
             return e_;
-        rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err);
+        rc = gemm<QT_Q6K, false>(L.w_down, H, c.ffn, sc->A, sc->Yp, H, P, splits_for(H, c.ffn, P), st, &pending, err,
+                        sc->cap_yp);
     }
     if (rc) return rc;
     if (lm) {  // batched lm_head next: the output norm of every column, each stream to its state
