@@ -1416,8 +1416,8 @@ __global__ void __launch_bounds__(256) pf_causal_attn_kernel(const float* Qn, co
     __shared__ __align__(16) float wacc[8][GS][kHd];
     const int p = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sq = seg_of(sg, p);
-    const float* __restrict__ kc = sg.kc[sq];
-    const float* __restrict__ vc = sg.vc[sq];
+    const float* kc = sg.kc[sq];
+    const float* vc = sg.vc[sq];
     const int max_seq = sg.max_seq[sq];
     const int nh = gridDim.y * GS, t_len = sg.pos0[sq] + (p - sg.col0[sq]) + 1;
     float q[GS][8], m[GS], l[GS], acc[GS][8];
