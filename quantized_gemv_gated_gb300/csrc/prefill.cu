@@ -1177,7 +1177,7 @@ __global__ void __launch_bounds__(256) pf_delta_kernel(const float* Cq_all, int 
     pdl_wait();               // everything earlier in the pass is complete and visible
     // segment blockIdx.y: its columns c0.. and its recurrent state
     const int c0 = sgs.col0[blockIdx.y], P = sgs.col0[blockIdx.y + 1] - c0;
-    float* __restrict__ S = sgs.ssm[blockIdx.y];
+    float* S = sgs.ssm[blockIdx.y];
     const float* Cq = Cq_all + static_cast<size_t>(c0) * C;
     const float* QKn = QKn_all + static_cast<size_t>(c0) * 2 * nk * kDk;
     const float* dt = dt_all + c0 * nv;
