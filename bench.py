@@ -231,16 +231,17 @@ def kernel_sources_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
+def ncu_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernel sources changed since the counters were taken."""
+    None when the counters were taken on other shapes than the workload's or
+    the kernel sources changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("sources") != kernel_sources_hash():
+    if not e or e.get("sources") != kernel_sources_hash() or workload not in e.get("shapes", ()):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -503,13 +504,13 @@ def run_ours(args, rank, world, local):
         "step_roofline": {"achieved": round(step_gbs / world, 1), "peak": peak, "unit": "GB/s",
                           "frac": round(step_gbs / world / peak, 4), "peak_kind": peak_kind},
         "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
-                     "frac": dom["frac"], "traffic": ncu_traffic(dom["kernel"]),
+                     "frac": dom["frac"], "traffic": ncu_traffic(dom["kernel"], args.workload),
                      "bytes_per_launch": dom["bytes_per_launch"], "launch_us": dom["us_per_launch"],
                      "share_of_step": dom["share"], "peak_kind": peak_kind,
                      "how": "CUDA events around a graph of PDL-chained launches of this kernel over the model's "
                             "layers (qg_bench_kernel), on the launching stream"},
         "roofline_lmhead": {"achieved": lm["GB/s"], "frac": lm["frac"], "launch_us": lm["us_per_launch"],
-                            "bytes_per_launch": lm["bytes_per_launch"], "traffic": ncu_traffic("lmhead")},
+                            "bytes_per_launch": lm["bytes_per_launch"], "traffic": ncu_traffic("lmhead", args.workload)},
         "kernels": kernels,
         "clocks": clocks,
         "e2e": ({"value": round(world * K / dt2, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,

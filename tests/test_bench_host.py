@@ -115,3 +115,18 @@ def test_bench_modes_are_registered():
     assert out.returncode == 0
     for flag in ("--kv-format", "--prefill", "--batch", "--kernels", "--impl", "--layer"):
         assert flag in out.stdout
+
+
+def test_traffic_records_apply_to_their_shapes_only():
+    """ncu DRAM bytes are reported only for the shapes they were captured on
+    (the 4B projections, shared by the 4b and 4b-long workloads) and only
+    while the step kernels' sources are those of the capture."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    for kind in ("ffn_up", "ffn_down", "dn_in", "ssm_out", "delta", "lmhead"):
+        e = records[kind]
+        fresh = e["sources"] == bench.kernel_sources_hash()
+        assert bench.ncu_traffic(kind, "4b") == (e["dram_bytes_read"] + e["dram_bytes_write"] if fresh else None)
+        assert bench.ncu_traffic(kind, "4b-long") == bench.ncu_traffic(kind, "4b")
+        assert bench.ncu_traffic(kind, "0.8b") is None
+    assert bench.ncu_traffic("no-such-kernel", "4b") is None
