@@ -157,30 +157,33 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int part, floa
 // dequantizes 16 weights of weight row r (the next quarter's raw bytes are
 // loaded before this quarter's are decoded).  A 17th warp issues each stage's
 // 24 MMAs.
-constexpr int kMmaTile = 128 * 128;      // bytes of one 128 x 64 bf16 operand tile
-constexpr int kMmaStage = 6 * kMmaTile;  // A hi, mid, lo, B hi, mid, lo
-constexpr int kMmaStages = 2;
+constexpr int kMmaTile = 128 * 64;       // bytes of one 128 x 32 bf16 operand tile (64-byte rows)
+constexpr int kMmaA = 3 * kMmaTile;      // a stage's weight tiles: hi, mid, lo
+constexpr int kMmaB = 6 * kMmaTile;      // its input tiles: hi, mid, lo of two 128-token tiles ([part][tile])
+constexpr int kMmaStage = kMmaA + kMmaB;  // one half-quarter (32 inputs) of a 128-row x 256-token tile
+constexpr int kMmaStages = 3;
 constexpr int kXtBytesPerValue = 6;      // a GEMM input value as put_xt tiles: hi, mid, lo
-constexpr int kXtTiles = kPfChunk / 128;  // token tiles of a chunk (input tile triples per quarter)
+constexpr int kXtPairs = kPfChunk / 256;  // 256-token tile pairs of a chunk (input blocks per half-quarter)
 constexpr int kMmaSmem = kMmaStages * kMmaStage + 1024 + 128;  // stages, 1024-byte alignment, barriers
 constexpr int kMmaBuilders = 512;                               // 16 warps build the stages
 constexpr int kMmaThreads = kMmaBuilders + 32;                  // + the warp that issues the MMAs
 // kind::f16 instruction descriptor: f32 accumulator (bits 4-5 = 1), bf16 A and
 // B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kMmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kMmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);  // M 128, N 256
+constexpr uint32_t kMmaIdescHalf = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);  // N 128
 
-// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle:
-// start address >> 4, leading offset 16 B (unused by this layout), 8-row
-// groups 1024 B apart, descriptor version 1, swizzle mode 2 (128 B).
+// Shared-memory matrix descriptor of a K-major tile with 64-byte rows and the
+// 64-byte swizzle: start address >> 4, leading offset 16 B (unused by this
+// layout), 8-row groups 512 B apart, descriptor version 1, swizzle mode 4 (64 B).
 __device__ __forceinline__ uint64_t mma_sdesc(uint32_t addr) {
     return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(4) << 61);
 }
-__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(a), "l"(b), "r"(kMmaIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -213,6 +216,10 @@ __device__ __forceinline__ void bf16x2_split3(float a, float b, uint32_t& h, uin
     m = *reinterpret_cast<const uint32_t*>(&mm);
     l = *reinterpret_cast<const uint32_t*>(&ll);
 }
+// Row r of a 64-byte-row tile: its 16-byte chunk c (8 bf16) at
+// r * 64 + (c ^ ((r >> 1) & 3)) * 16 (the 64-byte swizzle: byte-address bits
+// 4-5 xor bits 7-8).
+__device__ __forceinline__ int sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 // 16 values of row r (chunks c0, c0 + 1) into the hi, mid and lo tiles t0,
 // t0 + kMmaTile, t0 + 2 kMmaTile.
 __device__ __forceinline__ void put_row16(uint8_t* t0, int r, int c0, const float* v) {
@@ -221,25 +228,26 @@ __device__ __forceinline__ void put_row16(uint8_t* t0, int r, int c0, const floa
         uint32_t h[4], m[4], l[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) bf16x2_split3(v[8 * c + 2 * i], v[8 * c + 2 * i + 1], h[i], m[i], l[i]);
-        const int off = r * 128 + (((c0 + c) ^ (r & 7)) << 4);
+        const int off = sw64(r, c0 + c);
         *reinterpret_cast<uint4*>(t0 + off) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(t0 + kMmaTile + off) = make_uint4(m[0], m[1], m[2], m[3]);
         *reinterpret_cast<uint4*>(t0 + 2 * kMmaTile + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
 }
 // A GEMM input value (k, token p) of a prefill chunk in the tensor-core form:
-// the (quarter k / 64, token tile p / 128) triple of tiles [hi | mid | lo], 48 KB
-// each triple, kXtTiles triples per quarter, row p % 128, element k % 64.
-// Tokens P..kPfChunk-1 of a chunk are never read back.
+// for half-quarter k / 32 and 256-token pair p / 256 one 48 KB block of six
+// tiles [hi | mid | lo] x [tile 0 | tile 1] (128 tokens each), kXtPairs blocks
+// per half-quarter; row p % 128, element k % 32.  Tokens P..kPfChunk-1 of a
+// chunk are never stored.
 __device__ __forceinline__ void put_xt(uint8_t* xt, int k, int p, float v) {
-    uint8_t* t = xt + static_cast<size_t>((k >> 6) * kXtTiles + (p >> 7)) * (3 * kMmaTile);
+    uint8_t* t = xt + static_cast<size_t>((k >> 5) * kXtPairs + (p >> 8)) * kMmaB + ((p >> 7) & 1) * kMmaTile;
     const int row = p & 127;
-    const int off = row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + 2 * (k & 7);
+    const int off = sw64(row, (k & 31) >> 3) + 2 * (k & 7);
     __nv_bfloat16 h, m, l;
     bf16_split3(v, h, m, l);
     *reinterpret_cast<__nv_bfloat16*>(t + off) = h;
-    *reinterpret_cast<__nv_bfloat16*>(t + kMmaTile + off) = m;
-    *reinterpret_cast<__nv_bfloat16*>(t + 2 * kMmaTile + off) = l;
+    *reinterpret_cast<__nv_bfloat16*>(t + 2 * kMmaTile + off) = m;
+    *reinterpret_cast<__nv_bfloat16*>(t + 4 * kMmaTile + off) = l;
 }
 // A GEMM input of a pass: k-major f32 [k][ld], or (ld == 0) the tiles of put_xt.
 __device__ __forceinline__ void put_in(float* out, int ld, int k, int p, float v) {
@@ -271,19 +279,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     uint64_t* built = full + kMmaStages;                                         // a stage's weight tiles are written
     uint32_t* tslot = reinterpret_cast<uint32_t*>(built + kMmaStages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * 128, tok0 = blockIdx.y * 128;
+    const int row0 = blockIdx.x * 128, tok0 = blockIdx.y * 256;
     const int nb = k / 256, n8 = (n + 7) & ~7;
     const int q0 = blockIdx.z * q_per_split, q1 = min(4 * nb, q0 + q_per_split), nq = q1 - q0;
+    const int nh = 2 * nq;  // half-quarter stages of the split
     if (tid == 0) {
         for (int i = 0; i < kMmaStages; ++i) {
             mbar_init(&done[i], 1);
             mbar_init(&full[i], 1);
-            mbar_init(&built[i], kMmaBuilders / 32);
+            mbar_init(&built[i], kMmaBuilders / 64);  // the 8 warps of the half-quarter's builder group
         }
         fence_mbar_init();
     }
-    if (warp == 0) {  // 256 columns of tensor memory: two 128 x 128 f32 accumulators
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(256)
+    if (warp == 0) {  // all 512 columns of tensor memory: two 128 x 256 f32 accumulators
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)), "r"(512)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -292,24 +301,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tslot;
     if (warp == kMmaBuilders / 32) {  // the MMA warp
+        // a pair whose second token tile holds no token: 128-wide products
+        const uint32_t idesc = tok0 + 128 < P ? kMmaIdesc : kMmaIdescHalf;
         if (lane == 0) {
-            for (int j = 0, st = 0, use = 0; j < nq; ++j) {
+            for (int h = 0, st = 0, use = 0; h < nh; ++h) {
                 const bool ready = mbar_wait(&built[st], use & 1) && mbar_wait(&full[st], use & 1);
                 if (ready) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t ah = smem_u32(sm + st * kMmaStage), am = ah + kMmaTile, al = ah + 2 * kMmaTile,
-                                   bh = ah + 3 * kMmaTile, bm = ah + 4 * kMmaTile, bl = ah + 5 * kMmaTile;
+                    const uint32_t ah = smem_u32(sm + st * kMmaStage), am = ah + kMmaTile, al = ah + 2 * kMmaTile;
+                    // B: the two token tiles of a part are one 256-row operand
+                    const uint32_t bh = ah + kMmaA, bm = bh + 2 * kMmaTile, bl = bh + 4 * kMmaTile;
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {  // K steps of 16 (32 bytes into each 128-byte row)
+                    for (int s = 0; s < 2; ++s) {  // K steps of 16 (32 bytes into each 64-byte row)
                         const uint32_t o = 32 * s;
-                        const uint32_t acc = (j > 0 || s > 0) ? 1u : 0u;
-                        mma_bf16(tmem, mma_sdesc(ah + o), mma_sdesc(bh + o), acc);  // hi * hi
+                        const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
+                        mma_bf16(tmem, mma_sdesc(ah + o), mma_sdesc(bh + o), idesc, acc);  // hi * hi
                         // the corrections, apart from hi * hi
-                        mma_bf16(tmem + 128, mma_sdesc(ah + o), mma_sdesc(bm + o), acc);
-                        mma_bf16(tmem + 128, mma_sdesc(am + o), mma_sdesc(bh + o), 1u);
-                        mma_bf16(tmem + 128, mma_sdesc(ah + o), mma_sdesc(bl + o), 1u);
-                        mma_bf16(tmem + 128, mma_sdesc(al + o), mma_sdesc(bh + o), 1u);
-                        mma_bf16(tmem + 128, mma_sdesc(am + o), mma_sdesc(bm + o), 1u);
+                        mma_bf16(tmem + 256, mma_sdesc(ah + o), mma_sdesc(bm + o), idesc, acc);
+                        mma_bf16(tmem + 256, mma_sdesc(am + o), mma_sdesc(bh + o), idesc, 1u);
+                        mma_bf16(tmem + 256, mma_sdesc(ah + o), mma_sdesc(bl + o), idesc, 1u);
+                        mma_bf16(tmem + 256, mma_sdesc(al + o), mma_sdesc(bh + o), idesc, 1u);
+                        mma_bf16(tmem + 256, mma_sdesc(am + o), mma_sdesc(bm + o), idesc, 1u);
                     }
                 } else {
                     atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
@@ -322,23 +334,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
             }
         }
         __syncwarp();
-    } else {  // builders: thread (row r = tid & 127, part = tid >> 7)
-        const int r = tid & 127, part = tid >> 7;
+    } else {  // builders: thread (row r = tid & 127, part = tid >> 7), group part >> 1 builds half-quarter 2j + group
+        const int r = tid & 127, part = tid >> 7, grp = part >> 1;
         const int grow = row0 + r;
         const bool row_ok = grow < n8;  // rows n..n8-1 are zero in the layout
         const int GB = QT == QT_Q6K ? 1680 : 1152;
         Raw cur{};
         if (nq > 0 && row_ok) raw_load(W + grouped_offset(n8, nb, grow >> 3, q0 >> 2, GB), grow & 7, q0 & 3, part, cur);
         bool failed = false;
-        for (int j = 0, st = 0, use = 0; j < nq; ++j) {
-            const int qi = q0 + j;
+        for (int j = 0; j < nq; ++j) {
+            const int qi = q0 + j, h = 2 * j + grp, st = h % kMmaStages, use = h / kMmaStages;
             uint8_t* sb = sm + st * kMmaStage;
             const bool free = use == 0 || mbar_wait(&done[st], (use - 1) & 1);  // the MMAs that read this stage are done
             if (free) {
-                if (tid == 0) {  // this quarter's input tiles [hi | mid | lo] of the CTA's token tile
-                    mbar_arrive_expect_tx(&full[st], 3 * kMmaTile);
-                    bulk_g2s(sb + 3 * kMmaTile, XT + static_cast<size_t>(qi * kXtTiles + blockIdx.y) * (3 * kMmaTile),
-                             3 * kMmaTile, &full[st], policy_evict_first());
+                if ((tid & 255) == 0) {  // the half-quarter's input tiles of the CTA's two token tiles
+                    mbar_arrive_expect_tx(&full[st], kMmaB);
+                    bulk_g2s(sb + kMmaA, XT + static_cast<size_t>((2 * qi + grp) * kXtPairs + blockIdx.y) * kMmaB, kMmaB,
+                             &full[st], policy_evict_first());
                 }
                 Raw nxt{};  // the next quarter's raw bytes, in flight while this one is decoded
                 if (qi + 1 < q1 && row_ok)
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.0f;
                 }
-                put_row16(sb, r, 2 * part, v);
+                put_row16(sb, r, 2 * (part & 1), v);
                 cur = nxt;
             } else {
                 failed = true;
@@ -359,31 +371,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tiles, visible to the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(&built[st]);
-            if (++st == kMmaStages) {
-                st = 0;
-                ++use;
-            }
         }
         if (failed) atomicOr(err, static_cast<unsigned>(DEVERR_FULL_WAIT));
     }
-    bool ok = nq == 0 || mbar_wait(&done[(nq - 1) % kMmaStages], ((nq - 1) / kMmaStages) & 1);  // all MMAs done
+    bool ok = nh == 0 || mbar_wait(&done[(nh - 1) % kMmaStages], ((nh - 1) / kMmaStages) & 1);  // all MMAs done
     ok = __syncthreads_and(ok && !__ldcg(err)) != 0;  // uniform: the accumulator loads are warp-collective
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok && warp < kMmaBuilders / 32) {  // warp w: accumulator lanes 32 (w & 3) .., columns 32 (w >> 2) ..
-        const int lq = warp & 3, cb = 32 * (warp >> 2);
+    if (ok && warp < kMmaBuilders / 32) {  // warp w: accumulator lanes 32 (w & 3) .., token columns 64 (w >> 2) ..
+        const int lq = warp & 3, cb = 64 * (warp >> 2);
         const int row = row0 + 32 * lq + lane;
         float* Yz = Y + blockIdx.z * split_stride;
 #pragma unroll 1
-        for (int c = 0; c < 32; c += 16) {
+        for (int c = 0; c < 64; c += 16) {
+            const int tc = cb + c;  // the CTA's token column: tile tc >> 7, column tc & 127
             float v[16];
             if (nq > 0) {
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(cb + c);
-                uint32_t h[16], l[16];
-                tmem_ld16(ta, h);
-                tmem_ld16(ta + 128, l);
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + static_cast<uint32_t>(tc);
+                uint32_t hi[16], lo[16];
+                tmem_ld16(ta, hi);        // hi * hi, columns 0..255
+                tmem_ld16(ta + 256, lo);  // the corrections, columns 256..511
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(h[i]) + __uint_as_float(l[i]);
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.0f;
@@ -391,7 +400,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
             if (row < n) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int t = tok0 + cb + c + i;
+                    const int t = tok0 + tc + i;
                     if (t < P) {
                         if (ROW_MAJOR) Yz[static_cast<size_t>(row) * ldy + t] = v[i];
                         else Yz[static_cast<size_t>(t) * ldy + row] = v[i];
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) pf_mma_kernel(const uint8_t* _
     __syncthreads();
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
     }
 }
 
@@ -1596,20 +1605,24 @@ int scratch_of(const qg_model* m, qg_state* s, Scratch** out) {
     // the split-sum buffers: as many [n] vectors as the largest split layout
     // any projection of the model takes for any pass of 1..kPfChunk columns
     // (the rule of splits_for; gemm refuses a layout past these sizes)
-    size_t rows = 1;
+    // (per buffer: Yp takes the output projections and ffn_down, Zp the input
+    // projections and the gate, Up the up projection)
+    size_t rows_y = 1, rows_z = 1, rows_u = 1;
     for (int il = 0; il < c.n_layers; ++il) {
         const qg_layer_dev& L = m->layers[il];
         const int k_out = m->kinds[il] == QG_LAYER_DELTANET ? m->v_dim : m->q_dim;
-        for (int p = 1; p <= kPfChunk; ++p)
-            rows = std::max({rows, split_rows(L.n_in, c.hidden, p), split_rows(c.hidden, k_out, p),
-                             split_rows(c.ffn, c.hidden, p), split_rows(c.hidden, c.ffn, p)});
+        for (int p = 1; p <= kPfChunk; ++p) {
+            rows_y = std::max({rows_y, split_rows(c.hidden, k_out, p), split_rows(c.hidden, c.ffn, p)});
+            rows_z = std::max({rows_z, split_rows(L.n_in, c.hidden, p), split_rows(c.ffn, c.hidden, p)});
+            rows_u = std::max(rows_u, split_rows(c.ffn, c.hidden, p));
+        }
     }
     Scratch* sc = new (std::nothrow) Scratch();
     if (!sc) return set_err(QG_ERR_OOM, "prefill: host allocation");
     sc->chunk = kPfChunk;
-    sc->cap_yp = rows * H;
-    sc->cap_zp = rows * std::max(n_in, static_cast<size_t>(c.ffn));
-    sc->cap_up = rows * c.ffn;
+    sc->cap_yp = rows_y * H;
+    sc->cap_zp = rows_z * std::max(n_in, static_cast<size_t>(c.ffn));
+    sc->cap_up = rows_u * c.ffn;
     int rc = QG_OK;
     (void)((rc = pf_alloc(s, &sc->tok, P)) || (rc = pf_alloc(s, &sc->pos, kMaxSeg)) || (rc = pf_alloc(s, &sc->X, P * H)) || (rc = pf_alloc(s, &sc->Xn, P * H * kXtBytesPerValue / 4)) ||
            (rc = pf_alloc(s, &sc->Z, P * n_in)) || (rc = pf_alloc(s, &sc->Yp, sc->cap_yp)) ||
@@ -1668,26 +1681,33 @@ int gemm(const uint8_t* W, int n, int k, const float* X, float* Y, int ldy, int 
     if (static_cast<size_t>(z) * split_stride > cap)
         return set_err(QG_ERR_SHAPE, "prefill: %d K splits of a %d x %d GEMM exceed their buffer", z, n, k);
     if (int rc = grant_smem(reinterpret_cast<const void*>(pf_mma_kernel<QT, ROW_MAJOR>), kMmaSmem)) return rc;
-    const dim3 grid((n + 127) / 128, (P + 127) / 128, z);
+    const dim3 grid((n + 127) / 128, (P + 255) / 256, z);
     if (int e_ = launch_pdl(pf_mma_kernel<QT, ROW_MAJOR>, grid, dim3(kMmaThreads), kMmaSmem, st, false, W, n, k,
                             reinterpret_cast<const uint8_t*>(X), Y, ldy, split_stride, P, per, err))
         return e_;
     return QG_OK;
 }
 
-// K splits of a projection (one CTA per SM at a time).  Fewer row x token
-// tiles than SMs: as many splits as fill one wave (each split at least 4
-// quarters, at most kPfMaxSplit).  Otherwise a second split only where it
-// cuts the SMs left idle by the last wave by 10 points or more and K holds 32
-// quarters: the CTA's fixed costs (tensor memory, pipeline fill, the output
-// tile) stay small against its K loop.
+// K splits of a projection (one CTA per SM at a time).  Fewer row x 256-token
+// tiles than SMs: the split count, up to kPfMaxSplit with at least 8
+// quarters (512 inputs) a split, whose CTAs best fill their waves of SMs, a
+// further split only where it fills 10 points more.  Otherwise a second split
+// only where it cuts the SMs left idle by the last wave by 10 points or more
+// and K holds 32 quarters: the CTA's fixed costs (tensor memory, pipeline
+// fill, the output tile) stay small against its K loop.
 int splits_for(int n, int k, int P) {
-    const long long ctas = static_cast<long long>((n + 127) / 128) * ((P + 127) / 128), sms = device_sms();
-    if (ctas < sms) return std::max(1, static_cast<int>(std::min<long long>({sms / ctas, k / 256, kPfMaxSplit})));
+    const long long ctas = static_cast<long long>((n + 127) / 128) * ((P + 255) / 256), sms = device_sms();
     auto eff = [&](long long z) {
         const long long c = ctas * z, waves = (c + sms - 1) / sms;
         return static_cast<double>(c) / static_cast<double>(waves * sms);
     };
+    if (ctas < sms) {
+        const int zmax = std::max(1, std::min(kPfMaxSplit, k / 64 / 8));
+        int best = 1;
+        for (int z = 2; z <= zmax; ++z)
+            if (eff(z) > eff(best) + 0.1) best = z;
+        return best;
+    }
     return (k / 64 >= 32 && eff(2) > eff(1) + 0.1) ? 2 : 1;
 }
 
