@@ -131,32 +131,37 @@ __device__ __forceinline__ void raw_decode(const RawQ6& r, int q, int part, floa
 }
 
 // ------------------------------------------- prefill GEMM on the tensor cores
-// Y = W X for a chunk of P > 4 tokens with tcgen05.mma: the CTA's 128 weight
-// rows are the A operand (M = 128), its 128 tokens the B operand (N = 128),
-// both K-major bf16 tiles in shared memory, fp32 accumulators in tensor
-// memory.  Each operand value v is split three ways, hi = bf16(v), mid =
-// bf16(v - hi), lo = bf16(v - hi - mid) (24 significant bits, as f32 has), and
-// every 16-wide K step issues six products: hi*hi into one 128 x 128
-// accumulator, hi*mid, mid*hi, hi*lo, lo*hi and mid*mid into a second one
-// (columns 128..255), the two added in f32 when the tile is stored; the
-// dropped terms are below 2^-24 of the product.  Measured on one tile of
-// Q4_K-shaped weights against an fp64 product (K = 2560): 3.3e-6 relative,
-// against 2.2e-6 for an f32 FMA loop, 5.4e-6 for a two-way split (hi, lo; three
-// products) and 2.7e-3 for one bf16 product.  The two-way split's extra error,
-// amplified through 32 layers, put the 4B prefill's deep attention K/V rows
-// past 1e-3 of the oracle's.
+// Y = W X for a chunk of P > 8 tokens with tcgen05.mma: the CTA's 128 weight
+// rows are the A operand (M = 128), its 256 tokens (two 128-token tiles) the B
+// operand (N = 256, or 128 where the second tile holds no token), both K-major
+// bf16 tiles in shared memory, fp32 accumulators in tensor memory.  Each
+// operand value v is split three ways, hi = bf16(v), mid = bf16(v - hi), lo =
+// bf16(v - hi - mid) (24 significant bits, as f32 has), and every 16-wide K
+// step issues six products: hi*hi into one 128 x 256 accumulator, hi*mid,
+// mid*hi, hi*lo, lo*hi and mid*mid into a second one (columns 256..511), the
+// two added in f32 when the tile is stored; the dropped terms are below 2^-24
+// of the product.  Measured on one tile of Q4_K-shaped weights against an
+// fp64 product (K = 2560): 3.3e-6 relative, against 2.2e-6 for an f32 FMA
+// loop, 5.4e-6 for a two-way split (hi, lo; three products) and 2.7e-3 for
+// one bf16 product.  The two-way split's extra error, amplified through 32
+// layers, put the 4B prefill's deep attention K/V rows past 1e-3 of the
+// oracle's.
 //
-// Tiles.  A K step of 64 (a quarter super-block) is one 128-byte row per
-// matrix row: row r at r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16 (the
-// 128-byte swizzle; the matrix descriptor's groups of 8 rows are 1024 bytes
-// apart).  A stage holds six 16 KB tiles (A hi, mid, lo, B hi, mid, lo); two
-// stages.  The inputs arrive already in this form: the kernels that produce
-// a GEMM input write it as (quarter, 128-token tile) triples of hi, mid and
-// lo tiles (put_xt), and one bulk copy per stage brings the triple in.  512
-// threads build the A tiles: thread (row r = tid & 127, part = tid >> 7)
-// dequantizes 16 weights of weight row r (the next quarter's raw bytes are
-// loaded before this quarter's are decoded).  A 17th warp issues each stage's
-// 24 MMAs.
+// Tiles.  A stage is a half-quarter: 32 inputs, one 64-byte row per matrix
+// row, row r at r * 64, its 16-byte chunk c at (c ^ ((r >> 1) & 3)) * 16 (the
+// 64-byte swizzle; the matrix descriptor's groups of 8 rows are 512 bytes
+// apart).  A stage holds the weight tiles (hi, mid, lo: 8 KB each) and the
+// input tiles of both token tiles ([hi | mid | lo] x [tile 0 | tile 1], 48 KB;
+// a part's two token tiles are one 256-row operand); three 72 KB stages.  The
+// inputs arrive already in this form: the kernels that produce a GEMM input
+// write it as (half-quarter, 256-token pair) blocks (put_xt), and one bulk
+// copy per stage brings a block in.  512 threads build the weight tiles:
+// thread (row r = tid & 127, part = tid >> 7) dequantizes 16 weights of weight
+// row r per quarter (the next quarter's raw bytes are loaded before this
+// quarter's are decoded); parts 0, 1 fill a quarter's first half-quarter
+// stage and parts 2, 3 its second, so the two builder groups fill alternate
+// stages.  A 17th warp issues each stage's 12 MMAs.  A weight tile built once
+// serves 256 tokens, and one instruction does 128 x 256 x 16.
 constexpr int kMmaTile = 128 * 64;       // bytes of one 128 x 32 bf16 operand tile (64-byte rows)
 constexpr int kMmaA = 3 * kMmaTile;      // a stage's weight tiles: hi, mid, lo
 constexpr int kMmaB = 6 * kMmaTile;      // its input tiles: hi, mid, lo of two 128-token tiles ([part][tile])
