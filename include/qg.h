@@ -225,9 +225,9 @@ int qg_state_set_token_mask(qg_state* s, const uint32_t* allow, int n_words);
  * The first call on a state allocates its scratch, kept until
  * qg_state_destroy (later calls allocate nothing): about 1024 x (3 hidden +
  * ffn + max(ffn, w) + w + q_dim + 2 kv_dim + ...) floats plus the K-split
- * partial sums (S x (hidden + ffn + max(ffn, w)) floats, S the largest split
- * layout of the model's projections, 2048 at the 4B shape), w the widest
- * fused input projection: ~0.45 GB at the 4B shape.  Synchronous.
+ * partial sums (per buffer, the largest split layout of the projections that
+ * write it, from the split rule), w the widest fused input projection:
+ * ~0.5 GB at the 4B shape.  Synchronous.
  * Errors: QG_ERR_ARG (NULL, or a state of another model), QG_ERR_SHAPE
  * (n_tokens < 1, head_k_dim != 128, a GQA group other than 1, 2, 4),
  * QG_ERR_POS (positions past the cache), QG_ERR_TOKEN, QG_ERR_OOM,
