@@ -1127,6 +1127,52 @@ __global__ void pf_conv_gates_kernel(const float* Z, int ldz, int P, int C, int 
     }
 }
 
+// The same for a pass of one sequence (one segment starting at column 0)
+// with K = 4 taps: thread (channel c, block of kConvTB columns) keeps the
+// channel's taps and the block's inputs (and the 3 before it) in registers,
+// so each input is read once per block instead of once per tap; the gate
+// columns c >= C give dt and beta of the block's columns.  Same sums in the
+// same order as pf_conv_gates_kernel.  Grid (ceil((C + nv) / 256), ceil(P / kConvTB)).
+constexpr int kConvTB = 16;
+__global__ void pf_conv4_block_kernel(const float* Z, int ldz, int P, int C, int nv, const float* win,
+                                      const float* wconv, const float* dt_bias, const float* a, float* Cq,
+                                      float* dt, float* beta) {
+    pdl_launch_dependents();  // the next kernel of the pass may start its prologue
+    pdl_wait();               // everything earlier in the pass is complete and visible
+    const int c = blockIdx.x * blockDim.x + threadIdx.x, p0 = blockIdx.y * kConvTB;
+    if (c >= C + nv) return;
+    if (c >= C) {
+        const int h = c - C;  // dt = softplus(alpha + dt_bias) * a, beta = sigmoid(beta_raw)
+        for (int p = p0; p < min(P, p0 + kConvTB); ++p) {
+            dt[p * nv + h] = softplus(Z[static_cast<size_t>(p) * ldz + C + h] + dt_bias[h]) * a[h];
+            beta[p * nv + h] = sigmoid(Z[static_cast<size_t>(p) * ldz + C + nv + h]);
+        }
+        return;
+    }
+    float w[4], x[kConvTB + 3];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) w[t] = wconv[static_cast<size_t>(c) * 4 + t];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {  // the inputs before the block (the window before column 0)
+        const int q = p0 - 3 + i;
+        x[i] = q >= 0 ? Z[static_cast<size_t>(q) * ldz + c] : win[static_cast<size_t>(c) * 3 + 3 + q];
+    }
+#pragma unroll
+    for (int i = 0; i < kConvTB; ++i) {
+        const int q = p0 + i;
+        x[3 + i] = q < P ? Z[static_cast<size_t>(q) * ldz + c] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kConvTB; ++i) {
+        if (p0 + i >= P) break;
+        float acc = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 3; ++t) acc += w[t] * x[i + t];
+        acc += w[3] * x[i + 3];
+        Cq[static_cast<size_t>(p0 + i) * C + c] = silu(acc);
+    }
+}
+
 // Each segment's conv window after the pass: its last K-1 inputs, oldest
 // first (from the old window where the segment is shorter than that).  Grid
 // (rows / 256, segments).
@@ -1808,10 +1854,17 @@ int run_pass(const qg_model* m, const Pass& ps, Scratch* sc, cudaStream_t st, bo
         if (m->kinds[il] == QG_LAYER_DELTANET) {
             const int C = m->conv_dim, nv = c.n_v_heads, dv = c.head_v_dim;
             const long long cg = static_cast<long long>(P) * (C + nv);
-            if (int e_ = launch_pdl(pf_conv_gates_kernel, dim3(static_cast<unsigned>((cg + 255) / 256)), dim3(256), 0,
-                                    st, pdl, Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w, L.dt_bias, L.a, sc->Cq,
-                                    sc->dt, sc->beta))
+            if (ps.n == 1 && c.conv_kernel == 4 && P > kSmallBatch) {  // one sequence's prompt chunk
+                if (int e_ = launch_pdl(pf_conv4_block_kernel,
+                                        dim3(static_cast<unsigned>((C + nv + 255) / 256), (P + kConvTB - 1) / kConvTB),
+                                        dim3(256), 0, st, pdl, Z, L.n_in, P, C, nv, sg.conv[0], L.conv_w, L.dt_bias,
+                                        L.a, sc->Cq, sc->dt, sc->beta))
+                    return e_;
+            } else if (int e_ = launch_pdl(pf_conv_gates_kernel, dim3(static_cast<unsigned>((cg + 255) / 256)),
+                                           dim3(256), 0, st, pdl, Z, L.n_in, P, C, nv, c.conv_kernel, sg, L.conv_w,
+                                           L.dt_bias, L.a, sc->Cq, sc->dt, sc->beta)) {
                 return e_;
+            }
             if (int e_ = launch_pdl(pf_conv_window_kernel, dim3((C + 255) / 256, ps.n), dim3(256), 0, st, pdl, Z,
                                     L.n_in, C, c.conv_kernel, sg))
                 return e_;
