@@ -453,6 +453,7 @@ struct BmPasses {
     static constexpr int value = QT == QT_Q4K ? 3 : 2;  // row passes per stage (27 KB / 26 KB)
 };
 constexpr int kBmXs = kBmSliceK + kBmSliceK / 64 + kBmSliceK / 512;  // staged float4 slots (with the padding)
+constexpr int kBmXsum = kBmSliceK / 16 + kBmSliceK / 256;           // sub-block sum slots (with the padding)
 
 // Slot of input k in the staged slice: a row's lanes read inputs 64 (Q4_K) or
 // 256 (Q6_K) apart at the same time, which would fall on the same banks; one
@@ -461,6 +462,11 @@ constexpr int kBmXs = kBmSliceK + kBmSliceK / 64 + kBmSliceK / 512;  // staged f
 // of 64 inputs from a multiple of 64 stays contiguous, so a lane reads its
 // chunk at fixed offsets from one pointer.
 __device__ __forceinline__ int xs_at(int k) { return k + (k >> 6) + (k >> 9); }
+// Slot of sub-block sum i (of 32 inputs for Q4_K, 16 for Q6_K): the lanes of a
+// phase read sums 2 (Q4_K) or 16 (Q6_K) apart; one float4 of padding after
+// every 8 (Q4_K) or 16 (Q6_K) puts them on different bank groups.
+template <int QT>
+__device__ __forceinline__ int xsum_at(int i) { return QT == QT_Q4K ? i + (i >> 3) : i + (i >> 4); }
 
 // a += q x, as two packed f32x2 multiply-adds (each half rounds as fmaf does)
 __device__ __forceinline__ void fma4(float4& a, float q, const float4& x) {
@@ -585,7 +591,7 @@ __device__ void bm_q4_passes(const BmLane& L, const uint8_t* ps, const float4* x
             }
         }
     }
-    const float4 X0 = xsum[L.k0 >> 5], X1 = xsum[(L.k0 >> 5) + 1];
+    const float4 X0 = xsum[xsum_at<QT_Q4K>(L.k0 >> 5)], X1 = xsum[xsum_at<QT_Q4K>((L.k0 >> 5) + 1)];
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
         const uint4 hdr = *reinterpret_cast<const uint4*>(ps + t * PB + L.o0);
@@ -666,7 +672,7 @@ __device__ void bm_q6_passes(const BmLane& L, const uint8_t* ps, const float4* x
                 }
             }
         }
-        const float4 X = xsum[kk >> 4];
+        const float4 X = xsum[xsum_at<QT_Q6K>(kk >> 4)];
         const float4 m32 = make_float4(-32.0f * X.x, -32.0f * X.y, -32.0f * X.z, -32.0f * X.w);
 #pragma unroll
         for (int t = 0; t < NP; ++t) {
@@ -806,8 +812,8 @@ __global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, co
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
     float4* xs = reinterpret_cast<float4*>(smem + 16 * kMaxStages);  // [kBmXs]
-    float4* xsum = xs + kBmXs;                                        // [kBmSliceK / 16]: sums of 32 (Q4_K) or 16 inputs
-    float* ys = reinterpret_cast<float*>(xsum + kBmSliceK / 16);     // AM: [rows_cta][4]
+    float4* xsum = xs + kBmXs;                                        // [kBmXsum]: sums of 32 (Q4_K) or 16 inputs
+    float* ys = reinterpret_cast<float*>(xsum + kBmXsum);            // AM: [rows_cta][4]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();
     if (tid == 0) {
@@ -848,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 2) bm4_kernel(const GemvShape sh, co
             float a = 0.0f;
 #pragma unroll 8
             for (int i = 0; i < SL; ++i) a += reinterpret_cast<const float*>(xs + xs_at(SL * sb + i))[c];
-            reinterpret_cast<float*>(xsum)[e] = a;
+            reinterpret_cast<float*>(xsum + xsum_at<QT>(sb))[c] = a;
         }
         bar_sync(1, kConsumers);
         const BmOut o{Y + s * split_stride, ldy, ys, wk.r0, s == 0};
@@ -912,7 +918,7 @@ int launch_bm4(const uint8_t* W, int n, int k, const float* X, int xq, float* Y,
     sh.pp = PP;
     if (!AM) grid = static_cast<int>(std::min<long long>(2LL * device_sms(), static_cast<long long>(sh.units) * sh.nsl));
     const int ys_bytes = AM ? 16 * sh.rows_cta : 0;
-    const int ring_off = (16 * kMaxStages + 16 * kBmXs + 16 * (kBmSliceK / 16) + ys_bytes + 127) & ~127;
+    const int ring_off = (16 * kMaxStages + 16 * kBmXs + 16 * kBmXsum + ys_bytes + 127) & ~127;
     const int slot = PP * stage_bytes_of(QT);
     int stages = (kCtaSmemBytes - ring_off) / slot;
     if (stages > kMaxStages) stages = kMaxStages;
