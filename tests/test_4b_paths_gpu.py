@@ -4,8 +4,10 @@ times, through the C ABI, against the oracle decoding token by token.
 These shapes reach paths the smaller models do not: the input-projection and
 gate/up GEMMs over K = 2560 (a 32-chunk and an 8-chunk slice), ffn_down over
 K = 9216 (four 32-chunk slices and a 16-chunk one), the tensor-core prefill
-GEMM with K splits on few row tiles, and the batched lm_head whose row sums
-add up over two K slices before the per-sequence argmax.
+GEMM with K splits on few row tiles (a 40-token prompt: one 128-token tile,
+ffn_down and ssm_out split seven ways; 8 tokens take the small-batch GEMV),
+and the batched lm_head whose row sums add up over two K slices before the
+per-sequence argmax.
 
 Bars as in the prefill and batch tests: the token equals the oracle's (exact
 where its top-2 margin is decisive), the residual stream within 1e-3
@@ -48,9 +50,10 @@ def models():
     return qg.Model(w), oracle.Model(w)
 
 
-def test_prefill_4b_shapes(models):
+@pytest.mark.parametrize("n_prompt", [8, 40])  # the small-batch GEMV; the tensor-core GEMM
+def test_prefill_4b_shapes(models, n_prompt):
     m, om = models
-    toks = synth.prompt_tokens(CFG, 8)  # more than 4 tokens: the tensor-core GEMM
+    toks = synth.prompt_tokens(CFG, n_prompt)
     st, ost = qg.State(m, CFG.max_seq_len), oracle.State(om)
     got = qg.qg_prefill(m, st, toks)
     want = hid = logits = None
