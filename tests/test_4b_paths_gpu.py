@@ -5,7 +5,8 @@ These shapes reach paths the smaller models do not: the input-projection and
 gate/up GEMMs over K = 2560 (a 32-chunk and an 8-chunk slice), ffn_down over
 K = 9216 (four 32-chunk slices and a 16-chunk one), the tensor-core prefill
 GEMM with K splits on few row tiles (a 40-token prompt: one 128-token tile,
-ffn_down and ssm_out split seven ways; 8 tokens take the small-batch GEMV),
+ffn_down and ssm_out split seven ways; 136 tokens: the 256-wide instructions
+over a partly filled second tile; 8 tokens take the small-batch GEMV),
 and the batched lm_head whose row sums add up over two K slices before the
 per-sequence argmax.
 
@@ -50,7 +51,7 @@ def models():
     return qg.Model(w), oracle.Model(w)
 
 
-@pytest.mark.parametrize("n_prompt", [8, 40])  # the small-batch GEMV; the tensor-core GEMM
+@pytest.mark.parametrize("n_prompt", [8, 40, 136])  # the small-batch GEMV; the tensor-core GEMM (N 128, N 256)
 def test_prefill_4b_shapes(models, n_prompt):
     m, om = models
     toks = synth.prompt_tokens(CFG, n_prompt)
